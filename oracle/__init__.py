@@ -1,0 +1,155 @@
+"""Oracle for causal sliding-window softmax attention with attention sinks (fp64, CPU).
+
+TEST INFRASTRUCTURE. This package is the plain, slow, obviously-correct statement of the
+computation, used only by ``tests/``, ``__graft_entry__.smoke()`` and the CPU-baseline leg of
+``bench.py``. The GPU library never imports it and shares no code with it.
+
+The arithmetic lives in ``swa_oracle.c`` (plain C, fp64, POSIX threads); this module converts
+arrays to float64, calls it through ctypes and returns numpy arrays.
+
+Definition (0-indexed positions, m = w - s recent keys):
+    K(t) = { i <= t : i < s  or  i >= t - m + 1 }
+    o_t  = sum_{i in K(t)} exp(x_i - M) v_i / sum_{i in K(t)} exp(x_i - M),  x_i = scale * q_t.k_i
+    lse_t = M + log(sum_{i in K(t)} exp(x_i - M)),  M = max_{i in K(t)} x_i
+It follows the SWA formula of the hyper.ai summary of arXiv 2608.28444 (section
+"带 Sink 的滑动窗口注意力"; w keys including the query's own, the first s = 4 always attended in
+addition to the w - 4 window keys), equation (1) of "模糊窗口注意力" section 2.1 (causal softmax
+attention) and eq attn-fixed-softmax-sink of "滑窗与固定稀疏" (row normalisation).
+
+Parity status: every function here is pinned by ``tests/test_oracle.py`` against closed forms,
+textbook special cases and hand-derived golden values (``tests/golden/``).
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import subprocess
+
+import numpy as np
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_SRC = os.path.join(_HERE, "swa_oracle.c")
+_BUILD_DIR = os.path.join(_HERE, "_build")
+_LIB_PATH = os.path.join(_BUILD_DIR, "libswa_oracle.so")
+_lib = None
+
+_i64p = ctypes.POINTER(ctypes.c_int64)
+_f64p = ctypes.POINTER(ctypes.c_double)
+
+
+def build(force: bool = False) -> str:
+    """Compile the C oracle with gcc into ``oracle/_build/libswa_oracle.so``."""
+    os.makedirs(_BUILD_DIR, exist_ok=True)
+    if force or not os.path.exists(_LIB_PATH) or os.path.getmtime(_LIB_PATH) < os.path.getmtime(_SRC):
+        tmp = _LIB_PATH + f".tmp{os.getpid()}"
+        subprocess.check_call(["gcc", "-O2", "-std=c11", "-ffp-contract=off", "-fPIC", "-shared",
+                               "-pthread", _SRC, "-o", tmp, "-lm"])
+        os.replace(tmp, _LIB_PATH)
+    return _LIB_PATH
+
+
+def _get():
+    global _lib
+    if _lib is None:
+        lib = ctypes.CDLL(build())
+        lib.swa_oracle_is_key.restype = ctypes.c_int
+        lib.swa_oracle_is_key.argtypes = [ctypes.c_int64] * 4
+        lib.swa_oracle_mask.restype = None
+        lib.swa_oracle_mask.argtypes = [ctypes.c_int64] * 3 + [ctypes.POINTER(ctypes.c_uint8)]
+        lib.swa_oracle_attend.restype = None
+        lib.swa_oracle_attend.argtypes = [_f64p, _i64p, _f64p, _f64p, _i64p] + [ctypes.c_int64] * 6 + [
+            ctypes.c_double, _f64p, _f64p, ctypes.c_int]
+        lib.swa_oracle_cache_replay.restype = None
+        lib.swa_oracle_cache_replay.argtypes = [ctypes.c_int64] * 3 + [_i64p]
+        _lib = lib
+    return _lib
+
+
+def default_threads() -> int:
+    try:
+        return len(os.sched_getaffinity(0))
+    except AttributeError:  # pragma: no cover
+        return os.cpu_count() or 1
+
+
+def _f64(a) -> np.ndarray:
+    """Exact conversion of a numpy array or torch tensor (any float dtype) to contiguous float64."""
+    if hasattr(a, "detach"):  # torch tensor: bf16/fp32 -> fp32 (exact) -> fp64 (exact)
+        a = a.detach().to("cpu")
+        if str(a.dtype) != "torch.float64":
+            a = a.float()
+        a = a.numpy()
+    return np.ascontiguousarray(a, dtype=np.float64)
+
+
+def is_key(t: int, i: int, w: int, s: int) -> bool:
+    """Brute-force membership of key position i in the key set of query position t."""
+    return bool(_get().swa_oracle_is_key(t, i, w, s))
+
+
+def mask(L: int, w: int, s: int) -> np.ndarray:
+    """L x L uint8 matrix, 1 where query t attends key i."""
+    out = np.zeros((L, L), dtype=np.uint8)
+    _get().swa_oracle_mask(L, w, s, out.ctypes.data_as(ctypes.POINTER(ctypes.c_uint8)))
+    return out
+
+
+def attend(q, qpos, k, v, kpos, w: int, s: int, scale: float, nthreads: int | None = None):
+    """Queries against explicitly given keys.
+
+    q: [nh, nq, d]; k, v: [nh, nk, d]; qpos: [nq], kpos: [nk] absolute positions (any order).
+    Returns (o [nh, nq, d] float64, lse [nh, nq] float64).
+    """
+    q, k, v = _f64(q), _f64(k), _f64(v)
+    qpos = np.ascontiguousarray(qpos, dtype=np.int64)
+    kpos = np.ascontiguousarray(kpos, dtype=np.int64)
+    nh, nq, d = q.shape
+    nk = k.shape[1]
+    assert k.shape == (nh, nk, d) and v.shape == (nh, nk, d)
+    assert qpos.shape == (nq,) and kpos.shape == (nk,)
+    o = np.empty((nh, nq, d), dtype=np.float64)
+    lse = np.empty((nh, nq), dtype=np.float64)
+    _get().swa_oracle_attend(q.ctypes.data_as(_f64p), qpos.ctypes.data_as(_i64p), k.ctypes.data_as(_f64p),
+                             v.ctypes.data_as(_f64p), kpos.ctypes.data_as(_i64p), nh, nq, nk, d, w, s,
+                             float(scale), o.ctypes.data_as(_f64p), lse.ctypes.data_as(_f64p),
+                             int(nthreads or default_threads()))
+    return o, lse
+
+
+def prefill(q, k, v, w: int, s: int, scale: float, nthreads: int | None = None):
+    """Whole-sequence prefill: q, k, v [B, H, L, d] -> (o [B, H, L, d], lse [B, H, L]), fp64."""
+    q, k, v = _f64(q), _f64(k), _f64(v)
+    B, H, L, d = q.shape
+    pos = np.arange(L, dtype=np.int64)
+    o, lse = attend(q.reshape(B * H, L, d), pos, k.reshape(B * H, L, d), v.reshape(B * H, L, d), pos,
+                    w, s, scale, nthreads)
+    return o.reshape(B, H, L, d), lse.reshape(B, H, L)
+
+
+def prefill_rows(q_rows, rows, k, v, w: int, s: int, scale: float, nthreads: int | None = None):
+    """Selected query rows of a prefill: q_rows [nh, nr, d] at positions ``rows`` against the full key
+    history k, v [nh, L, d] (positions 0..L-1)."""
+    k, v = _f64(k), _f64(v)
+    kpos = np.arange(k.shape[1], dtype=np.int64)
+    return attend(q_rows, np.asarray(rows, dtype=np.int64), k, v, kpos, w, s, scale, nthreads)
+
+
+def decode(q_t, k_hist, v_hist, t: int, w: int, s: int, scale: float, nthreads: int | None = None):
+    """Streaming decode at position t from the full, un-cached history.
+
+    q_t: [nh, d]; k_hist, v_hist: [nh, t + 1, d] (positions 0..t). Returns (o [nh, d], lse [nh]).
+    The cache is never consulted: the definition is applied to the history.
+    """
+    q_t = _f64(q_t)
+    nh, d = q_t.shape
+    kpos = np.arange(t + 1, dtype=np.int64)
+    o, lse = attend(q_t.reshape(nh, 1, d), np.array([t], dtype=np.int64), k_hist, v_hist, kpos,
+                    w, s, scale, nthreads)
+    return o.reshape(nh, d), lse.reshape(nh)
+
+
+def cache_replay(w: int, s: int, npos: int) -> np.ndarray:
+    """Slot -> position held after writing positions 0..npos-1 one by one (-1 = never written)."""
+    out = np.empty(w, dtype=np.int64)
+    _get().swa_oracle_cache_replay(w, s, npos, out.ctypes.data_as(_i64p))
+    return out

@@ -1,0 +1,276 @@
+"""Pins of the oracle against what the pages and the mathematics fix (CPU only).
+
+Each test checks the oracle against something other than itself: hand-derived values, a textbook
+library routine on a special case, a closed form, or an invariant. Together they are chosen so that
+a plausible slip in the oracle (a window one key too wide or too narrow, sinks counted outside the
+window, a transposed operand, a wrong scale, a missing max-subtraction, a wrong slot formula) fails
+at least one of them.
+"""
+import json
+import math
+import os
+from fractions import Fraction
+
+import numpy as np
+import pytest
+import scipy.special
+
+import oracle
+
+GOLDEN = os.path.join(os.path.dirname(__file__), "golden")
+
+
+def rnd(shape, seed):
+    return np.random.default_rng(seed).standard_normal(shape)
+
+
+# ---------------------------------------------------------------------------------------------
+# Hand-derived worked examples (hyper.ai summary of arXiv 2608.28444, section
+# "带 Sink 的滑动窗口注意力": w keys, s sinks inside the window).
+# ---------------------------------------------------------------------------------------------
+def test_hand_derived_examples():
+    g = json.load(open(os.path.join(GOLDEN, "hand_sink_window.json")))
+    L = len(g["v"])
+    k = np.log(np.array(g["exp_k"], dtype=np.float64)).reshape(1, 1, L, 1)
+    v = np.array(g["v"], dtype=np.float64).reshape(1, 1, L, 1)
+    q = np.ones((1, 1, L, 1))
+    for case in g["cases"]:
+        o, lse = oracle.prefill(q, k, v, case["w"], case["s"], 1.0)
+        want = np.array([float(Fraction(x)) for x in case["o"]])
+        np.testing.assert_allclose(o[0, 0, :, 0], want, rtol=1e-13, atol=0)
+        np.testing.assert_allclose(lse[0, 0], np.log(np.array(case["lse_exp"], dtype=np.float64)),
+                                   rtol=0, atol=1e-13)
+
+
+# ---------------------------------------------------------------------------------------------
+# Special case w >= L: full causal softmax attention, equation (1) of "模糊窗口注意力" section 2.1,
+# computed here with numpy matmul + scipy.special.softmax on an explicit -inf mask.
+# ---------------------------------------------------------------------------------------------
+@pytest.mark.parametrize("L,d,w,s", [(37, 8, 37, 0), (37, 8, 50, 0), (29, 5, 29, 3), (64, 16, 64, 0)])
+def test_full_window_is_causal_attention(L, d, w, s):
+    q, k, v = rnd((2, 3, L, d), 1), rnd((2, 3, L, d), 2), rnd((2, 3, L, d), 3)
+    scale = 1.0 / math.sqrt(d)
+    o, lse = oracle.prefill(q, k, v, w, s, scale)
+    S = np.einsum("bhtc,bhic->bhti", q, k) / math.sqrt(d)
+    M = np.where(np.tril(np.ones((L, L), dtype=bool)), 0.0, -np.inf)
+    P = scipy.special.softmax(S + M, axis=-1)
+    np.testing.assert_allclose(o, P @ v, rtol=0, atol=1e-12)
+    np.testing.assert_allclose(lse, scipy.special.logsumexp(S + M, axis=-1), rtol=0, atol=1e-12)
+
+
+def test_w1_s0_returns_v():
+    # One-term sum of the SWA formula: x_t = v_t exactly.
+    q, k, v = rnd((1, 2, 23, 7), 4), rnd((1, 2, 23, 7), 5), rnd((1, 2, 23, 7), 6)
+    o, _ = oracle.prefill(q, k, v, 1, 0, 0.37)
+    assert np.array_equal(o, v)
+
+
+def test_w1_s1_is_sink_plus_self_only_through_sink():
+    # w = 1, s = 1: m = 0 recent keys, so every query sees only position 0 (and itself only if t = 0).
+    q, k, v = rnd((1, 1, 9, 4), 7), rnd((1, 1, 9, 4), 8), rnd((1, 1, 9, 4), 9)
+    o, _ = oracle.prefill(q, k, v, 1, 1, 0.5)
+    np.testing.assert_array_equal(o[0, 0], np.repeat(v[0, 0, :1], 9, axis=0))
+
+
+def test_two_key_window_closed_form():
+    # s = 0, w = 2: o_t = sigmoid(x_t - x_{t-1}) v_t + sigmoid(x_{t-1} - x_t) v_{t-1}.
+    L, d = 31, 6
+    q, k, v = rnd((1, 1, L, d), 10), rnd((1, 1, L, d), 11), rnd((1, 1, L, d), 12)
+    sc = 0.8
+    o, _ = oracle.prefill(q, k, v, 2, 0, sc)
+    q0, k0, v0 = q[0, 0], k[0, 0], v[0, 0]
+    np.testing.assert_array_equal(o[0, 0, 0], v0[0])
+    for t in range(1, L):
+        a = sc * q0[t] @ k0[t]
+        b = sc * q0[t] @ k0[t - 1]
+        want = scipy.special.expit(a - b) * v0[t] + scipy.special.expit(b - a) * v0[t - 1]
+        np.testing.assert_allclose(o[0, 0, t], want, rtol=0, atol=1e-13)
+
+
+# ---------------------------------------------------------------------------------------------
+# Key-set membership by an independent construction: the union of the sink range [0, s) and the
+# recent range [t - m + 1, t], built as Python sets (the StreamingLLM cache of page
+# "滑窗与固定稀疏", eq attn-fixed-streaming: k sinks + m recent).
+# ---------------------------------------------------------------------------------------------
+def keyset(t, w, s):
+    m = w - s
+    return (set(range(0, min(s, t + 1))) | set(range(max(0, t - m + 1), t + 1)))
+
+
+@pytest.mark.parametrize("L", [1, 2, 7, 13, 40])
+def test_mask_matches_set_construction(L):
+    for w in range(1, L + 3):
+        for s in range(0, w):
+            mk = oracle.mask(L, w, s)
+            for t in range(L):
+                assert set(np.nonzero(mk[t])[0].tolist()) == keyset(t, w, s), (L, w, s, t)
+
+
+def test_zero_query_gives_mean_over_keyset():
+    # q = 0 makes every score 0, so o_t is the plain mean of v over K(t): pins which keys and how many.
+    L, d = 45, 3
+    v = rnd((1, 1, L, d), 13)
+    for w, s in [(1, 0), (5, 0), (5, 2), (8, 4), (8, 7), (44, 4), (60, 4)]:
+        o, lse = oracle.prefill(np.zeros((1, 1, L, d)), rnd((1, 1, L, d), 14), v, w, s, 1.0)
+        for t in range(L):
+            ks = sorted(keyset(t, w, s))
+            np.testing.assert_allclose(o[0, 0, t], v[0, 0, ks].mean(axis=0), rtol=0, atol=1e-13)
+            assert abs(lse[0, 0, t] - math.log(len(ks))) < 1e-13
+
+
+def test_mask_picture_n32():
+    # The N = 32 StreamingLLM picture (recent band + sink bar on the left), stored as text.
+    g = open(os.path.join(GOLDEN, "streaming_mask_n32_w8_s4.txt")).read().split("\n")
+    rows = [r for r in g if r and set(r) <= {"#", "."}]
+    pic = np.array([[1 if ch == "#" else 0 for ch in r] for r in rows], dtype=np.uint8)
+    assert pic.shape == (32, 32)
+    np.testing.assert_array_equal(oracle.mask(32, 8, 4), pic)
+    # caption facts: lower-triangular, a full left bar of 4 columns below the diagonal, a band of 4
+    for t in range(32):
+        assert pic[t, t + 1:].sum() == 0
+        assert pic[t, :min(4, t + 1)].all()
+        assert pic[t, max(0, t - 3):t + 1].all()
+        assert pic[t].sum() == min(t + 1, 8)
+
+
+# ---------------------------------------------------------------------------------------------
+# Normalisation, page "滑窗与固定稀疏", eq attn-fixed-softmax-sink: with V = identity the output rows
+# are the attention weights; they sum to 1, are >= 0 and vanish outside K(t).
+# ---------------------------------------------------------------------------------------------
+def test_rows_are_probability_vectors():
+    L = 24
+    q, k = rnd((1, 1, L, L), 15), rnd((1, 1, L, L), 16)
+    v = np.eye(L).reshape(1, 1, L, L)
+    for w, s in [(6, 2), (6, 0), (24, 4), (3, 1)]:
+        P, _ = oracle.prefill(q, k, v, w, s, 0.3)
+        P = P[0, 0]
+        np.testing.assert_allclose(P.sum(axis=1), 1.0, rtol=0, atol=1e-12)
+        assert (P >= 0).all()
+        for t in range(L):
+            outside = [i for i in range(L) if i not in keyset(t, w, s)]
+            assert (P[t, outside] == 0).all()
+            assert (P[t, sorted(keyset(t, w, s))] > 0).all()
+
+
+def test_scale_is_applied_once():
+    # Scaling q by lam and the softmax scale by 1/lam leaves every score unchanged.
+    L, d = 33, 8
+    q, k, v = rnd((1, 2, L, d), 17), rnd((1, 2, L, d), 18), rnd((1, 2, L, d), 19)
+    o1, l1 = oracle.prefill(q, k, v, 9, 2, 0.25)
+    o2, l2 = oracle.prefill(q * 4.0, k, v, 9, 2, 0.0625)
+    np.testing.assert_allclose(o1, o2, rtol=0, atol=1e-13)
+    np.testing.assert_allclose(l1, l2, rtol=0, atol=1e-12)
+    o3, _ = oracle.prefill(q, k, v, 9, 2, 0.5)
+    assert np.abs(o3 - o1).max() > 1e-3  # the scale matters
+
+
+def test_large_sink_logits_stay_finite():
+    # Keys at positions 0..3 boosted (x4 and x1000): exp() of the raw scores would overflow in fp64;
+    # the max-subtracted softmax must stay finite and match scipy's logsumexp.
+    L, d = 40, 16
+    q, k, v = rnd((1, 1, L, d), 20) * 30, rnd((1, 1, L, d), 21), rnd((1, 1, L, d), 22)
+    k[..., :4, :] *= 1000.0
+    o, lse = oracle.prefill(q, k, v, 12, 4, 1.0)
+    assert np.isfinite(o).all() and np.isfinite(lse).all()
+    S = q[0, 0] @ k[0, 0].T
+    for t in range(L):
+        ks = sorted(keyset(t, 12, 4))
+        np.testing.assert_allclose(lse[0, 0, t], scipy.special.logsumexp(S[t, ks]), rtol=1e-14, atol=0)
+        P = scipy.special.softmax(S[t, ks])
+        np.testing.assert_allclose(o[0, 0, t], P @ v[0, 0, ks], rtol=0, atol=1e-10)
+
+
+# ---------------------------------------------------------------------------------------------
+# Rolling cache: slot replay (page "滑窗与固定稀疏", eq attn-fixed-rolling cache_slot(i) = i mod W,
+# and eq attn-fixed-streaming: sinks + recent, k + m slots) and the order-free decode
+# ("模糊窗口注意力" section 3: softmax attention is invariant to the order of the keys).
+# ---------------------------------------------------------------------------------------------
+@pytest.mark.parametrize("w", [1, 2, 5, 16])
+def test_slot_replay_s0_is_mod_w(w):
+    for npos in range(0, 4 * w + 3):
+        h = oracle.cache_replay(w, 0, npos)
+        for j in range(w):
+            held = [p for p in range(npos) if p % w == j]
+            assert h[j] == (held[-1] if held else -1)
+
+
+@pytest.mark.parametrize("w,s", [(8, 4), (5, 1), (6, 5), (16, 4)])
+def test_slot_replay_holds_sinks_and_recent(w, s):
+    m = w - s
+    for npos in range(0, 5 * w):
+        h = oracle.cache_replay(w, s, npos)
+        held = sorted(p for p in h.tolist() if p >= 0)
+        want = sorted(set(range(min(s, npos))) | set(range(max(s, npos - m), npos)))
+        assert held == want
+        assert len(h) == w  # constant footprint, k + m slots
+
+
+@pytest.mark.parametrize("w,s", [(8, 4), (5, 1), (6, 5), (16, 4), (4, 0)])
+def test_slot_index_fills_in_order_then_overwrites_oldest(w, s):
+    # The cache fills slot p with position p until it is full; from then on each new position takes
+    # the slot of the oldest recent position (the rolling buffer overwrites the oldest entry, page
+    # "滑窗与固定稀疏", rolling-buffer section), and the s sink slots are never overwritten.
+    m = w - s
+    for npos in range(0, w + 1):
+        h = oracle.cache_replay(w, s, npos)
+        assert h.tolist() == list(range(npos)) + [-1] * (w - npos)
+    prev = oracle.cache_replay(w, s, w)
+    for p in range(w, 6 * w):
+        cur = oracle.cache_replay(w, s, p + 1)
+        changed = [j for j in range(w) if cur[j] != prev[j]]
+        if m == 0:
+            assert changed == []
+        else:
+            oldest = min(x for x in prev.tolist() if x >= s)
+            assert changed == [prev.tolist().index(oldest)] and cur[changed[0]] == p
+        assert cur[:s].tolist() == list(range(s))
+        prev = cur
+
+
+@pytest.mark.parametrize("w,s,d", [(8, 4, 4), (5, 0, 3), (7, 2, 5), (1, 0, 2)])
+def test_cached_decode_equals_history_every_step(w, s, d):
+    T = 3 * w + 5
+    nh = 2
+    q, k, v = rnd((nh, T, d), 30 + w), rnd((nh, T, d), 31 + s), rnd((nh, T, d), 32)
+    k[:, :min(4, T), :] *= 4.0
+    sc = 1.0 / math.sqrt(d)
+    for t in range(T):
+        o_hist, l_hist = oracle.decode(q[:, t], k[:, :t + 1], v[:, :t + 1], t, w, s, sc)
+        h = oracle.cache_replay(w, s, t + 1)
+        slots = [j for j in range(w) if h[j] >= 0]
+        kpos = h[slots]
+        o_c, l_c = oracle.attend(q[:, t:t + 1], [t], k[:, kpos], v[:, kpos], kpos, w, s, sc)
+        np.testing.assert_allclose(o_c[:, 0], o_hist, rtol=0, atol=1e-13)
+        np.testing.assert_allclose(l_c[:, 0], l_hist, rtol=0, atol=1e-13)
+        # every cached key is in K(t): the cache is exactly the key set
+        assert set(kpos.tolist()) == keyset(t, w, s)
+
+
+def test_cache_footprint_ratio():
+    # Rolling buffer of W = 4096 slots vs the full cache: 8x at 32K tokens, 2x at 8K
+    # (page "滑窗与固定稀疏", rolling-buffer section).
+    for L, ratio in [(32768, 8), (8192, 2)]:
+        h = oracle.cache_replay(4096, 0, L)
+        assert L / len(h) == ratio
+
+
+def test_key_order_does_not_matter():
+    L, d = 50, 8
+    q, k, v = rnd((2, L, d), 40), rnd((2, L, d), 41), rnd((2, L, d), 42)
+    pos = np.arange(L)
+    perm = np.random.default_rng(3).permutation(L)
+    o1, l1 = oracle.attend(q, pos, k, v, pos, 11, 3, 0.4)
+    o2, l2 = oracle.attend(q, pos, k[:, perm], v[:, perm], pos[perm], 11, 3, 0.4)
+    np.testing.assert_allclose(o1, o2, rtol=0, atol=1e-13)
+    np.testing.assert_allclose(l1, l2, rtol=0, atol=1e-13)
+
+
+def test_rows_subset_and_threads_agree():
+    B, H, L, d = 1, 3, 70, 8
+    q, k, v = rnd((B, H, L, d), 50), rnd((B, H, L, d), 51), rnd((B, H, L, d), 52)
+    o, lse = oracle.prefill(q, k, v, 13, 4, 0.35, nthreads=1)
+    o4, lse4 = oracle.prefill(q, k, v, 13, 4, 0.35, nthreads=4)
+    assert np.array_equal(o, o4) and np.array_equal(lse, lse4)
+    rows = [0, 5, 12, 13, 14, 69]
+    orow, lrow = oracle.prefill_rows(q[0][:, rows], rows, k[0], v[0], 13, 4, 0.35)
+    assert np.array_equal(orow, o[0][:, rows]) and np.array_equal(lrow, lse[0][:, rows])
