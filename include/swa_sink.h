@@ -1,0 +1,168 @@
+/*
+ * swa_sink.h -- C ABI of the GB300 (sm_103a) library for causal sliding-window softmax attention
+ * with attention sinks: prefill, chunked prefill through a rolling KV cache, streaming decode.
+ *
+ * The operation.  For query position t (0-indexed) with window w and s sink tokens (m = w - s recent
+ * keys), the key set is
+ *     K(t) = { i <= t : i < s  or  i >= t - m + 1 }
+ * and the output is o_t = sum_{i in K(t)} softmax_i(scale * q_t.k_i) v_i.
+ *   - SWA formula (window of w keys ending at t) and sinks (the first s = 4 tokens attended in
+ *     addition to the w - 4 window tokens): hyper.ai summary of arXiv 2608.28444, section
+ *     "带 Sink 的滑动窗口注意力".
+ *   - Causal softmax attention: "模糊窗口注意力" (Blurry Window Attention), section 2.1, equation (1).
+ *   - Rolling cache and chunk-based prefill: "滑窗与固定稀疏", eq attn-fixed-rolling and the
+ *     paragraph after it; sink + recent cache of k + m slots: eq attn-fixed-streaming.
+ *
+ * Conventions for every entry point:
+ *   - Pointers are DEVICE pointers unless stated otherwise; the caller owns every buffer.  No entry
+ *     point allocates or frees device memory.
+ *   - Tensors are contiguous, row-major, innermost dimension last ([B, H, L, d]: d contiguous), and
+ *     16-byte aligned.  bf16 storage (SWA_BF16) or fp32 storage (SWA_F32).
+ *   - `stream` is a cudaStream_t passed as void* (NULL = the legacy default stream).  Work is
+ *     enqueued asynchronously on it.
+ *   - Argument errors return SWA_ERR_INVALID / SWA_ERR_UNSUPPORTED synchronously, before anything
+ *     is launched; a failed launch returns SWA_ERR_CUDA.  swa_last_error_string() explains the most
+ *     recent failure of the calling host thread.
+ *   - Every device-side wait in the library is bounded in time.  A wait that runs out records an
+ *     error word on the device and the kernel returns; swa_device_status() reports it.
+ *   - All batch rows share one position: one pos0 in prefill, one t in decode.
+ *   - Multi-head layout is one K/V head per query head (H_kv = H).
+ */
+#ifndef SWA_SINK_H
+#define SWA_SINK_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+    SWA_OK = 0,
+    SWA_ERR_INVALID = -1,     /* bad argument (null pointer, s >= w, misaligned, ...)          */
+    SWA_ERR_UNSUPPORTED = -2, /* valid but not implemented (e.g. bf16 with d != 128)          */
+    SWA_ERR_CUDA = -3,        /* a CUDA runtime call or kernel launch failed                 */
+    SWA_ERR_TIMEOUT = -4      /* a bounded device-side wait ran out (see swa_device_status)   */
+} swa_status;
+
+typedef enum { SWA_BF16 = 0, SWA_F32 = 1 } swa_dtype;
+
+/*
+ * swa_sink_prefill -- attention of L consecutive queries at absolute positions pos0 .. pos0+L-1.
+ *
+ *   q, k, v : [B, H, L, d], the queries and the keys/values of the same L positions.
+ *   o       : [B, H, L, d] output, same dtype as q.
+ *   lse     : optional [B, H, L] fp32 output, natural log of sum_{i in K(t)} exp(scale * q_t.k_i);
+ *             NULL to skip.
+ *   k_cache, v_cache : used only when pos0 > 0: [B, H, w, d] rolling cache holding the keys/values
+ *             of positions < pos0 in the layout kv_rolling_write produces (slot p for p < s, slot
+ *             s + ((p - s) mod m) otherwise), i.e. the cache state after positions 0..pos0-1 were
+ *             written.  May be NULL when pos0 == 0.  Not modified.
+ *   pos0    : absolute position of row 0 (0 = a whole-sequence prefill; > 0 = one chunk of a chunked
+ *             prefill, see the chunk-based prefill of "滑窗与固定稀疏").
+ *   B, H, L, d, w, s : batch, heads, rows, head dim, window (keys per query, sinks included), sinks.
+ *             Requires 0 <= s < w, L >= 0 (L == 0 is a no-op), pos0 + L < 2^31.
+ *   scale   : softmax scale (1/sqrt(d) for the usual attention).
+ *   dtype   : SWA_BF16 requires d == 128 (tensor-core path: TMA + tcgen05 + TMEM);
+ *             SWA_F32 accepts d in {16, 32, 64, 128} (CUDA-core path).
+ */
+int swa_sink_prefill(const void *q, const void *k, const void *v, void *o, float *lse,
+                     const void *k_cache, const void *v_cache, int64_t pos0,
+                     int B, int H, int64_t L, int d, int w, int s, float scale,
+                     int dtype, void *stream);
+
+/*
+ * swa_sink_prefill_chunked -- the chunk-based prefill of "滑窗与固定稀疏" (rolling-buffer section):
+ * the L positions are processed in chunks of `chunk` rows; chunk c attends the rolling cache as it was
+ * before the chunk plus its own keys (swa_sink_prefill with pos0 = c*chunk), then its keys/values are
+ * written into the cache (kv_rolling_write).  The result equals a whole-sequence prefill.
+ *
+ *   q, k, v, o, lse : whole-sequence tensors [B, H, L, d] (lse [B, H, L] or NULL).
+ *   k_cache, v_cache : [B, H, w, d] scratch cache owned by the caller; contents on entry are ignored,
+ *             on exit it holds the cache state after position L-1 (ready for streaming decode).
+ *   chunk   : rows per chunk, >= 1.
+ */
+int swa_sink_prefill_chunked(const void *q, const void *k, const void *v, void *o, float *lse,
+                             void *k_cache, void *v_cache,
+                             int B, int H, int64_t L, int d, int w, int s, float scale,
+                             int64_t chunk, int dtype, void *stream);
+
+/*
+ * kv_rolling_write -- write the keys/values of positions pos0 .. pos0+n-1 into the rolling cache:
+ * position p goes to slot p if p < s, else to slot s + ((p - s) mod m), m = w - s (with s = 0 this is
+ * the rolling buffer cache_slot(i) = i mod W of "滑窗与固定稀疏", eq attn-fixed-rolling; the sink
+ * block + recent block layout is eq attn-fixed-streaming).  When n > m several positions share a
+ * slot; only the last of them is written, so the result equals writing the positions one by one.
+ *
+ *   k_cache, v_cache : [B, H, w, d], updated in place.
+ *   k_new, v_new     : [B, H, n, d].
+ *   pos0 >= 0, n >= 0 (n == 0 is a no-op).  Bytes are copied exactly.
+ */
+int kv_rolling_write(void *k_cache, void *v_cache, const void *k_new, const void *v_new,
+                     int B, int H, int d, int w, int s, int64_t pos0, int64_t n,
+                     int dtype, void *stream);
+
+/*
+ * swa_sink_decode_step -- one streaming-decode step for the query at absolute position t, whose key
+ * and value are already in the cache (write, then attend).  The valid slots are 0 .. min(t+1, w)-1
+ * and they hold exactly K(t) (eq attn-fixed-streaming of "滑窗与固定稀疏": sinks + recent window).
+ *
+ *   q, o      : [B, H, d].
+ *   k_cache, v_cache : [B, H, w, d] as written by kv_rolling_write for positions 0..t.
+ *   lse       : optional [B, H] fp32 output (NULL to skip).
+ *   workspace : caller-owned device scratch of at least swa_sink_decode_workspace_size(B,H,d,w)
+ *               bytes, 256-byte aligned (split-K partial results); may be NULL if that size is 0.
+ *   dtype     : SWA_BF16 or SWA_F32; d in {16, 32, 64, 128}.
+ */
+int swa_sink_decode_step(const void *q, const void *k_cache, const void *v_cache, void *o,
+                         float *lse, int B, int H, int d, int w, int s, int64_t t, float scale,
+                         void *workspace, size_t workspace_bytes, int dtype, void *stream);
+
+/* Bytes of workspace swa_sink_decode_step needs for this shape (host-only, no CUDA call). */
+size_t swa_sink_decode_workspace_size(int B, int H, int d, int w);
+
+/* Human-readable reason of the calling host thread's most recent failure ("" if none). */
+const char *swa_last_error_string(void);
+
+/*
+ * swa_device_status -- synchronise `stream`, then read and clear the current device's error word.
+ * Returns SWA_OK, SWA_ERR_TIMEOUT (a bounded device wait ran out) or SWA_ERR_CUDA.
+ */
+int swa_device_status(void *stream);
+
+/*
+ * swa_selftest_wait_timeout -- diagnostics for the bounded waits: launches one small kernel whose
+ * thread waits on an mbarrier that nothing ever arrives on, with a limit of `timeout_ns`
+ * nanoseconds (1 .. 10^9).  The wait runs out, the kernel records the timeout and returns; a following
+ * swa_device_status() returns SWA_ERR_TIMEOUT.  No GPU fault, trap or hang is involved.
+ */
+int swa_selftest_wait_timeout(int64_t timeout_ns, void *stream);
+
+/*
+ * swa_selftest_umma -- diagnostics for the tensor-core building blocks of the bf16 prefill kernel:
+ * one CTA computes C = A * op(B) for 128 x 128 bf16 tiles with TMA loads, tcgen05.mma and a TMEM
+ * accumulator read back with tcgen05.ld.
+ *   a : [128, 128] bf16 row-major (M x K).
+ *   b : mode 0: [128, 128] (N x K), C = A * B^T  (both operands K-major, as in Q K^T)
+ *       mode 1: [128, 128] (K x N), C = A * B    (B MN-major, as in P V)
+ *       mode 2: as mode 1, but A is staged into shared memory by threads instead of TMA.
+ *   c : [128, 128] fp32 row-major output.
+ */
+int swa_selftest_umma(const void *a, const void *b, float *c, int mode, void *stream);
+
+/*
+ * swa_prefill_tile_plan -- diagnostics (host only, no CUDA call): the key tiles the bf16 prefill kernel
+ * walks for the query rows at absolute positions q0..q1 (one 128-row query tile) of a call starting at
+ * pos0.  For tile i, tiles[4i..4i+3] = {source (0 = the call's k/v, 1 = rolling cache), first source
+ * row, absolute position of column 0, last valid column}; columns c <= last valid column hold position
+ * (column-0 position + c).  Writes at most max_tiles entries; returns the tile count or a negative
+ * swa_status.
+ */
+int swa_prefill_tile_plan(int64_t q0, int64_t q1, int64_t pos0, int w, int s, int *tiles, int max_tiles);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* SWA_SINK_H */

@@ -54,6 +54,9 @@ def _get():
         lib = ctypes.CDLL(build())
         lib.swa_oracle_is_key.restype = ctypes.c_int
         lib.swa_oracle_is_key.argtypes = [ctypes.c_int64] * 4
+        lib.swa_oracle_is_key_many.restype = None
+        lib.swa_oracle_is_key_many.argtypes = [ctypes.c_int64, _i64p, ctypes.c_int64, ctypes.c_int64, ctypes.c_int64,
+                                               ctypes.POINTER(ctypes.c_uint8)]
         lib.swa_oracle_mask.restype = None
         lib.swa_oracle_mask.argtypes = [ctypes.c_int64] * 3 + [ctypes.POINTER(ctypes.c_uint8)]
         lib.swa_oracle_attend.restype = None
@@ -85,6 +88,15 @@ def _f64(a) -> np.ndarray:
 def is_key(t: int, i: int, w: int, s: int) -> bool:
     """Brute-force membership of key position i in the key set of query position t."""
     return bool(_get().swa_oracle_is_key(t, i, w, s))
+
+
+def is_key_many(t: int, positions, w: int, s: int) -> np.ndarray:
+    """Boolean array: membership of each key position in the key set of query position t."""
+    pos = np.ascontiguousarray(positions, dtype=np.int64)
+    out = np.zeros(pos.shape, dtype=np.uint8)
+    _get().swa_oracle_is_key_many(t, pos.ctypes.data_as(_i64p), pos.size, w, s,
+                                  out.ctypes.data_as(ctypes.POINTER(ctypes.c_uint8)))
+    return out.astype(bool)
 
 
 def mask(L: int, w: int, s: int) -> np.ndarray:

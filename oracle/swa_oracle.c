@@ -41,6 +41,12 @@ int swa_oracle_is_key(int64_t t, int64_t i, int64_t w, int64_t s)
     return i >= t - (w - s) + 1;
 }
 
+/* Membership of n key positions in the key set of query position t: out[j] = is_key(t, pos[j]). */
+void swa_oracle_is_key_many(int64_t t, const int64_t *pos, int64_t n, int64_t w, int64_t s, uint8_t *out)
+{
+    for (int64_t j = 0; j < n; ++j) out[j] = (uint8_t)swa_oracle_is_key(t, pos[j], w, s);
+}
+
 /* Dense 0/1 mask of an L x L problem: mask[t*L + i] = 1 iff key i is attended by query t.
  * This is the picture of the "StreamingLLM recent band + sink left bar" pattern (page
  * "滑窗与固定稀疏", figure fig-attn-four-mask-compare). */

@@ -1,0 +1,180 @@
+"""ctypes binding of the C ABI in include/swa_sink.h.
+
+Argument marshalling only: each function checks shapes/dtypes/devices of torch tensors, passes their
+device pointers and the current CUDA stream to the library, and raises on a non-zero status. Every
+step of the computation runs in the library's CUDA kernels; there is no CPU or PyTorch fallback. If
+the library is not built the first call raises.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+
+import torch
+
+from . import build as _build
+
+SWA_OK, SWA_ERR_INVALID, SWA_ERR_UNSUPPORTED, SWA_ERR_CUDA, SWA_ERR_TIMEOUT = 0, -1, -2, -3, -4
+SWA_BF16, SWA_F32 = 0, 1
+_STATUS_NAMES = {0: "SWA_OK", -1: "SWA_ERR_INVALID", -2: "SWA_ERR_UNSUPPORTED", -3: "SWA_ERR_CUDA",
+                 -4: "SWA_ERR_TIMEOUT"}
+
+_vp, _i, _i64, _f, _sz = ctypes.c_void_p, ctypes.c_int, ctypes.c_int64, ctypes.c_float, ctypes.c_size_t
+
+# name -> (restype, argtypes); mirrors include/swa_sink.h
+SIGNATURES = {
+    "swa_sink_prefill": (_i, [_vp, _vp, _vp, _vp, _vp, _vp, _vp, _i64, _i, _i, _i64, _i, _i, _i, _f, _i, _vp]),
+    "swa_sink_prefill_chunked": (_i, [_vp, _vp, _vp, _vp, _vp, _vp, _vp, _i, _i, _i64, _i, _i, _i, _f, _i64, _i,
+                                      _vp]),
+    "kv_rolling_write": (_i, [_vp, _vp, _vp, _vp, _i, _i, _i, _i, _i, _i64, _i64, _i, _vp]),
+    "swa_sink_decode_step": (_i, [_vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _i, _i64, _f, _vp, _sz, _i, _vp]),
+    "swa_sink_decode_workspace_size": (_sz, [_i, _i, _i, _i]),
+    "swa_last_error_string": (ctypes.c_char_p, []),
+    "swa_device_status": (_i, [_vp]),
+    "swa_selftest_wait_timeout": (_i, [_i64, _vp]),
+    "swa_selftest_umma": (_i, [_vp, _vp, _vp, _i, _vp]),
+    "swa_prefill_tile_plan": (_i, [_i64, _i64, _i64, _i, _i, ctypes.POINTER(ctypes.c_int), _i]),
+}
+
+_lib = None
+
+
+class SwaError(RuntimeError):
+    def __init__(self, fn: str, code: int, msg: str):
+        super().__init__(f"{fn} failed with {_STATUS_NAMES.get(code, code)}: {msg}")
+        self.code = code
+
+
+def library_path() -> str:
+    return _build.LIB
+
+
+def lib(build_if_missing: bool = False):
+    """The loaded library (ctypes.CDLL with typed entry points)."""
+    global _lib
+    if _lib is None:
+        path = _build.LIB
+        if build_if_missing:
+            path = _build.build()
+        if not os.path.exists(path):
+            raise RuntimeError(f"the CUDA library {path} is not built; run __graft_entry__.build() or "
+                               "python -m sliding_window_softmax_swa_gb300.build")
+        L = ctypes.CDLL(path)
+        for name, (res, args) in SIGNATURES.items():
+            f = getattr(L, name)
+            f.restype, f.argtypes = res, args
+        _lib = L
+    return _lib
+
+
+def last_error() -> str:
+    return lib().swa_last_error_string().decode()
+
+
+def _check(fn: str, rc: int):
+    if rc != SWA_OK:
+        raise SwaError(fn, rc, last_error())
+
+
+def _stream(stream) -> int:
+    if stream is None:
+        return torch.cuda.current_stream().cuda_stream
+    return stream.cuda_stream if hasattr(stream, "cuda_stream") else int(stream)
+
+
+def _dtype_code(t: torch.Tensor) -> int:
+    if t.dtype == torch.bfloat16:
+        return SWA_BF16
+    if t.dtype == torch.float32:
+        return SWA_F32
+    raise TypeError(f"unsupported dtype {t.dtype}; use bfloat16 or float32")
+
+
+def _dev(*ts):
+    for t in ts:
+        if t is None:
+            continue
+        if not t.is_cuda:
+            raise ValueError("tensors must live on a CUDA device")
+        if not t.is_contiguous():
+            raise ValueError("tensors must be contiguous")
+
+
+def _ptr(t):
+    return None if t is None else t.data_ptr()
+
+
+def swa_sink_prefill(q, k, v, w: int, s: int, scale: float | None = None, o=None, lse=None,
+                     k_cache=None, v_cache=None, pos0: int = 0, stream=None):
+    """Prefill of q, k, v [B, H, L, d] at absolute positions pos0..pos0+L-1 -> o [B, H, L, d].
+    With ``lse`` (a [B, H, L] float32 tensor) the log-sum-exp of each row is written too."""
+    B, H, L, d = q.shape
+    assert k.shape == q.shape and v.shape == q.shape and k.dtype == q.dtype and v.dtype == q.dtype
+    if o is None:
+        o = torch.empty_like(q)
+    _dev(q, k, v, o, lse, k_cache, v_cache)
+    scale = (1.0 / d ** 0.5) if scale is None else scale
+    _check("swa_sink_prefill", lib().swa_sink_prefill(
+        _ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), _ptr(k_cache), _ptr(v_cache), pos0, B, H, L, d, w, s,
+        scale, _dtype_code(q), _stream(stream)))
+    return o
+
+
+def swa_sink_prefill_chunked(q, k, v, w: int, s: int, chunk: int, k_cache, v_cache, scale: float | None = None,
+                             o=None, lse=None, stream=None):
+    """Chunked prefill through the rolling cache (k_cache/v_cache [B, H, w, d] are overwritten)."""
+    B, H, L, d = q.shape
+    if o is None:
+        o = torch.empty_like(q)
+    _dev(q, k, v, o, lse, k_cache, v_cache)
+    scale = (1.0 / d ** 0.5) if scale is None else scale
+    _check("swa_sink_prefill_chunked", lib().swa_sink_prefill_chunked(
+        _ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), _ptr(k_cache), _ptr(v_cache), B, H, L, d, w, s, scale,
+        chunk, _dtype_code(q), _stream(stream)))
+    return o
+
+
+def kv_rolling_write(k_cache, v_cache, k_new, v_new, w: int, s: int, pos0: int, stream=None):
+    """Write k_new/v_new [B, H, n, d] (positions pos0..pos0+n-1) into the caches [B, H, w, d]."""
+    B, H, n, d = k_new.shape
+    assert k_cache.shape == (B, H, w, d) and v_cache.shape == (B, H, w, d)
+    _dev(k_cache, v_cache, k_new, v_new)
+    _check("kv_rolling_write", lib().kv_rolling_write(
+        _ptr(k_cache), _ptr(v_cache), _ptr(k_new), _ptr(v_new), B, H, d, w, s, pos0, n, _dtype_code(k_new),
+        _stream(stream)))
+
+
+def swa_sink_decode_workspace_size(B: int, H: int, d: int, w: int) -> int:
+    return int(lib().swa_sink_decode_workspace_size(B, H, d, w))
+
+
+def swa_sink_decode_step(q, k_cache, v_cache, t: int, w: int, s: int, scale: float | None = None, o=None,
+                         lse=None, workspace=None, stream=None):
+    """Decode for q [B, H, d] at position t against the caches [B, H, w, d] -> o [B, H, d]."""
+    B, H, d = q.shape
+    if o is None:
+        o = torch.empty_like(q)
+    need = swa_sink_decode_workspace_size(B, H, d, w)
+    if workspace is None and need > 0:
+        workspace = torch.empty(need, dtype=torch.uint8, device=q.device)
+    _dev(q, k_cache, v_cache, o, lse, workspace)
+    scale = (1.0 / d ** 0.5) if scale is None else scale
+    wbytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    _check("swa_sink_decode_step", lib().swa_sink_decode_step(
+        _ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(o), _ptr(lse), B, H, d, w, s, t, scale, _ptr(workspace),
+        wbytes, _dtype_code(q), _stream(stream)))
+    return o
+
+
+def prefill_tile_plan(q0: int, q1: int, pos0: int, w: int, s: int):
+    """The key tiles the bf16 prefill walks for query rows q0..q1: list of (src, row0, pbase, chi)."""
+    buf = (ctypes.c_int * (4 * 256))()
+    n = lib().swa_prefill_tile_plan(q0, q1, pos0, w, s, buf, 256)
+    if n < 0:
+        raise SwaError("swa_prefill_tile_plan", n, last_error())
+    return [tuple(buf[4 * i:4 * i + 4]) for i in range(min(n, 256))]
+
+
+def swa_device_status(stream=None) -> int:
+    """Synchronise the stream and return (and clear) the device error status (0 = fine)."""
+    return lib().swa_device_status(_stream(stream))

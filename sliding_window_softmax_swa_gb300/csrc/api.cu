@@ -1,0 +1,247 @@
+// api.cu -- the C ABI of include/swa_sink.h: argument validation, dispatch to the kernels' launchers,
+// the per-device error word, the thread-local error string and the tensor-map encoder lookup.
+#include <stdarg.h>
+#include <stdio.h>
+#include <string.h>
+
+#include <mutex>
+
+#include "../../include/swa_sink.h"
+#include "swa_device.cuh"
+#include "swa_internal.h"
+
+namespace swa {
+
+// One error word per device.  Kernels receive its address; swa_device_status() reads and clears it.
+__device__ unsigned g_swa_status_word;
+
+static thread_local char t_err[512];
+
+int fail(int code, const char *fmt, ...) {
+    va_list ap;
+    va_start(ap, fmt);
+    vsnprintf(t_err, sizeof(t_err), fmt, ap);
+    va_end(ap);
+    return code;
+}
+
+unsigned *device_status_word() {
+    static std::mutex mu;
+    static unsigned *ptrs[64] = {nullptr};
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess || dev < 0 || dev >= 64) {
+        fail(SWA_ERR_CUDA, "cudaGetDevice: %s", cudaGetErrorString(e));
+        return nullptr;
+    }
+    std::lock_guard<std::mutex> lk(mu);
+    if (!ptrs[dev]) {
+        void *p = nullptr;
+        e = cudaGetSymbolAddress(&p, g_swa_status_word);
+        if (e != cudaSuccess) {
+            fail(SWA_ERR_CUDA, "cudaGetSymbolAddress(status word): %s", cudaGetErrorString(e));
+            return nullptr;
+        }
+        ptrs[dev] = static_cast<unsigned *>(p);
+    }
+    return ptrs[dev];
+}
+
+EncodeTiledFn encode_tiled_fn() {
+    static std::once_flag once;
+    static EncodeTiledFn fn = nullptr;
+    std::call_once(once, [] {
+        void *p = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
+                cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<EncodeTiledFn>(p);
+    });
+    return fn;
+}
+
+}  // namespace swa
+
+using namespace swa;
+
+static inline bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+static int esize_of(int dtype) { return dtype == SWA_BF16 ? 2 : dtype == SWA_F32 ? 4 : 0; }
+
+static int check_common(int B, int H, int d, int w, int s, int dtype) {
+    if (esize_of(dtype) == 0) return fail(SWA_ERR_INVALID, "dtype %d is neither SWA_BF16 nor SWA_F32", dtype);
+    if (B < 1 || H < 1) return fail(SWA_ERR_INVALID, "B=%d, H=%d must be >= 1", B, H);
+    if ((int64_t)B * H > 65535 * 32)
+        return fail(SWA_ERR_UNSUPPORTED, "B*H=%lld exceeds the supported %d", (long long)B * H, 65535 * 32);
+    if (w < 1) return fail(SWA_ERR_INVALID, "w=%d must be >= 1", w);
+    if (s < 0 || s >= w) return fail(SWA_ERR_INVALID, "need 0 <= s < w (s=%d, w=%d)", s, w);
+    if (!(d == 16 || d == 32 || d == 64 || d == 128))
+        return fail(SWA_ERR_UNSUPPORTED, "d=%d not in {16, 32, 64, 128}", d);
+    return SWA_OK;
+}
+
+extern "C" const char *swa_last_error_string(void) { return t_err; }
+
+extern "C" int swa_device_status(void *stream) {
+    t_err[0] = 0;
+    cudaError_t e = cudaStreamSynchronize(static_cast<cudaStream_t>(stream));
+    if (e != cudaSuccess) return fail(SWA_ERR_CUDA, "cudaStreamSynchronize: %s", cudaGetErrorString(e));
+    unsigned word = 0;
+    e = cudaMemcpyFromSymbol(&word, g_swa_status_word, sizeof(word));
+    if (e != cudaSuccess) return fail(SWA_ERR_CUDA, "reading the device error word: %s", cudaGetErrorString(e));
+    if (word != 0) {
+        unsigned zero = 0;
+        cudaMemcpyToSymbol(g_swa_status_word, &zero, sizeof(zero));
+        if (word & kDevTimeout)
+            return fail(SWA_ERR_TIMEOUT, "a bounded device wait ran out (error word 0x%08x, site %u)", word,
+                        (word >> kWhereShift) & 0xFFu);
+        return fail(SWA_ERR_CUDA, "device consistency check failed (error word 0x%08x)", word);
+    }
+    return SWA_OK;
+}
+
+static int prefill_impl(const void *q, const void *k, const void *v, void *o, float *lse, const void *k_cache,
+                        const void *v_cache, int64_t pos0, int B, int H, int64_t L, int d, int w, int s, float scale,
+                        int dtype, int64_t seq_stride, cudaStream_t stream) {
+    if (L == 0) return SWA_OK;
+    PrefillArgs a{q, k, v, o, lse, k_cache, v_cache, pos0, B * H, L, d, w, s, scale, seq_stride, stream};
+    if (dtype == SWA_BF16) {
+        if (d != 128) return fail(SWA_ERR_UNSUPPORTED, "bf16 prefill needs d = 128 (got %d)", d);
+        return launch_prefill_bf16_tc(a);
+    }
+    return launch_prefill_f32(a);
+}
+
+static int check_prefill(const void *q, const void *k, const void *v, const void *o, const float *lse,
+                         int64_t pos0, int B, int H, int64_t L, int d, int w, int s, float scale, int dtype) {
+    int rc = check_common(B, H, d, w, s, dtype);
+    if (rc) return rc;
+    if (L < 0) return fail(SWA_ERR_INVALID, "L=%lld must be >= 0", (long long)L);
+    if (pos0 < 0) return fail(SWA_ERR_INVALID, "pos0=%lld must be >= 0", (long long)pos0);
+    if (pos0 + L >= (int64_t(1) << 31))
+        return fail(SWA_ERR_UNSUPPORTED, "pos0 + L = %lld must be < 2^31", (long long)(pos0 + L));
+    if (!(scale == scale) || scale <= 0.f || scale > 1e30f)
+        return fail(SWA_ERR_INVALID, "scale must be a positive finite number");
+    if (L == 0) return SWA_OK;
+    if (!q || !k || !v || !o) return fail(SWA_ERR_INVALID, "q, k, v and o must be non-null");
+    if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o))
+        return fail(SWA_ERR_INVALID, "q, k, v and o must be 16-byte aligned");
+    if (lse && (reinterpret_cast<uintptr_t>(lse) & 3u)) return fail(SWA_ERR_INVALID, "lse must be 4-byte aligned");
+    return SWA_OK;
+}
+
+extern "C" int swa_sink_prefill(const void *q, const void *k, const void *v, void *o, float *lse,
+                                const void *k_cache, const void *v_cache, int64_t pos0, int B, int H, int64_t L,
+                                int d, int w, int s, float scale, int dtype, void *stream) {
+    t_err[0] = 0;
+    int rc = check_prefill(q, k, v, o, lse, pos0, B, H, L, d, w, s, scale, dtype);
+    if (rc) return rc;
+    if (L == 0) return SWA_OK;
+    if (pos0 > 0) {
+        if (!k_cache || !v_cache) return fail(SWA_ERR_INVALID, "pos0 > 0 needs k_cache and v_cache");
+        if (!aligned16(k_cache) || !aligned16(v_cache))
+            return fail(SWA_ERR_INVALID, "k_cache and v_cache must be 16-byte aligned");
+    }
+    return prefill_impl(q, k, v, o, lse, k_cache, v_cache, pos0, B, H, L, d, w, s, scale, dtype, L,
+                        static_cast<cudaStream_t>(stream));
+}
+
+extern "C" int swa_sink_prefill_chunked(const void *q, const void *k, const void *v, void *o, float *lse,
+                                        void *k_cache, void *v_cache, int B, int H, int64_t L, int d, int w, int s,
+                                        float scale, int64_t chunk, int dtype, void *stream) {
+    t_err[0] = 0;
+    int rc = check_prefill(q, k, v, o, lse, 0, B, H, L, d, w, s, scale, dtype);
+    if (rc) return rc;
+    if (chunk < 1) return fail(SWA_ERR_INVALID, "chunk=%lld must be >= 1", (long long)chunk);
+    if (L == 0) return SWA_OK;
+    if (!k_cache || !v_cache) return fail(SWA_ERR_INVALID, "k_cache and v_cache must be non-null");
+    if (!aligned16(k_cache) || !aligned16(v_cache))
+        return fail(SWA_ERR_INVALID, "k_cache and v_cache must be 16-byte aligned");
+    const int es = esize_of(dtype);
+    const size_t row_bytes = static_cast<size_t>(d) * es;
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    for (int64_t c0 = 0; c0 < L; c0 += chunk) {
+        const int64_t n = (L - c0 < chunk) ? (L - c0) : chunk;
+        const size_t off = static_cast<size_t>(c0) * row_bytes;
+        const char *qc = static_cast<const char *>(q) + off;
+        const char *kc = static_cast<const char *>(k) + off;
+        const char *vc = static_cast<const char *>(v) + off;
+        char *oc = static_cast<char *>(o) + off;
+        float *lc = lse ? lse + c0 : nullptr;
+        rc = prefill_impl(qc, kc, vc, oc, lc, k_cache, v_cache, c0, B, H, n, d, w, s, scale, dtype, L, st);
+        if (rc) return rc;
+        rc = launch_kv_write(k_cache, v_cache, kc, vc, B * H, d, w, s, c0, n, L, es, st);
+        if (rc) return rc;
+    }
+    return SWA_OK;
+}
+
+extern "C" int kv_rolling_write(void *k_cache, void *v_cache, const void *k_new, const void *v_new, int B, int H,
+                                int d, int w, int s, int64_t pos0, int64_t n, int dtype, void *stream) {
+    t_err[0] = 0;
+    int rc = check_common(B, H, d, w, s, dtype);
+    if (rc) return rc;
+    if (pos0 < 0 || n < 0) return fail(SWA_ERR_INVALID, "pos0=%lld and n=%lld must be >= 0", (long long)pos0,
+                                       (long long)n);
+    if (n == 0) return SWA_OK;
+    if (!k_cache || !v_cache || !k_new || !v_new)
+        return fail(SWA_ERR_INVALID, "k_cache, v_cache, k_new and v_new must be non-null");
+    if (!aligned16(k_cache) || !aligned16(v_cache) || !aligned16(k_new) || !aligned16(v_new))
+        return fail(SWA_ERR_INVALID, "cache and new tensors must be 16-byte aligned");
+    return launch_kv_write(k_cache, v_cache, k_new, v_new, B * H, d, w, s, pos0, n, n, esize_of(dtype),
+                           static_cast<cudaStream_t>(stream));
+}
+
+extern "C" size_t swa_sink_decode_workspace_size(int B, int H, int d, int w) {
+    if (B < 1 || H < 1 || d < 1 || w < 1) return 0;
+    return decode_workspace_bytes(B * H, d, w);
+}
+
+extern "C" int swa_sink_decode_step(const void *q, const void *k_cache, const void *v_cache, void *o, float *lse,
+                                    int B, int H, int d, int w, int s, int64_t t, float scale, void *workspace,
+                                    size_t workspace_bytes, int dtype, void *stream) {
+    t_err[0] = 0;
+    int rc = check_common(B, H, d, w, s, dtype);
+    if (rc) return rc;
+    if (t < 0 || t >= (int64_t(1) << 62)) return fail(SWA_ERR_INVALID, "t=%lld out of range", (long long)t);
+    if (!(scale == scale) || scale <= 0.f || scale > 1e30f)
+        return fail(SWA_ERR_INVALID, "scale must be a positive finite number");
+    if (!q || !k_cache || !v_cache || !o) return fail(SWA_ERR_INVALID, "q, caches and o must be non-null");
+    if (!aligned16(q) || !aligned16(k_cache) || !aligned16(v_cache) || !aligned16(o))
+        return fail(SWA_ERR_INVALID, "q, caches and o must be 16-byte aligned");
+    if (lse && (reinterpret_cast<uintptr_t>(lse) & 3u)) return fail(SWA_ERR_INVALID, "lse must be 4-byte aligned");
+    const size_t need = decode_workspace_bytes(B * H, d, w);
+    if (workspace_bytes < need)
+        return fail(SWA_ERR_INVALID, "workspace of %zu bytes is smaller than the %zu needed", workspace_bytes, need);
+    if (need > 0 && (!workspace || (reinterpret_cast<uintptr_t>(workspace) & 255u)))
+        return fail(SWA_ERR_INVALID, "workspace must be non-null and 256-byte aligned");
+    DecodeArgs a{q, k_cache, v_cache, o, lse, B * H, d, w, s, t, scale, workspace, workspace_bytes,
+                 esize_of(dtype), static_cast<cudaStream_t>(stream)};
+    return launch_decode(a);
+}
+
+extern "C" int swa_selftest_wait_timeout(int64_t timeout_ns, void *stream) {
+    t_err[0] = 0;
+    if (timeout_ns < 1 || timeout_ns > 1000000000LL)
+        return fail(SWA_ERR_INVALID, "timeout_ns=%lld not in [1, 1e9]", (long long)timeout_ns);
+    return launch_selftest_wait_timeout(static_cast<uint64_t>(timeout_ns), static_cast<cudaStream_t>(stream));
+}
+
+extern "C" int swa_selftest_umma(const void *a, const void *b, float *c, int mode, void *stream) {
+    t_err[0] = 0;
+    if (!a || !b || !c) return fail(SWA_ERR_INVALID, "a, b and c must be non-null");
+    if (!aligned16(a) || !aligned16(b) || !aligned16(c)) return fail(SWA_ERR_INVALID, "a, b, c must be 16-byte aligned");
+    if (mode < 0 || mode > 2) return fail(SWA_ERR_INVALID, "mode=%d not in {0, 1, 2}", mode);
+    return launch_selftest_umma(a, b, c, mode, static_cast<cudaStream_t>(stream));
+}
+
+extern "C" int swa_prefill_tile_plan(int64_t q0, int64_t q1, int64_t pos0, int w, int s, int *tiles, int max_tiles) {
+    t_err[0] = 0;
+    if (w < 1 || s < 0 || s >= w) return fail(SWA_ERR_INVALID, "need 0 <= s < w (s=%d, w=%d)", s, w);
+    if (pos0 < 0 || q0 < pos0 || q1 < q0 || q1 >= (int64_t(1) << 31))
+        return fail(SWA_ERR_INVALID, "need 0 <= pos0 <= q0 <= q1 < 2^31");
+    if (!tiles || max_tiles < 0) return fail(SWA_ERR_INVALID, "tiles must be non-null");
+    return prefill_tile_plan(static_cast<int>(q0), static_cast<int>(q1), static_cast<int>(pos0), w, s, tiles,
+                             max_tiles);
+}

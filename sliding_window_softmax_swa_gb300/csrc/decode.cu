@@ -1,0 +1,244 @@
+// decode.cu -- swa_sink_decode_step: one streaming-decode query per (b, h) against the rolling cache.
+//
+// After positions 0..t have been written, the cache slots 0..min(t+1, w)-1 hold exactly the key set
+// K(t) = sinks + the last m positions (page "滑窗与固定稀疏", eq attn-fixed-streaming), and softmax
+// attention does not depend on the order of its keys ("模糊窗口注意力", section 3 introduction), so the
+// kernel attends every valid slot in slot order without looking at positions.
+//
+// The work is HBM-bound: every step reads the whole valid cache (2 * nvalid * d * esize bytes per
+// (b, h)) once.  Design:
+//   * grid (nsplit, B*H); a split covers a contiguous slot range (split-K over the cache);
+//   * a row of the cache is read by LPR = d*esize/16 lanes with one 16-byte streaming load each
+//     (ld.global.cs: read once, evict first), so a warp reads RPW = 32/LPR whole rows per load and
+//     every load instruction is fully coalesced;
+//   * each lane issues U key loads and U value loads before using any of them (memory-level
+//     parallelism), then the partial dot products are summed over the LPR lanes of a row with
+//     xor-shuffles, and an online softmax (running max m, sum l, accumulator) is kept per row group;
+//   * the row groups of a CTA are merged through shared memory; with nsplit > 1 the CTA writes its
+//     partial (acc, m, l) to the caller's workspace and a second kernel merges the splits with the
+//     log-sum-exp identity  o = sum_j 2^(m_j - M) acc_j / sum_j 2^(m_j - M) l_j,  M = max_j m_j.
+// Scores are kept in log2 units (x = scale * log2(e) * q.k) so exp is a single exp2.
+#include <math.h>
+
+#include "../../include/swa_sink.h"
+#include "swa_device.cuh"
+#include "swa_internal.h"
+
+namespace swa {
+
+constexpr int kDecThreads = 256;
+constexpr int kDecWarps = kDecThreads / 32;
+constexpr int kMaxSplits = 64;
+constexpr int kMinSlotsPerSplit = 256;
+
+__device__ __forceinline__ void unpack16(const uint4 &u, float (&f)[8], __nv_bfloat16) {
+    const uint32_t w[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        f[2 * i] = __uint_as_float(w[i] << 16);
+        f[2 * i + 1] = __uint_as_float(w[i] & 0xFFFF0000u);
+    }
+}
+__device__ __forceinline__ void unpack16(const uint4 &u, float (&f)[4], float) {
+    f[0] = __uint_as_float(u.x);
+    f[1] = __uint_as_float(u.y);
+    f[2] = __uint_as_float(u.z);
+    f[3] = __uint_as_float(u.w);
+}
+__device__ __forceinline__ void store_out(__nv_bfloat16 *p, float x) { *p = __float2bfloat16_rn(x); }
+__device__ __forceinline__ void store_out(float *p, float x) { *p = x; }
+
+template <typename T, int D, int U>
+__global__ void __launch_bounds__(kDecThreads) decode_kernel(const T *__restrict__ q, const T *__restrict__ kc,
+                                                             const T *__restrict__ vc, T *__restrict__ o,
+                                                             float *__restrict__ lse, float *__restrict__ part,
+                                                             int w, int nvalid, int per_split, int nsplit,
+                                                             float scale_log2) {
+    constexpr int EPL = 16 / sizeof(T);  // elements per 16-byte chunk
+    constexpr int LPR = D / EPL;         // lanes per cache row
+    constexpr int RPW = 32 / LPR;        // rows per warp per load
+    constexpr int G = kDecWarps * RPW;   // row groups per CTA
+    static_assert(LPR >= 1 && LPR <= 32 && 32 % LPR == 0, "row must map onto a power-of-two lane group");
+
+    __shared__ float sm_m[G], sm_l[G];
+    __shared__ float sm_acc[G][D];
+
+    const int split = blockIdx.x;
+    const int64_t bh = blockIdx.y;
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    const int sub = lane % LPR;
+    const int grp = warp * RPW + lane / LPR;
+    const int j0 = split * per_split;
+    const int j1 = min(nvalid, j0 + per_split);
+
+    float qf[EPL];
+    {
+        const uint4 qu = __ldg(reinterpret_cast<const uint4 *>(q + bh * D) + sub);
+        unpack16(qu, qf, T());
+#pragma unroll
+        for (int e = 0; e < EPL; ++e) qf[e] *= scale_log2;
+    }
+    const uint4 *kb = reinterpret_cast<const uint4 *>(kc + bh * w * D) + sub;
+    const uint4 *vb = reinterpret_cast<const uint4 *>(vc + bh * w * D) + sub;
+
+    float m = -INFINITY, l = 0.f, acc[EPL];
+#pragma unroll
+    for (int e = 0; e < EPL; ++e) acc[e] = 0.f;
+
+    for (int jblk = j0; jblk < j1; jblk += G * U) {  // uniform over the CTA: shuffles stay converged
+        uint4 kr[U], vr[U];
+#pragma unroll
+        for (int u = 0; u < U; ++u) {
+            const int j = jblk + u * G + grp;
+            if (j < j1) {
+                kr[u] = __ldcs(kb + static_cast<int64_t>(j) * LPR);
+                vr[u] = __ldcs(vb + static_cast<int64_t>(j) * LPR);
+            } else {
+                kr[u] = make_uint4(0, 0, 0, 0);
+                vr[u] = make_uint4(0, 0, 0, 0);
+            }
+        }
+        float x[U];
+        float mt = -INFINITY;
+#pragma unroll
+        for (int u = 0; u < U; ++u) {
+            float kf[EPL];
+            unpack16(kr[u], kf, T());
+            float dot = 0.f;
+#pragma unroll
+            for (int e = 0; e < EPL; ++e) dot = fmaf(qf[e], kf[e], dot);
+#pragma unroll
+            for (int off = LPR / 2; off >= 1; off >>= 1) dot += __shfl_xor_sync(0xFFFFFFFFu, dot, off);
+            x[u] = (jblk + u * G + grp < j1) ? dot : -INFINITY;
+            mt = fmaxf(mt, x[u]);
+        }
+        const float mn = fmaxf(m, mt);
+        if (mn == -INFINITY) continue;  // this group had no valid row in the block
+        const float alpha = exp2f(m - mn);  // m == -inf -> 0
+        l *= alpha;
+#pragma unroll
+        for (int e = 0; e < EPL; ++e) acc[e] *= alpha;
+#pragma unroll
+        for (int u = 0; u < U; ++u) {
+            const float p = exp2f(x[u] - mn);  // invalid rows: exp2(-inf) = 0
+            float vf[EPL];
+            unpack16(vr[u], vf, T());
+            l += p;
+#pragma unroll
+            for (int e = 0; e < EPL; ++e) acc[e] = fmaf(p, vf[e], acc[e]);
+        }
+        m = mn;
+    }
+
+#pragma unroll
+    for (int e = 0; e < EPL; ++e) sm_acc[grp][sub * EPL + e] = acc[e];
+    if (sub == 0) {
+        sm_m[grp] = m;
+        sm_l[grp] = l;
+    }
+    __syncthreads();
+    if (threadIdx.x < D) {
+        const int c = threadIdx.x;
+        float M = -INFINITY;
+        for (int g = 0; g < G; ++g) M = fmaxf(M, sm_m[g]);
+        float L = 0.f, a = 0.f;
+        if (M != -INFINITY) {
+            for (int g = 0; g < G; ++g) {
+                const float f = exp2f(sm_m[g] - M);
+                L = fmaf(sm_l[g], f, L);
+                a = fmaf(sm_acc[g][c], f, a);
+            }
+        }
+        if (nsplit == 1) {
+            store_out(o + bh * D + c, a / L);
+            if (c == 0 && lse) lse[bh] = (M + log2f(L)) * 0.69314718055994531f;
+        } else {
+            float *pp = part + (bh * nsplit + split) * (D + 2);
+            pp[c] = a;
+            if (c == 0) {
+                pp[D] = M;
+                pp[D + 1] = L;
+            }
+        }
+    }
+}
+
+template <typename T, int D>
+__global__ void __launch_bounds__(D) decode_merge_kernel(const float *__restrict__ part, T *__restrict__ o,
+                                                         float *__restrict__ lse, int nsplit) {
+    const int64_t bh = blockIdx.x;
+    const int c = threadIdx.x;
+    const float *pp = part + bh * nsplit * (D + 2);
+    float M = -INFINITY;
+    for (int j = 0; j < nsplit; ++j) M = fmaxf(M, pp[j * (D + 2) + D]);
+    float L = 0.f, a = 0.f;
+    for (int j = 0; j < nsplit; ++j) {
+        const float mj = pp[j * (D + 2) + D];
+        if (mj == -INFINITY) continue;  // a split without a valid slot
+        const float f = exp2f(mj - M);
+        L = fmaf(pp[j * (D + 2) + D + 1], f, L);
+        a = fmaf(pp[j * (D + 2) + c], f, a);
+    }
+    store_out(o + bh * D + c, a / L);
+    if (c == 0 && lse) lse[bh] = (M + log2f(L)) * 0.69314718055994531f;
+}
+
+int decode_num_splits(int BH, int nvalid) {
+    const int target = 152 * 8;  // CTAs that keep every SM of a GB300 busy (8 x 256 threads per SM)
+    int ns = (target + BH - 1) / BH;
+    const int by_work = (nvalid + kMinSlotsPerSplit - 1) / kMinSlotsPerSplit;
+    if (ns > by_work) ns = by_work;
+    if (ns > kMaxSplits) ns = kMaxSplits;
+    if (ns < 1) ns = 1;
+    return ns;
+}
+
+size_t decode_workspace_bytes(int BH, int d, int w) {
+    const int ns = decode_num_splits(BH, w);  // the split count only grows with the valid slots (<= w)
+    if (ns <= 1) return 0;
+    return static_cast<size_t>(BH) * ns * (d + 2) * sizeof(float);
+}
+
+template <typename T, int D>
+static int launch_typed(const DecodeArgs &a, int nvalid, int ns, int per_split, float sl2) {
+    constexpr int U = (sizeof(T) == 2 && D >= 64) ? 4 : 2;
+    const dim3 grid(ns, a.BH), block(kDecThreads);
+    float *part = static_cast<float *>(a.workspace);
+    decode_kernel<T, D, U><<<grid, block, 0, a.stream>>>(
+        static_cast<const T *>(a.q), static_cast<const T *>(a.k_cache), static_cast<const T *>(a.v_cache),
+        static_cast<T *>(a.o), a.lse, part, a.w, nvalid, per_split, ns, sl2);
+    if (ns > 1)
+        decode_merge_kernel<T, D><<<a.BH, D, 0, a.stream>>>(part, static_cast<T *>(a.o), a.lse, ns);
+    return 0;
+}
+
+int launch_decode(const DecodeArgs &a) {
+    const int nvalid = static_cast<int>(a.t + 1 < a.w ? a.t + 1 : a.w);
+    const int ns = decode_num_splits(a.BH, nvalid);
+    const int per_split = (nvalid + ns - 1) / ns;
+    const float sl2 = a.scale * 1.4426950408889634f;
+    if (ns > 1 && (!a.workspace || a.workspace_bytes < static_cast<size_t>(a.BH) * ns * (a.d + 2) * sizeof(float)))
+        return fail(SWA_ERR_INVALID, "decode needs %d splits but the workspace is too small", ns);
+    if (a.esize == 2) {
+        switch (a.d) {
+            case 16: launch_typed<__nv_bfloat16, 16>(a, nvalid, ns, per_split, sl2); break;
+            case 32: launch_typed<__nv_bfloat16, 32>(a, nvalid, ns, per_split, sl2); break;
+            case 64: launch_typed<__nv_bfloat16, 64>(a, nvalid, ns, per_split, sl2); break;
+            case 128: launch_typed<__nv_bfloat16, 128>(a, nvalid, ns, per_split, sl2); break;
+            default: return fail(SWA_ERR_UNSUPPORTED, "decode: d=%d", a.d);
+        }
+    } else {
+        switch (a.d) {
+            case 16: launch_typed<float, 16>(a, nvalid, ns, per_split, sl2); break;
+            case 32: launch_typed<float, 32>(a, nvalid, ns, per_split, sl2); break;
+            case 64: launch_typed<float, 64>(a, nvalid, ns, per_split, sl2); break;
+            case 128: launch_typed<float, 128>(a, nvalid, ns, per_split, sl2); break;
+            default: return fail(SWA_ERR_UNSUPPORTED, "decode: d=%d", a.d);
+        }
+    }
+    cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) return fail(SWA_ERR_CUDA, "decode launch: %s", cudaGetErrorString(e));
+    return SWA_OK;
+}
+
+}  // namespace swa

@@ -1,0 +1,622 @@
+// prefill_tc.cu -- bf16 prefill of causal sliding-window attention with sinks on the sm_103a tensor
+// cores (TMA + tcgen05.mma + TMEM), plus two diagnostics kernels (bounded-wait timeout, UMMA tile).
+//
+// The computation (hyper.ai summary of arXiv 2608.28444, section "带 Sink 的滑动窗口注意力"; causal
+// softmax attention of "模糊窗口注意力" section 2.1, eq (1)): query t attends
+//     K(t) = { i <= t : i < s  or  i >= t - m + 1 },  m = w - s,
+// with softmax over scale * q.k.  A fixed sparsity pattern known from positions alone ("滑窗与固定稀疏":
+// O(n^2) -> O(n k), banded patterns are hardware friendly), so each CTA walks only the key tiles that
+// intersect the band or the sink block of its query tile; no skipped tile is ever loaded.
+//
+// CTA = one tile of 128 query rows of one (b, h); 192 threads in three roles:
+//   warps 0-3  softmax + epilogue: thread r owns query row r (= TMEM lane r);
+//   warp 4     TMA producer: Q once, then K/V tiles into a 2-stage ring (128 rows x 128 bf16 each,
+//              two 64-column boxes with the 128-byte swizzle);
+//   warp 5     MMA issuer (one thread): S_j = Q K_j^T into one of two TMEM S buffers, O += P_j V_j
+//              into the TMEM O accumulator.  P_j (bf16) is written by the softmax threads into shared
+//              memory in the same swizzled K-major layout TMA produces for Q.
+// TMEM: S0 = columns [0,128), S1 = [128,256), O = [256,384) (fp32, lane = query row).
+// Pipeline: QK_{j+1} runs on the tensor cores while the softmax threads work on S_j; PV_j starts as
+// soon as P_j is in shared memory.  The online softmax keeps a running max in log2 units and only
+// rescales O (TMEM load, multiply, store) when the max grows by more than 8 (a factor 256), so p <= 256
+// always fits bf16/fp32 and the rescale is rare; O and l always share the same reference max.
+//
+// Key tiles.  For the query tile [q0, q1] the key positions needed are the sinks [0, min(s, blo)) and
+// the band [blo, q1] with blo = max(0, q0 - m + 1).  Positions >= pos0 are rows of this call's k/v;
+// positions < pos0 (chunked prefill) live in the rolling cache: slot p for p < s, slot
+// s + ((p - s) mod m) for the rest ("滑窗与固定稀疏", eq attn-fixed-rolling and eq attn-fixed-streaming).
+// A contiguous position range maps to at most two contiguous slot runs (the ring wraps once), so every
+// range becomes a list of 128-row tiles, each with: source, first row, position of its column 0, and
+// the last valid column.  Columns past the range end, positions past t and positions outside the
+// window are masked per row; interior tiles need no mask at all.  Every key position appears in
+// exactly one tile.  TMA zero-fills rows outside the source tensor.
+//
+// Every mbarrier wait is bounded (1 s).  A wait that runs out records the timeout in the device error
+// word and sets a CTA-wide abort flag; all roles leave their loops, the producer waits (bounded) for
+// its copies in flight, the MMA thread waits for its MMAs, and TMEM is freed before the CTA exits.
+#include <math.h>
+
+#include "../../include/swa_sink.h"
+#include "swa_device.cuh"
+#include "swa_internal.h"
+
+namespace swa {
+namespace tc {
+
+constexpr int BM = 128;                    // query rows per CTA
+constexpr int BN = 128;                    // keys per tile
+constexpr int HD = 128;                    // head dimension
+constexpr int NST = 2;                     // K/V pipeline stages
+constexpr uint32_t HALF_BYTES = 128 * 128;  // one 64-column half of a 128-row bf16 tile (16 KB)
+constexpr uint32_t TILE_BYTES = 2 * HALF_BYTES;
+constexpr int MAX_TILES = 160;
+constexpr int kThreads = 192;
+constexpr uint32_t kTmemCols = 512;
+constexpr uint32_t kColS0 = 0, kColS1 = 128, kColO = 256;
+constexpr float kRescaleLog2 = 8.f;  // rescale O only when the running max grows by more than 2^8
+
+constexpr uint32_t OFF_Q = 0;
+constexpr uint32_t OFF_K = OFF_Q + TILE_BYTES;
+constexpr uint32_t OFF_V = OFF_K + NST * TILE_BYTES;
+constexpr uint32_t OFF_P = OFF_V + NST * TILE_BYTES;
+constexpr uint32_t OFF_BAR = OFF_P + TILE_BYTES;
+constexpr uint32_t OFF_MISC = OFF_BAR + 256;
+constexpr uint32_t OFF_TILES = OFF_MISC + 64;
+constexpr uint32_t SMEM_USED = OFF_TILES + MAX_TILES * 16;
+constexpr uint32_t SMEM_BYTES = SMEM_USED + 1024;  // slack to align the base to 1024 bytes
+
+constexpr uint32_t IDESC_QK = idesc_bf16_f32(128, 128, false, false);  // Q, K both K-major
+constexpr uint32_t IDESC_PV = idesc_bf16_f32(128, 128, false, true);   // P K-major, V MN-major
+
+struct Tile {
+    int row0;   // first source row (TMA row coordinate)
+    int pbase;  // absolute position of column 0
+    int chi;    // last valid column (columns past it belong to another tile or to nothing)
+    int src;    // 0 = this call's k/v rows, 1 = rolling cache
+};
+
+struct Params {
+    CUtensorMap tm_q, tm_k, tm_v, tm_kc, tm_vc;
+    void *o;
+    float *lse;
+    unsigned *status;
+    int64_t seq_stride;  // rows between (b, h) blocks of q/k/v/o/lse
+    int L, pos0, w, s, m, n_qtiles;
+    float scale_log2;
+    uint64_t timeout_ns;
+};
+
+// Build the key-tile list of the query tile [q0, q1] (absolute positions).  Returns the tile count
+// (entries past MAX_TILES are not stored; the caller treats a larger count as an error).
+__host__ __device__ int build_tiles(Tile *tl, int q0, int q1, int pos0, int s, int m, int w) {
+    int n = 0;
+    auto add_range = [&](int src, int pa, int pb, int rowbase) {  // positions [pa, pb]; row = p - rowbase
+        for (int p = pa; p <= pb; p += BN) {
+            if (n < MAX_TILES) {
+                tl[n].row0 = p - rowbase;
+                tl[n].pbase = p;
+                tl[n].chi = (pb - p < BN - 1) ? pb - p : BN - 1;
+                tl[n].src = src;
+            }
+            ++n;
+        }
+    };
+    const int blo = q0 - m + 1 > 0 ? q0 - m + 1 : 0;
+    const int sink_hi = s < blo ? s : blo;  // sinks [0, sink_hi) are not inside the band range
+    const int sink_cache = sink_hi < pos0 ? sink_hi : pos0;
+    // sinks first: their scores tend to be the largest, which keeps later rescales rare
+    if (sink_cache > 0) add_range(1, 0, sink_cache - 1, 0);
+    if (sink_hi > pos0) add_range(0, pos0, sink_hi - 1, pos0);
+    // band positions below pos0: in the cache
+    const int ce = q1 < pos0 - 1 ? q1 : pos0 - 1;
+    if (ce >= blo) {
+        const int ie = ce < s - 1 ? ce : s - 1;  // still in the sink block (slot = position)
+        if (ie >= blo) add_range(1, blo, ie, 0);
+        const int ra = blo > s ? blo : s;
+        if (ce >= ra) {  // ring positions [ra, ce]: one or two contiguous slot runs
+            const int sa = s + (ra - s) % m;
+            const int run1_end = ra + (w - 1 - sa);
+            if (ce <= run1_end) {
+                add_range(1, ra, ce, ra - sa);
+            } else {
+                add_range(1, ra, run1_end, ra - sa);
+                add_range(1, run1_end + 1, ce, run1_end + 1 - s);
+            }
+        }
+    }
+    // band positions from pos0 on: rows of this call's k/v
+    const int ca = blo > pos0 ? blo : pos0;
+    if (q1 >= ca) add_range(0, ca, q1, pos0);
+    return n;
+}
+
+__device__ __forceinline__ float ex2(float x) {
+    float y;
+    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+    return y;
+}
+
+// Bounded wait that ignores the CTA abort flag: used only to drain copies/MMAs before exit.
+__device__ __noinline__ bool mbar_wait_drain(uint64_t *bar, uint32_t parity) {
+    const uint32_t a = smem_u32(bar);
+    const uint64_t t0 = globaltimer_ns();
+    while (!mbar_try_wait(a, parity)) {
+        if (globaltimer_ns() - t0 > kWaitTimeoutNs) return false;
+    }
+    return true;
+}
+
+__device__ __forceinline__ void issue_qk(uint32_t d_tmem, uint32_t q_addr, uint32_t k_addr) {
+#pragma unroll
+    for (int kk = 0; kk < HD / 16; ++kk) {
+        const uint32_t off = (kk >> 2) * HALF_BYTES + (kk & 3) * 32;
+        umma_ss(d_tmem, sdesc_sw128(q_addr + off, 16, 1024), sdesc_sw128(k_addr + off, 16, 1024), IDESC_QK,
+                kk > 0 ? 1u : 0u);
+    }
+}
+
+__device__ __forceinline__ void issue_pv(uint32_t d_tmem, uint32_t p_addr, uint32_t v_addr, bool accumulate) {
+#pragma unroll
+    for (int kk = 0; kk < BN / 16; ++kk) {
+        const uint32_t a_off = (kk >> 2) * HALF_BYTES + (kk & 3) * 32;  // P: 16 keys along the K-major row
+        const uint32_t b_off = kk * 16 * 128;                            // V: 16 key rows of 128 bytes
+        umma_ss(d_tmem, sdesc_sw128(p_addr + a_off, 16, 1024), sdesc_sw128(v_addr + b_off, HALF_BYTES, 1024),
+                IDESC_PV, (accumulate || kk > 0) ? 1u : 0u);
+    }
+}
+
+__global__ void __launch_bounds__(kThreads, 1) swa_prefill_tc_kernel(const __grid_constant__ Params P) {
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t *sm = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    uint64_t *bars = reinterpret_cast<uint64_t *>(sm + OFF_BAR);
+    uint64_t *qfull = bars;
+    uint64_t *kfull = bars + 1;
+    uint64_t *vfull = kfull + NST;
+    uint64_t *kvempty = vfull + NST;
+    uint64_t *sfull = kvempty + NST;  // [2]
+    uint64_t *pfull = sfull + 2;
+    uint64_t *pvdone = pfull + 1;
+    uint64_t *ofull = pvdone + 1;
+    uint64_t *drain = ofull + 1;
+    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(sm + OFF_MISC);
+    volatile int *abort_flag = reinterpret_cast<volatile int *>(sm + OFF_MISC + 4);
+    int *ntiles_s = reinterpret_cast<int *>(sm + OFF_MISC + 8);
+    Tile *tiles = reinterpret_cast<Tile *>(sm + OFF_TILES);
+
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int qtile = P.n_qtiles - 1 - static_cast<int>(blockIdx.x);  // full-window tiles first
+    const int bh = blockIdx.y;
+    const int row_start = qtile * BM;  // first row of this call's rows
+    const int q0 = P.pos0 + row_start;
+    const int q1 = P.pos0 + min(row_start + BM, P.L) - 1;
+
+    if (threadIdx.x == 0) {
+        *abort_flag = 0;
+        *ntiles_s = build_tiles(tiles, q0, q1, P.pos0, P.s, P.m, P.w);
+        mbar_init(qfull, 1);
+        for (int i = 0; i < NST; ++i) {
+            mbar_init(&kfull[i], 1);
+            mbar_init(&vfull[i], 1);
+            mbar_init(&kvempty[i], 1);
+        }
+        mbar_init(&sfull[0], 1);
+        mbar_init(&sfull[1], 1);
+        mbar_init(pfull, BM);
+        mbar_init(pvdone, 1);
+        mbar_init(ofull, 1);
+        mbar_init(drain, 1);
+        mbar_init_fence();
+    }
+    if (warp == 0) {
+        tmem_alloc(tmem_slot, kTmemCols);
+        tmem_relinquish();
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = *tmem_slot;
+    const int nt = *ntiles_s;
+    const bool ok = nt >= 1 && nt <= MAX_TILES;
+    if (!ok && threadIdx.x == 0) atomicOr(P.status, kDevBadArg);
+    const WaitCtl wc{abort_flag, P.status, P.timeout_ns};
+
+    if (warp == 4) {
+        // ------------------------------------------------------------------ TMA producer
+        if (lane == 0 && ok) {
+            tma_prefetch_desc(&P.tm_q);
+            tma_prefetch_desc(&P.tm_k);
+            tma_prefetch_desc(&P.tm_v);
+            uint8_t *qs = sm + OFF_Q;
+            mbar_arrive_expect_tx(qfull, TILE_BYTES);
+            tma_load_3d(qs, &P.tm_q, qfull, 0, row_start, bh);
+            tma_load_3d(qs + HALF_BYTES, &P.tm_q, qfull, 64, row_start, bh);
+            int issued = 0;
+            for (int j = 0; j < nt; ++j) {
+                const int st = j % NST;
+                const uint32_t ph = (j / NST) & 1;
+                if (!mbar_wait(&kvempty[st], ph ^ 1, wc, 1)) break;
+                const Tile T = tiles[j];
+                const CUtensorMap *mk = T.src ? &P.tm_kc : &P.tm_k;
+                const CUtensorMap *mv = T.src ? &P.tm_vc : &P.tm_v;
+                uint8_t *ks = sm + OFF_K + st * TILE_BYTES;
+                uint8_t *vs = sm + OFF_V + st * TILE_BYTES;
+                mbar_arrive_expect_tx(&kfull[st], TILE_BYTES);
+                tma_load_3d(ks, mk, &kfull[st], 0, T.row0, bh);
+                tma_load_3d(ks + HALF_BYTES, mk, &kfull[st], 64, T.row0, bh);
+                mbar_arrive_expect_tx(&vfull[st], TILE_BYTES);
+                tma_load_3d(vs, mv, &vfull[st], 0, T.row0, bh);
+                tma_load_3d(vs + HALF_BYTES, mv, &vfull[st], 64, T.row0, bh);
+                issued = j + 1;
+            }
+            if (*abort_flag) {  // make sure no copy is still landing in shared memory
+                mbar_wait_drain(qfull, 0);
+                for (int j = (issued > NST ? issued - NST : 0); j < issued; ++j) {
+                    mbar_wait_drain(&kfull[j % NST], (j / NST) & 1);
+                    mbar_wait_drain(&vfull[j % NST], (j / NST) & 1);
+                }
+            }
+        }
+    } else if (warp == 5) {
+        // ------------------------------------------------------------------ MMA issuer
+        if (lane == 0 && ok) {
+            const uint32_t q_addr = smem_u32(sm + OFF_Q), p_addr = smem_u32(sm + OFF_P);
+            const uint32_t k_addr0 = smem_u32(sm + OFF_K), v_addr0 = smem_u32(sm + OFF_V);
+            bool issued_any = false, fine = true;
+            if (!mbar_wait(qfull, 0, wc, 2) || !mbar_wait(&kfull[0], 0, wc, 3)) fine = false;
+            if (fine) {
+                tc_fence_after();
+                issue_qk(tmem + kColS0, q_addr, k_addr0);
+                umma_commit(&sfull[0]);
+                issued_any = true;
+            }
+            for (int j = 0; fine && j < nt; ++j) {
+                if (j + 1 < nt) {
+                    const int st1 = (j + 1) % NST;
+                    if (!mbar_wait(&kfull[st1], ((j + 1) / NST) & 1, wc, 3)) { fine = false; break; }
+                    tc_fence_after();
+                    issue_qk(tmem + (((j + 1) & 1) ? kColS1 : kColS0), q_addr, k_addr0 + st1 * TILE_BYTES);
+                    umma_commit(&sfull[(j + 1) & 1]);
+                }
+                const int st = j % NST;
+                if (!mbar_wait(pfull, j & 1, wc, 4)) { fine = false; break; }
+                if (!mbar_wait(&vfull[st], (j / NST) & 1, wc, 5)) { fine = false; break; }
+                tc_fence_after();
+                issue_pv(tmem + kColO, p_addr, v_addr0 + st * TILE_BYTES, j > 0);
+                umma_commit(pvdone);
+                umma_commit(&kvempty[st]);
+            }
+            if (fine) umma_commit(ofull);
+            if (issued_any) {  // no MMA may still be running when TMEM is freed
+                umma_commit(drain);
+                mbar_wait_drain(drain, 0);
+            }
+        }
+    } else if (ok) {
+        // ------------------------------------------------------------------ softmax + epilogue
+        const int r = threadIdx.x;  // query row within the tile == TMEM lane
+        const int t = q0 + r;       // its absolute position
+        const uint32_t lane_base = static_cast<uint32_t>(warp * 32) << 16;
+        const uint32_t p_addr = smem_u32(sm + OFF_P);
+        const float sl2 = P.scale_log2;
+        float mrun = -INFINITY, lrun = 0.f;
+        bool fine = true;
+        for (int j = 0; j < nt; ++j) {
+            const int b = j & 1;
+            fine = __all_sync(0xFFFFFFFFu, mbar_wait(&sfull[b], (j >> 1) & 1, wc, 6));
+            if (!fine) break;
+            tc_fence_after();
+            float x[BN];
+            {
+                const uint32_t sa = tmem + lane_base + (b ? kColS1 : kColS0);
+                __syncwarp();
+                tmem_ld32(sa + 0, *reinterpret_cast<float(*)[32]>(&x[0]));
+                tmem_ld32(sa + 32, *reinterpret_cast<float(*)[32]>(&x[32]));
+                tmem_ld32(sa + 64, *reinterpret_cast<float(*)[32]>(&x[64]));
+                tmem_ld32(sa + 96, *reinterpret_cast<float(*)[32]>(&x[96]));
+            }
+            const Tile T = tiles[j];
+            // valid columns of this row: [0, b1] (sinks) and [a2, hc] (window), hc = last causal column
+            const int hc = min(T.chi, t - T.pbase);
+            const int b1 = min(hc, P.s - 1 - T.pbase);
+            const int a2 = max(0, t - P.m + 1 - T.pbase);
+            const bool full = (b1 >= BN - 1) || (hc >= BN - 1 && (a2 <= 0 || b1 >= a2 - 1));
+            float mx = -INFINITY;
+            if (full) {
+#pragma unroll
+                for (int c = 0; c < BN; ++c) {
+                    x[c] *= sl2;
+                    mx = fmaxf(mx, x[c]);
+                }
+            } else {
+#pragma unroll
+                for (int c = 0; c < BN; ++c) {
+                    const bool valid = (c <= b1) || (c >= a2 && c <= hc);
+                    x[c] = valid ? x[c] * sl2 : -INFINITY;
+                    mx = fmaxf(mx, x[c]);
+                }
+            }
+            float alpha = 1.f;
+            bool resc = false;
+            const float mnew = fmaxf(mrun, mx);
+            if (mnew > mrun + kRescaleLog2) {  // also taken when mrun is still -inf
+                if (mrun != -INFINITY) {
+                    alpha = ex2(mrun - mnew);
+                    resc = true;
+                }
+                mrun = mnew;
+            }
+            const float mu = (mrun == -INFINITY) ? 0.f : mrun;
+            uint32_t pk[BN / 2];
+            float rs = 0.f;
+#pragma unroll
+            for (int i = 0; i < BN / 2; ++i) {
+                const float p0 = ex2(x[2 * i] - mu), p1 = ex2(x[2 * i + 1] - mu);
+                rs += p0 + p1;
+                pk[i] = pack_bf16x2(p0, p1);
+            }
+            lrun = lrun * alpha + rs;
+            // the P buffer and O are free once PV_{j-1} has completed
+            if (j > 0) {
+                fine = __all_sync(0xFFFFFFFFu, mbar_wait(pvdone, (j - 1) & 1, wc, 7));
+                if (!fine) break;
+                tc_fence_after();
+            }
+            if (__any_sync(0xFFFFFFFFu, resc)) {
+                __syncwarp();
+#pragma unroll 1
+                for (int c = 0; c < HD; c += 32) {
+                    float ov[32];
+                    tmem_ld32(tmem + lane_base + kColO + c, ov);
+#pragma unroll
+                    for (int i = 0; i < 32; ++i) ov[i] *= alpha;
+                    tmem_st32(tmem + lane_base + kColO + c, ov);
+                }
+            }
+#pragma unroll
+            for (int ch = 0; ch < BN / 8; ++ch) {
+                const uint32_t addr = p_addr + (ch >> 3) * HALF_BYTES + sw128_offset(r, (ch & 7) * 8);
+                st_shared_v4(addr, pk[4 * ch], pk[4 * ch + 1], pk[4 * ch + 2], pk[4 * ch + 3]);
+            }
+            fence_proxy_async_smem();
+            tc_fence_before();
+            mbar_arrive(pfull);
+        }
+        if (fine) fine = __all_sync(0xFFFFFFFFu, mbar_wait(ofull, 0, wc, 8));
+        if (fine) {
+            tc_fence_after();
+            const float inv = (lrun > 0.f) ? 1.f / lrun : 0.f;
+            const bool store = (t <= q1);
+            __nv_bfloat16 *orow = static_cast<__nv_bfloat16 *>(P.o) +
+                                  (static_cast<int64_t>(bh) * P.seq_stride + row_start + r) * HD;
+            __syncwarp();
+#pragma unroll 1
+            for (int c = 0; c < HD; c += 32) {
+                float ov[32];
+                tmem_ld32(tmem + lane_base + kColO + c, ov);
+                if (store) {
+                    uint4 *dst = reinterpret_cast<uint4 *>(orow + c);
+#pragma unroll
+                    for (int i = 0; i < 4; ++i) {
+                        uint4 u;
+                        u.x = pack_bf16x2(ov[8 * i + 0] * inv, ov[8 * i + 1] * inv);
+                        u.y = pack_bf16x2(ov[8 * i + 2] * inv, ov[8 * i + 3] * inv);
+                        u.z = pack_bf16x2(ov[8 * i + 4] * inv, ov[8 * i + 5] * inv);
+                        u.w = pack_bf16x2(ov[8 * i + 6] * inv, ov[8 * i + 7] * inv);
+                        dst[i] = u;
+                    }
+                }
+            }
+            if (store && P.lse)
+                P.lse[static_cast<int64_t>(bh) * P.seq_stride + row_start + r] =
+                    (mrun + log2f(lrun)) * 0.69314718055994531f;
+        }
+    }
+
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 0) {
+        tc_fence_after();
+        tmem_dealloc(tmem, kTmemCols);
+    }
+}
+
+// ---------------------------------------------------------------------------------------- diagnostics
+__global__ void selftest_wait_kernel(unsigned *status, uint64_t timeout_ns) {
+    __shared__ uint64_t bar;
+    __shared__ int abort_flag;
+    if (threadIdx.x == 0) {
+        abort_flag = 0;
+        mbar_init(&bar, 1);
+        mbar_init_fence();
+    }
+    __syncthreads();
+    if (threadIdx.x == 0) {
+        // nothing ever arrives on `bar`: the wait runs out, records the timeout and returns
+        const WaitCtl wc{&abort_flag, status, timeout_ns};
+        mbar_wait(&bar, 0, wc, 99);
+    }
+}
+
+__global__ void __launch_bounds__(128, 1) selftest_umma_kernel(const __grid_constant__ CUtensorMap ma,
+                                                             const __grid_constant__ CUtensorMap mb,
+                                                             const __nv_bfloat16 *__restrict__ a_glob,
+                                                             float *__restrict__ c, int mode, unsigned *status) {
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t *sm = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    uint8_t *As = sm, *Bs = sm + TILE_BYTES;
+    uint64_t *load_bar = reinterpret_cast<uint64_t *>(sm + 2 * TILE_BYTES);
+    uint64_t *mma_bar = load_bar + 1;
+    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(load_bar + 2);
+    volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_slot + 1);
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, r = threadIdx.x;
+    if (threadIdx.x == 0) {
+        *abort_flag = 0;
+        mbar_init(load_bar, 1);
+        mbar_init(mma_bar, 1);
+        mbar_init_fence();
+    }
+    if (warp == 0) {
+        tmem_alloc(tmem_slot, 128);
+        tmem_relinquish();
+    }
+    if (mode == 2) {  // stage A by threads in the 128-byte-swizzled K-major layout
+        const uint4 *src = reinterpret_cast<const uint4 *>(a_glob + r * 128);
+        for (int ch = 0; ch < 16; ++ch) {
+            const uint4 u = src[ch];
+            st_shared_v4(smem_u32(As) + (ch >> 3) * HALF_BYTES + sw128_offset(r, (ch & 7) * 8), u.x, u.y, u.z, u.w);
+        }
+        fence_proxy_async_smem();
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = *tmem_slot;
+    const WaitCtl wc{abort_flag, status, kWaitTimeoutNs};
+    if (threadIdx.x == 0) {
+        mbar_arrive_expect_tx(load_bar, mode == 2 ? TILE_BYTES : 2 * TILE_BYTES);
+        if (mode != 2) {
+            tma_load_3d(As, &ma, load_bar, 0, 0, 0);
+            tma_load_3d(As + HALF_BYTES, &ma, load_bar, 64, 0, 0);
+        }
+        tma_load_3d(Bs, &mb, load_bar, 0, 0, 0);
+        tma_load_3d(Bs + HALF_BYTES, &mb, load_bar, 64, 0, 0);
+        if (mbar_wait(load_bar, 0, wc, 10)) {
+            tc_fence_after();
+            const uint32_t a_addr = smem_u32(As), b_addr = smem_u32(Bs);
+            for (int kk = 0; kk < 8; ++kk) {
+                const uint32_t a_off = (kk >> 2) * HALF_BYTES + (kk & 3) * 32;
+                if (mode == 0)
+                    umma_ss(tmem, sdesc_sw128(a_addr + a_off, 16, 1024), sdesc_sw128(b_addr + a_off, 16, 1024),
+                            IDESC_QK, kk > 0 ? 1u : 0u);
+                else
+                    umma_ss(tmem, sdesc_sw128(a_addr + a_off, 16, 1024),
+                            sdesc_sw128(b_addr + kk * 2048, HALF_BYTES, 1024), IDESC_PV, kk > 0 ? 1u : 0u);
+            }
+            umma_commit(mma_bar);
+            mbar_wait_drain(mma_bar, 0);
+        } else {
+            mbar_wait_drain(load_bar, 0);
+        }
+    }
+    const bool fine = __all_sync(0xFFFFFFFFu, mbar_wait(mma_bar, 0, wc, 11));
+    tc_fence_after();
+    if (fine) {
+        __syncwarp();
+        for (int cc = 0; cc < 128; cc += 32) {
+            float v[32];
+            tmem_ld32(tmem + (static_cast<uint32_t>(warp * 32) << 16) + cc, v);
+            for (int i = 0; i < 32; ++i) c[(warp * 32 + lane) * 128 + cc + i] = v[i];
+        }
+    }
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 0) {
+        tc_fence_after();
+        tmem_dealloc(tmem, 128);
+    }
+}
+
+}  // namespace tc
+
+// ---------------------------------------------------------------------------------------- host side
+static bool encode_rows_map(CUtensorMap *m, const void *base, uint64_t rows, uint64_t nbh, uint64_t bh_stride_rows) {
+    EncodeTiledFn enc = encode_tiled_fn();
+    if (!enc) return false;
+    const cuuint64_t dims[3] = {static_cast<cuuint64_t>(tc::HD), rows, nbh};
+    const cuuint64_t strides[2] = {tc::HD * 2, bh_stride_rows * tc::HD * 2};
+    const cuuint32_t box[3] = {64, 128, 1};
+    const cuuint32_t estr[3] = {1, 1, 1};
+    return enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void *>(base), dims, strides, box, estr,
+               CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+// Upper bound of the key tiles of one query tile (sink ranges, band ranges split at pos0 and at the
+// ring wrap).
+static int max_tiles_bound(int w, int s) {
+    const int m = w - s;
+    return (s + tc::BN - 1) / tc::BN + 1 + (m + 2 * tc::BN - 2) / tc::BN + 3;
+}
+
+int launch_prefill_bf16_tc(const PrefillArgs &a) {
+    using namespace tc;
+    if (a.d != HD) return fail(SWA_ERR_UNSUPPORTED, "tensor-core prefill needs d = %d", HD);
+    if (max_tiles_bound(a.w, a.s) > MAX_TILES)
+        return fail(SWA_ERR_UNSUPPORTED, "window w=%d needs more than %d key tiles per query tile", a.w, MAX_TILES);
+    if (a.BH > 65535) return fail(SWA_ERR_UNSUPPORTED, "B*H=%d > 65535", a.BH);
+    if (!encode_tiled_fn()) return fail(SWA_ERR_CUDA, "cuTensorMapEncodeTiled is not available");
+    unsigned *status = device_status_word();
+    if (!status) return SWA_ERR_CUDA;
+    Params p;
+    memset(&p, 0, sizeof(p));
+    const uint64_t L = static_cast<uint64_t>(a.L), st = static_cast<uint64_t>(a.seq_stride);
+    bool okm = encode_rows_map(&p.tm_q, a.q, L, a.BH, st) && encode_rows_map(&p.tm_k, a.k, L, a.BH, st) &&
+               encode_rows_map(&p.tm_v, a.v, L, a.BH, st);
+    if (a.pos0 > 0)
+        okm = okm && encode_rows_map(&p.tm_kc, a.k_cache, a.w, a.BH, a.w) &&
+              encode_rows_map(&p.tm_vc, a.v_cache, a.w, a.BH, a.w);
+    else
+        okm = okm && encode_rows_map(&p.tm_kc, a.k, L, a.BH, st) && encode_rows_map(&p.tm_vc, a.v, L, a.BH, st);
+    if (!okm) return fail(SWA_ERR_INVALID, "cuTensorMapEncodeTiled rejected a tensor (alignment or size)");
+    p.o = a.o;
+    p.lse = a.lse;
+    p.status = status;
+    p.seq_stride = a.seq_stride;
+    p.L = static_cast<int>(a.L);
+    p.pos0 = static_cast<int>(a.pos0);
+    p.w = a.w;
+    p.s = a.s;
+    p.m = a.w - a.s;
+    p.n_qtiles = static_cast<int>((a.L + BM - 1) / BM);
+    p.scale_log2 = a.scale * 1.4426950408889634f;
+    p.timeout_ns = kWaitTimeoutNs;
+    cudaError_t e = cudaFuncSetAttribute(swa_prefill_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         static_cast<int>(SMEM_BYTES));
+    if (e != cudaSuccess) return fail(SWA_ERR_CUDA, "prefill smem attribute: %s", cudaGetErrorString(e));
+    const dim3 grid(p.n_qtiles, a.BH), block(kThreads);
+    swa_prefill_tc_kernel<<<grid, block, SMEM_BYTES, a.stream>>>(p);
+    e = cudaGetLastError();
+    if (e != cudaSuccess) return fail(SWA_ERR_CUDA, "prefill launch: %s", cudaGetErrorString(e));
+    return SWA_OK;
+}
+
+int prefill_tile_plan(int q0, int q1, int pos0, int w, int s, int *out, int max_tiles) {
+    tc::Tile tl[tc::MAX_TILES];
+    const int n = tc::build_tiles(tl, q0, q1, pos0, s, w - s, w);
+    for (int i = 0; i < n && i < max_tiles && i < tc::MAX_TILES; ++i) {
+        out[4 * i + 0] = tl[i].src;
+        out[4 * i + 1] = tl[i].row0;
+        out[4 * i + 2] = tl[i].pbase;
+        out[4 * i + 3] = tl[i].chi;
+    }
+    return n;
+}
+
+int launch_selftest_wait_timeout(uint64_t timeout_ns, cudaStream_t stream) {
+    unsigned *status = device_status_word();
+    if (!status) return SWA_ERR_CUDA;
+    tc::selftest_wait_kernel<<<1, 32, 0, stream>>>(status, timeout_ns);
+    cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) return fail(SWA_ERR_CUDA, "selftest launch: %s", cudaGetErrorString(e));
+    return SWA_OK;
+}
+
+int launch_selftest_umma(const void *a, const void *b, float *c, int mode, cudaStream_t stream) {
+    unsigned *status = device_status_word();
+    if (!status) return SWA_ERR_CUDA;
+    if (!encode_tiled_fn()) return fail(SWA_ERR_CUDA, "cuTensorMapEncodeTiled is not available");
+    CUtensorMap ma, mb;
+    if (!encode_rows_map(&ma, a, 128, 1, 128) || !encode_rows_map(&mb, b, 128, 1, 128))
+        return fail(SWA_ERR_INVALID, "cuTensorMapEncodeTiled rejected a selftest operand");
+    const uint32_t smem = 2 * tc::TILE_BYTES + 64 + 1024;
+    cudaError_t e = cudaFuncSetAttribute(tc::selftest_umma_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         static_cast<int>(smem));
+    if (e != cudaSuccess) return fail(SWA_ERR_CUDA, "selftest smem attribute: %s", cudaGetErrorString(e));
+    tc::selftest_umma_kernel<<<1, 128, smem, stream>>>(ma, mb, static_cast<const __nv_bfloat16 *>(a), c, mode,
+                                                       status);
+    e = cudaGetLastError();
+    if (e != cudaSuccess) return fail(SWA_ERR_CUDA, "selftest launch: %s", cudaGetErrorString(e));
+    return SWA_OK;
+}
+
+}  // namespace swa

@@ -1,0 +1,65 @@
+// swa_internal.h -- host-side declarations shared by the library's translation units.
+#pragma once
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <stddef.h>
+#include <stdint.h>
+
+namespace swa {
+
+// Record the calling thread's error message (printf-style); returns `code` for convenience.
+int fail(int code, const char *fmt, ...);
+
+// Device error word of the current device (nullptr if it could not be resolved; the error is set).
+unsigned *device_status_word();
+
+// cuTensorMapEncodeTiled, resolved once through the runtime's driver entry point (no -lcuda).
+typedef CUresult (*EncodeTiledFn)(CUtensorMap *, CUtensorMapDataType, cuuint32_t, void *, const cuuint64_t *,
+                                  const cuuint64_t *, const cuuint32_t *, const cuuint32_t *, CUtensorMapInterleave,
+                                  CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+EncodeTiledFn encode_tiled_fn();
+
+// A prefill over L rows whose (b, h) blocks lie seq_stride rows apart in q/k/v/o (and lse).
+struct PrefillArgs {
+    const void *q, *k, *v;
+    void *o;
+    float *lse;
+    const void *k_cache, *v_cache;  // [BH, w, d]; used when pos0 > 0
+    int64_t pos0;
+    int BH;
+    int64_t L;
+    int d, w, s;
+    float scale;
+    int64_t seq_stride;  // rows between consecutive (b, h) blocks (== L for contiguous tensors)
+    cudaStream_t stream;
+};
+
+int launch_prefill_f32(const PrefillArgs &a);
+int launch_prefill_bf16_tc(const PrefillArgs &a);
+
+// Rolling-cache write of positions pos0..pos0+n-1; source rows of (b, h) start at bh*src_stride.
+int launch_kv_write(void *k_cache, void *v_cache, const void *k_new, const void *v_new, int BH, int d, int w,
+                    int s, int64_t pos0, int64_t n, int64_t src_stride, int esize, cudaStream_t stream);
+
+struct DecodeArgs {
+    const void *q, *k_cache, *v_cache;
+    void *o;
+    float *lse;
+    int BH, d, w, s;
+    int64_t t;
+    float scale;
+    void *workspace;
+    size_t workspace_bytes;
+    int esize;  // 2 = bf16, 4 = fp32
+    cudaStream_t stream;
+};
+int decode_num_splits(int BH, int nvalid);
+size_t decode_workspace_bytes(int BH, int d, int w);
+int launch_decode(const DecodeArgs &a);
+
+int prefill_tile_plan(int q0, int q1, int pos0, int w, int s, int *out, int max_tiles);
+int launch_selftest_wait_timeout(uint64_t timeout_ns, cudaStream_t stream);
+int launch_selftest_umma(const void *a, const void *b, float *c, int mode, cudaStream_t stream);
+
+}  // namespace swa

@@ -1,0 +1,110 @@
+"""The C-ABI library: builds, loads without a GPU, exports every symbol include/swa_sink.h declares, and
+rejects bad arguments before touching the GPU (CPU only)."""
+import ctypes
+import os
+import re
+
+import pytest
+
+import sliding_window_softmax_swa_gb300 as swa
+from sliding_window_softmax_swa_gb300 import build as swa_build
+
+HEADER = os.path.join(os.path.dirname(os.path.dirname(os.path.abspath(__file__))), "include", "swa_sink.h")
+
+
+def declared_functions():
+    src = open(HEADER).read()
+    src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+    names = re.findall(r"^\s*(?:const\s+)?[A-Za-z_][A-Za-z0-9_]*\s*\**\s*([A-Za-z_][A-Za-z0-9_]*)\s*\(",
+                       src, flags=re.M)
+    return sorted(set(names))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    swa_build.build()
+    return swa.lib()
+
+
+def test_header_declares_the_three_path_calls():
+    names = declared_functions()
+    for n in ("swa_sink_prefill", "swa_sink_decode_step", "kv_rolling_write"):
+        assert n in names
+
+
+def test_every_declared_symbol_is_exported(lib):
+    for n in declared_functions():
+        assert hasattr(lib, n), n
+    assert set(declared_functions()) == set(swa.SIGNATURES), "binding signatures out of sync with the header"
+
+
+def test_library_has_no_dynamic_cuda_dependency():
+    # the runtime is linked statically, so the library loads on a host without a GPU driver
+    ctypes.CDLL(swa_build.LIB)
+    needed = os.popen(f"readelf -d {swa_build.LIB}").read()
+    assert "libcudart" not in needed and "libcuda.so" not in needed
+
+
+@pytest.mark.parametrize("args,msg", [
+    (dict(w=4, s=4), "s < w"),
+    (dict(w=0, s=0), "w="),
+    (dict(d=96), "d=96"),
+    (dict(B=0), "B=0"),
+    (dict(dtype=7), "dtype"),
+    (dict(L=-1), "L=-1"),
+    (dict(scale=0.0), "scale"),
+    (dict(pos0=-3), "pos0"),
+])
+def test_prefill_rejects_bad_arguments(lib, args, msg):
+    a = dict(B=1, H=1, L=16, d=128, w=8, s=4, scale=0.1, dtype=0, pos0=0)
+    a.update(args)
+    fake = 1 << 20  # never dereferenced: validation fails first
+    rc = lib.swa_sink_prefill(fake, fake, fake, fake, None, None, None, a["pos0"], a["B"], a["H"], a["L"], a["d"],
+                              a["w"], a["s"], a["scale"], a["dtype"], None)
+    assert rc in (swa.SWA_ERR_INVALID, swa.SWA_ERR_UNSUPPORTED)
+    assert msg in swa.last_error()
+
+
+def test_prefill_null_and_misaligned(lib):
+    rc = lib.swa_sink_prefill(None, None, None, None, None, None, None, 0, 1, 1, 16, 128, 8, 4, 0.1, 0, None)
+    assert rc == swa.SWA_ERR_INVALID and "non-null" in swa.last_error()
+    rc = lib.swa_sink_prefill(1 << 20 | 8, 1 << 20, 1 << 20, 1 << 20, None, None, None, 0, 1, 1, 16, 128, 8, 4, 0.1,
+                              0, None)
+    assert rc == swa.SWA_ERR_INVALID and "aligned" in swa.last_error()
+    # chunked prefill with pos0 > 0 needs the cache
+    rc = lib.swa_sink_prefill(1 << 20, 1 << 20, 1 << 20, 1 << 20, None, None, None, 5, 1, 1, 16, 128, 8, 4, 0.1, 0,
+                              None)
+    assert rc == swa.SWA_ERR_INVALID and "cache" in swa.last_error()
+    # L == 0 is a no-op that succeeds without touching anything
+    assert lib.swa_sink_prefill(None, None, None, None, None, None, None, 0, 1, 1, 0, 128, 8, 4, 0.1, 0, None) == 0
+
+
+def test_bf16_prefill_needs_d128(lib):
+    f = 1 << 20
+    rc = lib.swa_sink_prefill(f, f, f, f, None, None, None, 0, 1, 1, 16, 64, 8, 4, 0.1, 0, None)
+    assert rc == swa.SWA_ERR_UNSUPPORTED
+
+
+def test_decode_and_write_reject_bad_arguments(lib):
+    f = 1 << 20
+    assert lib.swa_sink_decode_step(f, f, f, f, None, 1, 1, 128, 8, 8, 0, 0.1, None, 0, 0, None) == swa.SWA_ERR_INVALID
+    assert lib.swa_sink_decode_step(f, f, f, f, None, 1, 1, 128, 8, 4, -1, 0.1, None, 0, 0, None) == swa.SWA_ERR_INVALID
+    assert lib.kv_rolling_write(f, f, f, f, 1, 1, 128, 8, 4, -1, 1, 0, None) == swa.SWA_ERR_INVALID
+    assert lib.kv_rolling_write(None, None, None, None, 1, 1, 128, 8, 4, 0, 0, 0, None) == swa.SWA_OK  # n = 0
+    # a workspace smaller than required is refused
+    need = lib.swa_sink_decode_workspace_size(1, 2, 128, 4096)
+    assert need > 0
+    rc = lib.swa_sink_decode_step(f, f, f, f, None, 1, 2, 128, 4096, 4, 5000, 0.1, f, need - 1, 0, None)
+    assert rc == swa.SWA_ERR_INVALID and "workspace" in swa.last_error()
+
+
+def test_workspace_size_shapes(lib):
+    # a full GPU of (b, h) rows needs no split; few rows with a long window split the cache
+    assert lib.swa_sink_decode_workspace_size(64, 40, 128, 1024) == 0
+    assert lib.swa_sink_decode_workspace_size(1, 32, 128, 4096) == 32 * 16 * 130 * 4
+    assert lib.swa_sink_decode_workspace_size(0, 32, 128, 4096) == 0
+
+
+def test_selftests_validate(lib):
+    assert lib.swa_selftest_wait_timeout(0, None) == swa.SWA_ERR_INVALID
+    assert lib.swa_selftest_umma(None, None, None, 0, None) == swa.SWA_ERR_INVALID

@@ -104,6 +104,7 @@ def test_mask_matches_set_construction(L):
             mk = oracle.mask(L, w, s)
             for t in range(L):
                 assert set(np.nonzero(mk[t])[0].tolist()) == keyset(t, w, s), (L, w, s, t)
+                assert np.array_equal(oracle.is_key_many(t, np.arange(L), w, s), mk[t].astype(bool))
 
 
 def test_zero_query_gives_mean_over_keyset():

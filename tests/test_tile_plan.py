@@ -1,0 +1,87 @@
+"""The key-tile walk of the bf16 prefill kernel (host-callable, same function as on the device) covers
+every key of every query row exactly once, with the right position in every column (CPU only).
+
+For each tile the library reports (source, first row, position of column 0, last valid column).
+Column c <= last holds source row (first row + c).  For the rolling cache the position stored in a slot
+comes from the oracle's sequential replay of the writes; for the call's own rows it is pos0 + row.
+Membership of a position in the key set of row t is the oracle's brute-force predicate.
+"""
+import random
+
+import numpy as np
+import pytest
+
+import oracle
+import sliding_window_softmax_swa_gb300 as swa
+
+BN = 128
+
+
+def check_plan(q0, q1, pos0, w, s, L):
+    plan = swa.prefill_tile_plan(q0, q1, pos0, w, s)
+    holder = oracle.cache_replay(w, s, pos0) if pos0 > 0 else None
+    seen = {}  # position -> count, over columns the kernel keeps for at least one row
+    cols = []
+    for src, row0, pbase, chi in plan:
+        assert 0 <= chi < BN
+        assert row0 >= 0
+        for c in range(chi + 1):
+            p = pbase + c
+            row = row0 + c
+            if src == 1:
+                assert row < w, "cache column past the cache"
+                assert holder[row] == p, f"slot {row} holds {holder[row]}, tile says {p}"
+                assert p < pos0
+            else:
+                assert p >= pos0 and row == p - pos0
+                assert row < L or p > q1
+            cols.append(p)
+    cols = np.array(cols, dtype=np.int64)
+    allpos = np.arange(q1 + 1, dtype=np.int64)
+    for t in range(q0, q1 + 1):
+        got = np.sort(cols[oracle.is_key_many(t, cols, w, s)])
+        want = allpos[oracle.is_key_many(t, allpos, w, s)]
+        assert np.array_equal(got, want), (q0, q1, pos0, w, s, t)
+    return plan
+
+
+@pytest.mark.parametrize("w,s", [(1024, 4), (4096, 4), (4096, 0), (300, 4), (64, 16), (1, 0), (2, 1), (129, 4),
+                                 (300, 200), (256, 130), (17, 16)])
+def test_whole_sequence_tiles(w, s):
+    L = 3000
+    for qt in range(0, (L + BN - 1) // BN):
+        q0 = qt * BN
+        q1 = min(q0 + BN, L) - 1
+        check_plan(q0, q1, 0, w, s, L)
+
+
+def test_chunked_tiles_random():
+    rng = random.Random(1234)
+    for _ in range(300):
+        w = rng.choice([8, 40, 100, 128, 129, 300, 513, 1024])
+        s = rng.choice([0, 1, 4, min(w - 1, 16), w - 1])
+        pos0 = rng.choice([1, 2, s, s + 1, w - 1, w, w + 1, 3 * w + 7, rng.randrange(1, 5 * w + 10)])
+        pos0 = max(1, pos0)
+        L = rng.randrange(1, 700)
+        qt = rng.randrange(0, (L + BN - 1) // BN)
+        q0 = pos0 + qt * BN
+        q1 = pos0 + min(qt * BN + BN, L) - 1
+        check_plan(q0, q1, pos0, w, s, L)
+
+
+def test_chunked_tiles_long_window_boundaries():
+    # the chunk shapes of a 131072-token prompt in 4096-token chunks with w = 4096, s = 4
+    w, s, C = 4096, 4, 4096
+    for pos0 in (C, 2 * C, 7 * C, 31 * C):
+        for qt in (0, 1, 15, 16, 31):
+            q0 = pos0 + qt * BN
+            plan = check_plan(q0, q0 + BN - 1, pos0, w, s, C)
+            assert len(plan) <= 36
+
+
+def test_tile_count_is_minimal_for_full_windows():
+    # a full-window query tile walks ceil((m + 127) / 128) band tiles plus one sink tile
+    for w, s in [(1024, 4), (4096, 4), (4096, 0)]:
+        m = w - s
+        plan = swa.prefill_tile_plan(8192, 8192 + 127, 0, w, s)
+        assert len(plan) == (m + 127 + BN - 1) // BN + (1 if s else 0)
