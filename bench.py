@@ -1,0 +1,496 @@
+"""Benchmark of the sliding-window-attention-with-sinks library on GB300.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference] [--primary-only]
+
+Prints ONE JSON line. The primary metric is prefill banded TFLOP/s on the Llama-2-7B head shape
+(B=1, H=32, L=8192, d=128, w=1024, s=4, bf16): banded FLOPs = 4 * B * H * d * sum_t min(t+1, w).
+A step is one swa_sink_prefill call over that batch; inputs (256 MiB per step) are larger than L2.
+Secondary entries: prefill at the Mistral-7B window shape (s=0 and s=4), streaming decode
+(tokens/s, B=64, H=40, 4 sink + 1020 recent slots, 20480 steps) and chunked prefill
+(L=131072 in 4096-token chunks). Under torchrun each rank runs the same per-GPU workload on its own
+GPU (weak scaling; no collective on the data path) and the aggregate divides all ranks' work by the
+slowest rank's time.
+
+--impl reference times the oracle (fp64 C on the host cores) on a bounded sample of the same workload.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+PRIMARY = "prefill_llama7b_L8192_w1024_s4"
+METRIC = "prefill banded TFLOP/s"
+PEAKS_FALLBACK = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+
+
+# ------------------------------------------------------------------------------------------ accounting
+def banded_pairs(L: int, w: int, pos0: int = 0) -> int:
+    """sum over positions t in [pos0, pos0 + L) of min(t + 1, w): (query, key) pairs of the band."""
+    lo, hi = pos0, pos0 + L
+    ramp = min(hi, w)
+    total = (ramp * (ramp + 1) - lo * (lo + 1)) // 2 if ramp > lo else 0
+    return total + max(0, hi - max(lo, w)) * w
+
+
+def banded_flops(B, H, L, d, w) -> int:
+    return 4 * B * H * d * banded_pairs(L, w)
+
+
+def load_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            d = json.load(f)
+        return d, "measured"
+    return PEAKS_FALLBACK, "fallback"
+
+
+def kernel_source_hash(files) -> str:
+    h = hashlib.sha256()
+    for f in files:
+        with open(os.path.join(ROOT, f), "rb") as fh:
+            h.update(fh.read())
+    return h.hexdigest()[:16]
+
+
+def traffic_for(kernel: str, files, workload: str):
+    """DRAM bytes per launch from the committed ncu summary, or None if absent or taken on other code."""
+    p = os.path.join(ROOT, "profiles", "traffic.json")
+    if not os.path.exists(p):
+        return None
+    with open(p) as f:
+        d = json.load(f).get(kernel)
+    if not d or d.get("source_hash") != kernel_source_hash(files) or d.get("workload") != workload:
+        return None
+    return d.get("bytes_per_launch")
+
+
+# ------------------------------------------------------------------------------------------ distributed
+def dist_env():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return world, rank, local
+
+
+def reduce_max(x: float, world: int) -> float:
+    """Max of a float over ranks (identity on one rank)."""
+    if world == 1:
+        return x
+    import torch
+    import torch.distributed as dist
+    dev = "cuda" if dist.get_backend() == "nccl" else "cpu"
+    t = torch.tensor([x], dtype=torch.float64, device=dev)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def barrier(world: int):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def aggregate_rate(units_per_rank: float, world: int, t_max: float) -> float:
+    """Whole-job throughput: the units all ranks processed over the slowest rank's time."""
+    return units_per_rank * world / t_max
+
+
+# ------------------------------------------------------------------------------------------ clocks
+class ClockSampler:
+    """nvidia-smi sampled every 200 ms in the background; windows mark the timed regions."""
+    FIELDS = ("timestamp,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_id: str | None):
+        self.windows = []
+        self.proc = None
+        self.out = tempfile.NamedTemporaryFile(prefix="clocks", suffix=".csv", delete=False)
+        cmd = ["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits", "-lms", "200"]
+        if gpu_id:
+            cmd += ["-i", gpu_id]
+        try:
+            self.proc = subprocess.Popen(cmd, stdout=self.out, stderr=subprocess.DEVNULL)
+        except OSError:
+            self.proc = None
+
+    def mark(self, t0: float, t1: float):
+        self.windows.append((t0, t1))
+
+    def stop(self):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+        self.out.close()
+        rows = []
+        with open(self.out.name) as f:
+            for line in f:
+                parts = [x.strip() for x in line.split(",")]
+                if len(parts) != 9:
+                    continue
+                try:
+                    ts = time.mktime(time.strptime(parts[0].split(".")[0], "%Y/%m/%d %H:%M:%S"))
+                    ts += float("0." + parts[0].split(".")[1]) if "." in parts[0] else 0.0
+                    rows.append((ts, float(parts[1]), float(parts[2]), parts[3], parts[5:9]))
+                except (ValueError, IndexError):
+                    continue
+        os.unlink(self.out.name)
+        inside = [r for r in rows if any(a - 0.25 <= r[0] <= b + 0.25 for a, b in self.windows)]
+        use = inside or rows
+        if not use:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no nvidia-smi samples"], "samples": 0}
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for r in use for i, v in enumerate(r[4]) if v.lower().startswith("active")})
+        return {"sm_mhz": statistics.median(r[1] for r in use), "sm_max_mhz": max(r[2] for r in use),
+                "reasons": reasons, "samples": len(use), "in_timed_region": bool(inside)}
+
+
+# ------------------------------------------------------------------------------------------ GPU legs
+def _events():
+    import torch
+    return torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+
+
+def _check_status(swa):
+    rc = swa.swa_device_status()
+    if rc != 0:
+        raise RuntimeError(f"device status {rc}: {swa.last_error()}")
+
+
+def time_loop(step, steps, warmup, world, clocks):
+    """W untimed calls, then K calls bracketed by barrier + synchronize; returns max-over-ranks seconds."""
+    import torch
+    for _ in range(warmup):
+        step()
+    torch.cuda.synchronize()
+    barrier(world)
+    e0, e1 = _events()
+    t0 = time.time()
+    e0.record()
+    for _ in range(steps):
+        step()
+    e1.record()
+    torch.cuda.synchronize()
+    t1 = time.time()
+    barrier(world)
+    if clocks is not None:
+        clocks.mark(t0, t1)
+    return reduce_max(e0.elapsed_time(e1) / 1e3, world)
+
+
+def prefill_leg(swa, wl, steps, warmup, world, rank, clocks, e2e=False):
+    import torch
+    import swa_inputs
+    B, H, L, d, w, s = wl.B, wl.H, wl.L, wl.d, wl.w, wl.s
+    q, k, v = swa_inputs.prefill_inputs(B, H, L, d, wl.seed + 7919 * rank, wl.torch_dtype, "cuda", wl.sink_boost)
+    o = torch.empty_like(q)
+    lib = swa.lib()
+    stream = torch.cuda.current_stream().cuda_stream
+    args = (q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(), None, None, None, 0, B, H, L, d, w, s,
+            wl.scale, 0 if wl.dtype == "bf16" else 1, stream)
+
+    def step():
+        rc = lib.swa_sink_prefill(*args)
+        if rc:
+            raise RuntimeError(swa.last_error())
+
+    t = time_loop(step, steps, warmup, world, clocks)
+    _check_status(swa)
+    flops = banded_flops(B, H, L, d, w)
+    res = {"flops_per_step": flops, "seconds": t, "steps": steps, "tflops": flops * steps / t / 1e12,
+           "ms_per_step": t / steps * 1e3, "launches": steps}
+    if e2e:
+        # same step through the public call with host buffers: H2D of q/k/v, prefill, D2H of o, every step
+        qh, kh, vh = (x.cpu().pin_memory() for x in (q, k, v))
+        oh = torch.empty(o.shape, dtype=o.dtype, pin_memory=True)
+
+        def step_e2e():
+            q.copy_(qh, non_blocking=True)
+            k.copy_(kh, non_blocking=True)
+            v.copy_(vh, non_blocking=True)
+            step()
+            oh.copy_(o, non_blocking=True)
+
+        te = time_loop(step_e2e, steps, min(warmup, 3), world, None)
+        _check_status(swa)
+        res["e2e"] = {"seconds": te, "tflops": flops * steps / te / 1e12,
+                      "h2d_bytes_per_step": 3 * q.numel() * q.element_size(),
+                      "d2h_bytes_per_step": o.numel() * o.element_size()}
+    del q, k, v, o
+    torch.cuda.empty_cache()
+    return res
+
+
+def chunked_leg(swa, wl, steps, warmup, world, rank, clocks):
+    import torch
+    import swa_inputs
+    B, H, L, d, w, s, C = wl.B, wl.H, wl.L, wl.d, wl.w, wl.s, wl.chunk
+    q, k, v = swa_inputs.prefill_inputs(B, H, L, d, wl.seed + 7919 * rank, wl.torch_dtype, "cuda", wl.sink_boost)
+    o = torch.empty_like(q)
+    kc = torch.empty((B, H, w, d), dtype=q.dtype, device="cuda")
+    vc = torch.empty_like(kc)
+    lib = swa.lib()
+    stream = torch.cuda.current_stream().cuda_stream
+    args = (q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(), None, kc.data_ptr(), vc.data_ptr(), B, H, L, d,
+            w, s, wl.scale, C, 0, stream)
+
+    def step():
+        rc = lib.swa_sink_prefill_chunked(*args)
+        if rc:
+            raise RuntimeError(swa.last_error())
+
+    t = time_loop(step, steps, warmup, world, clocks)
+    _check_status(swa)
+    flops = banded_flops(B, H, L, d, w)
+    nch = (L + C - 1) // C
+    del q, k, v, o, kc, vc
+    torch.cuda.empty_cache()
+    return {"flops_per_step": flops, "seconds": t, "steps": steps, "tflops": flops * steps / t / 1e12,
+            "ms_per_step": t / steps * 1e3, "launches": steps * 2 * nch}
+
+
+def decode_leg(swa, wl, world, rank, clocks, steps=None):
+    """The whole streaming run: per step one rolling write of the new key/value and one decode."""
+    import torch
+    import swa_inputs
+    B, H, d, w, s = wl.B, wl.H, wl.d, wl.w, wl.s
+    T = wl.L if steps is None else steps
+    seed = wl.seed + 7919 * rank
+    qs = swa_inputs.normal((T, B, H, d), seed, swa_inputs.TID_Q, wl.torch_dtype, "cuda")
+    ks = swa_inputs.normal((T, B, H, d), seed, swa_inputs.TID_K, wl.torch_dtype, "cuda")
+    vs = swa_inputs.normal((T, B, H, d), seed, swa_inputs.TID_V, wl.torch_dtype, "cuda")
+    if wl.sink_boost:
+        ks[:4] *= 4.0
+    kc = torch.zeros((B, H, w, d), dtype=qs.dtype, device="cuda")
+    vc = torch.zeros_like(kc)
+    o = torch.empty((B, H, d), dtype=qs.dtype, device="cuda")
+    nws = swa.swa_sink_decode_workspace_size(B, H, d, w)
+    ws = torch.empty(max(nws, 256), dtype=torch.uint8, device="cuda")
+    lib = swa.lib()
+    stream = torch.cuda.current_stream().cuda_stream
+    row = B * H * d * qs.element_size()
+    qp, kp, vp = qs.data_ptr(), ks.data_ptr(), vs.data_ptr()
+    dt = 0 if wl.dtype == "bf16" else 1
+
+    def run(t0, t1):
+        for t in range(t0, t1):
+            rc = lib.kv_rolling_write(kc.data_ptr(), vc.data_ptr(), kp + t * row, vp + t * row, B, H, d, w, s, t, 1,
+                                      dt, stream)
+            rc |= lib.swa_sink_decode_step(qp + t * row, kc.data_ptr(), vc.data_ptr(), o.data_ptr(), None, B, H, d,
+                                           w, s, t, wl.scale, ws.data_ptr(), nws, dt, stream)
+            if rc:
+                raise RuntimeError(swa.last_error())
+
+    run(0, min(T, 64))  # warm-up on the first positions, then start the stream again from an empty cache
+    kc.zero_()
+    vc.zero_()
+    t = time_loop(lambda: run(0, T), 1, 0, world, clocks)
+    _check_status(swa)
+    kv_bytes = 2 * d * qs.element_size() * B * H * sum(min(x + 1, w) for x in range(T))
+    res = {"steps": T, "seconds": t, "tok_per_s": B * T / t, "kv_bytes_read": kv_bytes,
+           "launches": 2 * T}
+    # the decode kernel alone at a full cache, for its roofline
+    R = 200
+    tl = T - 1
+
+    def dstep():
+        rc = lib.swa_sink_decode_step(qp + tl * row, kc.data_ptr(), vc.data_ptr(), o.data_ptr(), None, B, H, d, w, s,
+                                      tl, wl.scale, ws.data_ptr(), nws, dt, stream)
+        if rc:
+            raise RuntimeError(swa.last_error())
+
+    tk = time_loop(dstep, R, 5, world, clocks)
+    _check_status(swa)
+    nvalid = min(tl + 1, w)
+    step_bytes = B * H * (2 * nvalid * d + 2 * d) * qs.element_size()
+    res["kernel"] = {"name": "decode_kernel", "avg_us": tk / R * 1e6, "bytes_per_launch": step_bytes,
+                     "gbs": step_bytes / (tk / R) / 1e9}
+    del qs, ks, vs, kc, vc
+    torch.cuda.empty_cache()
+    return res
+
+
+# ------------------------------------------------------------------------------------------ oracle legs
+def oracle_sample_inputs(wl, heads: int):
+    """Host copies of the first `heads` heads of the workload's inputs (drawn on the CPU)."""
+    import swa_inputs
+    q, k, v = swa_inputs.prefill_inputs(1, heads, wl.L, wl.d, wl.seed, wl.torch_dtype, "cpu", wl.sink_boost)
+    return q, k, v
+
+
+def oracle_run(wl, q, k, v, rows: int):
+    """The oracle over rows [0, rows) of the given heads; returns (seconds, banded flops computed)."""
+    import numpy as np
+    import oracle
+    H, d = q.shape[1], q.shape[3]
+    pos = np.arange(rows, dtype=np.int64)
+    qq, kk, vv = (oracle._f64(x[0, :, :rows]) for x in (q, k, v))
+    t0 = time.perf_counter()
+    oracle.attend(qq, pos, kk, vv, pos, wl.w, wl.s, wl.scale)
+    t = time.perf_counter() - t0
+    return t, 4 * H * d * banded_pairs(rows, wl.w)
+
+
+def cpu_baseline_leg(wl):
+    import oracle
+    heads = 8
+    q, k, v = oracle_sample_inputs(wl, heads)
+    t, flops = oracle_run(wl, q, k, v, wl.L)
+    return {"value": flops / t / 1e12, "unit": "TFLOP/s", "cores": oracle.default_threads(), "kind": "oracle",
+            "sample": f"{heads} of {wl.H} heads, all {wl.L} rows of {wl.name} (fp64 C, {t:.1f} s)",
+            "seconds": t}
+
+
+def reference_main(args, world, rank):
+    """The reference arm: the oracle, as it stands, on the host cores, a bounded sample per step."""
+    import oracle
+    import swa_inputs
+    if rank != 0:
+        return 0
+    wl = swa_inputs.WORKLOADS[PRIMARY]
+    q, k, v = oracle_sample_inputs(wl, 1)
+    rows = 2048  # one head, the first 2048 rows: a bounded sample of the workload per step
+    for _ in range(args.warmup):
+        oracle_run(wl, q, k, v, rows)
+    tot_t, tot_f = 0.0, 0
+    for _ in range(args.steps):
+        t, f = oracle_run(wl, q, k, v, rows)
+        tot_t += t
+        tot_f += f
+    value = tot_f / tot_t / 1e12
+    sample = f"per step: head 0, rows 0..{rows - 1} of {wl.name} (fp64 C oracle)"
+    line = {"impl": "reference", "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": args.gpus,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": tot_t / args.steps * 1e3,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": workload_config(wl),
+            "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": oracle.default_threads(), "kind": "oracle",
+                             "sample": sample},
+            "e2e": {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line))
+    return 0
+
+
+def workload_config(wl):
+    c = {"workload": wl.name, "B": wl.B, "H": wl.H, "L": wl.L, "d": wl.d, "w": wl.w, "s": wl.s, "dtype": wl.dtype,
+         "parallelism": "replicas (weak)", "l2": "inputs larger than L2 (129 MB) every step"}
+    if wl.chunk:
+        c["chunk"] = wl.chunk
+    return c
+
+
+# ------------------------------------------------------------------------------------------ main
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=200)
+    ap.add_argument("--warmup", type=int, default=10)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--primary-only", action="store_true", help="only the primary prefill leg")
+    ap.add_argument("--legs", default="primary,mistral,chunked,decode",
+                    help="comma list of legs to run (profiling runs pick one)")
+    ap.add_argument("--decode-steps", type=int, default=None, help="shorter decode stream (profiling only)")
+    args = ap.parse_args()
+    legs = set(args.legs.split(","))
+    if args.primary_only:
+        legs = {"primary"}
+    world, rank, local = dist_env()
+    if args.impl == "reference":
+        return reference_main(args, world, rank)
+    args.warmup = max(args.warmup, 3)
+
+    import torch
+    import sliding_window_softmax_swa_gb300 as swa
+    import swa_inputs
+
+    if world > 1:
+        import torch.distributed as dist
+        torch.cuda.set_device(local)
+        dist.init_process_group("nccl")
+    else:
+        torch.cuda.set_device(0)
+    swa.lib(build_if_missing=True)
+    peaks, peak_src = load_peaks()
+    uuid = None
+    try:
+        uuid = "GPU-" + str(torch.cuda.get_device_properties(torch.cuda.current_device()).uuid)
+    except Exception:
+        uuid = None
+    clocks = ClockSampler(uuid)
+
+    wl = swa_inputs.WORKLOADS[PRIMARY]
+    prim = prefill_leg(swa, wl, args.steps, args.warmup, world, rank, clocks, e2e=True) if "primary" in legs else None
+    secondary = {}
+    if "mistral" in legs:
+        for name in ("prefill_mistral_B2_L32768_w4096_s0", "prefill_mistral_B2_L32768_w4096_s4"):
+            r = prefill_leg(swa, swa_inputs.WORKLOADS[name], max(3, args.steps // 20), 3, world, rank, clocks)
+            secondary[name] = {"metric": METRIC, "value": aggregate_rate(r["tflops"], world, 1.0), "unit": "TFLOP/s",
+                               "ms_per_step": r["ms_per_step"],
+                               "frac_of_bf16_peak": r["tflops"] / peaks["bf16_tflops"]}
+    if "chunked" in legs:
+        cw = swa_inputs.WORKLOADS["chunked_mistral_L131072_w4096_s4_C4096"]
+        r = chunked_leg(swa, cw, 3, 1, world, rank, clocks)
+        secondary[cw.name] = {"metric": METRIC, "value": aggregate_rate(r["tflops"], world, 1.0), "unit": "TFLOP/s",
+                              "ms_per_step": r["ms_per_step"], "frac_of_bf16_peak": r["tflops"] / peaks["bf16_tflops"],
+                              "launches_per_step": r["launches"] // 3}
+    if "decode" in legs:
+        dw = swa_inputs.WORKLOADS["decode_llama13b_B64_w1024_s4_20480"]
+        r = decode_leg(swa, dw, world, rank, clocks, steps=args.decode_steps)
+        secondary[dw.name] = {"metric": "decode tok/s", "value": aggregate_rate(r["tok_per_s"], world, 1.0),
+                              "unit": "tok/s", "seconds": r["seconds"],
+                              "kv_read_gbs": r["kv_bytes_read"] / r["seconds"] / 1e9,
+                              "roofline": {"bound": "hbm", "kernel": "decode_kernel", "achieved": r["kernel"]["gbs"],
+                                           "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                                           "frac": r["kernel"]["gbs"] / peaks["hbm_gbs"],
+                                           "frac_of_8tbs_nominal": r["kernel"]["gbs"] / 8000.0,
+                                           "avg_us": r["kernel"]["avg_us"]}}
+    ck = clocks.stop()
+
+    if rank != 0:
+        return 0
+    if prim is None:  # a profiling run of secondary legs only
+        print(json.dumps({"metric": METRIC, "value": None, "secondary": secondary}))
+        return 0
+    t = prim["seconds"]
+    value = aggregate_rate(prim["flops_per_step"] * prim["steps"] / 1e12, world, t)
+    achieved = prim["flops_per_step"] / (t / prim["steps"]) / 1e12
+    kfiles = ["sliding_window_softmax_swa_gb300/csrc/prefill_tc.cu", "sliding_window_softmax_swa_gb300/csrc/swa_device.cuh"]
+    line = {
+        "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": t / args.steps * 1e3, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "bf16", "data": "synthetic (seeded iid N(0,1))",
+        "config": workload_config(wl),
+        "roofline": {"bound": "tensor", "kernel": "swa_prefill_tc_kernel", "achieved": achieved,
+                     "peak": peaks["bf16_tflops"], "peak_source": f"{peak_src} bf16 burst", "unit": "TFLOP/s",
+                     "frac": achieved / peaks["bf16_tflops"],
+                     "traffic": traffic_for("swa_prefill_tc_kernel", kfiles, wl.name)},
+        "e2e": {"value": aggregate_rate(prim["flops_per_step"] * prim["steps"] / 1e12, world, prim["e2e"]["seconds"]),
+                "unit": "TFLOP/s", "h2d_bytes_per_step": prim["e2e"]["h2d_bytes_per_step"],
+                "d2h_bytes_per_step": prim["e2e"]["d2h_bytes_per_step"]},
+        "gpu_launches": prim["launches"],
+        "clocks": {"sm_mhz": ck["sm_mhz"], "sm_max_mhz": ck["sm_max_mhz"], "reasons": ck["reasons"],
+                   "samples": ck["samples"]},
+        "secondary": secondary,
+    }
+    if world == 1:
+        line["cpu_baseline"] = cpu_baseline_leg(wl)
+    print(json.dumps(line))
+    return 0
+
+
+if __name__ == "__main__":
+    sys.exit(main())

@@ -552,9 +552,14 @@ int launch_prefill_bf16_tc(const PrefillArgs &a) {
     const uint64_t L = static_cast<uint64_t>(a.L), st = static_cast<uint64_t>(a.seq_stride);
     bool okm = encode_rows_map(&p.tm_q, a.q, L, a.BH, st) && encode_rows_map(&p.tm_k, a.k, L, a.BH, st) &&
                encode_rows_map(&p.tm_v, a.v, L, a.BH, st);
-    if (a.pos0 > 0)
-        okm = okm && encode_rows_map(&p.tm_kc, a.k_cache, a.w, a.BH, a.w) &&
-              encode_rows_map(&p.tm_vc, a.v_cache, a.w, a.BH, a.w);
+    if (a.pos0 > 0) {
+        // Only slots 0..min(pos0, w)-1 have been written; the map stops there so that TMA zero-fills the
+        // rest of a tile instead of loading stale bytes (a masked column still multiplies its V row by 0,
+        // and 0 * NaN would poison the accumulator).
+        const uint64_t written = static_cast<uint64_t>(a.pos0 < a.w ? a.pos0 : a.w);
+        okm = okm && encode_rows_map(&p.tm_kc, a.k_cache, written, a.BH, a.w) &&
+              encode_rows_map(&p.tm_vc, a.v_cache, written, a.BH, a.w);
+    }
     else
         okm = okm && encode_rows_map(&p.tm_kc, a.k, L, a.BH, st) && encode_rows_map(&p.tm_vc, a.v, L, a.BH, st);
     if (!okm) return fail(SWA_ERR_INVALID, "cuTensorMapEncodeTiled rejected a tensor (alignment or size)");

@@ -1,0 +1,89 @@
+"""Parity at the full workload sizes, in the launch configuration the benchmark times, on sampled
+outputs the oracle computes row by row (sampled heads x row blocks at the sequence start, around the
+window edge, in the middle, at chunk boundaries and at the ragged end)."""
+import math
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import swa_inputs
+from gpu_common import LSE_ABS, compare, oracle_rows, require_gpu
+
+pytestmark = pytest.mark.gpu
+
+
+def check_samples(name, o, lse, q, k, v, wl, heads, blocks):
+    B, H, L, d = q.shape
+    ref = oracle_rows(q, k, v, heads, blocks, wl.w, wl.s, wl.scale)
+    of = o.reshape(B * H, L, d)
+    lf = lse.reshape(B * H, L)
+    for (bh, r0), (o_ref, l_ref) in ref.items():
+        r1 = r0 + o_ref.shape[0]
+        compare(f"{name} bh={bh} rows {r0}..{r1 - 1}", of[bh, r0:r1], o_ref, torch.bfloat16)
+        assert np.abs(lf[bh, r0:r1].cpu().double().numpy() - l_ref).max() < LSE_ABS
+
+
+@pytest.mark.parametrize("name,heads,blocks", [
+    ("prefill_llama7b_L8192_w1024_s4", [0, 17, 31], [(0, 256), (894, 1154), (4000, 4128), (7992, 8192)]),
+    ("prefill_mistral_B2_L32768_w4096_s0", [0, 33, 63], [(0, 256), (3966, 4226), (16384, 16512), (32568, 32768)]),
+    ("prefill_mistral_B2_L32768_w4096_s4", [1, 40, 62], [(0, 256), (3966, 4226), (16384, 16512), (32568, 32768)]),
+])
+def test_full_size_prefill(name, heads, blocks):
+    swa = require_gpu()
+    wl = swa_inputs.WORKLOADS[name]
+    q, k, v = swa_inputs.workload_inputs(wl, "cuda")
+    lse = torch.empty((wl.B, wl.H, wl.L), dtype=torch.float32, device="cuda")
+    o = swa.swa_sink_prefill(q, k, v, wl.w, wl.s, lse=lse)
+    assert swa.swa_device_status() == swa.SWA_OK, swa.last_error()
+    assert torch.isfinite(o).all()
+    check_samples(name, o, lse, q, k, v, wl, heads, blocks)
+
+
+def test_full_size_chunked_prefill():
+    swa = require_gpu()
+    wl = swa_inputs.WORKLOADS["chunked_mistral_L131072_w4096_s4_C4096"]
+    q, k, v = swa_inputs.workload_inputs(wl, "cuda")
+    kc = torch.full((wl.B, wl.H, wl.w, wl.d), float("nan"), dtype=torch.bfloat16, device="cuda")
+    vc = torch.full_like(kc, float("nan"))
+    lse = torch.empty((wl.B, wl.H, wl.L), dtype=torch.float32, device="cuda")
+    o = swa.swa_sink_prefill_chunked(q, k, v, wl.w, wl.s, wl.chunk, kc, vc, lse=lse)
+    assert swa.swa_device_status() == swa.SWA_OK, swa.last_error()
+    assert torch.isfinite(o).all()
+    C = wl.chunk
+    blocks = [(0, 256), (C - 64, C + 192), (2 * C - 100, 2 * C + 100), (16 * C - 64, 16 * C + 64),
+              (31 * C - 1, 31 * C + 129), (wl.L - 256, wl.L)]
+    check_samples("chunked", o, lse, q, k, v, wl, [0, 13, 31], blocks)
+
+
+def test_full_size_streaming_decode():
+    # 20480 steps of write + decode at B=64, H=40, 4 sink + 1020 recent slots; 8 (b, h) pairs are checked
+    # against the oracle's history definition at every step
+    swa = require_gpu()
+    wl = swa_inputs.WORKLOADS["decode_llama13b_B64_w1024_s4_20480"]
+    B, H, d, w, s, T = wl.B, wl.H, wl.d, wl.w, wl.s, wl.L
+    qs = swa_inputs.normal((T, B, H, d), wl.seed, swa_inputs.TID_Q, torch.bfloat16, "cuda")
+    ks = swa_inputs.normal((T, B, H, d), wl.seed, swa_inputs.TID_K, torch.bfloat16, "cuda")
+    vs = swa_inputs.normal((T, B, H, d), wl.seed, swa_inputs.TID_V, torch.bfloat16, "cuda")
+    ks[:4] *= 4.0
+    kc = torch.zeros((B, H, w, d), dtype=torch.bfloat16, device="cuda")
+    vc = torch.zeros_like(kc)
+    pairs = torch.tensor([0, 1, 39, 40, 777, 1300, 2000, B * H - 1], device="cuda")
+    outs = torch.empty((T, len(pairs), d), dtype=torch.bfloat16, device="cuda")
+    lses = torch.empty((T, len(pairs)), dtype=torch.float32, device="cuda")
+    o = torch.empty((B, H, d), dtype=torch.bfloat16, device="cuda")
+    lse = torch.empty((B, H), dtype=torch.float32, device="cuda")
+    for t in range(T):
+        swa.kv_rolling_write(kc, vc, ks[t].unsqueeze(2), vs[t].unsqueeze(2), w, s, t)
+        swa.swa_sink_decode_step(qs[t], kc, vc, t, w, s, o=o, lse=lse)
+        outs[t] = o.reshape(B * H, d).index_select(0, pairs)
+        lses[t] = lse.reshape(B * H).index_select(0, pairs)
+    assert swa.swa_device_status() == swa.SWA_OK, swa.last_error()
+    pos = np.arange(T)
+    for j, bh in enumerate(pairs.tolist()):
+        b, h = divmod(bh, H)
+        qh, kh, vh = (x[:, b, h].float().cpu().numpy()[None] for x in (qs, ks, vs))
+        o_ref, l_ref = oracle.attend(qh, pos, kh, vh, pos, w, s, wl.scale)
+        compare(f"decode bh={bh}", outs[:, j], o_ref[0], torch.bfloat16)
+        assert np.abs(lses[:, j].cpu().double().numpy() - l_ref[0]).max() < LSE_ABS

@@ -81,8 +81,8 @@ def test_prefill_with_cache(dtype, d, L, w, s, pos0):
     swa = require_gpu()
     B, H = 1, 2
     q, k, v = inputs(B, H, pos0 + L, d, dtype, 40 + pos0, sink_boost=True)
-    kc = torch.zeros((B, H, w, d), dtype=dtype, device="cuda")
-    vc = torch.zeros_like(kc)
+    kc = torch.full((B, H, w, d), float("nan"), dtype=dtype, device="cuda")
+    vc = torch.full_like(kc, float("nan"))
     swa.kv_rolling_write(kc, vc, k[:, :, :pos0].contiguous(), v[:, :, :pos0].contiguous(), w, s, 0)
     qc, kk, vv = (x[:, :, pos0:].contiguous() for x in (q, k, v))
     lse = torch.empty((B, H, L), dtype=torch.float32, device="cuda")
@@ -99,8 +99,9 @@ def test_chunked_prefill(L, w, s, chunk):
     swa = require_gpu()
     B, H, d = 1, 2, 128
     q, k, v = inputs(B, H, L, d, torch.bfloat16, 60 + chunk, sink_boost=True)
-    kc = torch.empty((B, H, w, d), dtype=torch.bfloat16, device="cuda")
-    vc = torch.empty_like(kc)
+    # the scratch cache starts as NaN: slots not yet written must never reach the result
+    kc = torch.full((B, H, w, d), float("nan"), dtype=torch.bfloat16, device="cuda")
+    vc = torch.full_like(kc, float("nan"))
     lse = torch.empty((B, H, L), dtype=torch.float32, device="cuda")
     o = swa.swa_sink_prefill_chunked(q, k, v, w, s, chunk, kc, vc, lse=lse)
     o_full = swa.swa_sink_prefill(q, k, v, w, s)
@@ -121,8 +122,8 @@ def test_chunked_prefill_fp32():
     swa = require_gpu()
     B, H, L, d, w, s = 1, 1, 200, 16, 16, 4
     q, k, v = inputs(B, H, L, d, torch.float32, 3)
-    kc = torch.empty((B, H, w, d), device="cuda")
-    vc = torch.empty_like(kc)
+    kc = torch.full((B, H, w, d), float("nan"), device="cuda")
+    vc = torch.full_like(kc, float("nan"))
     o = swa.swa_sink_prefill_chunked(q, k, v, w, s, 37, kc, vc)
     o_ref, _ = oracle.prefill(q, k, v, w, s, 0.25)
     compare("chunked fp32", o, o_ref, torch.float32)
