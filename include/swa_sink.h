@@ -147,6 +147,7 @@ int swa_selftest_wait_timeout(int64_t timeout_ns, void *stream);
  *   b : mode 0: [128, 128] (N x K), C = A * B^T  (both operands K-major, as in Q K^T)
  *       mode 1: [128, 128] (K x N), C = A * B    (B MN-major, as in P V)
  *       mode 2: as mode 1, but A is staged into shared memory by threads instead of TMA.
+ *       mode 3: as mode 1, but A is read by the MMA from tensor memory (staged there with tcgen05.st).
  *   c : [128, 128] fp32 row-major output.
  */
 int swa_selftest_umma(const void *a, const void *b, float *c, int mode, void *stream);

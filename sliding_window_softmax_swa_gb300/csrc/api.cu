@@ -232,7 +232,7 @@ extern "C" int swa_selftest_umma(const void *a, const void *b, float *c, int mod
     t_err[0] = 0;
     if (!a || !b || !c) return fail(SWA_ERR_INVALID, "a, b and c must be non-null");
     if (!aligned16(a) || !aligned16(b) || !aligned16(c)) return fail(SWA_ERR_INVALID, "a, b, c must be 16-byte aligned");
-    if (mode < 0 || mode > 2) return fail(SWA_ERR_INVALID, "mode=%d not in {0, 1, 2}", mode);
+    if (mode < 0 || mode > 3) return fail(SWA_ERR_INVALID, "mode=%d not in {0, 1, 2, 3}", mode);
     return launch_selftest_umma(a, b, c, mode, static_cast<cudaStream_t>(stream));
 }
 

@@ -10,16 +10,19 @@
 //
 // CTA = one tile of 128 query rows of one (b, h); 192 threads in three roles:
 //   warps 0-3  softmax + epilogue: thread r owns query row r (= TMEM lane r);
-//   warp 4     TMA producer: Q once, then K/V tiles into a 2-stage ring (128 rows x 128 bf16 each,
-//              two 64-column boxes with the 128-byte swizzle);
-//   warp 5     MMA issuer (one thread): S_j = Q K_j^T into one of two TMEM S buffers, O += P_j V_j
-//              into the TMEM O accumulator.  P_j (bf16) is written by the softmax threads into shared
-//              memory in the same swizzled K-major layout TMA produces for Q.
-// TMEM: S0 = columns [0,128), S1 = [128,256), O = [256,384) (fp32, lane = query row).
-// Pipeline: QK_{j+1} runs on the tensor cores while the softmax threads work on S_j; PV_j starts as
-// soon as P_j is in shared memory.  The online softmax keeps a running max in log2 units and only
-// rescales O (TMEM load, multiply, store) when the max grows by more than 8 (a factor 256), so p <= 256
-// always fits bf16/fp32 and the rescale is rare; O and l always share the same reference max.
+//   warp 4     TMA producer: Q once, then K tiles into a 3-stage ring and V tiles into a 2-stage ring
+//              (128 rows x 128 bf16 each, two 64-column boxes with the 128-byte swizzle).  A K slot
+//              frees as soon as its QK product completes, a V slot after its PV product, so K loads run
+//              up to three tiles ahead;
+//   warp 5     MMA issuer (one thread): S_j = Q K_j^T into one of two TMEM S buffers, O += P_j V_j into
+//              the TMEM O accumulator, with P_j (bf16) read by the MMA straight from tensor memory.
+// TMEM: S0 = columns [0,128), S1 = [128,256), O = [256,384) (fp32, lane = query row).  The softmax
+// threads overwrite the first 64 columns of S_j with P_j (two bf16 per column) once they hold S_j in
+// registers.  Pipeline: QK_{j+1} runs on the tensor cores while the softmax threads work on S_j; PV_j
+// starts as soon as P_j is in TMEM, followed by QK_{j+2}.  The online softmax keeps a running max in
+// log2 units and only rescales O (TMEM load, multiply, store) when the max grows by more than 8 (a
+// factor 256), so p <= 256 always fits bf16/fp32 and the rescale is rare; O and l always share the same
+// reference max.
 //
 // Key tiles.  For the query tile [q0, q1] the key positions needed are the sinks [0, min(s, blo)) and
 // the band [blo, q1] with blo = max(0, q0 - m + 1).  Positions >= pos0 are rows of this call's k/v;
@@ -46,7 +49,8 @@ namespace tc {
 constexpr int BM = 128;                    // query rows per CTA
 constexpr int BN = 128;                    // keys per tile
 constexpr int HD = 128;                    // head dimension
-constexpr int NST = 2;                     // K/V pipeline stages
+constexpr int NK = 3;                      // K tile stages (a slot frees after its QK product)
+constexpr int NV = 2;                      // V tile stages (a slot frees after its PV product)
 constexpr uint32_t HALF_BYTES = 128 * 128;  // one 64-column half of a 128-row bf16 tile (16 KB)
 constexpr uint32_t TILE_BYTES = 2 * HALF_BYTES;
 constexpr int MAX_TILES = 160;
@@ -57,9 +61,8 @@ constexpr float kRescaleLog2 = 8.f;  // rescale O only when the running max grow
 
 constexpr uint32_t OFF_Q = 0;
 constexpr uint32_t OFF_K = OFF_Q + TILE_BYTES;
-constexpr uint32_t OFF_V = OFF_K + NST * TILE_BYTES;
-constexpr uint32_t OFF_P = OFF_V + NST * TILE_BYTES;
-constexpr uint32_t OFF_BAR = OFF_P + TILE_BYTES;
+constexpr uint32_t OFF_V = OFF_K + NK * TILE_BYTES;
+constexpr uint32_t OFF_BAR = OFF_V + NV * TILE_BYTES;
 constexpr uint32_t OFF_MISC = OFF_BAR + 256;
 constexpr uint32_t OFF_TILES = OFF_MISC + 64;
 constexpr uint32_t SMEM_USED = OFF_TILES + MAX_TILES * 16;
@@ -155,13 +158,12 @@ __device__ __forceinline__ void issue_qk(uint32_t d_tmem, uint32_t q_addr, uint3
     }
 }
 
-__device__ __forceinline__ void issue_pv(uint32_t d_tmem, uint32_t p_addr, uint32_t v_addr, bool accumulate) {
+__device__ __forceinline__ void issue_pv(uint32_t d_tmem, uint32_t p_tmem, uint32_t v_addr, bool accumulate) {
 #pragma unroll
     for (int kk = 0; kk < BN / 16; ++kk) {
-        const uint32_t a_off = (kk >> 2) * HALF_BYTES + (kk & 3) * 32;  // P: 16 keys along the K-major row
-        const uint32_t b_off = kk * 16 * 128;                            // V: 16 key rows of 128 bytes
-        umma_ss(d_tmem, sdesc_sw128(p_addr + a_off, 16, 1024), sdesc_sw128(v_addr + b_off, HALF_BYTES, 1024),
-                IDESC_PV, (accumulate || kk > 0) ? 1u : 0u);
+        // P from TMEM: 16 keys = 8 columns of packed bf16 pairs; V: 16 key rows of 128 bytes (MN-major)
+        umma_ts(d_tmem, p_tmem + kk * 8, sdesc_sw128(v_addr + kk * 16 * 128, HALF_BYTES, 1024), IDESC_PV,
+                (accumulate || kk > 0) ? 1u : 0u);
     }
 }
 
@@ -170,10 +172,11 @@ __global__ void __launch_bounds__(kThreads, 1) swa_prefill_tc_kernel(const __gri
     uint8_t *sm = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     uint64_t *bars = reinterpret_cast<uint64_t *>(sm + OFF_BAR);
     uint64_t *qfull = bars;
-    uint64_t *kfull = bars + 1;
-    uint64_t *vfull = kfull + NST;
-    uint64_t *kvempty = vfull + NST;
-    uint64_t *sfull = kvempty + NST;  // [2]
+    uint64_t *kfull = qfull + 1;     // [NK]
+    uint64_t *kempty = kfull + NK;   // [NK]
+    uint64_t *vfull = kempty + NK;   // [NV]
+    uint64_t *vempty = vfull + NV;   // [NV]
+    uint64_t *sfull = vempty + NV;   // [2]
     uint64_t *pfull = sfull + 2;
     uint64_t *pvdone = pfull + 1;
     uint64_t *ofull = pvdone + 1;
@@ -194,10 +197,13 @@ __global__ void __launch_bounds__(kThreads, 1) swa_prefill_tc_kernel(const __gri
         *abort_flag = 0;
         *ntiles_s = build_tiles(tiles, q0, q1, P.pos0, P.s, P.m, P.w);
         mbar_init(qfull, 1);
-        for (int i = 0; i < NST; ++i) {
+        for (int i = 0; i < NK; ++i) {
             mbar_init(&kfull[i], 1);
+            mbar_init(&kempty[i], 1);
+        }
+        for (int i = 0; i < NV; ++i) {
             mbar_init(&vfull[i], 1);
-            mbar_init(&kvempty[i], 1);
+            mbar_init(&vempty[i], 1);
         }
         mbar_init(&sfull[0], 1);
         mbar_init(&sfull[1], 1);
@@ -222,6 +228,8 @@ __global__ void __launch_bounds__(kThreads, 1) swa_prefill_tc_kernel(const __gri
 
     if (warp == 4) {
         // ------------------------------------------------------------------ TMA producer
+        // K tiles run up to NK tiles ahead of the V tiles: a K slot frees as soon as its QK product is
+        // done, a V slot only after its PV product.
         if (lane == 0 && ok) {
             tma_prefetch_desc(&P.tm_q);
             tma_prefetch_desc(&P.tm_k);
@@ -230,36 +238,41 @@ __global__ void __launch_bounds__(kThreads, 1) swa_prefill_tc_kernel(const __gri
             mbar_arrive_expect_tx(qfull, TILE_BYTES);
             tma_load_3d(qs, &P.tm_q, qfull, 0, row_start, bh);
             tma_load_3d(qs + HALF_BYTES, &P.tm_q, qfull, 64, row_start, bh);
-            int issued = 0;
-            for (int j = 0; j < nt; ++j) {
-                const int st = j % NST;
-                const uint32_t ph = (j / NST) & 1;
-                if (!mbar_wait(&kvempty[st], ph ^ 1, wc, 1)) break;
-                const Tile T = tiles[j];
-                const CUtensorMap *mk = T.src ? &P.tm_kc : &P.tm_k;
+            int jk = 0, jv = 0;
+            bool fine = true;
+            while (fine && jv < nt) {
+                while (jk < nt && jk < jv + NK) {
+                    const int st = jk % NK;
+                    if (!mbar_wait(&kempty[st], ((jk / NK) & 1) ^ 1, wc, 1)) { fine = false; break; }
+                    const Tile T = tiles[jk];
+                    const CUtensorMap *mk = T.src ? &P.tm_kc : &P.tm_k;
+                    uint8_t *ks = sm + OFF_K + st * TILE_BYTES;
+                    mbar_arrive_expect_tx(&kfull[st], TILE_BYTES);
+                    tma_load_3d(ks, mk, &kfull[st], 0, T.row0, bh);
+                    tma_load_3d(ks + HALF_BYTES, mk, &kfull[st], 64, T.row0, bh);
+                    ++jk;
+                }
+                if (!fine) break;
+                const int sv = jv % NV;
+                if (!mbar_wait(&vempty[sv], ((jv / NV) & 1) ^ 1, wc, 9)) break;
+                const Tile T = tiles[jv];
                 const CUtensorMap *mv = T.src ? &P.tm_vc : &P.tm_v;
-                uint8_t *ks = sm + OFF_K + st * TILE_BYTES;
-                uint8_t *vs = sm + OFF_V + st * TILE_BYTES;
-                mbar_arrive_expect_tx(&kfull[st], TILE_BYTES);
-                tma_load_3d(ks, mk, &kfull[st], 0, T.row0, bh);
-                tma_load_3d(ks + HALF_BYTES, mk, &kfull[st], 64, T.row0, bh);
-                mbar_arrive_expect_tx(&vfull[st], TILE_BYTES);
-                tma_load_3d(vs, mv, &vfull[st], 0, T.row0, bh);
-                tma_load_3d(vs + HALF_BYTES, mv, &vfull[st], 64, T.row0, bh);
-                issued = j + 1;
+                uint8_t *vs = sm + OFF_V + sv * TILE_BYTES;
+                mbar_arrive_expect_tx(&vfull[sv], TILE_BYTES);
+                tma_load_3d(vs, mv, &vfull[sv], 0, T.row0, bh);
+                tma_load_3d(vs + HALF_BYTES, mv, &vfull[sv], 64, T.row0, bh);
+                ++jv;
             }
             if (*abort_flag) {  // make sure no copy is still landing in shared memory
                 mbar_wait_drain(qfull, 0);
-                for (int j = (issued > NST ? issued - NST : 0); j < issued; ++j) {
-                    mbar_wait_drain(&kfull[j % NST], (j / NST) & 1);
-                    mbar_wait_drain(&vfull[j % NST], (j / NST) & 1);
-                }
+                for (int j = (jk > NK ? jk - NK : 0); j < jk; ++j) mbar_wait_drain(&kfull[j % NK], (j / NK) & 1);
+                for (int j = (jv > NV ? jv - NV : 0); j < jv; ++j) mbar_wait_drain(&vfull[j % NV], (j / NV) & 1);
             }
         }
     } else if (warp == 5) {
         // ------------------------------------------------------------------ MMA issuer
         if (lane == 0 && ok) {
-            const uint32_t q_addr = smem_u32(sm + OFF_Q), p_addr = smem_u32(sm + OFF_P);
+            const uint32_t q_addr = smem_u32(sm + OFF_Q);
             const uint32_t k_addr0 = smem_u32(sm + OFF_K), v_addr0 = smem_u32(sm + OFF_V);
             bool issued_any = false, fine = true;
             if (!mbar_wait(qfull, 0, wc, 2) || !mbar_wait(&kfull[0], 0, wc, 3)) fine = false;
@@ -267,23 +280,25 @@ __global__ void __launch_bounds__(kThreads, 1) swa_prefill_tc_kernel(const __gri
                 tc_fence_after();
                 issue_qk(tmem + kColS0, q_addr, k_addr0);
                 umma_commit(&sfull[0]);
+                umma_commit(&kempty[0]);
                 issued_any = true;
             }
             for (int j = 0; fine && j < nt; ++j) {
-                if (j + 1 < nt) {
-                    const int st1 = (j + 1) % NST;
-                    if (!mbar_wait(&kfull[st1], ((j + 1) / NST) & 1, wc, 3)) { fine = false; break; }
+                if (j + 1 < nt) {  // S_{j+1} = Q K_{j+1}^T while the softmax threads work on S_j
+                    const int sk = (j + 1) % NK;
+                    if (!mbar_wait(&kfull[sk], ((j + 1) / NK) & 1, wc, 3)) { fine = false; break; }
                     tc_fence_after();
-                    issue_qk(tmem + (((j + 1) & 1) ? kColS1 : kColS0), q_addr, k_addr0 + st1 * TILE_BYTES);
+                    issue_qk(tmem + (((j + 1) & 1) ? kColS1 : kColS0), q_addr, k_addr0 + sk * TILE_BYTES);
                     umma_commit(&sfull[(j + 1) & 1]);
+                    umma_commit(&kempty[sk]);
                 }
-                const int st = j % NST;
+                const int sv = j % NV;
                 if (!mbar_wait(pfull, j & 1, wc, 4)) { fine = false; break; }
-                if (!mbar_wait(&vfull[st], (j / NST) & 1, wc, 5)) { fine = false; break; }
+                if (!mbar_wait(&vfull[sv], (j / NV) & 1, wc, 5)) { fine = false; break; }
                 tc_fence_after();
-                issue_pv(tmem + kColO, p_addr, v_addr0 + st * TILE_BYTES, j > 0);
+                issue_pv(tmem + kColO, tmem + ((j & 1) ? kColS1 : kColS0), v_addr0 + sv * TILE_BYTES, j > 0);
                 umma_commit(pvdone);
-                umma_commit(&kvempty[st]);
+                umma_commit(&vempty[sv]);
             }
             if (fine) umma_commit(ofull);
             if (issued_any) {  // no MMA may still be running when TMEM is freed
@@ -296,45 +311,43 @@ __global__ void __launch_bounds__(kThreads, 1) swa_prefill_tc_kernel(const __gri
         const int r = threadIdx.x;  // query row within the tile == TMEM lane
         const int t = q0 + r;       // its absolute position
         const uint32_t lane_base = static_cast<uint32_t>(warp * 32) << 16;
-        const uint32_t p_addr = smem_u32(sm + OFF_P);
         const float sl2 = P.scale_log2;
-        float mrun = -INFINITY, lrun = 0.f;
+        float mrun = -INFINITY, lrun = 0.f;  // running max (log2 units) and sum
         bool fine = true;
         for (int j = 0; j < nt; ++j) {
             const int b = j & 1;
+            const uint32_t s_addr = tmem + lane_base + (b ? kColS1 : kColS0);
             fine = __all_sync(0xFFFFFFFFu, mbar_wait(&sfull[b], (j >> 1) & 1, wc, 6));
             if (!fine) break;
             tc_fence_after();
             float x[BN];
-            {
-                const uint32_t sa = tmem + lane_base + (b ? kColS1 : kColS0);
-                __syncwarp();
-                tmem_ld32(sa + 0, *reinterpret_cast<float(*)[32]>(&x[0]));
-                tmem_ld32(sa + 32, *reinterpret_cast<float(*)[32]>(&x[32]));
-                tmem_ld32(sa + 64, *reinterpret_cast<float(*)[32]>(&x[64]));
-                tmem_ld32(sa + 96, *reinterpret_cast<float(*)[32]>(&x[96]));
-            }
+            __syncwarp();
+            tmem_ld32(s_addr + 0, *reinterpret_cast<float(*)[32]>(&x[0]));
+            tmem_ld32(s_addr + 32, *reinterpret_cast<float(*)[32]>(&x[32]));
+            tmem_ld32(s_addr + 64, *reinterpret_cast<float(*)[32]>(&x[64]));
+            tmem_ld32(s_addr + 96, *reinterpret_cast<float(*)[32]>(&x[96]));
             const Tile T = tiles[j];
             // valid columns of this row: [0, b1] (sinks) and [a2, hc] (window), hc = last causal column
             const int hc = min(T.chi, t - T.pbase);
             const int b1 = min(hc, P.s - 1 - T.pbase);
             const int a2 = max(0, t - P.m + 1 - T.pbase);
             const bool full = (b1 >= BN - 1) || (hc >= BN - 1 && (a2 <= 0 || b1 >= a2 - 1));
-            float mx = -INFINITY;
+            float mx0 = -INFINITY, mx1 = -INFINITY;
             if (full) {
 #pragma unroll
-                for (int c = 0; c < BN; ++c) {
-                    x[c] *= sl2;
-                    mx = fmaxf(mx, x[c]);
+                for (int c = 0; c < BN; c += 2) {
+                    mx0 = fmaxf(mx0, x[c]);
+                    mx1 = fmaxf(mx1, x[c + 1]);
                 }
             } else {
 #pragma unroll
                 for (int c = 0; c < BN; ++c) {
                     const bool valid = (c <= b1) || (c >= a2 && c <= hc);
-                    x[c] = valid ? x[c] * sl2 : -INFINITY;
-                    mx = fmaxf(mx, x[c]);
+                    x[c] = valid ? x[c] : -INFINITY;
+                    if (c & 1) mx1 = fmaxf(mx1, x[c]); else mx0 = fmaxf(mx0, x[c]);
                 }
             }
+            const float mx = fmaxf(mx0, mx1) * sl2;  // the scale is positive: max commutes with it
             float alpha = 1.f;
             bool resc = false;
             const float mnew = fmaxf(mrun, mx);
@@ -345,23 +358,23 @@ __global__ void __launch_bounds__(kThreads, 1) swa_prefill_tc_kernel(const __gri
                 }
                 mrun = mnew;
             }
-            const float mu = (mrun == -INFINITY) ? 0.f : mrun;
+            const float nmu = (mrun == -INFINITY) ? 0.f : -mrun;
             uint32_t pk[BN / 2];
-            float rs = 0.f;
+            float rs0 = 0.f, rs1 = 0.f;
 #pragma unroll
             for (int i = 0; i < BN / 2; ++i) {
-                const float p0 = ex2(x[2 * i] - mu), p1 = ex2(x[2 * i + 1] - mu);
-                rs += p0 + p1;
+                const float p0 = ex2(fmaf(x[2 * i], sl2, nmu)), p1 = ex2(fmaf(x[2 * i + 1], sl2, nmu));
+                rs0 += p0;
+                rs1 += p1;
                 pk[i] = pack_bf16x2(p0, p1);
             }
-            lrun = lrun * alpha + rs;
-            // the P buffer and O are free once PV_{j-1} has completed
-            if (j > 0) {
-                fine = __all_sync(0xFFFFFFFFu, mbar_wait(pvdone, (j - 1) & 1, wc, 7));
-                if (!fine) break;
-                tc_fence_after();
-            }
-            if (__any_sync(0xFFFFFFFFu, resc)) {
+            lrun = lrun * alpha + (rs0 + rs1);
+            if (__any_sync(0xFFFFFFFFu, resc)) {  // O (up to PV_{j-1}) must be final before it is rescaled
+                if (j > 0) {
+                    fine = __all_sync(0xFFFFFFFFu, mbar_wait(pvdone, (j - 1) & 1, wc, 7));
+                    if (!fine) break;
+                    tc_fence_after();
+                }
                 __syncwarp();
 #pragma unroll 1
                 for (int c = 0; c < HD; c += 32) {
@@ -372,12 +385,11 @@ __global__ void __launch_bounds__(kThreads, 1) swa_prefill_tc_kernel(const __gri
                     tmem_st32(tmem + lane_base + kColO + c, ov);
                 }
             }
-#pragma unroll
-            for (int ch = 0; ch < BN / 8; ++ch) {
-                const uint32_t addr = p_addr + (ch >> 3) * HALF_BYTES + sw128_offset(r, (ch & 7) * 8);
-                st_shared_v4(addr, pk[4 * ch], pk[4 * ch + 1], pk[4 * ch + 2], pk[4 * ch + 3]);
-            }
-            fence_proxy_async_smem();
+            // P_j (bf16) over the first 64 columns of its S buffer: the A operand of PV_j.  The last reader
+            // of those columns, PV_{j-2}, completed before QK_j (tcgen05 MMAs of a thread run in order).
+            __syncwarp();
+            tmem_st32u(s_addr + 0, *reinterpret_cast<uint32_t(*)[32]>(&pk[0]));
+            tmem_st32u(s_addr + 32, *reinterpret_cast<uint32_t(*)[32]>(&pk[32]));
             tc_fence_before();
             mbar_arrive(pfull);
         }
@@ -456,7 +468,7 @@ __global__ void __launch_bounds__(128, 1) selftest_umma_kernel(const __grid_cons
         mbar_init_fence();
     }
     if (warp == 0) {
-        tmem_alloc(tmem_slot, 128);
+        tmem_alloc(tmem_slot, 256);
         tmem_relinquish();
     }
     if (mode == 2) {  // stage A by threads in the 128-byte-swizzled K-major layout
@@ -471,10 +483,22 @@ __global__ void __launch_bounds__(128, 1) selftest_umma_kernel(const __grid_cons
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem = *tmem_slot;
+    if (mode == 3) {  // stage A into TMEM columns [128, 192): lane = row, two bf16 per 32-bit column
+        const uint32_t *src = reinterpret_cast<const uint32_t *>(a_glob + r * 128);
+        uint32_t u[32];
+        __syncwarp();
+        for (int h = 0; h < 2; ++h) {
+            for (int i = 0; i < 32; ++i) u[i] = src[h * 32 + i];
+            tmem_st32u(tmem + (static_cast<uint32_t>(warp * 32) << 16) + 128 + h * 32, u);
+        }
+        tc_fence_before();
+    }
+    __syncthreads();
+    tc_fence_after();
     const WaitCtl wc{abort_flag, status, kWaitTimeoutNs};
     if (threadIdx.x == 0) {
-        mbar_arrive_expect_tx(load_bar, mode == 2 ? TILE_BYTES : 2 * TILE_BYTES);
-        if (mode != 2) {
+        mbar_arrive_expect_tx(load_bar, mode >= 2 ? TILE_BYTES : 2 * TILE_BYTES);
+        if (mode < 2) {
             tma_load_3d(As, &ma, load_bar, 0, 0, 0);
             tma_load_3d(As + HALF_BYTES, &ma, load_bar, 64, 0, 0);
         }
@@ -488,6 +512,9 @@ __global__ void __launch_bounds__(128, 1) selftest_umma_kernel(const __grid_cons
                 if (mode == 0)
                     umma_ss(tmem, sdesc_sw128(a_addr + a_off, 16, 1024), sdesc_sw128(b_addr + a_off, 16, 1024),
                             IDESC_QK, kk > 0 ? 1u : 0u);
+                else if (mode == 3)
+                    umma_ts(tmem, tmem + 128 + kk * 8, sdesc_sw128(b_addr + kk * 2048, HALF_BYTES, 1024), IDESC_PV,
+                            kk > 0 ? 1u : 0u);
                 else
                     umma_ss(tmem, sdesc_sw128(a_addr + a_off, 16, 1024),
                             sdesc_sw128(b_addr + kk * 2048, HALF_BYTES, 1024), IDESC_PV, kk > 0 ? 1u : 0u);
@@ -512,7 +539,7 @@ __global__ void __launch_bounds__(128, 1) selftest_umma_kernel(const __grid_cons
     __syncthreads();
     if (warp == 0) {
         tc_fence_after();
-        tmem_dealloc(tmem, 128);
+        tmem_dealloc(tmem, 256);
     }
 }
 

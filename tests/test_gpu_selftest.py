@@ -22,7 +22,7 @@ def test_wait_timeout_is_reported_and_context_survives():
     assert float((x * 2).sum()) == 8.0  # the context is still usable
 
 
-@pytest.mark.parametrize("mode", [0, 1, 2])
+@pytest.mark.parametrize("mode", [0, 1, 2, 3])
 def test_umma_tile_matches_matmul(mode):
     swa = require_gpu()
     g = torch.Generator(device="cpu").manual_seed(7 + mode)
