@@ -14,6 +14,8 @@ namespace swa {
 
 // One error word per device.  Kernels receive its address; swa_device_status() reads and clears it.
 __device__ unsigned g_swa_status_word;
+// Where the first bounded wait of the device ran out (see WaitCtl); cleared with the error word.
+__device__ unsigned long long g_swa_timeout_info;
 
 static thread_local char t_err[512];
 
@@ -43,6 +45,20 @@ unsigned *device_status_word() {
             return nullptr;
         }
         ptrs[dev] = static_cast<unsigned *>(p);
+    }
+    return ptrs[dev];
+}
+
+unsigned long long *device_timeout_info() {
+    static std::mutex mu;
+    static unsigned long long *ptrs[64] = {nullptr};
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return nullptr;
+    std::lock_guard<std::mutex> lk(mu);
+    if (!ptrs[dev]) {
+        void *p = nullptr;
+        if (cudaGetSymbolAddress(&p, g_swa_timeout_info) != cudaSuccess) return nullptr;
+        ptrs[dev] = static_cast<unsigned long long *>(p);
     }
     return ptrs[dev];
 }
@@ -92,10 +108,16 @@ extern "C" int swa_device_status(void *stream) {
     if (e != cudaSuccess) return fail(SWA_ERR_CUDA, "reading the device error word: %s", cudaGetErrorString(e));
     if (word != 0) {
         unsigned zero = 0;
+        unsigned long long info = 0, zero64 = 0;
+        cudaMemcpyFromSymbol(&info, g_swa_timeout_info, sizeof(info));
         cudaMemcpyToSymbol(g_swa_status_word, &zero, sizeof(zero));
+        cudaMemcpyToSymbol(g_swa_timeout_info, &zero64, sizeof(zero64));
         if (word & kDevTimeout)
-            return fail(SWA_ERR_TIMEOUT, "a bounded device wait ran out (error word 0x%08x, site %u)", word,
-                        (word >> kWhereShift) & 0xFFu);
+            return fail(SWA_ERR_TIMEOUT,
+                        "a bounded device wait ran out (error word 0x%08x; first: site %u, tag %u, warp %u, "
+                        "block (%u, %u))",
+                        word, unsigned(info & 0xFF), unsigned((info >> 8) & 0xFFF), unsigned((info >> 20) & 0xFFF),
+                        unsigned((info >> 32) & 0xFFFF), unsigned((info >> 48) & 0xFFFF));
         return fail(SWA_ERR_CUDA, "device consistency check failed (error word 0x%08x)", word);
     }
     return SWA_OK;

@@ -83,6 +83,7 @@ struct Params {
     void *o;
     float *lse;
     unsigned *status;
+    unsigned long long *info;
     int64_t seq_stride;  // rows between (b, h) blocks of q/k/v/o/lse
     int L, pos0, w, s, m, n_qtiles;
     float scale_log2;
@@ -224,7 +225,7 @@ __global__ void __launch_bounds__(kThreads, 1) swa_prefill_tc_kernel(const __gri
     const int nt = *ntiles_s;
     const bool ok = nt >= 1 && nt <= MAX_TILES;
     if (!ok && threadIdx.x == 0) atomicOr(P.status, kDevBadArg);
-    const WaitCtl wc{abort_flag, P.status, P.timeout_ns};
+    const WaitCtl wc{abort_flag, P.status, P.info, P.timeout_ns};
 
     if (warp == 4) {
         // ------------------------------------------------------------------ TMA producer
@@ -243,7 +244,7 @@ __global__ void __launch_bounds__(kThreads, 1) swa_prefill_tc_kernel(const __gri
             while (fine && jv < nt) {
                 while (jk < nt && jk < jv + NK) {
                     const int st = jk % NK;
-                    if (!mbar_wait(&kempty[st], ((jk / NK) & 1) ^ 1, wc, 1)) { fine = false; break; }
+                    if (!mbar_wait(&kempty[st], ((jk / NK) & 1) ^ 1, wc, 1, jk)) { fine = false; break; }
                     const Tile T = tiles[jk];
                     const CUtensorMap *mk = T.src ? &P.tm_kc : &P.tm_k;
                     uint8_t *ks = sm + OFF_K + st * TILE_BYTES;
@@ -254,7 +255,7 @@ __global__ void __launch_bounds__(kThreads, 1) swa_prefill_tc_kernel(const __gri
                 }
                 if (!fine) break;
                 const int sv = jv % NV;
-                if (!mbar_wait(&vempty[sv], ((jv / NV) & 1) ^ 1, wc, 9)) break;
+                if (!mbar_wait(&vempty[sv], ((jv / NV) & 1) ^ 1, wc, 9, jv)) break;
                 const Tile T = tiles[jv];
                 const CUtensorMap *mv = T.src ? &P.tm_vc : &P.tm_v;
                 uint8_t *vs = sm + OFF_V + sv * TILE_BYTES;
@@ -286,15 +287,15 @@ __global__ void __launch_bounds__(kThreads, 1) swa_prefill_tc_kernel(const __gri
             for (int j = 0; fine && j < nt; ++j) {
                 if (j + 1 < nt) {  // S_{j+1} = Q K_{j+1}^T while the softmax threads work on S_j
                     const int sk = (j + 1) % NK;
-                    if (!mbar_wait(&kfull[sk], ((j + 1) / NK) & 1, wc, 3)) { fine = false; break; }
+                    if (!mbar_wait(&kfull[sk], ((j + 1) / NK) & 1, wc, 3, j + 1)) { fine = false; break; }
                     tc_fence_after();
                     issue_qk(tmem + (((j + 1) & 1) ? kColS1 : kColS0), q_addr, k_addr0 + sk * TILE_BYTES);
                     umma_commit(&sfull[(j + 1) & 1]);
                     umma_commit(&kempty[sk]);
                 }
                 const int sv = j % NV;
-                if (!mbar_wait(pfull, j & 1, wc, 4)) { fine = false; break; }
-                if (!mbar_wait(&vfull[sv], (j / NV) & 1, wc, 5)) { fine = false; break; }
+                if (!mbar_wait(pfull, j & 1, wc, 4, j)) { fine = false; break; }
+                if (!mbar_wait(&vfull[sv], (j / NV) & 1, wc, 5, j)) { fine = false; break; }
                 tc_fence_after();
                 issue_pv(tmem + kColO, tmem + ((j & 1) ? kColS1 : kColS0), v_addr0 + sv * TILE_BYTES, j > 0);
                 umma_commit(pvdone);
@@ -317,7 +318,7 @@ __global__ void __launch_bounds__(kThreads, 1) swa_prefill_tc_kernel(const __gri
         for (int j = 0; j < nt; ++j) {
             const int b = j & 1;
             const uint32_t s_addr = tmem + lane_base + (b ? kColS1 : kColS0);
-            fine = __all_sync(0xFFFFFFFFu, mbar_wait(&sfull[b], (j >> 1) & 1, wc, 6));
+            fine = __all_sync(0xFFFFFFFFu, mbar_wait(&sfull[b], (j >> 1) & 1, wc, 6, j));
             if (!fine) break;
             tc_fence_after();
             float x[BN];
@@ -371,7 +372,7 @@ __global__ void __launch_bounds__(kThreads, 1) swa_prefill_tc_kernel(const __gri
             lrun = lrun * alpha + (rs0 + rs1);
             if (__any_sync(0xFFFFFFFFu, resc)) {  // O (up to PV_{j-1}) must be final before it is rescaled
                 if (j > 0) {
-                    fine = __all_sync(0xFFFFFFFFu, mbar_wait(pvdone, (j - 1) & 1, wc, 7));
+                    fine = __all_sync(0xFFFFFFFFu, mbar_wait(pvdone, (j - 1) & 1, wc, 7, j));
                     if (!fine) break;
                     tc_fence_after();
                 }
@@ -393,7 +394,7 @@ __global__ void __launch_bounds__(kThreads, 1) swa_prefill_tc_kernel(const __gri
             tc_fence_before();
             mbar_arrive(pfull);
         }
-        if (fine) fine = __all_sync(0xFFFFFFFFu, mbar_wait(ofull, 0, wc, 8));
+        if (fine) fine = __all_sync(0xFFFFFFFFu, mbar_wait(ofull, 0, wc, 8, nt));
         if (fine) {
             tc_fence_after();
             const float inv = (lrun > 0.f) ? 1.f / lrun : 0.f;
@@ -444,7 +445,7 @@ __global__ void selftest_wait_kernel(unsigned *status, uint64_t timeout_ns) {
     __syncthreads();
     if (threadIdx.x == 0) {
         // nothing ever arrives on `bar`: the wait runs out, records the timeout and returns
-        const WaitCtl wc{&abort_flag, status, timeout_ns};
+        const WaitCtl wc{&abort_flag, status, nullptr, timeout_ns};
         mbar_wait(&bar, 0, wc, 99);
     }
 }
@@ -495,7 +496,7 @@ __global__ void __launch_bounds__(128, 1) selftest_umma_kernel(const __grid_cons
     }
     __syncthreads();
     tc_fence_after();
-    const WaitCtl wc{abort_flag, status, kWaitTimeoutNs};
+    const WaitCtl wc{abort_flag, status, nullptr, kWaitTimeoutNs};
     if (threadIdx.x == 0) {
         mbar_arrive_expect_tx(load_bar, mode >= 2 ? TILE_BYTES : 2 * TILE_BYTES);
         if (mode < 2) {
@@ -593,6 +594,7 @@ int launch_prefill_bf16_tc(const PrefillArgs &a) {
     p.o = a.o;
     p.lse = a.lse;
     p.status = status;
+    p.info = device_timeout_info();
     p.seq_stride = a.seq_stride;
     p.L = static_cast<int>(a.L);
     p.pos0 = static_cast<int>(a.pos0);

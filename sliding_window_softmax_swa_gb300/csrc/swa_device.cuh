@@ -59,16 +59,19 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
 }
 
 // Shared state of the bounded waits of one CTA: once any wait of the CTA gives up, `abort` is set
-// and every other wait of the CTA returns false at its next check.
+// and every other wait of the CTA returns false at its next check.  The first wait of the device that
+// runs out also leaves a record in `info`: site | tag << 8 | warp << 20 | blockIdx.x << 32 | blockIdx.y << 48.
 struct WaitCtl {
     volatile int *abort;      // in shared memory
     unsigned *status;         // device error word (global)
+    unsigned long long *info; // first-timeout record (global), may be null
     uint64_t timeout_ns;
 };
 
 // Wait until the phase with the given parity of `bar` has completed.  Returns false when the wait
 // ran out (or another wait of the CTA did); the caller must then stop its pipeline role.
-static __device__ __noinline__ bool mbar_wait_slow(uint32_t a, uint32_t parity, const WaitCtl &c, unsigned where) {
+static __device__ __noinline__ bool mbar_wait_slow(uint32_t a, uint32_t parity, const WaitCtl &c, unsigned where,
+                                                   unsigned tag) {
     const uint64_t t0 = globaltimer_ns();
     for (uint32_t it = 1;; ++it) {
         if (mbar_try_wait(a, parity)) return true;
@@ -76,16 +79,23 @@ static __device__ __noinline__ bool mbar_wait_slow(uint32_t a, uint32_t parity, 
             if (*c.abort) return false;
             if (globaltimer_ns() - t0 > c.timeout_ns) {
                 *c.abort = 1;
-                atomicOr(c.status, kDevTimeout | (where << kWhereShift));
+                atomicOr(c.status, kDevTimeout | ((where & 0xFFu) << kWhereShift));
+                if (c.info) {
+                    const unsigned long long rec =
+                        (where & 0xFFull) | ((tag & 0xFFFull) << 8) | ((threadIdx.x >> 5 & 0xFFFull) << 20) |
+                        ((blockIdx.x & 0xFFFFull) << 32) | ((blockIdx.y & 0xFFFFull) << 48);
+                    atomicCAS(c.info, 0ull, rec);
+                }
                 return false;
             }
         }
     }
 }
-__device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity, const WaitCtl &c, unsigned where) {
+__device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity, const WaitCtl &c, unsigned where,
+                                          unsigned tag = 0) {
     const uint32_t a = smem_u32(bar);
     if (mbar_try_wait(a, parity)) return true;
-    return mbar_wait_slow(a, parity, c, where);
+    return mbar_wait_slow(a, parity, c, where, tag);
 }
 
 // ---- TMA ----------------------------------------------------------------------------------------

@@ -13,6 +13,8 @@ int fail(int code, const char *fmt, ...);
 
 // Device error word of the current device (nullptr if it could not be resolved; the error is set).
 unsigned *device_status_word();
+// First-timeout record of the current device (nullptr if it could not be resolved).
+unsigned long long *device_timeout_info();
 
 // cuTensorMapEncodeTiled, resolved once through the runtime's driver entry point (no -lcuda).
 typedef CUresult (*EncodeTiledFn)(CUtensorMap *, CUtensorMapDataType, cuuint32_t, void *, const cuuint64_t *,
