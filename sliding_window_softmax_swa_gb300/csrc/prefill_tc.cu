@@ -178,8 +178,10 @@ __global__ void __launch_bounds__(kThreads, 1) swa_prefill_tc_kernel(const __gri
     uint64_t *vfull = kempty + NK;   // [NV]
     uint64_t *vempty = vfull + NV;   // [NV]
     uint64_t *sfull = vempty + NV;   // [2]
-    uint64_t *pfull = sfull + 2;
-    uint64_t *pvdone = pfull + 1;
+    // P_j ready, by tile parity: a softmax warp can run one tile ahead of another (S_{j+1} is ready
+    // before every warp has finished tile j), so arrivals for tiles j and j+1 must not share a barrier.
+    uint64_t *pfull = sfull + 2;     // [2]
+    uint64_t *pvdone = pfull + 2;
     uint64_t *ofull = pvdone + 1;
     uint64_t *drain = ofull + 1;
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(sm + OFF_MISC);
@@ -208,7 +210,8 @@ __global__ void __launch_bounds__(kThreads, 1) swa_prefill_tc_kernel(const __gri
         }
         mbar_init(&sfull[0], 1);
         mbar_init(&sfull[1], 1);
-        mbar_init(pfull, BM);
+        mbar_init(&pfull[0], BM);
+        mbar_init(&pfull[1], BM);
         mbar_init(pvdone, 1);
         mbar_init(ofull, 1);
         mbar_init(drain, 1);
@@ -294,7 +297,7 @@ __global__ void __launch_bounds__(kThreads, 1) swa_prefill_tc_kernel(const __gri
                     umma_commit(&kempty[sk]);
                 }
                 const int sv = j % NV;
-                if (!mbar_wait(pfull, j & 1, wc, 4, j)) { fine = false; break; }
+                if (!mbar_wait(&pfull[j & 1], (j >> 1) & 1, wc, 4, j)) { fine = false; break; }
                 if (!mbar_wait(&vfull[sv], (j / NV) & 1, wc, 5, j)) { fine = false; break; }
                 tc_fence_after();
                 issue_pv(tmem + kColO, tmem + ((j & 1) ? kColS1 : kColS0), v_addr0 + sv * TILE_BYTES, j > 0);
@@ -392,7 +395,7 @@ __global__ void __launch_bounds__(kThreads, 1) swa_prefill_tc_kernel(const __gri
             tmem_st32u(s_addr + 0, *reinterpret_cast<uint32_t(*)[32]>(&pk[0]));
             tmem_st32u(s_addr + 32, *reinterpret_cast<uint32_t(*)[32]>(&pk[32]));
             tc_fence_before();
-            mbar_arrive(pfull);
+            mbar_arrive(&pfull[b]);
         }
         if (fine) fine = __all_sync(0xFFFFFFFFu, mbar_wait(ofull, 0, wc, 8, nt));
         if (fine) {

@@ -93,11 +93,14 @@ def test_prefill_with_cache(dtype, d, L, w, s, pos0):
     assert np.abs(lse.cpu().double().numpy() - l_ref[:, :, pos0:]).max() < LSE_ABS
 
 
-@pytest.mark.parametrize("L,w,s,chunk", [(1000, 300, 4, 256), (1000, 300, 4, 300), (777, 64, 4, 100),
-                                         (640, 128, 0, 128), (500, 200, 4, 1000), (1024, 512, 4, 96)])
-def test_chunked_prefill(L, w, s, chunk):
+@pytest.mark.parametrize("L,w,s,chunk,H", [(1000, 300, 4, 256, 2), (1000, 300, 4, 300, 2), (777, 64, 4, 100, 2),
+                                           (640, 128, 0, 128, 2), (500, 200, 4, 1000, 2), (1024, 512, 4, 96, 2),
+                                           # sink rescales make softmax warps drift a tile apart: a race here
+                                           # once mixed P-ready arrivals of two tiles on one barrier
+                                           (8192, 1024, 4, 1024, 4), (6144, 2048, 4, 2048, 2)])
+def test_chunked_prefill(L, w, s, chunk, H):
     swa = require_gpu()
-    B, H, d = 1, 2, 128
+    B, d = 1, 128
     q, k, v = inputs(B, H, L, d, torch.bfloat16, 60 + chunk, sink_boost=True)
     # the scratch cache starts as NaN: slots not yet written must never reach the result
     kc = torch.full((B, H, w, d), float("nan"), dtype=torch.bfloat16, device="cuda")
