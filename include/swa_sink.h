@@ -154,9 +154,10 @@ int swa_selftest_umma(const void *a, const void *b, float *c, int mode, void *st
 
 /*
  * swa_prefill_tile_plan -- diagnostics (host only, no CUDA call): the key tiles the bf16 prefill kernel
- * walks for the query rows at absolute positions q0..q1 (one 128-row query tile) of a call starting at
- * pos0.  For tile i, tiles[4i..4i+3] = {source (0 = the call's k/v, 1 = rolling cache), first source
- * row, absolute position of column 0, last valid column}; columns c <= last valid column hold position
+ * walks for the query rows at absolute positions q0..q1 (one CTA: two query tiles of 128 rows, rows
+ * q0..q0+127 and q0+128..q1) of a call starting at pos0.  For tile i, tiles[5i..5i+4] = {source (0 = the
+ * call's k/v, 1 = rolling cache), first source row, absolute position of column 0, last valid column,
+ * bit mask of the query tiles that use it}; columns c <= last valid column hold position
  * (column-0 position + c).  Writes at most max_tiles entries; returns the tile count or a negative
  * swa_status.
  */

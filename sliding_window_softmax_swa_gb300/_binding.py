@@ -167,12 +167,13 @@ def swa_sink_decode_step(q, k_cache, v_cache, t: int, w: int, s: int, scale: flo
 
 
 def prefill_tile_plan(q0: int, q1: int, pos0: int, w: int, s: int):
-    """The key tiles the bf16 prefill walks for query rows q0..q1: list of (src, row0, pbase, chi)."""
-    buf = (ctypes.c_int * (4 * 256))()
+    """The key tiles the bf16 prefill walks for query rows q0..q1 (one CTA: two 128-row query tiles):
+    list of (src, row0, pbase, chi, used_by_mask)."""
+    buf = (ctypes.c_int * (5 * 256))()
     n = lib().swa_prefill_tile_plan(q0, q1, pos0, w, s, buf, 256)
     if n < 0:
         raise SwaError("swa_prefill_tile_plan", n, last_error())
-    return [tuple(buf[4 * i:4 * i + 4]) for i in range(min(n, 256))]
+    return [tuple(buf[5 * i:5 * i + 5]) for i in range(min(n, 256))]
 
 
 def swa_device_status(stream=None) -> int:

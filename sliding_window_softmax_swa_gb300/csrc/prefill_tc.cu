@@ -8,23 +8,27 @@
 // O(n^2) -> O(n k), banded patterns are hardware friendly), so each CTA walks only the key tiles that
 // intersect the band or the sink block of its query tile; no skipped tile is ever loaded.
 //
-// CTA = one tile of 128 query rows of one (b, h); 192 threads in three roles:
-//   warps 0-3  softmax + epilogue: thread r owns query row r (= TMEM lane r);
-//   warp 4     TMA producer: Q once, then K tiles into a 3-stage ring and V tiles into a 2-stage ring
-//              (128 rows x 128 bf16 each, two 64-column boxes with the 128-byte swizzle).  A K slot
-//              frees as soon as its QK product completes, a V slot after its PV product, so K loads run
-//              up to three tiles ahead;
-//   warp 5     MMA issuer (one thread): S_j = Q K_j^T into one of two TMEM S buffers, O += P_j V_j into
-//              the TMEM O accumulator, with P_j (bf16) read by the MMA straight from tensor memory.
-// TMEM: S0 = columns [0,128), S1 = [128,256), O = [256,384) (fp32, lane = query row).  The softmax
-// threads overwrite the first 64 columns of S_j with P_j (two bf16 per column) once they hold S_j in
-// registers.  Pipeline: QK_{j+1} runs on the tensor cores while the softmax threads work on S_j; PV_j
-// starts as soon as P_j is in TMEM, followed by QK_{j+2}.  The online softmax keeps a running max in
-// log2 units and only rescales O (TMEM load, multiply, store) when the max grows by more than 8 (a
-// factor 256), so p <= 256 always fits bf16/fp32 and the rescale is rare; O and l always share the same
-// reference max.
+// CTA = two query tiles of 128 rows (256 consecutive rows) of one (b, h); 320 threads in four roles:
+//   warps 0-3 / 4-7  softmax + epilogue of query tile 0 / 1: thread r owns row r of its tile
+//              (= TMEM lane r);
+//   warp 8     TMA producer: Q_0 and Q_1 once, then K tiles into a 3-stage ring and V tiles into a
+//              2-stage ring (128 rows x 128 bf16 each, two 64-column boxes with the 128-byte swizzle).
+//              A K slot frees as soon as the QK products that read it complete, a V slot after its PV
+//              products, so K loads run up to three tiles ahead;
+//   warp 9     MMA issuer (one thread).  Per key tile j: PV_0(j), QK_0(j+1), PV_1(j), QK_1(j+1), where
+//              QK_x(j) is S_x = Q_x K_j^T and PV_x(j) is O_x += P_x V_j with P_x (bf16) read by the MMA
+//              straight from tensor memory.  While the tensor cores work on one query tile, the softmax
+//              warpgroup of the other turns its S into P (ping-pong), and each K/V tile loaded from L2
+//              serves 256 query rows.
+// TMEM (512 columns): S_0, S_1 = [0,128), [128,256); O_0, O_1 = [256,384), [384,512) (fp32, lane = row).
+// The softmax threads overwrite the first 64 columns of S_x with P_x (two bf16 per column) after
+// reading them.  The online softmax keeps a running max in log2 units and only rescales O (TMEM load,
+// multiply, store) when the max grows by more than 8 (a factor 256), so p <= 256 always fits
+// bf16/fp32 and the rescale is rare; O and l always share the same reference max.  With one S buffer
+// per query tile, S_x(j) complete implies PV_x of the previous tile complete (tcgen05 MMAs of a thread
+// complete in order), so neither the P store nor the rescale needs another wait.
 //
-// Key tiles.  For the query tile [q0, q1] the key positions needed are the sinks [0, min(s, blo)) and
+// Key tiles.  For the query rows [q0, q1] of a CTA the key positions needed are the sinks [0, min(s, blo)) and
 // the band [blo, q1] with blo = max(0, q0 - m + 1).  Positions >= pos0 are rows of this call's k/v;
 // positions < pos0 (chunked prefill) live in the rolling cache: slot p for p < s, slot
 // s + ((p - s) mod m) for the rest ("滑窗与固定稀疏", eq attn-fixed-rolling and eq attn-fixed-streaming).
@@ -46,27 +50,32 @@
 namespace swa {
 namespace tc {
 
-constexpr int BM = 128;                    // query rows per CTA
-constexpr int BN = 128;                    // keys per tile
+constexpr int BH_ROWS = 128;               // query rows per query tile (= TMEM lanes)
+constexpr int BM = 2 * BH_ROWS;            // query rows per CTA: two query tiles
+constexpr int BN = 128;                    // keys per key tile
 constexpr int HD = 128;                    // head dimension
-constexpr int NK = 3;                      // K tile stages (a slot frees after its QK product)
-constexpr int NV = 2;                      // V tile stages (a slot frees after its PV product)
+constexpr int NK = 3;                      // K tile stages (a slot frees after its QK products)
+constexpr int NV = 2;                      // V tile stages (a slot frees after its PV products)
 constexpr uint32_t HALF_BYTES = 128 * 128;  // one 64-column half of a 128-row bf16 tile (16 KB)
 constexpr uint32_t TILE_BYTES = 2 * HALF_BYTES;
-constexpr int MAX_TILES = 160;
-constexpr int kThreads = 192;
+constexpr int MAX_TILES = 96;
+constexpr int kThreads = 320;              // warps 0-3 / 4-7: softmax of query tile 0 / 1; 8: TMA; 9: MMA
+constexpr int kWarpTma = 8, kWarpMma = 9;
 constexpr uint32_t kTmemCols = 512;
-constexpr uint32_t kColS0 = 0, kColS1 = 128, kColO = 256;
+// TMEM columns: S_0, S_1 (scores, later P in their first 64 columns), O_0, O_1 (accumulators)
+__host__ __device__ constexpr uint32_t col_s(int x) { return static_cast<uint32_t>(x) * 128u; }
+__host__ __device__ constexpr uint32_t col_o(int x) { return 256u + static_cast<uint32_t>(x) * 128u; }
 constexpr float kRescaleLog2 = 8.f;  // rescale O only when the running max grows by more than 2^8
 
-constexpr uint32_t OFF_Q = 0;
-constexpr uint32_t OFF_K = OFF_Q + TILE_BYTES;
+constexpr uint32_t OFF_Q = 0;                         // Q_0, Q_1
+constexpr uint32_t OFF_K = OFF_Q + 2 * TILE_BYTES;
 constexpr uint32_t OFF_V = OFF_K + NK * TILE_BYTES;
 constexpr uint32_t OFF_BAR = OFF_V + NV * TILE_BYTES;
 constexpr uint32_t OFF_MISC = OFF_BAR + 256;
 constexpr uint32_t OFF_TILES = OFF_MISC + 64;
 constexpr uint32_t SMEM_USED = OFF_TILES + MAX_TILES * 16;
 constexpr uint32_t SMEM_BYTES = SMEM_USED + 1024;  // slack to align the base to 1024 bytes
+static_assert(SMEM_BYTES <= 232448, "shared memory budget of one CTA");
 
 constexpr uint32_t IDESC_QK = idesc_bf16_f32(128, 128, false, false);  // Q, K both K-major
 constexpr uint32_t IDESC_PV = idesc_bf16_f32(128, 128, false, true);   // P K-major, V MN-major
@@ -75,7 +84,7 @@ struct Tile {
     int row0;   // first source row (TMA row coordinate)
     int pbase;  // absolute position of column 0
     int chi;    // last valid column (columns past it belong to another tile or to nothing)
-    int src;    // 0 = this call's k/v rows, 1 = rolling cache
+    int flags;  // bit 0: source (0 = this call's k/v rows, 1 = rolling cache); bit 1 + x: needed by query tile x
 };
 
 struct Params {
@@ -100,7 +109,7 @@ __host__ __device__ int build_tiles(Tile *tl, int q0, int q1, int pos0, int s, i
                 tl[n].row0 = p - rowbase;
                 tl[n].pbase = p;
                 tl[n].chi = (pb - p < BN - 1) ? pb - p : BN - 1;
-                tl[n].src = src;
+                tl[n].flags = src;
             }
             ++n;
         }
@@ -132,6 +141,21 @@ __host__ __device__ int build_tiles(Tile *tl, int q0, int q1, int pos0, int s, i
     const int ca = blo > pos0 ? blo : pos0;
     if (q1 >= ca) add_range(0, ca, q1, pos0);
     return n;
+}
+
+// Which query tiles of the pair [q0, qlast] need each key tile: rows [ra, rb] need a tile holding
+// positions [pb, pb + chi] iff some position p <= rb in it is a sink (p < s) or lies in the window of
+// some row (p >= ra - m + 1).
+__host__ __device__ void mark_tiles(Tile *tl, int n, int q0, int qlast, int s, int m) {
+    for (int i = 0; i < n && i < MAX_TILES; ++i) {
+        const int pb = tl[i].pbase, pe = tl[i].pbase + tl[i].chi;
+        for (int x = 0; x < 2; ++x) {
+            const int ra = q0 + x * BH_ROWS;
+            const int rb = (q0 + x * BH_ROWS + BH_ROWS - 1 < qlast) ? q0 + x * BH_ROWS + BH_ROWS - 1 : qlast;
+            if (ra > rb) continue;
+            if (pb <= rb && (pb < s || pe >= ra - m + 1)) tl[i].flags |= 2 << x;
+        }
+    }
 }
 
 __device__ __forceinline__ float ex2(float x) {
@@ -177,12 +201,9 @@ __global__ void __launch_bounds__(kThreads, 1) swa_prefill_tc_kernel(const __gri
     uint64_t *kempty = kfull + NK;   // [NK]
     uint64_t *vfull = kempty + NK;   // [NV]
     uint64_t *vempty = vfull + NV;   // [NV]
-    uint64_t *sfull = vempty + NV;   // [2]
-    // P_j ready, by tile parity: a softmax warp can run one tile ahead of another (S_{j+1} is ready
-    // before every warp has finished tile j), so arrivals for tiles j and j+1 must not share a barrier.
-    uint64_t *pfull = sfull + 2;     // [2]
-    uint64_t *pvdone = pfull + 2;
-    uint64_t *ofull = pvdone + 1;
+    uint64_t *sfull = vempty + NV;   // [2]: S_X = Q_X K_j^T ready, one per query tile X
+    uint64_t *pfull = sfull + 2;     // [2]: P_X ready in TMEM (128 arrivals)
+    uint64_t *ofull = pfull + 2;     // all PV products done
     uint64_t *drain = ofull + 1;
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(sm + OFF_MISC);
     volatile int *abort_flag = reinterpret_cast<volatile int *>(sm + OFF_MISC + 4);
@@ -190,15 +211,17 @@ __global__ void __launch_bounds__(kThreads, 1) swa_prefill_tc_kernel(const __gri
     Tile *tiles = reinterpret_cast<Tile *>(sm + OFF_TILES);
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int qtile = P.n_qtiles - 1 - static_cast<int>(blockIdx.x);  // full-window tiles first
+    const int qpair = P.n_qtiles - 1 - static_cast<int>(blockIdx.x);  // full-window tiles first
     const int bh = blockIdx.y;
-    const int row_start = qtile * BM;  // first row of this call's rows
-    const int q0 = P.pos0 + row_start;
-    const int q1 = P.pos0 + min(row_start + BM, P.L) - 1;
+    const int row_start = qpair * BM;             // first row (of this call's rows) of query tile 0
+    const int q0 = P.pos0 + row_start;            // absolute position of that row
+    const int qlast = P.pos0 + min(row_start + BM, P.L) - 1;  // last real row of the pair
 
     if (threadIdx.x == 0) {
         *abort_flag = 0;
-        *ntiles_s = build_tiles(tiles, q0, q1, P.pos0, P.s, P.m, P.w);
+        const int n = build_tiles(tiles, q0, qlast, P.pos0, P.s, P.m, P.w);
+        mark_tiles(tiles, n, q0, qlast, P.s, P.m);
+        *ntiles_s = n;
         mbar_init(qfull, 1);
         for (int i = 0; i < NK; ++i) {
             mbar_init(&kfull[i], 1);
@@ -208,11 +231,10 @@ __global__ void __launch_bounds__(kThreads, 1) swa_prefill_tc_kernel(const __gri
             mbar_init(&vfull[i], 1);
             mbar_init(&vempty[i], 1);
         }
-        mbar_init(&sfull[0], 1);
-        mbar_init(&sfull[1], 1);
-        mbar_init(&pfull[0], BM);
-        mbar_init(&pfull[1], BM);
-        mbar_init(pvdone, 1);
+        for (int x = 0; x < 2; ++x) {
+            mbar_init(&sfull[x], 1);
+            mbar_init(&pfull[x], BH_ROWS);
+        }
         mbar_init(ofull, 1);
         mbar_init(drain, 1);
         mbar_init_fence();
@@ -225,23 +247,25 @@ __global__ void __launch_bounds__(kThreads, 1) swa_prefill_tc_kernel(const __gri
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem = *tmem_slot;
-    const int nt = *ntiles_s;
+    const int nt = min(*ntiles_s, MAX_TILES + 1);
     const bool ok = nt >= 1 && nt <= MAX_TILES;
     if (!ok && threadIdx.x == 0) atomicOr(P.status, kDevBadArg);
     const WaitCtl wc{abort_flag, P.status, P.info, P.timeout_ns};
 
-    if (warp == 4) {
+    if (warp == kWarpTma) {
         // ------------------------------------------------------------------ TMA producer
-        // K tiles run up to NK tiles ahead of the V tiles: a K slot frees as soon as its QK product is
-        // done, a V slot only after its PV product.
+        // K tiles run up to NK tiles ahead of the V tiles: a K slot frees as soon as the QK products
+        // that read it are done, a V slot only after its PV products.
         if (lane == 0 && ok) {
             tma_prefetch_desc(&P.tm_q);
             tma_prefetch_desc(&P.tm_k);
             tma_prefetch_desc(&P.tm_v);
             uint8_t *qs = sm + OFF_Q;
-            mbar_arrive_expect_tx(qfull, TILE_BYTES);
-            tma_load_3d(qs, &P.tm_q, qfull, 0, row_start, bh);
-            tma_load_3d(qs + HALF_BYTES, &P.tm_q, qfull, 64, row_start, bh);
+            mbar_arrive_expect_tx(qfull, 2 * TILE_BYTES);
+            for (int x = 0; x < 2; ++x) {
+                tma_load_3d(qs + x * TILE_BYTES, &P.tm_q, qfull, 0, row_start + x * BH_ROWS, bh);
+                tma_load_3d(qs + x * TILE_BYTES + HALF_BYTES, &P.tm_q, qfull, 64, row_start + x * BH_ROWS, bh);
+            }
             int jk = 0, jv = 0;
             bool fine = true;
             while (fine && jv < nt) {
@@ -249,7 +273,7 @@ __global__ void __launch_bounds__(kThreads, 1) swa_prefill_tc_kernel(const __gri
                     const int st = jk % NK;
                     if (!mbar_wait(&kempty[st], ((jk / NK) & 1) ^ 1, wc, 1, jk)) { fine = false; break; }
                     const Tile T = tiles[jk];
-                    const CUtensorMap *mk = T.src ? &P.tm_kc : &P.tm_k;
+                    const CUtensorMap *mk = (T.flags & 1) ? &P.tm_kc : &P.tm_k;
                     uint8_t *ks = sm + OFF_K + st * TILE_BYTES;
                     mbar_arrive_expect_tx(&kfull[st], TILE_BYTES);
                     tma_load_3d(ks, mk, &kfull[st], 0, T.row0, bh);
@@ -260,7 +284,7 @@ __global__ void __launch_bounds__(kThreads, 1) swa_prefill_tc_kernel(const __gri
                 const int sv = jv % NV;
                 if (!mbar_wait(&vempty[sv], ((jv / NV) & 1) ^ 1, wc, 9, jv)) break;
                 const Tile T = tiles[jv];
-                const CUtensorMap *mv = T.src ? &P.tm_vc : &P.tm_v;
+                const CUtensorMap *mv = (T.flags & 1) ? &P.tm_vc : &P.tm_v;
                 uint8_t *vs = sm + OFF_V + sv * TILE_BYTES;
                 mbar_arrive_expect_tx(&vfull[sv], TILE_BYTES);
                 tma_load_3d(vs, mv, &vfull[sv], 0, T.row0, bh);
@@ -273,36 +297,57 @@ __global__ void __launch_bounds__(kThreads, 1) swa_prefill_tc_kernel(const __gri
                 for (int j = (jv > NV ? jv - NV : 0); j < jv; ++j) mbar_wait_drain(&vfull[j % NV], (j / NV) & 1);
             }
         }
-    } else if (warp == 5) {
+    } else if (warp == kWarpMma) {
         // ------------------------------------------------------------------ MMA issuer
+        // Per key tile j: PV_0(j), QK_0(j+1), PV_1(j), QK_1(j+1).  While the tensor cores work on one
+        // query tile, the softmax warpgroup of the other one turns its S into P.
         if (lane == 0 && ok) {
             const uint32_t q_addr = smem_u32(sm + OFF_Q);
             const uint32_t k_addr0 = smem_u32(sm + OFF_K), v_addr0 = smem_u32(sm + OFF_V);
             bool issued_any = false, fine = true;
-            if (!mbar_wait(qfull, 0, wc, 2) || !mbar_wait(&kfull[0], 0, wc, 3)) fine = false;
+            int cnt[2] = {0, 0};  // PV products issued per query tile
+            if (!mbar_wait(qfull, 0, wc, 2) || !mbar_wait(&kfull[0], 0, wc, 3, 0)) fine = false;
             if (fine) {
                 tc_fence_after();
-                issue_qk(tmem + kColS0, q_addr, k_addr0);
-                umma_commit(&sfull[0]);
+                const int f = tiles[0].flags;
+                for (int x = 0; x < 2; ++x) {
+                    if (f & (2 << x)) {
+                        issue_qk(tmem + col_s(x), q_addr + x * TILE_BYTES, k_addr0);
+                        umma_commit(&sfull[x]);
+                    }
+                }
                 umma_commit(&kempty[0]);
                 issued_any = true;
             }
             for (int j = 0; fine && j < nt; ++j) {
-                if (j + 1 < nt) {  // S_{j+1} = Q K_{j+1}^T while the softmax threads work on S_j
-                    const int sk = (j + 1) % NK;
-                    if (!mbar_wait(&kfull[sk], ((j + 1) / NK) & 1, wc, 3, j + 1)) { fine = false; break; }
-                    tc_fence_after();
-                    issue_qk(tmem + (((j + 1) & 1) ? kColS1 : kColS0), q_addr, k_addr0 + sk * TILE_BYTES);
-                    umma_commit(&sfull[(j + 1) & 1]);
-                    umma_commit(&kempty[sk]);
+                const int fj = tiles[j].flags;
+                const int fn = (j + 1 < nt) ? tiles[j + 1].flags : 0;
+                const int sv = j % NV, sk = (j + 1) % NK;
+                bool v_ready = false, k_ready = (j + 1 >= nt);
+                for (int x = 0; x < 2 && fine; ++x) {
+                    if (fj & (2 << x)) {
+                        if (!mbar_wait(&pfull[x], cnt[x] & 1, wc, 4, j)) { fine = false; break; }
+                        if (!v_ready) {
+                            if (!mbar_wait(&vfull[sv], (j / NV) & 1, wc, 5, j)) { fine = false; break; }
+                            v_ready = true;
+                        }
+                        tc_fence_after();
+                        issue_pv(tmem + col_o(x), tmem + col_s(x), v_addr0 + sv * TILE_BYTES, cnt[x] > 0);
+                        ++cnt[x];
+                    }
+                    if (fn & (2 << x)) {  // S_x is free again once PV_x(j) has been issued
+                        if (!k_ready) {
+                            if (!mbar_wait(&kfull[sk], ((j + 1) / NK) & 1, wc, 3, j + 1)) { fine = false; break; }
+                            k_ready = true;
+                        }
+                        tc_fence_after();
+                        issue_qk(tmem + col_s(x), q_addr + x * TILE_BYTES, k_addr0 + sk * TILE_BYTES);
+                        umma_commit(&sfull[x]);
+                    }
                 }
-                const int sv = j % NV;
-                if (!mbar_wait(&pfull[j & 1], (j >> 1) & 1, wc, 4, j)) { fine = false; break; }
-                if (!mbar_wait(&vfull[sv], (j / NV) & 1, wc, 5, j)) { fine = false; break; }
-                tc_fence_after();
-                issue_pv(tmem + kColO, tmem + ((j & 1) ? kColS1 : kColS0), v_addr0 + sv * TILE_BYTES, j > 0);
-                umma_commit(pvdone);
+                if (!fine) break;
                 umma_commit(&vempty[sv]);
+                if (j + 1 < nt) umma_commit(&kempty[sk]);
             }
             if (fine) umma_commit(ofull);
             if (issued_any) {  // no MMA may still be running when TMEM is freed
@@ -312,46 +357,50 @@ __global__ void __launch_bounds__(kThreads, 1) swa_prefill_tc_kernel(const __gri
         }
     } else if (ok) {
         // ------------------------------------------------------------------ softmax + epilogue
-        const int r = threadIdx.x;  // query row within the tile == TMEM lane
-        const int t = q0 + r;       // its absolute position
-        const uint32_t lane_base = static_cast<uint32_t>(warp * 32) << 16;
+        const int x = warp >> 2;                    // query tile of this warpgroup
+        const int r = threadIdx.x & (BH_ROWS - 1);  // its row == TMEM lane
+        const int t = q0 + x * BH_ROWS + r;         // absolute position
+        const uint32_t lane_base = static_cast<uint32_t>((warp & 3) * 32) << 16;
+        const uint32_t s_addr = tmem + lane_base + col_s(x);
+        const uint32_t o_addr = tmem + lane_base + col_o(x);
         const float sl2 = P.scale_log2;
+        const int bit = 2 << x;
         float mrun = -INFINITY, lrun = 0.f;  // running max (log2 units) and sum
         bool fine = true;
+        int cnt = 0;
         for (int j = 0; j < nt; ++j) {
-            const int b = j & 1;
-            const uint32_t s_addr = tmem + lane_base + (b ? kColS1 : kColS0);
-            fine = __all_sync(0xFFFFFFFFu, mbar_wait(&sfull[b], (j >> 1) & 1, wc, 6, j));
+            const Tile T = tiles[j];
+            if (!(T.flags & bit)) continue;
+            fine = __all_sync(0xFFFFFFFFu, mbar_wait(&sfull[x], cnt & 1, wc, 6, j));
             if (!fine) break;
             tc_fence_after();
-            float x[BN];
-            __syncwarp();
-            tmem_ld32(s_addr + 0, *reinterpret_cast<float(*)[32]>(&x[0]));
-            tmem_ld32(s_addr + 32, *reinterpret_cast<float(*)[32]>(&x[32]));
-            tmem_ld32(s_addr + 64, *reinterpret_cast<float(*)[32]>(&x[64]));
-            tmem_ld32(s_addr + 96, *reinterpret_cast<float(*)[32]>(&x[96]));
-            const Tile T = tiles[j];
             // valid columns of this row: [0, b1] (sinks) and [a2, hc] (window), hc = last causal column
             const int hc = min(T.chi, t - T.pbase);
             const int b1 = min(hc, P.s - 1 - T.pbase);
             const int a2 = max(0, t - P.m + 1 - T.pbase);
             const bool full = (b1 >= BN - 1) || (hc >= BN - 1 && (a2 <= 0 || b1 >= a2 - 1));
-            float mx0 = -INFINITY, mx1 = -INFINITY;
-            if (full) {
+            // pass 1: the row maximum over all 128 scores (two 64-column loads)
+            float mx8[8];
 #pragma unroll
-                for (int c = 0; c < BN; c += 2) {
-                    mx0 = fmaxf(mx0, x[c]);
-                    mx1 = fmaxf(mx1, x[c + 1]);
-                }
-            } else {
+            for (int i = 0; i < 8; ++i) mx8[i] = -INFINITY;
 #pragma unroll
-                for (int c = 0; c < BN; ++c) {
-                    const bool valid = (c <= b1) || (c >= a2 && c <= hc);
-                    x[c] = valid ? x[c] : -INFINITY;
-                    if (c & 1) mx1 = fmaxf(mx1, x[c]); else mx0 = fmaxf(mx0, x[c]);
+            for (int hh = 0; hh < 2; ++hh) {
+                float sv[64];
+                __syncwarp();
+                tmem_ld64(s_addr + 64 * hh, sv);
+                if (!full) {
+#pragma unroll
+                    for (int i = 0; i < 64; ++i) {
+                        const int c = 64 * hh + i;
+                        const bool valid = (c <= b1) || (c >= a2 && c <= hc);
+                        sv[i] = valid ? sv[i] : -INFINITY;
+                    }
                 }
+#pragma unroll
+                for (int i = 0; i < 64; ++i) mx8[i & 7] = fmaxf(mx8[i & 7], sv[i]);
             }
-            const float mx = fmaxf(mx0, mx1) * sl2;  // the scale is positive: max commutes with it
+            const float mx = fmaxf(fmaxf(fmaxf(mx8[0], mx8[1]), fmaxf(mx8[2], mx8[3])),
+                                   fmaxf(fmaxf(mx8[4], mx8[5]), fmaxf(mx8[6], mx8[7]))) * sl2;
             float alpha = 1.f;
             bool resc = false;
             const float mnew = fmaxf(mrun, mx);
@@ -362,53 +411,64 @@ __global__ void __launch_bounds__(kThreads, 1) swa_prefill_tc_kernel(const __gri
                 }
                 mrun = mnew;
             }
-            const float nmu = (mrun == -INFINITY) ? 0.f : -mrun;
-            uint32_t pk[BN / 2];
-            float rs0 = 0.f, rs1 = 0.f;
-#pragma unroll
-            for (int i = 0; i < BN / 2; ++i) {
-                const float p0 = ex2(fmaf(x[2 * i], sl2, nmu)), p1 = ex2(fmaf(x[2 * i + 1], sl2, nmu));
-                rs0 += p0;
-                rs1 += p1;
-                pk[i] = pack_bf16x2(p0, p1);
-            }
-            lrun = lrun * alpha + (rs0 + rs1);
-            if (__any_sync(0xFFFFFFFFu, resc)) {  // O (up to PV_{j-1}) must be final before it is rescaled
-                if (j > 0) {
-                    fine = __all_sync(0xFFFFFFFFu, mbar_wait(pvdone, (j - 1) & 1, wc, 7, j));
-                    if (!fine) break;
-                    tc_fence_after();
-                }
+            if (__any_sync(0xFFFFFFFFu, resc)) {
+                // O_x holds the PV products of the earlier tiles; they are complete, because S_x (issued
+                // after the last of them) is, and tcgen05 MMAs of one thread complete in order.
                 __syncwarp();
 #pragma unroll 1
                 for (int c = 0; c < HD; c += 32) {
                     float ov[32];
-                    tmem_ld32(tmem + lane_base + kColO + c, ov);
+                    tmem_ld32(o_addr + c, ov);
 #pragma unroll
                     for (int i = 0; i < 32; ++i) ov[i] *= alpha;
-                    tmem_st32(tmem + lane_base + kColO + c, ov);
+                    tmem_st32(o_addr + c, ov);
                 }
             }
-            // P_j (bf16) over the first 64 columns of its S buffer: the A operand of PV_j.  The last reader
-            // of those columns, PV_{j-2}, completed before QK_j (tcgen05 MMAs of a thread run in order).
-            __syncwarp();
-            tmem_st32u(s_addr + 0, *reinterpret_cast<uint32_t(*)[32]>(&pk[0]));
-            tmem_st32u(s_addr + 32, *reinterpret_cast<uint32_t(*)[32]>(&pk[32]));
+            // pass 2: p = 2^(scale*log2(e)*s - m) per 32-column chunk; chunk q's bf16 pairs go to columns
+            // [16q, 16q + 16) of S_x (columns already read), the A operand of PV_x
+            const float nmu = (mrun == -INFINITY) ? 0.f : -mrun;
+            float rs8[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+            for (int q = 0; q < BN / 32; ++q) {
+                float sv[32];
+                __syncwarp();
+                tmem_ld32(s_addr + 32 * q, sv);
+                if (!full) {
+#pragma unroll
+                    for (int i = 0; i < 32; ++i) {
+                        const int c = 32 * q + i;
+                        const bool valid = (c <= b1) || (c >= a2 && c <= hc);
+                        sv[i] = valid ? sv[i] : -INFINITY;
+                    }
+                }
+                uint32_t pk[16];
+#pragma unroll
+                for (int i = 0; i < 16; ++i) {
+                    const float p0 = ex2(fmaf(sv[2 * i], sl2, nmu)), p1 = ex2(fmaf(sv[2 * i + 1], sl2, nmu));
+                    rs8[(2 * i) & 7] += p0;
+                    rs8[(2 * i + 1) & 7] += p1;
+                    pk[i] = pack_bf16x2(p0, p1);
+                }
+                tmem_st16u_nowait(s_addr + 16 * q, pk);
+            }
+            tmem_wait_st();
+            lrun = lrun * alpha + (((rs8[0] + rs8[1]) + (rs8[2] + rs8[3])) + ((rs8[4] + rs8[5]) + (rs8[6] + rs8[7])));
             tc_fence_before();
-            mbar_arrive(&pfull[b]);
+            mbar_arrive(&pfull[x]);
+            ++cnt;
         }
-        if (fine) fine = __all_sync(0xFFFFFFFFu, mbar_wait(ofull, 0, wc, 8, nt));
-        if (fine) {
+        if (fine && cnt > 0) fine = __all_sync(0xFFFFFFFFu, mbar_wait(ofull, 0, wc, 8, nt));
+        if (fine && cnt > 0) {
             tc_fence_after();
             const float inv = (lrun > 0.f) ? 1.f / lrun : 0.f;
-            const bool store = (t <= q1);
+            const bool store = (t <= qlast);
             __nv_bfloat16 *orow = static_cast<__nv_bfloat16 *>(P.o) +
-                                  (static_cast<int64_t>(bh) * P.seq_stride + row_start + r) * HD;
+                                  (static_cast<int64_t>(bh) * P.seq_stride + row_start + x * BH_ROWS + r) * HD;
             __syncwarp();
 #pragma unroll 1
             for (int c = 0; c < HD; c += 32) {
                 float ov[32];
-                tmem_ld32(tmem + lane_base + kColO + c, ov);
+                tmem_ld32(o_addr + c, ov);
                 if (store) {
                     uint4 *dst = reinterpret_cast<uint4 *>(orow + c);
 #pragma unroll
@@ -423,7 +483,7 @@ __global__ void __launch_bounds__(kThreads, 1) swa_prefill_tc_kernel(const __gri
                 }
             }
             if (store && P.lse)
-                P.lse[static_cast<int64_t>(bh) * P.seq_stride + row_start + r] =
+                P.lse[static_cast<int64_t>(bh) * P.seq_stride + row_start + x * BH_ROWS + r] =
                     (mrun + log2f(lrun)) * 0.69314718055994531f;
         }
     }
@@ -566,7 +626,7 @@ static bool encode_rows_map(CUtensorMap *m, const void *base, uint64_t rows, uin
 // ring wrap).
 static int max_tiles_bound(int w, int s) {
     const int m = w - s;
-    return (s + tc::BN - 1) / tc::BN + 1 + (m + 2 * tc::BN - 2) / tc::BN + 3;
+    return (s + tc::BN - 1) / tc::BN + 1 + (m + tc::BM - 1 + tc::BN - 1) / tc::BN + 3;
 }
 
 int launch_prefill_bf16_tc(const PrefillArgs &a) {
@@ -620,11 +680,13 @@ int launch_prefill_bf16_tc(const PrefillArgs &a) {
 int prefill_tile_plan(int q0, int q1, int pos0, int w, int s, int *out, int max_tiles) {
     tc::Tile tl[tc::MAX_TILES];
     const int n = tc::build_tiles(tl, q0, q1, pos0, s, w - s, w);
+    tc::mark_tiles(tl, n, q0, q1, s, w - s);
     for (int i = 0; i < n && i < max_tiles && i < tc::MAX_TILES; ++i) {
-        out[4 * i + 0] = tl[i].src;
-        out[4 * i + 1] = tl[i].row0;
-        out[4 * i + 2] = tl[i].pbase;
-        out[4 * i + 3] = tl[i].chi;
+        out[5 * i + 0] = tl[i].flags & 1;
+        out[5 * i + 1] = tl[i].row0;
+        out[5 * i + 2] = tl[i].pbase;
+        out[5 * i + 3] = tl[i].chi;
+        out[5 * i + 4] = tl[i].flags >> 1;
     }
     return n;
 }

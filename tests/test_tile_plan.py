@@ -14,17 +14,18 @@ import pytest
 import oracle
 import sliding_window_softmax_swa_gb300 as swa
 
-BN = 128
+BN = 128   # keys per tile and rows per query tile
+BM = 256   # query rows per CTA (two query tiles)
 
 
 def check_plan(q0, q1, pos0, w, s, L):
     plan = swa.prefill_tile_plan(q0, q1, pos0, w, s)
     holder = oracle.cache_replay(w, s, pos0) if pos0 > 0 else None
-    seen = {}  # position -> count, over columns the kernel keeps for at least one row
-    cols = []
-    for src, row0, pbase, chi in plan:
+    cols, users = [], []
+    for src, row0, pbase, chi, used in plan:
         assert 0 <= chi < BN
         assert row0 >= 0
+        assert used != 0, "a tile no query tile needs"
         for c in range(chi + 1):
             p = pbase + c
             row = row0 + c
@@ -36,10 +37,14 @@ def check_plan(q0, q1, pos0, w, s, L):
                 assert p >= pos0 and row == p - pos0
                 assert row < L or p > q1
             cols.append(p)
+            users.append(used)
     cols = np.array(cols, dtype=np.int64)
+    users = np.array(users, dtype=np.int64)
     allpos = np.arange(q1 + 1, dtype=np.int64)
     for t in range(q0, q1 + 1):
-        got = np.sort(cols[oracle.is_key_many(t, cols, w, s)])
+        x = (t - q0) // BN  # the query tile of row t
+        mine = cols[(users >> x) & 1 == 1]
+        got = np.sort(mine[oracle.is_key_many(t, mine, w, s)])
         want = allpos[oracle.is_key_many(t, allpos, w, s)]
         assert np.array_equal(got, want), (q0, q1, pos0, w, s, t)
     return plan
@@ -49,9 +54,9 @@ def check_plan(q0, q1, pos0, w, s, L):
                                  (300, 200), (256, 130), (17, 16)])
 def test_whole_sequence_tiles(w, s):
     L = 3000
-    for qt in range(0, (L + BN - 1) // BN):
-        q0 = qt * BN
-        q1 = min(q0 + BN, L) - 1
+    for qt in range(0, (L + BM - 1) // BM):
+        q0 = qt * BM
+        q1 = min(q0 + BM, L) - 1
         check_plan(q0, q1, 0, w, s, L)
 
 
@@ -63,9 +68,9 @@ def test_chunked_tiles_random():
         pos0 = rng.choice([1, 2, s, s + 1, w - 1, w, w + 1, 3 * w + 7, rng.randrange(1, 5 * w + 10)])
         pos0 = max(1, pos0)
         L = rng.randrange(1, 700)
-        qt = rng.randrange(0, (L + BN - 1) // BN)
-        q0 = pos0 + qt * BN
-        q1 = pos0 + min(qt * BN + BN, L) - 1
+        qt = rng.randrange(0, (L + BM - 1) // BM)
+        q0 = pos0 + qt * BM
+        q1 = pos0 + min(qt * BM + BM, L) - 1
         check_plan(q0, q1, pos0, w, s, L)
 
 
@@ -73,15 +78,19 @@ def test_chunked_tiles_long_window_boundaries():
     # the chunk shapes of a 131072-token prompt in 4096-token chunks with w = 4096, s = 4
     w, s, C = 4096, 4, 4096
     for pos0 in (C, 2 * C, 7 * C, 31 * C):
-        for qt in (0, 1, 15, 16, 31):
-            q0 = pos0 + qt * BN
-            plan = check_plan(q0, q0 + BN - 1, pos0, w, s, C)
-            assert len(plan) <= 36
+        for qt in (0, 1, 7, 8, 15):
+            q0 = pos0 + qt * BM
+            plan = check_plan(q0, q0 + BM - 1, pos0, w, s, C)
+            assert len(plan) <= 38
 
 
 def test_tile_count_is_minimal_for_full_windows():
-    # a full-window query tile walks ceil((m + 127) / 128) band tiles plus one sink tile
+    # a full-window pair of query tiles walks ceil((m + 255) / 128) band tiles plus one sink tile, and each
+    # query tile uses only the ceil((m + 127) / 128) band tiles its own rows reach (plus the sink tile)
     for w, s in [(1024, 4), (4096, 4), (4096, 0)]:
         m = w - s
-        plan = swa.prefill_tile_plan(8192, 8192 + 127, 0, w, s)
-        assert len(plan) == (m + 127 + BN - 1) // BN + (1 if s else 0)
+        plan = swa.prefill_tile_plan(8192, 8192 + BM - 1, 0, w, s)
+        assert len(plan) == (m + 255 + BN - 1) // BN + (1 if s else 0)
+        for x in (0, 1):
+            used = sum(1 for tl in plan if (tl[4] >> x) & 1)
+            assert used == (m + 127 + BN - 1) // BN + (1 if s else 0)
