@@ -88,7 +88,7 @@ struct Tile {
 };
 
 struct Params {
-    CUtensorMap tm_q, tm_k, tm_v, tm_kc, tm_vc;
+    CUtensorMap tm_q, tm_k, tm_v, tm_kc, tm_vc, tm_o;
     void *o;
     float *lse;
     unsigned *status;
@@ -158,6 +158,14 @@ __host__ __device__ void mark_tiles(Tile *tl, int n, int q0, int qlast, int s, i
     }
 }
 
+// Bits [lo, hi] of a 32-bit word (clipped to [0, 31]; 0 when the range is empty).
+__device__ __forceinline__ uint32_t range_bits(int lo, int hi) {
+    lo = lo < 0 ? 0 : lo;
+    hi = hi > 31 ? 31 : hi;
+    if (hi < lo) return 0u;
+    return (0xFFFFFFFFu >> (31 - hi)) & (0xFFFFFFFFu << lo);
+}
+
 __device__ __forceinline__ float ex2(float x) {
     float y;
     asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
@@ -205,6 +213,7 @@ __global__ void __launch_bounds__(kThreads, 1) swa_prefill_tc_kernel(const __gri
     uint64_t *pfull = sfull + 2;     // [2]: P_X ready in TMEM (128 arrivals)
     uint64_t *ofull = pfull + 2;     // all PV products done
     uint64_t *drain = ofull + 1;
+    uint64_t *ostaged = drain + 1;   // [2]: O_x rows staged in shared memory (128 arrivals)
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(sm + OFF_MISC);
     volatile int *abort_flag = reinterpret_cast<volatile int *>(sm + OFF_MISC + 4);
     int *ntiles_s = reinterpret_cast<int *>(sm + OFF_MISC + 8);
@@ -237,6 +246,8 @@ __global__ void __launch_bounds__(kThreads, 1) swa_prefill_tc_kernel(const __gri
         }
         mbar_init(ofull, 1);
         mbar_init(drain, 1);
+        mbar_init(&ostaged[0], BH_ROWS);
+        mbar_init(&ostaged[1], BH_ROWS);
         mbar_init_fence();
     }
     if (warp == 0) {
@@ -374,11 +385,17 @@ __global__ void __launch_bounds__(kThreads, 1) swa_prefill_tc_kernel(const __gri
             fine = __all_sync(0xFFFFFFFFu, mbar_wait(&sfull[x], cnt & 1, wc, 6, j));
             if (!fine) break;
             tc_fence_after();
-            // valid columns of this row: [0, b1] (sinks) and [a2, hc] (window), hc = last causal column
+            // valid columns of this row: [0, b1] (sinks) and [a2, hc] (window), hc = last causal column,
+            // as four 32-bit column masks; interior tiles need none
             const int hc = min(T.chi, t - T.pbase);
             const int b1 = min(hc, P.s - 1 - T.pbase);
             const int a2 = max(0, t - P.m + 1 - T.pbase);
             const bool full = (b1 >= BN - 1) || (hc >= BN - 1 && (a2 <= 0 || b1 >= a2 - 1));
+            const bool any_masked = __any_sync(0xFFFFFFFFu, !full);  // warp-uniform: no divergent paths
+            uint32_t mw[4];
+#pragma unroll
+            for (int k = 0; k < 4; ++k)
+                mw[k] = full ? 0xFFFFFFFFu : (range_bits(-32 * k, b1 - 32 * k) | range_bits(a2 - 32 * k, hc - 32 * k));
             // pass 1: the row maximum over all 128 scores (two 64-column loads)
             float mx8[8];
 #pragma unroll
@@ -388,12 +405,11 @@ __global__ void __launch_bounds__(kThreads, 1) swa_prefill_tc_kernel(const __gri
                 float sv[64];
                 __syncwarp();
                 tmem_ld64(s_addr + 64 * hh, sv);
-                if (!full) {
+                if (any_masked) {
 #pragma unroll
                     for (int i = 0; i < 64; ++i) {
                         const int c = 64 * hh + i;
-                        const bool valid = (c <= b1) || (c >= a2 && c <= hc);
-                        sv[i] = valid ? sv[i] : -INFINITY;
+                        sv[i] = (mw[c >> 5] & (1u << (c & 31))) ? sv[i] : -INFINITY;
                     }
                 }
 #pragma unroll
@@ -433,13 +449,9 @@ __global__ void __launch_bounds__(kThreads, 1) swa_prefill_tc_kernel(const __gri
                 float sv[32];
                 __syncwarp();
                 tmem_ld32(s_addr + 32 * q, sv);
-                if (!full) {
+                if (any_masked) {
 #pragma unroll
-                    for (int i = 0; i < 32; ++i) {
-                        const int c = 32 * q + i;
-                        const bool valid = (c <= b1) || (c >= a2 && c <= hc);
-                        sv[i] = valid ? sv[i] : -INFINITY;
-                    }
+                    for (int i = 0; i < 32; ++i) sv[i] = (mw[q] & (1u << i)) ? sv[i] : -INFINITY;
                 }
                 uint32_t pk[16];
 #pragma unroll
@@ -459,32 +471,38 @@ __global__ void __launch_bounds__(kThreads, 1) swa_prefill_tc_kernel(const __gri
         }
         if (fine && cnt > 0) fine = __all_sync(0xFFFFFFFFu, mbar_wait(ofull, 0, wc, 8, nt));
         if (fine && cnt > 0) {
+            // epilogue: O_x / l -> bf16, staged in the (now idle) Q_x buffer with the 128-byte swizzle,
+            // then written by two TMA stores (rows past the end of the sequence are clipped by TMA)
             tc_fence_after();
             const float inv = (lrun > 0.f) ? 1.f / lrun : 0.f;
-            const bool store = (t <= qlast);
-            __nv_bfloat16 *orow = static_cast<__nv_bfloat16 *>(P.o) +
-                                  (static_cast<int64_t>(bh) * P.seq_stride + row_start + x * BH_ROWS + r) * HD;
+            uint8_t *ost = sm + OFF_Q + x * TILE_BYTES;
+            const uint32_t obase = smem_u32(ost);
             __syncwarp();
 #pragma unroll 1
             for (int c = 0; c < HD; c += 32) {
                 float ov[32];
                 tmem_ld32(o_addr + c, ov);
-                if (store) {
-                    uint4 *dst = reinterpret_cast<uint4 *>(orow + c);
 #pragma unroll
-                    for (int i = 0; i < 4; ++i) {
-                        uint4 u;
-                        u.x = pack_bf16x2(ov[8 * i + 0] * inv, ov[8 * i + 1] * inv);
-                        u.y = pack_bf16x2(ov[8 * i + 2] * inv, ov[8 * i + 3] * inv);
-                        u.z = pack_bf16x2(ov[8 * i + 4] * inv, ov[8 * i + 5] * inv);
-                        u.w = pack_bf16x2(ov[8 * i + 6] * inv, ov[8 * i + 7] * inv);
-                        dst[i] = u;
-                    }
+                for (int i = 0; i < 4; ++i) {
+                    const int col = (c & 63) + 8 * i;  // column within the 64-column half
+                    st_shared_v4(obase + (c >> 6) * HALF_BYTES + sw128_offset(r, col),
+                                 pack_bf16x2(ov[8 * i + 0] * inv, ov[8 * i + 1] * inv),
+                                 pack_bf16x2(ov[8 * i + 2] * inv, ov[8 * i + 3] * inv),
+                                 pack_bf16x2(ov[8 * i + 4] * inv, ov[8 * i + 5] * inv),
+                                 pack_bf16x2(ov[8 * i + 6] * inv, ov[8 * i + 7] * inv));
                 }
             }
-            if (store && P.lse)
+            fence_proxy_async_smem();
+            mbar_arrive(&ostaged[x]);
+            if (t <= qlast && P.lse)
                 P.lse[static_cast<int64_t>(bh) * P.seq_stride + row_start + x * BH_ROWS + r] =
                     (mrun + log2f(lrun)) * 0.69314718055994531f;
+            if (r == 0 && mbar_wait(&ostaged[x], 0, wc, 10, x)) {
+                tma_store_3d(&P.tm_o, ost, 0, row_start + x * BH_ROWS, bh);
+                tma_store_3d(&P.tm_o, ost + HALF_BYTES, 64, row_start + x * BH_ROWS, bh);
+                bulk_commit_group();
+                bulk_wait_group_read0();
+            }
         }
     }
 
@@ -642,7 +660,7 @@ int launch_prefill_bf16_tc(const PrefillArgs &a) {
     memset(&p, 0, sizeof(p));
     const uint64_t L = static_cast<uint64_t>(a.L), st = static_cast<uint64_t>(a.seq_stride);
     bool okm = encode_rows_map(&p.tm_q, a.q, L, a.BH, st) && encode_rows_map(&p.tm_k, a.k, L, a.BH, st) &&
-               encode_rows_map(&p.tm_v, a.v, L, a.BH, st);
+               encode_rows_map(&p.tm_v, a.v, L, a.BH, st) && encode_rows_map(&p.tm_o, a.o, L, a.BH, st);
     if (a.pos0 > 0) {
         // Only slots 0..min(pos0, w)-1 have been written; the map stops there so that TMA zero-fills the
         // rest of a tile instead of loading stale bytes (a masked column still multiplies its V row by 0,
