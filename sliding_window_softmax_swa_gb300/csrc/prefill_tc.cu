@@ -337,9 +337,9 @@ __global__ void __launch_bounds__(kThreads, 1) swa_prefill_tc_kernel(const __gri
                 bool v_ready = false, k_ready = (j + 1 >= nt);
                 for (int x = 0; x < 2 && fine; ++x) {
                     if (fj & (2 << x)) {
-                        if (!mbar_wait_spin(&pfull[x], cnt[x] & 1, wc, 4, j)) { fine = false; break; }
+                        if (!mbar_wait(&pfull[x], cnt[x] & 1, wc, 4, j)) { fine = false; break; }
                         if (!v_ready) {
-                            if (!mbar_wait_spin(&vfull[sv], (j / NV) & 1, wc, 5, j)) { fine = false; break; }
+                            if (!mbar_wait(&vfull[sv], (j / NV) & 1, wc, 5, j)) { fine = false; break; }
                             v_ready = true;
                         }
                         tc_fence_after();
@@ -348,7 +348,7 @@ __global__ void __launch_bounds__(kThreads, 1) swa_prefill_tc_kernel(const __gri
                     }
                     if (fn & (2 << x)) {  // S_x is free again once PV_x(j) has been issued
                         if (!k_ready) {
-                            if (!mbar_wait_spin(&kfull[sk], ((j + 1) / NK) & 1, wc, 3, j + 1)) { fine = false; break; }
+                            if (!mbar_wait(&kfull[sk], ((j + 1) / NK) & 1, wc, 3, j + 1)) { fine = false; break; }
                             k_ready = true;
                         }
                         tc_fence_after();
@@ -406,12 +406,18 @@ __global__ void __launch_bounds__(kThreads, 1) swa_prefill_tc_kernel(const __gri
             float rs8[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
             auto process = [&](uint32_t (&cur)[32], const int q) {
                 float sv[32];
-                float cm = -INFINITY;
+                if (any_masked) {
 #pragma unroll
-                for (int i = 0; i < 32; ++i) {
-                    sv[i] = (!any_masked || (mw[q] & (1u << i))) ? __uint_as_float(cur[i]) : -INFINITY;
-                    cm = fmaxf(cm, sv[i]);
+                    for (int i = 0; i < 32; ++i) sv[i] = (mw[q] & (1u << i)) ? __uint_as_float(cur[i]) : -INFINITY;
+                } else {
+#pragma unroll
+                    for (int i = 0; i < 32; ++i) sv[i] = __uint_as_float(cur[i]);
                 }
+                float m8[8];
+#pragma unroll
+                for (int i = 0; i < 8; ++i) m8[i] = fmaxf(fmaxf(sv[i], sv[i + 8]), fmaxf(sv[i + 16], sv[i + 24]));
+                const float cm = fmaxf(fmaxf(fmaxf(m8[0], m8[1]), fmaxf(m8[2], m8[3])),
+                                       fmaxf(fmaxf(m8[4], m8[5]), fmaxf(m8[6], m8[7])));
                 const float cmx = cm * sl2;
                 const bool ovf = cmx > mrun + kRescaleLog2;  // also when mrun is still -inf
                 if (__any_sync(0xFFFFFFFFu, ovf)) {
