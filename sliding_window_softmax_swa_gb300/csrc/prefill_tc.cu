@@ -396,68 +396,63 @@ __global__ void __launch_bounds__(kThreads, 1) swa_prefill_tc_kernel(const __gri
 #pragma unroll
             for (int k = 0; k < 4; ++k)
                 mw[k] = full ? 0xFFFFFFFFu : (range_bits(-32 * k, b1 - 32 * k) | range_bits(a2 - 32 * k, hc - 32 * k));
-            // One pass over S_x in four 32-column chunks (the next chunk's TMEM load in flight while the
-            // current one is processed): p = 2^(scale*log2(e)*s - mrun) with the running max mrun.  While
-            // every score stays below mrun + 8 this is exact and p <= 256.  A chunk whose maximum exceeds
-            // that bound raises mrun to it; what was accumulated with the old reference (O_x, l, the sums
-            // of this tile, and the P chunks of this tile already in TMEM) is multiplied by
-            // 2^(old - new) first, so O_x and l always share one reference.  Chunk q's bf16 pairs go to
-            // columns [16q, 16q + 16) of S_x (columns already read), the A operand of PV_x.
-            float rs8[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
-            auto process = [&](uint32_t (&cur)[32], const int q) {
-                float sv[32];
+            // pass 1: the row maximum over all 128 scores (two 64-column loads)
+            float mx8[8];
+#pragma unroll
+            for (int i = 0; i < 8; ++i) mx8[i] = -INFINITY;
+#pragma unroll
+            for (int hh = 0; hh < 2; ++hh) {
+                float sv[64];
+                __syncwarp();
+                tmem_ld64(s_addr + 64 * hh, sv);
                 if (any_masked) {
 #pragma unroll
-                    for (int i = 0; i < 32; ++i) sv[i] = (mw[q] & (1u << i)) ? __uint_as_float(cur[i]) : -INFINITY;
-                } else {
-#pragma unroll
-                    for (int i = 0; i < 32; ++i) sv[i] = __uint_as_float(cur[i]);
-                }
-                float m8[8];
-#pragma unroll
-                for (int i = 0; i < 8; ++i) m8[i] = fmaxf(fmaxf(sv[i], sv[i + 8]), fmaxf(sv[i + 16], sv[i + 24]));
-                const float cm = fmaxf(fmaxf(fmaxf(m8[0], m8[1]), fmaxf(m8[2], m8[3])),
-                                       fmaxf(fmaxf(m8[4], m8[5]), fmaxf(m8[6], m8[7])));
-                const float cmx = cm * sl2;
-                const bool ovf = cmx > mrun + kRescaleLog2;  // also when mrun is still -inf
-                if (__any_sync(0xFFFFFFFFu, ovf)) {
-                    float alpha = 1.f;
-                    if (ovf) {
-                        alpha = (mrun == -INFINITY) ? 0.f : ex2(mrun - cmx);
-                        mrun = cmx;
-                    }
-                    lrun *= alpha;
-#pragma unroll
-                    for (int i = 0; i < 8; ++i) rs8[i] *= alpha;
-                    __syncwarp();
-                    if (cnt > 0) {
-                        // O_x holds the PV products of the earlier tiles; they are complete, because
-                        // S_x (issued after the last of them) is, and tcgen05 MMAs of one thread
-                        // complete in order.
-#pragma unroll 1
-                        for (int c = 0; c < HD; c += 32) {
-                            float ov[32];
-                            tmem_ld32(o_addr + c, ov);
-#pragma unroll
-                            for (int i = 0; i < 32; ++i) ov[i] *= alpha;
-                            tmem_st32(o_addr + c, ov);
-                        }
-                    }
-                    if (q > 0) {
-                        tmem_wait_st();
-#pragma unroll 1
-                        for (int k = 0; k < q; ++k) {
-                            uint32_t u[16];
-                            tmem_ld16u(s_addr + 16 * k, u);
-#pragma unroll
-                            for (int i = 0; i < 16; ++i)
-                                u[i] = pack_bf16x2(__uint_as_float(u[i] << 16) * alpha,
-                                                   __uint_as_float(u[i] & 0xFFFF0000u) * alpha);
-                            tmem_st16u_nowait(s_addr + 16 * k, u);
-                        }
+                    for (int i = 0; i < 64; ++i) {
+                        const int c = 64 * hh + i;
+                        sv[i] = (mw[c >> 5] & (1u << (c & 31))) ? sv[i] : -INFINITY;
                     }
                 }
-                const float nmu = (mrun == -INFINITY) ? 0.f : -mrun;
+#pragma unroll
+                for (int i = 0; i < 64; ++i) mx8[i & 7] = fmaxf(mx8[i & 7], sv[i]);
+            }
+            const float mx = fmaxf(fmaxf(fmaxf(mx8[0], mx8[1]), fmaxf(mx8[2], mx8[3])),
+                                   fmaxf(fmaxf(mx8[4], mx8[5]), fmaxf(mx8[6], mx8[7]))) * sl2;
+            float alpha = 1.f;
+            bool resc = false;
+            const float mnew = fmaxf(mrun, mx);
+            if (mnew > mrun + kRescaleLog2) {  // also taken when mrun is still -inf
+                if (mrun != -INFINITY) {
+                    alpha = ex2(mrun - mnew);
+                    resc = true;
+                }
+                mrun = mnew;
+            }
+            if (__any_sync(0xFFFFFFFFu, resc)) {
+                // O_x holds the PV products of the earlier tiles; they are complete, because S_x (issued
+                // after the last of them) is, and tcgen05 MMAs of one thread complete in order.
+                __syncwarp();
+#pragma unroll 1
+                for (int c = 0; c < HD; c += 32) {
+                    float ov[32];
+                    tmem_ld32(o_addr + c, ov);
+#pragma unroll
+                    for (int i = 0; i < 32; ++i) ov[i] *= alpha;
+                    tmem_st32(o_addr + c, ov);
+                }
+            }
+            // pass 2: p = 2^(scale*log2(e)*s - m) per 32-column chunk; chunk q's bf16 pairs go to columns
+            // [16q, 16q + 16) of S_x (columns already read), the A operand of PV_x
+            const float nmu = (mrun == -INFINITY) ? 0.f : -mrun;
+            float rs8[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+            for (int q = 0; q < BN / 32; ++q) {
+                float sv[32];
+                __syncwarp();
+                tmem_ld32(s_addr + 32 * q, sv);
+                if (any_masked) {
+#pragma unroll
+                    for (int i = 0; i < 32; ++i) sv[i] = (mw[q] & (1u << i)) ? sv[i] : -INFINITY;
+                }
                 uint32_t pk[16];
 #pragma unroll
                 for (int i = 0; i < 16; ++i) {
@@ -467,25 +462,9 @@ __global__ void __launch_bounds__(kThreads, 1) swa_prefill_tc_kernel(const __gri
                     pk[i] = pack_bf16x2(p0, p1);
                 }
                 tmem_st16u_nowait(s_addr + 16 * q, pk);
-            };
-            {
-                uint32_t ra[32], rb[32];
-                __syncwarp();
-                tmem_ld32_nowait(s_addr + 0, ra);
-                tmem_wait_ld_regs(ra);
-                tmem_ld32_nowait(s_addr + 32, rb);
-                process(ra, 0);
-                tmem_wait_ld_regs(rb);
-                tmem_ld32_nowait(s_addr + 64, ra);
-                process(rb, 1);
-                tmem_wait_ld_regs(ra);
-                tmem_ld32_nowait(s_addr + 96, rb);
-                process(ra, 2);
-                tmem_wait_ld_regs(rb);
-                process(rb, 3);
             }
             tmem_wait_st();
-            lrun += ((rs8[0] + rs8[1]) + (rs8[2] + rs8[3])) + ((rs8[4] + rs8[5]) + (rs8[6] + rs8[7]));
+            lrun = lrun * alpha + (((rs8[0] + rs8[1]) + (rs8[2] + rs8[3])) + ((rs8[4] + rs8[5]) + (rs8[6] + rs8[7])));
             tc_fence_before();
             mbar_arrive(&pfull[x]);
             ++cnt;
