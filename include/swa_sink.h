@@ -119,6 +119,27 @@ int swa_sink_decode_step(const void *q, const void *k_cache, const void *v_cache
                          float *lse, int B, int H, int d, int w, int s, int64_t t, float scale,
                          void *workspace, size_t workspace_bytes, int dtype, void *stream);
 
+/*
+ * swa_sink_decode_step_noalloc -- the same decode step as swa_sink_decode_step, for callers that cannot
+ * allocate device memory when they run it (an engine's plugin callback that must not allocate while it
+ * enqueues work, a server whose memory pool owns all device memory, a token loop that cannot afford the
+ * device synchronisation an allocation may cause).  It takes no workspace: the split-K partial results go
+ * to a fixed array of 2 MiB built into the library, which every GPU that loads the library keeps until the
+ * process exits.  The pages have no counterpart of this entry point; it is an interface convenience.
+ *
+ *   Arguments are those of swa_sink_decode_step without workspace/workspace_bytes; same layouts, same
+ *   results.  A shape whose split-K scratch (swa_sink_decode_workspace_size) exceeds 2 MiB is refused with
+ *   SWA_ERR_UNSUPPORTED and a message; nothing is launched.
+ *   The first call on a device looks up the array's device address (cudaGetSymbolAddress) with that
+ *   device current; make that first call before any stream capture.
+ *   Every call uses the same array and overwrites what the previous call left there (nothing in it needs
+ *   to start at zero).  Calls that run at the same time on the GPU -- on different streams, or from
+ *   several host threads -- overwrite each other's partials: serialise them.
+ */
+int swa_sink_decode_step_noalloc(const void *q, const void *k_cache, const void *v_cache, void *o,
+                                 float *lse, int B, int H, int d, int w, int s, int64_t t, float scale,
+                                 int dtype, void *stream);
+
 /* Bytes of workspace swa_sink_decode_step needs for this shape (host-only, no CUDA call). */
 size_t swa_sink_decode_workspace_size(int B, int H, int d, int w);
 

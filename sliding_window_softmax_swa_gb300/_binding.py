@@ -28,6 +28,7 @@ SIGNATURES = {
                                       _vp]),
     "kv_rolling_write": (_i, [_vp, _vp, _vp, _vp, _i, _i, _i, _i, _i, _i64, _i64, _i, _vp]),
     "swa_sink_decode_step": (_i, [_vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _i, _i64, _f, _vp, _sz, _i, _vp]),
+    "swa_sink_decode_step_noalloc": (_i, [_vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _i, _i64, _f, _i, _vp]),
     "swa_sink_decode_workspace_size": (_sz, [_i, _i, _i, _i]),
     "swa_last_error_string": (ctypes.c_char_p, []),
     "swa_device_status": (_i, [_vp]),

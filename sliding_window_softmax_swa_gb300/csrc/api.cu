@@ -267,3 +267,21 @@ extern "C" int swa_prefill_tile_plan(int64_t q0, int64_t q1, int64_t pos0, int w
     return prefill_tile_plan(static_cast<int>(q0), static_cast<int>(q1), static_cast<int>(pos0), w, s, tiles,
                              max_tiles);
 }
+
+extern "C" int swa_sink_decode_step_noalloc(const void *q, const void *k_cache, const void *v_cache, void *o,
+                                            float *lse, int B, int H, int d, int w, int s, int64_t t, float scale,
+                                            int dtype, void *stream) {
+    t_err[0] = 0;
+    int rc = check_common(B, H, d, w, s, dtype);
+    if (rc) return rc;
+    if (t < 0 || t >= (int64_t(1) << 62)) return fail(SWA_ERR_INVALID, "t=%lld out of range", (long long)t);
+    if (!(scale == scale) || scale <= 0.f || scale > 1e30f)
+        return fail(SWA_ERR_INVALID, "scale must be a positive finite number");
+    if (!q || !k_cache || !v_cache || !o) return fail(SWA_ERR_INVALID, "q, caches and o must be non-null");
+    if (!aligned16(q) || !aligned16(k_cache) || !aligned16(v_cache) || !aligned16(o))
+        return fail(SWA_ERR_INVALID, "q, caches and o must be 16-byte aligned");
+    if (lse && (reinterpret_cast<uintptr_t>(lse) & 3u)) return fail(SWA_ERR_INVALID, "lse must be 4-byte aligned");
+    DecodeArgs a{q, k_cache, v_cache, o, lse, B * H, d, w, s, t, scale, nullptr, 0,
+                 esize_of(dtype), static_cast<cudaStream_t>(stream)};
+    return launch_decode_noalloc(a);
+}

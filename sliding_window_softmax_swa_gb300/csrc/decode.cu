@@ -20,6 +20,8 @@
 // Scores are kept in log2 units (x = scale * log2(e) * q.k) so exp is a single exp2.
 #include <math.h>
 
+#include <mutex>
+
 #include "../../include/swa_sink.h"
 #include "swa_device.cuh"
 #include "swa_internal.h"
@@ -239,6 +241,66 @@ int launch_decode(const DecodeArgs &a) {
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return fail(SWA_ERR_CUDA, "decode launch: %s", cudaGetErrorString(e));
     return SWA_OK;
+}
+
+}  // namespace swa
+
+// ------------------------------------------------------------------------------------------------
+// Decode without a caller-provided workspace.
+//
+// Some callers cannot allocate device memory at the moment they run a decode step: an inference
+// engine's plugin or custom-op callback is often forbidden to allocate while it enqueues work, a server
+// whose device memory is handed out up front by its own pool allocator has nothing to give to a
+// library, and cudaMalloc may synchronise the device, which a latency-bound token loop cannot afford.
+// For them the split-K partial results go to this fixed, file-scope array instead.  Every GPU that
+// loads the library keeps it (kNoAllocScratchBytes) until the process exits.
+//
+// Every call shares the one array.  A call writes every partial it later reads, so nothing has to be
+// cleared between calls, but two calls that run at the same time on the GPU (on different streams, or
+// on the same device from several threads) overwrite each other's partials: serialise them.
+namespace swa {
+
+constexpr size_t kNoAllocScratchBytes = size_t(2) << 20;  // 2 MiB
+static __device__ __align__(256) unsigned char g_decode_scratch[kNoAllocScratchBytes];
+
+// Device address of g_decode_scratch on the current device.  In host code the array's name is only a
+// host-side stand-in, so the address is looked up once per device (with that device current) and kept.
+static void *decode_scratch_address() {
+    static std::mutex mu;
+    static void *ptrs[64] = {nullptr};
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess || dev < 0 || dev >= 64) {
+        fail(SWA_ERR_CUDA, "cudaGetDevice: %s", cudaGetErrorString(e));
+        return nullptr;
+    }
+    std::lock_guard<std::mutex> lk(mu);
+    if (!ptrs[dev]) {
+        void *p = nullptr;
+        e = cudaGetSymbolAddress(&p, g_decode_scratch);
+        if (e != cudaSuccess || !p) {
+            fail(SWA_ERR_CUDA, "cudaGetSymbolAddress(decode scratch): %s", cudaGetErrorString(e));
+            return nullptr;
+        }
+        ptrs[dev] = p;
+    }
+    return ptrs[dev];
+}
+
+size_t decode_noalloc_scratch_bytes() { return kNoAllocScratchBytes; }
+
+int launch_decode_noalloc(DecodeArgs a) {
+    const size_t need = decode_workspace_bytes(a.BH, a.d, a.w);
+    if (need > kNoAllocScratchBytes)
+        return fail(SWA_ERR_UNSUPPORTED,
+                    "this shape needs %zu bytes of split-K scratch, more than the %zu bytes of the built-in array; "
+                    "use swa_sink_decode_step with a workspace",
+                    need, kNoAllocScratchBytes);
+    void *scratch = decode_scratch_address();
+    if (!scratch) return SWA_ERR_CUDA;
+    a.workspace = scratch;
+    a.workspace_bytes = kNoAllocScratchBytes;
+    return launch_decode(a);
 }
 
 }  // namespace swa

@@ -59,6 +59,9 @@ struct DecodeArgs {
 int decode_num_splits(int BH, int nvalid);
 size_t decode_workspace_bytes(int BH, int d, int w);
 int launch_decode(const DecodeArgs &a);
+// The same decode with its split-K scratch in a built-in device array (no workspace argument).
+size_t decode_noalloc_scratch_bytes();
+int launch_decode_noalloc(DecodeArgs a);
 
 int prefill_tile_plan(int q0, int q1, int pos0, int w, int s, int *out, int max_tiles);
 int launch_selftest_wait_timeout(uint64_t timeout_ns, cudaStream_t stream);
