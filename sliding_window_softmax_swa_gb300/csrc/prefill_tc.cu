@@ -366,7 +366,7 @@ __global__ void __launch_bounds__(kThreads, 1) swa_prefill_tc_kernel(const __gri
                 mbar_wait_drain(drain, 0);
             }
         }
-    } else if (ok) {
+    } else if (warp < 8 && ok) {
         // ------------------------------------------------------------------ softmax + epilogue
         const int x = warp >> 2;                    // query tile of this warpgroup
         const int r = threadIdx.x & (BH_ROWS - 1);  // its row == TMEM lane
@@ -396,25 +396,19 @@ __global__ void __launch_bounds__(kThreads, 1) swa_prefill_tc_kernel(const __gri
 #pragma unroll
             for (int k = 0; k < 4; ++k)
                 mw[k] = full ? 0xFFFFFFFFu : (range_bits(-32 * k, b1 - 32 * k) | range_bits(a2 - 32 * k, hc - 32 * k));
-            // pass 1: the row maximum over all 128 scores (two 64-column loads)
+            // the whole row of S_x in registers (one TMEM load)
+            float sv[BN];
+            __syncwarp();
+            tmem_ld128(s_addr, sv);
+            if (any_masked) {
+#pragma unroll
+                for (int c = 0; c < BN; ++c) sv[c] = (mw[c >> 5] & (1u << (c & 31))) ? sv[c] : -INFINITY;
+            }
             float mx8[8];
 #pragma unroll
-            for (int i = 0; i < 8; ++i) mx8[i] = -INFINITY;
+            for (int i = 0; i < 8; ++i) mx8[i] = sv[i];
 #pragma unroll
-            for (int hh = 0; hh < 2; ++hh) {
-                float sv[64];
-                __syncwarp();
-                tmem_ld64(s_addr + 64 * hh, sv);
-                if (any_masked) {
-#pragma unroll
-                    for (int i = 0; i < 64; ++i) {
-                        const int c = 64 * hh + i;
-                        sv[i] = (mw[c >> 5] & (1u << (c & 31))) ? sv[i] : -INFINITY;
-                    }
-                }
-#pragma unroll
-                for (int i = 0; i < 64; ++i) mx8[i & 7] = fmaxf(mx8[i & 7], sv[i]);
-            }
+            for (int c = 8; c < BN; ++c) mx8[c & 7] = fmaxf(mx8[c & 7], sv[c]);
             const float mx = fmaxf(fmaxf(fmaxf(mx8[0], mx8[1]), fmaxf(mx8[2], mx8[3])),
                                    fmaxf(fmaxf(mx8[4], mx8[5]), fmaxf(mx8[6], mx8[7]))) * sl2;
             float alpha = 1.f;
@@ -440,28 +434,23 @@ __global__ void __launch_bounds__(kThreads, 1) swa_prefill_tc_kernel(const __gri
                     tmem_st32(o_addr + c, ov);
                 }
             }
-            // pass 2: p = 2^(scale*log2(e)*s - m) per 32-column chunk; chunk q's bf16 pairs go to columns
-            // [16q, 16q + 16) of S_x (columns already read), the A operand of PV_x
+            // p = 2^(scale*log2(e)*s - m); bf16 pairs of keys 0..63 / 64..127 go to columns [0, 32) /
+            // [32, 64) of S_x (already read): the A operand of PV_x
             const float nmu = (mrun == -INFINITY) ? 0.f : -mrun;
             float rs8[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
 #pragma unroll
-            for (int q = 0; q < BN / 32; ++q) {
-                float sv[32];
-                __syncwarp();
-                tmem_ld32(s_addr + 32 * q, sv);
-                if (any_masked) {
+            for (int h = 0; h < 2; ++h) {
+                uint32_t pk[32];
 #pragma unroll
-                    for (int i = 0; i < 32; ++i) sv[i] = (mw[q] & (1u << i)) ? sv[i] : -INFINITY;
-                }
-                uint32_t pk[16];
-#pragma unroll
-                for (int i = 0; i < 16; ++i) {
-                    const float p0 = ex2(fmaf(sv[2 * i], sl2, nmu)), p1 = ex2(fmaf(sv[2 * i + 1], sl2, nmu));
+                for (int i = 0; i < 32; ++i) {
+                    const int c = 64 * h + 2 * i;
+                    const float p0 = ex2(fmaf(sv[c], sl2, nmu)), p1 = ex2(fmaf(sv[c + 1], sl2, nmu));
                     rs8[(2 * i) & 7] += p0;
                     rs8[(2 * i + 1) & 7] += p1;
                     pk[i] = pack_bf16x2(p0, p1);
                 }
-                tmem_st16u_nowait(s_addr + 16 * q, pk);
+                __syncwarp();
+                tmem_st32u_nowait(s_addr + 32 * h, pk);
             }
             tmem_wait_st();
             lrun = lrun * alpha + (((rs8[0] + rs8[1]) + (rs8[2] + rs8[3])) + ((rs8[4] + rs8[5]) + (rs8[6] + rs8[7])));
