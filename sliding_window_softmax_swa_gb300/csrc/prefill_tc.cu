@@ -8,18 +8,24 @@
 // O(n^2) -> O(n k), banded patterns are hardware friendly), so each CTA walks only the key tiles that
 // intersect the band or the sink block of its query tile; no skipped tile is ever loaded.
 //
-// CTA = two query tiles of 128 rows (256 consecutive rows) of one (b, h); 320 threads in four roles:
+// Work item = two query tiles of 128 rows (256 consecutive rows) of one (b, h).  The kernel is
+// persistent: one CTA per SM walks the items blockIdx.x, blockIdx.x + gridDim.x, ..., ordered
+// longest-first (the last query pairs of every head, whose windows are full, come first).  320 threads
+// in four roles:
 //   warps 0-3 / 4-7  softmax + epilogue of query tile 0 / 1: thread r owns row r of its tile
 //              (= TMEM lane r);
-//   warp 8     TMA producer: Q_0 and Q_1 once, then K tiles into a 3-stage ring and V tiles into a
-//              2-stage ring (128 rows x 128 bf16 each, two 64-column boxes with the 128-byte swizzle).
-//              A K slot frees as soon as the QK products that read it complete, a V slot after its PV
-//              products, so K loads run up to three tiles ahead;
+//   warp 8     TMA producer: per item the key-tile list (double-buffered), Q_0 and Q_1 (as soon as the
+//              previous item's last QK product is done), then K tiles into a 3-stage ring and V tiles
+//              into a 2-stage ring (128 rows x 128 bf16 each, two 64-column boxes with the 128-byte
+//              swizzle).  A K slot frees as soon as the QK products that read it complete, a V slot after
+//              its PV products, so K loads run up to three tiles ahead;
 //   warp 9     MMA issuer (one thread).  Per key tile j: PV_0(j), QK_0(j+1), PV_1(j), QK_1(j+1), where
 //              QK_x(j) is S_x = Q_x K_j^T and PV_x(j) is O_x += P_x V_j with P_x (bf16) read by the MMA
 //              straight from tensor memory.  While the tensor cores work on one query tile, the softmax
 //              warpgroup of the other turns its S into P (ping-pong), and each K/V tile loaded from L2
-//              serves 256 query rows.
+//              serves 256 query rows.  The next item's first QK products follow the current item's last
+//              PV products, so they overlap its epilogue; the next item's first PV_x waits until the
+//              epilogue has read O_x.
 // TMEM (512 columns): S_0, S_1 = [0,128), [128,256); O_0, O_1 = [256,384), [384,512) (fp32, lane = row).
 // The softmax threads overwrite the first 64 columns of S_x with P_x (two bf16 per column) after
 // reading them.  The online softmax keeps a running max in log2 units and only rescales O (TMEM load,
@@ -58,7 +64,7 @@ constexpr int NK = 3;                      // K tile stages (a slot frees after 
 constexpr int NV = 2;                      // V tile stages (a slot frees after its PV products)
 constexpr uint32_t HALF_BYTES = 128 * 128;  // one 64-column half of a 128-row bf16 tile (16 KB)
 constexpr uint32_t TILE_BYTES = 2 * HALF_BYTES;
-constexpr int MAX_TILES = 96;
+constexpr int MAX_TILES = 64;
 constexpr int kThreads = 320;              // warps 0-3 / 4-7: softmax of query tile 0 / 1; 8: TMA; 9: MMA
 constexpr int kWarpTma = 8, kWarpMma = 9;
 constexpr uint32_t kTmemCols = 512;
@@ -73,7 +79,7 @@ constexpr uint32_t OFF_V = OFF_K + NK * TILE_BYTES;
 constexpr uint32_t OFF_BAR = OFF_V + NV * TILE_BYTES;
 constexpr uint32_t OFF_MISC = OFF_BAR + 256;
 constexpr uint32_t OFF_TILES = OFF_MISC + 64;
-constexpr uint32_t SMEM_USED = OFF_TILES + MAX_TILES * 16;
+constexpr uint32_t SMEM_USED = OFF_TILES + 2 * MAX_TILES * 12;  // two tile lists (current / next item)
 constexpr uint32_t SMEM_BYTES = SMEM_USED + 1024;  // slack to align the base to 1024 bytes
 static_assert(SMEM_BYTES <= 232448, "shared memory budget of one CTA");
 
@@ -81,20 +87,22 @@ constexpr uint32_t IDESC_QK = idesc_bf16_f32(128, 128, false, false);  // Q, K b
 constexpr uint32_t IDESC_PV = idesc_bf16_f32(128, 128, false, true);   // P K-major, V MN-major
 
 struct Tile {
-    int row0;   // first source row (TMA row coordinate)
-    int pbase;  // absolute position of column 0
-    int chi;    // last valid column (columns past it belong to another tile or to nothing)
-    int flags;  // bit 0: source (0 = this call's k/v rows, 1 = rolling cache); bit 1 + x: needed by query tile x
+    int row0;     // first source row (TMA row coordinate)
+    int pbase;    // absolute position of column 0
+    short chi;    // last valid column (columns past it belong to another tile or to nothing)
+    short flags;  // bit 0: source (0 = this call's k/v rows, 1 = rolling cache); bit 1 + x: needed by query tile x
 };
+static_assert(sizeof(Tile) == 12, "tile record");
 
 struct Params {
-    CUtensorMap tm_q, tm_k, tm_v, tm_kc, tm_vc, tm_o;
+    CUtensorMap tm_q, tm_k, tm_v, tm_kc, tm_vc;
     void *o;
     float *lse;
     unsigned *status;
     unsigned long long *info;
     int64_t seq_stride;  // rows between (b, h) blocks of q/k/v/o/lse
-    int L, pos0, w, s, m, n_qtiles;
+    int L, pos0, w, s, m, BH;
+    int n_qpairs, n_items;  // 256-row query pairs per (b, h); work items = n_qpairs * BH
     float scale_log2;
     uint64_t timeout_ns;
 };
@@ -108,8 +116,8 @@ __host__ __device__ int build_tiles(Tile *tl, int q0, int q1, int pos0, int s, i
             if (n < MAX_TILES) {
                 tl[n].row0 = p - rowbase;
                 tl[n].pbase = p;
-                tl[n].chi = (pb - p < BN - 1) ? pb - p : BN - 1;
-                tl[n].flags = src;
+                tl[n].chi = static_cast<short>((pb - p < BN - 1) ? pb - p : BN - 1);
+                tl[n].flags = static_cast<short>(src);
             }
             ++n;
         }
@@ -153,7 +161,7 @@ __host__ __device__ void mark_tiles(Tile *tl, int n, int q0, int qlast, int s, i
             const int ra = q0 + x * BH_ROWS;
             const int rb = (q0 + x * BH_ROWS + BH_ROWS - 1 < qlast) ? q0 + x * BH_ROWS + BH_ROWS - 1 : qlast;
             if (ra > rb) continue;
-            if (pb <= rb && (pb < s || pe >= ra - m + 1)) tl[i].flags |= 2 << x;
+            if (pb <= rb && (pb < s || pe >= ra - m + 1)) tl[i].flags = static_cast<short>(tl[i].flags | (2 << x));
         }
     }
 }
@@ -204,34 +212,31 @@ __global__ void __launch_bounds__(kThreads, 1) swa_prefill_tc_kernel(const __gri
     extern __shared__ uint8_t smem_raw[];
     uint8_t *sm = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     uint64_t *bars = reinterpret_cast<uint64_t *>(sm + OFF_BAR);
-    uint64_t *qfull = bars;
-    uint64_t *kfull = qfull + 1;     // [NK]
-    uint64_t *kempty = kfull + NK;   // [NK]
-    uint64_t *vfull = kempty + NK;   // [NV]
-    uint64_t *vempty = vfull + NV;   // [NV]
-    uint64_t *sfull = vempty + NV;   // [2]: S_X = Q_X K_j^T ready, one per query tile X
-    uint64_t *pfull = sfull + 2;     // [2]: P_X ready in TMEM (128 arrivals)
-    uint64_t *ofull = pfull + 2;     // all PV products done
-    uint64_t *drain = ofull + 1;
-    uint64_t *ostaged = drain + 1;   // [2]: O_x rows staged in shared memory (128 arrivals)
+    uint64_t *qfull = bars;           // Q_0, Q_1 of the current item landed
+    uint64_t *qempty = qfull + 1;     // the last QK product of an item is done: Q may be reloaded
+    uint64_t *kfull = qempty + 1;     // [NK]
+    uint64_t *kempty = kfull + NK;    // [NK]
+    uint64_t *vfull = kempty + NK;    // [NV]
+    uint64_t *vempty = vfull + NV;    // [NV]
+    uint64_t *sfull = vempty + NV;    // [2]: S_x = Q_x K_j^T ready, one per query tile x
+    uint64_t *pfull = sfull + 2;      // [2]: P_x ready in TMEM (128 arrivals)
+    uint64_t *ofull = pfull + 2;      // [2]: the last PV_x product of an item is done
+    uint64_t *oempty = ofull + 2;     // [2]: O_x has been read by the epilogue (128 arrivals)
+    uint64_t *lready = oempty + 2;    // [2]: tile list buffer b written (1 arrival)
+    uint64_t *lfree = lready + 2;     // [2]: tile list buffer b no longer read (8 softmax warps + MMA)
+    uint64_t *drain = lfree + 2;
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(sm + OFF_MISC);
     volatile int *abort_flag = reinterpret_cast<volatile int *>(sm + OFF_MISC + 4);
-    int *ntiles_s = reinterpret_cast<int *>(sm + OFF_MISC + 8);
-    Tile *tiles = reinterpret_cast<Tile *>(sm + OFF_TILES);
+    int *ntiles_s = reinterpret_cast<int *>(sm + OFF_MISC + 8);  // [2]
+    Tile *tiles_s = reinterpret_cast<Tile *>(sm + OFF_TILES);     // [2][MAX_TILES]
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int qpair = P.n_qtiles - 1 - static_cast<int>(blockIdx.x);  // full-window tiles first
-    const int bh = blockIdx.y;
-    const int row_start = qpair * BM;             // first row (of this call's rows) of query tile 0
-    const int q0 = P.pos0 + row_start;            // absolute position of that row
-    const int qlast = P.pos0 + min(row_start + BM, P.L) - 1;  // last real row of the pair
+    const int G = static_cast<int>(gridDim.x);
 
     if (threadIdx.x == 0) {
         *abort_flag = 0;
-        const int n = build_tiles(tiles, q0, qlast, P.pos0, P.s, P.m, P.w);
-        mark_tiles(tiles, n, q0, qlast, P.s, P.m);
-        *ntiles_s = n;
         mbar_init(qfull, 1);
+        mbar_init(qempty, 1);
         for (int i = 0; i < NK; ++i) {
             mbar_init(&kfull[i], 1);
             mbar_init(&kempty[i], 1);
@@ -243,11 +248,12 @@ __global__ void __launch_bounds__(kThreads, 1) swa_prefill_tc_kernel(const __gri
         for (int x = 0; x < 2; ++x) {
             mbar_init(&sfull[x], 1);
             mbar_init(&pfull[x], BH_ROWS);
+            mbar_init(&ofull[x], 1);
+            mbar_init(&oempty[x], BH_ROWS);
+            mbar_init(&lready[x], 1);
+            mbar_init(&lfree[x], 9);
         }
-        mbar_init(ofull, 1);
         mbar_init(drain, 1);
-        mbar_init(&ostaged[0], BH_ROWS);
-        mbar_init(&ostaged[1], BH_ROWS);
         mbar_init_fence();
     }
     if (warp == 0) {
@@ -258,239 +264,304 @@ __global__ void __launch_bounds__(kThreads, 1) swa_prefill_tc_kernel(const __gri
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem = *tmem_slot;
-    const int nt = min(*ntiles_s, MAX_TILES + 1);
-    const bool ok = nt >= 1 && nt <= MAX_TILES;
-    if (!ok && threadIdx.x == 0) atomicOr(P.status, kDevBadArg);
     const WaitCtl wc{abort_flag, P.status, P.info, P.timeout_ns};
 
     if (warp == kWarpTma) {
         // ------------------------------------------------------------------ TMA producer
-        // K tiles run up to NK tiles ahead of the V tiles: a K slot frees as soon as the QK products
-        // that read it are done, a V slot only after its PV products.
-        if (lane == 0 && ok) {
+        // Per item: the tile list (once its buffer is free), Q_0/Q_1 (once the previous item's last QK
+        // product is done), then the K and V tiles.  K tiles run up to NK tiles ahead of the V tiles: a
+        // K slot frees as soon as the QK products that read it are done, a V slot after its PV products.
+        if (lane == 0) {
             tma_prefetch_desc(&P.tm_q);
             tma_prefetch_desc(&P.tm_k);
             tma_prefetch_desc(&P.tm_v);
-            uint8_t *qs = sm + OFF_Q;
-            mbar_arrive_expect_tx(qfull, 2 * TILE_BYTES);
-            for (int x = 0; x < 2; ++x) {
-                tma_load_3d(qs + x * TILE_BYTES, &P.tm_q, qfull, 0, row_start + x * BH_ROWS, bh);
-                tma_load_3d(qs + x * TILE_BYTES + HALF_BYTES, &P.tm_q, qfull, 64, row_start + x * BH_ROWS, bh);
-            }
-            int jk = 0, jv = 0;
+            int gk = 0, gv = 0, nq = 0;  // K, V tiles and Q pairs issued so far
             bool fine = true;
-            while (fine && jv < nt) {
-                while (jk < nt && jk < jv + NK) {
-                    const int st = jk % NK;
-                    if (!mbar_wait(&kempty[st], ((jk / NK) & 1) ^ 1, wc, 1, jk)) { fine = false; break; }
-                    const Tile T = tiles[jk];
-                    const CUtensorMap *mk = (T.flags & 1) ? &P.tm_kc : &P.tm_k;
-                    uint8_t *ks = sm + OFF_K + st * TILE_BYTES;
-                    mbar_arrive_expect_tx(&kfull[st], TILE_BYTES);
-                    tma_load_3d(ks, mk, &kfull[st], 0, T.row0, bh);
-                    tma_load_3d(ks + HALF_BYTES, mk, &kfull[st], 64, T.row0, bh);
-                    ++jk;
+            for (int it = 0; fine; ++it) {
+                const int item = static_cast<int>(blockIdx.x) + it * G;
+                if (item >= P.n_items) break;
+                const int bh = item % P.BH;
+                const int row_start = (P.n_qpairs - 1 - item / P.BH) * BM;
+                const int q0 = P.pos0 + row_start;
+                const int qlast = P.pos0 + min(row_start + BM, P.L) - 1;
+                const int b = it & 1;
+                if (it >= 2 && !mbar_wait(&lfree[b], ((it - 2) >> 1) & 1, wc, 12, it)) break;
+                Tile *tl = tiles_s + b * MAX_TILES;
+                const int n = build_tiles(tl, q0, qlast, P.pos0, P.s, P.m, P.w);
+                if (n < 1 || n > MAX_TILES) {
+                    atomicOr(P.status, kDevBadArg);
+                    *abort_flag = 1;
+                    break;
                 }
-                if (!fine) break;
-                const int sv = jv % NV;
-                if (!mbar_wait(&vempty[sv], ((jv / NV) & 1) ^ 1, wc, 9, jv)) break;
-                const Tile T = tiles[jv];
-                const CUtensorMap *mv = (T.flags & 1) ? &P.tm_vc : &P.tm_v;
-                uint8_t *vs = sm + OFF_V + sv * TILE_BYTES;
-                mbar_arrive_expect_tx(&vfull[sv], TILE_BYTES);
-                tma_load_3d(vs, mv, &vfull[sv], 0, T.row0, bh);
-                tma_load_3d(vs + HALF_BYTES, mv, &vfull[sv], 64, T.row0, bh);
-                ++jv;
+                mark_tiles(tl, n, q0, qlast, P.s, P.m);
+                ntiles_s[b] = n;
+                mbar_arrive(&lready[b]);  // release: the list is visible to whoever sees the phase complete
+                if (it >= 1 && !mbar_wait(qempty, (it - 1) & 1, wc, 13, it)) break;
+                uint8_t *qs = sm + OFF_Q;
+                mbar_arrive_expect_tx(qfull, 2 * TILE_BYTES);
+                for (int x = 0; x < 2; ++x) {
+                    tma_load_3d(qs + x * TILE_BYTES, &P.tm_q, qfull, 0, row_start + x * BH_ROWS, bh);
+                    tma_load_3d(qs + x * TILE_BYTES + HALF_BYTES, &P.tm_q, qfull, 64, row_start + x * BH_ROWS, bh);
+                }
+                ++nq;
+                int jk = 0, jv = 0;
+                while (fine && jv < n) {
+                    while (jk < n && jk < jv + NK) {
+                        const int st = gk % NK;
+                        if (!mbar_wait(&kempty[st], ((gk / NK) & 1) ^ 1, wc, 1, jk)) { fine = false; break; }
+                        const Tile T = tl[jk];
+                        const CUtensorMap *mk = (T.flags & 1) ? &P.tm_kc : &P.tm_k;
+                        uint8_t *ks = sm + OFF_K + st * TILE_BYTES;
+                        mbar_arrive_expect_tx(&kfull[st], TILE_BYTES);
+                        tma_load_3d(ks, mk, &kfull[st], 0, T.row0, bh);
+                        tma_load_3d(ks + HALF_BYTES, mk, &kfull[st], 64, T.row0, bh);
+                        ++jk;
+                        ++gk;
+                    }
+                    if (!fine) break;
+                    const int sv = gv % NV;
+                    if (!mbar_wait(&vempty[sv], ((gv / NV) & 1) ^ 1, wc, 9, jv)) { fine = false; break; }
+                    const Tile T = tl[jv];
+                    const CUtensorMap *mv = (T.flags & 1) ? &P.tm_vc : &P.tm_v;
+                    uint8_t *vs = sm + OFF_V + sv * TILE_BYTES;
+                    mbar_arrive_expect_tx(&vfull[sv], TILE_BYTES);
+                    tma_load_3d(vs, mv, &vfull[sv], 0, T.row0, bh);
+                    tma_load_3d(vs + HALF_BYTES, mv, &vfull[sv], 64, T.row0, bh);
+                    ++jv;
+                    ++gv;
+                }
             }
             if (*abort_flag) {  // make sure no copy is still landing in shared memory
-                mbar_wait_drain(qfull, 0);
-                for (int j = (jk > NK ? jk - NK : 0); j < jk; ++j) mbar_wait_drain(&kfull[j % NK], (j / NK) & 1);
-                for (int j = (jv > NV ? jv - NV : 0); j < jv; ++j) mbar_wait_drain(&vfull[j % NV], (j / NV) & 1);
+                if (nq > 0) mbar_wait_drain(qfull, (nq - 1) & 1);
+                for (int g = (gk > NK ? gk - NK : 0); g < gk; ++g) mbar_wait_drain(&kfull[g % NK], (g / NK) & 1);
+                for (int g = (gv > NV ? gv - NV : 0); g < gv; ++g) mbar_wait_drain(&vfull[g % NV], (g / NV) & 1);
             }
         }
     } else if (warp == kWarpMma) {
         // ------------------------------------------------------------------ MMA issuer
         // Per key tile j: PV_0(j), QK_0(j+1), PV_1(j), QK_1(j+1).  While the tensor cores work on one
-        // query tile, the softmax warpgroup of the other one turns its S into P.
-        if (lane == 0 && ok) {
+        // query tile, the softmax warpgroup of the other one turns its S into P.  The first QK products
+        // of the next item follow the last PV products of the current one, so they overlap its epilogue.
+        if (lane == 0) {
             const uint32_t q_addr = smem_u32(sm + OFF_Q);
             const uint32_t k_addr0 = smem_u32(sm + OFF_K), v_addr0 = smem_u32(sm + OFF_V);
             bool issued_any = false, fine = true;
-            int cnt[2] = {0, 0};  // PV products issued per query tile
-            if (!mbar_wait(qfull, 0, wc, 2) || !mbar_wait(&kfull[0], 0, wc, 3, 0)) fine = false;
-            if (fine) {
+            int gk = 0, gv = 0;                // K, V tiles consumed
+            int cp[2] = {0, 0};                // PV_x products issued (pfull parity)
+            int ce[2] = {0, 0};                // items in which query tile x had PV products (oempty)
+            for (int it = 0; fine; ++it) {
+                const int item = static_cast<int>(blockIdx.x) + it * G;
+                if (item >= P.n_items) break;
+                const int b = it & 1;
+                if (!mbar_wait(qfull, it & 1, wc, 2, it)) break;  // Q of this item; its tile list is written
+                const Tile *tl = tiles_s + b * MAX_TILES;
+                const int n = ntiles_s[b];
+                int last_used[2] = {-1, -1};
+                for (int j = 0; j < n; ++j)
+                    for (int x = 0; x < 2; ++x)
+                        if (tl[j].flags & (2 << x)) last_used[x] = j;
+                if (!mbar_wait(&kfull[gk % NK], (gk / NK) & 1, wc, 3, 0)) { fine = false; break; }
                 tc_fence_after();
-                const int f = tiles[0].flags;
-                for (int x = 0; x < 2; ++x) {
-                    if (f & (2 << x)) {
-                        issue_qk(tmem + col_s(x), q_addr + x * TILE_BYTES, k_addr0);
-                        umma_commit(&sfull[x]);
+                {
+                    const int f = tl[0].flags;
+                    for (int x = 0; x < 2; ++x) {
+                        if (f & (2 << x)) {
+                            issue_qk(tmem + col_s(x), q_addr + x * TILE_BYTES, k_addr0 + (gk % NK) * TILE_BYTES);
+                            umma_commit(&sfull[x]);
+                        }
                     }
+                    if (n == 1) umma_commit(qempty);
+                    umma_commit(&kempty[gk % NK]);
+                    ++gk;
+                    issued_any = true;
                 }
-                umma_commit(&kempty[0]);
-                issued_any = true;
-            }
-            for (int j = 0; fine && j < nt; ++j) {
-                const int fj = tiles[j].flags;
-                const int fn = (j + 1 < nt) ? tiles[j + 1].flags : 0;
-                const int sv = j % NV, sk = (j + 1) % NK;
-                bool v_ready = false, k_ready = (j + 1 >= nt);
-                for (int x = 0; x < 2 && fine; ++x) {
-                    if (fj & (2 << x)) {
-                        if (!mbar_wait(&pfull[x], cnt[x] & 1, wc, 4, j)) { fine = false; break; }
-                        if (!v_ready) {
-                            if (!mbar_wait(&vfull[sv], (j / NV) & 1, wc, 5, j)) { fine = false; break; }
-                            v_ready = true;
+                bool first_pv[2] = {true, true};
+                for (int j = 0; fine && j < n; ++j) {
+                    const int fj = tl[j].flags;
+                    const int fn = (j + 1 < n) ? tl[j + 1].flags : 0;
+                    const int sv = gv % NV, sk = gk % NK;
+                    bool v_ready = false, k_ready = (j + 1 >= n);
+                    for (int x = 0; x < 2 && fine; ++x) {
+                        if (fj & (2 << x)) {
+                            if (!mbar_wait(&pfull[x], cp[x] & 1, wc, 4, j)) { fine = false; break; }
+                            if (first_pv[x]) {  // O_x must have been read by the previous item's epilogue
+                                if (!mbar_wait(&oempty[x], (ce[x] & 1) ^ 1, wc, 11, j)) { fine = false; break; }
+                                ++ce[x];
+                            }
+                            if (!v_ready) {
+                                if (!mbar_wait(&vfull[sv], (gv / NV) & 1, wc, 5, j)) { fine = false; break; }
+                                v_ready = true;
+                            }
+                            tc_fence_after();
+                            issue_pv(tmem + col_o(x), tmem + col_s(x), v_addr0 + sv * TILE_BYTES, !first_pv[x]);
+                            first_pv[x] = false;
+                            ++cp[x];
+                            if (j == last_used[x]) umma_commit(&ofull[x]);
                         }
-                        tc_fence_after();
-                        issue_pv(tmem + col_o(x), tmem + col_s(x), v_addr0 + sv * TILE_BYTES, cnt[x] > 0);
-                        ++cnt[x];
+                        if (fn & (2 << x)) {  // S_x is free again once PV_x(j) has been issued
+                            if (!k_ready) {
+                                if (!mbar_wait(&kfull[sk], (gk / NK) & 1, wc, 3, j + 1)) { fine = false; break; }
+                                k_ready = true;
+                            }
+                            tc_fence_after();
+                            issue_qk(tmem + col_s(x), q_addr + x * TILE_BYTES, k_addr0 + sk * TILE_BYTES);
+                            umma_commit(&sfull[x]);
+                        }
                     }
-                    if (fn & (2 << x)) {  // S_x is free again once PV_x(j) has been issued
-                        if (!k_ready) {
-                            if (!mbar_wait(&kfull[sk], ((j + 1) / NK) & 1, wc, 3, j + 1)) { fine = false; break; }
-                            k_ready = true;
-                        }
-                        tc_fence_after();
-                        issue_qk(tmem + col_s(x), q_addr + x * TILE_BYTES, k_addr0 + sk * TILE_BYTES);
-                        umma_commit(&sfull[x]);
+                    if (!fine) break;
+                    if (j + 2 == n) umma_commit(qempty);  // the item's last QK products were just issued
+                    umma_commit(&vempty[sv]);
+                    ++gv;
+                    if (j + 1 < n) {
+                        umma_commit(&kempty[sk]);
+                        ++gk;
                     }
                 }
                 if (!fine) break;
-                umma_commit(&vempty[sv]);
-                if (j + 1 < nt) umma_commit(&kempty[sk]);
+                mbar_arrive(&lfree[b]);
             }
-            if (fine) umma_commit(ofull);
             if (issued_any) {  // no MMA may still be running when TMEM is freed
                 umma_commit(drain);
                 mbar_wait_drain(drain, 0);
             }
         }
-    } else if (warp < 8 && ok) {
+    } else if (warp < 8) {
         // ------------------------------------------------------------------ softmax + epilogue
         const int x = warp >> 2;                    // query tile of this warpgroup
         const int r = threadIdx.x & (BH_ROWS - 1);  // its row == TMEM lane
-        const int t = q0 + x * BH_ROWS + r;         // absolute position
         const uint32_t lane_base = static_cast<uint32_t>((warp & 3) * 32) << 16;
         const uint32_t s_addr = tmem + lane_base + col_s(x);
         const uint32_t o_addr = tmem + lane_base + col_o(x);
         const float sl2 = P.scale_log2;
         const int bit = 2 << x;
-        float mrun = -INFINITY, lrun = 0.f;  // running max (log2 units) and sum
+        int cs = 0;  // tiles processed by this warpgroup (sfull / pfull parity)
+        int ne = 0;  // epilogues done (ofull parity)
         bool fine = true;
-        int cnt = 0;
-        for (int j = 0; j < nt; ++j) {
-            const Tile T = tiles[j];
-            if (!(T.flags & bit)) continue;
-            fine = __all_sync(0xFFFFFFFFu, mbar_wait(&sfull[x], cnt & 1, wc, 6, j));
+        for (int it = 0; fine; ++it) {
+            const int item = static_cast<int>(blockIdx.x) + it * G;
+            if (item >= P.n_items) break;
+            const int bh = item % P.BH;
+            const int row_start = (P.n_qpairs - 1 - item / P.BH) * BM;
+            const int q0 = P.pos0 + row_start;
+            const int qlast = P.pos0 + min(row_start + BM, P.L) - 1;
+            const int t = q0 + x * BH_ROWS + r;  // absolute position of this thread's row
+            const int b = it & 1;
+            fine = __all_sync(0xFFFFFFFFu, mbar_wait(&lready[b], (it >> 1) & 1, wc, 14, it));
             if (!fine) break;
-            tc_fence_after();
-            // valid columns of this row: [0, b1] (sinks) and [a2, hc] (window), hc = last causal column,
-            // as four 32-bit column masks; interior tiles need none
-            const int hc = min(T.chi, t - T.pbase);
-            const int b1 = min(hc, P.s - 1 - T.pbase);
-            const int a2 = max(0, t - P.m + 1 - T.pbase);
-            const bool full = (b1 >= BN - 1) || (hc >= BN - 1 && (a2 <= 0 || b1 >= a2 - 1));
-            const bool any_masked = __any_sync(0xFFFFFFFFu, !full);  // warp-uniform: no divergent paths
-            uint32_t mw[4];
+            const Tile *tl = tiles_s + b * MAX_TILES;
+            const int n = ntiles_s[b];
+            float mrun = -INFINITY, lrun = 0.f;  // running max (log2 units) and sum
+            int cnt = 0;
+            for (int j = 0; j < n; ++j) {
+                const Tile T = tl[j];
+                if (!(T.flags & bit)) continue;
+                fine = __all_sync(0xFFFFFFFFu, mbar_wait(&sfull[x], cs & 1, wc, 6, j));
+                if (!fine) break;
+                tc_fence_after();
+                // valid columns of this row: [0, b1] (sinks) and [a2, hc] (window), hc = last causal
+                // column, as four 32-bit column masks; interior tiles need none
+                const int hc = min(static_cast<int>(T.chi), t - T.pbase);
+                const int b1 = min(hc, P.s - 1 - T.pbase);
+                const int a2 = max(0, t - P.m + 1 - T.pbase);
+                const bool full = (b1 >= BN - 1) || (hc >= BN - 1 && (a2 <= 0 || b1 >= a2 - 1));
+                const bool any_masked = __any_sync(0xFFFFFFFFu, !full);  // warp-uniform: no divergent paths
+                uint32_t mw[4];
 #pragma unroll
-            for (int k = 0; k < 4; ++k)
-                mw[k] = full ? 0xFFFFFFFFu : (range_bits(-32 * k, b1 - 32 * k) | range_bits(a2 - 32 * k, hc - 32 * k));
-            // the whole row of S_x in registers (one TMEM load)
-            float sv[BN];
-            __syncwarp();
-            tmem_ld128(s_addr, sv);
-            if (any_masked) {
-#pragma unroll
-                for (int c = 0; c < BN; ++c) sv[c] = (mw[c >> 5] & (1u << (c & 31))) ? sv[c] : -INFINITY;
-            }
-            float mx8[8];
-#pragma unroll
-            for (int i = 0; i < 8; ++i) mx8[i] = sv[i];
-#pragma unroll
-            for (int c = 8; c < BN; ++c) mx8[c & 7] = fmaxf(mx8[c & 7], sv[c]);
-            const float mx = fmaxf(fmaxf(fmaxf(mx8[0], mx8[1]), fmaxf(mx8[2], mx8[3])),
-                                   fmaxf(fmaxf(mx8[4], mx8[5]), fmaxf(mx8[6], mx8[7]))) * sl2;
-            float alpha = 1.f;
-            bool resc = false;
-            const float mnew = fmaxf(mrun, mx);
-            if (mnew > mrun + kRescaleLog2) {  // also taken when mrun is still -inf
-                if (mrun != -INFINITY) {
-                    alpha = ex2(mrun - mnew);
-                    resc = true;
-                }
-                mrun = mnew;
-            }
-            if (__any_sync(0xFFFFFFFFu, resc)) {
-                // O_x holds the PV products of the earlier tiles; they are complete, because S_x (issued
-                // after the last of them) is, and tcgen05 MMAs of one thread complete in order.
+                for (int k = 0; k < 4; ++k)
+                    mw[k] = full ? 0xFFFFFFFFu : (range_bits(-32 * k, b1 - 32 * k) | range_bits(a2 - 32 * k, hc - 32 * k));
+                // the whole row of S_x in registers (one TMEM load)
+                float sv[BN];
                 __syncwarp();
+                tmem_ld128(s_addr, sv);
+                if (any_masked) {
+#pragma unroll
+                    for (int c = 0; c < BN; ++c) sv[c] = (mw[c >> 5] & (1u << (c & 31))) ? sv[c] : -INFINITY;
+                }
+                float mx8[8];
+#pragma unroll
+                for (int i = 0; i < 8; ++i) mx8[i] = sv[i];
+#pragma unroll
+                for (int c = 8; c < BN; ++c) mx8[c & 7] = fmaxf(mx8[c & 7], sv[c]);
+                const float mx = fmaxf(fmaxf(fmaxf(mx8[0], mx8[1]), fmaxf(mx8[2], mx8[3])),
+                                       fmaxf(fmaxf(mx8[4], mx8[5]), fmaxf(mx8[6], mx8[7]))) * sl2;
+                float alpha = 1.f;
+                bool resc = false;
+                const float mnew = fmaxf(mrun, mx);
+                if (mnew > mrun + kRescaleLog2) {  // also taken when mrun is still -inf
+                    if (mrun != -INFINITY) {
+                        alpha = ex2(mrun - mnew);
+                        resc = true;
+                    }
+                    mrun = mnew;
+                }
+                if (__any_sync(0xFFFFFFFFu, resc)) {
+                    // O_x holds the PV products of this item's earlier tiles; they are complete,
+                    // because S_x (issued after the last of them) is, and tcgen05 MMAs of one thread
+                    // complete in order.
+                    __syncwarp();
 #pragma unroll 1
-                for (int c = 0; c < HD; c += 32) {
-                    float ov[32];
-                    tmem_ld32(o_addr + c, ov);
+                    for (int c = 0; c < HD; c += 32) {
+                        float ov[32];
+                        tmem_ld32(o_addr + c, ov);
 #pragma unroll
-                    for (int i = 0; i < 32; ++i) ov[i] *= alpha;
-                    tmem_st32(o_addr + c, ov);
+                        for (int i = 0; i < 32; ++i) ov[i] *= alpha;
+                        tmem_st32(o_addr + c, ov);
+                    }
                 }
-            }
-            // p = 2^(scale*log2(e)*s - m); bf16 pairs of keys 0..63 / 64..127 go to columns [0, 32) /
-            // [32, 64) of S_x (already read): the A operand of PV_x
-            const float nmu = (mrun == -INFINITY) ? 0.f : -mrun;
-            float rs8[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+                // p = 2^(scale*log2(e)*s - m); bf16 pairs of keys 0..63 / 64..127 go to columns [0, 32) /
+                // [32, 64) of S_x (already read): the A operand of PV_x
+                const float nmu = (mrun == -INFINITY) ? 0.f : -mrun;
+                float rs8[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
 #pragma unroll
-            for (int h = 0; h < 2; ++h) {
-                uint32_t pk[32];
+                for (int h = 0; h < 2; ++h) {
+                    uint32_t pk[32];
 #pragma unroll
-                for (int i = 0; i < 32; ++i) {
-                    const int c = 64 * h + 2 * i;
-                    const float p0 = ex2(fmaf(sv[c], sl2, nmu)), p1 = ex2(fmaf(sv[c + 1], sl2, nmu));
-                    rs8[(2 * i) & 7] += p0;
-                    rs8[(2 * i + 1) & 7] += p1;
-                    pk[i] = pack_bf16x2(p0, p1);
+                    for (int i = 0; i < 32; ++i) {
+                        const int c = 64 * h + 2 * i;
+                        const float p0 = ex2(fmaf(sv[c], sl2, nmu)), p1 = ex2(fmaf(sv[c + 1], sl2, nmu));
+                        rs8[(2 * i) & 7] += p0;
+                        rs8[(2 * i + 1) & 7] += p1;
+                        pk[i] = pack_bf16x2(p0, p1);
+                    }
+                    __syncwarp();
+                    tmem_st32u_nowait(s_addr + 32 * h, pk);
                 }
-                __syncwarp();
-                tmem_st32u_nowait(s_addr + 32 * h, pk);
+                tmem_wait_st();
+                lrun = lrun * alpha +
+                       (((rs8[0] + rs8[1]) + (rs8[2] + rs8[3])) + ((rs8[4] + rs8[5]) + (rs8[6] + rs8[7])));
+                tc_fence_before();
+                mbar_arrive(&pfull[x]);
+                ++cnt;
+                ++cs;
             }
-            tmem_wait_st();
-            lrun = lrun * alpha + (((rs8[0] + rs8[1]) + (rs8[2] + rs8[3])) + ((rs8[4] + rs8[5]) + (rs8[6] + rs8[7])));
-            tc_fence_before();
-            mbar_arrive(&pfull[x]);
-            ++cnt;
-        }
-        if (fine && cnt > 0) fine = __all_sync(0xFFFFFFFFu, mbar_wait(ofull, 0, wc, 8, nt));
-        if (fine && cnt > 0) {
-            // epilogue: O_x / l -> bf16, staged in the (now idle) Q_x buffer with the 128-byte swizzle,
-            // then written by two TMA stores (rows past the end of the sequence are clipped by TMA)
+            if (!fine) break;
+            if (lane == 0) mbar_arrive(&lfree[b]);  // this warp no longer reads the tile list
+            if (cnt == 0) continue;                // no row of this query tile in the sequence
+            // epilogue: O_x / l -> bf16 in registers, O_x handed back to the MMA, then the rows are
+            // written to global memory (and lse)
+            fine = __all_sync(0xFFFFFFFFu, mbar_wait(&ofull[x], ne & 1, wc, 8, it));
+            if (!fine) break;
+            ++ne;
             tc_fence_after();
             const float inv = (lrun > 0.f) ? 1.f / lrun : 0.f;
-            uint8_t *ost = sm + OFF_Q + x * TILE_BYTES;
-            const uint32_t obase = smem_u32(ost);
+            uint32_t ob[HD / 2];
             __syncwarp();
-#pragma unroll 1
+#pragma unroll
             for (int c = 0; c < HD; c += 32) {
                 float ov[32];
                 tmem_ld32(o_addr + c, ov);
 #pragma unroll
-                for (int i = 0; i < 4; ++i) {
-                    const int col = (c & 63) + 8 * i;  // column within the 64-column half
-                    st_shared_v4(obase + (c >> 6) * HALF_BYTES + sw128_offset(r, col),
-                                 pack_bf16x2(ov[8 * i + 0] * inv, ov[8 * i + 1] * inv),
-                                 pack_bf16x2(ov[8 * i + 2] * inv, ov[8 * i + 3] * inv),
-                                 pack_bf16x2(ov[8 * i + 4] * inv, ov[8 * i + 5] * inv),
-                                 pack_bf16x2(ov[8 * i + 6] * inv, ov[8 * i + 7] * inv));
-                }
+                for (int i = 0; i < 16; ++i) ob[c / 2 + i] = pack_bf16x2(ov[2 * i] * inv, ov[2 * i + 1] * inv);
             }
-            fence_proxy_async_smem();
-            mbar_arrive(&ostaged[x]);
-            if (t <= qlast && P.lse)
-                P.lse[static_cast<int64_t>(bh) * P.seq_stride + row_start + x * BH_ROWS + r] =
-                    (mrun + log2f(lrun)) * 0.69314718055994531f;
-            if (r == 0 && mbar_wait(&ostaged[x], 0, wc, 10, x)) {
-                tma_store_3d(&P.tm_o, ost, 0, row_start + x * BH_ROWS, bh);
-                tma_store_3d(&P.tm_o, ost + HALF_BYTES, 64, row_start + x * BH_ROWS, bh);
-                bulk_commit_group();
-                bulk_wait_group_read0();
+            tc_fence_before();
+            mbar_arrive(&oempty[x]);
+            if (t <= qlast) {
+                const int64_t row = static_cast<int64_t>(bh) * P.seq_stride + row_start + x * BH_ROWS + r;
+                uint4 *dst = reinterpret_cast<uint4 *>(static_cast<__nv_bfloat16 *>(P.o) + row * HD);
+#pragma unroll
+                for (int i = 0; i < HD / 8; ++i)
+                    dst[i] = make_uint4(ob[4 * i], ob[4 * i + 1], ob[4 * i + 2], ob[4 * i + 3]);
+                if (P.lse) P.lse[row] = (mrun + log2f(lrun)) * 0.69314718055994531f;
             }
         }
     }
@@ -636,12 +707,24 @@ static int max_tiles_bound(int w, int s) {
     return (s + tc::BN - 1) / tc::BN + 1 + (m + tc::BM - 1 + tc::BN - 1) / tc::BN + 3;
 }
 
+static int sm_count() {
+    static int cached[64] = {0};
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return -1;
+    if (!cached[dev]) {
+        int n = 0;
+        if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return -1;
+        cached[dev] = n;
+    }
+    return cached[dev];
+}
+
 int launch_prefill_bf16_tc(const PrefillArgs &a) {
     using namespace tc;
     if (a.d != HD) return fail(SWA_ERR_UNSUPPORTED, "tensor-core prefill needs d = %d", HD);
     if (max_tiles_bound(a.w, a.s) > MAX_TILES)
         return fail(SWA_ERR_UNSUPPORTED, "window w=%d needs more than %d key tiles per query tile", a.w, MAX_TILES);
-    if (a.BH > 65535) return fail(SWA_ERR_UNSUPPORTED, "B*H=%d > 65535", a.BH);
+    if ((a.L + BM - 1) / BM * a.BH > 0x7FFFFFFF) return fail(SWA_ERR_UNSUPPORTED, "too many work items");
     if (!encode_tiled_fn()) return fail(SWA_ERR_CUDA, "cuTensorMapEncodeTiled is not available");
     unsigned *status = device_status_word();
     if (!status) return SWA_ERR_CUDA;
@@ -649,7 +732,7 @@ int launch_prefill_bf16_tc(const PrefillArgs &a) {
     memset(&p, 0, sizeof(p));
     const uint64_t L = static_cast<uint64_t>(a.L), st = static_cast<uint64_t>(a.seq_stride);
     bool okm = encode_rows_map(&p.tm_q, a.q, L, a.BH, st) && encode_rows_map(&p.tm_k, a.k, L, a.BH, st) &&
-               encode_rows_map(&p.tm_v, a.v, L, a.BH, st) && encode_rows_map(&p.tm_o, a.o, L, a.BH, st);
+               encode_rows_map(&p.tm_v, a.v, L, a.BH, st);
     if (a.pos0 > 0) {
         // Only slots 0..min(pos0, w)-1 have been written; the map stops there so that TMA zero-fills the
         // rest of a tile instead of loading stale bytes (a masked column still multiplies its V row by 0,
@@ -671,13 +754,18 @@ int launch_prefill_bf16_tc(const PrefillArgs &a) {
     p.w = a.w;
     p.s = a.s;
     p.m = a.w - a.s;
-    p.n_qtiles = static_cast<int>((a.L + BM - 1) / BM);
+    p.BH = a.BH;
+    p.n_qpairs = static_cast<int>((a.L + BM - 1) / BM);
+    p.n_items = p.n_qpairs * a.BH;
     p.scale_log2 = a.scale * 1.4426950408889634f;
     p.timeout_ns = kWaitTimeoutNs;
     cudaError_t e = cudaFuncSetAttribute(swa_prefill_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          static_cast<int>(SMEM_BYTES));
     if (e != cudaSuccess) return fail(SWA_ERR_CUDA, "prefill smem attribute: %s", cudaGetErrorString(e));
-    const dim3 grid(p.n_qtiles, a.BH), block(kThreads);
+    // persistent: one CTA per SM, each walking work items blockIdx.x, blockIdx.x + gridDim.x, ...
+    const int sms = sm_count();
+    if (sms <= 0) return fail(SWA_ERR_CUDA, "cannot read the multiprocessor count");
+    const dim3 grid(p.n_items < sms ? p.n_items : sms), block(kThreads);
     swa_prefill_tc_kernel<<<grid, block, SMEM_BYTES, a.stream>>>(p);
     e = cudaGetLastError();
     if (e != cudaSuccess) return fail(SWA_ERR_CUDA, "prefill launch: %s", cudaGetErrorString(e));
