@@ -9,8 +9,9 @@
 // intersect the band or the sink block of its query tile; no skipped tile is ever loaded.
 //
 // Work item = two query tiles of 128 rows (256 consecutive rows) of one (b, h).  The kernel is
-// persistent: one CTA per SM walks the items blockIdx.x, blockIdx.x + gridDim.x, ..., ordered
-// longest-first (the last query pairs of every head, whose windows are full, come first).  320 threads
+// persistent: one CTA per SM walks the items blockIdx.x, blockIdx.x + gridDim.x, ...  Items are
+// head-major (the items in flight share a few heads' key/value bands in L2) and, within a head,
+// longest-first (the last query pairs, whose windows are full, come first).  320 threads
 // in four roles:
 //   warps 0-3 / 4-7  softmax + epilogue of query tile 0 / 1: thread r owns row r of its tile
 //              (= TMEM lane r);
@@ -280,8 +281,8 @@ __global__ void __launch_bounds__(kThreads, 1) swa_prefill_tc_kernel(const __gri
             for (int it = 0; fine; ++it) {
                 const int item = static_cast<int>(blockIdx.x) + it * G;
                 if (item >= P.n_items) break;
-                const int bh = item % P.BH;
-                const int row_start = (P.n_qpairs - 1 - item / P.BH) * BM;
+                const int bh = item / P.n_qpairs;
+                const int row_start = (P.n_qpairs - 1 - item % P.n_qpairs) * BM;
                 const int q0 = P.pos0 + row_start;
                 const int qlast = P.pos0 + min(row_start + BM, P.L) - 1;
                 const int b = it & 1;
@@ -440,8 +441,8 @@ __global__ void __launch_bounds__(kThreads, 1) swa_prefill_tc_kernel(const __gri
         for (int it = 0; fine; ++it) {
             const int item = static_cast<int>(blockIdx.x) + it * G;
             if (item >= P.n_items) break;
-            const int bh = item % P.BH;
-            const int row_start = (P.n_qpairs - 1 - item / P.BH) * BM;
+            const int bh = item / P.n_qpairs;
+            const int row_start = (P.n_qpairs - 1 - item % P.n_qpairs) * BM;
             const int q0 = P.pos0 + row_start;
             const int qlast = P.pos0 + min(row_start + BM, P.L) - 1;
             const int t = q0 + x * BH_ROWS + r;  // absolute position of this thread's row
