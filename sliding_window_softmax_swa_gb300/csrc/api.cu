@@ -1,6 +1,7 @@
 // api.cu -- the C ABI of include/swa_sink.h: argument validation, dispatch to the kernels' launchers,
 // the per-device error word, the thread-local error string and the tensor-map encoder lookup.
 #include <stdarg.h>
+#include <stddef.h>
 #include <stdio.h>
 #include <string.h>
 
@@ -13,9 +14,8 @@
 namespace swa {
 
 // One error word per device.  Kernels receive its address; swa_device_status() reads and clears it.
-__device__ unsigned g_swa_status_word;
-// Where the first bounded wait of the device ran out (see WaitCtl); cleared with the error word.
-__device__ unsigned long long g_swa_timeout_info;
+// (with where the first bounded wait of the device ran out, cleared together with the word)
+__device__ DeviceStatus g_swa_status;
 
 static thread_local char t_err[512];
 
@@ -39,7 +39,7 @@ unsigned *device_status_word() {
     std::lock_guard<std::mutex> lk(mu);
     if (!ptrs[dev]) {
         void *p = nullptr;
-        e = cudaGetSymbolAddress(&p, g_swa_status_word);
+        e = cudaGetSymbolAddress(&p, g_swa_status);
         if (e != cudaSuccess) {
             fail(SWA_ERR_CUDA, "cudaGetSymbolAddress(status word): %s", cudaGetErrorString(e));
             return nullptr;
@@ -57,8 +57,8 @@ unsigned long long *device_timeout_info() {
     std::lock_guard<std::mutex> lk(mu);
     if (!ptrs[dev]) {
         void *p = nullptr;
-        if (cudaGetSymbolAddress(&p, g_swa_timeout_info) != cudaSuccess) return nullptr;
-        ptrs[dev] = static_cast<unsigned long long *>(p);
+        if (cudaGetSymbolAddress(&p, g_swa_status) != cudaSuccess) return nullptr;
+        ptrs[dev] = &static_cast<DeviceStatus *>(p)->info;
     }
     return ptrs[dev];
 }
@@ -104,14 +104,14 @@ extern "C" int swa_device_status(void *stream) {
     cudaError_t e = cudaStreamSynchronize(static_cast<cudaStream_t>(stream));
     if (e != cudaSuccess) return fail(SWA_ERR_CUDA, "cudaStreamSynchronize: %s", cudaGetErrorString(e));
     unsigned word = 0;
-    e = cudaMemcpyFromSymbol(&word, g_swa_status_word, sizeof(word));
+    e = cudaMemcpyFromSymbol(&word, g_swa_status, sizeof(word), offsetof(DeviceStatus, word));
     if (e != cudaSuccess) return fail(SWA_ERR_CUDA, "reading the device error word: %s", cudaGetErrorString(e));
     if (word != 0) {
         unsigned zero = 0;
         unsigned long long info = 0, zero64 = 0;
-        cudaMemcpyFromSymbol(&info, g_swa_timeout_info, sizeof(info));
-        cudaMemcpyToSymbol(g_swa_status_word, &zero, sizeof(zero));
-        cudaMemcpyToSymbol(g_swa_timeout_info, &zero64, sizeof(zero64));
+        cudaMemcpyFromSymbol(&info, g_swa_status, sizeof(info), offsetof(DeviceStatus, info));
+        cudaMemcpyToSymbol(g_swa_status, &zero, sizeof(zero), offsetof(DeviceStatus, word));
+        cudaMemcpyToSymbol(g_swa_status, &zero64, sizeof(zero64), offsetof(DeviceStatus, info));
         if (word & kDevTimeout)
             return fail(SWA_ERR_TIMEOUT,
                         "a bounded device wait ran out (error word 0x%08x; first: site %u, tag %u, warp %u, "

@@ -99,13 +99,12 @@ struct Params {
     CUtensorMap tm_q, tm_k, tm_v, tm_kc, tm_vc;
     void *o;
     float *lse;
-    unsigned *status;
-    unsigned long long *info;
+    DeviceStatus *status;
     int64_t seq_stride;  // rows between (b, h) blocks of q/k/v/o/lse
     int L, pos0, w, s, m, BH;
     int n_qpairs, n_items;  // 256-row query pairs per (b, h); work items = n_qpairs * BH
     float scale_log2;
-    uint64_t timeout_ns;
+    uint32_t timeout_us;
 };
 
 // Build the key-tile list of the query tile [q0, q1] (absolute positions).  Returns the tile count
@@ -265,7 +264,7 @@ __global__ void __launch_bounds__(kThreads, 1) swa_prefill_tc_kernel(const __gri
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem = *tmem_slot;
-    const WaitCtl wc{abort_flag, P.status, P.info, P.timeout_ns};
+    const WaitCtl wc{smem_u32(const_cast<int *>(abort_flag)), P.timeout_us, P.status};
 
     if (warp == kWarpTma) {
         // ------------------------------------------------------------------ TMA producer
@@ -290,7 +289,7 @@ __global__ void __launch_bounds__(kThreads, 1) swa_prefill_tc_kernel(const __gri
                 Tile *tl = tiles_s + b * MAX_TILES;
                 const int n = build_tiles(tl, q0, qlast, P.pos0, P.s, P.m, P.w);
                 if (n < 1 || n > MAX_TILES) {
-                    atomicOr(P.status, kDevBadArg);
+                    atomicOr(&P.status->word, kDevBadArg);
                     *abort_flag = 1;
                     break;
                 }
@@ -512,7 +511,7 @@ __global__ void __launch_bounds__(kThreads, 1) swa_prefill_tc_kernel(const __gri
                 // p = 2^(scale*log2(e)*s - m); bf16 pairs of keys 0..63 / 64..127 go to columns [0, 32) /
                 // [32, 64) of S_x (already read): the A operand of PV_x
                 const float nmu = (mrun == -INFINITY) ? 0.f : -mrun;
-                float rs8[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+                float rs4[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
                 for (int h = 0; h < 2; ++h) {
                     uint32_t pk[32];
@@ -520,16 +519,15 @@ __global__ void __launch_bounds__(kThreads, 1) swa_prefill_tc_kernel(const __gri
                     for (int i = 0; i < 32; ++i) {
                         const int c = 64 * h + 2 * i;
                         const float p0 = ex2(fmaf(sv[c], sl2, nmu)), p1 = ex2(fmaf(sv[c + 1], sl2, nmu));
-                        rs8[(2 * i) & 7] += p0;
-                        rs8[(2 * i + 1) & 7] += p1;
+                        rs4[(2 * i) & 3] += p0;
+                        rs4[(2 * i + 1) & 3] += p1;
                         pk[i] = pack_bf16x2(p0, p1);
                     }
                     __syncwarp();
                     tmem_st32u_nowait(s_addr + 32 * h, pk);
                 }
                 tmem_wait_st();
-                lrun = lrun * alpha +
-                       (((rs8[0] + rs8[1]) + (rs8[2] + rs8[3])) + ((rs8[4] + rs8[5]) + (rs8[6] + rs8[7])));
+                lrun = lrun * alpha + ((rs4[0] + rs4[1]) + (rs4[2] + rs4[3]));
                 tc_fence_before();
                 mbar_arrive(&pfull[x]);
                 ++cnt;
@@ -576,7 +574,7 @@ __global__ void __launch_bounds__(kThreads, 1) swa_prefill_tc_kernel(const __gri
 }
 
 // ---------------------------------------------------------------------------------------- diagnostics
-__global__ void selftest_wait_kernel(unsigned *status, uint64_t timeout_ns) {
+__global__ void selftest_wait_kernel(DeviceStatus *status, uint32_t timeout_us) {
     __shared__ uint64_t bar;
     __shared__ int abort_flag;
     if (threadIdx.x == 0) {
@@ -587,7 +585,7 @@ __global__ void selftest_wait_kernel(unsigned *status, uint64_t timeout_ns) {
     __syncthreads();
     if (threadIdx.x == 0) {
         // nothing ever arrives on `bar`: the wait runs out, records the timeout and returns
-        const WaitCtl wc{&abort_flag, status, nullptr, timeout_ns};
+        const WaitCtl wc{smem_u32(&abort_flag), timeout_us, status};
         mbar_wait(&bar, 0, wc, 99);
     }
 }
@@ -595,7 +593,7 @@ __global__ void selftest_wait_kernel(unsigned *status, uint64_t timeout_ns) {
 __global__ void __launch_bounds__(128, 1) selftest_umma_kernel(const __grid_constant__ CUtensorMap ma,
                                                              const __grid_constant__ CUtensorMap mb,
                                                              const __nv_bfloat16 *__restrict__ a_glob,
-                                                             float *__restrict__ c, int mode, unsigned *status) {
+                                                             float *__restrict__ c, int mode, DeviceStatus *status) {
     extern __shared__ uint8_t smem_raw[];
     uint8_t *sm = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     uint8_t *As = sm, *Bs = sm + TILE_BYTES;
@@ -638,7 +636,7 @@ __global__ void __launch_bounds__(128, 1) selftest_umma_kernel(const __grid_cons
     }
     __syncthreads();
     tc_fence_after();
-    const WaitCtl wc{abort_flag, status, nullptr, kWaitTimeoutNs};
+    const WaitCtl wc{smem_u32(const_cast<int *>(abort_flag)), kWaitTimeoutUs, status};
     if (threadIdx.x == 0) {
         mbar_arrive_expect_tx(load_bar, mode >= 2 ? TILE_BYTES : 2 * TILE_BYTES);
         if (mode < 2) {
@@ -747,8 +745,7 @@ int launch_prefill_bf16_tc(const PrefillArgs &a) {
     if (!okm) return fail(SWA_ERR_INVALID, "cuTensorMapEncodeTiled rejected a tensor (alignment or size)");
     p.o = a.o;
     p.lse = a.lse;
-    p.status = status;
-    p.info = device_timeout_info();
+    p.status = reinterpret_cast<DeviceStatus *>(status);
     p.seq_stride = a.seq_stride;
     p.L = static_cast<int>(a.L);
     p.pos0 = static_cast<int>(a.pos0);
@@ -759,7 +756,7 @@ int launch_prefill_bf16_tc(const PrefillArgs &a) {
     p.n_qpairs = static_cast<int>((a.L + BM - 1) / BM);
     p.n_items = p.n_qpairs * a.BH;
     p.scale_log2 = a.scale * 1.4426950408889634f;
-    p.timeout_ns = kWaitTimeoutNs;
+    p.timeout_us = kWaitTimeoutUs;
     cudaError_t e = cudaFuncSetAttribute(swa_prefill_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          static_cast<int>(SMEM_BYTES));
     if (e != cudaSuccess) return fail(SWA_ERR_CUDA, "prefill smem attribute: %s", cudaGetErrorString(e));
@@ -790,7 +787,8 @@ int prefill_tile_plan(int q0, int q1, int pos0, int w, int s, int *out, int max_
 int launch_selftest_wait_timeout(uint64_t timeout_ns, cudaStream_t stream) {
     unsigned *status = device_status_word();
     if (!status) return SWA_ERR_CUDA;
-    tc::selftest_wait_kernel<<<1, 32, 0, stream>>>(status, timeout_ns);
+    const uint32_t us = static_cast<uint32_t>((timeout_ns + 999) / 1000);
+    tc::selftest_wait_kernel<<<1, 32, 0, stream>>>(reinterpret_cast<DeviceStatus *>(status), us);
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return fail(SWA_ERR_CUDA, "selftest launch: %s", cudaGetErrorString(e));
     return SWA_OK;
@@ -808,7 +806,7 @@ int launch_selftest_umma(const void *a, const void *b, float *c, int mode, cudaS
                                          static_cast<int>(smem));
     if (e != cudaSuccess) return fail(SWA_ERR_CUDA, "selftest smem attribute: %s", cudaGetErrorString(e));
     tc::selftest_umma_kernel<<<1, 128, smem, stream>>>(ma, mb, static_cast<const __nv_bfloat16 *>(a), c, mode,
-                                                       status);
+                                                       reinterpret_cast<DeviceStatus *>(status));
     e = cudaGetLastError();
     if (e != cudaSuccess) return fail(SWA_ERR_CUDA, "selftest launch: %s", cudaGetErrorString(e));
     return SWA_OK;

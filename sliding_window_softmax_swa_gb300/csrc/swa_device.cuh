@@ -19,6 +19,7 @@ constexpr unsigned kWhereShift = 8;
 
 // Default limit of a pipeline wait.  Every kernel of this library finishes in milliseconds.
 constexpr uint64_t kWaitTimeoutNs = 1000000000ull;  // 1 s
+constexpr uint32_t kWaitTimeoutUs = 1000000u;
 
 __device__ __forceinline__ uint64_t globaltimer_ns() {
     uint64_t t;
@@ -58,40 +59,55 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
     return ok != 0;
 }
 
-// Shared state of the bounded waits of one CTA: once any wait of the CTA gives up, `abort` is set
-// and every other wait of the CTA returns false at its next check.  The first wait of the device that
-// runs out also leaves a record in `info`: site | tag << 8 | warp << 20 | blockIdx.x << 32 | blockIdx.y << 48.
-struct WaitCtl {
-    volatile int *abort;      // in shared memory
-    unsigned *status;         // device error word (global)
-    unsigned long long *info; // first-timeout record (global), may be null
-    uint64_t timeout_ns;
+// Per-device status record: the error word the kernels OR bits into, and where the first bounded wait
+// of the device ran out: site | tag << 8 | warp << 20 | blockIdx.x << 32 | blockIdx.y << 48.
+struct DeviceStatus {
+    unsigned word;
+    unsigned pad;
+    unsigned long long info;
 };
+
+// Shared state of the bounded waits of one CTA, kept small (4 registers) because it stays live across
+// the pipeline loops: once any wait of the CTA gives up, the abort flag (a shared-memory int) is set and
+// every other wait of the CTA returns false at its next check.
+struct WaitCtl {
+    uint32_t abort_smem;  // shared-memory address of the CTA's abort flag
+    uint32_t timeout_us;  // limit of one wait
+    DeviceStatus *status;
+};
+
+__device__ __forceinline__ int ld_abort(uint32_t a) {
+    int v;
+    asm volatile("ld.volatile.shared.u32 %0, [%1];" : "=r"(v) : "r"(a) : "memory");
+    return v;
+}
+__device__ __forceinline__ void st_abort(uint32_t a) {
+    asm volatile("st.volatile.shared.u32 [%0], %1;" ::"r"(a), "r"(1) : "memory");
+}
 
 // Wait until the phase with the given parity of `bar` has completed.  Returns false when the wait
 // ran out (or another wait of the CTA did); the caller must then stop its pipeline role.
-static __device__ __noinline__ bool mbar_wait_slow(uint32_t a, uint32_t parity, const WaitCtl &c, unsigned where,
+static __device__ __noinline__ bool mbar_wait_slow(uint32_t a, uint32_t parity, const WaitCtl c, unsigned where,
                                                    unsigned tag) {
     const uint64_t t0 = globaltimer_ns();
+    const uint64_t limit = static_cast<uint64_t>(c.timeout_us) * 1000ull;
     for (uint32_t it = 1;; ++it) {
         if (mbar_try_wait(a, parity)) return true;
         if ((it & 31u) == 0) {
-            if (*c.abort) return false;
-            if (globaltimer_ns() - t0 > c.timeout_ns) {
-                *c.abort = 1;
-                atomicOr(c.status, kDevTimeout | ((where & 0xFFu) << kWhereShift));
-                if (c.info) {
-                    const unsigned long long rec =
-                        (where & 0xFFull) | ((tag & 0xFFFull) << 8) | ((threadIdx.x >> 5 & 0xFFFull) << 20) |
-                        ((blockIdx.x & 0xFFFFull) << 32) | ((blockIdx.y & 0xFFFFull) << 48);
-                    atomicCAS(c.info, 0ull, rec);
-                }
+            if (ld_abort(c.abort_smem)) return false;
+            if (globaltimer_ns() - t0 > limit) {
+                st_abort(c.abort_smem);
+                atomicOr(&c.status->word, kDevTimeout | ((where & 0xFFu) << kWhereShift));
+                const unsigned long long rec =
+                    (where & 0xFFull) | ((tag & 0xFFFull) << 8) | ((threadIdx.x >> 5 & 0xFFFull) << 20) |
+                    ((blockIdx.x & 0xFFFFull) << 32) | ((blockIdx.y & 0xFFFFull) << 48);
+                atomicCAS(&c.status->info, 0ull, rec);
                 return false;
             }
         }
     }
 }
-__device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity, const WaitCtl &c, unsigned where,
+__device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity, const WaitCtl c, unsigned where,
                                           unsigned tag = 0) {
     const uint32_t a = smem_u32(bar);
     if (mbar_try_wait(a, parity)) return true;
@@ -113,7 +129,7 @@ __device__ __forceinline__ void tmem_wait_ld_regs(uint32_t (&r)[32]) {
 }
 // Spin on an mbarrier phase without suspending the thread (for a single latency-critical thread);
 // bounded like mbar_wait.
-static __device__ __noinline__ bool mbar_wait_spin_slow(uint32_t a, uint32_t parity, const WaitCtl &c,
+static __device__ __noinline__ bool mbar_wait_spin_slow(uint32_t a, uint32_t parity, const WaitCtl c,
                                                         unsigned where, unsigned tag) {
     const uint64_t t0 = globaltimer_ns();
     for (uint32_t it = 1;; ++it) {
@@ -127,12 +143,13 @@ static __device__ __noinline__ bool mbar_wait_spin_slow(uint32_t a, uint32_t par
             : "memory");
         if (ok) return true;
         if ((it & 255u) == 0) {
-            if (*c.abort) return false;
-            if (globaltimer_ns() - t0 > c.timeout_ns) return mbar_wait_slow(a, parity, c, where, tag);
+            if (ld_abort(c.abort_smem)) return false;
+            if (globaltimer_ns() - t0 > static_cast<uint64_t>(c.timeout_us) * 1000ull)
+                return mbar_wait_slow(a, parity, c, where, tag);
         }
     }
 }
-__device__ __forceinline__ bool mbar_wait_spin(uint64_t *bar, uint32_t parity, const WaitCtl &c, unsigned where,
+__device__ __forceinline__ bool mbar_wait_spin(uint64_t *bar, uint32_t parity, const WaitCtl c, unsigned where,
                                                unsigned tag = 0) {
     const uint32_t a = smem_u32(bar);
     if (mbar_try_wait(a, parity)) return true;
