@@ -9,13 +9,14 @@
 // intersect the band or the sink block of its query tile; no skipped tile is ever loaded.
 //
 // Work item = two query tiles of 128 rows (256 consecutive rows) of one (b, h).  The kernel is
-// persistent: one CTA per SM walks the items blockIdx.x, blockIdx.x + gridDim.x, ...  Items are
-// head-major (the items in flight share a few heads' key/value bands in L2) and, within a head,
-// longest-first (the last query pairs, whose windows are full, come first).  320 threads
+// persistent: one CTA per SM walks the items blockIdx.x, blockIdx.x + gridDim.x, ..., ordered
+// longest-first (the last query pairs of every head, whose windows are full, come first), so the short
+// items fall in the last rounds and the CTAs finish together.  320 threads
 // in four roles:
 //   warps 0-3 / 4-7  softmax + epilogue of query tile 0 / 1: thread r owns row r of its tile
 //              (= TMEM lane r);
-//   warp 8     TMA producer: per item the key-tile list (double-buffered), Q_0 and Q_1 (as soon as the
+//   warp 10    builds the key-tile list of each item into one of two buffers, one item ahead;
+//   warp 8     TMA producer: per item Q_0 and Q_1 (as soon as the
 //              previous item's last QK product is done), then K tiles into a 3-stage ring and V tiles
 //              into a 2-stage ring (128 rows x 128 bf16 each, two 64-column boxes with the 128-byte
 //              swizzle).  A K slot frees as soon as the QK products that read it complete, a V slot after
@@ -66,8 +67,8 @@ constexpr int NV = 2;                      // V tile stages (a slot frees after 
 constexpr uint32_t HALF_BYTES = 128 * 128;  // one 64-column half of a 128-row bf16 tile (16 KB)
 constexpr uint32_t TILE_BYTES = 2 * HALF_BYTES;
 constexpr int MAX_TILES = 64;
-constexpr int kThreads = 320;              // warps 0-3 / 4-7: softmax of query tile 0 / 1; 8: TMA; 9: MMA
-constexpr int kWarpTma = 8, kWarpMma = 9;
+constexpr int kThreads = 352;  // warps 0-3 / 4-7: softmax of query tile 0 / 1; 8: TMA; 9: MMA; 10: tile lists
+constexpr int kWarpTma = 8, kWarpMma = 9, kWarpList = 10;
 constexpr uint32_t kTmemCols = 512;
 // TMEM columns: S_0, S_1 (scores, later P in their first 64 columns), O_0, O_1 (accumulators)
 __host__ __device__ constexpr uint32_t col_s(int x) { return static_cast<uint32_t>(x) * 128u; }
@@ -223,7 +224,7 @@ __global__ void __launch_bounds__(kThreads, 1) swa_prefill_tc_kernel(const __gri
     uint64_t *ofull = pfull + 2;      // [2]: the last PV_x product of an item is done
     uint64_t *oempty = ofull + 2;     // [2]: O_x has been read by the epilogue (128 arrivals)
     uint64_t *lready = oempty + 2;    // [2]: tile list buffer b written (1 arrival)
-    uint64_t *lfree = lready + 2;     // [2]: tile list buffer b no longer read (8 softmax warps + MMA)
+    uint64_t *lfree = lready + 2;     // [2]: tile list buffer b no longer read (8 softmax warps, MMA, TMA)
     uint64_t *drain = lfree + 2;
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(sm + OFF_MISC);
     volatile int *abort_flag = reinterpret_cast<volatile int *>(sm + OFF_MISC + 4);
@@ -251,7 +252,7 @@ __global__ void __launch_bounds__(kThreads, 1) swa_prefill_tc_kernel(const __gri
             mbar_init(&ofull[x], 1);
             mbar_init(&oempty[x], BH_ROWS);
             mbar_init(&lready[x], 1);
-            mbar_init(&lfree[x], 9);
+            mbar_init(&lfree[x], 10);
         }
         mbar_init(drain, 1);
         mbar_init_fence();
@@ -280,22 +281,12 @@ __global__ void __launch_bounds__(kThreads, 1) swa_prefill_tc_kernel(const __gri
             for (int it = 0; fine; ++it) {
                 const int item = static_cast<int>(blockIdx.x) + it * G;
                 if (item >= P.n_items) break;
-                const int bh = item / P.n_qpairs;
-                const int row_start = (P.n_qpairs - 1 - item % P.n_qpairs) * BM;
-                const int q0 = P.pos0 + row_start;
-                const int qlast = P.pos0 + min(row_start + BM, P.L) - 1;
+                const int bh = item % P.BH;
+                const int row_start = (P.n_qpairs - 1 - item / P.BH) * BM;
                 const int b = it & 1;
-                if (it >= 2 && !mbar_wait(&lfree[b], ((it - 2) >> 1) & 1, wc, 12, it)) break;
-                Tile *tl = tiles_s + b * MAX_TILES;
-                const int n = build_tiles(tl, q0, qlast, P.pos0, P.s, P.m, P.w);
-                if (n < 1 || n > MAX_TILES) {
-                    atomicOr(&P.status->word, kDevBadArg);
-                    *abort_flag = 1;
-                    break;
-                }
-                mark_tiles(tl, n, q0, qlast, P.s, P.m);
-                ntiles_s[b] = n;
-                mbar_arrive(&lready[b]);  // release: the list is visible to whoever sees the phase complete
+                if (!mbar_wait(&lready[b], (it >> 1) & 1, wc, 15, it)) break;
+                const Tile *tl = tiles_s + b * MAX_TILES;
+                const int n = ntiles_s[b];
                 if (it >= 1 && !mbar_wait(qempty, (it - 1) & 1, wc, 13, it)) break;
                 uint8_t *qs = sm + OFF_Q;
                 mbar_arrive_expect_tx(qfull, 2 * TILE_BYTES);
@@ -330,11 +321,37 @@ __global__ void __launch_bounds__(kThreads, 1) swa_prefill_tc_kernel(const __gri
                     ++jv;
                     ++gv;
                 }
+                if (fine) mbar_arrive(&lfree[b]);  // the loads of this item no longer read its list
             }
             if (*abort_flag) {  // make sure no copy is still landing in shared memory
                 if (nq > 0) mbar_wait_drain(qfull, (nq - 1) & 1);
                 for (int g = (gk > NK ? gk - NK : 0); g < gk; ++g) mbar_wait_drain(&kfull[g % NK], (g / NK) & 1);
                 for (int g = (gv > NV ? gv - NV : 0); g < gv; ++g) mbar_wait_drain(&vfull[g % NV], (g / NV) & 1);
+            }
+        }
+    } else if (warp == kWarpList) {
+        // ------------------------------------------------------------------ tile lists
+        if (lane == 0) {
+            // list builder: the key-tile list of item it goes to buffer it & 1 as soon as the buffer's
+            // previous item (it - 2) has been released by every reader, one item ahead of the loads
+            for (int it = 0;; ++it) {
+                const int item = static_cast<int>(blockIdx.x) + it * G;
+                if (item >= P.n_items) break;
+                const int row_start = (P.n_qpairs - 1 - item / P.BH) * BM;
+                const int q0 = P.pos0 + row_start;
+                const int qlast = P.pos0 + min(row_start + BM, P.L) - 1;
+                const int b = it & 1;
+                if (it >= 2 && !mbar_wait(&lfree[b], ((it - 2) >> 1) & 1, wc, 12, it)) break;
+                Tile *tl = tiles_s + b * MAX_TILES;
+                const int n = build_tiles(tl, q0, qlast, P.pos0, P.s, P.m, P.w);
+                if (n < 1 || n > MAX_TILES) {
+                    atomicOr(&P.status->word, kDevBadArg);
+                    *abort_flag = 1;
+                    break;
+                }
+                mark_tiles(tl, n, q0, qlast, P.s, P.m);
+                ntiles_s[b] = n;
+                mbar_arrive(&lready[b]);  // release: the list is visible to whoever sees the phase complete
             }
         }
     } else if (warp == kWarpMma) {
@@ -353,7 +370,8 @@ __global__ void __launch_bounds__(kThreads, 1) swa_prefill_tc_kernel(const __gri
                 const int item = static_cast<int>(blockIdx.x) + it * G;
                 if (item >= P.n_items) break;
                 const int b = it & 1;
-                if (!mbar_wait(qfull, it & 1, wc, 2, it)) break;  // Q of this item; its tile list is written
+                if (!mbar_wait(&lready[b], (it >> 1) & 1, wc, 14, it)) break;  // the item's tile list
+                if (!mbar_wait(qfull, it & 1, wc, 2, it)) break;                 // Q of this item
                 const Tile *tl = tiles_s + b * MAX_TILES;
                 const int n = ntiles_s[b];
                 int last_used[2] = {-1, -1};
@@ -440,8 +458,8 @@ __global__ void __launch_bounds__(kThreads, 1) swa_prefill_tc_kernel(const __gri
         for (int it = 0; fine; ++it) {
             const int item = static_cast<int>(blockIdx.x) + it * G;
             if (item >= P.n_items) break;
-            const int bh = item / P.n_qpairs;
-            const int row_start = (P.n_qpairs - 1 - item % P.n_qpairs) * BM;
+            const int bh = item % P.BH;
+            const int row_start = (P.n_qpairs - 1 - item / P.BH) * BM;
             const int q0 = P.pos0 + row_start;
             const int qlast = P.pos0 + min(row_start + BM, P.L) - 1;
             const int t = q0 + x * BH_ROWS + r;  // absolute position of this thread's row
