@@ -11,16 +11,17 @@
 // Work item = two query tiles of 128 rows (256 consecutive rows) of one (b, h).  The kernel is
 // persistent: one CTA per SM walks the items blockIdx.x, blockIdx.x + gridDim.x, ..., ordered
 // longest-first (the last query pairs of every head, whose windows are full, come first), so the short
-// items fall in the last rounds and the CTAs finish together.  320 threads
-// in four roles:
+// items fall in the last rounds and the CTAs finish together.  352 threads in five roles:
 //   warps 0-3 / 4-7  softmax + epilogue of query tile 0 / 1: thread r owns row r of its tile
 //              (= TMEM lane r);
-//   warp 10    builds the key-tile list of each item into one of two buffers, one item ahead;
-//   warp 8     TMA producer: per item Q_0 and Q_1 (as soon as the
-//              previous item's last QK product is done), then K tiles into a 3-stage ring and V tiles
-//              into a 2-stage ring (128 rows x 128 bf16 each, two 64-column boxes with the 128-byte
-//              swizzle).  A K slot frees as soon as the QK products that read it complete, a V slot after
-//              its PV products, so K loads run up to three tiles ahead;
+//   warp 10    per item: builds the key-tile list into one of two buffers, one item ahead, loads Q_0 and
+//              Q_1 as soon as the previous item's last QK product is done, and prefetches the next
+//              item's Q into L2;
+//   warp 8     TMA producer: K tiles into a 3-stage ring and V tiles into a 2-stage ring (128 rows x
+//              128 bf16 each, two 64-column boxes with the 128-byte swizzle), as one stream over all
+//              items of the CTA.  A K slot frees as soon as the QK products that read it complete, a V
+//              slot after its PV products, so K loads run up to three tiles ahead, also into the next
+//              item;
 //   warp 9     MMA issuer (one thread).  Per key tile j: PV_0(j), QK_0(j+1), PV_1(j), QK_1(j+1), where
 //              QK_x(j) is S_x = Q_x K_j^T and PV_x(j) is O_x += P_x V_j with P_x (bf16) read by the MMA
 //              straight from tensor memory.  While the tensor cores work on one query tile, the softmax
@@ -167,6 +168,47 @@ __host__ __device__ void mark_tiles(Tile *tl, int n, int q0, int qlast, int s, i
     }
 }
 
+// Put an item's tiles in the order the MMA and softmax walk them: the first tile both query tiles use,
+// then the tiles only one of them uses, alternating (query tile 1's first), then the other shared tiles.
+// In position order query tile 0 alone needs the oldest band tile and query tile 1 alone the newest, so
+// one query tile would idle at the start of the item and the other at its end; in this order the
+// one-sided tiles sit next to each other, both query tiles end on the same tile and their epilogues
+// overlap.  The softmax does not depend on the order of the keys; the list stays a partition.
+__host__ __device__ void order_tiles(Tile *tl, int n) {
+    if (n < 2 || n > MAX_TILES) return;
+    // In place: position p takes the first remaining tile of the wanted kind (rotated into place, so
+    // each kind keeps its position order).  Kinds by flags & 6: 6 both query tiles, 4 query tile 1 only,
+    // 2 query tile 0 only.
+    int phase = 0;  // 0: first shared tile; 1: one-sided tiles, alternating; 2: shared; 3: the rest
+    int want1 = 4;  // in phase 1: the kind wanted next
+    for (int p = 0; p < n; ++p) {
+        int q = -1;
+        while (q < 0 && phase < 4) {
+            const int kind = phase == 0 ? 6 : phase == 1 ? want1 : phase == 2 ? 6 : -1;
+            for (int i = p; i < n && q < 0; ++i)
+                if (kind < 0 || (tl[i].flags & 6) == kind) q = i;
+            if (phase == 1) {
+                if (q < 0) {  // try the other one-sided kind before moving on
+                    const int other = want1 ^ 6;
+                    for (int i = p; i < n && q < 0; ++i)
+                        if ((tl[i].flags & 6) == other) q = i;
+                    if (q < 0) phase = 2;
+                } else {
+                    want1 ^= 6;  // 4 <-> 2
+                }
+            } else if (phase == 0) {
+                phase = 1;
+            } else if (q < 0) {
+                ++phase;
+            }
+        }
+        if (q < 0) break;
+        const Tile t = tl[q];
+        for (int i = q; i > p; --i) tl[i] = tl[i - 1];
+        tl[p] = t;
+    }
+}
+
 // Bits [lo, hi] of a 32-bit word (clipped to [0, 31]; 0 when the range is empty).
 __device__ __forceinline__ uint32_t range_bits(int lo, int hi) {
     lo = lo < 0 ? 0 : lo;
@@ -268,63 +310,78 @@ __global__ void __launch_bounds__(kThreads, 1) swa_prefill_tc_kernel(const __gri
     const WaitCtl wc{smem_u32(const_cast<int *>(abort_flag)), P.timeout_us, P.status};
 
     if (warp == kWarpTma) {
-        // ------------------------------------------------------------------ TMA producer
-        // Per item: the tile list (once its buffer is free), Q_0/Q_1 (once the previous item's last QK
-        // product is done), then the K and V tiles.  K tiles run up to NK tiles ahead of the V tiles: a
-        // K slot frees as soon as the QK products that read it are done, a V slot after its PV products.
+        // ------------------------------------------------------------------ TMA producer (K, V)
         if (lane == 0) {
-            tma_prefetch_desc(&P.tm_q);
             tma_prefetch_desc(&P.tm_k);
             tma_prefetch_desc(&P.tm_v);
-            int gk = 0, gv = 0, nq = 0;  // K, V tiles and Q pairs issued so far
-            bool fine = true;
-            for (int it = 0; fine; ++it) {
-                const int item = static_cast<int>(blockIdx.x) + it * G;
-                if (item >= P.n_items) break;
-                const int bh = item % P.BH;
-                const int row_start = (P.n_qpairs - 1 - item / P.BH) * BM;
-                const int b = it & 1;
-                if (!mbar_wait(&lready[b], (it >> 1) & 1, wc, 15, it)) break;
-                const Tile *tl = tiles_s + b * MAX_TILES;
-                const int n = ntiles_s[b];
-                if (it >= 1 && !mbar_wait(qempty, (it - 1) & 1, wc, 13, it)) break;
-                uint8_t *qs = sm + OFF_Q;
-                mbar_arrive_expect_tx(qfull, 2 * TILE_BYTES);
-                for (int x = 0; x < 2; ++x) {
-                    tma_load_3d(qs + x * TILE_BYTES, &P.tm_q, qfull, 0, row_start + x * BH_ROWS, bh);
-                    tma_load_3d(qs + x * TILE_BYTES + HALF_BYTES, &P.tm_q, qfull, 64, row_start + x * BH_ROWS, bh);
-                }
-                ++nq;
-                int jk = 0, jv = 0;
-                while (fine && jv < n) {
-                    while (jk < n && jk < jv + NK) {
-                        const int st = gk % NK;
-                        if (!mbar_wait(&kempty[st], ((gk / NK) & 1) ^ 1, wc, 1, jk)) { fine = false; break; }
-                        const Tile T = tl[jk];
-                        const CUtensorMap *mk = (T.flags & 1) ? &P.tm_kc : &P.tm_k;
-                        uint8_t *ks = sm + OFF_K + st * TILE_BYTES;
-                        mbar_arrive_expect_tx(&kfull[st], TILE_BYTES);
-                        tma_load_3d(ks, mk, &kfull[st], 0, T.row0, bh);
-                        tma_load_3d(ks + HALF_BYTES, mk, &kfull[st], 64, T.row0, bh);
-                        ++jk;
-                        ++gk;
+            // One stream of key tiles over all items of this CTA: the K cursor runs up to NK tiles ahead of
+            // the V cursor, across item boundaries, so the next item's first K tiles load while the current
+            // item's last V tiles are still in flight.
+            int gk = 0, gv = 0;                     // K, V tiles issued so far
+            int itk = -1, jk = 0, nk = 0, bhk = 0;  // K cursor: item, tile, tile count, head
+            int itv = 0, jv = 0;                    // V cursor
+            bool k_done = false, fine = true;
+            while (fine) {
+                while (!k_done && gk < gv + NK) {
+                    if (jk == nk) {  // next item for the K cursor
+                        // at most one item ahead of V: the list of item itv + 2 shares a buffer with item itv
+                        if (itk > itv) break;
+                        ++itk;
+                        const int item = static_cast<int>(blockIdx.x) + itk * G;
+                        if (item >= P.n_items) {
+                            k_done = true;
+                            break;
+                        }
+                        if (!mbar_wait(&lready[itk & 1], (itk >> 1) & 1, wc, 15, itk)) {
+                            fine = false;
+                            break;
+                        }
+                        nk = ntiles_s[itk & 1];
+                        bhk = item % P.BH;
+                        jk = 0;
+                        continue;
                     }
-                    if (!fine) break;
-                    const int sv = gv % NV;
-                    if (!mbar_wait(&vempty[sv], ((gv / NV) & 1) ^ 1, wc, 9, jv)) { fine = false; break; }
-                    const Tile T = tl[jv];
-                    const CUtensorMap *mv = (T.flags & 1) ? &P.tm_vc : &P.tm_v;
-                    uint8_t *vs = sm + OFF_V + sv * TILE_BYTES;
-                    mbar_arrive_expect_tx(&vfull[sv], TILE_BYTES);
-                    tma_load_3d(vs, mv, &vfull[sv], 0, T.row0, bh);
-                    tma_load_3d(vs + HALF_BYTES, mv, &vfull[sv], 64, T.row0, bh);
-                    ++jv;
-                    ++gv;
+                    const int st = gk % NK;
+                    if (!mbar_wait(&kempty[st], ((gk / NK) & 1) ^ 1, wc, 1, jk)) {
+                        fine = false;
+                        break;
+                    }
+                    const Tile T = tiles_s[(itk & 1) * MAX_TILES + jk];
+                    const CUtensorMap *mk = (T.flags & 1) ? &P.tm_kc : &P.tm_k;
+                    uint8_t *ks = sm + OFF_K + st * TILE_BYTES;
+                    mbar_arrive_expect_tx(&kfull[st], TILE_BYTES);
+                    tma_load_3d(ks, mk, &kfull[st], 0, T.row0, bhk);
+                    tma_load_3d(ks + HALF_BYTES, mk, &kfull[st], 64, T.row0, bhk);
+                    ++jk;
+                    ++gk;
                 }
-                if (fine) mbar_arrive(&lfree[b]);  // the loads of this item no longer read its list
+                if (!fine) break;
+                if (gv == gk) break;  // every issued K tile has its V tile: nothing left
+                // the V cursor follows the K cursor tile by tile (its item's list was waited for by K)
+                const int nv = ntiles_s[itv & 1];
+                if (jv == nv) {
+                    mbar_arrive(&lfree[itv & 1]);  // the loads of item itv no longer read its list
+                    ++itv;
+                    jv = 0;
+                    continue;
+                }
+                const int item = static_cast<int>(blockIdx.x) + itv * G;
+                const int sv = gv % NV;
+                if (!mbar_wait(&vempty[sv], ((gv / NV) & 1) ^ 1, wc, 9, jv)) {
+                    fine = false;
+                    break;
+                }
+                const Tile T = tiles_s[(itv & 1) * MAX_TILES + jv];
+                const CUtensorMap *mv = (T.flags & 1) ? &P.tm_vc : &P.tm_v;
+                uint8_t *vs = sm + OFF_V + sv * TILE_BYTES;
+                mbar_arrive_expect_tx(&vfull[sv], TILE_BYTES);
+                tma_load_3d(vs, mv, &vfull[sv], 0, T.row0, item % P.BH);
+                tma_load_3d(vs + HALF_BYTES, mv, &vfull[sv], 64, T.row0, item % P.BH);
+                ++jv;
+                ++gv;
             }
+            if (fine && jv > 0 && jv == ntiles_s[itv & 1]) mbar_arrive(&lfree[itv & 1]);
             if (*abort_flag) {  // make sure no copy is still landing in shared memory
-                if (nq > 0) mbar_wait_drain(qfull, (nq - 1) & 1);
                 for (int g = (gk > NK ? gk - NK : 0); g < gk; ++g) mbar_wait_drain(&kfull[g % NK], (g / NK) & 1);
                 for (int g = (gv > NV ? gv - NV : 0); g < gv; ++g) mbar_wait_drain(&vfull[g % NV], (g / NV) & 1);
             }
@@ -332,11 +389,15 @@ __global__ void __launch_bounds__(kThreads, 1) swa_prefill_tc_kernel(const __gri
     } else if (warp == kWarpList) {
         // ------------------------------------------------------------------ tile lists
         if (lane == 0) {
-            // list builder: the key-tile list of item it goes to buffer it & 1 as soon as the buffer's
-            // previous item (it - 2) has been released by every reader, one item ahead of the loads
+            // Per item: the key-tile list goes to buffer it & 1 as soon as the buffer's previous item
+            // (it - 2) has been released by every reader; then Q_0, Q_1 of the item, as soon as the previous
+            // item's last QK product is done (about two key tiles before that item ends), and the next
+            // item's Q into L2, so that its load does not wait for DRAM.
+            int nq = 0;
             for (int it = 0;; ++it) {
                 const int item = static_cast<int>(blockIdx.x) + it * G;
                 if (item >= P.n_items) break;
+                const int bh = item % P.BH;
                 const int row_start = (P.n_qpairs - 1 - item / P.BH) * BM;
                 const int q0 = P.pos0 + row_start;
                 const int qlast = P.pos0 + min(row_start + BM, P.L) - 1;
@@ -350,9 +411,27 @@ __global__ void __launch_bounds__(kThreads, 1) swa_prefill_tc_kernel(const __gri
                     break;
                 }
                 mark_tiles(tl, n, q0, qlast, P.s, P.m);
+                order_tiles(tl, n);
                 ntiles_s[b] = n;
                 mbar_arrive(&lready[b]);  // release: the list is visible to whoever sees the phase complete
+                if (it >= 1 && !mbar_wait(qempty, (it - 1) & 1, wc, 13, it)) break;
+                uint8_t *qs = sm + OFF_Q;
+                mbar_arrive_expect_tx(qfull, 2 * TILE_BYTES);
+                for (int x = 0; x < 2; ++x) {
+                    tma_load_3d(qs + x * TILE_BYTES, &P.tm_q, qfull, 0, row_start + x * BH_ROWS, bh);
+                    tma_load_3d(qs + x * TILE_BYTES + HALF_BYTES, &P.tm_q, qfull, 64, row_start + x * BH_ROWS, bh);
+                }
+                ++nq;
+                const int nitem = item + G;
+                if (nitem < P.n_items) {
+                    const int nrow = (P.n_qpairs - 1 - nitem / P.BH) * BM;
+                    for (int x = 0; x < 2; ++x) {
+                        tma_prefetch_3d(&P.tm_q, 0, nrow + x * BH_ROWS, nitem % P.BH);
+                        tma_prefetch_3d(&P.tm_q, 64, nrow + x * BH_ROWS, nitem % P.BH);
+                    }
+                }
             }
+            if (*abort_flag && nq > 0) mbar_wait_drain(qfull, (nq - 1) & 1);  // no copy may still be landing
         }
     } else if (warp == kWarpMma) {
         // ------------------------------------------------------------------ MMA issuer
@@ -792,6 +871,7 @@ int prefill_tile_plan(int q0, int q1, int pos0, int w, int s, int *out, int max_
     tc::Tile tl[tc::MAX_TILES];
     const int n = tc::build_tiles(tl, q0, q1, pos0, s, w - s, w);
     tc::mark_tiles(tl, n, q0, q1, s, w - s);
+    tc::order_tiles(tl, n);
     for (int i = 0; i < n && i < max_tiles && i < tc::MAX_TILES; ++i) {
         out[5 * i + 0] = tl[i].flags & 1;
         out[5 * i + 1] = tl[i].row0;

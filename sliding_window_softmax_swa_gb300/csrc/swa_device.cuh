@@ -59,6 +59,31 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
     return ok != 0;
 }
 
+// Non-blocking check of a phase (never suspends the thread).
+__device__ __forceinline__ bool mbar_test(uint32_t bar, uint32_t parity) {
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(bar), "r"(parity)
+        : "memory");
+    return ok != 0;
+}
+// Like mbar_try_wait, but the thread is suspended for at most about `hint_ns` nanoseconds.
+__device__ __forceinline__ bool mbar_try_wait_hint(uint32_t bar, uint32_t parity, uint32_t hint_ns) {
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(bar), "r"(parity), "r"(hint_ns)
+        : "memory");
+    return ok != 0;
+}
+
 // Per-device status record: the error word the kernels OR bits into, and where the first bounded wait
 // of the device ran out: site | tag << 8 | warp << 20 | blockIdx.x << 32 | blockIdx.y << 48.
 struct DeviceStatus {
@@ -85,6 +110,17 @@ __device__ __forceinline__ void st_abort(uint32_t a) {
     asm volatile("st.volatile.shared.u32 [%0], %1;" ::"r"(a), "r"(1) : "memory");
 }
 
+// A wait of this CTA ran out: set the CTA's abort flag and record the timeout (site `where`) in the
+// device status word, and where it happened in the first-timeout record.
+static __device__ __noinline__ void wait_gave_up(const WaitCtl c, unsigned where, unsigned tag) {
+    st_abort(c.abort_smem);
+    atomicOr(&c.status->word, kDevTimeout | ((where & 0xFFu) << kWhereShift));
+    const unsigned long long rec = (where & 0xFFull) | ((tag & 0xFFFull) << 8) |
+                                   ((threadIdx.x >> 5 & 0xFFFull) << 20) | ((blockIdx.x & 0xFFFFull) << 32) |
+                                   ((blockIdx.y & 0xFFFFull) << 48);
+    atomicCAS(&c.status->info, 0ull, rec);
+}
+
 // Wait until the phase with the given parity of `bar` has completed.  Returns false when the wait
 // ran out (or another wait of the CTA did); the caller must then stop its pipeline role.
 static __device__ __noinline__ bool mbar_wait_slow(uint32_t a, uint32_t parity, const WaitCtl c, unsigned where,
@@ -96,12 +132,7 @@ static __device__ __noinline__ bool mbar_wait_slow(uint32_t a, uint32_t parity, 
         if ((it & 31u) == 0) {
             if (ld_abort(c.abort_smem)) return false;
             if (globaltimer_ns() - t0 > limit) {
-                st_abort(c.abort_smem);
-                atomicOr(&c.status->word, kDevTimeout | ((where & 0xFFu) << kWhereShift));
-                const unsigned long long rec =
-                    (where & 0xFFull) | ((tag & 0xFFFull) << 8) | ((threadIdx.x >> 5 & 0xFFFull) << 20) |
-                    ((blockIdx.x & 0xFFFFull) << 32) | ((blockIdx.y & 0xFFFFull) << 48);
-                atomicCAS(&c.status->info, 0ull, rec);
+                wait_gave_up(c, where, tag);
                 return false;
             }
         }
@@ -167,6 +198,14 @@ __device__ __forceinline__ void tma_load_3d(void *dst, const CUtensorMap *m, uin
         " [%0], [%1, {%3, %4, %5}], [%2];" ::"r"(smem_u32(dst)),
         "l"(reinterpret_cast<uint64_t>(m)), "r"(smem_u32(bar)), "r"(x), "r"(y), "r"(z)
         : "memory");
+}
+
+// Prefetch a 3-D tile of global memory into L2 (no shared memory involved, no completion to wait for).
+__device__ __forceinline__ void tma_prefetch_3d(const CUtensorMap *m, int x, int y, int z) {
+    asm volatile("cp.async.bulk.prefetch.tensor.3d.L2.global.tile [%0, {%1, %2, %3}];" ::"l"(
+                     reinterpret_cast<uint64_t>(m)),
+                 "r"(x), "r"(y), "r"(z)
+                 : "memory");
 }
 
 // 3-D tiled store from shared memory (bulk-group completion); rows outside the tensor are clipped.
