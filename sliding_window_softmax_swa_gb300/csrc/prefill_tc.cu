@@ -223,6 +223,31 @@ __device__ __forceinline__ float ex2(float x) {
     return y;
 }
 
+// Maximum of three floats in one instruction (a NaN operand is ignored, as in fmaxf).
+__device__ __forceinline__ float fmax3(float a, float b, float c) {
+    float d;
+    asm("max.f32 %0, %1, %2, %3;" : "=f"(d) : "f"(a), "f"(b), "f"(c));
+    return d;
+}
+
+// Packed fp32 pairs (one instruction for two lanes of work): d = a * b + c and d = a + b, each lane
+// rounded like the scalar fmaf / add.
+__device__ __forceinline__ void ffma2(float &d0, float &d1, float a0, float a1, float b0, float b1, float c0,
+                                      float c1) {
+    asm("{\n\t.reg .b64 a, b, c, d;\n\t"
+        "mov.b64 a, {%2, %3};\n\tmov.b64 b, {%4, %5};\n\tmov.b64 c, {%6, %7};\n\t"
+        "fma.rn.f32x2 d, a, b, c;\n\tmov.b64 {%0, %1}, d;\n\t}"
+        : "=f"(d0), "=f"(d1)
+        : "f"(a0), "f"(a1), "f"(b0), "f"(b1), "f"(c0), "f"(c1));
+}
+__device__ __forceinline__ void fadd2(float &d0, float &d1, float a0, float a1, float b0, float b1) {
+    asm("{\n\t.reg .b64 a, b, d;\n\t"
+        "mov.b64 a, {%2, %3};\n\tmov.b64 b, {%4, %5};\n\t"
+        "add.rn.f32x2 d, a, b;\n\tmov.b64 {%0, %1}, d;\n\t}"
+        : "=f"(d0), "=f"(d1)
+        : "f"(a0), "f"(a1), "f"(b0), "f"(b1));
+}
+
 // Bounded wait that ignores the CTA abort flag: used only to drain copies/MMAs before exit.
 __device__ __noinline__ bool mbar_wait_drain(uint64_t *bar, uint32_t parity) {
     const uint32_t a = smem_u32(bar);
@@ -574,13 +599,15 @@ __global__ void __launch_bounds__(kThreads, 1) swa_prefill_tc_kernel(const __gri
 #pragma unroll
                     for (int c = 0; c < BN; ++c) sv[c] = (mw[c >> 5] & (1u << (c & 31))) ? sv[c] : -INFINITY;
                 }
-                float mx8[8];
+                float mx4[4];
 #pragma unroll
-                for (int i = 0; i < 8; ++i) mx8[i] = sv[i];
+                for (int i = 0; i < 4; ++i) mx4[i] = fmax3(sv[i], sv[4 + i], sv[8 + i]);
 #pragma unroll
-                for (int c = 8; c < BN; ++c) mx8[c & 7] = fmaxf(mx8[c & 7], sv[c]);
-                const float mx = fmaxf(fmaxf(fmaxf(mx8[0], mx8[1]), fmaxf(mx8[2], mx8[3])),
-                                       fmaxf(fmaxf(mx8[4], mx8[5]), fmaxf(mx8[6], mx8[7]))) * sl2;
+                for (int c = 12; c < BN - 4; c += 8)
+#pragma unroll
+                    for (int i = 0; i < 4; ++i) mx4[i] = fmax3(mx4[i], sv[c + i], sv[c + 4 + i]);
+                const float mx = fmax3(fmax3(mx4[0], mx4[1], sv[BN - 4]), fmax3(mx4[2], mx4[3], sv[BN - 3]),
+                                       fmaxf(sv[BN - 2], sv[BN - 1])) * sl2;
                 float alpha = 1.f;
                 bool resc = false;
                 const float mnew = fmaxf(mrun, mx);
@@ -615,9 +642,11 @@ __global__ void __launch_bounds__(kThreads, 1) swa_prefill_tc_kernel(const __gri
 #pragma unroll
                     for (int i = 0; i < 32; ++i) {
                         const int c = 64 * h + 2 * i;
-                        const float p0 = ex2(fmaf(sv[c], sl2, nmu)), p1 = ex2(fmaf(sv[c + 1], sl2, nmu));
-                        rs4[(2 * i) & 3] += p0;
-                        rs4[(2 * i + 1) & 3] += p1;
+                        float a0, a1;
+                        ffma2(a0, a1, sv[c], sv[c + 1], sl2, sl2, nmu, nmu);
+                        const float p0 = ex2(a0), p1 = ex2(a1);
+                        const int k = (i & 1) * 2;
+                        fadd2(rs4[k], rs4[k + 1], rs4[k], rs4[k + 1], p0, p1);
                         pk[i] = pack_bf16x2(p0, p1);
                     }
                     __syncwarp();
