@@ -82,6 +82,10 @@ int swa_sink_prefill(const void *q, const void *k, const void *v, void *o, float
  *   k_cache, v_cache : [B, H, w, d] scratch cache owned by the caller; contents on entry are ignored,
  *             on exit it holds the cache state after position L-1 (ready for streaming decode).
  *   chunk   : rows per chunk, >= 1.
+ * Asynchronous on `stream`.  The (b, h) rows are independent, so the library may split them into up
+ * to 2 groups that walk the chunks on streams of its own (created once per device), forked from and
+ * joined back to `stream` with events: the call allocates no device memory and can be captured into a
+ * CUDA graph like a single-stream call.
  */
 int swa_sink_prefill_chunked(const void *q, const void *k, const void *v, void *o, float *lse,
                              void *k_cache, void *v_cache,

@@ -169,6 +169,37 @@ extern "C" int swa_sink_prefill(const void *q, const void *k, const void *v, voi
                         static_cast<cudaStream_t>(stream));
 }
 
+// Streams and events of the chunked prefill's row groups: created once per device and kept (no
+// allocation of device memory; a chunked prefill call only records and waits on events).
+constexpr int kChunkGroups = 2;
+constexpr int kChunkGroupMinRows = 8;  // (b, h) rows per group at least
+struct ChunkStreams {
+    cudaStream_t stream[kChunkGroups];
+    cudaEvent_t fork;
+    cudaEvent_t join[kChunkGroups];
+};
+static ChunkStreams *chunk_streams() {
+    static std::mutex mu;
+    static ChunkStreams *per_dev[64] = {nullptr};
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return nullptr;
+    std::lock_guard<std::mutex> lk(mu);
+    if (!per_dev[dev]) {
+        ChunkStreams *c = new ChunkStreams();
+        bool ok = cudaEventCreateWithFlags(&c->fork, cudaEventDisableTiming) == cudaSuccess;
+        for (int g = 0; ok && g < kChunkGroups; ++g) {
+            ok = cudaStreamCreateWithFlags(&c->stream[g], cudaStreamNonBlocking) == cudaSuccess &&
+                 cudaEventCreateWithFlags(&c->join[g], cudaEventDisableTiming) == cudaSuccess;
+        }
+        if (!ok) {  // fall back to one stream (the caller's); nothing is released on this rare path
+            delete c;
+            return nullptr;
+        }
+        per_dev[dev] = c;
+    }
+    return per_dev[dev];
+}
+
 extern "C" int swa_sink_prefill_chunked(const void *q, const void *k, const void *v, void *o, float *lse,
                                         void *k_cache, void *v_cache, int B, int H, int64_t L, int d, int w, int s,
                                         float scale, int64_t chunk, int dtype, void *stream) {
@@ -183,18 +214,47 @@ extern "C" int swa_sink_prefill_chunked(const void *q, const void *k, const void
     const int es = esize_of(dtype);
     const size_t row_bytes = static_cast<size_t>(d) * es;
     cudaStream_t st = static_cast<cudaStream_t>(stream);
-    for (int64_t c0 = 0; c0 < L; c0 += chunk) {
-        const int64_t n = (L - c0 < chunk) ? (L - c0) : chunk;
-        const size_t off = static_cast<size_t>(c0) * row_bytes;
-        const char *qc = static_cast<const char *>(q) + off;
-        const char *kc = static_cast<const char *>(k) + off;
-        const char *vc = static_cast<const char *>(v) + off;
-        char *oc = static_cast<char *>(o) + off;
-        float *lc = lse ? lse + c0 : nullptr;
-        rc = prefill_impl(qc, kc, vc, oc, lc, k_cache, v_cache, c0, B, H, n, d, w, s, scale, dtype, L, st);
-        if (rc) return rc;
-        rc = launch_kv_write(k_cache, v_cache, kc, vc, B * H, d, w, s, c0, n, L, es, st);
-        if (rc) return rc;
+    // The (b, h) rows are independent; only the chunks of one row depend on each other, through its
+    // cache.  The rows are split into groups, each walking all chunks on its own stream, so that one
+    // group's next chunk fills the SMs that another group's chunk leaves idle at its end (a chunk of one
+    // group alone is a few waves of work items, the last one partly empty).
+    const int BH = B * H;
+    ChunkStreams *cs = chunk_streams();
+    const int groups = (cs && BH >= 2 * kChunkGroupMinRows) ? (BH / kChunkGroupMinRows < kChunkGroups ? BH / kChunkGroupMinRows : kChunkGroups) : 1;
+    if (groups > 1) {
+        cudaError_t e = cudaEventRecord(cs->fork, st);
+        for (int g = 0; e == cudaSuccess && g < groups; ++g) e = cudaStreamWaitEvent(cs->stream[g], cs->fork, 0);
+        if (e != cudaSuccess) return fail(SWA_ERR_CUDA, "chunked prefill fork: %s", cudaGetErrorString(e));
+    }
+    for (int g = 0; g < groups; ++g) {
+        const int r0 = static_cast<int>(static_cast<int64_t>(BH) * g / groups);
+        const int r1 = static_cast<int>(static_cast<int64_t>(BH) * (g + 1) / groups);
+        cudaStream_t gs = groups > 1 ? cs->stream[g] : st;
+        const size_t seq_off = static_cast<size_t>(r0) * static_cast<size_t>(L) * row_bytes;  // rows of q, k, v, o
+        const size_t cache_off = static_cast<size_t>(r0) * static_cast<size_t>(w) * row_bytes;
+        void *kcg = static_cast<char *>(k_cache) + cache_off;
+        void *vcg = static_cast<char *>(v_cache) + cache_off;
+        for (int64_t c0 = 0; c0 < L; c0 += chunk) {
+            const int64_t n = (L - c0 < chunk) ? (L - c0) : chunk;
+            const size_t off = seq_off + static_cast<size_t>(c0) * row_bytes;
+            const char *qc = static_cast<const char *>(q) + off;
+            const char *kc = static_cast<const char *>(k) + off;
+            const char *vc = static_cast<const char *>(v) + off;
+            char *oc = static_cast<char *>(o) + off;
+            float *lc = lse ? lse + static_cast<int64_t>(r0) * L + c0 : nullptr;
+            // prefill_impl treats its B as the number of (b, h) rows when H = 1
+            rc = prefill_impl(qc, kc, vc, oc, lc, kcg, vcg, c0, r1 - r0, 1, n, d, w, s, scale, dtype, L, gs);
+            if (rc) return rc;
+            rc = launch_kv_write(kcg, vcg, kc, vc, r1 - r0, d, w, s, c0, n, L, es, gs);
+            if (rc) return rc;
+        }
+    }
+    if (groups > 1) {
+        for (int g = 0; g < groups; ++g) {
+            cudaError_t e = cudaEventRecord(cs->join[g], cs->stream[g]);
+            if (e == cudaSuccess) e = cudaStreamWaitEvent(st, cs->join[g], 0);
+            if (e != cudaSuccess) return fail(SWA_ERR_CUDA, "chunked prefill join: %s", cudaGetErrorString(e));
+        }
     }
     return SWA_OK;
 }

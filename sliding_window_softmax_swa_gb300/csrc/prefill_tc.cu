@@ -63,7 +63,7 @@ constexpr int BH_ROWS = 128;               // query rows per query tile (= TMEM 
 constexpr int BM = 2 * BH_ROWS;            // query rows per CTA: two query tiles
 constexpr int BN = 128;                    // keys per key tile
 constexpr int HD = 128;                    // head dimension
-constexpr int NK = 3;                      // K tile stages (a slot frees after its QK products)
+constexpr int NK = 2;                      // K tile stages (a slot frees after its QK products)
 constexpr int NV = 2;                      // V tile stages (a slot frees after its PV products)
 constexpr uint32_t HALF_BYTES = 128 * 128;  // one 64-column half of a 128-row bf16 tile (16 KB)
 constexpr uint32_t TILE_BYTES = 2 * HALF_BYTES;
@@ -682,10 +682,11 @@ __global__ void __launch_bounds__(kThreads, 1) swa_prefill_tc_kernel(const __gri
             mbar_arrive(&oempty[x]);
             if (t <= qlast) {
                 const int64_t row = static_cast<int64_t>(bh) * P.seq_stride + row_start + x * BH_ROWS + r;
-                uint4 *dst = reinterpret_cast<uint4 *>(static_cast<__nv_bfloat16 *>(P.o) + row * HD);
+                uint8_t *dst = reinterpret_cast<uint8_t *>(static_cast<__nv_bfloat16 *>(P.o) + row * HD);
 #pragma unroll
-                for (int i = 0; i < HD / 8; ++i)
-                    dst[i] = make_uint4(ob[4 * i], ob[4 * i + 1], ob[4 * i + 2], ob[4 * i + 3]);
+                for (int i = 0; i < HD / 16; ++i)
+                    st_global_v8(dst + 32 * i, ob[8 * i], ob[8 * i + 1], ob[8 * i + 2], ob[8 * i + 3], ob[8 * i + 4],
+                                 ob[8 * i + 5], ob[8 * i + 6], ob[8 * i + 7]);
                 if (P.lse) P.lse[row] = (mrun + log2f(lrun)) * 0.69314718055994531f;
             }
         }

@@ -416,6 +416,14 @@ __device__ __forceinline__ void st_shared_v4(uint32_t addr, uint32_t a, uint32_t
 // Byte offset of element (row r, column c) of a [rows x 64] bf16 block stored with the 128-byte
 // swizzle (rows of 128 bytes; the 16-byte chunk index XORed with r mod 8).  The block must start on
 // a 1024-byte boundary.  This is the layout TMA writes with CU_TENSOR_MAP_SWIZZLE_128B.
+// 32-byte global store (one full sector per thread); `p` must be 32-byte aligned.
+__device__ __forceinline__ void st_global_v8(void *p, uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3, uint32_t a4,
+                                             uint32_t a5, uint32_t a6, uint32_t a7) {
+    asm volatile("st.global.v8.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8};" ::"l"(p), "r"(a0), "r"(a1), "r"(a2),
+                 "r"(a3), "r"(a4), "r"(a5), "r"(a6), "r"(a7)
+                 : "memory");
+}
+
 __host__ __device__ __forceinline__ uint32_t sw128_offset(uint32_t r, uint32_t c) {
     return r * 128u + ((((c >> 3) ^ r) & 7u) << 4) + ((c & 7u) << 1);
 }

@@ -97,7 +97,10 @@ def test_prefill_with_cache(dtype, d, L, w, s, pos0):
                                            (640, 128, 0, 128, 2), (500, 200, 4, 1000, 2), (1024, 512, 4, 96, 2),
                                            # sink rescales make softmax warps drift a tile apart: a race here
                                            # once mixed P-ready arrivals of two tiles on one barrier
-                                           (8192, 1024, 4, 1024, 4), (6144, 2048, 4, 2048, 2)])
+                                           (8192, 1024, 4, 1024, 4), (6144, 2048, 4, 2048, 2),
+                                           # 17 (b, h) rows: split into two uneven row groups that walk the
+                                           # chunks on separate streams
+                                           (700, 256, 4, 200, 17)])
 def test_chunked_prefill(L, w, s, chunk, H):
     swa = require_gpu()
     B, d = 1, 128
