@@ -1,6 +1,7 @@
-"""Parity at the full workload sizes, in the launch configuration the benchmark times, on sampled
-outputs the oracle computes row by row (sampled heads x row blocks at the sequence start, around the
-window edge, in the middle, at chunk boundaries and at the ragged end)."""
+"""Parity at the full workload sizes, in the launch configuration the benchmark times: the primary
+prefill in full; for the two B=2 L=32768 prefills every row of four heads and every row with t < w + 128
+in every head; for the chunked prefill every row of chunks 0, 1, 2 and 31 and the rows around every chunk
+boundary in every head; for decode every step of 8 (b, h) rows."""
 import math
 
 import numpy as np
@@ -25,23 +26,37 @@ def check_samples(name, o, lse, q, k, v, wl, heads, blocks):
         assert np.abs(lf[bh, r0:r1].cpu().double().numpy() - l_ref).max() < LSE_ABS
 
 
-@pytest.mark.parametrize("name,heads,blocks", [
-    ("prefill_llama7b_L8192_w1024_s4", [0, 17, 31], [(0, 256), (894, 1154), (4000, 4128), (7992, 8192)]),
-    ("prefill_mistral_B2_L32768_w4096_s0", [0, 33, 63], [(0, 256), (3966, 4226), (16384, 16512), (32568, 32768)]),
-    ("prefill_mistral_B2_L32768_w4096_s4", [1, 40, 62], [(0, 256), (3966, 4226), (16384, 16512), (32568, 32768)]),
-])
-def test_full_size_prefill(name, heads, blocks):
-    swa = require_gpu()
-    wl = swa_inputs.WORKLOADS[name]
+def _full_size_prefill_outputs(swa, wl):
     q, k, v = swa_inputs.workload_inputs(wl, "cuda")
     lse = torch.empty((wl.B, wl.H, wl.L), dtype=torch.float32, device="cuda")
     o = swa.swa_sink_prefill(q, k, v, wl.w, wl.s, lse=lse)
     assert swa.swa_device_status() == swa.SWA_OK, swa.last_error()
     assert torch.isfinite(o).all()
-    check_samples(name, o, lse, q, k, v, wl, heads, blocks)
+    return q, k, v, o, lse
+
+
+def test_full_size_prefill_llama7b_every_row():
+    # the primary workload in full: every row of every head against the oracle
+    swa = require_gpu()
+    wl = swa_inputs.WORKLOADS["prefill_llama7b_L8192_w1024_s4"]
+    q, k, v, o, lse = _full_size_prefill_outputs(swa, wl)
+    check_samples(wl.name, o, lse, q, k, v, wl, list(range(wl.B * wl.H)), [(0, wl.L)])
+
+
+@pytest.mark.parametrize("name", ["prefill_mistral_B2_L32768_w4096_s0", "prefill_mistral_B2_L32768_w4096_s4"])
+def test_full_size_prefill_mistral(name):
+    # every row of four heads (both batch entries), and in every head every row with t < w + 128 (the
+    # rows whose key set is still growing, plus the first full-window tile)
+    swa = require_gpu()
+    wl = swa_inputs.WORKLOADS[name]
+    q, k, v, o, lse = _full_size_prefill_outputs(swa, wl)
+    check_samples(name, o, lse, q, k, v, wl, [0, 21, 42, 63], [(0, wl.L)])
+    others = [bh for bh in range(wl.B * wl.H) if bh not in (0, 21, 42, 63)]
+    check_samples(name, o, lse, q, k, v, wl, others, [(0, wl.w + 128)])
 
 
 def test_full_size_chunked_prefill():
+    # every row of chunks 0, 1, 2 and 31 in every head, and the rows around every chunk boundary
     swa = require_gpu()
     wl = swa_inputs.WORKLOADS["chunked_mistral_L131072_w4096_s4_C4096"]
     q, k, v = swa_inputs.workload_inputs(wl, "cuda")
@@ -52,9 +67,9 @@ def test_full_size_chunked_prefill():
     assert swa.swa_device_status() == swa.SWA_OK, swa.last_error()
     assert torch.isfinite(o).all()
     C = wl.chunk
-    blocks = [(0, 256), (C - 64, C + 192), (2 * C - 100, 2 * C + 100), (16 * C - 64, 16 * C + 64),
-              (31 * C - 1, 31 * C + 129), (wl.L - 256, wl.L)]
-    check_samples("chunked", o, lse, q, k, v, wl, [0, 13, 31], blocks)
+    nch = wl.L // C
+    blocks = [(0, 3 * C), ((nch - 1) * C, nch * C)] + [(c * C - 4, c * C + 4) for c in range(3, nch - 1)]
+    check_samples("chunked", o, lse, q, k, v, wl, list(range(wl.B * wl.H)), blocks)
 
 
 def test_full_size_streaming_decode():
