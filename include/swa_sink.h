@@ -73,6 +73,25 @@ int swa_sink_prefill(const void *q, const void *k, const void *v, void *o, float
                      int dtype, void *stream);
 
 /*
+ * swa_sink_prefill_host -- swa_sink_prefill (pos0 = 0) of q, k, v held in host memory, with the output
+ * copied back to host memory: the end-to-end form of the prefill of "带 Sink 的滑动窗口注意力".  The
+ * (b, h) rows are independent, so they are split into groups whose host-to-device copies, prefill and
+ * device-to-host copies are pipelined on streams of the library (created once per device, forked from
+ * and joined back to `stream` with events); per row the result is the same as swa_sink_prefill's.
+ *
+ *   q_h, k_h, v_h : host [B, H, L, d] inputs; o_h : host [B, H, L, d] output; lse_h : optional host
+ *             [B, H, L] fp32 output (NULL to skip).  Page-locked (pinned) host memory lets the copies
+ *             overlap the compute; pageable memory is correct but serialises them.
+ *   q_d, k_d, v_d, o_d : caller-owned device buffers of [B, H, L, d]; lse_d : device [B, H, L] fp32,
+ *             required when lse_h is given.  The library allocates nothing.
+ *   Other arguments as swa_sink_prefill.  Asynchronous on `stream`: the host buffers must stay valid
+ *   and unchanged until `stream` has reached this point.
+ */
+int swa_sink_prefill_host(const void *q_h, const void *k_h, const void *v_h, void *o_h, float *lse_h,
+                          void *q_d, void *k_d, void *v_d, void *o_d, float *lse_d,
+                          int B, int H, int64_t L, int d, int w, int s, float scale, int dtype, void *stream);
+
+/*
  * swa_sink_prefill_chunked -- the chunk-based prefill of "滑窗与固定稀疏" (rolling-buffer section):
  * the L positions are processed in chunks of `chunk` rows; chunk c attends the rolling cache as it was
  * before the chunk plus its own keys (swa_sink_prefill with pos0 = c*chunk), then its keys/values are

@@ -26,6 +26,8 @@ SIGNATURES = {
     "swa_sink_prefill": (_i, [_vp, _vp, _vp, _vp, _vp, _vp, _vp, _i64, _i, _i, _i64, _i, _i, _i, _f, _i, _vp]),
     "swa_sink_prefill_chunked": (_i, [_vp, _vp, _vp, _vp, _vp, _vp, _vp, _i, _i, _i64, _i, _i, _i, _f, _i64, _i,
                                       _vp]),
+    "swa_sink_prefill_host": (_i, [_vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _i, _i, _i64, _i, _i, _i, _f,
+                                   _i, _vp]),
     "kv_rolling_write": (_i, [_vp, _vp, _vp, _vp, _i, _i, _i, _i, _i, _i64, _i64, _i, _vp]),
     "swa_sink_decode_step": (_i, [_vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _i, _i64, _f, _vp, _sz, _i, _vp]),
     "swa_sink_decode_step_noalloc": (_i, [_vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _i, _i64, _f, _i, _vp]),
@@ -133,6 +135,30 @@ def swa_sink_prefill_chunked(q, k, v, w: int, s: int, chunk: int, k_cache, v_cac
         _ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), _ptr(k_cache), _ptr(v_cache), B, H, L, d, w, s, scale,
         chunk, _dtype_code(q), _stream(stream)))
     return o
+
+
+def swa_sink_prefill_host(q_h, k_h, v_h, w: int, s: int, q_d, k_d, v_d, o_d, o_h=None, lse_h=None, lse_d=None,
+                          scale: float | None = None, stream=None):
+    """Prefill of host tensors q_h, k_h, v_h [B, H, L, d] (pinned for overlap) through the caller's device
+    buffers q_d, k_d, v_d, o_d; the output lands in o_h (host).  Copies and compute are pipelined by the
+    library over groups of (b, h) rows.  Asynchronous: synchronise the stream before reading o_h."""
+    B, H, L, d = q_h.shape
+    for t in (q_h, k_h, v_h):
+        assert t.device.type == "cpu" and t.is_contiguous() and t.shape == q_h.shape and t.dtype == q_h.dtype
+    if o_h is None:
+        o_h = torch.empty(q_h.shape, dtype=q_h.dtype, pin_memory=q_h.is_pinned())
+    assert o_h.device.type == "cpu" and o_h.is_contiguous() and o_h.shape == q_h.shape
+    if lse_h is not None:
+        assert lse_h.device.type == "cpu" and lse_h.is_contiguous() and lse_d is not None
+    for t in (q_d, k_d, v_d, o_d):
+        assert t.shape == q_h.shape and t.dtype == q_h.dtype
+    _dev(q_d, k_d, v_d, o_d, lse_d)
+    scale = (1.0 / d ** 0.5) if scale is None else scale
+    _check("swa_sink_prefill_host", lib().swa_sink_prefill_host(
+        q_h.data_ptr(), k_h.data_ptr(), v_h.data_ptr(), o_h.data_ptr(), lse_h.data_ptr() if lse_h is not None else None,
+        _ptr(q_d), _ptr(k_d), _ptr(v_d), _ptr(o_d), _ptr(lse_d), B, H, L, d, w, s, scale, _dtype_code(q_h),
+        _stream(stream)))
+    return o_h
 
 
 def kv_rolling_write(k_cache, v_cache, k_new, v_new, w: int, s: int, pos0: int, stream=None):

@@ -259,6 +259,97 @@ extern "C" int swa_sink_prefill_chunked(const void *q, const void *k, const void
     return SWA_OK;
 }
 
+// Streams and events of the host-buffer prefill pipeline (copies in, compute, copies out), created once
+// per device.
+constexpr int kHostGroups = 8;
+struct HostPipe {
+    cudaStream_t in, comp, out;
+    cudaEvent_t fork, join_out;
+    cudaEvent_t copied[kHostGroups], computed[kHostGroups];
+};
+static HostPipe *host_pipe() {
+    static std::mutex mu;
+    static HostPipe *per_dev[64] = {nullptr};
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return nullptr;
+    std::lock_guard<std::mutex> lk(mu);
+    if (!per_dev[dev]) {
+        HostPipe *h = new HostPipe();
+        bool ok = cudaStreamCreateWithFlags(&h->in, cudaStreamNonBlocking) == cudaSuccess &&
+                  cudaStreamCreateWithFlags(&h->comp, cudaStreamNonBlocking) == cudaSuccess &&
+                  cudaStreamCreateWithFlags(&h->out, cudaStreamNonBlocking) == cudaSuccess &&
+                  cudaEventCreateWithFlags(&h->fork, cudaEventDisableTiming) == cudaSuccess &&
+                  cudaEventCreateWithFlags(&h->join_out, cudaEventDisableTiming) == cudaSuccess;
+        for (int g = 0; ok && g < kHostGroups; ++g)
+            ok = cudaEventCreateWithFlags(&h->copied[g], cudaEventDisableTiming) == cudaSuccess &&
+                 cudaEventCreateWithFlags(&h->computed[g], cudaEventDisableTiming) == cudaSuccess;
+        if (!ok) {
+            delete h;
+            return nullptr;
+        }
+        per_dev[dev] = h;
+    }
+    return per_dev[dev];
+}
+
+extern "C" int swa_sink_prefill_host(const void *q_h, const void *k_h, const void *v_h, void *o_h, float *lse_h,
+                                     void *q_d, void *k_d, void *v_d, void *o_d, float *lse_d, int B, int H,
+                                     int64_t L, int d, int w, int s, float scale, int dtype, void *stream) {
+    t_err[0] = 0;
+    int rc = check_prefill(q_d, k_d, v_d, o_d, lse_d, 0, B, H, L, d, w, s, scale, dtype);
+    if (rc) return rc;
+    if (L == 0) return SWA_OK;
+    if (!q_h || !k_h || !v_h || !o_h) return fail(SWA_ERR_INVALID, "q_h, k_h, v_h and o_h must be non-null");
+    if (lse_h && !lse_d) return fail(SWA_ERR_INVALID, "lse_h needs a device lse_d");
+    HostPipe *hp = host_pipe();
+    if (!hp) return fail(SWA_ERR_CUDA, "cannot create the streams of the host-buffer pipeline");
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    const int BH = B * H;
+    const int groups = BH < kHostGroups ? BH : kHostGroups;
+    const size_t row_bytes = static_cast<size_t>(d) * esize_of(dtype);
+    const size_t bh_bytes = static_cast<size_t>(L) * row_bytes;  // one (b, h) block of q, k, v or o
+    cudaError_t e = cudaEventRecord(hp->fork, st);
+    if (e == cudaSuccess) e = cudaStreamWaitEvent(hp->in, hp->fork, 0);
+    if (e == cudaSuccess) e = cudaStreamWaitEvent(hp->comp, hp->fork, 0);
+    if (e == cudaSuccess) e = cudaStreamWaitEvent(hp->out, hp->fork, 0);
+    for (int g = 0; e == cudaSuccess && g < groups; ++g) {
+        const int r0 = static_cast<int>(static_cast<int64_t>(BH) * g / groups);
+        const int r1 = static_cast<int>(static_cast<int64_t>(BH) * (g + 1) / groups);
+        const size_t off = static_cast<size_t>(r0) * bh_bytes, bytes = static_cast<size_t>(r1 - r0) * bh_bytes;
+        // inputs of the group: three contiguous blocks
+        cudaStream_t in = hp->in;
+        e = cudaMemcpyAsync(static_cast<char *>(q_d) + off, static_cast<const char *>(q_h) + off, bytes,
+                            cudaMemcpyHostToDevice, in);
+        if (e == cudaSuccess)
+            e = cudaMemcpyAsync(static_cast<char *>(k_d) + off, static_cast<const char *>(k_h) + off, bytes,
+                                cudaMemcpyHostToDevice, in);
+        if (e == cudaSuccess)
+            e = cudaMemcpyAsync(static_cast<char *>(v_d) + off, static_cast<const char *>(v_h) + off, bytes,
+                                cudaMemcpyHostToDevice, in);
+        if (e == cudaSuccess) e = cudaEventRecord(hp->copied[g], in);
+        if (e == cudaSuccess) e = cudaStreamWaitEvent(hp->comp, hp->copied[g], 0);
+        if (e != cudaSuccess) break;
+        float *lg = lse_d ? lse_d + static_cast<int64_t>(r0) * L : nullptr;
+        rc = prefill_impl(static_cast<char *>(q_d) + off, static_cast<char *>(k_d) + off,
+                          static_cast<char *>(v_d) + off, static_cast<char *>(o_d) + off, lg, nullptr, nullptr, 0,
+                          r1 - r0, 1, L, d, w, s, scale, dtype, L, hp->comp);
+        if (rc) return rc;
+        e = cudaEventRecord(hp->computed[g], hp->comp);
+        if (e == cudaSuccess) e = cudaStreamWaitEvent(hp->out, hp->computed[g], 0);
+        if (e == cudaSuccess)
+            e = cudaMemcpyAsync(static_cast<char *>(o_h) + off, static_cast<char *>(o_d) + off, bytes,
+                                cudaMemcpyDeviceToHost, hp->out);
+        if (e == cudaSuccess && lse_h)
+            e = cudaMemcpyAsync(lse_h + static_cast<int64_t>(r0) * L, lg, static_cast<size_t>(r1 - r0) * L * 4,
+                                cudaMemcpyDeviceToHost, hp->out);
+    }
+    // the output stream finishes last (it waited for every group's compute); the caller's stream joins it
+    if (e == cudaSuccess) e = cudaEventRecord(hp->join_out, hp->out);
+    if (e == cudaSuccess) e = cudaStreamWaitEvent(st, hp->join_out, 0);
+    if (e != cudaSuccess) return fail(SWA_ERR_CUDA, "host-buffer prefill pipeline: %s", cudaGetErrorString(e));
+    return SWA_OK;
+}
+
 extern "C" int kv_rolling_write(void *k_cache, void *v_cache, const void *k_new, const void *v_new, int B, int H,
                                 int d, int w, int s, int64_t pos0, int64_t n, int dtype, void *stream) {
     t_err[0] = 0;

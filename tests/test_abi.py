@@ -108,3 +108,17 @@ def test_workspace_size_shapes(lib):
 def test_selftests_validate(lib):
     assert lib.swa_selftest_wait_timeout(0, None) == swa.SWA_ERR_INVALID
     assert lib.swa_selftest_umma(None, None, None, 0, None) == swa.SWA_ERR_INVALID
+
+
+def test_host_prefill_validates_before_any_cuda_call(lib):
+    f = 1 << 20  # never dereferenced: validation fails first
+    args = [f, f, f, f, None, f, f, f, f, None, 1, 1, 128, 128, 64, 4, 0.1, 0, None]
+    bad = list(args)
+    bad[0] = None  # no host q
+    assert lib.swa_sink_prefill_host(*bad) == swa.SWA_ERR_INVALID
+    bad = list(args)
+    bad[4] = f  # host lse without a device lse
+    assert lib.swa_sink_prefill_host(*bad) == swa.SWA_ERR_INVALID
+    bad = list(args)
+    bad[15] = 64  # s >= w
+    assert lib.swa_sink_prefill_host(*bad) == swa.SWA_ERR_INVALID

@@ -133,3 +133,25 @@ def test_chunked_prefill_fp32():
     o = swa.swa_sink_prefill_chunked(q, k, v, w, s, 37, kc, vc)
     o_ref, _ = oracle.prefill(q, k, v, w, s, 0.25)
     compare("chunked fp32", o, o_ref, torch.float32)
+
+
+def test_prefill_from_host_buffers():
+    # the host-buffer entry point (copies pipelined over row groups) gives exactly the device-buffer
+    # result, row group by row group, including a ragged last tile and lse
+    swa = require_gpu()
+    B, H, L, d, w, s = 1, 13, 1000, 128, 256, 4
+    q, k, v = inputs(B, H, L, d, torch.bfloat16, 777, sink_boost=True)
+    lse_ref = torch.empty((B, H, L), dtype=torch.float32, device="cuda")
+    o_ref = swa.swa_sink_prefill(q, k, v, w, s, lse=lse_ref)
+    qh, kh, vh = (x.cpu().pin_memory() for x in (q, k, v))
+    qd, kd, vd = (torch.full_like(x, float("nan")) for x in (q, k, v))
+    od = torch.empty_like(q)
+    lse_d = torch.empty_like(lse_ref)
+    lse_h = torch.empty((B, H, L), dtype=torch.float32).pin_memory()
+    o_h = swa.swa_sink_prefill_host(qh, kh, vh, w, s, qd, kd, vd, od, lse_h=lse_h, lse_d=lse_d)
+    torch.cuda.synchronize()
+    assert swa.swa_device_status() == swa.SWA_OK, swa.last_error()
+    assert torch.equal(o_h, o_ref.cpu())
+    assert torch.equal(lse_h, lse_ref.cpu())
+    o_or, _ = oracle.prefill(q, k, v, w, s, 1.0 / math.sqrt(d))
+    compare("host-buffer prefill", o_h, o_or, torch.bfloat16)
