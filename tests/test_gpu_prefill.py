@@ -155,3 +155,34 @@ def test_prefill_from_host_buffers():
     assert torch.equal(lse_h, lse_ref.cpu())
     o_or, _ = oracle.prefill(q, k, v, w, s, 1.0 / math.sqrt(d))
     compare("host-buffer prefill", o_h, o_or, torch.bfloat16)
+
+
+def test_multi_stream_calls_capture_into_a_cuda_graph():
+    # the chunked and the host-buffer prefill fork work onto library streams and join it back with
+    # events; both must capture into a CUDA graph and replay to the same result as a direct call
+    swa = require_gpu()
+    B, H, L, d, w, s, chunk = 1, 17, 600, 128, 256, 4, 200
+    q, k, v = inputs(B, H, L, d, torch.bfloat16, 4321, sink_boost=True)
+    kc = torch.zeros((B, H, w, d), dtype=torch.bfloat16, device="cuda")
+    vc = torch.zeros_like(kc)
+    o_direct = swa.swa_sink_prefill_chunked(q, k, v, w, s, chunk, kc, vc)
+    qh, kh, vh = (x.cpu().pin_memory() for x in (q, k, v))
+    qd, kd, vd, od = (torch.empty_like(x) for x in (q, k, v, q))
+    oh = torch.empty(q.shape, dtype=q.dtype).pin_memory()
+    o_g = torch.empty_like(q)
+    kc2, vc2 = torch.zeros_like(kc), torch.zeros_like(vc)
+    side = torch.cuda.Stream()
+    side.wait_stream(torch.cuda.current_stream())
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph, stream=side):
+        swa.swa_sink_prefill_chunked(q, k, v, w, s, chunk, kc2, vc2, o=o_g)
+        swa.swa_sink_prefill_host(qh, kh, vh, w, s, qd, kd, vd, od, o_h=oh)
+    for _ in range(2):
+        o_g.fill_(float("nan"))
+        oh.fill_(float("nan"))
+        graph.replay()
+        torch.cuda.synchronize()
+        assert swa.swa_device_status() == swa.SWA_OK, swa.last_error()
+        assert torch.equal(o_g, o_direct)
+        assert torch.equal(kc2, kc) and torch.equal(vc2, vc)
+        assert torch.equal(oh, swa.swa_sink_prefill(q, k, v, w, s).cpu())
