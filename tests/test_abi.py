@@ -122,3 +122,9 @@ def test_host_prefill_validates_before_any_cuda_call(lib):
     bad = list(args)
     bad[15] = 64  # s >= w
     assert lib.swa_sink_prefill_host(*bad) == swa.SWA_ERR_INVALID
+
+
+def test_bf16_prefill_rejects_windows_past_the_tile_list(lib):
+    f = 1 << 20  # never dereferenced: the window check comes first
+    rc = lib.swa_sink_prefill(f, f, f, f, None, None, None, 0, 1, 1, 9000, 128, 7400, 4, 0.1, swa.SWA_BF16, None)
+    assert rc == swa.SWA_ERR_UNSUPPORTED

@@ -54,6 +54,8 @@ BF16_SHAPES = [
     (1, 3, 5, 3, 1),
     (1, 1, 2048, 1536, 4),
     (1, 1, 900, 300, 200),
+    (1, 1, 9000, 7296, 4),   # the largest window the 64-entry key-tile list takes at s = 4
+    (8, 300, 64, 16, 4),     # 2400 (b, h) rows of one short query pair: many rounds of the persistent grid
     (1, 1, 640, 256, 130),
 ]
 
