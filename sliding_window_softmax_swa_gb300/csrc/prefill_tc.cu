@@ -168,47 +168,6 @@ __host__ __device__ void mark_tiles(Tile *tl, int n, int q0, int qlast, int s, i
     }
 }
 
-// Put an item's tiles in the order the MMA and softmax walk them: the first tile both query tiles use,
-// then the tiles only one of them uses, alternating (query tile 1's first), then the other shared tiles.
-// In position order query tile 0 alone needs the oldest band tile and query tile 1 alone the newest, so
-// one query tile would idle at the start of the item and the other at its end; in this order the
-// one-sided tiles sit next to each other, both query tiles end on the same tile and their epilogues
-// overlap.  The softmax does not depend on the order of the keys; the list stays a partition.
-__host__ __device__ void order_tiles(Tile *tl, int n) {
-    if (n < 2 || n > MAX_TILES) return;
-    // In place: position p takes the first remaining tile of the wanted kind (rotated into place, so
-    // each kind keeps its position order).  Kinds by flags & 6: 6 both query tiles, 4 query tile 1 only,
-    // 2 query tile 0 only.
-    int phase = 0;  // 0: first shared tile; 1: one-sided tiles, alternating; 2: shared; 3: the rest
-    int want1 = 4;  // in phase 1: the kind wanted next
-    for (int p = 0; p < n; ++p) {
-        int q = -1;
-        while (q < 0 && phase < 4) {
-            const int kind = phase == 0 ? 6 : phase == 1 ? want1 : phase == 2 ? 6 : -1;
-            for (int i = p; i < n && q < 0; ++i)
-                if (kind < 0 || (tl[i].flags & 6) == kind) q = i;
-            if (phase == 1) {
-                if (q < 0) {  // try the other one-sided kind before moving on
-                    const int other = want1 ^ 6;
-                    for (int i = p; i < n && q < 0; ++i)
-                        if ((tl[i].flags & 6) == other) q = i;
-                    if (q < 0) phase = 2;
-                } else {
-                    want1 ^= 6;  // 4 <-> 2
-                }
-            } else if (phase == 0) {
-                phase = 1;
-            } else if (q < 0) {
-                ++phase;
-            }
-        }
-        if (q < 0) break;
-        const Tile t = tl[q];
-        for (int i = q; i > p; --i) tl[i] = tl[i - 1];
-        tl[p] = t;
-    }
-}
-
 // Bits [lo, hi] of a 32-bit word (clipped to [0, 31]; 0 when the range is empty).
 __device__ __forceinline__ uint32_t range_bits(int lo, int hi) {
     lo = lo < 0 ? 0 : lo;
@@ -436,7 +395,6 @@ __global__ void __launch_bounds__(kThreads, 1) swa_prefill_tc_kernel(const __gri
                     break;
                 }
                 mark_tiles(tl, n, q0, qlast, P.s, P.m);
-                order_tiles(tl, n);
                 ntiles_s[b] = n;
                 mbar_arrive(&lready[b]);  // release: the list is visible to whoever sees the phase complete
                 if (it >= 1 && !mbar_wait(qempty, (it - 1) & 1, wc, 13, it)) break;
@@ -901,7 +859,6 @@ int prefill_tile_plan(int q0, int q1, int pos0, int w, int s, int *out, int max_
     tc::Tile tl[tc::MAX_TILES];
     const int n = tc::build_tiles(tl, q0, q1, pos0, s, w - s, w);
     tc::mark_tiles(tl, n, q0, q1, s, w - s);
-    tc::order_tiles(tl, n);
     for (int i = 0; i < n && i < max_tiles && i < tc::MAX_TILES; ++i) {
         out[5 * i + 0] = tl[i].flags & 1;
         out[5 * i + 1] = tl[i].row0;
