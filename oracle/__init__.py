@@ -16,6 +16,9 @@ It follows the SWA formula of the hyper.ai summary of arXiv 2608.28444 (section
 addition to the w - 4 window keys), equation (1) of "模糊窗口注意力" section 2.1 (causal softmax
 attention) and eq attn-fixed-softmax-sink of "滑窗与固定稀疏" (row normalisation).
 
+``rope`` and ``decode_rope`` state the streaming decode with positions re-assigned inside the cache
+and rotary embedding (StreamingLLM section of "滑窗与固定稀疏").
+
 Parity status: every function here is pinned by ``tests/test_oracle.py`` against closed forms,
 textbook special cases and hand-derived golden values (``tests/golden/``).
 """
@@ -157,6 +160,46 @@ def decode(q_t, k_hist, v_hist, t: int, w: int, s: int, scale: float, nthreads: 
     kpos = np.arange(t + 1, dtype=np.int64)
     o, lse = attend(q_t.reshape(nh, 1, d), np.array([t], dtype=np.int64), k_hist, v_hist, kpos,
                     w, s, scale, nthreads)
+    return o.reshape(nh, d), lse.reshape(nh)
+
+
+def rope(x, pos, base: float = 10000.0) -> np.ndarray:
+    """Rotary position embedding of rows x [..., n, d] at positions pos [n] (fp64).
+
+    The pages name RoPE without printing it (StreamingLLM section of "滑窗与固定稀疏"); this is its plain
+    reading in the form of the Llama-2 / Mistral models the pages use: dimension i of the first half and
+    dimension i + d/2 form a pair that is rotated by the angle pos * base^(-2i/d), i = 0 .. d/2 - 1.
+    """
+    x = np.asarray(x, dtype=np.float64)
+    d = x.shape[-1]
+    half = d // 2
+    theta = base ** (-2.0 * np.arange(half, dtype=np.float64) / d)
+    ang = np.asarray(pos, dtype=np.float64)[:, None] * theta[None, :]
+    c, sn = np.cos(ang), np.sin(ang)
+    x1, x2 = x[..., :half], x[..., half:]
+    return np.concatenate([x1 * c - x2 * sn, x1 * sn + x2 * c], axis=-1)
+
+
+def decode_rope(q_t, k_hist, v_hist, t: int, w: int, s: int, scale: float, base: float = 10000.0,
+                nthreads: int | None = None):
+    """Streaming decode at position t with positions re-assigned inside the cache (StreamingLLM section
+    of "滑窗与固定稀疏": the cache holds the s sinks and the m most recent tokens, their positional
+    encoding is their consecutive position inside the cache, 0 .. s+m-1, not the original position, and
+    RoPE is applied each step to keys kept unrotated).
+
+    q_t: [nh, d] unrotated query; k_hist, v_hist: [nh, t + 1, d] unrotated history (positions 0..t).
+    The key set K(t) is decided per key by the brute-force test; its members, in increasing original
+    position (the sinks first, then the window), take cache positions 0 .. n-1; the query, whose own
+    key is the newest member, takes position n - 1.  Returns (o [nh, d], lse [nh]).
+    """
+    q_t = _f64(q_t)
+    nh, d = q_t.shape
+    members = np.array([i for i in range(t + 1) if is_key(t, i, w, s)], dtype=np.int64)
+    cpos = np.arange(len(members), dtype=np.float64)
+    k_rot = rope(_f64(k_hist)[:, members], cpos, base)
+    v_sel = np.ascontiguousarray(_f64(v_hist)[:, members])
+    q_rot = rope(q_t[:, None, :], np.array([len(members) - 1.0]), base)
+    o, lse = attend(q_rot, np.array([t], dtype=np.int64), k_rot, v_sel, members, w, s, scale, nthreads)
     return o.reshape(nh, d), lse.reshape(nh)
 
 

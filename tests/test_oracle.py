@@ -275,3 +275,101 @@ def test_rows_subset_and_threads_agree():
     rows = [0, 5, 12, 13, 14, 69]
     orow, lrow = oracle.prefill_rows(q[0][:, rows], rows, k[0], v[0], 13, 4, 0.35)
     assert np.array_equal(orow, o[0][:, rows]) and np.array_equal(lrow, lse[0][:, rows])
+
+
+# ---------------------------------------------------------------- RoPE at positions inside the cache
+def test_rope_matches_complex_rotation():
+    # the rotation written as complex multiplication: (x_i + i x_{i+d/2}) * exp(i * pos * base^(-2i/d))
+    rng = np.random.default_rng(11)
+    d, n = 16, 9
+    x = rng.standard_normal((3, n, d))
+    pos = rng.integers(0, 5000, n).astype(np.float64)
+    theta = 10000.0 ** (-np.arange(d // 2) * 2.0 / d)
+    z = (x[..., : d // 2] + 1j * x[..., d // 2:]) * np.exp(1j * pos[:, None] * theta[None, :])
+    want = np.concatenate([z.real, z.imag], axis=-1)
+    np.testing.assert_allclose(oracle.rope(x, pos), want, rtol=0, atol=1e-12)
+
+
+def test_rope_scores_depend_on_relative_position_only():
+    rng = np.random.default_rng(12)
+    d = 32
+    q, k = rng.standard_normal((1, 1, d)), rng.standard_normal((1, 1, d))
+    for p, pk, shift in [(5.0, 2.0, 100.0), (0.0, 17.0, 3.0), (1000.0, 4.0, 1.0)]:
+        a = (oracle.rope(q, [p]) * oracle.rope(k, [pk])).sum()
+        b = (oracle.rope(q, [p + shift]) * oracle.rope(k, [pk + shift])).sum()
+        assert abs(a - b) < 1e-9
+
+
+def test_decode_rope_hand_example():
+    g = json.load(open(os.path.join(GOLDEN, "rope_cache_positions_d4.json")))
+    t, w, s, d = 5, 3, 1, 4
+    k = np.zeros((1, t + 1, d))
+    v = np.zeros((1, t + 1, d))
+    for p in g["filler_positions"]:  # outside K(5): must not matter
+        k[0, p] = 100.0
+        v[0, p] = -7.0
+    for p, row in g["keys"].items():
+        k[0, int(p)] = row
+    for p, row in g["values"].items():
+        v[0, int(p)] = row
+    o, lse = oracle.decode_rope(np.array([g["q"]]), k, v, t, w, s, 1.0)
+    np.testing.assert_allclose(o[0], g["o"], rtol=0, atol=1e-12)
+    assert abs(lse[0] - g["lse"]) < 1e-12
+
+
+def test_decode_rope_before_the_window_fills_is_plain_rope():
+    # while t < w every position is in the cache, in order: cache position == original position
+    rng = np.random.default_rng(13)
+    nh, d, w, s = 2, 16, 12, 4
+    for t in (0, 3, 11):
+        q = rng.standard_normal((nh, d))
+        k, v = rng.standard_normal((nh, t + 1, d)), rng.standard_normal((nh, t + 1, d))
+        pos = np.arange(t + 1, dtype=np.float64)
+        o_ref, l_ref = oracle.attend(oracle.rope(q[:, None], [float(t)]), [t], oracle.rope(k, pos), v,
+                                     np.arange(t + 1), w, s, 0.25)
+        o, lse = oracle.decode_rope(q, k, v, t, w, s, 0.25)
+        np.testing.assert_allclose(o, o_ref[:, 0], atol=1e-12)
+        np.testing.assert_allclose(lse, l_ref[:, 0], atol=1e-12)
+
+
+def test_decode_rope_without_sinks_keeps_relative_distances():
+    # s = 0: the cache holds the last w positions in order, so re-assigning positions only shifts them by
+    # a constant and RoPE at the original positions gives the same result
+    rng = np.random.default_rng(14)
+    nh, d, w = 2, 16, 6
+    for t in (6, 20, 57):
+        q = rng.standard_normal((nh, d))
+        k, v = rng.standard_normal((nh, t + 1, d)), rng.standard_normal((nh, t + 1, d))
+        pos = np.arange(t + 1, dtype=np.float64)
+        o_ref, _ = oracle.attend(oracle.rope(q[:, None], [float(t)]), [t], oracle.rope(k, pos), v,
+                                 np.arange(t + 1), w, 0, 0.3)
+        o, _ = oracle.decode_rope(q, k, v, t, w, 0, 0.3)
+        np.testing.assert_allclose(o, o_ref[:, 0], atol=1e-10)
+
+
+def test_decode_rope_sinks_sit_at_fixed_distance_once_the_window_is_full():
+    # with the window full, sink i sits at distance w - 1 - i from the query whatever t is: advancing t
+    # with the same window contents and sinks leaves the result unchanged (plain RoPE would not)
+    rng = np.random.default_rng(15)
+    nh, d, w, s = 1, 16, 8, 2
+    m = w - s
+    sinks_k, sinks_v = rng.standard_normal((nh, s, d)), rng.standard_normal((nh, s, d))
+    win_k, win_v = rng.standard_normal((nh, m, d)), rng.standard_normal((nh, m, d))
+    q = rng.standard_normal((nh, d))
+    outs = []
+    for t in (20, 45):
+        k, v = rng.standard_normal((nh, t + 1, d)), rng.standard_normal((nh, t + 1, d))
+        k[:, :s], v[:, :s] = sinks_k, sinks_v
+        k[:, t - m + 1:], v[:, t - m + 1:] = win_k, win_v
+        outs.append(oracle.decode_rope(q, k, v, t, w, s, 0.3)[0])
+    np.testing.assert_allclose(outs[0], outs[1], atol=1e-12)
+    # and differs from RoPE at the original positions
+    t = 45
+    k = rng.standard_normal((nh, t + 1, d))
+    v = rng.standard_normal((nh, t + 1, d))
+    o_new, _ = oracle.decode_rope(q, k, v, t, w, s, 0.3)
+    members = np.array([i for i in range(t + 1) if oracle.is_key(t, i, w, s)])
+    o_plain, _ = oracle.attend(oracle.rope(q[:, None], [float(t)]), [t],
+                               oracle.rope(k[:, members], members.astype(np.float64)), v[:, members], members,
+                               w, s, 0.3)
+    assert np.abs(o_new - o_plain[:, 0]).max() > 1e-3
