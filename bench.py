@@ -266,8 +266,9 @@ def chunked_leg(swa, wl, steps, warmup, world, rank, clocks):
             "ms_per_step": t / steps * 1e3, "launches": steps * 2 * nch * groups}
 
 
-def decode_leg(swa, wl, world, rank, clocks, steps=None):
-    """The whole streaming run: per step one rolling write of the new key/value and one decode."""
+def decode_leg(swa, wl, world, rank, clocks, steps=None, rope=False):
+    """The whole streaming run: per step one rolling write of the new key/value and one decode (with
+    ``rope``: the decode with RoPE at the positions inside the cache, base 10000, unrotated keys)."""
     import torch
     import swa_inputs
     B, H, d, w, s = wl.B, wl.H, wl.d, wl.w, wl.s
@@ -281,9 +282,10 @@ def decode_leg(swa, wl, world, rank, clocks, steps=None):
     kc = torch.zeros((B, H, w, d), dtype=qs.dtype, device="cuda")
     vc = torch.zeros_like(kc)
     o = torch.empty((B, H, d), dtype=qs.dtype, device="cuda")
-    nws = swa.swa_sink_decode_workspace_size(B, H, d, w)
-    ws = torch.empty(max(nws, 256), dtype=torch.uint8, device="cuda")
     lib = swa.lib()
+    nws = (lib.swa_sink_decode_rope_workspace_size(B, H, d, w) if rope
+           else swa.swa_sink_decode_workspace_size(B, H, d, w))
+    ws = torch.empty(max(nws, 256), dtype=torch.uint8, device="cuda")
     stream = torch.cuda.current_stream().cuda_stream
     row = B * H * d * qs.element_size()
     qp, kp, vp = qs.data_ptr(), ks.data_ptr(), vs.data_ptr()
@@ -293,8 +295,12 @@ def decode_leg(swa, wl, world, rank, clocks, steps=None):
         for t in range(t0, t1):
             rc = lib.kv_rolling_write(kc.data_ptr(), vc.data_ptr(), kp + t * row, vp + t * row, B, H, d, w, s, t, 1,
                                       dt, stream)
-            rc |= lib.swa_sink_decode_step(qp + t * row, kc.data_ptr(), vc.data_ptr(), o.data_ptr(), None, B, H, d,
-                                           w, s, t, wl.scale, ws.data_ptr(), nws, dt, stream)
+            if rope:
+                rc |= lib.swa_sink_decode_step_rope(qp + t * row, kc.data_ptr(), vc.data_ptr(), o.data_ptr(), None, B,
+                                                    H, d, w, s, t, wl.scale, 10000.0, ws.data_ptr(), nws, dt, stream)
+            else:
+                rc |= lib.swa_sink_decode_step(qp + t * row, kc.data_ptr(), vc.data_ptr(), o.data_ptr(), None, B, H,
+                                               d, w, s, t, wl.scale, ws.data_ptr(), nws, dt, stream)
             if rc:
                 raise RuntimeError(swa.last_error())
 
@@ -311,8 +317,12 @@ def decode_leg(swa, wl, world, rank, clocks, steps=None):
     tl = T - 1
 
     def dstep():
-        rc = lib.swa_sink_decode_step(qp + tl * row, kc.data_ptr(), vc.data_ptr(), o.data_ptr(), None, B, H, d, w, s,
-                                      tl, wl.scale, ws.data_ptr(), nws, dt, stream)
+        if rope:
+            rc = lib.swa_sink_decode_step_rope(qp + tl * row, kc.data_ptr(), vc.data_ptr(), o.data_ptr(), None, B, H,
+                                               d, w, s, tl, wl.scale, 10000.0, ws.data_ptr(), nws, dt, stream)
+        else:
+            rc = lib.swa_sink_decode_step(qp + tl * row, kc.data_ptr(), vc.data_ptr(), o.data_ptr(), None, B, H, d,
+                                          w, s, tl, wl.scale, ws.data_ptr(), nws, dt, stream)
         if rc:
             raise RuntimeError(swa.last_error())
 
@@ -408,7 +418,7 @@ def main():
     ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--primary-only", action="store_true", help="only the primary prefill leg")
-    ap.add_argument("--legs", default="primary,mistral,chunked,decode",
+    ap.add_argument("--legs", default="primary,mistral,chunked,decode,decode_rope",
                     help="comma list of legs to run (profiling runs pick one)")
     ap.add_argument("--decode-steps", type=int, default=None, help="shorter decode stream (profiling only)")
     args = ap.parse_args()
@@ -465,6 +475,16 @@ def main():
                                            "frac": r["kernel"]["gbs"] / peaks["hbm_gbs"],
                                            "frac_of_8tbs_nominal": r["kernel"]["gbs"] / 8000.0,
                                            "avg_us": r["kernel"]["avg_us"]}}
+    if "decode_rope" in legs:
+        dw = swa_inputs.WORKLOADS["decode_llama13b_B64_w1024_s4_20480"]
+        r = decode_leg(swa, dw, world, rank, clocks, steps=args.decode_steps, rope=True)
+        secondary["decode_rope_llama13b_B64_w1024_s4_20480"] = {
+            "metric": "decode tok/s", "value": aggregate_rate(r["tok_per_s"], world, 1.0), "unit": "tok/s",
+            "seconds": r["seconds"], "what": "RoPE at the positions inside the cache (base 10000), unrotated keys",
+            "roofline": {"bound": "hbm", "kernel": "decode_kernel (rope)", "achieved": r["kernel"]["gbs"],
+                         "peak": peaks["hbm_gbs"], "unit": "GB/s", "frac": r["kernel"]["gbs"] / peaks["hbm_gbs"],
+                         "avg_us": r["kernel"]["avg_us"],
+                         "note": "bytes = the cache K/V rows + q/o (the d/2 angle steps, 512 B, stay in L1/L2; sin/cos are computed in registers)"}}
     ck = clocks.stop()
 
     if rank != 0:

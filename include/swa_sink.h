@@ -166,6 +166,29 @@ int swa_sink_decode_step_noalloc(const void *q, const void *k_cache, const void 
 /* Bytes of workspace swa_sink_decode_step needs for this shape (host-only, no CUDA call). */
 size_t swa_sink_decode_workspace_size(int B, int H, int d, int w);
 
+/*
+ * swa_sink_decode_step_rope -- swa_sink_decode_step with rotary position embedding applied at the
+ * positions the entries have inside the cache, as the StreamingLLM section of "滑窗与固定稀疏" describes:
+ * the cache keeps the keys unrotated; at every step its valid entries, sinks first and then the window
+ * from oldest to newest, take the consecutive positions 0 .. n-1 (n = min(t + 1, w)), and the query, whose
+ * own key is the newest entry, takes position n - 1.  RoPE rotates dimension pair (i, i + d/2) by
+ * position * rope_base^(-2i/d) (the half-split form of the Llama-2 / Mistral models; the pages name
+ * RoPE without printing it).
+ *
+ *   q       : [B, H, d] unrotated query at position t; k_cache / v_cache as for swa_sink_decode_step,
+ *             with unrotated keys.
+ *   rope_base : the RoPE base (10000 for Llama-2), finite and > 1.
+ *   workspace : caller-owned device scratch of at least swa_sink_decode_rope_workspace_size(B,H,d,w)
+ *             bytes, 256-byte aligned; it holds the d/2 angle steps (written by the call) and the split-K
+ *             partials.
+ *   t < 2^31, w <= 4096 (SWA_ERR_UNSUPPORTED otherwise).  Other arguments and errors as
+ *   swa_sink_decode_step.
+ */
+int swa_sink_decode_step_rope(const void *q, const void *k_cache, const void *v_cache, void *o, float *lse,
+                              int B, int H, int d, int w, int s, int64_t t, float scale, double rope_base,
+                              void *workspace, size_t workspace_bytes, int dtype, void *stream);
+size_t swa_sink_decode_rope_workspace_size(int B, int H, int d, int w);
+
 /* Human-readable reason of the calling host thread's most recent failure ("" if none). */
 const char *swa_last_error_string(void);
 

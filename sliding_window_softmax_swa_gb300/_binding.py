@@ -32,6 +32,9 @@ SIGNATURES = {
     "swa_sink_decode_step": (_i, [_vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _i, _i64, _f, _vp, _sz, _i, _vp]),
     "swa_sink_decode_step_noalloc": (_i, [_vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _i, _i64, _f, _i, _vp]),
     "swa_sink_decode_workspace_size": (_sz, [_i, _i, _i, _i]),
+    "swa_sink_decode_step_rope": (_i, [_vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _i, _i64, _f, ctypes.c_double, _vp,
+                                       _sz, _i, _vp]),
+    "swa_sink_decode_rope_workspace_size": (_sz, [_i, _i, _i, _i]),
     "swa_last_error_string": (ctypes.c_char_p, []),
     "swa_device_status": (_i, [_vp]),
     "swa_selftest_wait_timeout": (_i, [_i64, _vp]),
@@ -169,6 +172,24 @@ def kv_rolling_write(k_cache, v_cache, k_new, v_new, w: int, s: int, pos0: int, 
     _check("kv_rolling_write", lib().kv_rolling_write(
         _ptr(k_cache), _ptr(v_cache), _ptr(k_new), _ptr(v_new), B, H, d, w, s, pos0, n, _dtype_code(k_new),
         _stream(stream)))
+
+
+def swa_sink_decode_step_rope(q, k_cache, v_cache, t: int, w: int, s: int, rope_base: float = 10000.0,
+                              scale: float | None = None, o=None, lse=None, workspace=None, stream=None):
+    """Decode step at position t with RoPE at the positions inside the cache (unrotated q and keys)."""
+    B, H, d = q.shape
+    assert k_cache.shape == (B, H, w, d) and v_cache.shape == (B, H, w, d)
+    if o is None:
+        o = torch.empty_like(q)
+    nws = lib().swa_sink_decode_rope_workspace_size(B, H, d, w)
+    if workspace is None:
+        workspace = torch.empty(nws, dtype=torch.uint8, device=q.device)
+    _dev(q, k_cache, v_cache, o, lse, workspace)
+    scale = (1.0 / d ** 0.5) if scale is None else scale
+    _check("swa_sink_decode_step_rope", lib().swa_sink_decode_step_rope(
+        _ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(o), _ptr(lse), B, H, d, w, s, t, scale, float(rope_base),
+        _ptr(workspace), workspace.numel() * workspace.element_size(), _dtype_code(q), _stream(stream)))
+    return o
 
 
 def swa_sink_decode_workspace_size(B: int, H: int, d: int, w: int) -> int:

@@ -394,6 +394,37 @@ extern "C" int swa_sink_decode_step(const void *q, const void *k_cache, const vo
     return launch_decode(a);
 }
 
+extern "C" int swa_sink_decode_step_rope(const void *q, const void *k_cache, const void *v_cache, void *o,
+                                         float *lse, int B, int H, int d, int w, int s, int64_t t, float scale,
+                                         double rope_base, void *workspace, size_t workspace_bytes, int dtype,
+                                         void *stream) {
+    t_err[0] = 0;
+    int rc = check_common(B, H, d, w, s, dtype);
+    if (rc) return rc;
+    if (t < 0 || t >= (int64_t(1) << 31)) return fail(SWA_ERR_INVALID, "t=%lld out of range", (long long)t);
+    if (!(scale == scale) || scale <= 0.f || scale > 1e30f)
+        return fail(SWA_ERR_INVALID, "scale must be a positive finite number");
+    if (!(rope_base == rope_base) || rope_base <= 1.0 || rope_base > 1e30)
+        return fail(SWA_ERR_INVALID, "rope_base must be a finite number > 1");
+    if (!q || !k_cache || !v_cache || !o) return fail(SWA_ERR_INVALID, "q, caches and o must be non-null");
+    if (!aligned16(q) || !aligned16(k_cache) || !aligned16(v_cache) || !aligned16(o))
+        return fail(SWA_ERR_INVALID, "q, caches and o must be 16-byte aligned");
+    if (lse && (reinterpret_cast<uintptr_t>(lse) & 3u)) return fail(SWA_ERR_INVALID, "lse must be 4-byte aligned");
+    const size_t need = decode_rope_workspace_bytes(B * H, d, w);
+    if (workspace_bytes < need)
+        return fail(SWA_ERR_INVALID, "workspace of %zu bytes is smaller than the %zu needed", workspace_bytes, need);
+    if (!workspace || (reinterpret_cast<uintptr_t>(workspace) & 255u))
+        return fail(SWA_ERR_INVALID, "workspace must be non-null and 256-byte aligned");
+    DecodeArgs a{q, k_cache, v_cache, o, lse, B * H, d, w, s, t, scale, workspace, workspace_bytes,
+                 esize_of(dtype), static_cast<cudaStream_t>(stream)};
+    return launch_decode_rope(a, rope_base);
+}
+
+extern "C" size_t swa_sink_decode_rope_workspace_size(int B, int H, int d, int w) {
+    if (B < 1 || H < 1 || w < 1 || (d != 16 && d != 32 && d != 64 && d != 128)) return 0;
+    return decode_rope_workspace_bytes(B * H, d, w);
+}
+
 extern "C" int swa_selftest_wait_timeout(int64_t timeout_ns, void *stream) {
     t_err[0] = 0;
     if (timeout_ns < 1 || timeout_ns > 1000000000LL)

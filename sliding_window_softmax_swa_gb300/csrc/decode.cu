@@ -50,12 +50,26 @@ __device__ __forceinline__ void unpack16(const uint4 &u, float (&f)[4], float) {
 __device__ __forceinline__ void store_out(__nv_bfloat16 *p, float x) { *p = __float2bfloat16_rn(x); }
 __device__ __forceinline__ void store_out(float *p, float x) { *p = x; }
 
-template <typename T, int D, int U>
+// Rotary embedding at positions inside the cache (StreamingLLM section of "滑窗与固定稀疏": the cache's
+// entries take the consecutive positions 0 .. n-1, sinks first, then the window in order; keys are kept
+// unrotated and rotated at every step).  Dimensions i and i + D/2 form a pair rotated by pos * theta_i.
+// With relative position delta = c_key - c_query the score of a pair is
+//     q_i (k_i cos - k_{i+D/2} sin) + q_{i+D/2} (k_i sin + k_{i+D/2} cos),  angle = delta * theta_i,
+// so the query stays unrotated and each key row meets cos/sin of its own delta.
+struct RopeArgs {
+    // theta_i / (2 pi) for i = 0 .. D/2-1 as hi + lo: hi keeps 12 significant bits, so |delta| * hi
+    // (|delta| < 2^12) is exact in fp32 and its fraction of a turn loses nothing; lo carries the rest
+    const float2 *theta;   // [D/2]
+    int s, m;            // sinks, ring slots
+    int t;               // position of the query
+};
+
+template <typename T, int D, int U, bool ROPE>
 __global__ void __launch_bounds__(kDecThreads) decode_kernel(const T *__restrict__ q, const T *__restrict__ kc,
                                                              const T *__restrict__ vc, T *__restrict__ o,
                                                              float *__restrict__ lse, float *__restrict__ part,
                                                              int w, int nvalid, int per_split, int nsplit,
-                                                             float scale_log2) {
+                                                             float scale_log2, RopeArgs ra) {
     constexpr int EPL = 16 / sizeof(T);  // elements per 16-byte chunk
     constexpr int LPR = D / EPL;         // lanes per cache row
     constexpr int RPW = 32 / LPR;        // rows per warp per load
@@ -73,14 +87,38 @@ __global__ void __launch_bounds__(kDecThreads) decode_kernel(const T *__restrict
     const int j0 = split * per_split;
     const int j1 = min(nvalid, j0 + per_split);
 
+    // Without rotary embedding a lane holds one 16-byte chunk of q and of each key row: elements
+    // sub*EPL .. sub*EPL+EPL-1.  With it (half-split pairs (i, i + D/2)) a lane holds both halves of
+    // its EPL/2 pairs: elements sub*EPL/2 + p in qf[p] and D/2 + sub*EPL/2 + p in qf[EPL/2 + p], read as
+    // two 8-byte halves (each half of a row still coalesces into LPR * 8 contiguous bytes).
+    constexpr int HPL = EPL / 2;  // pairs per lane
     float qf[EPL];
     {
-        const uint4 qu = __ldg(reinterpret_cast<const uint4 *>(q + bh * D) + sub);
+        uint4 qu;
+        if constexpr (ROPE) {
+            const uint2 *q2 = reinterpret_cast<const uint2 *>(q + bh * D);
+            const uint2 a = __ldg(q2 + sub), b = __ldg(q2 + LPR + sub);
+            qu = make_uint4(a.x, a.y, b.x, b.y);
+        } else {
+            qu = __ldg(reinterpret_cast<const uint4 *>(q + bh * D) + sub);
+        }
         unpack16(qu, qf, T());
 #pragma unroll
         for (int e = 0; e < EPL; ++e) qf[e] *= scale_log2;
     }
+    float2 th[ROPE ? HPL : 1];  // theta / (2 pi) of the lane's pairs, hi + lo
+    int cq = 0;                 // cache position of the query
+    int jnew = 0;               // ring slot of the newest position (t), once the ring is full
+    bool full = false;
+    if constexpr (ROPE) {
+        full = ra.t >= ra.s + ra.m - 1;
+        if (full) jnew = ra.s + (ra.t - ra.s) % ra.m;
+        cq = nvalid - 1;  // the query's own key is the newest entry of the cache
+#pragma unroll
+        for (int p = 0; p < HPL; ++p) th[p] = __ldg(ra.theta + sub * HPL + p);
+    }
     const uint4 *kb = reinterpret_cast<const uint4 *>(kc + bh * w * D) + sub;
+    const uint2 *kb2 = reinterpret_cast<const uint2 *>(kc + bh * w * D) + sub;
     const uint4 *vb = reinterpret_cast<const uint4 *>(vc + bh * w * D) + sub;
 
     float m = -INFINITY, l = 0.f, acc[EPL];
@@ -93,7 +131,13 @@ __global__ void __launch_bounds__(kDecThreads) decode_kernel(const T *__restrict
         for (int u = 0; u < U; ++u) {
             const int j = jblk + u * G + grp;
             if (j < j1) {
-                kr[u] = __ldcs(kb + static_cast<int64_t>(j) * LPR);
+                if constexpr (ROPE) {
+                    const uint2 a = __ldcs(kb2 + static_cast<int64_t>(j) * (2 * LPR));
+                    const uint2 b = __ldcs(kb2 + static_cast<int64_t>(j) * (2 * LPR) + LPR);
+                    kr[u] = make_uint4(a.x, a.y, b.x, b.y);
+                } else {
+                    kr[u] = __ldcs(kb + static_cast<int64_t>(j) * LPR);
+                }
                 vr[u] = __ldcs(vb + static_cast<int64_t>(j) * LPR);
             } else {
                 kr[u] = make_uint4(0, 0, 0, 0);
@@ -107,8 +151,32 @@ __global__ void __launch_bounds__(kDecThreads) decode_kernel(const T *__restrict
             float kf[EPL];
             unpack16(kr[u], kf, T());
             float dot = 0.f;
+            if constexpr (ROPE) {
+                const int j = min(jblk + u * G + grp, j1 - 1);  // rows past j1 are masked below
+                // |delta| = cache position of the query - that of slot j.  Before the ring is full every
+                // valid slot j holds position j at cache position j, and the query sits at t.  Once it is
+                // full the query sits at w - 1, a sink j at j, and a ring slot at w - 1 - its age (how many
+                // ring writes ago it was written, counted back from the slot of position t).
+                const int ad = !full ? ra.t - j : (j < ra.s ? cq - j : (j <= jnew ? jnew - j : jnew - j + ra.m));
+                const float fad = static_cast<float>(ad);
 #pragma unroll
-            for (int e = 0; e < EPL; ++e) dot = fmaf(qf[e], kf[e], dot);
+                for (int p = 0; p < HPL; ++p) {
+                    // angle in turns, reduced to [-1/2, 1/2] exactly, then sin/cos of at most pi radians
+                    float turns = fad * th[p].x;
+                    turns -= rintf(turns);
+                    turns = fmaf(fad, th[p].y, turns);
+                    float sn, c;
+                    __sincosf(turns * 6.283185307179586f, &sn, &c);
+                    // q . R(delta theta) k over the pair, with sin(delta theta) = -sin(|delta| theta):
+                    // k_i (q_i c - q_{i+D/2} sn) + k_{i+D/2} (q_{i+D/2} c + q_i sn)
+                    const float qa = qf[p], qb = qf[HPL + p];
+                    dot = fmaf(fmaf(qa, c, -qb * sn), kf[p], dot);
+                    dot = fmaf(fmaf(qb, c, qa * sn), kf[HPL + p], dot);
+                }
+            } else {
+#pragma unroll
+                for (int e = 0; e < EPL; ++e) dot = fmaf(qf[e], kf[e], dot);
+            }
 #pragma unroll
             for (int off = LPR / 2; off >= 1; off >>= 1) dot += __shfl_xor_sync(0xFFFFFFFFu, dot, off);
             x[u] = (jblk + u * G + grp < j1) ? dot : -INFINITY;
@@ -202,16 +270,44 @@ size_t decode_workspace_bytes(int BH, int d, int w) {
 }
 
 template <typename T, int D>
-static int launch_typed(const DecodeArgs &a, int nvalid, int ns, int per_split, float sl2) {
+static int launch_typed(const DecodeArgs &a, int nvalid, int ns, int per_split, float sl2, const RopeArgs *ra) {
     constexpr int U = (sizeof(T) == 2 && D >= 64) ? 4 : 2;
     const dim3 grid(ns, a.BH), block(kDecThreads);
     float *part = static_cast<float *>(a.workspace);
-    decode_kernel<T, D, U><<<grid, block, 0, a.stream>>>(
-        static_cast<const T *>(a.q), static_cast<const T *>(a.k_cache), static_cast<const T *>(a.v_cache),
-        static_cast<T *>(a.o), a.lse, part, a.w, nvalid, per_split, ns, sl2);
+    if (ra)
+        decode_kernel<T, D, U, true><<<grid, block, 0, a.stream>>>(
+            static_cast<const T *>(a.q), static_cast<const T *>(a.k_cache), static_cast<const T *>(a.v_cache),
+            static_cast<T *>(a.o), a.lse, part, a.w, nvalid, per_split, ns, sl2, *ra);
+    else
+        decode_kernel<T, D, U, false><<<grid, block, 0, a.stream>>>(
+            static_cast<const T *>(a.q), static_cast<const T *>(a.k_cache), static_cast<const T *>(a.v_cache),
+            static_cast<T *>(a.o), a.lse, part, a.w, nvalid, per_split, ns, sl2, RopeArgs{});
     if (ns > 1)
         decode_merge_kernel<T, D><<<a.BH, D, 0, a.stream>>>(part, static_cast<T *>(a.o), a.lse, ns);
     return 0;
+}
+
+static int dispatch_decode(const DecodeArgs &a, int nvalid, int ns, int per_split, float sl2, const RopeArgs *ra) {
+    if (a.esize == 2) {
+        switch (a.d) {
+            case 16: launch_typed<__nv_bfloat16, 16>(a, nvalid, ns, per_split, sl2, ra); break;
+            case 32: launch_typed<__nv_bfloat16, 32>(a, nvalid, ns, per_split, sl2, ra); break;
+            case 64: launch_typed<__nv_bfloat16, 64>(a, nvalid, ns, per_split, sl2, ra); break;
+            case 128: launch_typed<__nv_bfloat16, 128>(a, nvalid, ns, per_split, sl2, ra); break;
+            default: return fail(SWA_ERR_UNSUPPORTED, "decode: d=%d", a.d);
+        }
+    } else {
+        switch (a.d) {
+            case 16: launch_typed<float, 16>(a, nvalid, ns, per_split, sl2, ra); break;
+            case 32: launch_typed<float, 32>(a, nvalid, ns, per_split, sl2, ra); break;
+            case 64: launch_typed<float, 64>(a, nvalid, ns, per_split, sl2, ra); break;
+            case 128: launch_typed<float, 128>(a, nvalid, ns, per_split, sl2, ra); break;
+            default: return fail(SWA_ERR_UNSUPPORTED, "decode: d=%d", a.d);
+        }
+    }
+    cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) return fail(SWA_ERR_CUDA, "decode launch: %s", cudaGetErrorString(e));
+    return SWA_OK;
 }
 
 int launch_decode(const DecodeArgs &a) {
@@ -221,26 +317,43 @@ int launch_decode(const DecodeArgs &a) {
     const float sl2 = a.scale * 1.4426950408889634f;
     if (ns > 1 && (!a.workspace || a.workspace_bytes < static_cast<size_t>(a.BH) * ns * (a.d + 2) * sizeof(float)))
         return fail(SWA_ERR_INVALID, "decode needs %d splits but the workspace is too small", ns);
-    if (a.esize == 2) {
-        switch (a.d) {
-            case 16: launch_typed<__nv_bfloat16, 16>(a, nvalid, ns, per_split, sl2); break;
-            case 32: launch_typed<__nv_bfloat16, 32>(a, nvalid, ns, per_split, sl2); break;
-            case 64: launch_typed<__nv_bfloat16, 64>(a, nvalid, ns, per_split, sl2); break;
-            case 128: launch_typed<__nv_bfloat16, 128>(a, nvalid, ns, per_split, sl2); break;
-            default: return fail(SWA_ERR_UNSUPPORTED, "decode: d=%d", a.d);
-        }
-    } else {
-        switch (a.d) {
-            case 16: launch_typed<float, 16>(a, nvalid, ns, per_split, sl2); break;
-            case 32: launch_typed<float, 32>(a, nvalid, ns, per_split, sl2); break;
-            case 64: launch_typed<float, 64>(a, nvalid, ns, per_split, sl2); break;
-            case 128: launch_typed<float, 128>(a, nvalid, ns, per_split, sl2); break;
-            default: return fail(SWA_ERR_UNSUPPORTED, "decode: d=%d", a.d);
-        }
-    }
-    cudaError_t e = cudaGetLastError();
-    if (e != cudaSuccess) return fail(SWA_ERR_CUDA, "decode launch: %s", cudaGetErrorString(e));
-    return SWA_OK;
+    return dispatch_decode(a, nvalid, ns, per_split, sl2, nullptr);
+}
+
+// theta_i / (2 pi), theta_i = base^(-2i/d), i = 0 .. d/2 - 1, evaluated in fp64 and split into an fp32
+// part with 12 significant bits and an fp32 remainder.  (A table of cos/sin values in fp16 measured a
+// log-sum-exp error of ~2e-3 with the x4 sink keys; one in fp32 costs four loads per key row.)
+__global__ void rope_theta_kernel(float2 *theta, int half, double base) {
+    const int i = threadIdx.x;
+    if (i >= half) return;
+    const double t = pow(base, -2.0 * i / (2.0 * half)) / 6.283185307179586476925286766559;
+    int ex = 0;
+    const double mant = frexp(t, &ex);                     // t = mant * 2^ex, mant in [0.5, 1)
+    const double hi = ldexp(floor(ldexp(mant, 12)), ex - 12);  // 12 significant bits
+    theta[i] = make_float2(static_cast<float>(hi), static_cast<float>(t - hi));
+}
+
+static size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
+
+size_t decode_rope_workspace_bytes(int BH, int d, int w) {
+    return align256(decode_workspace_bytes(BH, d, w)) + static_cast<size_t>(d / 2) * sizeof(float2);
+}
+
+int launch_decode_rope(const DecodeArgs &a, double base) {
+    if (a.t >= (int64_t(1) << 31)) return fail(SWA_ERR_UNSUPPORTED, "rope decode: t must be < 2^31");
+    if (a.w > 4096) return fail(SWA_ERR_UNSUPPORTED, "rope decode: w = %d > 4096 (exact angle reduction)", a.w);
+    const int nvalid = static_cast<int>(a.t + 1 < a.w ? a.t + 1 : a.w);
+    const int ns = decode_num_splits(a.BH, nvalid);
+    const int per_split = (nvalid + ns - 1) / ns;
+    const float sl2 = a.scale * 1.4426950408889634f;
+    const size_t need = decode_rope_workspace_bytes(a.BH, a.d, a.w);
+    if (!a.workspace || a.workspace_bytes < need)
+        return fail(SWA_ERR_INVALID, "rope decode needs a workspace of %zu bytes (got %zu)", need, a.workspace_bytes);
+    float2 *tab = reinterpret_cast<float2 *>(static_cast<char *>(a.workspace) +
+                                             align256(decode_workspace_bytes(a.BH, a.d, a.w)));
+    rope_theta_kernel<<<1, 64, 0, a.stream>>>(tab, a.d / 2, base);
+    const RopeArgs ra{tab, a.s, a.w - a.s, static_cast<int>(a.t)};
+    return dispatch_decode(a, nvalid, ns, per_split, sl2, &ra);
 }
 
 }  // namespace swa

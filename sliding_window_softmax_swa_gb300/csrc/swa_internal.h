@@ -59,6 +59,10 @@ struct DecodeArgs {
 int decode_num_splits(int BH, int nvalid);
 size_t decode_workspace_bytes(int BH, int d, int w);
 int launch_decode(const DecodeArgs &a);
+// The same decode with rotary embedding at positions inside the cache; the workspace also holds the
+// d/2 per-pair angle steps (in turns, split into an exactly-multipliable high part and a remainder).
+size_t decode_rope_workspace_bytes(int BH, int d, int w);
+int launch_decode_rope(const DecodeArgs &a, double base);
 // The same decode with its split-K scratch in a built-in device array (no workspace argument).
 size_t decode_noalloc_scratch_bytes();
 int launch_decode_noalloc(DecodeArgs a);

@@ -128,3 +128,19 @@ def test_bf16_prefill_rejects_windows_past_the_tile_list(lib):
     f = 1 << 20  # never dereferenced: the window check comes first
     rc = lib.swa_sink_prefill(f, f, f, f, None, None, None, 0, 1, 1, 9000, 128, 7400, 4, 0.1, swa.SWA_BF16, None)
     assert rc == swa.SWA_ERR_UNSUPPORTED
+
+
+def test_rope_decode_validates_before_launch(lib):
+    f = 1 << 20  # never dereferenced: validation fails first
+    need = lib.swa_sink_decode_rope_workspace_size(1, 1, 128, 64)
+    assert need >= 64 * 8  # the per-pair angle steps
+    ok = [f, f, f, f, None, 1, 1, 128, 64, 4, 10, 0.1, 10000.0, f << 8, need, 0, None]
+    bad = list(ok)
+    bad[12] = 1.0  # base must be > 1
+    assert lib.swa_sink_decode_step_rope(*bad) == swa.SWA_ERR_INVALID
+    bad = list(ok)
+    bad[14] = need - 1  # workspace too small
+    assert lib.swa_sink_decode_step_rope(*bad) == swa.SWA_ERR_INVALID
+    bad = list(ok)
+    bad[10] = 1 << 31  # t past 2^31 - 1
+    assert lib.swa_sink_decode_step_rope(*bad) == swa.SWA_ERR_INVALID

@@ -137,3 +137,56 @@ def test_decode_resume_from_copied_cache():
         swa.kv_rolling_write(kc2, vc2, k[:, :, t:t + 1].contiguous(), v[:, :, t:t + 1].contiguous(), w, s, t)
         o2 = swa.swa_sink_decode_step(q[:, :, t].contiguous(), kc2, vc2, t, w, s)
         assert torch.equal(o2, outs[t])
+
+
+# ------------------------------------------------- RoPE at the positions the entries have inside the cache
+@pytest.mark.parametrize("dtype,d,w,s,base", [
+    (torch.bfloat16, 128, 40, 4, 10000.0),
+    (torch.bfloat16, 64, 24, 0, 10000.0),
+    (torch.bfloat16, 16, 17, 16, 500.0),
+    (torch.float32, 16, 16, 4, 10000.0),
+    (torch.float32, 128, 9, 1, 10000.0),
+])
+def test_rope_streaming_decode_every_step(dtype, d, w, s, base):
+    # write unrotated keys, decode with positions re-assigned inside the cache, at every step against the
+    # oracle's history definition (through the window filling, the ring wrapping and long after)
+    swa = require_gpu()
+    B, H = 2, 3
+    T = 3 * w + 5
+    q, k, v = swa_inputs.prefill_inputs(B, H, T, d, 91 + d, dtype, "cpu", sink_boost=True)
+    kc = torch.zeros((B, H, w, d), dtype=dtype, device="cuda")
+    vc = torch.zeros_like(kc)
+    qg, kg, vg = q.cuda(), k.cuda(), v.cuda()
+    outs, lses = [], []
+    for t in range(T):
+        swa.kv_rolling_write(kc, vc, kg[:, :, t:t + 1].contiguous(), vg[:, :, t:t + 1].contiguous(), w, s, t)
+        lse = torch.empty((B, H), dtype=torch.float32, device="cuda")
+        o = swa.swa_sink_decode_step_rope(qg[:, :, t].contiguous(), kc, vc, t, w, s, rope_base=base, lse=lse)
+        outs.append(o.cpu())
+        lses.append(lse.cpu())
+    assert swa.swa_device_status() == swa.SWA_OK, swa.last_error()
+    scale = 1.0 / math.sqrt(d)
+    for t in range(T):
+        o_ref, l_ref = oracle.decode_rope(q[:, :, t].reshape(B * H, d), k[:, :, :t + 1].reshape(B * H, t + 1, d),
+                                          v[:, :, :t + 1].reshape(B * H, t + 1, d), t, w, s, scale, base)
+        compare(f"rope decode t={t}", outs[t].reshape(B * H, d), o_ref, dtype)
+        assert np.abs(lses[t].double().numpy().reshape(-1) - l_ref).max() < LSE_ABS
+
+
+@pytest.mark.parametrize("t", [0, 700, 2047, 2048, 3000, 9000])
+def test_rope_split_decode_long_window(t):
+    # few (b, h) rows and a long window: split-K over the cache with the rotation table
+    swa = require_gpu()
+    B, H, d, w, s = 1, 2, 128, 2048, 4
+    n = t + 1
+    q, k, v = swa_inputs.prefill_inputs(B, H, n, d, 500 + t, torch.bfloat16, "cpu", sink_boost=True)
+    kc = torch.zeros((B, H, w, d), dtype=torch.bfloat16, device="cuda")
+    vc = torch.zeros_like(kc)
+    swa.kv_rolling_write(kc, vc, k.cuda(), v.cuda(), w, s, 0)
+    lse = torch.empty((B, H), dtype=torch.float32, device="cuda")
+    o = swa.swa_sink_decode_step_rope(q[:, :, t].contiguous().cuda(), kc, vc, t, w, s, lse=lse)
+    assert swa.swa_device_status() == swa.SWA_OK, swa.last_error()
+    o_ref, l_ref = oracle.decode_rope(q[:, :, t].reshape(B * H, d), k.reshape(B * H, n, d), v.reshape(B * H, n, d),
+                                      t, w, s, 1.0 / math.sqrt(d))
+    compare(f"rope split decode t={t}", o.cpu().reshape(B * H, d), o_ref, torch.bfloat16)
+    assert np.abs(lse.cpu().double().numpy().reshape(-1) - l_ref).max() < LSE_ABS

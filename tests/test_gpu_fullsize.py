@@ -102,3 +102,40 @@ def test_full_size_streaming_decode():
         o_ref, l_ref = oracle.attend(qh, pos, kh, vh, pos, w, s, wl.scale)
         compare(f"decode bh={bh}", outs[:, j], o_ref[0], torch.bfloat16)
         assert np.abs(lses[:, j].cpu().double().numpy() - l_ref[0]).max() < LSE_ABS
+
+
+def test_full_size_streaming_decode_rope():
+    # the same 20480-step stream with RoPE at the positions inside the cache; 8 (b, h) rows are checked
+    # against the oracle's history definition at sampled steps (window filling, first wraps, deep in)
+    swa = require_gpu()
+    wl = swa_inputs.WORKLOADS["decode_llama13b_B64_w1024_s4_20480"]
+    B, H, d, w, s, T = wl.B, wl.H, wl.d, wl.w, wl.s, wl.L
+    qs = swa_inputs.normal((T, B, H, d), wl.seed, swa_inputs.TID_Q, torch.bfloat16, "cuda")
+    ks = swa_inputs.normal((T, B, H, d), wl.seed, swa_inputs.TID_K, torch.bfloat16, "cuda")
+    vs = swa_inputs.normal((T, B, H, d), wl.seed, swa_inputs.TID_V, torch.bfloat16, "cuda")
+    ks[:4] *= 4.0
+    kc = torch.zeros((B, H, w, d), dtype=torch.bfloat16, device="cuda")
+    vc = torch.zeros_like(kc)
+    pairs = torch.tensor([0, 1, 39, 40, 777, 1300, 2000, B * H - 1], device="cuda")
+    steps = sorted({0, 1, 3, 4, 5, 100, 1019, 1022, 1023, 1024, 1025, 1026, 2045, 2046, 2047, 3070, 4099, 7777,
+                    10000, 15000, T - 2, T - 1} | set(range(997, T, 997)))
+    outs = torch.empty((len(steps), len(pairs), d), dtype=torch.bfloat16, device="cuda")
+    lses = torch.empty((len(steps), len(pairs)), dtype=torch.float32, device="cuda")
+    o = torch.empty((B, H, d), dtype=torch.bfloat16, device="cuda")
+    lse = torch.empty((B, H), dtype=torch.float32, device="cuda")
+    ws = torch.empty(swa.lib().swa_sink_decode_rope_workspace_size(B, H, d, w), dtype=torch.uint8, device="cuda")
+    k_at = {t: i for i, t in enumerate(steps)}
+    for t in range(T):
+        swa.kv_rolling_write(kc, vc, ks[t].unsqueeze(2), vs[t].unsqueeze(2), w, s, t)
+        swa.swa_sink_decode_step_rope(qs[t], kc, vc, t, w, s, o=o, lse=lse, workspace=ws)
+        if t in k_at:
+            outs[k_at[t]] = o.reshape(B * H, d).index_select(0, pairs)
+            lses[k_at[t]] = lse.reshape(B * H).index_select(0, pairs)
+    assert swa.swa_device_status() == swa.SWA_OK, swa.last_error()
+    for j, bh in enumerate(pairs.tolist()):
+        b, h = divmod(bh, H)
+        qh, kh, vh = (x[:, b, h].float().cpu().numpy() for x in (qs, ks, vs))
+        for i, t in enumerate(steps):
+            o_ref, l_ref = oracle.decode_rope(qh[t][None], kh[None, :t + 1], vh[None, :t + 1], t, w, s, wl.scale)
+            compare(f"rope decode bh={bh} t={t}", outs[i, j][None], o_ref, torch.bfloat16)
+            assert abs(float(lses[i, j]) - l_ref[0]) < LSE_ABS
