@@ -484,7 +484,7 @@ def main():
             "roofline": {"bound": "hbm", "kernel": "decode_kernel (rope)", "achieved": r["kernel"]["gbs"],
                          "peak": peaks["hbm_gbs"], "unit": "GB/s", "frac": r["kernel"]["gbs"] / peaks["hbm_gbs"],
                          "avg_us": r["kernel"]["avg_us"],
-                         "note": "bytes = the cache K/V rows + q/o (the d/2 angle steps, 512 B, stay in L1/L2; sin/cos are computed in registers)"}}
+                         "note": "bytes = the cache K/V rows + q/o (the per-pair angle rates are kernel parameters; sin/cos are computed in registers)"}}
     ck = clocks.stop()
 
     if rank != 0:

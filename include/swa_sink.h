@@ -179,9 +179,11 @@ size_t swa_sink_decode_workspace_size(int B, int H, int d, int w);
  *             with unrotated keys.
  *   rope_base : the RoPE base (10000 for Llama-2), finite and > 1.
  *   workspace : caller-owned device scratch of at least swa_sink_decode_rope_workspace_size(B,H,d,w)
- *             bytes, 256-byte aligned; it holds the d/2 angle steps (written by the call) and the split-K
- *             partials.
- *   t < 2^31, w <= 4096 (SWA_ERR_UNSUPPORTED otherwise).  Other arguments and errors as
+ *             bytes (the split-K partials; 0 bytes when the step runs unsplit, and then it may be NULL),
+ *             256-byte aligned.
+ *   t < 2^31 and w <= 65536 (SWA_ERR_UNSUPPORTED otherwise).  The per-pair rate theta_i / 2 pi is
+ *   evaluated on the host in double and split in two fp32 parts so that whole turns drop out exactly
+ *   for every distance inside the cache; sin and cos are fp32.  Other arguments and errors as
  *   swa_sink_decode_step.
  */
 int swa_sink_decode_step_rope(const void *q, const void *k_cache, const void *v_cache, void *o, float *lse,

@@ -413,7 +413,7 @@ extern "C" int swa_sink_decode_step_rope(const void *q, const void *k_cache, con
     const size_t need = decode_rope_workspace_bytes(B * H, d, w);
     if (workspace_bytes < need)
         return fail(SWA_ERR_INVALID, "workspace of %zu bytes is smaller than the %zu needed", workspace_bytes, need);
-    if (!workspace || (reinterpret_cast<uintptr_t>(workspace) & 255u))
+    if (need > 0 && (!workspace || (reinterpret_cast<uintptr_t>(workspace) & 255u)))
         return fail(SWA_ERR_INVALID, "workspace must be non-null and 256-byte aligned");
     DecodeArgs a{q, k_cache, v_cache, o, lse, B * H, d, w, s, t, scale, workspace, workspace_bytes,
                  esize_of(dtype), static_cast<cudaStream_t>(stream)};

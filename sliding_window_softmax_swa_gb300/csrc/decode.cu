@@ -20,6 +20,8 @@
 // Scores are kept in log2 units (x = scale * log2(e) * q.k) so exp is a single exp2.
 #include <math.h>
 
+#include <cmath>
+
 #include <mutex>
 
 #include "../../include/swa_sink.h"
@@ -56,20 +58,35 @@ __device__ __forceinline__ void store_out(float *p, float x) { *p = x; }
 // With relative position delta = c_key - c_query the score of a pair is
 //     q_i (k_i cos - k_{i+D/2} sin) + q_{i+D/2} (k_i sin + k_{i+D/2} cos),  angle = delta * theta_i,
 // so the query stays unrotated and each key row meets cos/sin of its own delta.
+constexpr int kMaxRopePairs = 64;         // d <= 128
+constexpr int kMaxRopeWindowBits = 16;     // w <= 2^16
 struct RopeArgs {
-    // theta_i / (2 pi) for i = 0 .. D/2-1 as hi + lo: hi keeps 12 significant bits, so |delta| * hi
-    // (|delta| < 2^12) is exact in fp32 and its fraction of a turn loses nothing; lo carries the rest
-    const float2 *theta;   // [D/2]
-    int s, m;            // sinks, ring slots
-    int t;               // position of the query
+    // theta_i / (2 pi) in turns as hi + lo (fp32).  hi keeps 24 - k significant bits, where every distance
+    // inside the cache is below 2^k (k = ceil(log2 w)), so distance * hi is exact in fp32 and its whole
+    // turns drop out exactly; lo is the rest, and distance * lo rounds to within theta_i 2^(2k-47) turns.
+    float2 theta[kMaxRopePairs];
+    int s, m;  // sinks, ring slots
+    int t;     // position of the query
 };
 
+// sin and cos of the angle a * theta_i, reduced to [-pi, pi] as above
+__device__ __forceinline__ void rope_sincos(int a, float2 th, float &sn, float &c) {
+    const float fa = static_cast<float>(a);
+    float turns = fa * th.x;
+    turns -= rintf(turns);
+    turns = fmaf(fa, th.y, turns);
+    __sincosf(turns * 6.283185307179586f, &sn, &c);
+}
+
+// Blocks per SM in the launch bounds (measured): the plain form compiled for 1 keeps every load of a
+// block in flight in its 80 registers (7 % faster than the compiler's default of 60); the RoPE form
+// compiled for 3 stays at 80 registers, so three 256-thread blocks still fit on an SM.
 template <typename T, int D, int U, bool ROPE>
-__global__ void __launch_bounds__(kDecThreads) decode_kernel(const T *__restrict__ q, const T *__restrict__ kc,
+__global__ void __launch_bounds__(kDecThreads, ROPE ? 3 : 1) decode_kernel(const T *__restrict__ q, const T *__restrict__ kc,
                                                              const T *__restrict__ vc, T *__restrict__ o,
                                                              float *__restrict__ lse, float *__restrict__ part,
                                                              int w, int nvalid, int per_split, int nsplit,
-                                                             float scale_log2, RopeArgs ra) {
+                                                             float scale_log2, const __grid_constant__ RopeArgs ra) {
     constexpr int EPL = 16 / sizeof(T);  // elements per 16-byte chunk
     constexpr int LPR = D / EPL;         // lanes per cache row
     constexpr int RPW = 32 / LPR;        // rows per warp per load
@@ -115,7 +132,11 @@ __global__ void __launch_bounds__(kDecThreads) decode_kernel(const T *__restrict
         if (full) jnew = ra.s + (ra.t - ra.s) % ra.m;
         cq = nvalid - 1;  // the query's own key is the newest entry of the cache
 #pragma unroll
-        for (int p = 0; p < HPL; ++p) th[p] = __ldg(ra.theta + sub * HPL + p);
+        for (int p = 0; p < HPL; ++p) th[p] = ra.theta[sub * HPL + p];
+        // pin the rates in registers: re-reading them per row from the parameter bank, at 16 addresses per
+        // warp, serialises
+#pragma unroll
+        for (int p = 0; p < HPL; ++p) asm volatile("" : "+f"(th[p].x), "+f"(th[p].y));
     }
     const uint4 *kb = reinterpret_cast<const uint4 *>(kc + bh * w * D) + sub;
     const uint2 *kb2 = reinterpret_cast<const uint2 *>(kc + bh * w * D) + sub;
@@ -158,15 +179,10 @@ __global__ void __launch_bounds__(kDecThreads) decode_kernel(const T *__restrict
                 // full the query sits at w - 1, a sink j at j, and a ring slot at w - 1 - its age (how many
                 // ring writes ago it was written, counted back from the slot of position t).
                 const int ad = !full ? ra.t - j : (j < ra.s ? cq - j : (j <= jnew ? jnew - j : jnew - j + ra.m));
-                const float fad = static_cast<float>(ad);
 #pragma unroll
                 for (int p = 0; p < HPL; ++p) {
-                    // angle in turns, reduced to [-1/2, 1/2] exactly, then sin/cos of at most pi radians
-                    float turns = fad * th[p].x;
-                    turns -= rintf(turns);
-                    turns = fmaf(fad, th[p].y, turns);
                     float sn, c;
-                    __sincosf(turns * 6.283185307179586f, &sn, &c);
+                    rope_sincos(ad, th[p], sn, c);
                     // q . R(delta theta) k over the pair, with sin(delta theta) = -sin(|delta| theta):
                     // k_i (q_i c - q_{i+D/2} sn) + k_{i+D/2} (q_{i+D/2} c + q_i sn)
                     const float qa = qf[p], qb = qf[HPL + p];
@@ -320,39 +336,33 @@ int launch_decode(const DecodeArgs &a) {
     return dispatch_decode(a, nvalid, ns, per_split, sl2, nullptr);
 }
 
-// theta_i / (2 pi), theta_i = base^(-2i/d), i = 0 .. d/2 - 1, evaluated in fp64 and split into an fp32
-// part with 12 significant bits and an fp32 remainder.  (A table of cos/sin values in fp16 measured a
-// log-sum-exp error of ~2e-3 with the x4 sink keys; one in fp32 costs four loads per key row.)
-__global__ void rope_theta_kernel(float2 *theta, int half, double base) {
-    const int i = threadIdx.x;
-    if (i >= half) return;
-    const double t = pow(base, -2.0 * i / (2.0 * half)) / 6.283185307179586476925286766559;
-    int ex = 0;
-    const double mant = frexp(t, &ex);                     // t = mant * 2^ex, mant in [0.5, 1)
-    const double hi = ldexp(floor(ldexp(mant, 12)), ex - 12);  // 12 significant bits
-    theta[i] = make_float2(static_cast<float>(hi), static_cast<float>(t - hi));
-}
-
-static size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
-
-size_t decode_rope_workspace_bytes(int BH, int d, int w) {
-    return align256(decode_workspace_bytes(BH, d, w)) + static_cast<size_t>(d / 2) * sizeof(float2);
-}
+size_t decode_rope_workspace_bytes(int BH, int d, int w) { return decode_workspace_bytes(BH, d, w); }
 
 int launch_decode_rope(const DecodeArgs &a, double base) {
     if (a.t >= (int64_t(1) << 31)) return fail(SWA_ERR_UNSUPPORTED, "rope decode: t must be < 2^31");
-    if (a.w > 4096) return fail(SWA_ERR_UNSUPPORTED, "rope decode: w = %d > 4096 (exact angle reduction)", a.w);
+    if (a.d / 2 > kMaxRopePairs) return fail(SWA_ERR_UNSUPPORTED, "rope decode: d=%d", a.d);
+    if (a.w > (1 << kMaxRopeWindowBits))
+        return fail(SWA_ERR_UNSUPPORTED, "rope decode: w = %d > %d", a.w, 1 << kMaxRopeWindowBits);
     const int nvalid = static_cast<int>(a.t + 1 < a.w ? a.t + 1 : a.w);
     const int ns = decode_num_splits(a.BH, nvalid);
     const int per_split = (nvalid + ns - 1) / ns;
     const float sl2 = a.scale * 1.4426950408889634f;
-    const size_t need = decode_rope_workspace_bytes(a.BH, a.d, a.w);
-    if (!a.workspace || a.workspace_bytes < need)
-        return fail(SWA_ERR_INVALID, "rope decode needs a workspace of %zu bytes (got %zu)", need, a.workspace_bytes);
-    float2 *tab = reinterpret_cast<float2 *>(static_cast<char *>(a.workspace) +
-                                             align256(decode_workspace_bytes(a.BH, a.d, a.w)));
-    rope_theta_kernel<<<1, 64, 0, a.stream>>>(tab, a.d / 2, base);
-    const RopeArgs ra{tab, a.s, a.w - a.s, static_cast<int>(a.t)};
+    if (ns > 1 && (!a.workspace || a.workspace_bytes < static_cast<size_t>(a.BH) * ns * (a.d + 2) * sizeof(float)))
+        return fail(SWA_ERR_INVALID, "rope decode needs %d splits but the workspace is too small", ns);
+    RopeArgs ra{};
+    int k = 0;  // distances are 0 .. w - 1 < 2^k
+    while ((1 << k) < a.w) ++k;
+    // theta_i / (2 pi) = base^(-2i/d) / (2 pi), evaluated in double; hi = its leading 24 - k bits
+    for (int i = 0; i < a.d / 2; ++i) {
+        const double f = std::pow(base, -2.0 * i / a.d) / 6.283185307179586476925286766559;
+        int ex = 0;
+        const double mant = std::frexp(f, &ex);  // f = mant 2^ex, mant in [0.5, 1)
+        const double hi = std::ldexp(std::floor(std::ldexp(mant, 24 - k)), ex - (24 - k));
+        ra.theta[i] = make_float2(static_cast<float>(hi), static_cast<float>(f - hi));
+    }
+    ra.s = a.s;
+    ra.m = a.w - a.s;
+    ra.t = static_cast<int>(a.t);
     return dispatch_decode(a, nvalid, ns, per_split, sl2, &ra);
 }
 

@@ -132,9 +132,9 @@ def test_bf16_prefill_rejects_windows_past_the_tile_list(lib):
 
 def test_rope_decode_validates_before_launch(lib):
     f = 1 << 20  # never dereferenced: validation fails first
-    need = lib.swa_sink_decode_rope_workspace_size(1, 1, 128, 64)
-    assert need >= 64 * 8  # the per-pair angle steps
-    ok = [f, f, f, f, None, 1, 1, 128, 64, 4, 10, 0.1, 10000.0, f << 8, need, 0, None]
+    need = lib.swa_sink_decode_rope_workspace_size(1, 1, 128, 4096)
+    assert need == lib.swa_sink_decode_workspace_size(1, 1, 128, 4096) > 0  # split-K partials only
+    ok = [f, f, f, f, None, 1, 1, 128, 4096, 4, 5000, 0.1, 10000.0, f << 8, need, 0, None]
     bad = list(ok)
     bad[12] = 1.0  # base must be > 1
     assert lib.swa_sink_decode_step_rope(*bad) == swa.SWA_ERR_INVALID
@@ -144,3 +144,7 @@ def test_rope_decode_validates_before_launch(lib):
     bad = list(ok)
     bad[10] = 1 << 31  # t past 2^31 - 1
     assert lib.swa_sink_decode_step_rope(*bad) == swa.SWA_ERR_INVALID
+    bad = list(ok)
+    bad[8], bad[10] = 70000, 80000  # window past 2^16
+    bad[14] = lib.swa_sink_decode_rope_workspace_size(1, 1, 128, 70000)
+    assert lib.swa_sink_decode_step_rope(*bad) == swa.SWA_ERR_UNSUPPORTED

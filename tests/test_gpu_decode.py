@@ -173,20 +173,23 @@ def test_rope_streaming_decode_every_step(dtype, d, w, s, base):
         assert np.abs(lses[t].double().numpy().reshape(-1) - l_ref).max() < LSE_ABS
 
 
-@pytest.mark.parametrize("t", [0, 700, 2047, 2048, 3000, 9000])
-def test_rope_split_decode_long_window(t):
-    # few (b, h) rows and a long window: split-K over the cache with the rotation table
+@pytest.mark.parametrize("w,t,base", [(2048, 0, 1e4), (2048, 700, 1e4), (2048, 2047, 1e4), (2048, 2048, 1e4),
+                                      (2048, 3000, 1e4), (2048, 9000, 1e4), (16384, 16383, 1e4),
+                                      (16384, 40000, 1e4), (8192, 20000, 5e5)])
+def test_rope_split_decode_long_window(w, t, base):
+    # few (b, h) rows and a long window: split-K over the cache; distances up to w - 1 = 16383 and a base
+    # of 500000 check the angle reduction
     swa = require_gpu()
-    B, H, d, w, s = 1, 2, 128, 2048, 4
+    B, H, d, s = 1, 2, 128, 4
     n = t + 1
     q, k, v = swa_inputs.prefill_inputs(B, H, n, d, 500 + t, torch.bfloat16, "cpu", sink_boost=True)
     kc = torch.zeros((B, H, w, d), dtype=torch.bfloat16, device="cuda")
     vc = torch.zeros_like(kc)
     swa.kv_rolling_write(kc, vc, k.cuda(), v.cuda(), w, s, 0)
     lse = torch.empty((B, H), dtype=torch.float32, device="cuda")
-    o = swa.swa_sink_decode_step_rope(q[:, :, t].contiguous().cuda(), kc, vc, t, w, s, lse=lse)
+    o = swa.swa_sink_decode_step_rope(q[:, :, t].contiguous().cuda(), kc, vc, t, w, s, rope_base=base, lse=lse)
     assert swa.swa_device_status() == swa.SWA_OK, swa.last_error()
     o_ref, l_ref = oracle.decode_rope(q[:, :, t].reshape(B * H, d), k.reshape(B * H, n, d), v.reshape(B * H, n, d),
-                                      t, w, s, 1.0 / math.sqrt(d))
+                                      t, w, s, 1.0 / math.sqrt(d), base)
     compare(f"rope split decode t={t}", o.cpu().reshape(B * H, d), o_ref, torch.bfloat16)
     assert np.abs(lse.cpu().double().numpy().reshape(-1) - l_ref).max() < LSE_ABS
