@@ -193,7 +193,9 @@ def time_loop(step, steps, warmup, world, clocks):
     return reduce_max(e0.elapsed_time(e1) / 1e3, world)
 
 
-def prefill_leg(swa, wl, steps, warmup, world, rank, clocks, e2e=False):
+def prefill_leg(swa, wl, steps, warmup, world, rank, clocks, e2e=False, rope=False):
+    """Prefill steps; with ``rope`` the RoPE prefill at the positions inside the cache (base 10000): a
+    rotation pass over q and k, then the tensor-core prefill on the rotated rows (2 launches a step)."""
     import torch
     import swa_inputs
     B, H, L, d, w, s = wl.B, wl.H, wl.L, wl.d, wl.w, wl.s
@@ -201,11 +203,20 @@ def prefill_leg(swa, wl, steps, warmup, world, rank, clocks, e2e=False):
     o = torch.empty_like(q)
     lib = swa.lib()
     stream = torch.cuda.current_stream().cuda_stream
-    args = (q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(), None, None, None, 0, B, H, L, d, w, s,
-            wl.scale, 0 if wl.dtype == "bf16" else 1, stream)
+    dt = 0 if wl.dtype == "bf16" else 1
+    if rope:
+        nws = lib.swa_sink_prefill_rope_workspace_size(B, H, L, d)
+        ws = torch.empty(nws, dtype=torch.uint8, device="cuda")
+        args = (q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(), None, B, H, L, d, w, s, wl.scale, 10000.0,
+                ws.data_ptr(), nws, dt, stream)
+        call = lib.swa_sink_prefill_rope
+    else:
+        args = (q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(), None, None, None, 0, B, H, L, d, w, s,
+                wl.scale, dt, stream)
+        call = lib.swa_sink_prefill
 
     def step():
-        rc = lib.swa_sink_prefill(*args)
+        rc = call(*args)
         if rc:
             raise RuntimeError(swa.last_error())
 
@@ -213,7 +224,7 @@ def prefill_leg(swa, wl, steps, warmup, world, rank, clocks, e2e=False):
     _check_status(swa)
     flops = banded_flops(B, H, L, d, w)
     res = {"flops_per_step": flops, "seconds": t, "steps": steps, "tflops": flops * steps / t / 1e12,
-           "ms_per_step": t / steps * 1e3, "launches": steps}
+           "ms_per_step": t / steps * 1e3, "launches": (2 if rope else 1) * steps}
     if e2e:
         # the same prefill through the public host-buffer call: every step copies q/k/v from pinned host
         # memory and o back (the library pipelines the copies against the compute over row groups)
@@ -418,7 +429,7 @@ def main():
     ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--primary-only", action="store_true", help="only the primary prefill leg")
-    ap.add_argument("--legs", default="primary,mistral,chunked,decode,decode_rope",
+    ap.add_argument("--legs", default="primary,mistral,chunked,decode,decode_rope,prefill_rope",
                     help="comma list of legs to run (profiling runs pick one)")
     ap.add_argument("--decode-steps", type=int, default=None, help="shorter decode stream (profiling only)")
     args = ap.parse_args()
@@ -458,6 +469,13 @@ def main():
             secondary[name] = {"metric": METRIC, "value": aggregate_rate(r["tflops"], world, 1.0), "unit": "TFLOP/s",
                                "ms_per_step": r["ms_per_step"],
                                "frac_of_bf16_peak": r["tflops"] / peaks["bf16_tflops"]}
+    if "prefill_rope" in legs:
+        r = prefill_leg(swa, wl, max(3, args.steps // 2), 3, world, rank, clocks, rope=True)
+        secondary["prefill_rope_llama7b_L8192_w1024_s4"] = {
+            "metric": METRIC, "value": aggregate_rate(r["tflops"], world, 1.0), "unit": "TFLOP/s",
+            "ms_per_step": r["ms_per_step"], "frac_of_bf16_peak": r["tflops"] / peaks["bf16_tflops"],
+            "what": "RoPE at the positions inside the cache (base 10000): rotation pass + tensor-core prefill",
+            "launches_per_step": 2}
     if "chunked" in legs:
         cw = swa_inputs.WORKLOADS["chunked_mistral_L131072_w4096_s4_C4096"]
         r = chunked_leg(swa, cw, 3, 1, world, rank, clocks)

@@ -92,6 +92,27 @@ int swa_sink_prefill_host(const void *q_h, const void *k_h, const void *v_h, voi
                           int B, int H, int64_t L, int d, int w, int s, float scale, int dtype, void *stream);
 
 /*
+ * swa_sink_prefill_rope -- swa_sink_prefill (pos0 = 0) with rotary position embedding at the positions
+ * the keys have inside the cache of the StreamingLLM section of "滑窗与固定稀疏": for query t the cache holds
+ * K(t), sinks first and then the window in order, at positions 0 .. |K(t)| - 1, and the query is the
+ * newest entry.  This equals plain RoPE (q at t, key i at i) for the window keys and puts the query at
+ * min(t, w - 1) for the sink scores.  RoPE rotates dimension pair (i, i + d/2) by position *
+ * rope_base^(-2i/d).  Row t equals swa_sink_decode_step_rope at step t over the same keys.
+ *
+ *   q, k, v, o, lse : as swa_sink_prefill, with q and k unrotated; bf16, d = 128, contiguous.
+ *   rope_base : finite and > 1.
+ *   workspace : caller-owned device scratch of swa_sink_prefill_rope_workspace_size(B, H, L, d) bytes
+ *             (3 x B*H*L*d bf16: the rotated q, the sink-rotated q and the rotated k), 256-byte aligned.
+ *   s <= 128, pos0 = 0 only (SWA_ERR_UNSUPPORTED otherwise).  The rotated q and k are rounded to bf16
+ *   before the tensor-core products, which adds up to 2^-8 relative error per product term to the
+ *   scores.  Other arguments and errors as swa_sink_prefill.
+ */
+int swa_sink_prefill_rope(const void *q, const void *k, const void *v, void *o, float *lse, int B, int H,
+                          int64_t L, int d, int w, int s, float scale, double rope_base, void *workspace,
+                          size_t workspace_bytes, int dtype, void *stream);
+size_t swa_sink_prefill_rope_workspace_size(int B, int H, int64_t L, int d);
+
+/*
  * swa_sink_prefill_chunked -- the chunk-based prefill of "滑窗与固定稀疏" (rolling-buffer section):
  * the L positions are processed in chunks of `chunk` rows; chunk c attends the rolling cache as it was
  * before the chunk plus its own keys (swa_sink_prefill with pos0 = c*chunk), then its keys/values are
@@ -231,6 +252,9 @@ int swa_selftest_umma(const void *a, const void *b, float *c, int mode, void *st
  * swa_status.
  */
 int swa_prefill_tile_plan(int64_t q0, int64_t q1, int64_t pos0, int w, int s, int *tiles, int max_tiles);
+/* The same for swa_sink_prefill_rope (pos0 = 0): the sinks form the first tile on their own, the band
+ * starts at position s.  s <= 128. */
+int swa_prefill_tile_plan_rope(int64_t q0, int64_t q1, int w, int s, int *tiles, int max_tiles);
 
 #ifdef __cplusplus
 }

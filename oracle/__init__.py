@@ -16,8 +16,8 @@ It follows the SWA formula of the hyper.ai summary of arXiv 2608.28444 (section
 addition to the w - 4 window keys), equation (1) of "模糊窗口注意力" section 2.1 (causal softmax
 attention) and eq attn-fixed-softmax-sink of "滑窗与固定稀疏" (row normalisation).
 
-``rope`` and ``decode_rope`` state the streaming decode with positions re-assigned inside the cache
-and rotary embedding (StreamingLLM section of "滑窗与固定稀疏").
+``rope``, ``decode_rope`` and ``prefill_rope`` state the streaming decode and the prefill with
+positions re-assigned inside the cache and rotary embedding (StreamingLLM section of "滑窗与固定稀疏").
 
 Parity status: every function here is pinned by ``tests/test_oracle.py`` against closed forms,
 textbook special cases and hand-derived golden values (``tests/golden/``).
@@ -201,6 +201,26 @@ def decode_rope(q_t, k_hist, v_hist, t: int, w: int, s: int, scale: float, base:
     q_rot = rope(q_t[:, None, :], np.array([len(members) - 1.0]), base)
     o, lse = attend(q_rot, np.array([t], dtype=np.int64), k_rot, v_sel, members, w, s, scale, nthreads)
     return o.reshape(nh, d), lse.reshape(nh)
+
+
+def prefill_rope(q, k, v, w: int, s: int, scale: float, base: float = 10000.0, rows=None,
+                 nthreads: int | None = None):
+    """Prefill with positions re-assigned inside the cache (StreamingLLM section of "滑窗与固定稀疏"):
+    row t is the streaming decode at step t over the same unrotated keys (``decode_rope``), i.e. the
+    members of K(t) take cache positions 0 .. |K(t)| - 1 and the query the last of them.
+
+    q, k, v: [B, H, L, d] unrotated; ``rows``: query positions to compute (default all).
+    Returns (o [B, H, len(rows), d], lse [B, H, len(rows)]).
+    """
+    q, k, v = _f64(q), _f64(k), _f64(v)
+    B, H, L, d = q.shape
+    rows = list(range(L)) if rows is None else [int(t) for t in rows]
+    o = np.empty((B * H, len(rows), d))
+    lse = np.empty((B * H, len(rows)))
+    qf, kf, vf = q.reshape(B * H, L, d), k.reshape(B * H, L, d), v.reshape(B * H, L, d)
+    for j, t in enumerate(rows):
+        o[:, j], lse[:, j] = decode_rope(qf[:, t], kf[:, :t + 1], vf[:, :t + 1], t, w, s, scale, base, nthreads)
+    return o.reshape(B, H, len(rows), d), lse.reshape(B, H, len(rows))
 
 
 def cache_replay(w: int, s: int, npos: int) -> np.ndarray:

@@ -1,15 +1,18 @@
 """GB300 (sm_103a) library for causal sliding-window softmax attention with attention sinks.
 
 Prefill (TMA + tcgen05 tensor cores), chunked prefill through a rolling KV cache, and streaming decode
-(split-K over the cache), behind the C ABI of include/swa_sink.h. This package is the thin Python
-binding of that ABI; the kernels live in csrc/ and are built with ``build.build()``.
+(split-K over the cache), with or without RoPE at the positions inside the cache, behind the C ABI of
+include/swa_sink.h. This package is the thin Python binding of that ABI; the kernels live in csrc/ and are
+built with ``build.build()``.
 """
 from ._binding import (SWA_BF16, SWA_ERR_CUDA, SWA_ERR_INVALID, SWA_ERR_TIMEOUT, SWA_ERR_UNSUPPORTED, SWA_F32,
                        SWA_OK, SIGNATURES, SwaError, kv_rolling_write, last_error, lib, library_path,
-                       prefill_tile_plan, swa_device_status, swa_sink_decode_step, swa_sink_decode_step_rope, swa_sink_decode_workspace_size, swa_sink_prefill,
-                       swa_sink_prefill_chunked, swa_sink_prefill_host)
+                       prefill_tile_plan, prefill_tile_plan_rope, swa_device_status, swa_sink_decode_step,
+                       swa_sink_decode_step_rope, swa_sink_decode_workspace_size, swa_sink_prefill,
+                       swa_sink_prefill_chunked, swa_sink_prefill_host, swa_sink_prefill_rope)
 
-__all__ = ["swa_sink_prefill", "swa_sink_prefill_chunked", "swa_sink_prefill_host", "kv_rolling_write", "swa_sink_decode_step", "swa_sink_decode_step_rope",
-           "swa_sink_decode_workspace_size", "swa_device_status", "prefill_tile_plan", "last_error", "lib", "library_path",
-           "SwaError", "SIGNATURES", "SWA_OK", "SWA_ERR_INVALID", "SWA_ERR_UNSUPPORTED", "SWA_ERR_CUDA",
-           "SWA_ERR_TIMEOUT", "SWA_BF16", "SWA_F32"]
+__all__ = ["swa_sink_prefill", "swa_sink_prefill_chunked", "swa_sink_prefill_host", "swa_sink_prefill_rope",
+           "kv_rolling_write", "swa_sink_decode_step", "swa_sink_decode_step_rope",
+           "swa_sink_decode_workspace_size", "swa_device_status", "prefill_tile_plan", "prefill_tile_plan_rope",
+           "last_error", "lib", "library_path", "SwaError", "SIGNATURES", "SWA_OK", "SWA_ERR_INVALID",
+           "SWA_ERR_UNSUPPORTED", "SWA_ERR_CUDA", "SWA_ERR_TIMEOUT", "SWA_BF16", "SWA_F32"]

@@ -446,8 +446,49 @@ extern "C" int swa_prefill_tile_plan(int64_t q0, int64_t q1, int64_t pos0, int w
     if (pos0 < 0 || q0 < pos0 || q1 < q0 || q1 >= (int64_t(1) << 31))
         return fail(SWA_ERR_INVALID, "need 0 <= pos0 <= q0 <= q1 < 2^31");
     if (!tiles || max_tiles < 0) return fail(SWA_ERR_INVALID, "tiles must be non-null");
-    return prefill_tile_plan(static_cast<int>(q0), static_cast<int>(q1), static_cast<int>(pos0), w, s, tiles,
+    return prefill_tile_plan(static_cast<int>(q0), static_cast<int>(q1), static_cast<int>(pos0), w, s, 0, tiles,
                              max_tiles);
+}
+
+extern "C" int swa_prefill_tile_plan_rope(int64_t q0, int64_t q1, int w, int s, int *tiles, int max_tiles) {
+    t_err[0] = 0;
+    if (w < 1 || s < 0 || s >= w) return fail(SWA_ERR_INVALID, "need 0 <= s < w (s=%d, w=%d)", s, w);
+    if (s > 128) return fail(SWA_ERR_UNSUPPORTED, "RoPE prefill needs s <= 128");
+    if (q0 < 0 || q1 < q0 || q1 >= (int64_t(1) << 31)) return fail(SWA_ERR_INVALID, "need 0 <= q0 <= q1 < 2^31");
+    if (!tiles || max_tiles < 0) return fail(SWA_ERR_INVALID, "tiles must be non-null");
+    return prefill_tile_plan(static_cast<int>(q0), static_cast<int>(q1), 0, w, s, 1, tiles, max_tiles);
+}
+
+extern "C" size_t swa_sink_prefill_rope_workspace_size(int B, int H, int64_t L, int d) {
+    if (B < 1 || H < 1 || L < 0 || d != 128) return 0;
+    return rope_prefill_workspace_bytes(B * H, L, d);
+}
+
+extern "C" int swa_sink_prefill_rope(const void *q, const void *k, const void *v, void *o, float *lse, int B, int H,
+                                     int64_t L, int d, int w, int s, float scale, double rope_base, void *workspace,
+                                     size_t workspace_bytes, int dtype, void *stream) {
+    t_err[0] = 0;
+    int rc = check_prefill(q, k, v, o, lse, 0, B, H, L, d, w, s, scale, dtype);
+    if (rc) return rc;
+    if (dtype != SWA_BF16 || d != 128) return fail(SWA_ERR_UNSUPPORTED, "RoPE prefill runs on bf16 with d = 128");
+    if (s > 128) return fail(SWA_ERR_UNSUPPORTED, "RoPE prefill needs s <= 128 (s=%d)", s);
+    if (!(rope_base == rope_base) || rope_base <= 1.0 || rope_base > 1e30)
+        return fail(SWA_ERR_INVALID, "rope_base must be a finite number > 1");
+    const size_t need = rope_prefill_workspace_bytes(B * H, L, d);
+    if (workspace_bytes < need)
+        return fail(SWA_ERR_INVALID, "workspace of %zu bytes is smaller than the %zu needed", workspace_bytes, need);
+    if (L == 0) return SWA_OK;
+    if (!workspace || (reinterpret_cast<uintptr_t>(workspace) & 255u))
+        return fail(SWA_ERR_INVALID, "workspace must be non-null and 256-byte aligned");
+    const cudaStream_t st = static_cast<cudaStream_t>(stream);
+    char *ws = static_cast<char *>(workspace);
+    const size_t one = need / 3;  // one [B, H, L, d] bf16 tensor; a multiple of 256 bytes
+    void *qr = ws, *qs = ws + one, *kr = ws + 2 * one;
+    rc = launch_rope_prep(q, k, qr, qs, kr, B * H, L, d, w, rope_base, st);
+    if (rc) return rc;
+    PrefillArgs a{qr, kr, v, o, lse, nullptr, nullptr, 0, B * H, L, d, w, s, scale, L, st};
+    a.q_sink = qs;
+    return launch_prefill_bf16_tc(a);
 }
 
 extern "C" int swa_sink_decode_step_noalloc(const void *q, const void *k_cache, const void *v_cache, void *o,

@@ -99,19 +99,23 @@ static_assert(sizeof(Tile) == 12, "tile record");
 
 struct Params {
     CUtensorMap tm_q, tm_k, tm_v, tm_kc, tm_vc;
+    CUtensorMap tm_qs;  // RoPE mode: query rows rotated for the sink keys
     void *o;
     float *lse;
     DeviceStatus *status;
     int64_t seq_stride;  // rows between (b, h) blocks of q/k/v/o/lse
     int L, pos0, w, s, m, BH;
+    int rope;  // RoPE mode: the sink tile (first in every list) is scored with tm_qs, the band with tm_q
     int n_qpairs, n_items;  // 256-row query pairs per (b, h); work items = n_qpairs * BH
     float scale_log2;
     uint32_t timeout_us;
 };
 
 // Build the key-tile list of the query tile [q0, q1] (absolute positions).  Returns the tile count
-// (entries past MAX_TILES are not stored; the caller treats a larger count as an error).
-__host__ __device__ int build_tiles(Tile *tl, int q0, int q1, int pos0, int s, int m, int w) {
+// (entries past MAX_TILES are not stored; the caller treats a larger count as an error).  In RoPE mode
+// (pos0 == 0, s <= BN) the sinks [0, min(s, q1 + 1)) always form the first tile, on their own, and the band
+// starts at position s: the sink scores use another query rotation than the band's.
+__host__ __device__ int build_tiles(Tile *tl, int q0, int q1, int pos0, int s, int m, int w, bool rope) {
     int n = 0;
     auto add_range = [&](int src, int pa, int pb, int rowbase) {  // positions [pa, pb]; row = p - rowbase
         for (int p = pa; p <= pb; p += BN) {
@@ -124,8 +128,12 @@ __host__ __device__ int build_tiles(Tile *tl, int q0, int q1, int pos0, int s, i
             ++n;
         }
     };
-    const int blo = q0 - m + 1 > 0 ? q0 - m + 1 : 0;
-    const int sink_hi = s < blo ? s : blo;  // sinks [0, sink_hi) are not inside the band range
+    int blo = q0 - m + 1 > 0 ? q0 - m + 1 : 0;
+    int sink_hi = s < blo ? s : blo;  // sinks [0, sink_hi) are not inside the band range
+    if (rope) {
+        sink_hi = s < q1 + 1 ? s : q1 + 1;
+        blo = blo > s ? blo : s;
+    }
     const int sink_cache = sink_hi < pos0 ? sink_hi : pos0;
     // sinks first: their scores tend to be the largest, which keeps later rescales rare
     if (sink_cache > 0) add_range(1, 0, sink_cache - 1, 0);
@@ -388,7 +396,7 @@ __global__ void __launch_bounds__(kThreads, 1) swa_prefill_tc_kernel(const __gri
                 const int b = it & 1;
                 if (it >= 2 && !mbar_wait(&lfree[b], ((it - 2) >> 1) & 1, wc, 12, it)) break;
                 Tile *tl = tiles_s + b * MAX_TILES;
-                const int n = build_tiles(tl, q0, qlast, P.pos0, P.s, P.m, P.w);
+                const int n = build_tiles(tl, q0, qlast, P.pos0, P.s, P.m, P.w, P.rope != 0);
                 if (n < 1 || n > MAX_TILES) {
                     atomicOr(&P.status->word, kDevBadArg);
                     *abort_flag = 1;
@@ -397,22 +405,37 @@ __global__ void __launch_bounds__(kThreads, 1) swa_prefill_tc_kernel(const __gri
                 mark_tiles(tl, n, q0, qlast, P.s, P.m);
                 ntiles_s[b] = n;
                 mbar_arrive(&lready[b]);  // release: the list is visible to whoever sees the phase complete
-                if (it >= 1 && !mbar_wait(qempty, (it - 1) & 1, wc, 13, it)) break;
-                uint8_t *qs = sm + OFF_Q;
-                mbar_arrive_expect_tx(qfull, 2 * TILE_BYTES);
-                for (int x = 0; x < 2; ++x) {
-                    tma_load_3d(qs + x * TILE_BYTES, &P.tm_q, qfull, 0, row_start + x * BH_ROWS, bh);
-                    tma_load_3d(qs + x * TILE_BYTES + HALF_BYTES, &P.tm_q, qfull, 64, row_start + x * BH_ROWS, bh);
-                }
-                ++nq;
-                const int nitem = item + G;
-                if (nitem < P.n_items) {
-                    const int nrow = (P.n_qpairs - 1 - nitem / P.BH) * BM;
+                // Q loads of the item: one (tm_q), or in RoPE mode with sinks the sink-rotated rows for
+                // the first tile and then, once its QK products are done, the band-rotated rows.  Every
+                // load waits until the QK products of the previous one are done.
+                const CUtensorMap *mq0 = (P.rope && P.s > 0) ? &P.tm_qs : &P.tm_q;
+                const bool two = P.rope && P.s > 0 && n >= 2;
+                bool ok = true;
+                for (int ph = 0; ph < (two ? 2 : 1) && ok; ++ph) {
+                    const CUtensorMap *mq = ph == 0 ? mq0 : &P.tm_q;
+                    if (nq >= 1 && !mbar_wait(qempty, (nq - 1) & 1, wc, 13, it)) {
+                        ok = false;
+                        break;
+                    }
+                    uint8_t *qs = sm + OFF_Q;
+                    mbar_arrive_expect_tx(qfull, 2 * TILE_BYTES);
                     for (int x = 0; x < 2; ++x) {
-                        tma_prefetch_3d(&P.tm_q, 0, nrow + x * BH_ROWS, nitem % P.BH);
-                        tma_prefetch_3d(&P.tm_q, 64, nrow + x * BH_ROWS, nitem % P.BH);
+                        tma_load_3d(qs + x * TILE_BYTES, mq, qfull, 0, row_start + x * BH_ROWS, bh);
+                        tma_load_3d(qs + x * TILE_BYTES + HALF_BYTES, mq, qfull, 64, row_start + x * BH_ROWS, bh);
+                    }
+                    ++nq;
+                    // into L2 meanwhile: the band rows of this item (RoPE), else the next item's first rows
+                    const int nitem = (two && ph == 0) ? item : item + G;
+                    const CUtensorMap *mp = (two && ph == 0) ? &P.tm_q : mq0;
+                    if (nitem < P.n_items) {
+                        const int nrow = (P.n_qpairs - 1 - nitem / P.BH) * BM;
+                        for (int x = 0; x < 2; ++x) {
+                            tma_prefetch_3d(mp, 0, nrow + x * BH_ROWS, nitem % P.BH);
+                            tma_prefetch_3d(mp, 64, nrow + x * BH_ROWS, nitem % P.BH);
+                        }
                     }
                 }
+                if (!ok) break;
             }
             if (*abort_flag && nq > 0) mbar_wait_drain(qfull, (nq - 1) & 1);  // no copy may still be landing
         }
@@ -428,14 +451,19 @@ __global__ void __launch_bounds__(kThreads, 1) swa_prefill_tc_kernel(const __gri
             int gk = 0, gv = 0;                // K, V tiles consumed
             int cp[2] = {0, 0};                // PV_x products issued (pfull parity)
             int ce[2] = {0, 0};                // items in which query tile x had PV products (oempty)
+            int nqf = 0;                       // Q loads consumed (qfull parity)
             for (int it = 0; fine; ++it) {
                 const int item = static_cast<int>(blockIdx.x) + it * G;
                 if (item >= P.n_items) break;
                 const int b = it & 1;
                 if (!mbar_wait(&lready[b], (it >> 1) & 1, wc, 14, it)) break;  // the item's tile list
-                if (!mbar_wait(qfull, it & 1, wc, 2, it)) break;                 // Q of this item
+                if (!mbar_wait(qfull, nqf & 1, wc, 2, it)) break;                // Q of this item
+                ++nqf;
                 const Tile *tl = tiles_s + b * MAX_TILES;
                 const int n = ntiles_s[b];
+                // RoPE mode with sinks: tile 0 (the sinks) uses the first Q load, the band a second one
+                const bool two = P.rope && P.s > 0 && n >= 2;
+                bool q_band = !two;
                 int last_used[2] = {-1, -1};
                 for (int j = 0; j < n; ++j)
                     for (int x = 0; x < 2; ++x)
@@ -450,7 +478,7 @@ __global__ void __launch_bounds__(kThreads, 1) swa_prefill_tc_kernel(const __gri
                             umma_commit(&sfull[x]);
                         }
                     }
-                    if (n == 1) umma_commit(qempty);
+                    if (n == 1 || two) umma_commit(qempty);  // the first Q load is no longer read
                     umma_commit(&kempty[gk % NK]);
                     ++gk;
                     issued_any = true;
@@ -482,6 +510,11 @@ __global__ void __launch_bounds__(kThreads, 1) swa_prefill_tc_kernel(const __gri
                             if (!k_ready) {
                                 if (!mbar_wait(&kfull[sk], (gk / NK) & 1, wc, 3, j + 1)) { fine = false; break; }
                                 k_ready = true;
+                            }
+                            if (!q_band) {  // the band-rotated Q rows
+                                if (!mbar_wait(qfull, nqf & 1, wc, 2, j + 1)) { fine = false; break; }
+                                ++nqf;
+                                q_band = true;
                             }
                             tc_fence_after();
                             issue_qk(tmem + col_s(x), q_addr + x * TILE_BYTES, k_addr0 + sk * TILE_BYTES);
@@ -806,7 +839,10 @@ static int sm_count() {
 int launch_prefill_bf16_tc(const PrefillArgs &a) {
     using namespace tc;
     if (a.d != HD) return fail(SWA_ERR_UNSUPPORTED, "tensor-core prefill needs d = %d", HD);
-    if (max_tiles_bound(a.w, a.s) > MAX_TILES)
+    const bool rope = a.q_sink != nullptr;
+    if (rope && (a.pos0 != 0 || a.s > BN))
+        return fail(SWA_ERR_UNSUPPORTED, "RoPE prefill needs pos0 = 0 and s <= %d", BN);
+    if (max_tiles_bound(a.w, a.s) + (rope ? 1 : 0) > MAX_TILES)
         return fail(SWA_ERR_UNSUPPORTED, "window w=%d needs more than %d key tiles per query tile", a.w, MAX_TILES);
     if ((a.L + BM - 1) / BM * a.BH > 0x7FFFFFFF) return fail(SWA_ERR_UNSUPPORTED, "too many work items");
     if (!encode_tiled_fn()) return fail(SWA_ERR_CUDA, "cuTensorMapEncodeTiled is not available");
@@ -827,7 +863,9 @@ int launch_prefill_bf16_tc(const PrefillArgs &a) {
     }
     else
         okm = okm && encode_rows_map(&p.tm_kc, a.k, L, a.BH, st) && encode_rows_map(&p.tm_vc, a.v, L, a.BH, st);
+    okm = okm && encode_rows_map(&p.tm_qs, rope ? a.q_sink : a.q, L, a.BH, st);
     if (!okm) return fail(SWA_ERR_INVALID, "cuTensorMapEncodeTiled rejected a tensor (alignment or size)");
+    p.rope = rope ? 1 : 0;
     p.o = a.o;
     p.lse = a.lse;
     p.status = reinterpret_cast<DeviceStatus *>(status);
@@ -855,9 +893,9 @@ int launch_prefill_bf16_tc(const PrefillArgs &a) {
     return SWA_OK;
 }
 
-int prefill_tile_plan(int q0, int q1, int pos0, int w, int s, int *out, int max_tiles) {
+int prefill_tile_plan(int q0, int q1, int pos0, int w, int s, int rope, int *out, int max_tiles) {
     tc::Tile tl[tc::MAX_TILES];
-    const int n = tc::build_tiles(tl, q0, q1, pos0, s, w - s, w);
+    const int n = tc::build_tiles(tl, q0, q1, pos0, s, w - s, w, rope != 0);
     tc::mark_tiles(tl, n, q0, q1, s, w - s);
     for (int i = 0; i < n && i < max_tiles && i < tc::MAX_TILES; ++i) {
         out[5 * i + 0] = tl[i].flags & 1;

@@ -1,0 +1,135 @@
+// rope.cu -- the rotation pass of prefill with RoPE at the positions inside the cache.
+//
+// The StreamingLLM section of "滑窗与固定稀疏" gives every entry of the cache its position inside the cache
+// (sinks 0..s-1, then the recent keys in order) rather than its position in the text.  For a whole
+// sequence that rule differs from plain RoPE in one place only: the query of row t scores its window keys
+// at distance t - i, as plain RoPE does, but the sinks at distance min(t, w - 1) - i, because once the
+// cache is full the query sits at position w - 1.  So the tensor-core prefill runs on
+//     Qr = R(t) q_t,  Kr = R(i) k_i   (band tiles)   and   Qs = R(min(t, w - 1)) q_t   (the sink tile),
+// which this pass writes, bf16, into the caller's workspace.  R(a) rotates the half-split pair
+// (x_i, x_{i+d/2}) by a * base^(-2i/d): (x cos - y sin, x sin + y cos).
+//
+// Angles are reduced exactly for every position < 2^31: theta_i / (2 pi) is held as the 64-bit fraction
+// F_i = round(2^64 theta_i / (2 pi)) (host, double), and the fraction of a turn of a * theta_i is
+// (a F_i) mod 2^64, whose top 32 bits are a * F_hi + umulhi(a, F_lo).  The error is that of F_i, at most
+// a * 2^-65 turns; sin and cos are fp32.  The pass is HBM-bound: per row it reads q and k and writes three
+// rows (5 x 256 bytes at d = 128), 16 lanes per row, each lane holding both halves of its 4 pairs.
+#include <cuda_bf16.h>
+
+#include <cmath>
+
+#include "../../include/swa_sink.h"
+#include "swa_device.cuh"
+#include "swa_internal.h"
+
+namespace swa {
+
+constexpr int kRopeD = 128;
+constexpr int kRopeLanes = 16;               // lanes per row
+constexpr int kRopePpl = kRopeD / 2 / kRopeLanes;  // pairs per lane (4)
+
+struct RopePrep {
+    uint2 frac[kRopeD / 2];  // F_i as (low 32 bits, high 32 bits)
+};
+
+__device__ __forceinline__ void turn_sincos(uint32_t a, uint2 f, float &sn, float &c) {
+    const uint32_t top = a * f.y + __umulhi(a, f.x);                                        // (a F) >> 32, mod 2^32
+    const float turns = static_cast<float>(static_cast<int32_t>(top)) * 2.3283064365386963e-10f;  // [-1/2, 1/2)
+    __sincosf(turns * 6.283185307179586f, &sn, &c);
+}
+
+__device__ __forceinline__ void unpack4(uint2 u, float (&f)[4]) {
+    f[0] = __uint_as_float(u.x << 16);
+    f[1] = __uint_as_float(u.x & 0xFFFF0000u);
+    f[2] = __uint_as_float(u.y << 16);
+    f[3] = __uint_as_float(u.y & 0xFFFF0000u);
+}
+
+__device__ __forceinline__ uint32_t pack2(float lo, float hi) {
+    const __nv_bfloat162 h = __floats2bfloat162_rn(lo, hi);
+    return *reinterpret_cast<const uint32_t *>(&h);
+}
+
+// Rotates the pairs (a[p], b[p]) by the angles (sn[p], c[p]) and writes the two halves of one row.
+__device__ __forceinline__ void rotate_store(const float (&a)[4], const float (&b)[4], const float (&sn)[4],
+                                             const float (&c)[4], uint2 *dst_a, uint2 *dst_b) {
+    float x[4], y[4];
+#pragma unroll
+    for (int p = 0; p < 4; ++p) {
+        x[p] = fmaf(a[p], c[p], -b[p] * sn[p]);
+        y[p] = fmaf(a[p], sn[p], b[p] * c[p]);
+    }
+    *dst_a = make_uint2(pack2(x[0], x[1]), pack2(x[2], x[3]));
+    *dst_b = make_uint2(pack2(y[0], y[1]), pack2(y[2], y[3]));
+}
+
+// Rows of [BH, L, 128] bf16 viewed as 32 uint2 each: lane `sub` of a row holds elements 4 sub .. 4 sub + 3
+// (uint2 index sub) and their partners 64 + 4 sub .. (uint2 index 16 + sub).
+__global__ void __launch_bounds__(256) rope_prep_kernel(const uint2 *__restrict__ q, const uint2 *__restrict__ k,
+                                                        uint2 *__restrict__ qr, uint2 *__restrict__ qs,
+                                                        uint2 *__restrict__ kr, int64_t rows, int64_t L, int w,
+                                                        const __grid_constant__ RopePrep rp) {
+    const int sub = threadIdx.x % kRopeLanes;
+    uint2 f[kRopePpl];
+#pragma unroll
+    for (int p = 0; p < kRopePpl; ++p) {
+        f[p] = rp.frac[sub * kRopePpl + p];
+        asm volatile("" : "+r"(f[p].x), "+r"(f[p].y));  // keep them in registers, not re-read per row
+    }
+    // the sink rotation of every row t >= w - 1: angle (w - 1) theta_i
+    float sw[kRopePpl], cw[kRopePpl];
+#pragma unroll
+    for (int p = 0; p < kRopePpl; ++p) turn_sincos(static_cast<uint32_t>(w - 1), f[p], sw[p], cw[p]);
+
+    const int rows_per_cta = blockDim.x / kRopeLanes;
+    const int64_t step = static_cast<int64_t>(gridDim.x) * rows_per_cta;
+    for (int64_t row = static_cast<int64_t>(blockIdx.x) * rows_per_cta + threadIdx.x / kRopeLanes; row < rows;
+         row += step) {
+        const int64_t t = row % L;
+        const int64_t ia = row * 32 + sub, ib = ia + 16;
+        float qa[4], qb[4], ka[4], kb[4];
+        unpack4(__ldg(q + ia), qa);
+        unpack4(__ldg(q + ib), qb);
+        unpack4(__ldg(k + ia), ka);
+        unpack4(__ldg(k + ib), kb);
+        float sn[kRopePpl], c[kRopePpl];
+#pragma unroll
+        for (int p = 0; p < kRopePpl; ++p) turn_sincos(static_cast<uint32_t>(t), f[p], sn[p], c[p]);
+        rotate_store(qa, qb, sn, c, qr + ia, qr + ib);
+        rotate_store(ka, kb, sn, c, kr + ia, kr + ib);
+        if (t < w - 1)
+            rotate_store(qa, qb, sn, c, qs + ia, qs + ib);
+        else
+            rotate_store(qa, qb, sw, cw, qs + ia, qs + ib);
+    }
+}
+
+size_t rope_prefill_workspace_bytes(int BH, int64_t L, int d) {
+    return 3 * static_cast<size_t>(BH) * static_cast<size_t>(L) * static_cast<size_t>(d) * 2;
+}
+
+int launch_rope_prep(const void *q, const void *k, void *qr, void *qs, void *kr, int BH, int64_t L, int d, int w,
+                     double base, cudaStream_t stream) {
+    if (d != kRopeD) return fail(SWA_ERR_UNSUPPORTED, "rope prefill needs d = %d", kRopeD);
+    RopePrep rp{};
+    // theta_i / (2 pi) = base^(-2i/d) / (2 pi) < 1/6 in double, rounded to a 64-bit fraction in two 32-bit
+    // steps (each exact in double; a carry out of the low step is absorbed by the 64-bit sum)
+    for (int i = 0; i < d / 2; ++i) {
+        const double fr = std::pow(base, -2.0 * i / d) / 6.283185307179586476925286766559;
+        const double hi = std::floor(std::ldexp(fr, 32));
+        const double lo = std::nearbyint(std::ldexp(std::ldexp(fr, 32) - hi, 32));
+        const uint64_t F = (static_cast<uint64_t>(hi) << 32) + static_cast<uint64_t>(lo);
+        rp.frac[i] = make_uint2(static_cast<uint32_t>(F), static_cast<uint32_t>(F >> 32));
+    }
+    const int64_t rows = static_cast<int64_t>(BH) * L;
+    const int64_t ctas_needed = (rows + 256 / kRopeLanes - 1) / (256 / kRopeLanes);
+    const int ctas = static_cast<int>(ctas_needed < 152 * 8 ? ctas_needed : 152 * 8);
+    rope_prep_kernel<<<ctas, 256, 0, stream>>>(static_cast<const uint2 *>(q), static_cast<const uint2 *>(k),
+                                               static_cast<uint2 *>(qr), static_cast<uint2 *>(qs),
+                                               static_cast<uint2 *>(kr), rows, L, w, rp);
+    cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) return fail(SWA_ERR_CUDA, "rope prefill pass launch: %s", cudaGetErrorString(e));
+    return SWA_OK;
+}
+
+}  // namespace swa

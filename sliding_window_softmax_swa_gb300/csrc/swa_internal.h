@@ -35,10 +35,19 @@ struct PrefillArgs {
     float scale;
     int64_t seq_stride;  // rows between consecutive (b, h) blocks (== L for contiguous tensors)
     cudaStream_t stream;
+    // RoPE at the positions inside the cache (bf16 tensor-core prefill, pos0 == 0): q and k are rotated
+    // rows, q_sink the query rows rotated for the sink keys; the sinks get their own key tile, scored
+    // with q_sink, and the band starts at position s
+    const void *q_sink = nullptr;
 };
 
 int launch_prefill_f32(const PrefillArgs &a);
 int launch_prefill_bf16_tc(const PrefillArgs &a);
+// The rotation pass of RoPE prefill: qr = R(t) q, kr = R(t) k, qs = R(min(t, w - 1)) q for the rows of
+// [BH, L, d] (d = 128, bf16); workspace = qr | qs | kr.
+size_t rope_prefill_workspace_bytes(int BH, int64_t L, int d);
+int launch_rope_prep(const void *q, const void *k, void *qr, void *qs, void *kr, int BH, int64_t L, int d, int w,
+                     double base, cudaStream_t stream);
 
 // Rolling-cache write of positions pos0..pos0+n-1; source rows of (b, h) start at bh*src_stride.
 int launch_kv_write(void *k_cache, void *v_cache, const void *k_new, const void *v_new, int BH, int d, int w,
@@ -67,7 +76,7 @@ int launch_decode_rope(const DecodeArgs &a, double base);
 size_t decode_noalloc_scratch_bytes();
 int launch_decode_noalloc(DecodeArgs a);
 
-int prefill_tile_plan(int q0, int q1, int pos0, int w, int s, int *out, int max_tiles);
+int prefill_tile_plan(int q0, int q1, int pos0, int w, int s, int rope, int *out, int max_tiles);
 int launch_selftest_wait_timeout(uint64_t timeout_ns, cudaStream_t stream);
 int launch_selftest_umma(const void *a, const void *b, float *c, int mode, cudaStream_t stream);
 

@@ -10,7 +10,7 @@ import torch
 
 import oracle
 import swa_inputs
-from gpu_common import LSE_ABS, compare, oracle_rows, require_gpu
+from gpu_common import LSE_ABS, check_rope_prefill, compare, oracle_rows, require_gpu, rope_workspace_operands
 
 pytestmark = pytest.mark.gpu
 
@@ -139,3 +139,29 @@ def test_full_size_streaming_decode_rope():
             o_ref, l_ref = oracle.decode_rope(qh[t][None], kh[None, :t + 1], vh[None, :t + 1], t, w, s, wl.scale)
             compare(f"rope decode bh={bh} t={t}", outs[i, j][None], o_ref, torch.bfloat16)
             assert abs(float(lses[i, j]) - l_ref[0]) < LSE_ABS
+
+
+def test_full_size_prefill_rope_sampled_rows():
+    # the primary shape with RoPE at the positions inside the cache: every head at rows around the tile,
+    # pair and window boundaries, the last rows and a few random ones, against the oracle's definition;
+    # checked as in tests/test_gpu_prefill_rope.py (rotated operands, attention on them, exact definition)
+    swa = require_gpu()
+    wl = swa_inputs.WORKLOADS["prefill_llama7b_L8192_w1024_s4"]
+    q, k, v = swa_inputs.workload_inputs(wl, "cuda")
+    lse = torch.empty((wl.B, wl.H, wl.L), dtype=torch.float32, device="cuda")
+    ws = torch.empty(swa.lib().swa_sink_prefill_rope_workspace_size(wl.B, wl.H, wl.L, wl.d), dtype=torch.uint8,
+                     device="cuda")
+    o = swa.swa_sink_prefill_rope(q, k, v, wl.w, wl.s, lse=lse, workspace=ws)
+    assert swa.swa_device_status() == swa.SWA_OK, swa.last_error()
+    rng = np.random.default_rng(5)
+    rows = sorted({0, 1, 3, 4, 127, 128, 255, 256, 1022, 1023, 1024, 1025, 1026, 1279, 1280, 2047, 2048, 4095,
+                   4096, 8190, 8191} | set(int(x) for x in rng.integers(0, wl.L, 12)))
+    qc, kc_, vc_ = q.cpu(), k.cpu(), v.cpu()
+    o_ref, l_ref = oracle.prefill_rope(qc, kc_, vc_, wl.w, wl.s, wl.scale, rows=rows)
+    nh, d = wl.B * wl.H, wl.d
+    qf, kf, vf = (x.double().numpy().reshape(nh, wl.L, d) for x in (qc, kc_, vc_))
+    check_rope_prefill("rope prefill llama7b sampled rows",
+                       o[:, :, rows].reshape(nh, len(rows), d).cpu().double().numpy(),
+                       lse[:, :, rows].reshape(nh, len(rows)).cpu().double().numpy(),
+                       rope_workspace_operands(ws, wl.B, wl.H, wl.L, d, rows), qf, kf, vf, rows, wl.w, wl.s,
+                       wl.scale, 10000.0, o_ref.reshape(nh, len(rows), d), l_ref.reshape(nh, len(rows)))

@@ -1,0 +1,76 @@
+"""GPU parity of the prefill with RoPE at the positions inside the cache (swa_sink_prefill_rope) against
+the oracle's definition (row t = the streaming decode at step t over unrotated keys), element by element.
+
+The kernel rounds the rotated q and k to bf16, the tensor-core operand type, which the plain prefill does
+not need (its q and k are bf16 already).  So each row is checked in three parts (gpu_common.check_rope_prefill):
+the rotated operands the kernel leaves in its workspace against the oracle's fp64 rotation (one bf16 ulp),
+the attention against fp64 attention on those operands (the bf16 tolerances of every path), and the result
+against the oracle's exact definition within the bound that operand rounding allows.
+"""
+import math
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import swa_inputs
+from gpu_common import check_rope_prefill, compare, require_gpu, rope_workspace_operands
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.mark.parametrize("B,H,L,w,s,base", [
+    (1, 2, 700, 256, 4, 1e4),     # several key tiles, rows far past the window, a ragged tail
+    (1, 2, 600, 128, 16, 1e4),
+    (2, 1, 300, 64, 0, 1e4),      # no sinks: plain RoPE over the band
+    (1, 1, 520, 520, 4, 1e4),     # w = L: nothing is evicted
+    (1, 1, 1000, 300, 100, 5e5),  # many sinks, another base
+    (1, 2, 257, 40, 4, 1e4),      # one row past a query pair
+    (1, 1, 3, 2, 1, 1e4),         # fewer rows than sinks + 1
+])
+def test_rope_prefill_every_row(B, H, L, w, s, base):
+    swa = require_gpu()
+    d = 128
+    q, k, v = swa_inputs.prefill_inputs(B, H, L, d, 900 + L + s, torch.bfloat16, "cpu", sink_boost=True)
+    lse = torch.empty((B, H, L), dtype=torch.float32, device="cuda")
+    ws = torch.empty(swa.lib().swa_sink_prefill_rope_workspace_size(B, H, L, d), dtype=torch.uint8, device="cuda")
+    o = swa.swa_sink_prefill_rope(q.cuda(), k.cuda(), v.cuda(), w, s, rope_base=base, lse=lse, workspace=ws)
+    assert swa.swa_device_status() == swa.SWA_OK, swa.last_error()
+    scale = 1.0 / math.sqrt(d)
+    o_ref, l_ref = oracle.prefill_rope(q, k, v, w, s, scale, base)
+    nh = B * H
+    rows = list(range(L))
+    qf, kf, vf = (x.double().numpy().reshape(nh, L, d) for x in (q, k, v))
+    check_rope_prefill(f"rope prefill {B, H, L, w, s}", o.cpu().double().numpy().reshape(nh, L, d),
+                       lse.cpu().double().numpy().reshape(nh, L), rope_workspace_operands(ws, B, H, L, d, rows),
+                       qf, kf, vf, rows, w, s, scale, base, o_ref.reshape(nh, L, d), l_ref.reshape(nh, L))
+
+
+def test_rope_prefill_row_equals_rope_decode_step():
+    # the same unrotated keys through the decode path: row t of the prefill is step t of the stream
+    swa = require_gpu()
+    B, H, L, d, w, s = 1, 2, 400, 128, 96, 4
+    q, k, v = (x.cuda() for x in swa_inputs.prefill_inputs(B, H, L, d, 77, torch.bfloat16, "cpu", True))
+    o = swa.swa_sink_prefill_rope(q, k, v, w, s)
+    kc = torch.zeros((B, H, w, d), dtype=torch.bfloat16, device="cuda")
+    vc = torch.zeros_like(kc)
+    for t in range(L):
+        swa.kv_rolling_write(kc, vc, k[:, :, t:t + 1].contiguous(), v[:, :, t:t + 1].contiguous(), w, s, t)
+        if t in (0, 50, 95, 96, 97, 200, 399):
+            od = swa.swa_sink_decode_step_rope(q[:, :, t].contiguous(), kc, vc, t, w, s)
+            # the prefill rounds its rotated operands to bf16, the decode rotates in fp32 registers: the
+            # two agree within twice the operand-rounding slack the parity test allows each of them
+            compare(f"prefill row {t} vs decode", o[:, :, t].float().cpu().numpy().astype(np.float64),
+                    od.float().cpu().numpy().astype(np.float64), torch.bfloat16, max_abs=4e-2, mean_abs=4e-3)
+    assert swa.swa_device_status() == swa.SWA_OK, swa.last_error()
+
+
+def test_rope_prefill_workspace_is_checked():
+    swa = require_gpu()
+    q = torch.zeros((1, 1, 300, 128), dtype=torch.bfloat16, device="cuda")
+    need = swa.lib().swa_sink_prefill_rope_workspace_size(1, 1, 300, 128)
+    assert need == 3 * 300 * 128 * 2
+    ws = torch.empty(need - 256, dtype=torch.uint8, device="cuda")
+    with pytest.raises(swa.SwaError):
+        swa.swa_sink_prefill_rope(q, q, q, 64, 4, workspace=ws)

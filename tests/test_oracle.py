@@ -373,3 +373,66 @@ def test_decode_rope_sinks_sit_at_fixed_distance_once_the_window_is_full():
                                oracle.rope(k[:, members], members.astype(np.float64)), v[:, members], members,
                                w, s, 0.3)
     assert np.abs(o_new - o_plain[:, 0]).max() > 1e-3
+
+
+def _rope_rows_closed_form(q, k, v, w, s, scale, base=10000.0):
+    # the reading of the cache-position rule for a whole sequence, written out directly: query t scores
+    # its window keys i at (q at t, k at i), as plain RoPE does, and the sinks at (q at min(t, w - 1),
+    # k at i), since a full cache puts the query at position w - 1 and sink i at i
+    nh, L, d = q.shape
+    m = w - s
+    pos = np.arange(L, dtype=np.float64)
+    kr = oracle.rope(k, pos, base)
+    o = np.empty((nh, L, d))
+    lse = np.empty((nh, L))
+    for t in range(L):
+        win = np.arange(max(s, t - m + 1), t + 1)
+        snk = np.arange(0, min(s, t + 1))
+        qw = oracle.rope(q[:, t:t + 1], [float(t)], base)[:, 0]
+        qs = oracle.rope(q[:, t:t + 1], [float(min(t, w - 1))], base)[:, 0]
+        x = np.concatenate([np.einsum("hd,hnd->hn", qs, kr[:, snk]), np.einsum("hd,hnd->hn", qw, kr[:, win])],
+                           axis=1) * scale
+        idx = np.concatenate([snk, win])
+        p = scipy.special.softmax(x, axis=1)
+        o[:, t] = np.einsum("hn,hnd->hd", p, v[:, idx])
+        lse[:, t] = scipy.special.logsumexp(x, axis=1)
+    return o, lse
+
+
+@pytest.mark.parametrize("L,w,s", [(40, 12, 4), (33, 8, 1), (25, 6, 5), (30, 30, 4), (21, 50, 3), (28, 9, 0)])
+def test_prefill_rope_equals_the_closed_form(L, w, s):
+    rng = np.random.default_rng(16 + L + w + s)
+    nh, d = 2, 16
+    q, k, v = (rng.standard_normal((1, nh, L, d)) for _ in range(3))
+    o, lse = oracle.prefill_rope(q, k, v, w, s, 0.3)
+    o_ref, l_ref = _rope_rows_closed_form(q[0], k[0], v[0], w, s, 0.3)
+    np.testing.assert_allclose(o[0], o_ref, atol=1e-10)
+    np.testing.assert_allclose(lse[0], l_ref, atol=1e-10)
+
+
+def test_prefill_rope_without_eviction_is_causal_rope_attention():
+    # w >= L: nothing leaves the cache and every position is its own: causal softmax attention on
+    # RoPE-rotated q and k (scipy), whatever s is
+    rng = np.random.default_rng(17)
+    nh, L, d, scale = 2, 24, 16, 0.25
+    q, k, v = (rng.standard_normal((1, nh, L, d)) for _ in range(3))
+    pos = np.arange(L, dtype=np.float64)
+    x = np.einsum("hid,hjd->hij", oracle.rope(q[0], pos), oracle.rope(k[0], pos)) * scale
+    x = np.where(np.tril(np.ones((L, L), dtype=bool)), x, -np.inf)
+    p = scipy.special.softmax(x, axis=2)
+    for s in (0, 3):
+        o, lse = oracle.prefill_rope(q, k, v, L + 5, s, scale)
+        np.testing.assert_allclose(o[0], np.einsum("hij,hjd->hid", p, v[0]), atol=1e-12)
+        np.testing.assert_allclose(lse[0], scipy.special.logsumexp(x, axis=2), atol=1e-12)
+
+
+def test_prefill_rope_without_sinks_is_the_band_oracle_on_rotated_inputs():
+    # s = 0: distances are the original ones, so the plain oracle (C) on RoPE-rotated q, k agrees
+    rng = np.random.default_rng(18)
+    nh, L, d, w = 2, 50, 16, 7
+    q, k, v = (rng.standard_normal((1, nh, L, d)) for _ in range(3))
+    pos = np.arange(L, dtype=np.float64)
+    o_ref, l_ref = oracle.prefill(oracle.rope(q, pos), oracle.rope(k, pos), v, w, 0, 0.2)
+    o, lse = oracle.prefill_rope(q, k, v, w, 0, 0.2, rows=range(0, L, 3))
+    np.testing.assert_allclose(o, o_ref[:, :, ::3], atol=1e-10)
+    np.testing.assert_allclose(lse, l_ref[:, :, ::3], atol=1e-10)

@@ -18,8 +18,8 @@ BN = 128   # keys per tile and rows per query tile
 BM = 256   # query rows per CTA (two query tiles)
 
 
-def check_plan(q0, q1, pos0, w, s, L):
-    plan = swa.prefill_tile_plan(q0, q1, pos0, w, s)
+def check_plan(q0, q1, pos0, w, s, L, plan=None):
+    plan = swa.prefill_tile_plan(q0, q1, pos0, w, s) if plan is None else plan
     holder = oracle.cache_replay(w, s, pos0) if pos0 > 0 else None
     cols, users = [], []
     for src, row0, pbase, chi, used in plan:
@@ -94,3 +94,20 @@ def test_tile_count_is_minimal_for_full_windows():
         for x in (0, 1):
             used = sum(1 for tl in plan if (tl[4] >> x) & 1)
             assert used == (m + 127 + BN - 1) // BN + (1 if s else 0)
+
+
+@pytest.mark.parametrize("w,s", [(1024, 4), (4096, 4), (4096, 0), (300, 4), (64, 16), (2, 1), (129, 4), (300, 128),
+                                 (256, 100), (17, 16), (1, 0)])
+def test_rope_tiles(w, s):
+    # RoPE prefill: the sinks [0, min(s, q1 + 1)) are the first tile, alone (their scores use another
+    # query rotation); every other tile starts at or after position s; coverage stays exact
+    L = 3000
+    for qt in range(0, (L + BM - 1) // BM):
+        q0 = qt * BM
+        q1 = min(q0 + BM, L) - 1
+        plan = check_plan(q0, q1, 0, w, s, L, swa.prefill_tile_plan_rope(q0, q1, w, s))
+        if s > 0:
+            src, row0, pbase, chi, used = plan[0]
+            assert (src, row0, pbase, chi) == (0, 0, 0, min(s, q1 + 1) - 1)
+        for src, row0, pbase, chi, used in plan[1 if s > 0 else 0:]:
+            assert pbase >= s
