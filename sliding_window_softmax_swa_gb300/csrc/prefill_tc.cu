@@ -99,13 +99,13 @@ static_assert(sizeof(Tile) == 12, "tile record");
 
 struct Params {
     CUtensorMap tm_q, tm_k, tm_v, tm_kc, tm_vc;
-    CUtensorMap tm_qs;  // RoPE mode: query rows rotated for the sink keys
+    CUtensorMap tm_qs;  // RoPE mode: query rows rotated for the sink keys (the sink tile, first in every
+                        // list, is scored with them; the band with tm_q)
     void *o;
     float *lse;
     DeviceStatus *status;
     int64_t seq_stride;  // rows between (b, h) blocks of q/k/v/o/lse
     int L, pos0, w, s, m, BH;
-    int rope;  // RoPE mode: the sink tile (first in every list) is scored with tm_qs, the band with tm_q
     int n_qpairs, n_items;  // 256-row query pairs per (b, h); work items = n_qpairs * BH
     float scale_log2;
     uint32_t timeout_us;
@@ -243,6 +243,8 @@ __device__ __forceinline__ void issue_pv(uint32_t d_tmem, uint32_t p_tmem, uint3
     }
 }
 
+// ROPE: the RoPE mode (compiled apart, so that the plain kernel's MMA loop carries none of its checks)
+template <bool ROPE>
 __global__ void __launch_bounds__(kThreads, 1) swa_prefill_tc_kernel(const __grid_constant__ Params P) {
     extern __shared__ uint8_t smem_raw[];
     uint8_t *sm = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -396,7 +398,7 @@ __global__ void __launch_bounds__(kThreads, 1) swa_prefill_tc_kernel(const __gri
                 const int b = it & 1;
                 if (it >= 2 && !mbar_wait(&lfree[b], ((it - 2) >> 1) & 1, wc, 12, it)) break;
                 Tile *tl = tiles_s + b * MAX_TILES;
-                const int n = build_tiles(tl, q0, qlast, P.pos0, P.s, P.m, P.w, P.rope != 0);
+                const int n = build_tiles(tl, q0, qlast, P.pos0, P.s, P.m, P.w, ROPE);
                 if (n < 1 || n > MAX_TILES) {
                     atomicOr(&P.status->word, kDevBadArg);
                     *abort_flag = 1;
@@ -408,8 +410,8 @@ __global__ void __launch_bounds__(kThreads, 1) swa_prefill_tc_kernel(const __gri
                 // Q loads of the item: one (tm_q), or in RoPE mode with sinks the sink-rotated rows for
                 // the first tile and then, once its QK products are done, the band-rotated rows.  Every
                 // load waits until the QK products of the previous one are done.
-                const CUtensorMap *mq0 = (P.rope && P.s > 0) ? &P.tm_qs : &P.tm_q;
-                const bool two = P.rope && P.s > 0 && n >= 2;
+                const CUtensorMap *mq0 = (ROPE && P.s > 0) ? &P.tm_qs : &P.tm_q;
+                const bool two = ROPE && P.s > 0 && n >= 2;
                 bool ok = true;
                 for (int ph = 0; ph < (two ? 2 : 1) && ok; ++ph) {
                     const CUtensorMap *mq = ph == 0 ? mq0 : &P.tm_q;
@@ -462,7 +464,7 @@ __global__ void __launch_bounds__(kThreads, 1) swa_prefill_tc_kernel(const __gri
                 const Tile *tl = tiles_s + b * MAX_TILES;
                 const int n = ntiles_s[b];
                 // RoPE mode with sinks: tile 0 (the sinks) uses the first Q load, the band a second one
-                const bool two = P.rope && P.s > 0 && n >= 2;
+                const bool two = ROPE && P.s > 0 && n >= 2;
                 bool q_band = !two;
                 int last_used[2] = {-1, -1};
                 for (int j = 0; j < n; ++j)
@@ -478,7 +480,7 @@ __global__ void __launch_bounds__(kThreads, 1) swa_prefill_tc_kernel(const __gri
                             umma_commit(&sfull[x]);
                         }
                     }
-                    if (n == 1 || two) umma_commit(qempty);  // the first Q load is no longer read
+                    if (n == 1 || (ROPE && two)) umma_commit(qempty);  // the first Q load is no longer read
                     umma_commit(&kempty[gk % NK]);
                     ++gk;
                     issued_any = true;
@@ -511,7 +513,7 @@ __global__ void __launch_bounds__(kThreads, 1) swa_prefill_tc_kernel(const __gri
                                 if (!mbar_wait(&kfull[sk], (gk / NK) & 1, wc, 3, j + 1)) { fine = false; break; }
                                 k_ready = true;
                             }
-                            if (!q_band) {  // the band-rotated Q rows
+                            if (ROPE && !q_band) {  // the band-rotated Q rows
                                 if (!mbar_wait(qfull, nqf & 1, wc, 2, j + 1)) { fine = false; break; }
                                 ++nqf;
                                 q_band = true;
@@ -865,7 +867,6 @@ int launch_prefill_bf16_tc(const PrefillArgs &a) {
         okm = okm && encode_rows_map(&p.tm_kc, a.k, L, a.BH, st) && encode_rows_map(&p.tm_vc, a.v, L, a.BH, st);
     okm = okm && encode_rows_map(&p.tm_qs, rope ? a.q_sink : a.q, L, a.BH, st);
     if (!okm) return fail(SWA_ERR_INVALID, "cuTensorMapEncodeTiled rejected a tensor (alignment or size)");
-    p.rope = rope ? 1 : 0;
     p.o = a.o;
     p.lse = a.lse;
     p.status = reinterpret_cast<DeviceStatus *>(status);
@@ -880,14 +881,15 @@ int launch_prefill_bf16_tc(const PrefillArgs &a) {
     p.n_items = p.n_qpairs * a.BH;
     p.scale_log2 = a.scale * 1.4426950408889634f;
     p.timeout_us = kWaitTimeoutUs;
-    cudaError_t e = cudaFuncSetAttribute(swa_prefill_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+    auto *kern = rope ? swa_prefill_tc_kernel<true> : swa_prefill_tc_kernel<false>;
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          static_cast<int>(SMEM_BYTES));
     if (e != cudaSuccess) return fail(SWA_ERR_CUDA, "prefill smem attribute: %s", cudaGetErrorString(e));
     // persistent: one CTA per SM, each walking work items blockIdx.x, blockIdx.x + gridDim.x, ...
     const int sms = sm_count();
     if (sms <= 0) return fail(SWA_ERR_CUDA, "cannot read the multiprocessor count");
     const dim3 grid(p.n_items < sms ? p.n_items : sms), block(kThreads);
-    swa_prefill_tc_kernel<<<grid, block, SMEM_BYTES, a.stream>>>(p);
+    kern<<<grid, block, SMEM_BYTES, a.stream>>>(p);
     e = cudaGetLastError();
     if (e != cudaSuccess) return fail(SWA_ERR_CUDA, "prefill launch: %s", cudaGetErrorString(e));
     return SWA_OK;
