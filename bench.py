@@ -248,7 +248,9 @@ def prefill_leg(swa, wl, steps, warmup, world, rank, clocks, e2e=False, rope=Fal
     return res
 
 
-def chunked_leg(swa, wl, steps, warmup, world, rank, clocks):
+def chunked_leg(swa, wl, steps, warmup, world, rank, clocks, rope=False):
+    """Chunked prefill steps; with ``rope`` the chunked prefill with RoPE at the positions inside the cache
+    (one rotation pass over the sequence, then per chunk the prefill and two rolling writes)."""
     import torch
     import swa_inputs
     B, H, L, d, w, s, C = wl.B, wl.H, wl.L, wl.d, wl.w, wl.s, wl.chunk
@@ -258,11 +260,19 @@ def chunked_leg(swa, wl, steps, warmup, world, rank, clocks):
     vc = torch.empty_like(kc)
     lib = swa.lib()
     stream = torch.cuda.current_stream().cuda_stream
-    args = (q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(), None, kc.data_ptr(), vc.data_ptr(), B, H, L, d,
-            w, s, wl.scale, C, 0, stream)
+    if rope:
+        nws = lib.swa_sink_prefill_chunked_rope_workspace_size(B, H, L, d, w)
+        ws = torch.empty(nws, dtype=torch.uint8, device="cuda")
+        args = (q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(), None, kc.data_ptr(), vc.data_ptr(), B, H, L,
+                d, w, s, wl.scale, C, 10000.0, ws.data_ptr(), nws, 0, stream)
+        call = lib.swa_sink_prefill_chunked_rope
+    else:
+        args = (q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(), None, kc.data_ptr(), vc.data_ptr(), B, H, L,
+                d, w, s, wl.scale, C, 0, stream)
+        call = lib.swa_sink_prefill_chunked
 
     def step():
-        rc = lib.swa_sink_prefill_chunked(*args)
+        rc = call(*args)
         if rc:
             raise RuntimeError(swa.last_error())
 
@@ -273,8 +283,9 @@ def chunked_leg(swa, wl, steps, warmup, world, rank, clocks):
     groups = 2 if B * H >= 16 else 1  # the library walks >= 16 (b, h) rows as two row groups
     del q, k, v, o, kc, vc
     torch.cuda.empty_cache()
+    per_chunk = 3 if rope else 2
     return {"flops_per_step": flops, "seconds": t, "steps": steps, "tflops": flops * steps / t / 1e12,
-            "ms_per_step": t / steps * 1e3, "launches": steps * 2 * nch * groups}
+            "ms_per_step": t / steps * 1e3, "launches": steps * (per_chunk * nch * groups + (1 if rope else 0))}
 
 
 def decode_leg(swa, wl, world, rank, clocks, steps=None, rope=False):
@@ -429,7 +440,7 @@ def main():
     ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--primary-only", action="store_true", help="only the primary prefill leg")
-    ap.add_argument("--legs", default="primary,mistral,chunked,decode,decode_rope,prefill_rope",
+    ap.add_argument("--legs", default="primary,mistral,chunked,decode,decode_rope,prefill_rope,chunked_rope",
                     help="comma list of legs to run (profiling runs pick one)")
     ap.add_argument("--decode-steps", type=int, default=None, help="shorter decode stream (profiling only)")
     args = ap.parse_args()
@@ -482,6 +493,15 @@ def main():
         secondary[cw.name] = {"metric": METRIC, "value": aggregate_rate(r["tflops"], world, 1.0), "unit": "TFLOP/s",
                               "ms_per_step": r["ms_per_step"], "frac_of_bf16_peak": r["tflops"] / peaks["bf16_tflops"],
                               "launches_per_step": r["launches"] // 3}
+    if "chunked_rope" in legs:
+        cw = swa_inputs.WORKLOADS["chunked_mistral_L131072_w4096_s4_C4096"]
+        r = chunked_leg(swa, cw, 3, 1, world, rank, clocks, rope=True)
+        secondary["chunked_rope_mistral_L131072_w4096_s4_C4096"] = {
+            "metric": METRIC, "value": aggregate_rate(r["tflops"], world, 1.0), "unit": "TFLOP/s",
+            "ms_per_step": r["ms_per_step"], "frac_of_bf16_peak": r["tflops"] / peaks["bf16_tflops"],
+            "what": "RoPE at the positions inside the cache (base 10000): one rotation pass, then per chunk the "
+                    "prefill and the rolling writes of rotated and unrotated keys",
+            "launches_per_step": r["launches"] // 3}
     if "decode" in legs:
         dw = swa_inputs.WORKLOADS["decode_llama13b_B64_w1024_s4_20480"]
         r = decode_leg(swa, dw, world, rank, clocks, steps=args.decode_steps)

@@ -113,6 +113,28 @@ int swa_sink_prefill_rope(const void *q, const void *k, const void *v, void *o, 
 size_t swa_sink_prefill_rope_workspace_size(int B, int H, int64_t L, int d);
 
 /*
+ * swa_sink_prefill_chunked_rope -- swa_sink_prefill_chunked with RoPE at the positions inside the cache
+ * (as swa_sink_prefill_rope): chunk c attends the cache state left by the earlier chunks plus its own keys,
+ * then its keys/values are written into the cache.  The result equals swa_sink_prefill_rope of the whole
+ * sequence, and k_cache / v_cache end up holding the unrotated keys and the values, as
+ * swa_sink_prefill_chunked leaves them (ready for swa_sink_decode_step_rope).
+ *
+ *   q, k, v, o, lse, k_cache, v_cache, chunk : as swa_sink_prefill_chunked; q and k unrotated; bf16,
+ *             d = 128; chunk >= max(1, s).
+ *   rope_base : finite and > 1.
+ *   workspace : caller-owned device scratch of swa_sink_prefill_chunked_rope_workspace_size(B, H, L, d, w)
+ *             bytes, 256-byte aligned: the rotated q, the sink-rotated q and the rotated k of the whole
+ *             sequence (one rotation pass serves every chunk: rotations depend on absolute positions only)
+ *             and a [B, H, w, d] cache of rotated keys.
+ *   s <= 128 (SWA_ERR_UNSUPPORTED otherwise).  Other arguments and errors as swa_sink_prefill_chunked.
+ */
+int swa_sink_prefill_chunked_rope(const void *q, const void *k, const void *v, void *o, float *lse, void *k_cache,
+                                  void *v_cache, int B, int H, int64_t L, int d, int w, int s, float scale,
+                                  int64_t chunk, double rope_base, void *workspace, size_t workspace_bytes, int dtype,
+                                  void *stream);
+size_t swa_sink_prefill_chunked_rope_workspace_size(int B, int H, int64_t L, int d, int w);
+
+/*
  * swa_sink_prefill_chunked -- the chunk-based prefill of "滑窗与固定稀疏" (rolling-buffer section):
  * the L positions are processed in chunks of `chunk` rows; chunk c attends the rolling cache as it was
  * before the chunk plus its own keys (swa_sink_prefill with pos0 = c*chunk), then its keys/values are
@@ -252,9 +274,9 @@ int swa_selftest_umma(const void *a, const void *b, float *c, int mode, void *st
  * swa_status.
  */
 int swa_prefill_tile_plan(int64_t q0, int64_t q1, int64_t pos0, int w, int s, int *tiles, int max_tiles);
-/* The same for swa_sink_prefill_rope (pos0 = 0): the sinks form the first tile on their own, the band
- * starts at position s.  s <= 128. */
-int swa_prefill_tile_plan_rope(int64_t q0, int64_t q1, int w, int s, int *tiles, int max_tiles);
+/* The same for the RoPE prefills (pos0 = 0, or pos0 >= s in chunked prefill): the sinks form the first
+ * tile on their own, the band starts at position s.  s <= 128. */
+int swa_prefill_tile_plan_rope(int64_t q0, int64_t q1, int64_t pos0, int w, int s, int *tiles, int max_tiles);
 
 #ifdef __cplusplus
 }

@@ -40,7 +40,10 @@ SIGNATURES = {
     "swa_selftest_wait_timeout": (_i, [_i64, _vp]),
     "swa_selftest_umma": (_i, [_vp, _vp, _vp, _i, _vp]),
     "swa_prefill_tile_plan": (_i, [_i64, _i64, _i64, _i, _i, ctypes.POINTER(ctypes.c_int), _i]),
-    "swa_prefill_tile_plan_rope": (_i, [_i64, _i64, _i, _i, ctypes.POINTER(ctypes.c_int), _i]),
+    "swa_prefill_tile_plan_rope": (_i, [_i64, _i64, _i64, _i, _i, ctypes.POINTER(ctypes.c_int), _i]),
+    "swa_sink_prefill_chunked_rope": (_i, [_vp, _vp, _vp, _vp, _vp, _vp, _vp, _i, _i, _i64, _i, _i, _i, _f, _i64,
+                                           ctypes.c_double, _vp, _sz, _i, _vp]),
+    "swa_sink_prefill_chunked_rope_workspace_size": (_sz, [_i, _i, _i64, _i, _i]),
     "swa_sink_prefill_rope": (_i, [_vp, _vp, _vp, _vp, _vp, _i, _i, _i64, _i, _i, _i, _f, ctypes.c_double, _vp,
                                    _sz, _i, _vp]),
     "swa_sink_prefill_rope_workspace_size": (_sz, [_i, _i, _i64, _i]),
@@ -148,6 +151,26 @@ def swa_sink_prefill_rope(q, k, v, w: int, s: int, rope_base: float = 10000.0, s
     return o
 
 
+def swa_sink_prefill_chunked_rope(q, k, v, w: int, s: int, chunk: int, k_cache, v_cache, rope_base: float = 10000.0,
+                                  scale: float | None = None, o=None, lse=None, workspace=None, stream=None):
+    """Chunked prefill with RoPE at the positions inside the cache (unrotated q, k; the caches end up
+    holding unrotated keys and the values)."""
+    B, H, L, d = q.shape
+    w_ = k_cache.shape[2]
+    if o is None:
+        o = torch.empty_like(q)
+    nws = lib().swa_sink_prefill_chunked_rope_workspace_size(B, H, L, d, w_)
+    if workspace is None:
+        workspace = torch.empty(max(nws, 256), dtype=torch.uint8, device=q.device)
+    _dev(q, k, v, o, lse, k_cache, v_cache, workspace)
+    scale = (1.0 / d ** 0.5) if scale is None else scale
+    _check("swa_sink_prefill_chunked_rope", lib().swa_sink_prefill_chunked_rope(
+        _ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), _ptr(k_cache), _ptr(v_cache), B, H, L, d, w, s, scale, chunk,
+        float(rope_base), _ptr(workspace), workspace.numel() * workspace.element_size(), _dtype_code(q),
+        _stream(stream)))
+    return o
+
+
 def swa_sink_prefill_chunked(q, k, v, w: int, s: int, chunk: int, k_cache, v_cache, scale: float | None = None,
                              o=None, lse=None, stream=None):
     """Chunked prefill through the rolling cache (k_cache/v_cache [B, H, w, d] are overwritten)."""
@@ -246,10 +269,10 @@ def prefill_tile_plan(q0: int, q1: int, pos0: int, w: int, s: int):
     return [tuple(buf[5 * i:5 * i + 5]) for i in range(min(n, 256))]
 
 
-def prefill_tile_plan_rope(q0: int, q1: int, w: int, s: int):
-    """The key tiles of the RoPE prefill (pos0 = 0) for query rows q0..q1, as prefill_tile_plan."""
+def prefill_tile_plan_rope(q0: int, q1: int, pos0: int, w: int, s: int):
+    """The key tiles of the RoPE prefills for query rows q0..q1 of a call at pos0, as prefill_tile_plan."""
     buf = (ctypes.c_int * (5 * 256))()
-    n = lib().swa_prefill_tile_plan_rope(q0, q1, w, s, buf, 256)
+    n = lib().swa_prefill_tile_plan_rope(q0, q1, pos0, w, s, buf, 256)
     if n < 0:
         raise SwaError("swa_prefill_tile_plan_rope", n, last_error())
     return [tuple(buf[5 * i:5 * i + 5]) for i in range(min(n, 256))]

@@ -200,20 +200,20 @@ static ChunkStreams *chunk_streams() {
     return per_dev[dev];
 }
 
-extern "C" int swa_sink_prefill_chunked(const void *q, const void *k, const void *v, void *o, float *lse,
-                                        void *k_cache, void *v_cache, int B, int H, int64_t L, int d, int w, int s,
-                                        float scale, int64_t chunk, int dtype, void *stream) {
-    t_err[0] = 0;
-    int rc = check_prefill(q, k, v, o, lse, 0, B, H, L, d, w, s, scale, dtype);
-    if (rc) return rc;
-    if (chunk < 1) return fail(SWA_ERR_INVALID, "chunk=%lld must be >= 1", (long long)chunk);
-    if (L == 0) return SWA_OK;
-    if (!k_cache || !v_cache) return fail(SWA_ERR_INVALID, "k_cache and v_cache must be non-null");
-    if (!aligned16(k_cache) || !aligned16(v_cache))
-        return fail(SWA_ERR_INVALID, "k_cache and v_cache must be 16-byte aligned");
+// RoPE mode of the chunk loop: q and k passed to it are the rotated rows; these are the rest.
+struct ChunkRope {
+    const void *q_sink;  // [BH, L, d] query rows rotated for the sink keys
+    const void *k_raw;   // [BH, L, d] unrotated keys: they go into the caller's cache
+    void *kc_rot;        // [BH, w, d] scratch cache of rotated keys, read by the prefill for positions < pos0
+};
+
+// The chunk loop of chunked prefill (validated arguments, L > 0).
+static int chunk_loop(const void *q, const void *k, const void *v, void *o, float *lse, void *k_cache, void *v_cache,
+                      int B, int H, int64_t L, int d, int w, int s, float scale, int64_t chunk, int dtype,
+                      cudaStream_t st, const ChunkRope *rp) {
     const int es = esize_of(dtype);
     const size_t row_bytes = static_cast<size_t>(d) * es;
-    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    int rc = SWA_OK;
     // The (b, h) rows are independent; only the chunks of one row depend on each other, through its
     // cache.  The rows are split into groups, each walking all chunks on its own stream, so that one
     // group's next chunk fills the SMs that another group's chunk leaves idle at its end (a chunk of one
@@ -234,6 +234,7 @@ extern "C" int swa_sink_prefill_chunked(const void *q, const void *k, const void
         const size_t cache_off = static_cast<size_t>(r0) * static_cast<size_t>(w) * row_bytes;
         void *kcg = static_cast<char *>(k_cache) + cache_off;
         void *vcg = static_cast<char *>(v_cache) + cache_off;
+        void *krg = rp ? static_cast<char *>(rp->kc_rot) + cache_off : nullptr;
         for (int64_t c0 = 0; c0 < L; c0 += chunk) {
             const int64_t n = (L - c0 < chunk) ? (L - c0) : chunk;
             const size_t off = seq_off + static_cast<size_t>(c0) * row_bytes;
@@ -242,11 +243,25 @@ extern "C" int swa_sink_prefill_chunked(const void *q, const void *k, const void
             const char *vc = static_cast<const char *>(v) + off;
             char *oc = static_cast<char *>(o) + off;
             float *lc = lse ? lse + static_cast<int64_t>(r0) * L + c0 : nullptr;
-            // prefill_impl treats its B as the number of (b, h) rows when H = 1
-            rc = prefill_impl(qc, kc, vc, oc, lc, kcg, vcg, c0, r1 - r0, 1, n, d, w, s, scale, dtype, L, gs);
-            if (rc) return rc;
-            rc = launch_kv_write(kcg, vcg, kc, vc, r1 - r0, d, w, s, c0, n, L, es, gs);
-            if (rc) return rc;
+            if (!rp) {
+                // prefill_impl treats its B as the number of (b, h) rows when H = 1
+                rc = prefill_impl(qc, kc, vc, oc, lc, kcg, vcg, c0, r1 - r0, 1, n, d, w, s, scale, dtype, L, gs);
+                if (rc) return rc;
+                rc = launch_kv_write(kcg, vcg, kc, vc, r1 - r0, d, w, s, c0, n, L, es, gs);
+                if (rc) return rc;
+            } else {
+                // rotated rows against the rotated cache; then the chunk's rotated keys into the scratch
+                // cache and its unrotated keys into the caller's (the values go to the caller's cache twice)
+                PrefillArgs a{qc, kc, vc, oc, lc, krg, vcg, c0, r1 - r0, n, d, w, s, scale, L, gs};
+                a.q_sink = static_cast<const char *>(rp->q_sink) + off;
+                rc = launch_prefill_bf16_tc(a);
+                if (rc) return rc;
+                rc = launch_kv_write(krg, vcg, kc, vc, r1 - r0, d, w, s, c0, n, L, es, gs);
+                if (rc) return rc;
+                rc = launch_kv_write(kcg, vcg, static_cast<const char *>(rp->k_raw) + off, vc, r1 - r0, d, w, s, c0,
+                                     n, L, es, gs);
+                if (rc) return rc;
+            }
         }
     }
     if (groups > 1) {
@@ -257,6 +272,59 @@ extern "C" int swa_sink_prefill_chunked(const void *q, const void *k, const void
         }
     }
     return SWA_OK;
+}
+
+extern "C" int swa_sink_prefill_chunked(const void *q, const void *k, const void *v, void *o, float *lse,
+                                        void *k_cache, void *v_cache, int B, int H, int64_t L, int d, int w, int s,
+                                        float scale, int64_t chunk, int dtype, void *stream) {
+    t_err[0] = 0;
+    int rc = check_prefill(q, k, v, o, lse, 0, B, H, L, d, w, s, scale, dtype);
+    if (rc) return rc;
+    if (chunk < 1) return fail(SWA_ERR_INVALID, "chunk=%lld must be >= 1", (long long)chunk);
+    if (L == 0) return SWA_OK;
+    if (!k_cache || !v_cache) return fail(SWA_ERR_INVALID, "k_cache and v_cache must be non-null");
+    if (!aligned16(k_cache) || !aligned16(v_cache))
+        return fail(SWA_ERR_INVALID, "k_cache and v_cache must be 16-byte aligned");
+    return chunk_loop(q, k, v, o, lse, k_cache, v_cache, B, H, L, d, w, s, scale, chunk, dtype,
+                      static_cast<cudaStream_t>(stream), nullptr);
+}
+
+extern "C" size_t swa_sink_prefill_chunked_rope_workspace_size(int B, int H, int64_t L, int d, int w) {
+    if (B < 1 || H < 1 || L < 0 || d != 128 || w < 1) return 0;
+    return rope_prefill_workspace_bytes(B * H, L, d) + static_cast<size_t>(B) * H * w * d * 2;
+}
+
+extern "C" int swa_sink_prefill_chunked_rope(const void *q, const void *k, const void *v, void *o, float *lse,
+                                             void *k_cache, void *v_cache, int B, int H, int64_t L, int d, int w,
+                                             int s, float scale, int64_t chunk, double rope_base, void *workspace,
+                                             size_t workspace_bytes, int dtype, void *stream) {
+    t_err[0] = 0;
+    int rc = check_prefill(q, k, v, o, lse, 0, B, H, L, d, w, s, scale, dtype);
+    if (rc) return rc;
+    if (dtype != SWA_BF16 || d != 128) return fail(SWA_ERR_UNSUPPORTED, "RoPE prefill runs on bf16 with d = 128");
+    if (s > 128) return fail(SWA_ERR_UNSUPPORTED, "RoPE prefill needs s <= 128 (s=%d)", s);
+    if (chunk < 1 || chunk < s)
+        return fail(SWA_ERR_INVALID, "chunk=%lld must be >= max(1, s) with RoPE", (long long)chunk);
+    if (!(rope_base == rope_base) || rope_base <= 1.0 || rope_base > 1e30)
+        return fail(SWA_ERR_INVALID, "rope_base must be a finite number > 1");
+    const size_t need = swa_sink_prefill_chunked_rope_workspace_size(B, H, L, d, w);
+    if (workspace_bytes < need)
+        return fail(SWA_ERR_INVALID, "workspace of %zu bytes is smaller than the %zu needed", workspace_bytes, need);
+    if (L == 0) return SWA_OK;
+    if (!k_cache || !v_cache) return fail(SWA_ERR_INVALID, "k_cache and v_cache must be non-null");
+    if (!aligned16(k_cache) || !aligned16(v_cache))
+        return fail(SWA_ERR_INVALID, "k_cache and v_cache must be 16-byte aligned");
+    if (!workspace || (reinterpret_cast<uintptr_t>(workspace) & 255u))
+        return fail(SWA_ERR_INVALID, "workspace must be non-null and 256-byte aligned");
+    const cudaStream_t st = static_cast<cudaStream_t>(stream);
+    char *ws = static_cast<char *>(workspace);
+    const size_t one = rope_prefill_workspace_bytes(B * H, L, d) / 3;  // one [B, H, L, d] bf16 tensor
+    void *qr = ws, *qs = ws + one, *kr = ws + 2 * one, *kc_rot = ws + 3 * one;
+    // the rotations depend on absolute positions only, so one pass serves every chunk
+    rc = launch_rope_prep(q, k, qr, qs, kr, B * H, L, d, w, rope_base, st);
+    if (rc) return rc;
+    const ChunkRope rp{qs, k, kc_rot};
+    return chunk_loop(qr, kr, v, o, lse, k_cache, v_cache, B, H, L, d, w, s, scale, chunk, dtype, st, &rp);
 }
 
 // Streams and events of the host-buffer prefill pipeline (copies in, compute, copies out), created once
@@ -450,13 +518,17 @@ extern "C" int swa_prefill_tile_plan(int64_t q0, int64_t q1, int64_t pos0, int w
                              max_tiles);
 }
 
-extern "C" int swa_prefill_tile_plan_rope(int64_t q0, int64_t q1, int w, int s, int *tiles, int max_tiles) {
+extern "C" int swa_prefill_tile_plan_rope(int64_t q0, int64_t q1, int64_t pos0, int w, int s, int *tiles,
+                                          int max_tiles) {
     t_err[0] = 0;
     if (w < 1 || s < 0 || s >= w) return fail(SWA_ERR_INVALID, "need 0 <= s < w (s=%d, w=%d)", s, w);
     if (s > 128) return fail(SWA_ERR_UNSUPPORTED, "RoPE prefill needs s <= 128");
-    if (q0 < 0 || q1 < q0 || q1 >= (int64_t(1) << 31)) return fail(SWA_ERR_INVALID, "need 0 <= q0 <= q1 < 2^31");
+    if (pos0 > 0 && pos0 < s) return fail(SWA_ERR_UNSUPPORTED, "RoPE prefill needs pos0 = 0 or pos0 >= s");
+    if (pos0 < 0 || q0 < pos0 || q1 < q0 || q1 >= (int64_t(1) << 31))
+        return fail(SWA_ERR_INVALID, "need 0 <= pos0 <= q0 <= q1 < 2^31");
     if (!tiles || max_tiles < 0) return fail(SWA_ERR_INVALID, "tiles must be non-null");
-    return prefill_tile_plan(static_cast<int>(q0), static_cast<int>(q1), 0, w, s, 1, tiles, max_tiles);
+    return prefill_tile_plan(static_cast<int>(q0), static_cast<int>(q1), static_cast<int>(pos0), w, s, 1, tiles,
+                             max_tiles);
 }
 
 extern "C" size_t swa_sink_prefill_rope_workspace_size(int B, int H, int64_t L, int d) {

@@ -113,8 +113,9 @@ struct Params {
 
 // Build the key-tile list of the query tile [q0, q1] (absolute positions).  Returns the tile count
 // (entries past MAX_TILES are not stored; the caller treats a larger count as an error).  In RoPE mode
-// (pos0 == 0, s <= BN) the sinks [0, min(s, q1 + 1)) always form the first tile, on their own, and the band
-// starts at position s: the sink scores use another query rotation than the band's.
+// (pos0 = 0 or pos0 >= s, s <= BN) the sinks [0, min(s, q1 + 1)) always form the first tile, on their own
+// (from the cache when pos0 >= s), and the band starts at position s: the sink scores use another query
+// rotation than the band's.
 __host__ __device__ int build_tiles(Tile *tl, int q0, int q1, int pos0, int s, int m, int w, bool rope) {
     int n = 0;
     auto add_range = [&](int src, int pa, int pb, int rowbase) {  // positions [pa, pb]; row = p - rowbase
@@ -842,8 +843,8 @@ int launch_prefill_bf16_tc(const PrefillArgs &a) {
     using namespace tc;
     if (a.d != HD) return fail(SWA_ERR_UNSUPPORTED, "tensor-core prefill needs d = %d", HD);
     const bool rope = a.q_sink != nullptr;
-    if (rope && (a.pos0 != 0 || a.s > BN))
-        return fail(SWA_ERR_UNSUPPORTED, "RoPE prefill needs pos0 = 0 and s <= %d", BN);
+    if (rope && ((a.pos0 > 0 && a.pos0 < a.s) || a.s > BN))
+        return fail(SWA_ERR_UNSUPPORTED, "RoPE prefill needs pos0 = 0 or pos0 >= s, and s <= %d", BN);
     if (max_tiles_bound(a.w, a.s) + (rope ? 1 : 0) > MAX_TILES)
         return fail(SWA_ERR_UNSUPPORTED, "window w=%d needs more than %d key tiles per query tile", a.w, MAX_TILES);
     if ((a.L + BM - 1) / BM * a.BH > 0x7FFFFFFF) return fail(SWA_ERR_UNSUPPORTED, "too many work items");

@@ -1,5 +1,5 @@
-"""Parity at the full workload sizes, in the launch configuration the benchmark times: the primary
-prefill in full; for the two B=2 L=32768 prefills every row of four heads and every row with t < w + 128
+"""Parity at the full workload sizes, in the launch configuration the benchmark times (the RoPE forms on
+sampled rows): the primary prefill in full; for the two B=2 L=32768 prefills every row of four heads and every row with t < w + 128
 in every head; for the chunked prefill every row of chunks 0, 1, 2 and 31 and the rows around every chunk
 boundary in every head; for decode every step of 8 (b, h) rows."""
 import math
@@ -165,3 +165,33 @@ def test_full_size_prefill_rope_sampled_rows():
                        lse[:, :, rows].reshape(nh, len(rows)).cpu().double().numpy(),
                        rope_workspace_operands(ws, wl.B, wl.H, wl.L, d, rows), qf, kf, vf, rows, wl.w, wl.s,
                        wl.scale, 10000.0, o_ref.reshape(nh, len(rows), d), l_ref.reshape(nh, len(rows)))
+
+
+def test_full_size_chunked_prefill_rope_sampled_rows():
+    # the chunked workload (L = 131072 in 4096-token chunks, w = 4096, s = 4) with RoPE at the positions
+    # inside the cache, in the launch configuration the benchmark times: every head at rows of the first
+    # three chunks around the chunk boundaries (the ring has wrapped by the third) and random rows there
+    swa = require_gpu()
+    wl = swa_inputs.WORKLOADS["chunked_mistral_L131072_w4096_s4_C4096"]
+    q, k, v = swa_inputs.workload_inputs(wl, "cuda")
+    kc = torch.zeros((wl.B, wl.H, wl.w, wl.d), dtype=torch.bfloat16, device="cuda")
+    vc = torch.zeros_like(kc)
+    lse = torch.empty((wl.B, wl.H, wl.L), dtype=torch.float32, device="cuda")
+    ws = torch.empty(swa.lib().swa_sink_prefill_chunked_rope_workspace_size(wl.B, wl.H, wl.L, wl.d, wl.w),
+                     dtype=torch.uint8, device="cuda")
+    o = swa.swa_sink_prefill_chunked_rope(q, k, v, wl.w, wl.s, wl.chunk, kc, vc, lse=lse, workspace=ws)
+    assert swa.swa_device_status() == swa.SWA_OK, swa.last_error()
+    rng = np.random.default_rng(6)
+    C = wl.chunk
+    rows = sorted({0, 3, 4, C - 1, C, C + 1, 2 * C - 1, 2 * C, 2 * C + 1, 3 * C - 1}
+                  | set(int(x) for x in rng.integers(0, 3 * C, 6)))
+    top = max(rows) + 1
+    qc, kc_, vc_ = (x[:, :, :top].cpu() for x in (q, k, v))
+    o_ref, l_ref = oracle.prefill_rope(qc, kc_, vc_, wl.w, wl.s, wl.scale, rows=rows)
+    nh, d = wl.B * wl.H, wl.d
+    qf, kf, vf = (x.double().numpy().reshape(nh, top, d) for x in (qc, kc_, vc_))
+    ops = rope_workspace_operands(ws, wl.B, wl.H, wl.L, d, rows)
+    check_rope_prefill("rope chunked L131072 sampled rows",
+                       o[:, :, rows].reshape(nh, len(rows), d).cpu().double().numpy(),
+                       lse[:, :, rows].reshape(nh, len(rows)).cpu().double().numpy(), ops, qf, kf, vf, rows, wl.w,
+                       wl.s, wl.scale, 10000.0, o_ref.reshape(nh, len(rows), d), l_ref.reshape(nh, len(rows)))

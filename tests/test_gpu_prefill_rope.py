@@ -74,3 +74,47 @@ def test_rope_prefill_workspace_is_checked():
     ws = torch.empty(need - 256, dtype=torch.uint8, device="cuda")
     with pytest.raises(swa.SwaError):
         swa.swa_sink_prefill_rope(q, q, q, 64, 4, workspace=ws)
+
+
+@pytest.mark.parametrize("B,H,L,w,s,C", [
+    (1, 2, 700, 256, 4, 128),
+    (1, 2, 600, 128, 16, 200),
+    (2, 1, 300, 64, 0, 50),      # no sinks
+    (1, 1, 1000, 300, 100, 256),  # many sinks, chunk >= s
+    (1, 2, 3000, 512, 4, 256),   # 12 chunks: the ring wraps several times
+    (16, 2, 300, 100, 4, 64),    # 32 (b, h) rows: two row groups on two streams
+])
+def test_rope_chunked_prefill_every_row(B, H, L, w, s, C):
+    # chunked prefill with RoPE equals the whole-sequence definition (the oracle's prefill_rope), and
+    # leaves the caller's caches as a plain rolling write of all positions does (unrotated keys)
+    swa = require_gpu()
+    d = 128
+    q, k, v = swa_inputs.prefill_inputs(B, H, L, d, 1300 + L + s, torch.bfloat16, "cpu", sink_boost=True)
+    kc = torch.full((B, H, w, d), float("nan"), dtype=torch.bfloat16, device="cuda")
+    vc = torch.full_like(kc, float("nan"))
+    lse = torch.empty((B, H, L), dtype=torch.float32, device="cuda")
+    ws = torch.empty(swa.lib().swa_sink_prefill_chunked_rope_workspace_size(B, H, L, d, w), dtype=torch.uint8,
+                     device="cuda")
+    o = swa.swa_sink_prefill_chunked_rope(q.cuda(), k.cuda(), v.cuda(), w, s, C, kc, vc, lse=lse, workspace=ws)
+    assert swa.swa_device_status() == swa.SWA_OK, swa.last_error()
+    scale = 1.0 / math.sqrt(d)
+    o_ref, l_ref = oracle.prefill_rope(q, k, v, w, s, scale)
+    nh = B * H
+    rows = list(range(L))
+    qf, kf, vf = (x.double().numpy().reshape(nh, L, d) for x in (q, k, v))
+    check_rope_prefill(f"rope chunked {B, H, L, w, s, C}", o.cpu().double().numpy().reshape(nh, L, d),
+                       lse.cpu().double().numpy().reshape(nh, L), rope_workspace_operands(ws, B, H, L, d, rows),
+                       qf, kf, vf, rows, w, s, scale, 10000.0, o_ref.reshape(nh, L, d), l_ref.reshape(nh, L))
+    kc2 = torch.full_like(kc, float("nan"))
+    vc2 = torch.full_like(vc, float("nan"))
+    swa.kv_rolling_write(kc2, vc2, k.cuda(), v.cuda(), w, s, 0)
+    assert torch.equal(kc.view(torch.int16), kc2.view(torch.int16))
+    assert torch.equal(vc.view(torch.int16), vc2.view(torch.int16))
+
+
+def test_rope_chunked_prefill_rejects_chunks_shorter_than_the_sinks():
+    swa = require_gpu()
+    q = torch.zeros((1, 1, 64, 128), dtype=torch.bfloat16, device="cuda")
+    kc = torch.zeros((1, 1, 32, 128), dtype=torch.bfloat16, device="cuda")
+    with pytest.raises(swa.SwaError):
+        swa.swa_sink_prefill_chunked_rope(q, q, q, 32, 8, 4, kc, kc.clone())

@@ -105,9 +105,27 @@ def test_rope_tiles(w, s):
     for qt in range(0, (L + BM - 1) // BM):
         q0 = qt * BM
         q1 = min(q0 + BM, L) - 1
-        plan = check_plan(q0, q1, 0, w, s, L, swa.prefill_tile_plan_rope(q0, q1, w, s))
+        plan = check_plan(q0, q1, 0, w, s, L, swa.prefill_tile_plan_rope(q0, q1, 0, w, s))
         if s > 0:
             src, row0, pbase, chi, used = plan[0]
             assert (src, row0, pbase, chi) == (0, 0, 0, min(s, q1 + 1) - 1)
+        for src, row0, pbase, chi, used in plan[1 if s > 0 else 0:]:
+            assert pbase >= s
+
+
+def test_rope_chunked_tiles_random():
+    # chunked RoPE prefill (pos0 >= s): the sinks come from the cache as the first tile, alone
+    rng = random.Random(4321)
+    for _ in range(300):
+        w = rng.choice([8, 40, 100, 128, 129, 300, 513, 1024])
+        s = rng.choice([0, 1, 4, min(w - 1, 16), min(w - 1, 128)])
+        pos0 = max(s, 1, rng.choice([1, s, s + 1, w - 1, w, w + 1, 3 * w + 7, rng.randrange(1, 5 * w + 10)]))
+        L = rng.randrange(1, 700)
+        qt = rng.randrange(0, (L + BM - 1) // BM)
+        q0 = pos0 + qt * BM
+        q1 = pos0 + min(qt * BM + BM, L) - 1
+        plan = check_plan(q0, q1, pos0, w, s, L, swa.prefill_tile_plan_rope(q0, q1, pos0, w, s))
+        if s > 0:
+            assert plan[0][0] == 1 and plan[0][2] == 0 and plan[0][3] == s - 1, plan[0]
         for src, row0, pbase, chi, used in plan[1 if s > 0 else 0:]:
             assert pbase >= s
