@@ -18,6 +18,8 @@ attention) and eq attn-fixed-softmax-sink of "滑窗与固定稀疏" (row normal
 
 ``rope``, ``decode_rope`` and ``prefill_rope`` state the streaming decode and the prefill with
 positions re-assigned inside the cache and rotary embedding (StreamingLLM section of "滑窗与固定稀疏").
+``is_key_dilated`` and ``prefill_dilated`` state the dilated window with sinks (the dilated sliding
+window of "滑窗与固定稀疏", glossary and Longformer section: attended positions skip r - 1 tokens).
 
 Parity status: every function here is pinned by ``tests/test_oracle.py`` against closed forms,
 textbook special cases and hand-derived golden values (``tests/golden/``).
@@ -220,6 +222,40 @@ def prefill_rope(q, k, v, w: int, s: int, scale: float, base: float = 10000.0, r
     qf, kf, vf = q.reshape(B * H, L, d), k.reshape(B * H, L, d), v.reshape(B * H, L, d)
     for j, t in enumerate(rows):
         o[:, j], lse[:, j] = decode_rope(qf[:, t], kf[:, :t + 1], vf[:, :t + 1], t, w, s, scale, base, nthreads)
+    return o.reshape(B, H, len(rows), d), lse.reshape(B, H, len(rows))
+
+
+def is_key_dilated(t: int, i: int, w: int, s: int, r: int) -> bool:
+    """Brute-force membership of key position i in the dilated key set of query t: the s sinks, and the
+    m = w - s window keys t, t - r, ..., t - (m-1) r, each skipping r - 1 positions (the dilated window of
+    the fixed-sparsity page, in its causal form with sinks)."""
+    m = w - s
+    if i < 0 or i > t:
+        return False
+    return i < s or ((t - i) % r == 0 and (t - i) // r < m)
+
+
+def prefill_dilated(q, k, v, w: int, s: int, r: int, scale: float, rows=None):
+    """Whole-sequence prefill over the dilated key sets (fp64, numpy): row t attends
+    {i < s} | {t - j r : 0 <= j < m}, restricted to i <= t, softmax of scale * q.k.
+
+    q, k, v: [B, H, L, d]; ``rows``: query positions to compute (default all).
+    Returns (o [B, H, len(rows), d], lse [B, H, len(rows)]).
+    """
+    q, k, v = _f64(q), _f64(k), _f64(v)
+    B, H, L, d = q.shape
+    rows = list(range(L)) if rows is None else [int(t) for t in rows]
+    qf, kf, vf = q.reshape(B * H, L, d), k.reshape(B * H, L, d), v.reshape(B * H, L, d)
+    o = np.empty((B * H, len(rows), d))
+    lse = np.empty((B * H, len(rows)))
+    for j, t in enumerate(rows):
+        members = np.array([i for i in range(t + 1) if is_key_dilated(t, i, w, s, r)], dtype=np.int64)
+        x = np.einsum("hd,hnd->hn", qf[:, t], kf[:, members]) * scale
+        mx = x.max(axis=1, keepdims=True)
+        e = np.exp(x - mx)
+        den = e.sum(axis=1)
+        o[:, j] = np.einsum("hn,hnd->hd", e, vf[:, members]) / den[:, None]
+        lse[:, j] = mx[:, 0] + np.log(den)
     return o.reshape(B, H, len(rows), d), lse.reshape(B, H, len(rows))
 
 

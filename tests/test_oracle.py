@@ -436,3 +436,70 @@ def test_prefill_rope_without_sinks_is_the_band_oracle_on_rotated_inputs():
     o, lse = oracle.prefill_rope(q, k, v, w, 0, 0.2, rows=range(0, L, 3))
     np.testing.assert_allclose(o, o_ref[:, :, ::3], atol=1e-10)
     np.testing.assert_allclose(lse, l_ref[:, :, ::3], atol=1e-10)
+
+
+# ------------------------------------------------------------------ dilated window with sinks
+def test_dilated_mask_matches_hand_derived_golden():
+    path = os.path.join(GOLDEN, "dilated_mask_L14_w5_s2_r3.txt")
+    rows = [l.strip() for l in open(path) if l.strip() and not l.startswith("#")]
+    assert len(rows) == 14
+    for t in range(14):
+        for i in range(14):
+            assert (rows[t][i] == "1") == oracle.is_key_dilated(t, i, 5, 2, 3), (t, i)
+
+
+@pytest.mark.parametrize("w,s", [(5, 2), (8, 0), (3, 2), (40, 4)])
+def test_dilation_one_is_the_plain_key_set(w, s):
+    for t in range(60):
+        for i in range(60):
+            assert oracle.is_key_dilated(t, i, w, s, 1) == oracle.is_key(t, i, w, s)
+
+
+def test_dilated_key_count_closed_form():
+    # |K(t)| = min(s, t + 1) + min(m, t // r + 1) - (sinks that are also window keys: i < s, i <= t,
+    # t - i divisible by r and (t - i) / r < m), counted without the membership function
+    for w, s, r in [(5, 2, 3), (9, 4, 2), (7, 0, 5), (12, 3, 1)]:
+        m = w - s
+        for t in range(80):
+            both = sum(1 for i in range(min(s, t + 1)) if (t - i) % r == 0 and (t - i) // r < m)
+            want = min(s, t + 1) + min(m, t // r + 1) - both
+            got = sum(oracle.is_key_dilated(t, i, w, s, r) for i in range(t + 1))
+            assert got == want, (w, s, r, t)
+
+
+def test_prefill_dilated_with_dilation_one_equals_the_plain_oracle():
+    # independent code paths: numpy per row (dilated) against the C oracle (plain)
+    rng = np.random.default_rng(19)
+    q, k, v = (rng.standard_normal((1, 2, 45, 16)) for _ in range(3))
+    o, lse = oracle.prefill_dilated(q, k, v, 9, 3, 1, 0.3)
+    o_ref, l_ref = oracle.prefill(q, k, v, 9, 3, 0.3)
+    np.testing.assert_allclose(o, o_ref, atol=1e-12)
+    np.testing.assert_allclose(lse, l_ref, atol=1e-12)
+
+
+def test_prefill_dilated_zero_query_is_the_mean_over_the_key_set():
+    # q = 0: uniform weights, so o = mean of v over K(t) and lse = ln |K(t)| (members from the golden's rule)
+    rng = np.random.default_rng(20)
+    L, w, s, r = 30, 6, 2, 4
+    q = np.zeros((1, 1, L, 8))
+    k, v = rng.standard_normal((1, 1, L, 8)), rng.standard_normal((1, 1, L, 8))
+    o, lse = oracle.prefill_dilated(q, k, v, w, s, r, 1.0)
+    m = w - s
+    for t in range(L):
+        members = sorted(set(range(min(s, t + 1))) | {t - j * r for j in range(m) if t - j * r >= 0})
+        np.testing.assert_allclose(o[0, 0, t], v[0, 0, members].mean(axis=0), atol=1e-12)
+        assert abs(lse[0, 0, t] - math.log(len(members))) < 1e-12
+
+
+def test_prefill_dilated_without_sinks_is_plain_attention_on_each_residue_class():
+    # s = 0: row t only meets positions of its own residue class mod r, as a window of m on that
+    # subsequence -- the plain oracle on the subsequence gives the same rows
+    rng = np.random.default_rng(21)
+    L, d, w, r = 41, 8, 5, 3
+    q, k, v = (rng.standard_normal((1, 1, L, d)) for _ in range(3))
+    o, lse = oracle.prefill_dilated(q, k, v, w, 0, r, 0.5)
+    for c in range(r):
+        idx = np.arange(c, L, r)
+        o_c, l_c = oracle.prefill(q[:, :, idx], k[:, :, idx], v[:, :, idx], w, 0, 0.5)
+        np.testing.assert_allclose(o[:, :, idx], o_c, atol=1e-12)
+        np.testing.assert_allclose(lse[:, :, idx], l_c, atol=1e-12)
