@@ -193,7 +193,18 @@ def time_loop(step, steps, warmup, world, clocks):
     return reduce_max(e0.elapsed_time(e1) / 1e3, world)
 
 
-def prefill_leg(swa, wl, steps, warmup, world, rank, clocks, e2e=False, rope=False):
+def dilated_flops(B, H, L, d, w, s, r):
+    """4 d per (query, key) pair of the dilated key sets: sinks i < min(s, t + 1) plus min(m, t // r + 1)
+    window keys, less the sinks that are also window keys."""
+    m = w - s
+    pairs = 0
+    for t in range(L):
+        both = sum(1 for i in range(min(s, t + 1)) if (t - i) % r == 0 and (t - i) // r < m)
+        pairs += min(s, t + 1) + min(m, t // r + 1) - both
+    return 4.0 * B * H * d * pairs
+
+
+def prefill_leg(swa, wl, steps, warmup, world, rank, clocks, e2e=False, rope=False, dilation=0):
     """Prefill steps; with ``rope`` the RoPE prefill at the positions inside the cache (base 10000): a
     rotation pass over q and k, then the tensor-core prefill on the rotated rows (2 launches a step)."""
     import torch
@@ -204,7 +215,13 @@ def prefill_leg(swa, wl, steps, warmup, world, rank, clocks, e2e=False, rope=Fal
     lib = swa.lib()
     stream = torch.cuda.current_stream().cuda_stream
     dt = 0 if wl.dtype == "bf16" else 1
-    if rope:
+    if dilation:
+        nws = lib.swa_sink_prefill_dilated_workspace_size(B, H, L, d, s, dilation, dt)
+        ws = torch.empty(nws, dtype=torch.uint8, device="cuda")
+        args = (q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(), None, B, H, L, d, w, s, dilation, wl.scale,
+                ws.data_ptr(), nws, dt, stream)
+        call = lib.swa_sink_prefill_dilated
+    elif rope:
         nws = lib.swa_sink_prefill_rope_workspace_size(B, H, L, d)
         ws = torch.empty(nws, dtype=torch.uint8, device="cuda")
         args = (q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(), None, B, H, L, d, w, s, wl.scale, 10000.0,
@@ -222,9 +239,9 @@ def prefill_leg(swa, wl, steps, warmup, world, rank, clocks, e2e=False, rope=Fal
 
     t = time_loop(step, steps, warmup, world, clocks)
     _check_status(swa)
-    flops = banded_flops(B, H, L, d, w)
+    flops = dilated_flops(B, H, L, d, w, s, dilation) if dilation else banded_flops(B, H, L, d, w)
     res = {"flops_per_step": flops, "seconds": t, "steps": steps, "tflops": flops * steps / t / 1e12,
-           "ms_per_step": t / steps * 1e3, "launches": (2 if rope else 1) * steps}
+           "ms_per_step": t / steps * 1e3, "launches": (3 if dilation else 2 if rope else 1) * steps}
     if e2e:
         # the same prefill through the public host-buffer call: every step copies q/k/v from pinned host
         # memory and o back (the library pipelines the copies against the compute over row groups)
@@ -440,7 +457,7 @@ def main():
     ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--primary-only", action="store_true", help="only the primary prefill leg")
-    ap.add_argument("--legs", default="primary,mistral,chunked,decode,decode_rope,prefill_rope,chunked_rope",
+    ap.add_argument("--legs", default="primary,mistral,chunked,decode,decode_rope,prefill_rope,chunked_rope,dilated",
                     help="comma list of legs to run (profiling runs pick one)")
     ap.add_argument("--decode-steps", type=int, default=None, help="shorter decode stream (profiling only)")
     args = ap.parse_args()
@@ -493,6 +510,13 @@ def main():
         secondary[cw.name] = {"metric": METRIC, "value": aggregate_rate(r["tflops"], world, 1.0), "unit": "TFLOP/s",
                               "ms_per_step": r["ms_per_step"], "frac_of_bf16_peak": r["tflops"] / peaks["bf16_tflops"],
                               "launches_per_step": r["launches"] // 3}
+    if "dilated" in legs:
+        r = prefill_leg(swa, wl, max(3, args.steps // 2), 3, world, rank, clocks, dilation=2)
+        secondary["prefill_dilated_llama7b_L8192_w1024_s4_r2"] = {
+            "metric": METRIC, "value": aggregate_rate(r["tflops"], world, 1.0), "unit": "TFLOP/s",
+            "ms_per_step": r["ms_per_step"], "frac_of_bf16_peak": r["tflops"] / peaks["bf16_tflops"],
+            "what": "dilated window with sinks, r = 2 (FLOPs over the dilated key sets): gather into virtual "
+                    "heads + tensor-core prefill + scatter", "launches_per_step": 3}
     if "chunked_rope" in legs:
         cw = swa_inputs.WORKLOADS["chunked_mistral_L131072_w4096_s4_C4096"]
         r = chunked_leg(swa, cw, 3, 1, world, rank, clocks, rope=True)

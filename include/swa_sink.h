@@ -135,6 +135,26 @@ int swa_sink_prefill_chunked_rope(const void *q, const void *k, const void *v, v
 size_t swa_sink_prefill_chunked_rope_workspace_size(int B, int H, int64_t L, int d, int w);
 
 /*
+ * swa_sink_prefill_dilated -- whole-sequence prefill over a dilated window with sinks: the dilated sliding
+ * window of "滑窗与固定稀疏" (glossary and Longformer section: attended window positions skip r - 1 tokens),
+ * causal and with the sinks of the StreamingLLM section.  Row t attends
+ *     {i < s}  |  {t - j r : 0 <= j < m},  m = w - s,  restricted to i <= t  (each key once),
+ * so the window reaches (m - 1) r + 1 positions back at the cost of m keys; r = 1 is swa_sink_prefill.
+ * Runs as a gather into r virtual heads per (b, h) (the sinks, then one residue class of positions mod r),
+ * the prefill of swa_sink_prefill on them, and a scatter back.
+ *
+ *   q, k, v, o, lse : as swa_sink_prefill (pos0 = 0), bf16 with d = 128 (tensor cores) or fp32.
+ *   r       : dilation, 1 <= r <= 65536, B * H * r <= 65535 * 32.
+ *   workspace : caller-owned device scratch of swa_sink_prefill_dilated_workspace_size(B, H, L, d, s, r,
+ *             dtype) bytes, 256-byte aligned (q, k, v, o of the virtual heads and their lse).
+ *   Other arguments and errors as swa_sink_prefill.
+ */
+int swa_sink_prefill_dilated(const void *q, const void *k, const void *v, void *o, float *lse, int B, int H,
+                             int64_t L, int d, int w, int s, int r, float scale, void *workspace,
+                             size_t workspace_bytes, int dtype, void *stream);
+size_t swa_sink_prefill_dilated_workspace_size(int B, int H, int64_t L, int d, int s, int r, int dtype);
+
+/*
  * swa_sink_prefill_chunked -- the chunk-based prefill of "滑窗与固定稀疏" (rolling-buffer section):
  * the L positions are processed in chunks of `chunk` rows; chunk c attends the rolling cache as it was
  * before the chunk plus its own keys (swa_sink_prefill with pos0 = c*chunk), then its keys/values are

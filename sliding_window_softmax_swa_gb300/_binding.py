@@ -41,6 +41,8 @@ SIGNATURES = {
     "swa_selftest_umma": (_i, [_vp, _vp, _vp, _i, _vp]),
     "swa_prefill_tile_plan": (_i, [_i64, _i64, _i64, _i, _i, ctypes.POINTER(ctypes.c_int), _i]),
     "swa_prefill_tile_plan_rope": (_i, [_i64, _i64, _i64, _i, _i, ctypes.POINTER(ctypes.c_int), _i]),
+    "swa_sink_prefill_dilated": (_i, [_vp, _vp, _vp, _vp, _vp, _i, _i, _i64, _i, _i, _i, _i, _f, _vp, _sz, _i, _vp]),
+    "swa_sink_prefill_dilated_workspace_size": (_sz, [_i, _i, _i64, _i, _i, _i, _i]),
     "swa_sink_prefill_chunked_rope": (_i, [_vp, _vp, _vp, _vp, _vp, _vp, _vp, _i, _i, _i64, _i, _i, _i, _f, _i64,
                                            ctypes.c_double, _vp, _sz, _i, _vp]),
     "swa_sink_prefill_chunked_rope_workspace_size": (_sz, [_i, _i, _i64, _i, _i]),
@@ -130,6 +132,24 @@ def swa_sink_prefill(q, k, v, w: int, s: int, scale: float | None = None, o=None
     _check("swa_sink_prefill", lib().swa_sink_prefill(
         _ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), _ptr(k_cache), _ptr(v_cache), pos0, B, H, L, d, w, s,
         scale, _dtype_code(q), _stream(stream)))
+    return o
+
+
+def swa_sink_prefill_dilated(q, k, v, w: int, s: int, r: int, scale: float | None = None, o=None, lse=None,
+                             workspace=None, stream=None):
+    """Prefill over the dilated window with sinks: row t attends the s sinks and t, t - r, ..., t - (m-1) r."""
+    B, H, L, d = q.shape
+    assert k.shape == q.shape and v.shape == q.shape and k.dtype == q.dtype and v.dtype == q.dtype
+    if o is None:
+        o = torch.empty_like(q)
+    nws = lib().swa_sink_prefill_dilated_workspace_size(B, H, L, d, s, r, _dtype_code(q))
+    if workspace is None:
+        workspace = torch.empty(max(nws, 256), dtype=torch.uint8, device=q.device)
+    _dev(q, k, v, o, lse, workspace)
+    scale = (1.0 / d ** 0.5) if scale is None else scale
+    _check("swa_sink_prefill_dilated", lib().swa_sink_prefill_dilated(
+        _ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), B, H, L, d, w, s, r, scale, _ptr(workspace),
+        workspace.numel() * workspace.element_size(), _dtype_code(q), _stream(stream)))
     return o
 
 

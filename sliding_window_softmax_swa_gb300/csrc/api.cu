@@ -531,6 +531,46 @@ extern "C" int swa_prefill_tile_plan_rope(int64_t q0, int64_t q1, int64_t pos0, 
                              max_tiles);
 }
 
+static size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
+
+extern "C" size_t swa_sink_prefill_dilated_workspace_size(int B, int H, int64_t L, int d, int s, int r, int dtype) {
+    const int es = esize_of(dtype);
+    if (B < 1 || H < 1 || L < 0 || s < 0 || r < 1 || es == 0 || !(d == 16 || d == 32 || d == 64 || d == 128)) return 0;
+    const size_t rows = static_cast<size_t>(B) * H * r * static_cast<size_t>(dilated_rows(L, s, r));
+    return 4 * align256(rows * d * es) + align256(rows * sizeof(float));
+}
+
+extern "C" int swa_sink_prefill_dilated(const void *q, const void *k, const void *v, void *o, float *lse, int B, int H,
+                                        int64_t L, int d, int w, int s, int r, float scale, void *workspace,
+                                        size_t workspace_bytes, int dtype, void *stream) {
+    t_err[0] = 0;
+    int rc = check_prefill(q, k, v, o, lse, 0, B, H, L, d, w, s, scale, dtype);
+    if (rc) return rc;
+    if (r < 1 || r > 65536) return fail(SWA_ERR_INVALID, "dilation r=%d must be in [1, 65536]", r);
+    if (static_cast<int64_t>(B) * H * r > 65535 * 32)
+        return fail(SWA_ERR_UNSUPPORTED, "B*H*r=%lld exceeds the supported %d", (long long)B * H * r, 65535 * 32);
+    const size_t need = swa_sink_prefill_dilated_workspace_size(B, H, L, d, s, r, dtype);
+    if (workspace_bytes < need)
+        return fail(SWA_ERR_INVALID, "workspace of %zu bytes is smaller than the %zu needed", workspace_bytes, need);
+    if (L == 0) return SWA_OK;
+    if (!workspace || (reinterpret_cast<uintptr_t>(workspace) & 255u))
+        return fail(SWA_ERR_INVALID, "workspace must be non-null and 256-byte aligned");
+    const cudaStream_t st = static_cast<cudaStream_t>(stream);
+    const int es = esize_of(dtype);
+    const int VH = B * H * r;
+    const int64_t Lv = dilated_rows(L, s, r);
+    const size_t one = align256(static_cast<size_t>(VH) * Lv * d * es);
+    char *ws = static_cast<char *>(workspace);
+    void *qv = ws, *kv = ws + one, *vv = ws + 2 * one, *ov = ws + 3 * one;
+    float *lsev = reinterpret_cast<float *>(ws + 4 * one);
+    rc = launch_dilate_gather(q, k, v, qv, kv, vv, B * H, L, d, es, s, r, st);
+    if (rc) return rc;
+    // the virtual heads as (b, h) rows of a plain prefill: s sinks, window w
+    rc = prefill_impl(qv, kv, vv, ov, lsev, nullptr, nullptr, 0, VH, 1, Lv, d, w, s, scale, dtype, Lv, st);
+    if (rc) return rc;
+    return launch_dilate_scatter(ov, lsev, o, lse, B * H, L, d, es, s, r, st);
+}
+
 extern "C" size_t swa_sink_prefill_rope_workspace_size(int B, int H, int64_t L, int d) {
     if (B < 1 || H < 1 || L < 0 || d != 128) return 0;
     return rope_prefill_workspace_bytes(B * H, L, d);

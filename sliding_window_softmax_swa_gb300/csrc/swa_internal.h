@@ -45,6 +45,13 @@ int launch_prefill_f32(const PrefillArgs &a);
 int launch_prefill_bf16_tc(const PrefillArgs &a);
 // The rotation pass of RoPE prefill: qr = R(t) q, kr = R(t) k, qs = R(min(t, w - 1)) q for the rows of
 // [BH, L, d] (d = 128, bf16); workspace = qr | qs | kr.
+// Layout passes of the dilated-window prefill: rows of one virtual head (sinks + one residue class), the
+// gather of q, k, v into the virtual heads [BH * r, Lv, d] and the scatter of o (and lse) back.
+int64_t dilated_rows(int64_t L, int s, int r);
+int launch_dilate_gather(const void *q, const void *k, const void *v, void *qv, void *kv, void *vv, int BH, int64_t L,
+                         int d, int esize, int s, int r, cudaStream_t stream);
+int launch_dilate_scatter(const void *ov, const float *lsev, void *o, float *lse, int BH, int64_t L, int d, int esize,
+                          int s, int r, cudaStream_t stream);
 size_t rope_prefill_workspace_bytes(int BH, int64_t L, int d);
 int launch_rope_prep(const void *q, const void *k, void *qr, void *qs, void *kr, int BH, int64_t L, int d, int w,
                      double base, cudaStream_t stream);

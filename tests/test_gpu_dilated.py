@@ -1,0 +1,48 @@
+"""GPU parity of the prefill over a dilated window with sinks (swa_sink_prefill_dilated) against the oracle's
+definition, element by element: bf16 outputs within the tolerances of every bf16 path (the virtual heads go
+through the same tensor-core prefill, one rounding of o), fp32 within 1e-4, lse within 1e-3."""
+import math
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import swa_inputs
+from gpu_common import LSE_ABS, compare, require_gpu
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.mark.parametrize("B,H,L,d,w,s,r,dtype", [
+    (1, 2, 700, 128, 256, 4, 2, torch.bfloat16),   # several tiles per virtual head, ragged classes
+    (1, 2, 600, 128, 128, 16, 3, torch.bfloat16),
+    (2, 1, 300, 128, 64, 0, 4, torch.bfloat16),    # no sinks: independent residue classes
+    (1, 1, 1001, 128, 200, 4, 7, torch.bfloat16),  # L not a multiple of r
+    (16, 2, 300, 128, 100, 4, 2, torch.bfloat16),  # 64 virtual heads
+    (1, 1, 200, 128, 40, 32, 5, torch.bfloat16),   # many sinks
+    (1, 1, 3, 128, 2, 1, 3, torch.bfloat16),       # fewer rows than r
+    (1, 2, 130, 16, 16, 4, 3, torch.float32),      # the fp32 path
+])
+def test_dilated_prefill_every_row(B, H, L, d, w, s, r, dtype):
+    swa = require_gpu()
+    q, k, v = swa_inputs.prefill_inputs(B, H, L, d, 3000 + L + r, dtype, "cpu", sink_boost=True)
+    lse = torch.empty((B, H, L), dtype=torch.float32, device="cuda")
+    o = swa.swa_sink_prefill_dilated(q.cuda(), k.cuda(), v.cuda(), w, s, r, lse=lse)
+    assert swa.swa_device_status() == swa.SWA_OK, swa.last_error()
+    o_ref, l_ref = oracle.prefill_dilated(q, k, v, w, s, r, 1.0 / math.sqrt(d))
+    compare(f"dilated {B, H, L, d, w, s, r}", o.cpu(), o_ref, dtype)
+    assert np.abs(lse.cpu().double().numpy() - l_ref).max() < LSE_ABS
+
+
+def test_dilation_one_is_the_plain_prefill_bit_for_bit():
+    # r = 1: the single virtual head is the sequence itself, so the same kernel sees the same bytes
+    swa = require_gpu()
+    q, k, v = (x.cuda() for x in swa_inputs.prefill_inputs(1, 4, 900, 128, 31, torch.bfloat16, "cpu", True))
+    la = torch.empty((1, 4, 900), dtype=torch.float32, device="cuda")
+    lb = torch.empty_like(la)
+    a = swa.swa_sink_prefill_dilated(q, k, v, 300, 4, 1, lse=la)
+    b = swa.swa_sink_prefill(q, k, v, 300, 4, lse=lb)
+    assert swa.swa_device_status() == swa.SWA_OK, swa.last_error()
+    assert torch.equal(a.view(torch.int16), b.view(torch.int16))
+    assert torch.equal(la, lb)

@@ -195,3 +195,23 @@ def test_full_size_chunked_prefill_rope_sampled_rows():
                        o[:, :, rows].reshape(nh, len(rows), d).cpu().double().numpy(),
                        lse[:, :, rows].reshape(nh, len(rows)).cpu().double().numpy(), ops, qf, kf, vf, rows, wl.w,
                        wl.s, wl.scale, 10000.0, o_ref.reshape(nh, len(rows), d), l_ref.reshape(nh, len(rows)))
+
+
+def test_full_size_prefill_dilated_sampled_rows():
+    # the primary shape with dilation 2 (window reaching 2 * 1019 + 1 positions back), in the launch
+    # configuration the benchmark times: every head at rows around the window, tile and class boundaries
+    swa = require_gpu()
+    wl = swa_inputs.WORKLOADS["prefill_llama7b_L8192_w1024_s4"]
+    r = 2
+    q, k, v = swa_inputs.workload_inputs(wl, "cuda")
+    lse = torch.empty((wl.B, wl.H, wl.L), dtype=torch.float32, device="cuda")
+    o = swa.swa_sink_prefill_dilated(q, k, v, wl.w, wl.s, r, lse=lse)
+    assert swa.swa_device_status() == swa.SWA_OK, swa.last_error()
+    rng = np.random.default_rng(7)
+    rows = sorted({0, 1, 3, 4, 5, 255, 256, 1023, 2041, 2042, 2043, 2044, 2045, 4096, 4097, 8190, 8191}
+                  | set(int(x) for x in rng.integers(0, wl.L, 10)))
+    o_ref, l_ref = oracle.prefill_dilated(q.cpu(), k.cpu(), v.cpu(), wl.w, wl.s, r, wl.scale, rows=rows)
+    nh, d = wl.B * wl.H, wl.d
+    compare("dilated llama7b sampled rows", o[:, :, rows].reshape(nh, len(rows), d), o_ref.reshape(nh, len(rows), d),
+            torch.bfloat16)
+    assert np.abs(lse[:, :, rows].cpu().double().numpy() - l_ref).max() < LSE_ABS

@@ -503,3 +503,24 @@ def test_prefill_dilated_without_sinks_is_plain_attention_on_each_residue_class(
         o_c, l_c = oracle.prefill(q[:, :, idx], k[:, :, idx], v[:, :, idx], w, 0, 0.5)
         np.testing.assert_allclose(o[:, :, idx], o_c, atol=1e-12)
         np.testing.assert_allclose(lse[:, :, idx], l_c, atol=1e-12)
+
+
+@pytest.mark.parametrize("L,w,s,r", [(60, 9, 3, 4), (41, 6, 2, 3), (25, 5, 0, 2), (30, 7, 4, 1), (10, 6, 4, 3),
+                                     (50, 4, 3, 9)])
+def test_dilated_window_is_the_plain_window_on_virtual_heads(L, w, s, r):
+    # the layout the GPU path uses: virtual head c = the s sinks, then the positions >= s of residue class
+    # c (mod r); the plain key set (s sinks, window w) of a row there is the dilated key set of that row
+    # in the sequence, and rows t < s are the sink prefix of head 0
+    rng = np.random.default_rng(22 + L + r)
+    d = 8
+    q, k, v = (rng.standard_normal((1, 1, L, d)) for _ in range(3))
+    o, lse = oracle.prefill_dilated(q, k, v, w, s, r, 0.4)
+    got_o, got_l = np.full_like(o, np.nan), np.full_like(lse, np.nan)
+    for c in range(r):
+        pos = list(range(min(s, L))) + [p for p in range(s, L) if p % r == c]
+        ov, lv = oracle.prefill(q[:, :, pos], k[:, :, pos], v[:, :, pos], w, s, 0.4)
+        for u, p in enumerate(pos):
+            if p >= s or c == 0:
+                got_o[:, :, p], got_l[:, :, p] = ov[:, :, u], lv[:, :, u]
+    np.testing.assert_allclose(got_o, o, atol=1e-12)
+    np.testing.assert_allclose(got_l, lse, atol=1e-12)
