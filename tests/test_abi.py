@@ -148,3 +148,54 @@ def test_rope_decode_validates_before_launch(lib):
     bad[8], bad[10] = 70000, 80000  # window past 2^16
     bad[14] = lib.swa_sink_decode_rope_workspace_size(1, 1, 128, 70000)
     assert lib.swa_sink_decode_step_rope(*bad) == swa.SWA_ERR_UNSUPPORTED
+
+
+def test_rope_prefills_validate_before_launch(lib):
+    f = 1 << 20  # never dereferenced: validation fails first
+    need = lib.swa_sink_prefill_rope_workspace_size(1, 2, 300, 128)
+    assert need == 3 * 2 * 300 * 128 * 2
+    ok = [f, f, f, f, None, 1, 2, 300, 128, 64, 4, 0.1, 10000.0, f << 8, need, swa.SWA_BF16, None]
+    bad = list(ok)
+    bad[15] = swa.SWA_F32  # the RoPE prefill runs on the tensor cores only
+    assert lib.swa_sink_prefill_rope(*bad) == swa.SWA_ERR_UNSUPPORTED
+    bad = list(ok)
+    bad[9], bad[10] = 300, 129  # more sinks than one key tile
+    assert lib.swa_sink_prefill_rope(*bad) == swa.SWA_ERR_UNSUPPORTED
+    bad = list(ok)
+    bad[12] = 0.5  # base must be > 1
+    assert lib.swa_sink_prefill_rope(*bad) == swa.SWA_ERR_INVALID
+    bad = list(ok)
+    bad[14] = need - 1
+    assert lib.swa_sink_prefill_rope(*bad) == swa.SWA_ERR_INVALID
+    # chunked: chunks shorter than the sinks are refused, and the workspace adds a rotated-key cache
+    cneed = lib.swa_sink_prefill_chunked_rope_workspace_size(1, 2, 300, 128, 64)
+    assert cneed == need + 2 * 64 * 128 * 2
+    cok = [f, f, f, f, None, f, f, 1, 2, 300, 128, 64, 8, 0.1, 32, 10000.0, f << 8, cneed, swa.SWA_BF16, None]
+    bad = list(cok)
+    bad[14] = 4  # chunk < s
+    assert lib.swa_sink_prefill_chunked_rope(*bad) == swa.SWA_ERR_INVALID
+    bad = list(cok)
+    bad[17] = cneed - 256
+    assert lib.swa_sink_prefill_chunked_rope(*bad) == swa.SWA_ERR_INVALID
+    # the RoPE tile plan refuses a chunk start inside the sinks
+    buf = (ctypes.c_int * (5 * 64))()
+    assert lib.swa_prefill_tile_plan_rope(8, 300, 3, 64, 8, buf, 64) == swa.SWA_ERR_UNSUPPORTED
+
+
+def test_dilated_prefill_validates_before_launch(lib):
+    f = 1 << 20
+    need = lib.swa_sink_prefill_dilated_workspace_size(1, 2, 300, 128, 4, 3, swa.SWA_BF16)
+    rows = 2 * 3 * (4 + (300 - 4 + 2) // 3)  # virtual heads x (sinks + the longest residue class)
+    assert need >= 4 * rows * 128 * 2 + rows * 4
+    ok = [f, f, f, f, None, 1, 2, 300, 128, 64, 4, 3, 0.1, f << 8, need, swa.SWA_BF16, None]
+    bad = list(ok)
+    bad[11] = 0  # dilation >= 1
+    assert lib.swa_sink_prefill_dilated(*bad) == swa.SWA_ERR_INVALID
+    bad = list(ok)
+    bad[14] = need - 1
+    assert lib.swa_sink_prefill_dilated(*bad) == swa.SWA_ERR_INVALID
+    bad = list(ok)
+    bad[5], bad[6], bad[11] = 65535, 32, 2  # B * H * r past the supported virtual heads
+    bad[14] = lib.swa_sink_prefill_dilated_workspace_size(65535, 32, 300, 128, 4, 2, swa.SWA_BF16)
+    assert lib.swa_sink_prefill_dilated(*bad) == swa.SWA_ERR_UNSUPPORTED
+    assert lib.swa_sink_prefill_dilated_workspace_size(1, 2, 300, 128, 4, 0, swa.SWA_BF16) == 0
