@@ -251,12 +251,12 @@ static int chunk_loop(const void *q, const void *k, const void *v, void *o, floa
                 if (rc) return rc;
             } else {
                 // rotated rows against the rotated cache; then the chunk's rotated keys into the scratch
-                // cache and its unrotated keys into the caller's (the values go to the caller's cache twice)
+                // cache, its unrotated keys and its values into the caller's
                 PrefillArgs a{qc, kc, vc, oc, lc, krg, vcg, c0, r1 - r0, n, d, w, s, scale, L, gs};
                 a.q_sink = static_cast<const char *>(rp->q_sink) + off;
                 rc = launch_prefill_bf16_tc(a);
                 if (rc) return rc;
-                rc = launch_kv_write(krg, vcg, kc, vc, r1 - r0, d, w, s, c0, n, L, es, gs);
+                rc = launch_kv_write(krg, nullptr, kc, nullptr, r1 - r0, d, w, s, c0, n, L, es, gs);
                 if (rc) return rc;
                 rc = launch_kv_write(kcg, vcg, static_cast<const char *>(rp->k_raw) + off, vc, r1 - r0, d, w, s, c0,
                                      n, L, es, gs);

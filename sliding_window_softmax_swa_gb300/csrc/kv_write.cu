@@ -33,9 +33,8 @@ __global__ void __launch_bounds__(256) kv_write_kernel(uint4 *__restrict__ kc, u
         const int64_t src = (bh * src_stride + (p - pos0)) * CHUNKS + c;
         const int64_t dst = (bh * w + slot) * CHUNKS + c;
         const uint4 kx = __ldg(kn + src);
-        const uint4 vx = __ldg(vn + src);
         kc[dst] = kx;
-        vc[dst] = vx;
+        if (vn != nullptr) vc[dst] = __ldg(vn + src);  // keys only when no values are given
     }
 }
 

@@ -56,7 +56,8 @@ size_t rope_prefill_workspace_bytes(int BH, int64_t L, int d);
 int launch_rope_prep(const void *q, const void *k, void *qr, void *qs, void *kr, int BH, int64_t L, int d, int w,
                      double base, cudaStream_t stream);
 
-// Rolling-cache write of positions pos0..pos0+n-1; source rows of (b, h) start at bh*src_stride.
+// Rolling-cache write of positions pos0..pos0+n-1; source rows of (b, h) start at bh*src_stride.  With
+// v_new == nullptr only the keys are written.
 int launch_kv_write(void *k_cache, void *v_cache, const void *k_new, const void *v_new, int BH, int d, int w,
                     int s, int64_t pos0, int64_t n, int64_t src_stride, int esize, cudaStream_t stream);
 
