@@ -305,9 +305,10 @@ def chunked_leg(swa, wl, steps, warmup, world, rank, clocks, rope=False):
             "ms_per_step": t / steps * 1e3, "launches": steps * (per_chunk * nch * groups + (1 if rope else 0))}
 
 
-def decode_leg(swa, wl, world, rank, clocks, steps=None, rope=False):
+def decode_leg(swa, wl, world, rank, clocks, steps=None, rope=False, dilation=0):
     """The whole streaming run: per step one rolling write of the new key/value and one decode (with
-    ``rope``: the decode with RoPE at the positions inside the cache, base 10000, unrotated keys)."""
+    ``rope``: the decode with RoPE at the positions inside the cache, base 10000, unrotated keys; with
+    ``dilation``: the dilated window, one rolling cache per residue class)."""
     import torch
     import swa_inputs
     B, H, d, w, s = wl.B, wl.H, wl.d, wl.w, wl.s
@@ -318,7 +319,7 @@ def decode_leg(swa, wl, world, rank, clocks, steps=None, rope=False):
     vs = swa_inputs.normal((T, B, H, d), seed, swa_inputs.TID_V, wl.torch_dtype, "cuda")
     if wl.sink_boost:
         ks[:4] *= 4.0
-    kc = torch.zeros((B, H, w, d), dtype=qs.dtype, device="cuda")
+    kc = torch.zeros(((dilation,) if dilation else ()) + (B, H, w, d), dtype=qs.dtype, device="cuda")
     vc = torch.zeros_like(kc)
     o = torch.empty((B, H, d), dtype=qs.dtype, device="cuda")
     lib = swa.lib()
@@ -332,6 +333,15 @@ def decode_leg(swa, wl, world, rank, clocks, steps=None, rope=False):
 
     def run(t0, t1):
         for t in range(t0, t1):
+            if dilation:
+                rc = lib.swa_sink_dilated_cache_write(kc.data_ptr(), vc.data_ptr(), kp + t * row, vp + t * row, B, H,
+                                                      d, w, s, dilation, t, dt, stream)
+                rc |= lib.swa_sink_decode_step_dilated(qp + t * row, kc.data_ptr(), vc.data_ptr(), o.data_ptr(),
+                                                       None, B, H, d, w, s, dilation, t, wl.scale, ws.data_ptr(), nws,
+                                                       dt, stream)
+                if rc:
+                    raise RuntimeError(swa.last_error())
+                continue
             rc = lib.kv_rolling_write(kc.data_ptr(), vc.data_ptr(), kp + t * row, vp + t * row, B, H, d, w, s, t, 1,
                                       dt, stream)
             if rope:
@@ -356,7 +366,10 @@ def decode_leg(swa, wl, world, rank, clocks, steps=None, rope=False):
     tl = T - 1
 
     def dstep():
-        if rope:
+        if dilation:
+            rc = lib.swa_sink_decode_step_dilated(qp + tl * row, kc.data_ptr(), vc.data_ptr(), o.data_ptr(), None, B,
+                                                  H, d, w, s, dilation, tl, wl.scale, ws.data_ptr(), nws, dt, stream)
+        elif rope:
             rc = lib.swa_sink_decode_step_rope(qp + tl * row, kc.data_ptr(), vc.data_ptr(), o.data_ptr(), None, B, H,
                                                d, w, s, tl, wl.scale, 10000.0, ws.data_ptr(), nws, dt, stream)
         else:
@@ -457,7 +470,8 @@ def main():
     ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--primary-only", action="store_true", help="only the primary prefill leg")
-    ap.add_argument("--legs", default="primary,mistral,chunked,decode,decode_rope,prefill_rope,chunked_rope,dilated",
+    ap.add_argument("--legs", default="primary,mistral,chunked,decode,decode_rope,prefill_rope,chunked_rope,dilated,"
+                                      "decode_dilated",
                     help="comma list of legs to run (profiling runs pick one)")
     ap.add_argument("--decode-steps", type=int, default=None, help="shorter decode stream (profiling only)")
     args = ap.parse_args()
@@ -537,6 +551,15 @@ def main():
                                            "frac": r["kernel"]["gbs"] / peaks["hbm_gbs"],
                                            "frac_of_8tbs_nominal": r["kernel"]["gbs"] / 8000.0,
                                            "avg_us": r["kernel"]["avg_us"]}}
+    if "decode_dilated" in legs:
+        dw = swa_inputs.WORKLOADS["decode_llama13b_B64_w1024_s4_20480"]
+        r = decode_leg(swa, dw, world, rank, clocks, steps=args.decode_steps, dilation=2)
+        secondary["decode_dilated_llama13b_B64_w1024_s4_r2_20480"] = {
+            "metric": "decode tok/s", "value": aggregate_rate(r["tok_per_s"], world, 1.0), "unit": "tok/s",
+            "seconds": r["seconds"], "what": "dilated window with sinks, r = 2: one rolling cache per residue class",
+            "roofline": {"bound": "hbm", "kernel": "decode_kernel", "achieved": r["kernel"]["gbs"],
+                         "peak": peaks["hbm_gbs"], "unit": "GB/s", "frac": r["kernel"]["gbs"] / peaks["hbm_gbs"],
+                         "avg_us": r["kernel"]["avg_us"]}}
     if "decode_rope" in legs:
         dw = swa_inputs.WORKLOADS["decode_llama13b_B64_w1024_s4_20480"]
         r = decode_leg(swa, dw, world, rank, clocks, steps=args.decode_steps, rope=True)

@@ -230,6 +230,26 @@ int swa_sink_decode_step_noalloc(const void *q, const void *k_cache, const void 
 size_t swa_sink_decode_workspace_size(int B, int H, int d, int w);
 
 /*
+ * swa_sink_dilated_cache_write / swa_sink_decode_step_dilated -- streaming decode over the dilated window
+ * with sinks (as swa_sink_prefill_dilated: step t attends the s sinks and t, t - r, ..., t - (m-1) r).
+ * The cache is r rolling caches, one per residue class of positions mod r, class-major
+ * [r, B, H, w, d]: cache c holds the sinks in slots 0..s-1 and a ring of m slots for the positions p >= s
+ * with p = c (mod r).  Per step, write then attend: swa_sink_dilated_cache_write(t) puts the new key/value
+ * ([B, H, d]) into cache t mod r (a sink into all r caches), and swa_sink_decode_step_dilated(t) runs the
+ * decode of swa_sink_decode_step on cache t mod r: it reads w rows per (b, h), as the plain decode does.
+ *
+ *   k_cache, v_cache : [r, B, H, w, d], zero-initialised or never read before written.
+ *   r       : dilation, 1 <= r <= 65536; r = 1 is the plain rolling cache and decode.
+ *   workspace / workspace_bytes : as swa_sink_decode_step (swa_sink_decode_workspace_size(B, H, d, w)).
+ *   Other arguments and errors as kv_rolling_write (one position) and swa_sink_decode_step.
+ */
+int swa_sink_dilated_cache_write(void *k_cache, void *v_cache, const void *k_new, const void *v_new, int B, int H,
+                                 int d, int w, int s, int r, int64_t t, int dtype, void *stream);
+int swa_sink_decode_step_dilated(const void *q, const void *k_cache, const void *v_cache, void *o, float *lse,
+                                 int B, int H, int d, int w, int s, int r, int64_t t, float scale, void *workspace,
+                                 size_t workspace_bytes, int dtype, void *stream);
+
+/*
  * swa_sink_decode_step_rope -- swa_sink_decode_step with rotary position embedding applied at the
  * positions the entries have inside the cache, as the StreamingLLM section of "滑窗与固定稀疏" describes:
  * the cache keeps the keys unrotated; at every step its valid entries, sinks first and then the window

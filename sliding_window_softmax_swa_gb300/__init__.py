@@ -8,13 +8,15 @@ built with ``build.build()``.
 from ._binding import (SWA_BF16, SWA_ERR_CUDA, SWA_ERR_INVALID, SWA_ERR_TIMEOUT, SWA_ERR_UNSUPPORTED, SWA_F32,
                        SWA_OK, SIGNATURES, SwaError, kv_rolling_write, last_error, lib, library_path,
                        prefill_tile_plan, prefill_tile_plan_rope, swa_device_status, swa_sink_decode_step,
+                       swa_sink_decode_step_dilated, swa_sink_dilated_cache_write,
                        swa_sink_decode_step_rope, swa_sink_decode_workspace_size, swa_sink_prefill,
                        swa_sink_prefill_chunked, swa_sink_prefill_chunked_rope, swa_sink_prefill_dilated,
                        swa_sink_prefill_host, swa_sink_prefill_rope)
 
 __all__ = ["swa_sink_prefill", "swa_sink_prefill_chunked", "swa_sink_prefill_host", "swa_sink_prefill_rope",
            "swa_sink_prefill_chunked_rope", "swa_sink_prefill_dilated",
-           "kv_rolling_write", "swa_sink_decode_step", "swa_sink_decode_step_rope",
+           "kv_rolling_write", "swa_sink_decode_step", "swa_sink_decode_step_rope", "swa_sink_dilated_cache_write",
+           "swa_sink_decode_step_dilated",
            "swa_sink_decode_workspace_size", "swa_device_status", "prefill_tile_plan", "prefill_tile_plan_rope",
            "last_error", "lib", "library_path", "SwaError", "SIGNATURES", "SWA_OK", "SWA_ERR_INVALID",
            "SWA_ERR_UNSUPPORTED", "SWA_ERR_CUDA", "SWA_ERR_TIMEOUT", "SWA_BF16", "SWA_F32"]

@@ -42,6 +42,9 @@ SIGNATURES = {
     "swa_prefill_tile_plan": (_i, [_i64, _i64, _i64, _i, _i, ctypes.POINTER(ctypes.c_int), _i]),
     "swa_prefill_tile_plan_rope": (_i, [_i64, _i64, _i64, _i, _i, ctypes.POINTER(ctypes.c_int), _i]),
     "swa_sink_prefill_dilated": (_i, [_vp, _vp, _vp, _vp, _vp, _i, _i, _i64, _i, _i, _i, _i, _f, _vp, _sz, _i, _vp]),
+    "swa_sink_dilated_cache_write": (_i, [_vp, _vp, _vp, _vp, _i, _i, _i, _i, _i, _i, _i64, _i, _vp]),
+    "swa_sink_decode_step_dilated": (_i, [_vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _i, _i, _i64, _f, _vp, _sz, _i,
+                                          _vp]),
     "swa_sink_prefill_dilated_workspace_size": (_sz, [_i, _i, _i64, _i, _i, _i, _i]),
     "swa_sink_prefill_chunked_rope": (_i, [_vp, _vp, _vp, _vp, _vp, _vp, _vp, _i, _i, _i64, _i, _i, _i, _f, _i64,
                                            ctypes.c_double, _vp, _sz, _i, _vp]),
@@ -132,6 +135,35 @@ def swa_sink_prefill(q, k, v, w: int, s: int, scale: float | None = None, o=None
     _check("swa_sink_prefill", lib().swa_sink_prefill(
         _ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), _ptr(k_cache), _ptr(v_cache), pos0, B, H, L, d, w, s,
         scale, _dtype_code(q), _stream(stream)))
+    return o
+
+
+def swa_sink_dilated_cache_write(k_cache, v_cache, k_new, v_new, s: int, r: int, t: int, stream=None):
+    """Write position t's key/value ([B, H, d]) into the dilated caches [r, B, H, w, d] (write, then attend)."""
+    r_, B, H, w, d = k_cache.shape
+    assert r_ == r and k_new.shape == (B, H, d) and v_new.shape == (B, H, d)
+    _dev(k_cache, v_cache, k_new, v_new)
+    _check("swa_sink_dilated_cache_write", lib().swa_sink_dilated_cache_write(
+        _ptr(k_cache), _ptr(v_cache), _ptr(k_new), _ptr(v_new), B, H, d, w, s, r, t, _dtype_code(k_cache),
+        _stream(stream)))
+
+
+def swa_sink_decode_step_dilated(q, k_cache, v_cache, s: int, r: int, t: int, scale: float | None = None, o=None,
+                                 lse=None, workspace=None, stream=None):
+    """Decode step at position t over the dilated window with sinks (caches [r, B, H, w, d])."""
+    B, H, d = q.shape
+    r_, _, _, w, _ = k_cache.shape
+    assert r_ == r
+    if o is None:
+        o = torch.empty_like(q)
+    nws = lib().swa_sink_decode_workspace_size(B, H, d, w)
+    if workspace is None:
+        workspace = torch.empty(max(nws, 256), dtype=torch.uint8, device=q.device)
+    _dev(q, k_cache, v_cache, o, lse, workspace)
+    scale = (1.0 / d ** 0.5) if scale is None else scale
+    _check("swa_sink_decode_step_dilated", lib().swa_sink_decode_step_dilated(
+        _ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(o), _ptr(lse), B, H, d, w, s, r, t, scale, _ptr(workspace),
+        workspace.numel() * workspace.element_size(), _dtype_code(q), _stream(stream)))
     return o
 
 

@@ -462,6 +462,65 @@ extern "C" int swa_sink_decode_step(const void *q, const void *k_cache, const vo
     return launch_decode(a);
 }
 
+// The dilated window in streaming form.  r rolling caches, one per residue class of positions mod r, laid
+// out class-major [r, B, H, w, d]: cache c holds the s sinks in slots 0..s-1 and a ring of m slots for the
+// positions p >= s with p = c (mod r), each at its class-local position s + (p - p0(c)) / r, p0(c) the first
+// such position.  At step t cache (t mod r) then holds exactly the dilated key set of t, so the plain
+// rolling write and decode run on it at t's class-local position.  Rows t < s use cache 0.
+static int64_t dilated_local(int64_t t, int s, int r, int *cls) {
+    if (t < s) {
+        *cls = 0;
+        return t;
+    }
+    const int c = static_cast<int>(t % r);
+    const int64_t p0 = s + ((c - s) % r + r) % r;
+    *cls = c;
+    return s + (t - p0) / r;
+}
+
+extern "C" int swa_sink_dilated_cache_write(void *k_cache, void *v_cache, const void *k_new, const void *v_new,
+                                            int B, int H, int d, int w, int s, int r, int64_t t, int dtype,
+                                            void *stream) {
+    t_err[0] = 0;
+    int rc = check_common(B, H, d, w, s, dtype);
+    if (rc) return rc;
+    if (r < 1 || r > 65536) return fail(SWA_ERR_INVALID, "dilation r=%d must be in [1, 65536]", r);
+    if (t < 0 || t >= (int64_t(1) << 62)) return fail(SWA_ERR_INVALID, "t=%lld out of range", (long long)t);
+    if (!k_cache || !v_cache || !k_new || !v_new)
+        return fail(SWA_ERR_INVALID, "k_cache, v_cache, k_new and v_new must be non-null");
+    if (!aligned16(k_cache) || !aligned16(v_cache) || !aligned16(k_new) || !aligned16(v_new))
+        return fail(SWA_ERR_INVALID, "cache and new tensors must be 16-byte aligned");
+    const int es = esize_of(dtype);
+    const size_t slab = static_cast<size_t>(B) * H * w * d * es;  // one class's cache
+    const cudaStream_t st = static_cast<cudaStream_t>(stream);
+    int c = 0;
+    const int64_t local = dilated_local(t, s, r, &c);
+    for (int cc = (t < s ? 0 : c); cc < (t < s ? r : c + 1); ++cc) {  // a sink goes into every class's cache
+        rc = launch_kv_write(static_cast<char *>(k_cache) + cc * slab, static_cast<char *>(v_cache) + cc * slab, k_new,
+                             v_new, B * H, d, w, s, local, 1, 1, es, st);
+        if (rc) return rc;
+    }
+    return SWA_OK;
+}
+
+extern "C" int swa_sink_decode_step_dilated(const void *q, const void *k_cache, const void *v_cache, void *o,
+                                            float *lse, int B, int H, int d, int w, int s, int r, int64_t t,
+                                            float scale, void *workspace, size_t workspace_bytes, int dtype,
+                                            void *stream) {
+    t_err[0] = 0;
+    if (r < 1 || r > 65536) return fail(SWA_ERR_INVALID, "dilation r=%d must be in [1, 65536]", r);
+    if (t < 0 || t >= (int64_t(1) << 62)) return fail(SWA_ERR_INVALID, "t=%lld out of range", (long long)t);
+    int rc = check_common(B, H, d, w, s, dtype);
+    if (rc) return rc;
+    if (!k_cache || !v_cache) return fail(SWA_ERR_INVALID, "caches must be non-null");
+    int c = 0;
+    const int64_t local = dilated_local(t, s, r, &c);
+    const size_t slab = static_cast<size_t>(B) * H * w * d * esize_of(dtype);
+    return swa_sink_decode_step(q, static_cast<const char *>(k_cache) + c * slab,
+                                static_cast<const char *>(v_cache) + c * slab, o, lse, B, H, d, w, s, local, scale,
+                                workspace, workspace_bytes, dtype, stream);
+}
+
 extern "C" int swa_sink_decode_step_rope(const void *q, const void *k_cache, const void *v_cache, void *o,
                                          float *lse, int B, int H, int d, int w, int s, int64_t t, float scale,
                                          double rope_base, void *workspace, size_t workspace_bytes, int dtype,

@@ -46,3 +46,32 @@ def test_dilation_one_is_the_plain_prefill_bit_for_bit():
     assert swa.swa_device_status() == swa.SWA_OK, swa.last_error()
     assert torch.equal(a.view(torch.int16), b.view(torch.int16))
     assert torch.equal(la, lb)
+
+
+@pytest.mark.parametrize("dtype,d,w,s,r", [
+    (torch.bfloat16, 128, 40, 4, 3),
+    (torch.bfloat16, 64, 24, 0, 2),
+    (torch.bfloat16, 16, 17, 16, 4),
+    (torch.float32, 16, 16, 4, 2),
+    (torch.bfloat16, 128, 9, 1, 1),
+])
+def test_dilated_streaming_decode_every_step(dtype, d, w, s, r):
+    # write, then attend, through the per-class caches; every step against the oracle's dilated key set
+    swa = require_gpu()
+    B, H = 2, 3
+    T = 3 * w * r + 5
+    q, k, v = swa_inputs.prefill_inputs(B, H, T, d, 400 + d + r, dtype, "cpu", sink_boost=True)
+    kc = torch.zeros((r, B, H, w, d), dtype=dtype, device="cuda")
+    vc = torch.zeros_like(kc)
+    qg, kg, vg = q.cuda(), k.cuda(), v.cuda()
+    outs, lses = [], []
+    for t in range(T):
+        swa.swa_sink_dilated_cache_write(kc, vc, kg[:, :, t].contiguous(), vg[:, :, t].contiguous(), s, r, t)
+        lse = torch.empty((B, H), dtype=torch.float32, device="cuda")
+        outs.append(swa.swa_sink_decode_step_dilated(qg[:, :, t].contiguous(), kc, vc, s, r, t, lse=lse).cpu())
+        lses.append(lse.cpu())
+    assert swa.swa_device_status() == swa.SWA_OK, swa.last_error()
+    o_ref, l_ref = oracle.prefill_dilated(q, k, v, w, s, r, 1.0 / math.sqrt(d))
+    for t in range(T):
+        compare(f"dilated decode t={t}", outs[t], o_ref[:, :, t], dtype)
+        assert np.abs(lses[t].double().numpy() - l_ref[:, :, t]).max() < LSE_ABS

@@ -524,3 +524,18 @@ def test_dilated_window_is_the_plain_window_on_virtual_heads(L, w, s, r):
                 got_o[:, :, p], got_l[:, :, p] = ov[:, :, u], lv[:, :, u]
     np.testing.assert_allclose(got_o, o, atol=1e-12)
     np.testing.assert_allclose(got_l, lse, atol=1e-12)
+
+
+@pytest.mark.parametrize("w,s,r", [(5, 2, 3), (8, 0, 2), (6, 4, 4), (9, 3, 1)])
+def test_dilated_class_caches_hold_the_dilated_key_set(w, s, r):
+    # the streaming layout: one rolling cache per residue class mod r, holding the sinks and the class's
+    # positions >= s at class-local positions s, s + 1, ...; after writing step t, cache t mod r (cache 0
+    # for t < s) holds exactly the dilated key set of t (the oracle's own slot replay per class)
+    for t in range(70):
+        c = 0 if t < s else t % r
+        p0 = s + ((c - s) % r)
+        local = t if t < s else s + (t - p0) // r
+        held = oracle.cache_replay(w, s, local + 1)  # class-local position held by each slot
+        orig = {int(x) if x < s else p0 + (int(x) - s) * r for x in held if x >= 0}
+        want = {i for i in range(t + 1) if oracle.is_key_dilated(t, i, w, s, r)}
+        assert orig == want, (w, s, r, t)
