@@ -140,8 +140,8 @@ size_t swa_sink_prefill_chunked_rope_workspace_size(int B, int H, int64_t L, int
  * causal and with the sinks of the StreamingLLM section.  Row t attends
  *     {i < s}  |  {t - j r : 0 <= j < m},  m = w - s,  restricted to i <= t  (each key once),
  * so the window reaches (m - 1) r + 1 positions back at the cost of m keys; r = 1 is swa_sink_prefill.
- * Runs as a gather into r virtual heads per (b, h) (the sinks, then one residue class of positions mod r),
- * the prefill of swa_sink_prefill on them, and a scatter back.
+ * Runs as a gather into r virtual heads per (b, h) (the sinks, then one residue class of positions mod r;
+ * class-major), the prefill of swa_sink_prefill on them, and a scatter back.
  *
  *   q, k, v, o, lse : as swa_sink_prefill (pos0 = 0), bf16 with d = 128 (tensor cores) or fp32.
  *   r       : dilation, 1 <= r <= 65536, B * H * r <= 65535 * 32.
@@ -153,6 +153,17 @@ int swa_sink_prefill_dilated(const void *q, const void *k, const void *v, void *
                              int64_t L, int d, int w, int s, int r, float scale, void *workspace,
                              size_t workspace_bytes, int dtype, void *stream);
 size_t swa_sink_prefill_dilated_workspace_size(int B, int H, int64_t L, int d, int s, int r, int dtype);
+
+/*
+ * swa_sink_prefill_chunked_dilated -- swa_sink_prefill_dilated through the per-class rolling caches of
+ * swa_sink_decode_step_dilated: the virtual heads (class-major) go through the chunk loop of
+ * swa_sink_prefill_chunked, chunk / r class-local rows at a time.  The rows equal swa_sink_prefill_dilated's,
+ * and k_cache / v_cache ([r, B, H, w, d], overwritten) end up as L calls of swa_sink_dilated_cache_write
+ * leave them, ready for swa_sink_decode_step_dilated at t = L.  workspace as swa_sink_prefill_dilated.
+ */
+int swa_sink_prefill_chunked_dilated(const void *q, const void *k, const void *v, void *o, float *lse, void *k_cache,
+                                     void *v_cache, int B, int H, int64_t L, int d, int w, int s, int r, float scale,
+                                     int64_t chunk, void *workspace, size_t workspace_bytes, int dtype, void *stream);
 
 /*
  * swa_sink_prefill_chunked -- the chunk-based prefill of "滑窗与固定稀疏" (rolling-buffer section):

@@ -10,11 +10,12 @@ from ._binding import (SWA_BF16, SWA_ERR_CUDA, SWA_ERR_INVALID, SWA_ERR_TIMEOUT,
                        prefill_tile_plan, prefill_tile_plan_rope, swa_device_status, swa_sink_decode_step,
                        swa_sink_decode_step_dilated, swa_sink_dilated_cache_write,
                        swa_sink_decode_step_rope, swa_sink_decode_workspace_size, swa_sink_prefill,
-                       swa_sink_prefill_chunked, swa_sink_prefill_chunked_rope, swa_sink_prefill_dilated,
+                       swa_sink_prefill_chunked, swa_sink_prefill_chunked_dilated, swa_sink_prefill_chunked_rope,
+                       swa_sink_prefill_dilated,
                        swa_sink_prefill_host, swa_sink_prefill_rope)
 
 __all__ = ["swa_sink_prefill", "swa_sink_prefill_chunked", "swa_sink_prefill_host", "swa_sink_prefill_rope",
-           "swa_sink_prefill_chunked_rope", "swa_sink_prefill_dilated",
+           "swa_sink_prefill_chunked_rope", "swa_sink_prefill_dilated", "swa_sink_prefill_chunked_dilated",
            "kv_rolling_write", "swa_sink_decode_step", "swa_sink_decode_step_rope", "swa_sink_dilated_cache_write",
            "swa_sink_decode_step_dilated",
            "swa_sink_decode_workspace_size", "swa_device_status", "prefill_tile_plan", "prefill_tile_plan_rope",

@@ -42,6 +42,8 @@ SIGNATURES = {
     "swa_prefill_tile_plan": (_i, [_i64, _i64, _i64, _i, _i, ctypes.POINTER(ctypes.c_int), _i]),
     "swa_prefill_tile_plan_rope": (_i, [_i64, _i64, _i64, _i, _i, ctypes.POINTER(ctypes.c_int), _i]),
     "swa_sink_prefill_dilated": (_i, [_vp, _vp, _vp, _vp, _vp, _i, _i, _i64, _i, _i, _i, _i, _f, _vp, _sz, _i, _vp]),
+    "swa_sink_prefill_chunked_dilated": (_i, [_vp, _vp, _vp, _vp, _vp, _vp, _vp, _i, _i, _i64, _i, _i, _i, _i, _f, _i64,
+                                              _vp, _sz, _i, _vp]),
     "swa_sink_dilated_cache_write": (_i, [_vp, _vp, _vp, _vp, _i, _i, _i, _i, _i, _i, _i64, _i, _vp]),
     "swa_sink_decode_step_dilated": (_i, [_vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _i, _i, _i64, _f, _vp, _sz, _i,
                                           _vp]),
@@ -135,6 +137,25 @@ def swa_sink_prefill(q, k, v, w: int, s: int, scale: float | None = None, o=None
     _check("swa_sink_prefill", lib().swa_sink_prefill(
         _ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), _ptr(k_cache), _ptr(v_cache), pos0, B, H, L, d, w, s,
         scale, _dtype_code(q), _stream(stream)))
+    return o
+
+
+def swa_sink_prefill_chunked_dilated(q, k, v, s: int, r: int, chunk: int, k_cache, v_cache,
+                                     scale: float | None = None, o=None, lse=None, workspace=None, stream=None):
+    """Chunked prefill over the dilated window through the per-class caches [r, B, H, w, d] (overwritten)."""
+    B, H, L, d = q.shape
+    w = k_cache.shape[3]
+    assert k_cache.shape == (r, B, H, w, d)
+    if o is None:
+        o = torch.empty_like(q)
+    nws = lib().swa_sink_prefill_dilated_workspace_size(B, H, L, d, s, r, _dtype_code(q))
+    if workspace is None:
+        workspace = torch.empty(max(nws, 256), dtype=torch.uint8, device=q.device)
+    _dev(q, k, v, o, lse, k_cache, v_cache, workspace)
+    scale = (1.0 / d ** 0.5) if scale is None else scale
+    _check("swa_sink_prefill_chunked_dilated", lib().swa_sink_prefill_chunked_dilated(
+        _ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), _ptr(k_cache), _ptr(v_cache), B, H, L, d, w, s, r, scale,
+        chunk, _ptr(workspace), workspace.numel() * workspace.element_size(), _dtype_code(q), _stream(stream)))
     return o
 
 

@@ -207,10 +207,11 @@ struct ChunkRope {
     void *kc_rot;        // [BH, w, d] scratch cache of rotated keys, read by the prefill for positions < pos0
 };
 
-// The chunk loop of chunked prefill (validated arguments, L > 0).
+// The chunk loop of chunked prefill (validated arguments, L > 0): L rows per (b, h), consecutive (b, h)
+// blocks of q/k/v/o (and lse) `stride` rows apart.
 static int chunk_loop(const void *q, const void *k, const void *v, void *o, float *lse, void *k_cache, void *v_cache,
-                      int B, int H, int64_t L, int d, int w, int s, float scale, int64_t chunk, int dtype,
-                      cudaStream_t st, const ChunkRope *rp) {
+                      int B, int H, int64_t L, int64_t stride, int d, int w, int s, float scale, int64_t chunk,
+                      int dtype, cudaStream_t st, const ChunkRope *rp) {
     const int es = esize_of(dtype);
     const size_t row_bytes = static_cast<size_t>(d) * es;
     int rc = SWA_OK;
@@ -230,7 +231,7 @@ static int chunk_loop(const void *q, const void *k, const void *v, void *o, floa
         const int r0 = static_cast<int>(static_cast<int64_t>(BH) * g / groups);
         const int r1 = static_cast<int>(static_cast<int64_t>(BH) * (g + 1) / groups);
         cudaStream_t gs = groups > 1 ? cs->stream[g] : st;
-        const size_t seq_off = static_cast<size_t>(r0) * static_cast<size_t>(L) * row_bytes;  // rows of q, k, v, o
+        const size_t seq_off = static_cast<size_t>(r0) * static_cast<size_t>(stride) * row_bytes;  // q, k, v, o
         const size_t cache_off = static_cast<size_t>(r0) * static_cast<size_t>(w) * row_bytes;
         void *kcg = static_cast<char *>(k_cache) + cache_off;
         void *vcg = static_cast<char *>(v_cache) + cache_off;
@@ -242,24 +243,24 @@ static int chunk_loop(const void *q, const void *k, const void *v, void *o, floa
             const char *kc = static_cast<const char *>(k) + off;
             const char *vc = static_cast<const char *>(v) + off;
             char *oc = static_cast<char *>(o) + off;
-            float *lc = lse ? lse + static_cast<int64_t>(r0) * L + c0 : nullptr;
+            float *lc = lse ? lse + static_cast<int64_t>(r0) * stride + c0 : nullptr;
             if (!rp) {
                 // prefill_impl treats its B as the number of (b, h) rows when H = 1
-                rc = prefill_impl(qc, kc, vc, oc, lc, kcg, vcg, c0, r1 - r0, 1, n, d, w, s, scale, dtype, L, gs);
+                rc = prefill_impl(qc, kc, vc, oc, lc, kcg, vcg, c0, r1 - r0, 1, n, d, w, s, scale, dtype, stride, gs);
                 if (rc) return rc;
-                rc = launch_kv_write(kcg, vcg, kc, vc, r1 - r0, d, w, s, c0, n, L, es, gs);
+                rc = launch_kv_write(kcg, vcg, kc, vc, r1 - r0, d, w, s, c0, n, stride, es, gs);
                 if (rc) return rc;
             } else {
                 // rotated rows against the rotated cache; then the chunk's rotated keys into the scratch
                 // cache, its unrotated keys and its values into the caller's
-                PrefillArgs a{qc, kc, vc, oc, lc, krg, vcg, c0, r1 - r0, n, d, w, s, scale, L, gs};
+                PrefillArgs a{qc, kc, vc, oc, lc, krg, vcg, c0, r1 - r0, n, d, w, s, scale, stride, gs};
                 a.q_sink = static_cast<const char *>(rp->q_sink) + off;
                 rc = launch_prefill_bf16_tc(a);
                 if (rc) return rc;
-                rc = launch_kv_write(krg, nullptr, kc, nullptr, r1 - r0, d, w, s, c0, n, L, es, gs);
+                rc = launch_kv_write(krg, nullptr, kc, nullptr, r1 - r0, d, w, s, c0, n, stride, es, gs);
                 if (rc) return rc;
                 rc = launch_kv_write(kcg, vcg, static_cast<const char *>(rp->k_raw) + off, vc, r1 - r0, d, w, s, c0,
-                                     n, L, es, gs);
+                                     n, stride, es, gs);
                 if (rc) return rc;
             }
         }
@@ -285,7 +286,7 @@ extern "C" int swa_sink_prefill_chunked(const void *q, const void *k, const void
     if (!k_cache || !v_cache) return fail(SWA_ERR_INVALID, "k_cache and v_cache must be non-null");
     if (!aligned16(k_cache) || !aligned16(v_cache))
         return fail(SWA_ERR_INVALID, "k_cache and v_cache must be 16-byte aligned");
-    return chunk_loop(q, k, v, o, lse, k_cache, v_cache, B, H, L, d, w, s, scale, chunk, dtype,
+    return chunk_loop(q, k, v, o, lse, k_cache, v_cache, B, H, L, L, d, w, s, scale, chunk, dtype,
                       static_cast<cudaStream_t>(stream), nullptr);
 }
 
@@ -324,7 +325,7 @@ extern "C" int swa_sink_prefill_chunked_rope(const void *q, const void *k, const
     rc = launch_rope_prep(q, k, qr, qs, kr, B * H, L, d, w, rope_base, st);
     if (rc) return rc;
     const ChunkRope rp{qs, k, kc_rot};
-    return chunk_loop(qr, kr, v, o, lse, k_cache, v_cache, B, H, L, d, w, s, scale, chunk, dtype, st, &rp);
+    return chunk_loop(qr, kr, v, o, lse, k_cache, v_cache, B, H, L, L, d, w, s, scale, chunk, dtype, st, &rp);
 }
 
 // Streams and events of the host-buffer prefill pipeline (copies in, compute, copies out), created once
@@ -627,6 +628,65 @@ extern "C" int swa_sink_prefill_dilated(const void *q, const void *k, const void
     // the virtual heads as (b, h) rows of a plain prefill: s sinks, window w
     rc = prefill_impl(qv, kv, vv, ov, lsev, nullptr, nullptr, 0, VH, 1, Lv, d, w, s, scale, dtype, Lv, st);
     if (rc) return rc;
+    return launch_dilate_scatter(ov, lsev, o, lse, B * H, L, d, es, s, r, st);
+}
+
+extern "C" int swa_sink_prefill_chunked_dilated(const void *q, const void *k, const void *v, void *o, float *lse,
+                                                void *k_cache, void *v_cache, int B, int H, int64_t L, int d, int w,
+                                                int s, int r, float scale, int64_t chunk, void *workspace,
+                                                size_t workspace_bytes, int dtype, void *stream) {
+    t_err[0] = 0;
+    int rc = check_prefill(q, k, v, o, lse, 0, B, H, L, d, w, s, scale, dtype);
+    if (rc) return rc;
+    if (r < 1 || r > 65536) return fail(SWA_ERR_INVALID, "dilation r=%d must be in [1, 65536]", r);
+    if (chunk < 1) return fail(SWA_ERR_INVALID, "chunk=%lld must be >= 1", (long long)chunk);
+    if (static_cast<int64_t>(B) * H * r > 65535 * 32)
+        return fail(SWA_ERR_UNSUPPORTED, "B*H*r=%lld exceeds the supported %d", (long long)B * H * r, 65535 * 32);
+    const size_t need = swa_sink_prefill_dilated_workspace_size(B, H, L, d, s, r, dtype);
+    if (workspace_bytes < need)
+        return fail(SWA_ERR_INVALID, "workspace of %zu bytes is smaller than the %zu needed", workspace_bytes, need);
+    if (L == 0) return SWA_OK;
+    if (!k_cache || !v_cache) return fail(SWA_ERR_INVALID, "k_cache and v_cache must be non-null");
+    if (!aligned16(k_cache) || !aligned16(v_cache))
+        return fail(SWA_ERR_INVALID, "k_cache and v_cache must be 16-byte aligned");
+    if (!workspace || (reinterpret_cast<uintptr_t>(workspace) & 255u))
+        return fail(SWA_ERR_INVALID, "workspace must be non-null and 256-byte aligned");
+    const cudaStream_t st = static_cast<cudaStream_t>(stream);
+    const int es = esize_of(dtype);
+    const int VH = B * H * r;
+    const int64_t Lv = dilated_rows(L, s, r);
+    const size_t one = align256(static_cast<size_t>(VH) * Lv * d * es);
+    char *ws = static_cast<char *>(workspace);
+    void *qv = ws, *kv = ws + one, *vv = ws + 2 * one, *ov = ws + 3 * one;
+    float *lsev = reinterpret_cast<float *>(ws + 4 * one);
+    rc = launch_dilate_gather(q, k, v, qv, kv, vv, B * H, L, d, es, s, r, st);
+    if (rc) return rc;
+    // The virtual heads (class-major, as the per-class caches [r, B, H, w, d]) through the plain chunk loop,
+    // chunk / r class-local rows at a time.  Each class runs at its own length (the sinks + its positions
+    // >= s; the classes differ by at most one row), so that no padding row is ever written into a cache:
+    // runs of classes of equal length share one loop (the longer classes form one cyclic run, so at most
+    // three loops).
+    const int64_t vchunk = chunk / r > 0 ? chunk / r : 1;
+    const int64_t head = L < s ? L : s;
+    const size_t rb = static_cast<size_t>(d) * es;
+    auto class_rows = [&](int c) -> int64_t {  // rows of virtual head class c
+        if (L <= s) return head;
+        const int64_t p0 = s + ((c - s) % r + r) % r;
+        return head + (p0 < L ? (L - 1 - p0) / r + 1 : 0);
+    };
+    const int BH = B * H;
+    for (int ca = 0; ca < r;) {
+        const int64_t n = class_rows(ca);
+        int cb = ca + 1;
+        while (cb < r && class_rows(cb) == n) ++cb;
+        const size_t vo = static_cast<size_t>(ca) * BH * Lv, co = static_cast<size_t>(ca) * BH * w;
+        rc = chunk_loop(static_cast<char *>(qv) + vo * rb, static_cast<char *>(kv) + vo * rb,
+                        static_cast<char *>(vv) + vo * rb, static_cast<char *>(ov) + vo * rb, lsev + vo,
+                        static_cast<char *>(k_cache) + co * rb, static_cast<char *>(v_cache) + co * rb, (cb - ca) * BH, 1,
+                        n, Lv, d, w, s, scale, vchunk, dtype, st, nullptr);
+        if (rc) return rc;
+        ca = cb;
+    }
     return launch_dilate_scatter(ov, lsev, o, lse, B * H, L, d, es, s, r, st);
 }
 

@@ -3,8 +3,8 @@
 // The dilated sliding window of "滑窗与固定稀疏" (glossary and Longformer section) lets the attended window
 // positions skip r - 1 tokens: causal, with the sinks of the StreamingLLM section, row t attends
 //     K_r(t) = {i < s} | {t - j r : 0 <= j < m},  m = w - s, restricted to i <= t.
-// Re-laid out, this is the plain band with sinks of the tensor-core prefill.  Virtual head (b, h, c),
-// c = 0 .. r-1, is the sequence
+// Re-laid out, this is the plain band with sinks of the tensor-core prefill.  Virtual head (c, b, h),
+// c = 0 .. r-1 (class-major: the layout of the streaming decode's per-class caches), is the sequence
 //     positions 0 .. s-1 (the sinks), then the positions p >= s with p = c (mod r), increasing.
 // A row t >= s of class c = t mod r sits in it after the sinks, and its plain key set there -- the sinks
 // and the m rows back from it -- holds exactly the sinks and t, t - r, ..., t - (m-1) r (those below s
@@ -41,11 +41,11 @@ __global__ void __launch_bounds__(256) dilate_gather_kernel(const uint4 *__restr
     for (int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; i < total;
          i += static_cast<int64_t>(gridDim.x) * blockDim.x) {
         const int ch = static_cast<int>(i % chunks);
-        const int64_t row = i / chunks;  // (vh, u)
+        const int64_t row = i / chunks;  // (vh, u), vh = c * BH + bh
         const int64_t u = row % Lv;
         const int64_t vh = row / Lv;
-        const int c = static_cast<int>(vh % r);
-        const int64_t bh = vh / r;
+        const int c = static_cast<int>(vh / BH);
+        const int64_t bh = vh % BH;
         const int64_t p = dilated_source(u, c, s, r, L);
         uint4 a = make_uint4(0, 0, 0, 0), b = a, e = a;
         if (p >= 0) {
@@ -78,7 +78,7 @@ __global__ void __launch_bounds__(256) dilate_scatter_kernel(const uint4 *__rest
             const int64_t p0 = s + ((c - s) % r + r) % r;
             u = s + (t - p0) / r;
         }
-        const int64_t src_row = (bh * r + c) * Lv + u;
+        const int64_t src_row = (static_cast<int64_t>(c) * BH + bh) * Lv + u;
         o[i] = __ldg(ov + src_row * chunks + ch);
         if (lse && ch == 0) lse[row] = __ldg(lsev + src_row);
     }

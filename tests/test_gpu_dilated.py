@@ -75,3 +75,31 @@ def test_dilated_streaming_decode_every_step(dtype, d, w, s, r):
     for t in range(T):
         compare(f"dilated decode t={t}", outs[t], o_ref[:, :, t], dtype)
         assert np.abs(lses[t].double().numpy() - l_ref[:, :, t]).max() < LSE_ABS
+
+
+@pytest.mark.parametrize("B,H,L,d,w,s,r,C,dtype", [
+    (1, 2, 700, 128, 256, 4, 2, 128, torch.bfloat16),
+    (2, 1, 600, 128, 100, 0, 3, 90, torch.bfloat16),
+    (16, 1, 300, 128, 64, 4, 2, 64, torch.bfloat16),   # 32 virtual heads: two row groups
+    (1, 2, 130, 16, 16, 4, 3, 20, torch.float32),
+])
+def test_chunked_dilated_prefill_rows_and_caches(B, H, L, d, w, s, r, C, dtype):
+    # the rows equal the dilated definition, and the per-class caches end as L streaming writes leave them
+    swa = require_gpu()
+    q, k, v = swa_inputs.prefill_inputs(B, H, L, d, 5000 + L + r, dtype, "cpu", sink_boost=True)
+    qg, kg, vg = q.cuda(), k.cuda(), v.cuda()
+    kc = torch.full((r, B, H, w, d), float("nan"), dtype=dtype, device="cuda")
+    vc = torch.full_like(kc, float("nan"))
+    lse = torch.empty((B, H, L), dtype=torch.float32, device="cuda")
+    o = swa.swa_sink_prefill_chunked_dilated(qg, kg, vg, s, r, C, kc, vc, lse=lse)
+    assert swa.swa_device_status() == swa.SWA_OK, swa.last_error()
+    o_ref, l_ref = oracle.prefill_dilated(q, k, v, w, s, r, 1.0 / math.sqrt(d))
+    compare(f"chunked dilated {B, H, L, w, s, r, C}", o.cpu(), o_ref, dtype)
+    assert np.abs(lse.cpu().double().numpy() - l_ref).max() < LSE_ABS
+    kc2 = torch.full_like(kc, float("nan"))
+    vc2 = torch.full_like(vc, float("nan"))
+    for t in range(L):
+        swa.swa_sink_dilated_cache_write(kc2, vc2, kg[:, :, t].contiguous(), vg[:, :, t].contiguous(), s, r, t)
+    iv = torch.int16 if dtype == torch.bfloat16 else torch.int32
+    assert torch.equal(kc.view(iv), kc2.view(iv))
+    assert torch.equal(vc.view(iv), vc2.view(iv))
