@@ -55,3 +55,13 @@ def test_banded_flop_accounting():
         assert bench.banded_pairs(L, w, pos0) == sum(min(t + 1, w) for t in range(pos0, pos0 + L))
     assert bench.banded_flops(1, 32, 8192, 128, 1024) == 4 * 32 * 128 * 7864832
     assert bench.banded_flops(2, 32, 32768, 128, 4096) == 4 * 64 * 128 * 125831168
+
+
+def test_dilated_flop_accounting():
+    import bench
+    import oracle
+    # 4 d per pair of the dilated key sets, against the oracle's brute-force membership
+    for L, w, s, r in [(60, 9, 3, 4), (41, 6, 2, 3), (30, 7, 0, 2), (25, 5, 4, 1), (12, 30, 4, 5)]:
+        pairs = sum(oracle.is_key_dilated(t, i, w, s, r) for t in range(L) for i in range(t + 1))
+        assert bench.dilated_flops(2, 3, L, 16, w, s, r) == 4.0 * 2 * 3 * 16 * pairs
+    assert bench.dilated_flops(1, 2, 50, 128, 10, 2, 1) == bench.banded_flops(1, 2, 50, 128, 10)
