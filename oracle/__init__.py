@@ -18,6 +18,9 @@ attention) and eq attn-fixed-softmax-sink of "滑窗与固定稀疏" (row normal
 
 ``rope``, ``decode_rope`` and ``prefill_rope`` state the streaming decode and the prefill with
 positions re-assigned inside the cache and rotary embedding (StreamingLLM section of "滑窗与固定稀疏").
+``is_key_blocksparse`` and ``prefill_blocksparse`` state the BigBird-style union (window, global
+tokens inside the sequence, given random key blocks) in causal form with sinks: an oracle ahead of its GPU
+path.
 ``is_key_dilated`` and ``prefill_dilated`` state the dilated window with sinks (the dilated sliding
 window of "滑窗与固定稀疏", glossary and Longformer section: attended positions skip r - 1 tokens).
 
@@ -250,6 +253,45 @@ def prefill_dilated(q, k, v, w: int, s: int, r: int, scale: float, rows=None):
     lse = np.empty((B * H, len(rows)))
     for j, t in enumerate(rows):
         members = np.array([i for i in range(t + 1) if is_key_dilated(t, i, w, s, r)], dtype=np.int64)
+        x = np.einsum("hd,hnd->hn", qf[:, t], kf[:, members]) * scale
+        mx = x.max(axis=1, keepdims=True)
+        e = np.exp(x - mx)
+        den = e.sum(axis=1)
+        o[:, j] = np.einsum("hn,hnd->hd", e, vf[:, members]) / den[:, None]
+        lse[:, j] = mx[:, 0] + np.log(den)
+    return o.reshape(B, H, len(rows), d), lse.reshape(B, H, len(rows))
+
+
+def is_key_blocksparse(t: int, i: int, w: int, s: int, globals_=(), block: int = 1, rand_blocks=None) -> bool:
+    """Membership in the BigBird-style key set of query t (the union of local window, global and random
+    connections of the fixed-sparsity page, eq attn-fixed-bigbird, with global tokens placed inside the
+    sequence (ITC)), in causal form with the sinks: i <= t and one of
+      i < s (sink), i >= t - m + 1 (window), i a global position, t a global position (a global query sees
+      every earlier key), or key block i // block in rand_blocks[t // block] (the query block's random key
+      blocks; the random choice is an input)."""
+    m = w - s
+    if i < 0 or i > t:
+        return False
+    if i < s or i >= t - m + 1 or i in globals_ or t in globals_:
+        return True
+    return rand_blocks is not None and (i // block) in rand_blocks.get(t // block, ())
+
+
+def prefill_blocksparse(q, k, v, w: int, s: int, scale: float, globals_=(), block: int = 1, rand_blocks=None,
+                        rows=None):
+    """Whole-sequence prefill over the key sets of ``is_key_blocksparse`` (fp64, numpy per row).
+    q, k, v: [B, H, L, d]; globals_: positions of the global tokens; rand_blocks: {query block: key blocks}.
+    Returns (o [B, H, len(rows), d], lse [B, H, len(rows)])."""
+    q, k, v = _f64(q), _f64(k), _f64(v)
+    B, H, L, d = q.shape
+    rows = list(range(L)) if rows is None else [int(t) for t in rows]
+    g = set(int(x) for x in globals_)
+    qf, kf, vf = q.reshape(B * H, L, d), k.reshape(B * H, L, d), v.reshape(B * H, L, d)
+    o = np.empty((B * H, len(rows), d))
+    lse = np.empty((B * H, len(rows)))
+    for j, t in enumerate(rows):
+        members = np.array([i for i in range(t + 1) if is_key_blocksparse(t, i, w, s, g, block, rand_blocks)],
+                           dtype=np.int64)
         x = np.einsum("hd,hnd->hn", qf[:, t], kf[:, members]) * scale
         mx = x.max(axis=1, keepdims=True)
         e = np.exp(x - mx)

@@ -539,3 +539,42 @@ def test_dilated_class_caches_hold_the_dilated_key_set(w, s, r):
         orig = {int(x) if x < s else p0 + (int(x) - s) * r for x in held if x >= 0}
         want = {i for i in range(t + 1) if oracle.is_key_dilated(t, i, w, s, r)}
         assert orig == want, (w, s, r, t)
+
+
+# ------------------------------------------------------------------ BigBird-style union (oracle ahead of its GPU path)
+def test_blocksparse_mask_matches_hand_derived_golden():
+    path = os.path.join(GOLDEN, "blocksparse_mask_L12_w3_s1_g5_b4.txt")
+    rows = [l.strip() for l in open(path) if l.strip() and not l.startswith("#")]
+    for t in range(12):
+        for i in range(12):
+            assert (rows[t][i] == "1") == oracle.is_key_blocksparse(t, i, 3, 1, {5}, 4, {2: [0]}), (t, i)
+
+
+def test_blocksparse_without_globals_or_random_blocks_is_the_plain_oracle():
+    rng = np.random.default_rng(23)
+    q, k, v = (rng.standard_normal((1, 2, 40, 16)) for _ in range(3))
+    o, lse = oracle.prefill_blocksparse(q, k, v, 9, 3, 0.3)
+    o_ref, l_ref = oracle.prefill(q, k, v, 9, 3, 0.3)
+    np.testing.assert_allclose(o, o_ref, atol=1e-12)
+    np.testing.assert_allclose(lse, l_ref, atol=1e-12)
+
+
+def test_blocksparse_every_position_global_is_full_causal_attention():
+    rng = np.random.default_rng(24)
+    L, d = 20, 8
+    q, k, v = (rng.standard_normal((1, 1, L, d)) for _ in range(3))
+    o, lse = oracle.prefill_blocksparse(q, k, v, 3, 1, 0.5, globals_=range(L))
+    x = np.einsum("id,jd->ij", q[0, 0], k[0, 0]) * 0.5
+    x = np.where(np.tril(np.ones((L, L), dtype=bool)), x, -np.inf)
+    np.testing.assert_allclose(o[0, 0], scipy.special.softmax(x, axis=1) @ v[0, 0], atol=1e-12)
+    np.testing.assert_allclose(lse[0, 0], scipy.special.logsumexp(x, axis=1), atol=1e-12)
+
+
+def test_blocksparse_random_blocks_add_whole_earlier_blocks():
+    # with w = 1, s = 0 a row attends itself and exactly the causal part of its random key blocks
+    block = 4
+    rand = {2: [0], 3: [1, 3], 1: [1]}
+    for t in range(16):
+        want = {t} | {i for kb in rand.get(t // block, ()) for i in range(kb * block, kb * block + block) if i <= t}
+        got = {i for i in range(t + 1) if oracle.is_key_blocksparse(t, i, 1, 0, (), block, rand)}
+        assert got == want, t
