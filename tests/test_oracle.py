@@ -578,3 +578,24 @@ def test_blocksparse_random_blocks_add_whole_earlier_blocks():
         want = {t} | {i for kb in rand.get(t // block, ()) for i in range(kb * block, kb * block + block) if i <= t}
         got = {i for i in range(t + 1) if oracle.is_key_blocksparse(t, i, 1, 0, (), block, rand)}
         assert got == want, t
+
+
+def test_rope_and_dilated_single_key_windows_return_v():
+    # w = 1, s = 0: every row attends only itself, so o = v and lse = scale q.k of the rotated pair
+    # (RoPE: a key at the query's own position has rotation distance 0, so lse = scale q.k)
+    rng = np.random.default_rng(25)
+    q, k, v = (rng.standard_normal((1, 2, 15, 8)) for _ in range(3))
+    o, lse = oracle.prefill_rope(q, k, v, 1, 0, 0.3)
+    np.testing.assert_allclose(o, v, atol=1e-12)
+    np.testing.assert_allclose(lse, 0.3 * np.einsum("bhld,bhld->bhl", q, k), atol=1e-12)
+    for r in (1, 3, 100):
+        o, lse = oracle.prefill_dilated(q, k, v, 1, 0, r, 0.3)
+        np.testing.assert_allclose(o, v, atol=1e-12)
+
+
+def test_dilation_past_the_sequence_leaves_sinks_and_self():
+    # r >= L: the window holds only t itself, so row t attends the sinks and t
+    L, w, s = 20, 5, 2
+    for t in range(L):
+        got = {i for i in range(t + 1) if oracle.is_key_dilated(t, i, w, s, L + 3)}
+        assert got == set(range(min(s, t + 1))) | {t}
