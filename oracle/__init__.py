@@ -18,6 +18,8 @@ attention) and eq attn-fixed-softmax-sink of "滑窗与固定稀疏" (row normal
 
 ``rope``, ``decode_rope`` and ``prefill_rope`` state the streaming decode and the prefill with
 positions re-assigned inside the cache and rotary embedding (StreamingLLM section of "滑窗与固定稀疏").
+``hedgehog`` and ``hybrid_linear`` state the SWA + linear-attention hybrid (a stated reading of the
+combination; an oracle ahead of its GPU path).
 ``is_key_blocksparse`` and ``prefill_blocksparse`` state the BigBird-style union (window, global
 tokens inside the sequence, given random key blocks) in causal form with sinks: an oracle ahead of its GPU
 path.
@@ -299,6 +301,42 @@ def prefill_blocksparse(q, k, v, w: int, s: int, scale: float, globals_=(), bloc
         o[:, j] = np.einsum("hn,hnd->hd", e, vf[:, members]) / den[:, None]
         lse[:, j] = mx[:, 0] + np.log(den)
     return o.reshape(B, H, len(rows), d), lse.reshape(B, H, len(rows))
+
+
+def hedgehog(x, wf) -> np.ndarray:
+    """The Hedgehog feature map of the linear-attention section of the hyper.ai summary of 2608.28444:
+    phi(x) = (exp(f(x)), exp(-f(x))) with f(x) = x wf a linear projection from d to d/2 (wf: [d, d/2],
+    a given matrix -- the learned one needs weights).  x: [..., d] -> [..., d]."""
+    f = np.asarray(x, dtype=np.float64) @ np.asarray(wf, dtype=np.float64)
+    return np.concatenate([np.exp(f), np.exp(-f)], axis=-1)
+
+
+def hybrid_linear(q, k, v, w: int, s: int, scale: float, wf):
+    """SWA with sinks plus a linear-attention branch for the keys that left the window (the hybrid of
+    the hyper.ai summary of 2608.28444: the SWA branch keeps local detail, the linear branch aggregates
+    the rest).  Reading, as in the LoLCATs model that summary discusses: one shared normaliser,
+        o_t = (sum_{i in K(t)} e^{x_i} v_i + phi(q_t) s_t) / (sum_{i in K(t)} e^{x_i} + phi(q_t) z_t),
+    x_i = scale q_t.k_i, K(t) the sinks + window, and (s_t, z_t) the running state of the keys outside it,
+    updated by the page's recurrence s <- s + phi(k)^T v, z <- z + phi(k)^T as each key leaves the window
+    (key i leaves at step i + m; the sinks never do).  q, k, v: [nh, L, d]; returns o [nh, L, d] (fp64)."""
+    q, k, v = _f64(q), _f64(k), _f64(v)
+    nh, L, d = q.shape
+    m = w - s
+    pq, pk = hedgehog(q, wf), hedgehog(k, wf)
+    S = np.zeros((nh, d, d))
+    z = np.zeros((nh, d))
+    o = np.empty((nh, L, d))
+    for t in range(L):
+        i_out = t - m  # the key that leaves the window at step t (sinks excepted)
+        if i_out >= s:
+            S += np.einsum("hi,hj->hij", pk[:, i_out], v[:, i_out])
+            z += pk[:, i_out]
+        members = np.array([i for i in range(t + 1) if is_key(t, i, w, s)], dtype=np.int64)
+        e = np.exp(np.einsum("hd,hnd->hn", q[:, t], k[:, members]) * scale)
+        num = np.einsum("hn,hnd->hd", e, v[:, members]) + np.einsum("hi,hij->hj", pq[:, t], S)
+        den = e.sum(axis=1) + np.einsum("hi,hi->h", pq[:, t], z)
+        o[:, t] = num / den[:, None]
+    return o
 
 
 def cache_replay(w: int, s: int, npos: int) -> np.ndarray:

@@ -599,3 +599,64 @@ def test_dilation_past_the_sequence_leaves_sinks_and_self():
     for t in range(L):
         got = {i for i in range(t + 1) if oracle.is_key_dilated(t, i, w, s, L + 3)}
         assert got == set(range(min(s, t + 1))) | {t}
+
+
+# ------------------------------------------------------------------ SWA + linear-attention hybrid (oracle ahead of its GPU path)
+def _hybrid_direct(q, k, v, w, s, scale, wf):
+    # the same quantity summed directly over the keys outside K(t) (no running state)
+    nh, L, d = q.shape
+    pq, pk = oracle.hedgehog(q, wf), oracle.hedgehog(k, wf)
+    o = np.empty_like(q)
+    for t in range(L):
+        inside = [i for i in range(t + 1) if oracle.is_key(t, i, w, s)]
+        outside = [i for i in range(t + 1) if not oracle.is_key(t, i, w, s)]
+        e = np.exp(np.einsum("hd,hnd->hn", q[:, t], k[:, inside]) * scale)
+        a = np.einsum("hd,hnd->hn", pq[:, t], pk[:, outside]) if outside else np.zeros((nh, 0))
+        num = np.einsum("hn,hnd->hd", e, v[:, inside]) + (np.einsum("hn,hnd->hd", a, v[:, outside]) if outside else 0)
+        o[:, t] = num / (e.sum(axis=1) + a.sum(axis=1))[:, None]
+    return o
+
+
+def test_hedgehog_feature_map():
+    # phi(x) = (exp(x W), exp(-x W)): positive, so phi(q).phi(k) > 0 (the monotone, positive kernel the page
+    # asks for); with W = 0 it is all ones and phi(q).phi(k) = d
+    rng = np.random.default_rng(26)
+    x, y = rng.standard_normal((5, 8)), rng.standard_normal((7, 8))
+    wf = rng.standard_normal((8, 4)) * 0.3
+    px, py = oracle.hedgehog(x, wf), oracle.hedgehog(y, wf)
+    assert px.shape == (5, 8) and (px > 0).all() and (px @ py.T > 0).all()
+    np.testing.assert_allclose(px[:, :4] * px[:, 4:], 1.0, atol=1e-12)  # exp(f) * exp(-f) = 1
+    np.testing.assert_allclose(oracle.hedgehog(x, np.zeros((8, 4))) @ oracle.hedgehog(y, np.zeros((8, 4))).T, 8.0)
+
+
+def test_hybrid_running_state_equals_the_direct_sum():
+    # the page's recurrence (s_t, z_t), applied as keys leave the window, against direct summation
+    rng = np.random.default_rng(27)
+    q, k, v = (rng.standard_normal((2, 40, 8)) for _ in range(3))
+    wf = rng.standard_normal((8, 4)) * 0.2
+    for w, s in [(6, 2), (5, 0), (9, 4)]:
+        np.testing.assert_allclose(oracle.hybrid_linear(q, k, v, w, s, 0.35, wf),
+                                   _hybrid_direct(q, k, v, w, s, 0.35, wf), atol=1e-10)
+
+
+def test_hybrid_without_evicted_keys_is_softmax_attention():
+    # w >= L: no key ever leaves the window, so the linear branch is empty
+    rng = np.random.default_rng(28)
+    q, k, v = (rng.standard_normal((1, 2, 30, 8)) for _ in range(3))
+    o = oracle.hybrid_linear(q[0], k[0], v[0], 40, 3, 0.3, rng.standard_normal((8, 4)))
+    o_ref, _ = oracle.prefill(q, k, v, 40, 3, 0.3)
+    np.testing.assert_allclose(o, o_ref[0], atol=1e-12)
+
+
+def test_hybrid_with_a_flat_feature_map_in_closed_form():
+    # W = 0: every evicted key weighs d, so o = (sum_K e^x v + d sum_R v) / (sum_K e^x + d |R|)
+    rng = np.random.default_rng(29)
+    L, d, w, s = 25, 8, 6, 2
+    q, k, v = (rng.standard_normal((1, L, d)) for _ in range(3))
+    o = oracle.hybrid_linear(q, k, v, w, s, 0.4, np.zeros((d, d // 2)))
+    for t in range(L):
+        K = [i for i in range(t + 1) if oracle.is_key(t, i, w, s)]
+        R = [i for i in range(t + 1) if i not in K]
+        e = np.exp(0.4 * q[0, t] @ k[0, K].T)
+        want = (e @ v[0, K] + d * v[0, R].sum(axis=0)) / (e.sum() + d * len(R))
+        np.testing.assert_allclose(o[0, t], want, atol=1e-12)
