@@ -16,6 +16,7 @@ slowest rank's time.
 from __future__ import annotations
 
 import argparse
+import ctypes
 import hashlib
 import json
 import math
@@ -24,6 +25,7 @@ import statistics
 import subprocess
 import sys
 import tempfile
+import threading
 import time
 
 ROOT = os.path.dirname(os.path.abspath(__file__))
@@ -160,6 +162,74 @@ class ClockSampler:
                 "reasons": reasons, "samples": len(use), "in_timed_region": bool(inside)}
 
 
+class NvmlWindowSampler:
+    """Reads the SM clock and the active clock-event reasons of one GPU through NVML (read only; nothing is
+    set) every ~0.5 ms from a background thread while a timed region runs, so that even a region of a few
+    milliseconds gets its own clock samples.  NVML is reached through ctypes (libnvidia-ml.so.1)."""
+    # clock-event reason bits of NVML
+    REASONS = {0x4: "sw_power_cap", 0x8: "hw_slowdown", 0x20: "sw_thermal_slowdown", 0x40: "hw_thermal_slowdown",
+               0x80: "hw_power_brake_slowdown"}
+
+    def __init__(self, uuid: str | None):
+        self.ok = False
+        self.samples = []
+        try:
+            self.nv = ctypes.CDLL("libnvidia-ml.so.1")
+            if self.nv.nvmlInit_v2() != 0:
+                return
+            self.h = ctypes.c_void_p()
+            if uuid:
+                rc = self.nv.nvmlDeviceGetHandleByUUID(uuid.encode(), ctypes.byref(self.h))
+            else:
+                rc = self.nv.nvmlDeviceGetHandleByIndex_v2(0, ctypes.byref(self.h))
+            if rc != 0:
+                return
+            self.reasons_fn = getattr(self.nv, "nvmlDeviceGetCurrentClocksEventReasons", None) or \
+                getattr(self.nv, "nvmlDeviceGetCurrentClocksThrottleReasons")
+            self.ok = True
+        except (OSError, AttributeError):
+            self.ok = False
+
+    def _read(self):
+        clk = ctypes.c_uint()
+        rs = ctypes.c_ulonglong()
+        if self.nv.nvmlDeviceGetClockInfo(self.h, 1, ctypes.byref(clk)) != 0:  # 1 = NVML_CLOCK_SM
+            return None
+        self.reasons_fn(self.h, ctypes.byref(rs))
+        return clk.value, rs.value
+
+    def __enter__(self):
+        self._stop = threading.Event()
+        self.samples = []
+
+        def loop():
+            while not self._stop.is_set():
+                r = self._read()
+                if r is not None:
+                    self.samples.append(r)
+                time.sleep(0.0005)
+
+        if self.ok:
+            self._thr = threading.Thread(target=loop, daemon=True)
+            self._thr.start()
+        return self
+
+    def __exit__(self, *exc):
+        if self.ok:
+            self._stop.set()
+            self._thr.join()
+
+    def summary(self):
+        if not self.samples:
+            return {"samples": 0}
+        bits = 0
+        for _, r in self.samples:
+            bits |= r
+        return {"samples": len(self.samples), "sm_mhz": statistics.median(c for c, _ in self.samples),
+                "sm_mhz_min": min(c for c, _ in self.samples),
+                "reasons": sorted(v for k, v in self.REASONS.items() if bits & k)}
+
+
 # ------------------------------------------------------------------------------------------ GPU legs
 def _events():
     import torch
@@ -172,21 +242,24 @@ def _check_status(swa):
         raise RuntimeError(f"device status {rc}: {swa.last_error()}")
 
 
-def time_loop(step, steps, warmup, world, clocks):
-    """W untimed calls, then K calls bracketed by barrier + synchronize; returns max-over-ranks seconds."""
+def time_loop(step, steps, warmup, world, clocks, window=None):
+    """W untimed calls, then K calls bracketed by barrier + synchronize; returns max-over-ranks seconds.
+    ``window``: an NvmlWindowSampler that samples the clocks inside the timed region itself."""
+    import contextlib
     import torch
     for _ in range(warmup):
         step()
     torch.cuda.synchronize()
     barrier(world)
     e0, e1 = _events()
-    t0 = time.time()
-    e0.record()
-    for _ in range(steps):
-        step()
-    e1.record()
-    torch.cuda.synchronize()
-    t1 = time.time()
+    with (window if window is not None else contextlib.nullcontext()):
+        t0 = time.time()
+        e0.record()
+        for _ in range(steps):
+            step()
+        e1.record()
+        torch.cuda.synchronize()
+        t1 = time.time()
     barrier(world)
     if clocks is not None:
         clocks.mark(t0, t1)
@@ -204,7 +277,7 @@ def dilated_flops(B, H, L, d, w, s, r):
     return 4.0 * B * H * d * pairs
 
 
-def prefill_leg(swa, wl, steps, warmup, world, rank, clocks, e2e=False, rope=False, dilation=0):
+def prefill_leg(swa, wl, steps, warmup, world, rank, clocks, e2e=False, rope=False, dilation=0, window=None):
     """Prefill steps; with ``rope`` the RoPE prefill at the positions inside the cache (base 10000): a
     rotation pass over q and k, then the tensor-core prefill on the rotated rows (2 launches a step)."""
     import torch
@@ -237,7 +310,7 @@ def prefill_leg(swa, wl, steps, warmup, world, rank, clocks, e2e=False, rope=Fal
         if rc:
             raise RuntimeError(swa.last_error())
 
-    t = time_loop(step, steps, warmup, world, clocks)
+    t = time_loop(step, steps, warmup, world, clocks, window)
     _check_status(swa)
     flops = dilated_flops(B, H, L, d, w, s, dilation) if dilation else banded_flops(B, H, L, d, w)
     res = {"flops_per_step": flops, "seconds": t, "steps": steps, "tflops": flops * steps / t / 1e12,
@@ -503,7 +576,9 @@ def main():
     clocks = ClockSampler(uuid)
 
     wl = swa_inputs.WORKLOADS[PRIMARY]
-    prim = prefill_leg(swa, wl, args.steps, args.warmup, world, rank, clocks, e2e=True) if "primary" in legs else None
+    prim_window = NvmlWindowSampler(uuid)
+    prim = prefill_leg(swa, wl, args.steps, args.warmup, world, rank, clocks, e2e=True,
+                       window=prim_window) if "primary" in legs else None
     secondary = {}
     if "mistral" in legs:
         for name in ("prefill_mistral_B2_L32768_w4096_s0", "prefill_mistral_B2_L32768_w4096_s4"):
@@ -595,7 +670,10 @@ def main():
                 "d2h_bytes_per_step": prim["e2e"]["d2h_bytes_per_step"]},
         "gpu_launches": prim["launches"],
         "clocks": {"sm_mhz": ck["sm_mhz"], "sm_max_mhz": ck["sm_max_mhz"], "reasons": ck["reasons"],
-                   "samples": ck["samples"]},
+                   "samples": ck["samples"],
+                   # NVML read every ~0.5 ms inside the primary timed region itself (nvidia-smi's 200 ms
+                   # samples above cover all timed regions of the run)
+                   "primary_window": prim_window.summary()},
         "secondary": secondary,
     }
     if world == 1:

@@ -228,7 +228,9 @@ int swa_sink_decode_step(const void *q, const void *k_cache, const void *v_cache
  *   results.  A shape whose split-K scratch (swa_sink_decode_workspace_size) exceeds 2 MiB is refused with
  *   SWA_ERR_UNSUPPORTED and a message; nothing is launched.
  *   The first call on a device looks up the array's device address (cudaGetSymbolAddress) with that
- *   device current; make that first call before any stream capture.
+ *   device current and keeps it for the life of the process; make that first call before any stream
+ *   capture, and do not keep using the library on a device after cudaDeviceReset (the kept address
+ *   would then be stale).
  *   Every call uses the same array and overwrites what the previous call left there (nothing in it needs
  *   to start at zero).  Calls that run at the same time on the GPU -- on different streams, or from
  *   several host threads -- overwrite each other's partials: serialise them.

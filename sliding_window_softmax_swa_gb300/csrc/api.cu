@@ -496,12 +496,10 @@ extern "C" int swa_sink_dilated_cache_write(void *k_cache, void *v_cache, const 
     const cudaStream_t st = static_cast<cudaStream_t>(stream);
     int c = 0;
     const int64_t local = dilated_local(t, s, r, &c);
-    for (int cc = (t < s ? 0 : c); cc < (t < s ? r : c + 1); ++cc) {  // a sink goes into every class's cache
-        rc = launch_kv_write(static_cast<char *>(k_cache) + cc * slab, static_cast<char *>(v_cache) + cc * slab, k_new,
-                             v_new, B * H, d, w, s, local, 1, 1, es, st);
-        if (rc) return rc;
-    }
-    return SWA_OK;
+    // a sink goes into every class's cache (one launch over the r caches), any other position into its own
+    const size_t first = t < s ? 0 : static_cast<size_t>(c) * slab;
+    return launch_kv_write_classes(static_cast<char *>(k_cache) + first, static_cast<char *>(v_cache) + first, k_new,
+                                   v_new, B * H, d, w, s, local, 1, 1, es, t < s ? r : 1, st);
 }
 
 extern "C" int swa_sink_decode_step_dilated(const void *q, const void *k_cache, const void *v_cache, void *o,

@@ -60,6 +60,10 @@ int launch_rope_prep(const void *q, const void *k, void *qr, void *qs, void *kr,
 // v_new == nullptr only the keys are written.
 int launch_kv_write(void *k_cache, void *v_cache, const void *k_new, const void *v_new, int BH, int d, int w,
                     int s, int64_t pos0, int64_t n, int64_t src_stride, int esize, cudaStream_t stream);
+// The same rows into nclass caches of [BH, w, d] that lie one after the other (one launch).
+int launch_kv_write_classes(void *k_cache, void *v_cache, const void *k_new, const void *v_new, int BH, int d, int w,
+                            int s, int64_t pos0, int64_t n, int64_t src_stride, int esize, int nclass,
+                            cudaStream_t stream);
 
 struct DecodeArgs {
     const void *q, *k_cache, *v_cache;

@@ -120,7 +120,8 @@ def test_zero_query_gives_mean_over_keyset():
 
 
 def test_mask_picture_n32():
-    # The N = 32 StreamingLLM picture (recent band + sink bar on the left), stored as text.
+    # The N = 32 StreamingLLM picture (recent band + sink bar on the left), drawn from the figure's
+    # description by tests/golden/make_golden.py without the oracle, stored as text.
     g = open(os.path.join(GOLDEN, "streaming_mask_n32_w8_s4.txt")).read().split("\n")
     rows = [r for r in g if r and set(r) <= {"#", "."}]
     pic = np.array([[1 if ch == "#" else 0 for ch in r] for r in rows], dtype=np.uint8)
