@@ -63,6 +63,11 @@ unsigned long long *device_timeout_info() {
     return ptrs[dev];
 }
 
+int launch_prefill_bf16_tc(const PrefillArgs &a) {
+    if (a.q_sink != nullptr || a.d == 64) return launch_prefill_bf16_tc_sub(a);
+    return launch_prefill_bf16_tc_plain(a);
+}
+
 EncodeTiledFn encode_tiled_fn() {
     static std::once_flag once;
     static EncodeTiledFn fn = nullptr;
@@ -129,7 +134,7 @@ static int prefill_impl(const void *q, const void *k, const void *v, void *o, fl
     if (L == 0) return SWA_OK;
     PrefillArgs a{q, k, v, o, lse, k_cache, v_cache, pos0, B * H, L, d, w, s, scale, seq_stride, stream};
     if (dtype == SWA_BF16) {
-        if (d != 128) return fail(SWA_ERR_UNSUPPORTED, "bf16 prefill needs d = 128 (got %d)", d);
+        if (d != 64 && d != 128) return fail(SWA_ERR_UNSUPPORTED, "bf16 prefill needs d = 64 or 128 (got %d)", d);
         return launch_prefill_bf16_tc(a);
     }
     return launch_prefill_f32(a);
@@ -200,11 +205,14 @@ static ChunkStreams *chunk_streams() {
     return per_dev[dev];
 }
 
-// RoPE mode of the chunk loop: q and k passed to it are the rotated rows; these are the rest.
+// RoPE mode of the chunk loop: q and k passed to it are the rotated rows (hi parts); these are the rest.
 struct ChunkRope {
-    const void *q_sink;  // [BH, L, d] query rows rotated for the sink keys
-    const void *k_raw;   // [BH, L, d] unrotated keys: they go into the caller's cache
-    void *kc_rot;        // [BH, w, d] scratch cache of rotated keys, read by the prefill for positions < pos0
+    const void *q_lo;                  // [BH, L, d] lo parts of the rotated query rows
+    const void *q_sink, *q_sink_lo;    // [BH, L, d] query rows rotated for the sink keys (hi, lo)
+    const void *k_lo;                  // [BH, L, d] lo parts of the rotated keys
+    const void *k_raw;                 // [BH, L, d] unrotated keys: they go into the caller's cache
+    void *kc_rot, *kc_rot_lo;          // [BH, w, d] scratch cache of rotated keys (hi, lo), read by the
+                                       // prefill for positions < pos0
 };
 
 // The chunk loop of chunked prefill (validated arguments, L > 0): L rows per (b, h), consecutive (b, h)
@@ -236,6 +244,7 @@ static int chunk_loop(const void *q, const void *k, const void *v, void *o, floa
         void *kcg = static_cast<char *>(k_cache) + cache_off;
         void *vcg = static_cast<char *>(v_cache) + cache_off;
         void *krg = rp ? static_cast<char *>(rp->kc_rot) + cache_off : nullptr;
+        void *krg_lo = rp ? static_cast<char *>(rp->kc_rot_lo) + cache_off : nullptr;
         for (int64_t c0 = 0; c0 < L; c0 += chunk) {
             const int64_t n = (L - c0 < chunk) ? (L - c0) : chunk;
             const size_t off = seq_off + static_cast<size_t>(c0) * row_bytes;
@@ -251,13 +260,18 @@ static int chunk_loop(const void *q, const void *k, const void *v, void *o, floa
                 rc = launch_kv_write(kcg, vcg, kc, vc, r1 - r0, d, w, s, c0, n, stride, es, gs);
                 if (rc) return rc;
             } else {
-                // rotated rows against the rotated cache; then the chunk's rotated keys into the scratch
-                // cache, its unrotated keys and its values into the caller's
+                // rotated rows against the rotated cache; then the chunk's rotated keys (hi and lo) into the
+                // scratch caches, its unrotated keys and its values into the caller's
                 PrefillArgs a{qc, kc, vc, oc, lc, krg, vcg, c0, r1 - r0, n, d, w, s, scale, stride, gs};
                 a.q_sink = static_cast<const char *>(rp->q_sink) + off;
+                a.q_sink_lo = static_cast<const char *>(rp->q_sink_lo) + off;
+                a.q_lo = static_cast<const char *>(rp->q_lo) + off;
+                a.k_lo = static_cast<const char *>(rp->k_lo) + off;
+                a.k_cache_lo = krg_lo;
                 rc = launch_prefill_bf16_tc(a);
                 if (rc) return rc;
-                rc = launch_kv_write(krg, nullptr, kc, nullptr, r1 - r0, d, w, s, c0, n, stride, es, gs);
+                rc = launch_kv_write(krg, krg_lo, kc, static_cast<const char *>(rp->k_lo) + off, r1 - r0, d, w, s, c0, n,
+                                     stride, es, gs);
                 if (rc) return rc;
                 rc = launch_kv_write(kcg, vcg, static_cast<const char *>(rp->k_raw) + off, vc, r1 - r0, d, w, s, c0,
                                      n, stride, es, gs);
@@ -292,7 +306,7 @@ extern "C" int swa_sink_prefill_chunked(const void *q, const void *k, const void
 
 extern "C" size_t swa_sink_prefill_chunked_rope_workspace_size(int B, int H, int64_t L, int d, int w) {
     if (B < 1 || H < 1 || L < 0 || d != 128 || w < 1) return 0;
-    return rope_prefill_workspace_bytes(B * H, L, d) + static_cast<size_t>(B) * H * w * d * 2;
+    return rope_prefill_workspace_bytes(B * H, L, d) + 2 * static_cast<size_t>(B) * H * w * d * 2;
 }
 
 extern "C" int swa_sink_prefill_chunked_rope(const void *q, const void *k, const void *v, void *o, float *lse,
@@ -319,13 +333,14 @@ extern "C" int swa_sink_prefill_chunked_rope(const void *q, const void *k, const
         return fail(SWA_ERR_INVALID, "workspace must be non-null and 256-byte aligned");
     const cudaStream_t st = static_cast<cudaStream_t>(stream);
     char *ws = static_cast<char *>(workspace);
-    const size_t one = rope_prefill_workspace_bytes(B * H, L, d) / 3;  // one [B, H, L, d] bf16 tensor
-    void *qr = ws, *qs = ws + one, *kr = ws + 2 * one, *kc_rot = ws + 3 * one;
+    const RopeParts rpt = rope_parts(ws, B * H, L, d);
+    char *kc_rot = ws + rope_prefill_workspace_bytes(B * H, L, d);
+    char *kc_rot_lo = kc_rot + static_cast<size_t>(B) * H * w * d * 2;
     // the rotations depend on absolute positions only, so one pass serves every chunk
-    rc = launch_rope_prep(q, k, qr, qs, kr, B * H, L, d, w, rope_base, st);
+    rc = launch_rope_prep(q, k, rpt, B * H, L, d, w, rope_base, st);
     if (rc) return rc;
-    const ChunkRope rp{qs, k, kc_rot};
-    return chunk_loop(qr, kr, v, o, lse, k_cache, v_cache, B, H, L, L, d, w, s, scale, chunk, dtype, st, &rp);
+    const ChunkRope rp{rpt.qr_lo, rpt.qs, rpt.qs_lo, rpt.kr_lo, k, kc_rot, kc_rot_lo};
+    return chunk_loop(rpt.qr, rpt.kr, v, o, lse, k_cache, v_cache, B, H, L, L, d, w, s, scale, chunk, dtype, st, &rp);
 }
 
 // Streams and events of the host-buffer prefill pipeline (copies in, compute, copies out), created once
@@ -710,13 +725,14 @@ extern "C" int swa_sink_prefill_rope(const void *q, const void *k, const void *v
     if (!workspace || (reinterpret_cast<uintptr_t>(workspace) & 255u))
         return fail(SWA_ERR_INVALID, "workspace must be non-null and 256-byte aligned");
     const cudaStream_t st = static_cast<cudaStream_t>(stream);
-    char *ws = static_cast<char *>(workspace);
-    const size_t one = need / 3;  // one [B, H, L, d] bf16 tensor; a multiple of 256 bytes
-    void *qr = ws, *qs = ws + one, *kr = ws + 2 * one;
-    rc = launch_rope_prep(q, k, qr, qs, kr, B * H, L, d, w, rope_base, st);
+    const RopeParts rpt = rope_parts(workspace, B * H, L, d);
+    rc = launch_rope_prep(q, k, rpt, B * H, L, d, w, rope_base, st);
     if (rc) return rc;
-    PrefillArgs a{qr, kr, v, o, lse, nullptr, nullptr, 0, B * H, L, d, w, s, scale, L, st};
-    a.q_sink = qs;
+    PrefillArgs a{rpt.qr, rpt.kr, v, o, lse, nullptr, nullptr, 0, B * H, L, d, w, s, scale, L, st};
+    a.q_sink = rpt.qs;
+    a.q_sink_lo = rpt.qs_lo;
+    a.q_lo = rpt.qr_lo;
+    a.k_lo = rpt.kr_lo;
     return launch_prefill_bf16_tc(a);
 }
 

@@ -17,10 +17,10 @@
 //   warp 10    per item: builds the key-tile list into one of two buffers, one item ahead, loads Q_0 and
 //              Q_1 as soon as the previous item's last QK product is done, and prefetches the next
 //              item's Q into L2;
-//   warp 8     TMA producer: K tiles into a 3-stage ring and V tiles into a 2-stage ring (128 rows x
+//   warp 8     TMA producer: K tiles into a 2-stage ring and V tiles into a 2-stage ring (128 rows x
 //              128 bf16 each, two 64-column boxes with the 128-byte swizzle), as one stream over all
 //              items of the CTA.  A K slot frees as soon as the QK products that read it complete, a V
-//              slot after its PV products, so K loads run up to three tiles ahead, also into the next
+//              slot after its PV products, so K loads run up to two tiles ahead, also into the next
 //              item;
 //   warp 9     MMA issuer (one thread).  Per key tile j: PV_0(j), QK_0(j+1), PV_1(j), QK_1(j+1), where
 //              QK_x(j) is S_x = Q_x K_j^T and PV_x(j) is O_x += P_x V_j with P_x (bf16) read by the MMA
@@ -839,13 +839,11 @@ static int sm_count() {
     return cached[dev];
 }
 
-int launch_prefill_bf16_tc(const PrefillArgs &a) {
+int launch_prefill_bf16_tc_plain(const PrefillArgs &a) {
     using namespace tc;
     if (a.d != HD) return fail(SWA_ERR_UNSUPPORTED, "tensor-core prefill needs d = %d", HD);
-    const bool rope = a.q_sink != nullptr;
-    if (rope && ((a.pos0 > 0 && a.pos0 < a.s) || a.s > BN))
-        return fail(SWA_ERR_UNSUPPORTED, "RoPE prefill needs pos0 = 0 or pos0 >= s, and s <= %d", BN);
-    if (max_tiles_bound(a.w, a.s) + (rope ? 1 : 0) > MAX_TILES)
+    if (a.q_sink) return fail(SWA_ERR_INVALID, "the RoPE prefill runs on the sub-tile kernel");
+    if (max_tiles_bound(a.w, a.s) > MAX_TILES)
         return fail(SWA_ERR_UNSUPPORTED, "window w=%d needs more than %d key tiles per query tile", a.w, MAX_TILES);
     if ((a.L + BM - 1) / BM * a.BH > 0x7FFFFFFF) return fail(SWA_ERR_UNSUPPORTED, "too many work items");
     if (!encode_tiled_fn()) return fail(SWA_ERR_CUDA, "cuTensorMapEncodeTiled is not available");
@@ -866,7 +864,7 @@ int launch_prefill_bf16_tc(const PrefillArgs &a) {
     }
     else
         okm = okm && encode_rows_map(&p.tm_kc, a.k, L, a.BH, st) && encode_rows_map(&p.tm_vc, a.v, L, a.BH, st);
-    okm = okm && encode_rows_map(&p.tm_qs, rope ? a.q_sink : a.q, L, a.BH, st);
+    okm = okm && encode_rows_map(&p.tm_qs, a.q, L, a.BH, st);
     if (!okm) return fail(SWA_ERR_INVALID, "cuTensorMapEncodeTiled rejected a tensor (alignment or size)");
     p.o = a.o;
     p.lse = a.lse;
@@ -882,7 +880,7 @@ int launch_prefill_bf16_tc(const PrefillArgs &a) {
     p.n_items = p.n_qpairs * a.BH;
     p.scale_log2 = a.scale * 1.4426950408889634f;
     p.timeout_us = kWaitTimeoutUs;
-    auto *kern = rope ? swa_prefill_tc_kernel<true> : swa_prefill_tc_kernel<false>;
+    auto *kern = swa_prefill_tc_kernel<false>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          static_cast<int>(SMEM_BYTES));
     if (e != cudaSuccess) return fail(SWA_ERR_CUDA, "prefill smem attribute: %s", cudaGetErrorString(e));
@@ -897,6 +895,7 @@ int launch_prefill_bf16_tc(const PrefillArgs &a) {
 }
 
 int prefill_tile_plan(int q0, int q1, int pos0, int w, int s, int rope, int *out, int max_tiles) {
+    if (rope) return prefill_tile_plan_sub(q0, q1, pos0, w, s, rope, out, max_tiles);
     tc::Tile tl[tc::MAX_TILES];
     const int n = tc::build_tiles(tl, q0, q1, pos0, s, w - s, w, rope != 0);
     tc::mark_tiles(tl, n, q0, q1, s, w - s);

@@ -6,14 +6,16 @@
 // at distance t - i, as plain RoPE does, but the sinks at distance min(t, w - 1) - i, because once the
 // cache is full the query sits at position w - 1.  So the tensor-core prefill runs on
 //     Qr = R(t) q_t,  Kr = R(i) k_i   (band tiles)   and   Qs = R(min(t, w - 1)) q_t   (the sink tile),
-// which this pass writes, bf16, into the caller's workspace.  R(a) rotates the half-split pair
-// (x_i, x_{i+d/2}) by a * base^(-2i/d): (x cos - y sin, x sin + y cos).
+// which this pass writes into the caller's workspace.  R(a) rotates the half-split pair (x_i, x_{i+d/2})
+// by a * base^(-2i/d): (x cos - y sin, x sin + y cos).  Each rotated value x (fp32) is written as two
+// bf16 numbers, hi = bf16(x) and lo = bf16(x - hi), so hi + lo holds x to about 2^-17 relative and the
+// prefill's three products hi hi + hi lo + lo hi give scores with the error of fp32 operands.
 //
 // Angles are reduced exactly for every position < 2^31: theta_i / (2 pi) is held as the 64-bit fraction
 // F_i = round(2^64 theta_i / (2 pi)) (host, double), and the fraction of a turn of a * theta_i is
 // (a F_i) mod 2^64, whose top 32 bits are a * F_hi + umulhi(a, F_lo).  The error is that of F_i, at most
-// a * 2^-65 turns; sin and cos are fp32.  The pass is HBM-bound: per row it reads q and k and writes three
-// rows (5 x 256 bytes at d = 128), 16 lanes per row, each lane holding both halves of its 4 pairs.
+// a * 2^-65 turns; sin and cos are fp32.  The pass is HBM-bound: per row it reads q and k and writes six
+// rows (8 x 256 bytes at d = 128), 16 lanes per row, each lane holding both halves of its 4 pairs.
 #include <cuda_bf16.h>
 
 #include <cmath>
@@ -50,24 +52,38 @@ __device__ __forceinline__ uint32_t pack2(float lo, float hi) {
     return *reinterpret_cast<const uint32_t *>(&h);
 }
 
-// Rotates the pairs (a[p], b[p]) by the angles (sn[p], c[p]) and writes the two halves of one row.
+// Rotates the pairs (a[p], b[p]) by the angles (sn[p], c[p]) and writes the two halves of one row as
+// (hi, lo) bf16 pairs.
 __device__ __forceinline__ void rotate_store(const float (&a)[4], const float (&b)[4], const float (&sn)[4],
-                                             const float (&c)[4], uint2 *dst_a, uint2 *dst_b) {
+                                             const float (&c)[4], uint2 *hi, uint2 *lo, int64_t ia, int64_t ib) {
     float x[4], y[4];
 #pragma unroll
     for (int p = 0; p < 4; ++p) {
         x[p] = fmaf(a[p], c[p], -b[p] * sn[p]);
         y[p] = fmaf(a[p], sn[p], b[p] * c[p]);
     }
-    *dst_a = make_uint2(pack2(x[0], x[1]), pack2(x[2], x[3]));
-    *dst_b = make_uint2(pack2(y[0], y[1]), pack2(y[2], y[3]));
+    uint32_t xh[2], yh[2], xl[2], yl[2];
+#pragma unroll
+    for (int p = 0; p < 2; ++p) {
+        xh[p] = pack2(x[2 * p], x[2 * p + 1]);
+        yh[p] = pack2(y[2 * p], y[2 * p + 1]);
+        // the rounding residues x - bf16(x), exact in fp32, rounded to bf16 in turn
+        xl[p] = pack2(x[2 * p] - __uint_as_float(xh[p] << 16), x[2 * p + 1] - __uint_as_float(xh[p] & 0xFFFF0000u));
+        yl[p] = pack2(y[2 * p] - __uint_as_float(yh[p] << 16), y[2 * p + 1] - __uint_as_float(yh[p] & 0xFFFF0000u));
+    }
+    hi[ia] = make_uint2(xh[0], xh[1]);
+    hi[ib] = make_uint2(yh[0], yh[1]);
+    lo[ia] = make_uint2(xl[0], xl[1]);
+    lo[ib] = make_uint2(yl[0], yl[1]);
 }
 
 // Rows of [BH, L, 128] bf16 viewed as 32 uint2 each: lane `sub` of a row holds elements 4 sub .. 4 sub + 3
 // (uint2 index sub) and their partners 64 + 4 sub .. (uint2 index 16 + sub).
+struct RopeOut {
+    uint2 *qr, *qr_lo, *qs, *qs_lo, *kr, *kr_lo;
+};
 __global__ void __launch_bounds__(256) rope_prep_kernel(const uint2 *__restrict__ q, const uint2 *__restrict__ k,
-                                                        uint2 *__restrict__ qr, uint2 *__restrict__ qs,
-                                                        uint2 *__restrict__ kr, int64_t rows, int64_t L, int w,
+                                                        const RopeOut out, int64_t rows, int64_t L, int w,
                                                         const __grid_constant__ RopePrep rp) {
     const int sub = threadIdx.x % kRopeLanes;
     uint2 f[kRopePpl];
@@ -95,21 +111,27 @@ __global__ void __launch_bounds__(256) rope_prep_kernel(const uint2 *__restrict_
         float sn[kRopePpl], c[kRopePpl];
 #pragma unroll
         for (int p = 0; p < kRopePpl; ++p) turn_sincos(static_cast<uint32_t>(t), f[p], sn[p], c[p]);
-        rotate_store(qa, qb, sn, c, qr + ia, qr + ib);
-        rotate_store(ka, kb, sn, c, kr + ia, kr + ib);
+        rotate_store(qa, qb, sn, c, out.qr, out.qr_lo, ia, ib);
+        rotate_store(ka, kb, sn, c, out.kr, out.kr_lo, ia, ib);
         if (t < w - 1)
-            rotate_store(qa, qb, sn, c, qs + ia, qs + ib);
+            rotate_store(qa, qb, sn, c, out.qs, out.qs_lo, ia, ib);
         else
-            rotate_store(qa, qb, sw, cw, qs + ia, qs + ib);
+            rotate_store(qa, qb, sw, cw, out.qs, out.qs_lo, ia, ib);
     }
 }
 
 size_t rope_prefill_workspace_bytes(int BH, int64_t L, int d) {
-    return 3 * static_cast<size_t>(BH) * static_cast<size_t>(L) * static_cast<size_t>(d) * 2;
+    return 6 * static_cast<size_t>(BH) * static_cast<size_t>(L) * static_cast<size_t>(d) * 2;
 }
 
-int launch_rope_prep(const void *q, const void *k, void *qr, void *qs, void *kr, int BH, int64_t L, int d, int w,
-                     double base, cudaStream_t stream) {
+RopeParts rope_parts(void *workspace, int BH, int64_t L, int d) {
+    char *ws = static_cast<char *>(workspace);
+    const size_t one = static_cast<size_t>(BH) * static_cast<size_t>(L) * static_cast<size_t>(d) * 2;
+    return RopeParts{ws, ws + one, ws + 2 * one, ws + 3 * one, ws + 4 * one, ws + 5 * one};
+}
+
+int launch_rope_prep(const void *q, const void *k, const RopeParts &o, int BH, int64_t L, int d, int w, double base,
+                     cudaStream_t stream) {
     if (d != kRopeD) return fail(SWA_ERR_UNSUPPORTED, "rope prefill needs d = %d", kRopeD);
     RopePrep rp{};
     // theta_i / (2 pi) = base^(-2i/d) / (2 pi) < 1/6 in double, rounded to a 64-bit fraction in two 32-bit
@@ -124,9 +146,10 @@ int launch_rope_prep(const void *q, const void *k, void *qr, void *qs, void *kr,
     const int64_t rows = static_cast<int64_t>(BH) * L;
     const int64_t ctas_needed = (rows + 256 / kRopeLanes - 1) / (256 / kRopeLanes);
     const int ctas = static_cast<int>(ctas_needed < 152 * 8 ? ctas_needed : 152 * 8);
-    rope_prep_kernel<<<ctas, 256, 0, stream>>>(static_cast<const uint2 *>(q), static_cast<const uint2 *>(k),
-                                               static_cast<uint2 *>(qr), static_cast<uint2 *>(qs),
-                                               static_cast<uint2 *>(kr), rows, L, w, rp);
+    const RopeOut out{static_cast<uint2 *>(o.qr), static_cast<uint2 *>(o.qr_lo), static_cast<uint2 *>(o.qs),
+                      static_cast<uint2 *>(o.qs_lo), static_cast<uint2 *>(o.kr), static_cast<uint2 *>(o.kr_lo)};
+    rope_prep_kernel<<<ctas, 256, 0, stream>>>(static_cast<const uint2 *>(q), static_cast<const uint2 *>(k), out,
+                                               rows, L, w, rp);
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return fail(SWA_ERR_CUDA, "rope prefill pass launch: %s", cudaGetErrorString(e));
     return SWA_OK;

@@ -35,16 +35,21 @@ struct PrefillArgs {
     float scale;
     int64_t seq_stride;  // rows between consecutive (b, h) blocks (== L for contiguous tensors)
     cudaStream_t stream;
-    // RoPE at the positions inside the cache (bf16 tensor-core prefill, pos0 == 0): q and k are rotated
-    // rows, q_sink the query rows rotated for the sink keys; the sinks get their own key tile, scored
-    // with q_sink, and the band starts at position s
+    // RoPE at the positions inside the cache (bf16 tensor-core prefill, d = 128): q and k are the rotated
+    // rows (their bf16 hi parts), q_sink the query rows rotated for the sink keys; the sinks get their own
+    // key tile, scored with q_sink, and the band starts at position s.  Every rotated operand comes as a
+    // (hi, lo) bf16 pair whose sum is the fp32 rotation: q_lo, q_sink_lo, k_lo, and k_cache_lo for the
+    // rotated keys of the cache (pos0 > 0)
     const void *q_sink = nullptr;
+    const void *q_lo = nullptr, *q_sink_lo = nullptr, *k_lo = nullptr, *k_cache_lo = nullptr;
 };
 
 int launch_prefill_f32(const PrefillArgs &a);
+// The bf16 tensor-core prefill: the sub-tile kernel for RoPE (hi/lo operands) and d = 64, the 128-key-tile
+// kernel for plain d = 128.
 int launch_prefill_bf16_tc(const PrefillArgs &a);
-// The rotation pass of RoPE prefill: qr = R(t) q, kr = R(t) k, qs = R(min(t, w - 1)) q for the rows of
-// [BH, L, d] (d = 128, bf16); workspace = qr | qs | kr.
+int launch_prefill_bf16_tc_plain(const PrefillArgs &a);
+int launch_prefill_bf16_tc_sub(const PrefillArgs &a);
 // Layout passes of the dilated-window prefill: rows of one virtual head (sinks + one residue class), the
 // gather of q, k, v into the virtual heads [BH * r, Lv, d] and the scatter of o (and lse) back.
 int64_t dilated_rows(int64_t L, int s, int r);
@@ -52,9 +57,16 @@ int launch_dilate_gather(const void *q, const void *k, const void *v, void *qv, 
                          int d, int esize, int s, int r, cudaStream_t stream);
 int launch_dilate_scatter(const void *ov, const float *lsev, void *o, float *lse, int BH, int64_t L, int d, int esize,
                           int s, int r, cudaStream_t stream);
+// The rotation pass of RoPE prefill: for the rows of [BH, L, d] (d = 128, bf16) qr = R(t) q, qs = R(min(t, w - 1)) q
+// and kr = R(t) k, each written as a bf16 (hi, lo) pair with hi + lo the fp32 rotation.  The workspace holds
+// the six [BH, L, d] tensors in this order.
+struct RopeParts {
+    void *qr, *qr_lo, *qs, *qs_lo, *kr, *kr_lo;
+};
 size_t rope_prefill_workspace_bytes(int BH, int64_t L, int d);
-int launch_rope_prep(const void *q, const void *k, void *qr, void *qs, void *kr, int BH, int64_t L, int d, int w,
-                     double base, cudaStream_t stream);
+RopeParts rope_parts(void *workspace, int BH, int64_t L, int d);
+int launch_rope_prep(const void *q, const void *k, const RopeParts &out, int BH, int64_t L, int d, int w, double base,
+                     cudaStream_t stream);
 
 // Rolling-cache write of positions pos0..pos0+n-1; source rows of (b, h) start at bh*src_stride.  With
 // v_new == nullptr only the keys are written.
@@ -88,7 +100,10 @@ int launch_decode_rope(const DecodeArgs &a, double base);
 size_t decode_noalloc_scratch_bytes();
 int launch_decode_noalloc(DecodeArgs a);
 
+// Key walks of the prefill kernels (host): the plain kernel's 128-key tiles, or (rope) the sub-tile kernel's
+// 64-key sub-tiles.
 int prefill_tile_plan(int q0, int q1, int pos0, int w, int s, int rope, int *out, int max_tiles);
+int prefill_tile_plan_sub(int q0, int q1, int pos0, int w, int s, int rope, int *out, int max_tiles);
 int launch_selftest_wait_timeout(uint64_t timeout_ns, cudaStream_t stream);
 int launch_selftest_umma(const void *a, const void *b, float *c, int mode, cudaStream_t stream);
 

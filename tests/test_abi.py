@@ -79,10 +79,12 @@ def test_prefill_null_and_misaligned(lib):
     assert lib.swa_sink_prefill(None, None, None, None, None, None, None, 0, 1, 1, 0, 128, 8, 4, 0.1, 0, None) == 0
 
 
-def test_bf16_prefill_needs_d128(lib):
+def test_bf16_prefill_takes_d64_and_d128_only(lib):
+    # the tensor-core path runs at d = 64 and d = 128; other head dimensions are refused before any launch
     f = 1 << 20
-    rc = lib.swa_sink_prefill(f, f, f, f, None, None, None, 0, 1, 1, 16, 64, 8, 4, 0.1, 0, None)
-    assert rc == swa.SWA_ERR_UNSUPPORTED
+    for d in (16, 32):
+        rc = lib.swa_sink_prefill(f, f, f, f, None, None, None, 0, 1, 1, 16, d, 8, 4, 0.1, 0, None)
+        assert rc == swa.SWA_ERR_UNSUPPORTED, d
 
 
 def test_decode_and_write_reject_bad_arguments(lib):
@@ -153,7 +155,7 @@ def test_rope_decode_validates_before_launch(lib):
 def test_rope_prefills_validate_before_launch(lib):
     f = 1 << 20  # never dereferenced: validation fails first
     need = lib.swa_sink_prefill_rope_workspace_size(1, 2, 300, 128)
-    assert need == 3 * 2 * 300 * 128 * 2
+    assert need == 6 * 2 * 300 * 128 * 2  # rotated q, sink-rotated q and rotated k, each as a (hi, lo) pair
     ok = [f, f, f, f, None, 1, 2, 300, 128, 64, 4, 0.1, 10000.0, f << 8, need, swa.SWA_BF16, None]
     bad = list(ok)
     bad[15] = swa.SWA_F32  # the RoPE prefill runs on the tensor cores only
@@ -169,7 +171,7 @@ def test_rope_prefills_validate_before_launch(lib):
     assert lib.swa_sink_prefill_rope(*bad) == swa.SWA_ERR_INVALID
     # chunked: chunks shorter than the sinks are refused, and the workspace adds a rotated-key cache
     cneed = lib.swa_sink_prefill_chunked_rope_workspace_size(1, 2, 300, 128, 64)
-    assert cneed == need + 2 * 64 * 128 * 2
+    assert cneed == need + 2 * 2 * 64 * 128 * 2  # + the rotated-key cache (hi, lo)
     cok = [f, f, f, f, None, f, f, 1, 2, 300, 128, 64, 8, 0.1, 32, 10000.0, f << 8, cneed, swa.SWA_BF16, None]
     bad = list(cok)
     bad[14] = 4  # chunk < s

@@ -144,7 +144,7 @@ def test_full_size_streaming_decode_rope():
 def test_full_size_prefill_rope_sampled_rows():
     # the primary shape with RoPE at the positions inside the cache: every head at rows around the tile,
     # pair and window boundaries, the last rows and a few random ones, against the oracle's definition;
-    # checked as in tests/test_gpu_prefill_rope.py (rotated operands, attention on them, exact definition)
+    # checked as in tests/test_gpu_prefill_rope.py (rotated operands, then the exact definition)
     swa = require_gpu()
     wl = swa_inputs.WORKLOADS["prefill_llama7b_L8192_w1024_s4"]
     q, k, v = swa_inputs.workload_inputs(wl, "cuda")

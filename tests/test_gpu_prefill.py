@@ -60,9 +60,10 @@ BF16_SHAPES = [
 ]
 
 
+@pytest.mark.parametrize("d", [128, 64])
 @pytest.mark.parametrize("B,H,L,w,s", BF16_SHAPES)
-def test_bf16_tensor_core_prefill(B, H, L, w, s):
-    run_and_check(B, H, L, 128, w, s, torch.bfloat16, 1000 + L + w + s)
+def test_bf16_tensor_core_prefill(B, H, L, w, s, d):
+    run_and_check(B, H, L, d, w, s, torch.bfloat16, 1000 + L + w + s + d)
 
 
 def test_bf16_sink_boost_stability():
@@ -76,7 +77,7 @@ def test_bf16_sink_boost_stability():
     compare("sink boost", o, o_ref, torch.bfloat16)
 
 
-@pytest.mark.parametrize("dtype,d", [(torch.bfloat16, 128), (torch.float32, 64)])
+@pytest.mark.parametrize("dtype,d", [(torch.bfloat16, 128), (torch.bfloat16, 64), (torch.float32, 64)])
 @pytest.mark.parametrize("L,w,s,pos0", [(300, 100, 4, 257), (200, 64, 0, 1000), (150, 300, 4, 2), (129, 40, 8, 64)])
 def test_prefill_with_cache(dtype, d, L, w, s, pos0):
     # rows pos0..pos0+L-1 against the rolling cache of positions < pos0 plus their own keys
@@ -124,6 +125,24 @@ def test_chunked_prefill(L, w, s, chunk, H):
     held = holder >= 0
     assert torch.equal(kc.cpu()[:, :, held], k.cpu()[:, :, holder[held]])
     assert torch.equal(vc.cpu()[:, :, held], v.cpu()[:, :, holder[held]])
+
+
+@pytest.mark.parametrize("L,w,s,chunk,H", [(1000, 300, 4, 256, 2), (2048, 1024, 4, 512, 17)])
+def test_chunked_prefill_d64(L, w, s, chunk, H):
+    swa = require_gpu()
+    B, d = 1, 64
+    q, k, v = inputs(B, H, L, d, torch.bfloat16, 90 + chunk, sink_boost=True)
+    kc = torch.full((B, H, w, d), float("nan"), dtype=torch.bfloat16, device="cuda")
+    vc = torch.full_like(kc, float("nan"))
+    lse = torch.empty((B, H, L), dtype=torch.float32, device="cuda")
+    o = swa.swa_sink_prefill_chunked(q, k, v, w, s, chunk, kc, vc, lse=lse)
+    assert swa.swa_device_status() == swa.SWA_OK, swa.last_error()
+    o_ref, l_ref = oracle.prefill(q, k, v, w, s, 1.0 / math.sqrt(d))
+    compare("chunked d64", o, o_ref, torch.bfloat16)
+    assert np.abs(lse.cpu().double().numpy() - l_ref).max() < LSE_ABS
+    holder = torch.as_tensor(oracle.cache_replay(w, s, L))
+    held = holder >= 0
+    assert torch.equal(kc.cpu()[:, :, held], k.cpu()[:, :, holder[held]])
 
 
 def test_chunked_prefill_fp32():

@@ -1,10 +1,11 @@
-"""The key-tile walk of the bf16 prefill kernel (host-callable, same function as on the device) covers
-every key of every query row exactly once, with the right position in every column (CPU only).
+"""The key walks of the bf16 prefill kernels (host-callable, same functions as on the device) cover every
+key of every query row exactly once, with the right position in every column (CPU only).
 
-For each tile the library reports (source, first row, position of column 0, last valid column).
-Column c <= last holds source row (first row + c).  For the rolling cache the position stored in a slot
-comes from the oracle's sequential replay of the writes; for the call's own rows it is pos0 + row.
-Membership of a position in the key set of row t is the oracle's brute-force predicate.
+The plain kernel walks tiles of up to 128 keys, the RoPE kernel sub-tiles of up to 64; for each the library
+reports (source, first row, position of column 0, last valid column, mask of the query tiles that compute
+it).  Column c <= last holds source row (first row + c).  For the rolling cache the position stored in a slot comes from the oracle's sequential
+replay of the writes; for the call's own rows it is pos0 + row.  Membership of a position in the key set of
+row t is the oracle's brute-force predicate.
 """
 import random
 
@@ -14,16 +15,18 @@ import pytest
 import oracle
 import sliding_window_softmax_swa_gb300 as swa
 
-BN = 128   # keys per tile and rows per query tile
+BN = 128   # keys per tile of the plain kernel's walk
+SUB = 64   # keys per sub-tile of the RoPE kernel's walk
+BQ = 128   # rows per query tile
 BM = 256   # query rows per CTA (two query tiles)
 
 
-def check_plan(q0, q1, pos0, w, s, L, plan=None):
+def check_plan(q0, q1, pos0, w, s, L, plan=None, width=BN):
     plan = swa.prefill_tile_plan(q0, q1, pos0, w, s) if plan is None else plan
     holder = oracle.cache_replay(w, s, pos0) if pos0 > 0 else None
     cols, users = [], []
     for src, row0, pbase, chi, used in plan:
-        assert 0 <= chi < BN
+        assert 0 <= chi < width
         assert row0 >= 0
         assert used != 0, "a tile no query tile needs"
         for c in range(chi + 1):
@@ -42,7 +45,7 @@ def check_plan(q0, q1, pos0, w, s, L, plan=None):
     users = np.array(users, dtype=np.int64)
     allpos = np.arange(q1 + 1, dtype=np.int64)
     for t in range(q0, q1 + 1):
-        x = (t - q0) // BN  # the query tile of row t
+        x = (t - q0) // BQ  # the query tile of row t
         mine = cols[(users >> x) & 1 == 1]
         got = np.sort(mine[oracle.is_key_many(t, mine, w, s)])
         want = allpos[oracle.is_key_many(t, allpos, w, s)]
@@ -96,6 +99,18 @@ def test_tile_count_is_minimal_for_full_windows():
             assert used == (m + 127 + BN - 1) // BN + (1 if s else 0)
 
 
+def test_rope_sub_tile_count_is_minimal_for_full_windows():
+    # the RoPE kernel's walk: ceil((m' + 255) / 64) band sub-tiles (the band starts at s) plus the sinks, and
+    # each query tile computes only the ceil((m' + 127) / 64) its own rows reach
+    for w, s in [(1024, 4), (4096, 4), (4096, 0)]:
+        m = w - s
+        plan = swa.prefill_tile_plan_rope(8192, 8192 + BM - 1, 0, w, s)
+        assert len(plan) == (m + 255 + SUB - 1) // SUB + (1 if s else 0)
+        for x in (0, 1):
+            used = sum(1 for tl in plan if (tl[4] >> x) & 1)
+            assert used == (m + 127 + SUB - 1) // SUB + (1 if s else 0)
+
+
 @pytest.mark.parametrize("w,s", [(1024, 4), (4096, 4), (4096, 0), (300, 4), (64, 16), (2, 1), (129, 4), (300, 128),
                                  (256, 100), (17, 16), (1, 0)])
 def test_rope_tiles(w, s):
@@ -105,12 +120,25 @@ def test_rope_tiles(w, s):
     for qt in range(0, (L + BM - 1) // BM):
         q0 = qt * BM
         q1 = min(q0 + BM, L) - 1
-        plan = check_plan(q0, q1, 0, w, s, L, swa.prefill_tile_plan_rope(q0, q1, 0, w, s))
-        if s > 0:
-            src, row0, pbase, chi, used = plan[0]
-            assert (src, row0, pbase, chi) == (0, 0, 0, min(s, q1 + 1) - 1)
-        for src, row0, pbase, chi, used in plan[1 if s > 0 else 0:]:
+        plan = check_plan(q0, q1, 0, w, s, L, swa.prefill_tile_plan_rope(q0, q1, 0, w, s), SUB)
+        ns = sink_prefix(plan, s, min(s, q1 + 1), src=0)
+        for src, row0, pbase, chi, used in plan[ns:]:
             assert pbase >= s
+
+
+def sink_prefix(plan, s, nsink, src):
+    """The RoPE walk starts with the sinks [0, nsink) on their own (one or two sub-tiles, consecutive
+    positions from 0); returns how many entries they take."""
+    if s == 0:
+        return 0
+    k, p = 0, 0
+    while k < len(plan) and plan[k][2] < s:
+        e = plan[k]
+        assert e[0] == src and e[2] == p and e[2] + e[3] < nsink, e
+        p = e[2] + e[3] + 1
+        k += 1
+    assert p == nsink and 1 <= k <= 2
+    return k
 
 
 def test_rope_chunked_tiles_random():
@@ -124,8 +152,7 @@ def test_rope_chunked_tiles_random():
         qt = rng.randrange(0, (L + BM - 1) // BM)
         q0 = pos0 + qt * BM
         q1 = pos0 + min(qt * BM + BM, L) - 1
-        plan = check_plan(q0, q1, pos0, w, s, L, swa.prefill_tile_plan_rope(q0, q1, pos0, w, s))
-        if s > 0:
-            assert plan[0][0] == 1 and plan[0][2] == 0 and plan[0][3] == s - 1, plan[0]
-        for src, row0, pbase, chi, used in plan[1 if s > 0 else 0:]:
+        plan = check_plan(q0, q1, pos0, w, s, L, swa.prefill_tile_plan_rope(q0, q1, pos0, w, s), SUB)
+        ns = sink_prefix(plan, s, s, src=1)
+        for src, row0, pbase, chi, used in plan[ns:]:
             assert pbase >= s
