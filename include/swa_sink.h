@@ -166,6 +166,36 @@ int swa_sink_prefill_chunked_dilated(const void *q, const void *k, const void *v
                                      int64_t chunk, void *workspace, size_t workspace_bytes, int dtype, void *stream);
 
 /*
+ * swa_sink_prefill_blocksparse -- whole-sequence prefill over the BigBird-style union of the fixed-sparsity page
+ * ("滑窗与固定稀疏", Longformer and BigBird sections, eq attn-fixed-bigbird: a local window, global tokens and
+ * random key blocks, at block granularity), in causal form with the sinks of the StreamingLLM section.  Row t
+ * attends the keys i <= t with
+ *     i < s (sink)  or  i >= t - (w - s) + 1 (window)  or  i a global token  or  t a global token
+ *     or  i in one of the random key blocks given for t's query block (block index t / block),
+ * each key once; with no global token and no random block it is swa_sink_prefill.  Global tokens sit inside the
+ * sequence (a global row sees every earlier key; every later row sees a global key).  One pattern serves every
+ * (b, h).  Rows run on the tensor cores (per-pair key-tile lists built on the host, per-row column masks); the
+ * global rows are recomputed over their whole causal prefix by a CUDA-core pass.
+ *
+ *   q, k, v, o, lse : as swa_sink_prefill (pos0 = 0); bf16, d = 128.
+ *   globals   : HOST int32 array of n_globals distinct positions in [0, L), ascending (NULL if n_globals = 0).
+ *   block     : block size of the random key blocks, >= 1.
+ *   rand_blocks : HOST int32 [ceil(L / block), r]: the key blocks (index i covers positions i*block ..
+ *             i*block + block - 1) attended by each query block, -1 for an unused entry; 0 <= r <= 16.  The random
+ *             choice is the caller's: the library draws nothing.
+ *   workspace : caller-owned device scratch of swa_sink_prefill_blocksparse_workspace_size(L, n_globals, block, r)
+ *             bytes, 256-byte aligned (the tile lists and the pattern, uploaded with cudaMemcpyAsync from pageable
+ *             host memory: the call is not capturable into a CUDA graph).
+ *   A query pair (256 rows) whose keys need more than 64 tiles of 128 keys is refused with SWA_ERR_UNSUPPORTED.
+ *   Other arguments and errors as swa_sink_prefill.
+ */
+int swa_sink_prefill_blocksparse(const void *q, const void *k, const void *v, void *o, float *lse, int B, int H,
+                                 int64_t L, int d, int w, int s, float scale, const int32_t *globals, int n_globals,
+                                 int block, const int32_t *rand_blocks, int r, void *workspace, size_t workspace_bytes,
+                                 int dtype, void *stream);
+size_t swa_sink_prefill_blocksparse_workspace_size(int64_t L, int n_globals, int block, int r);
+
+/*
  * swa_sink_prefill_chunked -- the chunk-based prefill of "滑窗与固定稀疏" (rolling-buffer section):
  * the L positions are processed in chunks of `chunk` rows; chunk c attends the rolling cache as it was
  * before the chunk plus its own keys (swa_sink_prefill with pos0 = c*chunk), then its keys/values are
@@ -330,6 +360,13 @@ int swa_prefill_tile_plan(int64_t q0, int64_t q1, int64_t pos0, int w, int s, in
 /* The same for the RoPE prefills (pos0 = 0, or pos0 >= s in chunked prefill): the sinks form the first
  * tile on their own, the band starts at position s.  s <= 128. */
 int swa_prefill_tile_plan_rope(int64_t q0, int64_t q1, int64_t pos0, int w, int s, int *tiles, int max_tiles);
+/* The same for swa_sink_prefill_blocksparse (host only, no CUDA call): the key tiles of query pair `pair`
+ * (rows 256*pair .. 256*pair + 255) for the pattern (globals, block, rand_blocks, r) of a sequence of L
+ * positions.  For tile i, tiles[7i..7i+6] = {absolute position of column 0, last valid column, bit mask of
+ * the query tiles that use it, and four 32-bit words whose bit c (of word c / 32) marks a column holding a
+ * global token}.  Pattern arguments and errors as swa_sink_prefill_blocksparse. */
+int swa_prefill_blocksparse_plan(int64_t L, int w, int s, const int32_t *globals, int n_globals, int block,
+                                 const int32_t *rand_blocks, int r, int64_t pair, int *tiles, int max_tiles);
 
 #ifdef __cplusplus
 }

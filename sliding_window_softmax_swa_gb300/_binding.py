@@ -41,6 +41,7 @@ SIGNATURES = {
     "swa_selftest_umma": (_i, [_vp, _vp, _vp, _i, _vp]),
     "swa_prefill_tile_plan": (_i, [_i64, _i64, _i64, _i, _i, ctypes.POINTER(ctypes.c_int), _i]),
     "swa_prefill_tile_plan_rope": (_i, [_i64, _i64, _i64, _i, _i, ctypes.POINTER(ctypes.c_int), _i]),
+    "swa_prefill_blocksparse_plan": (_i, [_i64, _i, _i, _vp, _i, _i, _vp, _i, _i64, ctypes.POINTER(ctypes.c_int), _i]),
     "swa_sink_prefill_dilated": (_i, [_vp, _vp, _vp, _vp, _vp, _i, _i, _i64, _i, _i, _i, _i, _f, _vp, _sz, _i, _vp]),
     "swa_sink_prefill_chunked_dilated": (_i, [_vp, _vp, _vp, _vp, _vp, _vp, _vp, _i, _i, _i64, _i, _i, _i, _i, _f, _i64,
                                               _vp, _sz, _i, _vp]),
@@ -54,6 +55,9 @@ SIGNATURES = {
     "swa_sink_prefill_rope": (_i, [_vp, _vp, _vp, _vp, _vp, _i, _i, _i64, _i, _i, _i, _f, ctypes.c_double, _vp,
                                    _sz, _i, _vp]),
     "swa_sink_prefill_rope_workspace_size": (_sz, [_i, _i, _i64, _i]),
+    "swa_sink_prefill_blocksparse": (_i, [_vp, _vp, _vp, _vp, _vp, _i, _i, _i64, _i, _i, _i, _f, _vp, _i, _i, _vp, _i,
+                                          _vp, _sz, _i, _vp]),
+    "swa_sink_prefill_blocksparse_workspace_size": (_sz, [_i64, _i, _i, _i]),
 }
 
 _lib = None
@@ -244,6 +248,38 @@ def swa_sink_prefill_chunked_rope(q, k, v, w: int, s: int, chunk: int, k_cache, 
     return o
 
 
+def _pattern(globals_, rand_blocks):
+    """Host int32 arrays of a block-sparse pattern, as given (the library checks them): (globals, r, rand)."""
+    import numpy as np
+    g = np.ascontiguousarray([int(x) for x in globals_], dtype=np.int32)
+    if rand_blocks is None:
+        return g, 0, np.zeros((0,), dtype=np.int32)
+    rb = np.ascontiguousarray(rand_blocks, dtype=np.int32)
+    return g, (rb.shape[1] if rb.ndim == 2 else 0), rb
+
+
+def swa_sink_prefill_blocksparse(q, k, v, w: int, s: int, globals_=(), block: int = 64, rand_blocks=None,
+                                 scale: float | None = None, o=None, lse=None, workspace=None, stream=None):
+    """Prefill over the BigBird-style union (window + sinks + global tokens + random key blocks), causal.
+    globals_: positions of the global tokens; rand_blocks: int array [ceil(L / block), r] of key blocks per query
+    block (-1 = none), or None."""
+    B, H, L, d = q.shape
+    assert k.shape == q.shape and v.shape == q.shape and k.dtype == q.dtype and v.dtype == q.dtype
+    if o is None:
+        o = torch.empty_like(q)
+    g, r, rb = _pattern(globals_, rand_blocks)
+    nws = lib().swa_sink_prefill_blocksparse_workspace_size(L, g.size, block, r)
+    if workspace is None:
+        workspace = torch.empty(max(nws, 256), dtype=torch.uint8, device=q.device)
+    _dev(q, k, v, o, lse, workspace)
+    scale = (1.0 / d ** 0.5) if scale is None else scale
+    _check("swa_sink_prefill_blocksparse", lib().swa_sink_prefill_blocksparse(
+        _ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), B, H, L, d, w, s, scale,
+        g.ctypes.data if g.size else None, g.size, block, rb.ctypes.data if r else None, r, _ptr(workspace),
+        workspace.numel() * workspace.element_size(), _dtype_code(q), _stream(stream)))
+    return o
+
+
 def swa_sink_prefill_chunked(q, k, v, w: int, s: int, chunk: int, k_cache, v_cache, scale: float | None = None,
                              o=None, lse=None, stream=None):
     """Chunked prefill through the rolling cache (k_cache/v_cache [B, H, w, d] are overwritten)."""
@@ -349,6 +385,23 @@ def prefill_tile_plan_rope(q0: int, q1: int, pos0: int, w: int, s: int):
     if n < 0:
         raise SwaError("swa_prefill_tile_plan_rope", n, last_error())
     return [tuple(buf[5 * i:5 * i + 5]) for i in range(min(n, 256))]
+
+
+def prefill_blocksparse_plan(L: int, w: int, s: int, globals_, block: int, rand_blocks, pair: int):
+    """The key tiles of the block-sparse prefill for query pair ``pair`` (rows 256*pair ..): list of
+    (pbase, chi, used_by_mask, global-column mask as one 128-bit int)."""
+    g, r, rb = _pattern(globals_, rand_blocks)
+    buf = (ctypes.c_int * (7 * 64))()
+    n = lib().swa_prefill_blocksparse_plan(L, w, s, g.ctypes.data if g.size else None, g.size, block,
+                                           rb.ctypes.data if r else None, r, pair, buf, 64)
+    if n < 0:
+        raise SwaError("swa_prefill_blocksparse_plan", n, last_error())
+    out = []
+    for i in range(min(n, 64)):
+        rec = buf[7 * i:7 * i + 7]
+        gm = sum((rec[3 + k] & 0xFFFFFFFF) << (32 * k) for k in range(4))
+        out.append((rec[0], rec[1], rec[2], gm))
+    return out
 
 
 def swa_device_status(stream=None) -> int:

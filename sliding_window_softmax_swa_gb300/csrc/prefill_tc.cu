@@ -52,6 +52,10 @@
 // its copies in flight, the MMA thread waits for its MMAs, and TMEM is freed before the CTA exits.
 #include <math.h>
 
+#include <algorithm>
+#include <utility>
+#include <vector>
+
 #include "../../include/swa_sink.h"
 #include "swa_device.cuh"
 #include "swa_internal.h"
@@ -82,7 +86,8 @@ constexpr uint32_t OFF_V = OFF_K + NK * TILE_BYTES;
 constexpr uint32_t OFF_BAR = OFF_V + NV * TILE_BYTES;
 constexpr uint32_t OFF_MISC = OFF_BAR + 256;
 constexpr uint32_t OFF_TILES = OFF_MISC + 64;
-constexpr uint32_t SMEM_USED = OFF_TILES + 2 * MAX_TILES * 12;  // two tile lists (current / next item)
+constexpr uint32_t OFF_GMASK = OFF_TILES + 2 * MAX_TILES * 12;  // two tile lists (current / next item)
+constexpr uint32_t SMEM_USED = OFF_GMASK + 2 * MAX_TILES * 16;     // and their global-key columns (block-sparse)
 constexpr uint32_t SMEM_BYTES = SMEM_USED + 1024;  // slack to align the base to 1024 bytes
 static_assert(SMEM_BYTES <= 232448, "shared memory budget of one CTA");
 
@@ -97,10 +102,20 @@ struct Tile {
 };
 static_assert(sizeof(Tile) == 12, "tile record");
 
+// Block-sparse mode: per column of a key tile, whether it holds a global key (bit c of word c / 32).
+struct TileMask {
+    uint32_t w[4];
+};
+
 struct Params {
     CUtensorMap tm_q, tm_k, tm_v, tm_kc, tm_vc;
-    CUtensorMap tm_qs;  // RoPE mode: query rows rotated for the sink keys (the sink tile, first in every
-                        // list, is scored with them; the band with tm_q)
+    // block-sparse mode: the host-built key-tile lists of every 256-row query pair (MAX_TILES entries per pair,
+    // bs_count[pair] used), their global-key columns, and the random key blocks of each query block
+    const Tile *bs_tiles;
+    const TileMask *bs_gmask;
+    const int *bs_count;
+    const int *bs_rand;  // [ceil(L / bs_block)][bs_r]; -1 = no block
+    int bs_block, bs_r;
     void *o;
     float *lse;
     DeviceStatus *status;
@@ -244,8 +259,9 @@ __device__ __forceinline__ void issue_pv(uint32_t d_tmem, uint32_t p_tmem, uint3
     }
 }
 
-// ROPE: the RoPE mode (compiled apart, so that the plain kernel's MMA loop carries none of its checks)
-template <bool ROPE>
+// BS: the block-sparse mode (host-built tile lists with global keys and random key blocks; compiled apart, so
+// that the plain kernel carries none of its checks)
+template <bool BS>
 __global__ void __launch_bounds__(kThreads, 1) swa_prefill_tc_kernel(const __grid_constant__ Params P) {
     extern __shared__ uint8_t smem_raw[];
     uint8_t *sm = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -267,6 +283,7 @@ __global__ void __launch_bounds__(kThreads, 1) swa_prefill_tc_kernel(const __gri
     volatile int *abort_flag = reinterpret_cast<volatile int *>(sm + OFF_MISC + 4);
     int *ntiles_s = reinterpret_cast<int *>(sm + OFF_MISC + 8);  // [2]
     Tile *tiles_s = reinterpret_cast<Tile *>(sm + OFF_TILES);     // [2][MAX_TILES]
+    TileMask *gmask_s = reinterpret_cast<TileMask *>(sm + OFF_GMASK);  // [2][MAX_TILES] (block-sparse)
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int G = static_cast<int>(gridDim.x);
@@ -399,46 +416,47 @@ __global__ void __launch_bounds__(kThreads, 1) swa_prefill_tc_kernel(const __gri
                 const int b = it & 1;
                 if (it >= 2 && !mbar_wait(&lfree[b], ((it - 2) >> 1) & 1, wc, 12, it)) break;
                 Tile *tl = tiles_s + b * MAX_TILES;
-                const int n = build_tiles(tl, q0, qlast, P.pos0, P.s, P.m, P.w, ROPE);
+                int n;
+                if (BS) {  // the pair's list, built on the host
+                    const int qp = row_start / BM;
+                    n = P.bs_count[qp];
+                    if (n >= 1 && n <= MAX_TILES) {
+                        const Tile *src = P.bs_tiles + static_cast<int64_t>(qp) * MAX_TILES;
+                        const TileMask *gsrc = P.bs_gmask + static_cast<int64_t>(qp) * MAX_TILES;
+                        for (int i = 0; i < n; ++i) {
+                            tl[i] = src[i];
+                            gmask_s[b * MAX_TILES + i] = gsrc[i];
+                        }
+                    }
+                } else {
+                    n = build_tiles(tl, q0, qlast, P.pos0, P.s, P.m, P.w, false);
+                }
                 if (n < 1 || n > MAX_TILES) {
                     atomicOr(&P.status->word, kDevBadArg);
                     *abort_flag = 1;
                     break;
                 }
-                mark_tiles(tl, n, q0, qlast, P.s, P.m);
+                if (!BS) mark_tiles(tl, n, q0, qlast, P.s, P.m);
                 ntiles_s[b] = n;
                 mbar_arrive(&lready[b]);  // release: the list is visible to whoever sees the phase complete
-                // Q loads of the item: one (tm_q), or in RoPE mode with sinks the sink-rotated rows for
-                // the first tile and then, once its QK products are done, the band-rotated rows.  Every
-                // load waits until the QK products of the previous one are done.
-                const CUtensorMap *mq0 = (ROPE && P.s > 0) ? &P.tm_qs : &P.tm_q;
-                const bool two = ROPE && P.s > 0 && n >= 2;
-                bool ok = true;
-                for (int ph = 0; ph < (two ? 2 : 1) && ok; ++ph) {
-                    const CUtensorMap *mq = ph == 0 ? mq0 : &P.tm_q;
-                    if (nq >= 1 && !mbar_wait(qempty, (nq - 1) & 1, wc, 13, it)) {
-                        ok = false;
-                        break;
-                    }
-                    uint8_t *qs = sm + OFF_Q;
-                    mbar_arrive_expect_tx(qfull, 2 * TILE_BYTES);
+                // Q_0, Q_1 of the item, once the QK products of the previous item's Q are done
+                if (nq >= 1 && !mbar_wait(qempty, (nq - 1) & 1, wc, 13, it)) break;
+                uint8_t *qs = sm + OFF_Q;
+                mbar_arrive_expect_tx(qfull, 2 * TILE_BYTES);
+                for (int x = 0; x < 2; ++x) {
+                    tma_load_3d(qs + x * TILE_BYTES, &P.tm_q, qfull, 0, row_start + x * BH_ROWS, bh);
+                    tma_load_3d(qs + x * TILE_BYTES + HALF_BYTES, &P.tm_q, qfull, 64, row_start + x * BH_ROWS, bh);
+                }
+                ++nq;
+                // into L2 meanwhile: the next item's Q rows
+                const int nitem = item + G;
+                if (nitem < P.n_items) {
+                    const int nrow = (P.n_qpairs - 1 - nitem / P.BH) * BM;
                     for (int x = 0; x < 2; ++x) {
-                        tma_load_3d(qs + x * TILE_BYTES, mq, qfull, 0, row_start + x * BH_ROWS, bh);
-                        tma_load_3d(qs + x * TILE_BYTES + HALF_BYTES, mq, qfull, 64, row_start + x * BH_ROWS, bh);
-                    }
-                    ++nq;
-                    // into L2 meanwhile: the band rows of this item (RoPE), else the next item's first rows
-                    const int nitem = (two && ph == 0) ? item : item + G;
-                    const CUtensorMap *mp = (two && ph == 0) ? &P.tm_q : mq0;
-                    if (nitem < P.n_items) {
-                        const int nrow = (P.n_qpairs - 1 - nitem / P.BH) * BM;
-                        for (int x = 0; x < 2; ++x) {
-                            tma_prefetch_3d(mp, 0, nrow + x * BH_ROWS, nitem % P.BH);
-                            tma_prefetch_3d(mp, 64, nrow + x * BH_ROWS, nitem % P.BH);
-                        }
+                        tma_prefetch_3d(&P.tm_q, 0, nrow + x * BH_ROWS, nitem % P.BH);
+                        tma_prefetch_3d(&P.tm_q, 64, nrow + x * BH_ROWS, nitem % P.BH);
                     }
                 }
-                if (!ok) break;
             }
             if (*abort_flag && nq > 0) mbar_wait_drain(qfull, (nq - 1) & 1);  // no copy may still be landing
         }
@@ -464,9 +482,6 @@ __global__ void __launch_bounds__(kThreads, 1) swa_prefill_tc_kernel(const __gri
                 ++nqf;
                 const Tile *tl = tiles_s + b * MAX_TILES;
                 const int n = ntiles_s[b];
-                // RoPE mode with sinks: tile 0 (the sinks) uses the first Q load, the band a second one
-                const bool two = ROPE && P.s > 0 && n >= 2;
-                bool q_band = !two;
                 int last_used[2] = {-1, -1};
                 for (int j = 0; j < n; ++j)
                     for (int x = 0; x < 2; ++x)
@@ -481,7 +496,7 @@ __global__ void __launch_bounds__(kThreads, 1) swa_prefill_tc_kernel(const __gri
                             umma_commit(&sfull[x]);
                         }
                     }
-                    if (n == 1 || (ROPE && two)) umma_commit(qempty);  // the first Q load is no longer read
+                    if (n == 1) umma_commit(qempty);  // the item's only QK products: Q is no longer read
                     umma_commit(&kempty[gk % NK]);
                     ++gk;
                     issued_any = true;
@@ -513,11 +528,6 @@ __global__ void __launch_bounds__(kThreads, 1) swa_prefill_tc_kernel(const __gri
                             if (!k_ready) {
                                 if (!mbar_wait(&kfull[sk], (gk / NK) & 1, wc, 3, j + 1)) { fine = false; break; }
                                 k_ready = true;
-                            }
-                            if (ROPE && !q_band) {  // the band-rotated Q rows
-                                if (!mbar_wait(qfull, nqf & 1, wc, 2, j + 1)) { fine = false; break; }
-                                ++nqf;
-                                q_band = true;
                             }
                             tc_fence_after();
                             issue_qk(tmem + col_s(x), q_addr + x * TILE_BYTES, k_addr0 + sk * TILE_BYTES);
@@ -579,12 +589,28 @@ __global__ void __launch_bounds__(kThreads, 1) swa_prefill_tc_kernel(const __gri
                 const int hc = min(static_cast<int>(T.chi), t - T.pbase);
                 const int b1 = min(hc, P.s - 1 - T.pbase);
                 const int a2 = max(0, t - P.m + 1 - T.pbase);
-                const bool full = (b1 >= BN - 1) || (hc >= BN - 1 && (a2 <= 0 || b1 >= a2 - 1));
-                const bool any_masked = __any_sync(0xFFFFFFFFu, !full);  // warp-uniform: no divergent paths
+                bool full = (b1 >= BN - 1) || (hc >= BN - 1 && (a2 <= 0 || b1 >= a2 - 1));
                 uint32_t mw[4];
 #pragma unroll
                 for (int k = 0; k < 4; ++k)
                     mw[k] = full ? 0xFFFFFFFFu : (range_bits(-32 * k, b1 - 32 * k) | range_bits(a2 - 32 * k, hc - 32 * k));
+                if (BS && !full && t <= qlast) {
+                    // block-sparse: also the global keys of the tile and the row's random key blocks, up to hc
+                    const TileMask gm = gmask_s[b * MAX_TILES + j];
+                    const int* rb = P.bs_rand + static_cast<int64_t>(t / P.bs_block) * P.bs_r;
+                    for (int i = 0; i < P.bs_r; ++i) {
+                        const int kb = rb[i];
+                        if (kb < 0) continue;
+                        const int lo = kb * P.bs_block - T.pbase;
+                        const int hi = min(lo + P.bs_block - 1, hc);
+#pragma unroll
+                        for (int k = 0; k < 4; ++k) mw[k] |= range_bits(lo - 32 * k, hi - 32 * k);
+                    }
+#pragma unroll
+                    for (int k = 0; k < 4; ++k) mw[k] |= gm.w[k] & range_bits(-32 * k, hc - 32 * k);
+                    full = (mw[0] & mw[1] & mw[2] & mw[3]) == 0xFFFFFFFFu;
+                }
+                const bool any_masked = __any_sync(0xFFFFFFFFu, !full);  // warp-uniform: no divergent paths
                 // the whole row of S_x in registers (one TMEM load)
                 float sv[BN];
                 __syncwarp();
@@ -839,11 +865,11 @@ static int sm_count() {
     return cached[dev];
 }
 
-int launch_prefill_bf16_tc_plain(const PrefillArgs &a) {
+static int launch_impl(const PrefillArgs &a, const BlockSparseDev *bs) {
     using namespace tc;
     if (a.d != HD) return fail(SWA_ERR_UNSUPPORTED, "tensor-core prefill needs d = %d", HD);
     if (a.q_sink) return fail(SWA_ERR_INVALID, "the RoPE prefill runs on the sub-tile kernel");
-    if (max_tiles_bound(a.w, a.s) > MAX_TILES)
+    if (!bs && max_tiles_bound(a.w, a.s) > MAX_TILES)
         return fail(SWA_ERR_UNSUPPORTED, "window w=%d needs more than %d key tiles per query tile", a.w, MAX_TILES);
     if ((a.L + BM - 1) / BM * a.BH > 0x7FFFFFFF) return fail(SWA_ERR_UNSUPPORTED, "too many work items");
     if (!encode_tiled_fn()) return fail(SWA_ERR_CUDA, "cuTensorMapEncodeTiled is not available");
@@ -864,7 +890,6 @@ int launch_prefill_bf16_tc_plain(const PrefillArgs &a) {
     }
     else
         okm = okm && encode_rows_map(&p.tm_kc, a.k, L, a.BH, st) && encode_rows_map(&p.tm_vc, a.v, L, a.BH, st);
-    okm = okm && encode_rows_map(&p.tm_qs, a.q, L, a.BH, st);
     if (!okm) return fail(SWA_ERR_INVALID, "cuTensorMapEncodeTiled rejected a tensor (alignment or size)");
     p.o = a.o;
     p.lse = a.lse;
@@ -880,7 +905,15 @@ int launch_prefill_bf16_tc_plain(const PrefillArgs &a) {
     p.n_items = p.n_qpairs * a.BH;
     p.scale_log2 = a.scale * 1.4426950408889634f;
     p.timeout_us = kWaitTimeoutUs;
-    auto *kern = swa_prefill_tc_kernel<false>;
+    if (bs) {
+        p.bs_tiles = static_cast<const Tile *>(bs->tiles);
+        p.bs_gmask = static_cast<const TileMask *>(bs->gmask);
+        p.bs_count = bs->count;
+        p.bs_rand = bs->rand;
+        p.bs_block = bs->block;
+        p.bs_r = bs->r;
+    }
+    auto *kern = bs ? swa_prefill_tc_kernel<true> : swa_prefill_tc_kernel<false>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          static_cast<int>(SMEM_BYTES));
     if (e != cudaSuccess) return fail(SWA_ERR_CUDA, "prefill smem attribute: %s", cudaGetErrorString(e));
@@ -891,6 +924,88 @@ int launch_prefill_bf16_tc_plain(const PrefillArgs &a) {
     kern<<<grid, block, SMEM_BYTES, a.stream>>>(p);
     e = cudaGetLastError();
     if (e != cudaSuccess) return fail(SWA_ERR_CUDA, "prefill launch: %s", cudaGetErrorString(e));
+    return SWA_OK;
+}
+
+int launch_prefill_bf16_tc_plain(const PrefillArgs &a) { return launch_impl(a, nullptr); }
+
+int launch_prefill_bf16_tc_blocksparse(const PrefillArgs &a, const BlockSparseDev &bs) { return launch_impl(a, &bs); }
+
+// Host: the key-tile lists of the block-sparse prefill, one per 256-row query pair, in the kernel's layout.  A
+// pair [q0, qlast] needs the sinks, its band [q0 - m + 1, qlast], every global position <= qlast, and the
+// random key blocks (<= qlast) of every query block it overlaps: these ranges are merged into disjoint runs,
+// so that each key position appears in exactly one tile, and cut into tiles of up to 128 keys.  Per tile the
+// columns holding a global key are listed (the per-row masks of the kernel add them to the band and sinks),
+// and the tile is marked for the query tiles that have some row it can serve.  Returns SWA_OK or an error.
+size_t blocksparse_tile_list_bytes(int64_t L) {
+    const size_t pairs = static_cast<size_t>((L + tc::BM - 1) / tc::BM);
+    return pairs * tc::MAX_TILES * (sizeof(tc::Tile) + sizeof(tc::TileMask));
+}
+
+int blocksparse_build_lists(int64_t L, int w, int s, const int32_t *globals, int n_globals, int block,
+                            const int32_t *rand, int r, void *tiles_out, void *gmask_out, int *count_out) {
+    using namespace tc;
+    const int m = w - s;
+    const int pairs = static_cast<int>((L + BM - 1) / BM);
+    Tile *tiles = static_cast<Tile *>(tiles_out);
+    TileMask *gmask = static_cast<TileMask *>(gmask_out);
+    std::vector<std::pair<int, int>> iv;
+    for (int qp = 0; qp < pairs; ++qp) {
+        const int q0 = qp * BM;
+        const int qlast = static_cast<int>(std::min<int64_t>(q0 + BM, L)) - 1;
+        const int blo = std::max(0, q0 - m + 1);
+        iv.clear();
+        if (s > 0) iv.emplace_back(0, std::min(s, qlast + 1) - 1);
+        iv.emplace_back(blo, qlast);
+        for (int i = 0; i < n_globals && globals[i] <= qlast; ++i) iv.emplace_back(globals[i], globals[i]);
+        for (int qb = q0 / block; qb <= qlast / block; ++qb)
+            for (int i = 0; i < r; ++i) {
+                const int kb = rand[static_cast<int64_t>(qb) * r + i];
+                if (kb < 0 || static_cast<int64_t>(kb) * block > qlast) continue;
+                iv.emplace_back(kb * block, static_cast<int>(std::min<int64_t>(static_cast<int64_t>(kb) * block + block - 1, qlast)));
+            }
+        std::sort(iv.begin(), iv.end());
+        int n = 0;
+        Tile *tl = tiles + static_cast<int64_t>(qp) * MAX_TILES;
+        TileMask *gm = gmask + static_cast<int64_t>(qp) * MAX_TILES;
+        size_t k = 0;
+        while (k < iv.size()) {
+            int a = iv[k].first, b = iv[k].second;
+            for (++k; k < iv.size() && iv[k].first <= b + 1; ++k) b = std::max(b, iv[k].second);
+            for (int p = a; p <= b; p += BN) {
+                if (n >= MAX_TILES)
+                    return fail(SWA_ERR_UNSUPPORTED, "query rows %d..%d need more than %d key tiles", q0, qlast, MAX_TILES);
+                Tile &T = tl[n];
+                T.row0 = p;
+                T.pbase = p;
+                T.chi = static_cast<short>(std::min(b - p, BN - 1));
+                TileMask &G = gm[n];
+                G.w[0] = G.w[1] = G.w[2] = G.w[3] = 0;
+                const int32_t *g0 = std::lower_bound(globals, globals + n_globals, p);
+                for (const int32_t *gp = g0; gp < globals + n_globals && *gp <= p + T.chi; ++gp)
+                    G.w[(*gp - p) >> 5] |= 1u << ((*gp - p) & 31);
+                // query tiles served: band / sink criterion, a global key at or before the tile's last row, or a
+                // random key block of one of its query blocks
+                int f = 0;
+                const int pe = p + T.chi;
+                for (int x = 0; x < 2; ++x) {
+                    const int ra = q0 + x * BH_ROWS, rb = std::min(q0 + x * BH_ROWS + BH_ROWS - 1, qlast);
+                    if (ra > rb || p > rb) continue;
+                    bool need = p < s || pe >= ra - m + 1;
+                    for (const int32_t *gp = g0; !need && gp < globals + n_globals && *gp <= std::min(pe, rb); ++gp) need = true;
+                    for (int qb = ra / block; !need && qb <= rb / block; ++qb)
+                        for (int i = 0; i < r && !need; ++i) {
+                            const int64_t kb = rand[static_cast<int64_t>(qb) * r + i];
+                            need = kb >= 0 && kb * block <= pe && kb * block + block - 1 >= p;
+                        }
+                    if (need) f |= 2 << x;
+                }
+                T.flags = static_cast<short>(f);
+                if (f) ++n;  // a tile no query tile needs is dropped
+            }
+        }
+        count_out[qp] = n;
+    }
     return SWA_OK;
 }
 

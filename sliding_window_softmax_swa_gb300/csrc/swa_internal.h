@@ -49,6 +49,18 @@ int launch_prefill_f32(const PrefillArgs &a);
 // kernel for plain d = 128.
 int launch_prefill_bf16_tc(const PrefillArgs &a);
 int launch_prefill_bf16_tc_plain(const PrefillArgs &a);
+// Block-sparse prefill (bf16, d = 128, pos0 = 0): the host-built tile lists of every 256-row query pair (see
+// blocksparse_build_lists) and the random key blocks of every query block, all in device memory.
+struct BlockSparseDev {
+    const void *tiles, *gmask;
+    const int *count;
+    const int *rand;
+    int block, r;
+};
+int launch_prefill_bf16_tc_blocksparse(const PrefillArgs &a, const BlockSparseDev &bs);
+size_t blocksparse_tile_list_bytes(int64_t L);  // tiles and global-key masks of all query pairs
+int blocksparse_build_lists(int64_t L, int w, int s, const int32_t *globals, int n_globals, int block,
+                            const int32_t *rand, int r, void *tiles_out, void *gmask_out, int *count_out);
 int launch_prefill_bf16_tc_sub(const PrefillArgs &a);
 // Layout passes of the dilated-window prefill: rows of one virtual head (sinks + one residue class), the
 // gather of q, k, v into the virtual heads [BH * r, Lv, d] and the scatter of o (and lse) back.

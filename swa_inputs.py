@@ -97,3 +97,26 @@ def workload_inputs(wl: Workload, device="cpu"):
     """The full input set of a prefill/chunked workload ([B, H, L, d] each), or of a decode workload
     (per-step q/k/v streams [B, H, steps, d])."""
     return prefill_inputs(wl.B, wl.H, wl.L, wl.d, wl.seed, wl.torch_dtype, device, wl.sink_boost)
+
+
+def bigbird_pattern(L: int, block: int, n_global_blocks: int, r: int, seed: int):
+    """A BigBird-style pattern for the block-sparse prefill (fixed-sparsity page, BigBird section: global tokens
+    inside the sequence (ITC) plus r random key blocks per query block).  The global tokens are the first
+    n_global_blocks blocks; each query block qb draws r distinct key blocks uniformly from its causal blocks
+    0..qb (all of them when there are fewer than r), -1 filling unused entries.  The draw is seeded (numpy), and
+    the same arrays go to the library and to the oracle.  Returns (globals list, rand int32 [ceil(L/block), r])."""
+    import numpy as np
+    rng = np.random.default_rng(seed)
+    nqb = (L + block - 1) // block
+    globals_ = list(range(min(L, n_global_blocks * block)))
+    rand = np.full((nqb, r), -1, dtype=np.int32)
+    for qb in range(nqb):
+        k = min(r, qb + 1)
+        if k > 0:
+            rand[qb, :k] = np.sort(rng.choice(qb + 1, size=k, replace=False))
+    return globals_, rand
+
+
+def rand_blocks_dict(rand):
+    """The random key blocks as {query block: [key blocks]} (the oracle's form), -1 entries dropped."""
+    return {qb: [int(x) for x in row if x >= 0] for qb, row in enumerate(rand)}
