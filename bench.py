@@ -277,9 +277,48 @@ def dilated_flops(B, H, L, d, w, s, r):
     return 4.0 * B * H * d * pairs
 
 
-def prefill_leg(swa, wl, steps, warmup, world, rank, clocks, e2e=False, rope=False, dilation=0, window=None):
+def blocksparse_pairs(L, w, s, globals_, block, rand) -> int:
+    """Sum over the rows t of |K(t)| for the block-sparse key sets (causal union of sinks, window, global
+    tokens, the random key blocks of t's query block; a global row sees all t + 1 earlier keys), counted as a
+    union of position intervals per row."""
+    m = w - s
+    g = sorted(int(x) for x in globals_)
+    runs = []  # global tokens as runs of consecutive positions
+    for x in g:
+        if runs and runs[-1][1] == x - 1:
+            runs[-1][1] = x
+        else:
+            runs.append([x, x])
+    gset = set(g)
+    total = 0
+    for t in range(L):
+        if t in gset:
+            total += t + 1
+            continue
+        iv = [(0, min(s, t + 1) - 1), (max(0, t - m + 1), t)]
+        iv += [(a, min(b, t)) for a, b in runs if a <= t]
+        if rand is not None:
+            iv += [(kb * block, min(kb * block + block - 1, t)) for kb in rand[t // block] if 0 <= kb * block <= t]
+        iv.sort()
+        hi = -1
+        for a, b in iv:
+            if b < a:
+                continue
+            if a > hi:
+                total += b - a + 1
+                hi = b
+            elif b > hi:
+                total += b - hi
+                hi = b
+    return total
+
+
+def prefill_leg(swa, wl, steps, warmup, world, rank, clocks, e2e=False, rope=False, dilation=0, window=None,
+                blocksparse=None):
     """Prefill steps; with ``rope`` the RoPE prefill at the positions inside the cache (base 10000): a
-    rotation pass over q and k, then the tensor-core prefill on the rotated rows (2 launches a step)."""
+    rotation pass over q and k, then the tensor-core prefill on the rotated rows (2 launches a step);
+    ``blocksparse`` = (globals, block, rand): the block-sparse prefill with that pattern."""
+    import numpy as np
     import torch
     import swa_inputs
     B, H, L, d, w, s = wl.B, wl.H, wl.L, wl.d, wl.w, wl.s
@@ -288,7 +327,16 @@ def prefill_leg(swa, wl, steps, warmup, world, rank, clocks, e2e=False, rope=Fal
     lib = swa.lib()
     stream = torch.cuda.current_stream().cuda_stream
     dt = 0 if wl.dtype == "bf16" else 1
-    if dilation:
+    if blocksparse is not None:
+        globals_, block, rand = blocksparse
+        g = np.ascontiguousarray(globals_, dtype=np.int32)
+        rb = np.ascontiguousarray(rand, dtype=np.int32)
+        nws = lib.swa_sink_prefill_blocksparse_workspace_size(L, g.size, block, rb.shape[1])
+        ws = torch.empty(nws, dtype=torch.uint8, device="cuda")
+        args = (q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(), None, B, H, L, d, w, s, wl.scale,
+                g.ctypes.data, g.size, block, rb.ctypes.data, rb.shape[1], ws.data_ptr(), nws, dt, stream)
+        call = lib.swa_sink_prefill_blocksparse
+    elif dilation:
         nws = lib.swa_sink_prefill_dilated_workspace_size(B, H, L, d, s, dilation, dt)
         ws = torch.empty(nws, dtype=torch.uint8, device="cuda")
         args = (q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(), None, B, H, L, d, w, s, dilation, wl.scale,
@@ -312,9 +360,14 @@ def prefill_leg(swa, wl, steps, warmup, world, rank, clocks, e2e=False, rope=Fal
 
     t = time_loop(step, steps, warmup, world, clocks, window)
     _check_status(swa)
-    flops = dilated_flops(B, H, L, d, w, s, dilation) if dilation else banded_flops(B, H, L, d, w)
+    if blocksparse is not None:
+        flops = 4.0 * B * H * d * blocksparse_pairs(L, w, s, globals_, block, rand)
+        launches = 2 if len(globals_) else 1
+    else:
+        flops = dilated_flops(B, H, L, d, w, s, dilation) if dilation else banded_flops(B, H, L, d, w)
+        launches = 3 if dilation else 2 if rope else 1
     res = {"flops_per_step": flops, "seconds": t, "steps": steps, "tflops": flops * steps / t / 1e12,
-           "ms_per_step": t / steps * 1e3, "launches": (3 if dilation else 2 if rope else 1) * steps}
+           "ms_per_step": t / steps * 1e3, "launches": launches * steps}
     if e2e:
         # the same prefill through the public host-buffer call: every step copies q/k/v from pinned host
         # memory and o back (the library pipelines the copies against the compute over row groups)
@@ -544,7 +597,7 @@ def main():
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--primary-only", action="store_true", help="only the primary prefill leg")
     ap.add_argument("--legs", default="primary,mistral,chunked,decode,decode_rope,prefill_rope,chunked_rope,dilated,"
-                                      "decode_dilated",
+                                      "decode_dilated,blocksparse",
                     help="comma list of legs to run (profiling runs pick one)")
     ap.add_argument("--decode-steps", type=int, default=None, help="shorter decode stream (profiling only)")
     args = ap.parse_args()
@@ -606,6 +659,15 @@ def main():
             "ms_per_step": r["ms_per_step"], "frac_of_bf16_peak": r["tflops"] / peaks["bf16_tflops"],
             "what": "dilated window with sinks, r = 2 (FLOPs over the dilated key sets): gather into virtual "
                     "heads + tensor-core prefill + scatter", "launches_per_step": 3}
+    if "blocksparse" in legs:
+        globals_, rand = swa_inputs.bigbird_pattern(wl.L, 64, 2, 3, seed=2024)
+        r = prefill_leg(swa, wl, max(3, args.steps // 2), 3, world, rank, clocks, blocksparse=(globals_, 64, rand))
+        secondary["prefill_blocksparse_llama7b_L8192_w1024_s4_g128_b64_r3"] = {
+            "metric": METRIC, "value": aggregate_rate(r["tflops"], world, 1.0), "unit": "TFLOP/s",
+            "ms_per_step": r["ms_per_step"], "frac_of_bf16_peak": r["tflops"] / peaks["bf16_tflops"],
+            "what": "block-sparse: window + sinks + 128 global tokens + 3 random key blocks of 64 per query block "
+                    "(FLOPs over those key sets): host tile lists + their upload, tensor-core prefill, global rows",
+            "launches_per_step": r["launches"] // max(3, args.steps // 2)}
     if "chunked_rope" in legs:
         cw = swa_inputs.WORKLOADS["chunked_mistral_L131072_w4096_s4_C4096"]
         r = chunked_leg(swa, cw, 3, 1, world, rank, clocks, rope=True)

@@ -65,3 +65,21 @@ def test_dilated_flop_accounting():
         pairs = sum(oracle.is_key_dilated(t, i, w, s, r) for t in range(L) for i in range(t + 1))
         assert bench.dilated_flops(2, 3, L, 16, w, s, r) == 4.0 * 2 * 3 * 16 * pairs
     assert bench.dilated_flops(1, 2, 50, 128, 10, 2, 1) == bench.banded_flops(1, 2, 50, 128, 10)
+
+
+def test_blocksparse_pairs_counts_the_oracle_key_sets():
+    import bench
+    import oracle
+    import swa_inputs
+    for L, w, s, ng, block, r, seed in [(90, 12, 2, 1, 8, 2, 1), (130, 40, 0, 0, 16, 3, 2), (75, 9, 3, 2, 5, 1, 3)]:
+        globals_, rand = swa_inputs.bigbird_pattern(L, block, ng, r, seed)
+        rd = swa_inputs.rand_blocks_dict(rand)
+        g = set(globals_)
+        want = sum(1 for t in range(L) for i in range(t + 1) if oracle.is_key_blocksparse(t, i, w, s, g, block, rd))
+        assert bench.blocksparse_pairs(L, w, s, globals_, block, rand) == want
+    # scattered globals, no random blocks
+    g = [3, 4, 20, 51]
+    want = sum(1 for t in range(60) for i in range(t + 1) if oracle.is_key_blocksparse(t, i, 10, 2, set(g), 4, None))
+    assert bench.blocksparse_pairs(60, 10, 2, g, 4, None) == want
+    # no pattern: the banded count
+    assert bench.blocksparse_pairs(300, 50, 4, [], 16, None) == bench.banded_pairs(300, 50)
