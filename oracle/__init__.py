@@ -19,7 +19,8 @@ attention) and eq attn-fixed-softmax-sink of "滑窗与固定稀疏" (row normal
 ``rope``, ``decode_rope`` and ``prefill_rope`` state the streaming decode and the prefill with
 positions re-assigned inside the cache and rotary embedding (StreamingLLM section of "滑窗与固定稀疏").
 ``hedgehog`` and ``hybrid_linear`` state the SWA + linear-attention hybrid (a stated reading of the
-combination; an oracle ahead of its GPU path).
+combination); ``hybrid_linear_rows`` evaluates it at selected rows with the state summed in closed form
+(pinned against the recurrence), for sampled rows of large cases.
 ``is_key_blocksparse`` and ``prefill_blocksparse`` state the BigBird-style union (window, global
 tokens inside the sequence, given random key blocks) in causal form with sinks: an oracle ahead of its GPU
 path.
@@ -336,6 +337,35 @@ def hybrid_linear(q, k, v, w: int, s: int, scale: float, wf):
         num = np.einsum("hn,hnd->hd", e, v[:, members]) + np.einsum("hi,hij->hj", pq[:, t], S)
         den = e.sum(axis=1) + np.einsum("hi,hi->h", pq[:, t], z)
         o[:, t] = num / den[:, None]
+    return o
+
+
+def hybrid_linear_rows(q, k, v, w: int, s: int, scale: float, wf, rows):
+    """``hybrid_linear`` at selected rows, with the state in closed form: S_t = sum_{i=s}^{t-m} phi(k_i)^T v_i,
+    z_t = sum_{i=s}^{t-m} phi(k_i)^T (the page's recurrence summed out), accumulated between consecutive rows
+    in increasing order.  q, k, v: [nh, L, d]; returns o [nh, len(rows), d] (fp64) in the order of ``rows``."""
+    q, k, v = _f64(q), _f64(k), _f64(v)
+    nh, L, d = q.shape
+    m = w - s
+    pk = hedgehog(k, wf)
+    order = sorted(range(len(rows)), key=lambda j: int(rows[j]))
+    S = np.zeros((nh, d, d))
+    z = np.zeros((nh, d))
+    upto = s  # keys s .. upto-1 are in the state
+    o = np.empty((nh, len(rows), d))
+    for j in order:
+        t = int(rows[j])
+        end = t - m + 1  # keys s .. t-m have left the window
+        if end > upto:
+            S += np.matmul(pk[:, upto:end].transpose(0, 2, 1), v[:, upto:end])
+            z += pk[:, upto:end].sum(axis=1)
+            upto = end
+        members = np.array([i for i in range(t + 1) if is_key(t, i, w, s)], dtype=np.int64)
+        e = np.exp(np.einsum("hd,hnd->hn", q[:, t], k[:, members]) * scale)
+        pq = hedgehog(q[:, t], wf)
+        num = np.einsum("hn,hnd->hd", e, v[:, members]) + np.einsum("hi,hij->hj", pq, S)
+        den = e.sum(axis=1) + np.einsum("hi,hi->h", pq, z)
+        o[:, j] = num / den[:, None]
     return o
 
 

@@ -120,3 +120,11 @@ def bigbird_pattern(L: int, block: int, n_global_blocks: int, r: int, seed: int)
 def rand_blocks_dict(rand):
     """The random key blocks as {query block: [key blocks]} (the oracle's form), -1 entries dropped."""
     return {qb: [int(x) for x in row if x >= 0] for qb, row in enumerate(rand)}
+
+
+def hedgehog_weights(d: int, seed: int, dtype=torch.bfloat16, device="cpu") -> torch.Tensor:
+    """A stand-in for the learned Hedgehog projection wf [d, d/2] (no trained weights are available): iid
+    N(0, 1/d) entries, so that f(x) = x wf has unit variance for x ~ N(0, I)."""
+    g = _gen(device, seed, 7)
+    x = torch.randn((d, d // 2), generator=g, device=device, dtype=torch.float32) / float(d) ** 0.5
+    return x.to(dtype)

@@ -661,3 +661,14 @@ def test_hybrid_with_a_flat_feature_map_in_closed_form():
         e = np.exp(0.4 * q[0, t] @ k[0, K].T)
         want = (e @ v[0, K] + d * v[0, R].sum(axis=0)) / (e.sum() + d * len(R))
         np.testing.assert_allclose(o[0, t], want, atol=1e-12)
+
+
+def test_hybrid_rows_equal_the_running_state():
+    # the closed-form state at selected rows (any order, repeats) against the page's recurrence
+    rng = np.random.default_rng(30)
+    q, k, v = (rng.standard_normal((2, 50, 8)) for _ in range(3))
+    wf = rng.standard_normal((8, 4)) * 0.25
+    for w, s in [(7, 2), (5, 0), (12, 4)]:
+        full = oracle.hybrid_linear(q, k, v, w, s, 0.3, wf)
+        rows = [49, 0, 13, 13, 6, 30, 7]
+        np.testing.assert_allclose(oracle.hybrid_linear_rows(q, k, v, w, s, 0.3, wf, rows), full[:, rows], atol=1e-10)
