@@ -196,6 +196,49 @@ int swa_sink_prefill_blocksparse(const void *q, const void *k, const void *v, vo
 size_t swa_sink_prefill_blocksparse_workspace_size(int64_t L, int n_globals, int block, int r);
 
 /*
+ * swa_hybrid_prefill -- sliding-window softmax attention with sinks plus a linear-attention branch for the
+ * keys that have left the window: the SWA / linear-attention hybrid of the hyper.ai summary of arXiv
+ * 2608.28444 (linear-attention section: running state s_t = s_{t-1} + phi(k_t)^T v_t, z_t = z_{t-1} + phi(k_t)^T,
+ * Hedgehog feature map phi(x) = (exp(x wf), exp(-x wf))).  Both branches share one normaliser (the LoLCATs
+ * reading that summary discusses):
+ *     o_t = (sum_{i in K(t)} e^{x_i} v_i + phi(q_t) S_t) / (sum_{i in K(t)} e^{x_i} + phi(q_t) z_t)
+ * with x_i = scale q_t.k_i, K(t) the sinks + window of swa_sink_prefill, and S_t = sum phi(k_i)^T v_i,
+ * z_t = sum phi(k_i)^T over the keys s <= i <= t - (w - s) that have left the window (the sinks never leave).
+ *
+ *   q, k, v, o : [B, H, L, d] bf16, d = 128, 16-byte aligned.
+ *   wf        : [d, d/2] bf16 row-major, the feature projection (f(x) = x wf); phi has d components.
+ *   state_s, state_z : NULL, or fp32 [B, H, d, d] and [B, H, d] (16-byte aligned) that receive S and z after
+ *             row L-1 (the state swa_hybrid_decode_step continues from at t = L).
+ *   workspace : device scratch of swa_hybrid_prefill_workspace_size(B, H, L, d) bytes, 256-byte aligned
+ *             (the SWA branch's lse and the linear branch's per-chunk states).
+ * Launches the SWA prefill, the chunk states, their scan, the linear branch with the combination (in place
+ * over o) and, with state_s, the final state; asynchronous on `stream`, no allocation, capturable.
+ */
+int swa_hybrid_prefill(const void *q, const void *k, const void *v, const void *wf, void *o, float *state_s,
+                       float *state_z, int B, int H, int64_t L, int d, int w, int s, float scale, void *workspace,
+                       size_t workspace_bytes, int dtype, void *stream);
+size_t swa_hybrid_prefill_workspace_size(int B, int H, int64_t L, int d);
+
+/*
+ * swa_hybrid_decode_step -- one streaming-decode step of the hybrid of swa_hybrid_prefill at position t.
+ * In order: the key that leaves the window at this step (position t - (w - s), when >= s) is read from its
+ * rolling-cache slot and folded into the state (S += phi(k)^T v, z += phi(k)^T); k_new, v_new (the key and
+ * value of position t) are written into that slot (kv_rolling_write's slot rule); the SWA decode step attends
+ * the cache; the result is combined with phi(q_t) S_t and phi(q_t) z_t.
+ *
+ *   q, k_new, v_new : [B, H, d] bf16 (q 16-byte aligned); k_cache, v_cache : [B, H, w, d] bf16, updated.
+ *   state_s, state_z : fp32 [B, H, d, d] and [B, H, d], updated in place (zeros before position 0, or the
+ *             state swa_hybrid_prefill returned).
+ *   wf        : [d, d/2] bf16 as swa_hybrid_prefill.   o : [B, H, d] bf16.
+ *   workspace : device scratch of swa_hybrid_decode_workspace_size(B, H, d, w) bytes, 256-byte aligned.
+ * bf16, d = 128.  Three launches on `stream`, no allocation, capturable.  Other errors as swa_sink_decode_step.
+ */
+int swa_hybrid_decode_step(const void *q, const void *k_new, const void *v_new, void *k_cache, void *v_cache,
+                           float *state_s, float *state_z, const void *wf, void *o, int B, int H, int d, int w, int s,
+                           int64_t t, float scale, void *workspace, size_t workspace_bytes, int dtype, void *stream);
+size_t swa_hybrid_decode_workspace_size(int B, int H, int d, int w);
+
+/*
  * swa_sink_prefill_chunked -- the chunk-based prefill of "滑窗与固定稀疏" (rolling-buffer section):
  * the L positions are processed in chunks of `chunk` rows; chunk c attends the rolling cache as it was
  * before the chunk plus its own keys (swa_sink_prefill with pos0 = c*chunk), then its keys/values are

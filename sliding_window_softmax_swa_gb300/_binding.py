@@ -58,6 +58,11 @@ SIGNATURES = {
     "swa_sink_prefill_blocksparse": (_i, [_vp, _vp, _vp, _vp, _vp, _i, _i, _i64, _i, _i, _i, _f, _vp, _i, _i, _vp, _i,
                                           _vp, _sz, _i, _vp]),
     "swa_sink_prefill_blocksparse_workspace_size": (_sz, [_i64, _i, _i, _i]),
+    "swa_hybrid_prefill": (_i, [_vp, _vp, _vp, _vp, _vp, _vp, _vp, _i, _i, _i64, _i, _i, _i, _f, _vp, _sz, _i, _vp]),
+    "swa_hybrid_prefill_workspace_size": (_sz, [_i, _i, _i64, _i]),
+    "swa_hybrid_decode_step": (_i, [_vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _i, _i64, _f, _vp, _sz,
+                                    _i, _vp]),
+    "swa_hybrid_decode_workspace_size": (_sz, [_i, _i, _i, _i]),
 }
 
 _lib = None
@@ -277,6 +282,45 @@ def swa_sink_prefill_blocksparse(q, k, v, w: int, s: int, globals_=(), block: in
         _ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), B, H, L, d, w, s, scale,
         g.ctypes.data if g.size else None, g.size, block, rb.ctypes.data if r else None, r, _ptr(workspace),
         workspace.numel() * workspace.element_size(), _dtype_code(q), _stream(stream)))
+    return o
+
+
+def swa_hybrid_prefill(q, k, v, wf, w: int, s: int, scale: float | None = None, o=None, state_s=None,
+                       state_z=None, workspace=None, stream=None):
+    """SWA with sinks + a Hedgehog linear-attention branch over the keys that left the window (one shared
+    normaliser).  q, k, v [B, H, L, 128] bf16, wf [128, 64] bf16.  With state_s/state_z (fp32 [B, H, 128, 128]
+    and [B, H, 128]) the state after the last row is written there."""
+    B, H, L, d = q.shape
+    assert k.shape == q.shape and v.shape == q.shape
+    if o is None:
+        o = torch.empty_like(q)
+    nws = lib().swa_hybrid_prefill_workspace_size(B, H, L, d)
+    if workspace is None:
+        workspace = torch.empty(max(nws, 256), dtype=torch.uint8, device=q.device)
+    _dev(q, k, v, o, wf, state_s, state_z, workspace)
+    scale = (1.0 / d ** 0.5) if scale is None else scale
+    _check("swa_hybrid_prefill", lib().swa_hybrid_prefill(
+        _ptr(q), _ptr(k), _ptr(v), _ptr(wf), _ptr(o), _ptr(state_s), _ptr(state_z), B, H, L, d, w, s, scale,
+        _ptr(workspace), workspace.numel() * workspace.element_size(), _dtype_code(q), _stream(stream)))
+    return o
+
+
+def swa_hybrid_decode_step(q, k_new, v_new, k_cache, v_cache, state_s, state_z, wf, w: int, s: int, t: int,
+                           scale: float | None = None, o=None, workspace=None, stream=None):
+    """One decode step of the hybrid at position t: fold the evicted key into the state, write k_new/v_new
+    into the rolling cache, attend, combine.  q, k_new, v_new [B, H, 128] bf16; caches [B, H, w, 128]."""
+    B, H, d = q.shape
+    if o is None:
+        o = torch.empty_like(q)
+    nws = lib().swa_hybrid_decode_workspace_size(B, H, d, w)
+    if workspace is None:
+        workspace = torch.empty(max(nws, 256), dtype=torch.uint8, device=q.device)
+    _dev(q, k_new, v_new, k_cache, v_cache, state_s, state_z, wf, o, workspace)
+    scale = (1.0 / d ** 0.5) if scale is None else scale
+    _check("swa_hybrid_decode_step", lib().swa_hybrid_decode_step(
+        _ptr(q), _ptr(k_new), _ptr(v_new), _ptr(k_cache), _ptr(v_cache), _ptr(state_s), _ptr(state_z), _ptr(wf),
+        _ptr(o), B, H, d, w, s, t, scale, _ptr(workspace), workspace.numel() * workspace.element_size(),
+        _dtype_code(q), _stream(stream)))
     return o
 
 

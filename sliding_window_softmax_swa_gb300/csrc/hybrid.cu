@@ -1,0 +1,634 @@
+// hybrid.cu -- sliding-window softmax attention with sinks plus a linear-attention branch for the keys that
+// have left the window (the SWA / linear-attention hybrid of the hyper.ai summary of arXiv 2608.28444, its
+// linear-attention section: running state s_t = s_{t-1} + phi(k_t)^T v_t, z_t = z_{t-1} + phi(k_t)^T, and the
+// Hedgehog feature map phi(x) = (exp(f(x)), exp(-f(x))), f(x) = x wf with wf a d x d/2 projection).  The two
+// branches share one normaliser (the LoLCATs reading that summary discusses):
+//     o_t = (sum_{i in K(t)} e^{x_i} v_i + phi(q_t) S_t) / (sum_{i in K(t)} e^{x_i} + phi(q_t) z_t),
+// K(t) the sinks + window, S_t, z_t the sums over the keys s <= i <= t - m that left it (the sinks never do).
+// With the SWA prefill's output o' and lse the first terms are o' e^{lse} and e^{lse}, so
+//     o_t = (o'_t + phi(q_t) S_t e^{-lse_t}) / (1 + phi(q_t) z_t e^{-lse_t}).
+//
+// Prefill (bf16, d = 128), all contractions on the tensor cores (tcgen05, operands in 128-byte-swizzled
+// shared memory, fp32 accumulators in TMEM), with W2 = [wf^T ; -wf^T] (128 x d) so that one product gives
+// both halves of f and phi is exp of it:
+//   1. chunk states, per (head, key chunk j of 128 keys): f(K_j)^T = W2 K_j^T, phi(K_j)^T = exp(.) with the
+//      sinks and the keys past the end zeroed, D_j = phi(K_j)^T V_j (d x d) and z_j = phi(K_j)^T 1;
+//   2. an exclusive scan over j in place: P_j = sum_{j' < j} D_j' (the state of the keys before chunk j);
+//   3. per (head, query tile of 128 rows at a): J = floor((a - m + 1) / 128) (every key below 128 J has left
+//      the window of every row of the tile), then
+//          num = phi(Q) P_J + sum over the <= 2 key tiles from 128 J: (phi(Q) phi(K)^T masked to i <= t - m,
+//                i >= s) V,   den = phi(Q) z_J + the masked row sums,
+//      and the combination above, in place over the SWA prefill's output.
+// Decode: per (b, h) one pass over the state: fold the key that leaves the window at this step (it sits in
+// the rolling slot the new key goes to) into S and z, write the new key and value into that slot, and form
+// phi(q) S and phi(q) z; the SWA decode step with lse follows, then the combination.
+#include <cuda_bf16.h>
+#include <math.h>
+
+#include "../../include/swa_sink.h"
+#include "swa_device.cuh"
+#include "swa_internal.h"
+
+namespace swa {
+namespace hy {
+
+constexpr int D = 128;                      // head dimension (and feature dimension of phi)
+constexpr int C = 128;                      // keys per chunk / rows per query tile
+constexpr uint32_t HALF = 128 * 128;        // one 64-column half of a [128 x 128] bf16 tile
+constexpr uint32_t TILE = 2 * HALF;
+constexpr int STATE_FLOATS = D * D + D;     // D_j / P_j (row-major [feature][column]) then z_j
+constexpr uint32_t IDESC_KK = idesc_bf16_f32(128, 128, false, false);  // A K-major, B K-major (A B^T)
+constexpr uint32_t IDESC_KM = idesc_bf16_f32(128, 128, false, true);   // A K-major, B MN-major (A B)
+constexpr float LOG2E = 1.4426950408889634f;
+
+// D (+)= A B^T: A and B [128 x 128] tiles whose rows are M (resp. N) and whose columns are K.
+__device__ __forceinline__ void mma_abt(uint32_t d, uint32_t a, uint32_t b, bool acc) {
+#pragma unroll
+    for (int kk = 0; kk < 8; ++kk) {
+        const uint32_t off = (kk >> 2) * HALF + (kk & 3) * 32;
+        umma_ss(d, sdesc_sw128(a + off, 16, 1024), sdesc_sw128(b + off, 16, 1024), IDESC_KK, (acc || kk) ? 1u : 0u);
+    }
+}
+// D (+)= A B: A [128 x 128] with rows M and columns K, B [128 x 128] with rows K and columns N.
+__device__ __forceinline__ void mma_ab(uint32_t d, uint32_t a, uint32_t b, bool acc) {
+#pragma unroll
+    for (int kk = 0; kk < 8; ++kk) {
+        const uint32_t a_off = (kk >> 2) * HALF + (kk & 3) * 32;
+        umma_ss(d, sdesc_sw128(a + a_off, 16, 1024), sdesc_sw128(b + kk * 2048, HALF, 1024), IDESC_KM,
+                (acc || kk) ? 1u : 0u);
+    }
+}
+
+// Row r, columns c0..c0+31 of a [128 x 128] bf16 tile in the swizzled two-half layout, from 32 floats.
+__device__ __forceinline__ void st_row32(uint32_t tile, int r, int c0, const float (&x)[32]) {
+#pragma unroll
+    for (int g = 0; g < 4; ++g) {
+        const int c = c0 + 8 * g;
+        st_shared_v4(tile + (c >> 6) * HALF + sw128_offset(r, c & 63), pack_bf16x2(x[8 * g], x[8 * g + 1]),
+                     pack_bf16x2(x[8 * g + 2], x[8 * g + 3]), pack_bf16x2(x[8 * g + 4], x[8 * g + 5]),
+                     pack_bf16x2(x[8 * g + 6], x[8 * g + 7]));
+    }
+}
+
+// W2 = [wf^T ; -wf^T] into a tile (row j = feature j, columns = the d input coordinates); 128 threads.
+// wf: [d][d/2] bf16 row-major (f = x wf).  Negating a bf16 is exact.
+__device__ __forceinline__ void stage_w2(uint32_t tile, const __nv_bfloat16 *__restrict__ wf) {
+    const int j = threadIdx.x;
+    const int col = j & 63;
+    const uint16_t sign = j >= 64 ? 0x8000u : 0u;
+    for (int c0 = 0; c0 < D; c0 += 8) {
+        uint32_t u[4];
+#pragma unroll
+        for (int h = 0; h < 4; ++h) {
+            const uint16_t lo = __bfloat16_as_ushort(wf[(c0 + 2 * h) * (D / 2) + col]) ^ sign;
+            const uint16_t hi = __bfloat16_as_ushort(wf[(c0 + 2 * h + 1) * (D / 2) + col]) ^ sign;
+            u[h] = static_cast<uint32_t>(lo) | (static_cast<uint32_t>(hi) << 16);
+        }
+        st_shared_v4(tile + (c0 >> 6) * HALF + sw128_offset(j, c0 & 63), u[0], u[1], u[2], u[3]);
+    }
+}
+
+__device__ __forceinline__ uint32_t lane_addr(uint32_t tmem, int col) {
+    return tmem + (static_cast<uint32_t>((threadIdx.x >> 5) * 32) << 16) + col;
+}
+
+// Shared state of one CTA: barriers, TMEM base, abort flag.
+struct Ctl {
+    uint64_t load_bar, mma_bar;
+    uint32_t tmem;
+    int abort_flag;
+};
+
+// TMA of a [128 rows x 128] bf16 tile (two 64-column boxes) of (bh, row0); one thread.
+__device__ __forceinline__ void load_tile(uint8_t *dst, const CUtensorMap *m, uint64_t *bar, int row0, int bh) {
+    tma_load_3d(dst, m, bar, 0, row0, bh);
+    tma_load_3d(dst + HALF, m, bar, 64, row0, bh);
+}
+
+// Wait for the MMAs committed to mma_bar (phase `ph`) on every thread; false once any wait of the CTA gave up.
+__device__ __forceinline__ bool wait_mma(Ctl *ctl, int ph, const WaitCtl &wc, unsigned site) {
+    const bool ok = __syncthreads_and(mbar_wait(&ctl->mma_bar, ph & 1, wc, site));
+    tc_fence_after();
+    return ok;
+}
+
+// Issue (thread 0) after shared-memory operand writes by all threads.
+__device__ __forceinline__ void operands_written() {
+    fence_proxy_async_smem();
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+}
+
+// ---- 1. chunk states ------------------------------------------------------------------------------
+// grid (chunks, BH), 128 threads.  Key chunk j: keys j*C .. j*C + C - 1; a key counts when s <= key < key_end.
+// out: [BH][chunks][STATE_FLOATS].  Final mode (prefix != nullptr): one chunk per head (index chunk0); the
+// prefix state of that chunk (from the scanned states) is added and the sum goes to out_s [BH][d][d] and
+// out_z [BH][d].
+__global__ void __launch_bounds__(128, 1) chunk_state_kernel(const __grid_constant__ CUtensorMap mk,
+                                                             const __grid_constant__ CUtensorMap mv,
+                                                             const __nv_bfloat16 *__restrict__ wf, float *out,
+                                                             const float *__restrict__ prefix, float *out_s,
+                                                             float *out_z, int chunk0, int nchunks, int s,
+                                                             int64_t key_end, DeviceStatus *status) {
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t *sm = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    uint8_t *Tw = sm, *Tk = sm + TILE, *Tv = sm + 2 * TILE;
+    Ctl *ctl = reinterpret_cast<Ctl *>(sm + 3 * TILE);
+    const int j = chunk0 + static_cast<int>(blockIdx.x), bh = blockIdx.y, r = threadIdx.x;
+    if (r == 0) {
+        ctl->abort_flag = 0;
+        mbar_init(&ctl->load_bar, 1);
+        mbar_init(&ctl->mma_bar, 1);
+        mbar_init_fence();
+    }
+    if (r < 32) {
+        tmem_alloc(&ctl->tmem, 256);
+        tmem_relinquish();
+    }
+    stage_w2(smem_u32(Tw), wf);
+    operands_written();
+    const uint32_t tmem = ctl->tmem;
+    const WaitCtl wc{smem_u32(&ctl->abort_flag), kWaitTimeoutUs, status};
+    if (r == 0) {
+        tma_prefetch_desc(&mk);
+        tma_prefetch_desc(&mv);
+        mbar_arrive_expect_tx(&ctl->load_bar, 2 * TILE);
+        load_tile(Tk, &mk, &ctl->load_bar, j * C, bh);
+        load_tile(Tv, &mv, &ctl->load_bar, j * C, bh);
+        if (mbar_wait(&ctl->load_bar, 0, wc, 40)) {
+            tc_fence_after();
+            mma_abt(tmem, smem_u32(Tw), smem_u32(Tk), false);  // f(K)^T: [feature][key]
+        } else {
+            mbar_wait_drain(&ctl->load_bar, 0);
+        }
+        umma_commit(&ctl->mma_bar);
+    }
+    bool fine = wait_mma(ctl, 0, wc, 41);
+    float z = 0.f;
+    if (fine) {
+        // phi(K)^T row r (feature r) over the 128 keys; uncounted keys are zero
+        const int64_t k0 = static_cast<int64_t>(j) * C;
+        for (int c0 = 0; c0 < C; c0 += 32) {
+            float x[32];
+            tmem_ld32(lane_addr(tmem, c0), x);
+#pragma unroll
+            for (int i = 0; i < 32; ++i) {
+                const int64_t key = k0 + c0 + i;
+                x[i] = (key >= s && key < key_end) ? exp2f(x[i] * LOG2E) : 0.f;
+                z += x[i];
+            }
+            st_row32(smem_u32(Tk), r, c0, x);
+        }
+    }
+    operands_written();
+    if (r == 0) {
+        if (fine) mma_ab(tmem + 128, smem_u32(Tk), smem_u32(Tv), false);  // phi(K)^T V: [feature][column]
+        umma_commit(&ctl->mma_bar);
+    }
+    fine = wait_mma(ctl, 1, wc, 42) && fine;
+    if (fine) {
+        const bool fin = prefix != nullptr;
+        float *dst = fin ? out_s + static_cast<int64_t>(bh) * D * D
+                         : out + (static_cast<int64_t>(bh) * nchunks + j) * STATE_FLOATS;
+        const float *pre = fin ? prefix + (static_cast<int64_t>(bh) * nchunks + j) * STATE_FLOATS : nullptr;
+        for (int c0 = 0; c0 < D; c0 += 32) {
+            float x[32];
+            tmem_ld32(lane_addr(tmem, 128 + c0), x);
+            if (fin) {
+#pragma unroll
+                for (int i = 0; i < 32; ++i) x[i] += pre[r * D + c0 + i];
+            }
+            float4 *p4 = reinterpret_cast<float4 *>(dst + r * D + c0);
+#pragma unroll
+            for (int i = 0; i < 8; ++i) p4[i] = make_float4(x[4 * i], x[4 * i + 1], x[4 * i + 2], x[4 * i + 3]);
+        }
+        if (fin)
+            out_z[static_cast<int64_t>(bh) * D + r] = z + pre[D * D + r];
+        else
+            dst[D * D + r] = z;
+    }
+    tc_fence_before();
+    __syncthreads();
+    if (r < 32) {
+        tc_fence_after();
+        tmem_dealloc(tmem, 256);
+    }
+}
+
+// ---- 2. exclusive scan over the chunks, in place ------------------------------------------------------
+__global__ void __launch_bounds__(256) scan_kernel(float *st, int nchunks, int64_t total) {
+    const int64_t e = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
+    if (e >= total) return;
+    const int64_t bh = e / STATE_FLOATS, k = e % STATE_FLOATS;
+    float *p = st + bh * nchunks * STATE_FLOATS + k;
+    float run = 0.f;
+    for (int j = 0; j < nchunks; ++j) {
+        const float x = p[static_cast<int64_t>(j) * STATE_FLOATS];
+        p[static_cast<int64_t>(j) * STATE_FLOATS] = run;
+        run += x;
+    }
+}
+
+// ---- 3. linear branch + combination ----------------------------------------------------------------------
+// grid (query tiles, BH), 128 threads; thread r owns query row a + r (and feature r where a tile is indexed by
+// feature).  o holds the SWA prefill's output on entry and the hybrid output on exit; lse is the SWA prefill's.
+__global__ void __launch_bounds__(128, 1) linear_kernel(const __grid_constant__ CUtensorMap mq,
+                                                        const __grid_constant__ CUtensorMap mk,
+                                                        const __grid_constant__ CUtensorMap mv,
+                                                        const __nv_bfloat16 *__restrict__ wf,
+                                                        const float *__restrict__ pstate, __nv_bfloat16 *o,
+                                                        const float *__restrict__ lse, int64_t L, int m, int s,
+                                                        int nchunks, DeviceStatus *status) {
+    const int64_t a = static_cast<int64_t>(blockIdx.x) * C;
+    const int bh = blockIdx.y, r = threadIdx.x;
+    const int64_t last = (a + C < L ? a + C : L) - 1;
+    if (last - m < s) return;  // no row of the tile has a key outside its window yet
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t *sm = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    uint8_t *Tq = sm, *Tw = sm + TILE, *Tk = sm + 2 * TILE, *Tv = sm + 3 * TILE, *Tp = sm + 4 * TILE;
+    Ctl *ctl = reinterpret_cast<Ctl *>(sm + 5 * TILE);
+    if (r == 0) {
+        ctl->abort_flag = 0;
+        mbar_init(&ctl->load_bar, 1);
+        mbar_init(&ctl->mma_bar, 1);
+        mbar_init_fence();
+    }
+    if (r < 32) {
+        tmem_alloc(&ctl->tmem, 512);
+        tmem_relinquish();
+    }
+    stage_w2(smem_u32(Tw), wf);
+    operands_written();
+    const uint32_t tmem = ctl->tmem;
+    const uint32_t T_FQ = tmem, T_FK = tmem + 128, T_S = tmem + 256, T_NUM = tmem + 384;
+    const WaitCtl wc{smem_u32(&ctl->abort_flag), kWaitTimeoutUs, status};
+    const int64_t J = a - m + 1 > 0 ? (a - m + 1) / C : 0;
+    const float *PJ = pstate + (static_cast<int64_t>(bh) * nchunks + J) * STATE_FLOATS;
+    int lp = 0, mp = 0;  // load / mma phases
+    if (r == 0) {
+        tma_prefetch_desc(&mq);
+        mbar_arrive_expect_tx(&ctl->load_bar, TILE);
+        load_tile(Tq, &mq, &ctl->load_bar, static_cast<int>(a), bh);
+        if (mbar_wait(&ctl->load_bar, 0, wc, 43)) {
+            tc_fence_after();
+            mma_abt(T_FQ, smem_u32(Tq), smem_u32(Tw), false);  // f(Q): [row][feature]
+        } else {
+            mbar_wait_drain(&ctl->load_bar, 0);
+        }
+        umma_commit(&ctl->mma_bar);
+    }
+    ++lp;
+    bool fine = wait_mma(ctl, mp++, wc, 44);
+    float den = 0.f;
+    if (fine) {  // phi(Q) (bf16, over the Q tile) and phi(q) z_J (fp32)
+        for (int c0 = 0; c0 < D; c0 += 32) {
+            float x[32];
+            tmem_ld32(lane_addr(T_FQ, c0), x);
+#pragma unroll
+            for (int i = 0; i < 32; ++i) {
+                x[i] = exp2f(x[i] * LOG2E);
+                den = fmaf(x[i], PJ[D * D + c0 + i], den);
+            }
+            st_row32(smem_u32(Tq), r, c0, x);
+        }
+    }
+    const int64_t t = a + r;  // this thread's query row
+    bool any_num = false;
+    for (int u = 0; u < 2; ++u) {
+        const int64_t kt = J * C + u * C;  // first key of the intra tile
+        if (kt > last - m) break;
+        operands_written();  // phi(Q) (first pass) and the end of the previous tile's readers
+        if (r == 0) {
+            mbar_arrive_expect_tx(&ctl->load_bar, 2 * TILE);
+            load_tile(Tk, &mk, &ctl->load_bar, static_cast<int>(kt), bh);
+            load_tile(Tv, &mv, &ctl->load_bar, static_cast<int>(kt), bh);
+            if (fine && mbar_wait(&ctl->load_bar, lp & 1, wc, 45)) {
+                tc_fence_after();
+                mma_abt(T_FK, smem_u32(Tw), smem_u32(Tk), false);  // f(K)^T: [feature][key]
+            } else {
+                mbar_wait_drain(&ctl->load_bar, lp & 1);
+            }
+            umma_commit(&ctl->mma_bar);
+        }
+        ++lp;
+        fine = wait_mma(ctl, mp++, wc, 46) && fine;
+        if (fine) {
+            for (int c0 = 0; c0 < C; c0 += 32) {
+                float x[32];
+                tmem_ld32(lane_addr(T_FK, c0), x);
+#pragma unroll
+                for (int i = 0; i < 32; ++i) x[i] = exp2f(x[i] * LOG2E);
+                st_row32(smem_u32(Tk), r, c0, x);  // phi(K)^T over the K tile
+            }
+        }
+        operands_written();
+        if (r == 0) {
+            if (fine) mma_ab(T_S, smem_u32(Tq), smem_u32(Tk), false);  // phi(Q) phi(K)^T: [row][key]
+            umma_commit(&ctl->mma_bar);
+        }
+        fine = wait_mma(ctl, mp++, wc, 47) && fine;
+        if (fine) {  // keep s <= key <= t - m; row sums (fp32) into the denominator
+            for (int c0 = 0; c0 < C; c0 += 32) {
+                float x[32];
+                tmem_ld32(lane_addr(T_S, c0), x);
+#pragma unroll
+                for (int i = 0; i < 32; ++i) {
+                    const int64_t key = kt + c0 + i;
+                    x[i] = (key >= s && key <= t - m) ? x[i] : 0.f;
+                    den += x[i];
+                }
+                st_row32(smem_u32(Tp), r, c0, x);
+            }
+        }
+        operands_written();
+        if (r == 0) {
+            if (fine) mma_ab(T_NUM, smem_u32(Tp), smem_u32(Tv), any_num);  // masked scores x V
+            umma_commit(&ctl->mma_bar);
+        }
+        fine = wait_mma(ctl, mp++, wc, 48) && fine;
+        any_num = true;
+    }
+    if (J > 0) {  // phi(Q) P_J: P_J rows are features, columns value columns
+        if (fine) {
+            const float4 *src = reinterpret_cast<const float4 *>(PJ + r * D);
+            for (int c0 = 0; c0 < D; c0 += 32) {
+                float x[32];
+#pragma unroll
+                for (int i = 0; i < 8; ++i) {
+                    const float4 f = src[c0 / 4 + i];
+                    x[4 * i] = f.x, x[4 * i + 1] = f.y, x[4 * i + 2] = f.z, x[4 * i + 3] = f.w;
+                }
+                st_row32(smem_u32(Tp), r, c0, x);
+            }
+        }
+        operands_written();
+        if (r == 0) {
+            if (fine) mma_ab(T_NUM, smem_u32(Tq), smem_u32(Tp), any_num);
+            umma_commit(&ctl->mma_bar);
+        }
+        fine = wait_mma(ctl, mp++, wc, 49) && fine;
+        any_num = true;
+    }
+    if (fine) {
+        // tcgen05.ld is warp-collective: every thread loads, only rows t < L read o', lse and write o
+        const bool live = t < L;
+        const int64_t row = static_cast<int64_t>(bh) * L + (live ? t : 0);
+        const float e = live ? exp2f(-lse[row] * LOG2E) : 0.f;  // e^{-lse}
+        const float inv = 1.f / fmaf(den, e, 1.f);
+        __nv_bfloat16 *orow = o + row * D;
+        for (int c0 = 0; c0 < D; c0 += 32) {
+            float x[32];
+            if (any_num) {
+                tmem_ld32(lane_addr(T_NUM, c0), x);
+            } else {
+#pragma unroll
+                for (int i = 0; i < 32; ++i) x[i] = 0.f;
+            }
+            if (!live) continue;
+            uint4 *p = reinterpret_cast<uint4 *>(orow + c0);
+#pragma unroll
+            for (int g = 0; g < 4; ++g) {
+                const uint4 ov = p[g];
+                const uint32_t w4[4] = {ov.x, ov.y, ov.z, ov.w};
+                uint32_t res[4];
+#pragma unroll
+                for (int h = 0; h < 4; ++h) {
+                    const float lo = __uint_as_float(w4[h] << 16), hi = __uint_as_float(w4[h] & 0xFFFF0000u);
+                    res[h] = pack_bf16x2(fmaf(x[8 * g + 2 * h], e, lo) * inv, fmaf(x[8 * g + 2 * h + 1], e, hi) * inv);
+                }
+                p[g] = make_uint4(res[0], res[1], res[2], res[3]);
+            }
+        }
+    }
+    tc_fence_before();
+    __syncthreads();
+    if (r < 32) {
+        tc_fence_after();
+        tmem_dealloc(tmem, 512);
+    }
+}
+
+// ---- decode ----------------------------------------------------------------------------------------
+// grid BH, 128 threads (thread c: feature c / value column c).  Folds the key leaving the window at step t
+// (position t - m >= s, in the slot key t goes to) into S, z; writes k_new, v_new into that slot; writes
+// lin[bh] = (phi(q) S_t [d], phi(q) z_t).
+__global__ void __launch_bounds__(128) decode_state_kernel(const __nv_bfloat16 *__restrict__ q,
+                                                           const __nv_bfloat16 *__restrict__ k_new,
+                                                           const __nv_bfloat16 *__restrict__ v_new,
+                                                           __nv_bfloat16 *k_cache, __nv_bfloat16 *v_cache, float *S,
+                                                           float *z, const __nv_bfloat16 *__restrict__ wf, float *lin,
+                                                           int w, int s, int64_t t) {
+    __shared__ float kev[D], vev[D], qs[D], phk[D], phq[D], red[4];
+    const int bh = blockIdx.x, c = threadIdx.x;
+    const int m = w - s;
+    const int64_t slot = t < s ? t : s + (t - s) % m;
+    const bool evict = t - m >= s;
+    const int64_t crow = (static_cast<int64_t>(bh) * w + slot) * D;
+    kev[c] = __bfloat162float(k_cache[crow + c]);
+    vev[c] = __bfloat162float(v_cache[crow + c]);
+    qs[c] = __bfloat162float(q[static_cast<int64_t>(bh) * D + c]);
+    __syncthreads();
+    k_cache[crow + c] = k_new[static_cast<int64_t>(bh) * D + c];
+    v_cache[crow + c] = v_new[static_cast<int64_t>(bh) * D + c];
+    {  // f = x wf for the evicted key and the query; thread c < 64 computes column c of both
+        const int col = c & 63;
+        const float *x = c < 64 ? kev : qs;
+        float f = 0.f;
+        for (int i = 0; i < D; ++i) f = fmaf(x[i], __bfloat162float(wf[i * (D / 2) + col]), f);
+        float *dst = c < 64 ? phk : phq;
+        dst[col] = exp2f(f * LOG2E);
+        dst[col + 64] = exp2f(-f * LOG2E);
+    }
+    __syncthreads();
+    float *Sh = S + static_cast<int64_t>(bh) * D * D;
+    float num = 0.f;
+    const float vc = evict ? vev[c] : 0.f;
+    for (int j = 0; j < D; ++j) {
+        float x = Sh[j * D + c];
+        if (evict) {
+            x = fmaf(phk[j], vc, x);
+            Sh[j * D + c] = x;
+        }
+        num = fmaf(phq[j], x, num);
+    }
+    float zc = z[static_cast<int64_t>(bh) * D + c];
+    if (evict) {
+        zc += phk[c];
+        z[static_cast<int64_t>(bh) * D + c] = zc;
+    }
+    float dn = phq[c] * zc;
+    for (int off = 16; off > 0; off >>= 1) dn += __shfl_xor_sync(0xFFFFFFFFu, dn, off);
+    if ((c & 31) == 0) red[c >> 5] = dn;
+    __syncthreads();
+    lin[static_cast<int64_t>(bh) * (D + 1) + c] = num;
+    if (c == 0) lin[static_cast<int64_t>(bh) * (D + 1) + D] = (red[0] + red[1]) + (red[2] + red[3]);
+}
+
+// o = (o' + num e^{-lse}) / (1 + den e^{-lse}) per (b, h) row; grid BH, 128 threads.
+__global__ void __launch_bounds__(128) combine_kernel(__nv_bfloat16 *o, const float *__restrict__ lse,
+                                                      const float *__restrict__ lin) {
+    const int bh = blockIdx.x, c = threadIdx.x;
+    const float e = exp2f(-lse[bh] * LOG2E);
+    const float *l = lin + static_cast<int64_t>(bh) * (D + 1);
+    const float inv = 1.f / fmaf(l[D], e, 1.f);
+    const int64_t i = static_cast<int64_t>(bh) * D + c;
+    o[i] = __float2bfloat16_rn(fmaf(l[c], e, __bfloat162float(o[i])) * inv);
+}
+
+}  // namespace hy
+
+static size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
+
+static bool encode_tile_map(CUtensorMap *m, const void *base, int64_t L, int BH) {
+    EncodeTiledFn enc = encode_tiled_fn();
+    if (!enc) return false;
+    const cuuint64_t dims[3] = {static_cast<cuuint64_t>(hy::D), static_cast<cuuint64_t>(L), static_cast<cuuint64_t>(BH)};
+    const cuuint64_t strides[2] = {hy::D * 2, static_cast<cuuint64_t>(L) * hy::D * 2};
+    const cuuint32_t box[3] = {64, 128, 1};
+    const cuuint32_t estr[3] = {1, 1, 1};
+    return enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void *>(base), dims, strides, box, estr,
+               CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+static int64_t n_chunks(int64_t L) { return (L + hy::C - 1) / hy::C; }
+
+}  // namespace swa
+
+using namespace swa;
+
+extern "C" size_t swa_hybrid_prefill_workspace_size(int B, int H, int64_t L, int d) {
+    if (B < 1 || H < 1 || L < 1 || d != hy::D) return 0;
+    const int64_t BH = static_cast<int64_t>(B) * H;
+    return align256(static_cast<size_t>(BH * L) * 4) + align256(static_cast<size_t>(BH * n_chunks(L)) * hy::STATE_FLOATS * 4);
+}
+
+extern "C" int swa_hybrid_prefill(const void *q, const void *k, const void *v, const void *wf, void *o, float *state_s,
+                                  float *state_z, int B, int H, int64_t L, int d, int w, int s, float scale,
+                                  void *workspace, size_t workspace_bytes, int dtype, void *stream) {
+    fail(SWA_OK, "%s", "");
+    if (dtype != SWA_BF16 || d != hy::D) return fail(SWA_ERR_UNSUPPORTED, "hybrid prefill runs on bf16 with d = 128");
+    if (B < 1 || H < 1 || static_cast<int64_t>(B) * H > 65535) return fail(SWA_ERR_INVALID, "need 1 <= B*H <= 65535");
+    if (w < 1 || s < 0 || s >= w) return fail(SWA_ERR_INVALID, "need 0 <= s < w (s=%d, w=%d)", s, w);
+    if (L < 0 || L >= (int64_t(1) << 31)) return fail(SWA_ERR_INVALID, "L=%lld out of range", (long long)L);
+    if (!(scale == scale) || scale <= 0.f || scale > 1e30f)
+        return fail(SWA_ERR_INVALID, "scale must be a positive finite number");
+    if ((state_s == nullptr) != (state_z == nullptr))
+        return fail(SWA_ERR_INVALID, "state_s and state_z are given together or not at all");
+    const int BH = B * H;
+    const int m = w - s;
+    const cudaStream_t st = static_cast<cudaStream_t>(stream);
+    if (L == 0) {
+        if (state_s) {
+            cudaError_t e = cudaMemsetAsync(state_s, 0, static_cast<size_t>(BH) * hy::D * hy::D * 4, st);
+            if (e == cudaSuccess) e = cudaMemsetAsync(state_z, 0, static_cast<size_t>(BH) * hy::D * 4, st);
+            if (e != cudaSuccess) return fail(SWA_ERR_CUDA, "state reset: %s", cudaGetErrorString(e));
+        }
+        return SWA_OK;
+    }
+    if (!q || !k || !v || !o || !wf) return fail(SWA_ERR_INVALID, "q, k, v, wf and o must be non-null");
+    if ((reinterpret_cast<uintptr_t>(q) | reinterpret_cast<uintptr_t>(k) | reinterpret_cast<uintptr_t>(v) |
+         reinterpret_cast<uintptr_t>(o)) & 15u)
+        return fail(SWA_ERR_INVALID, "q, k, v and o must be 16-byte aligned");
+    if (reinterpret_cast<uintptr_t>(wf) & 1u) return fail(SWA_ERR_INVALID, "wf must be 2-byte aligned");
+    if ((reinterpret_cast<uintptr_t>(state_s) | reinterpret_cast<uintptr_t>(state_z)) & 15u)
+        return fail(SWA_ERR_INVALID, "state_s and state_z must be 16-byte aligned");
+    const size_t need = swa_hybrid_prefill_workspace_size(B, H, L, d);
+    if (workspace_bytes < need)
+        return fail(SWA_ERR_INVALID, "workspace of %zu bytes is smaller than the %zu needed", workspace_bytes, need);
+    if (!workspace || (reinterpret_cast<uintptr_t>(workspace) & 255u))
+        return fail(SWA_ERR_INVALID, "workspace must be non-null and 256-byte aligned");
+    unsigned *status = device_status_word();
+    if (!status) return SWA_ERR_CUDA;
+    float *lse = static_cast<float *>(workspace);
+    float *states = reinterpret_cast<float *>(static_cast<char *>(workspace) + align256(static_cast<size_t>(BH) * L * 4));
+    const int nch = static_cast<int>(n_chunks(L));
+
+    // the SWA branch: o' and lse
+    PrefillArgs a{q, k, v, o, lse, nullptr, nullptr, 0, BH, L, d, w, s, scale, L, st};
+    if (int rc = launch_prefill_bf16_tc(a)) return rc;
+
+    CUtensorMap mq, mk, mv;
+    if (!encode_tile_map(&mq, q, L, BH) || !encode_tile_map(&mk, k, L, BH) || !encode_tile_map(&mv, v, L, BH))
+        return fail(SWA_ERR_INVALID, "cuTensorMapEncodeTiled rejected q, k or v");
+    const __nv_bfloat16 *wfb = static_cast<const __nv_bfloat16 *>(wf);
+    DeviceStatus *ds = reinterpret_cast<DeviceStatus *>(status);
+    const uint32_t smem_a = 3 * hy::TILE + 1024 + 64, smem_b = 5 * hy::TILE + 1024 + 64;
+    static bool attr_done = false;  // per process; the attribute is per function and idempotent
+    if (!attr_done) {
+        cudaError_t e = cudaFuncSetAttribute(hy::chunk_state_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem_a);
+        if (e == cudaSuccess)
+            e = cudaFuncSetAttribute(hy::linear_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem_b);
+        if (e != cudaSuccess) return fail(SWA_ERR_CUDA, "hybrid kernels: %s", cudaGetErrorString(e));
+        attr_done = true;
+    }
+    // the linear branch: chunk states, their exclusive scan, then per query tile
+    hy::chunk_state_kernel<<<dim3(nch, BH), 128, smem_a, st>>>(mk, mv, wfb, states, nullptr, nullptr, nullptr, 0,
+                                                               nch, s, L, ds);
+    const int64_t total = static_cast<int64_t>(BH) * hy::STATE_FLOATS;
+    hy::scan_kernel<<<static_cast<unsigned>((total + 255) / 256), 256, 0, st>>>(states, nch, total);
+    hy::linear_kernel<<<dim3(nch, BH), 128, smem_b, st>>>(mq, mk, mv, wfb, states, static_cast<__nv_bfloat16 *>(o),
+                                                          lse, L, m, s, nch, ds);
+    if (state_s) {
+        // the state after the last row (keys s .. L-1-m): the prefix of chunk jf plus its keys below L - m
+        const int64_t jf = L - m > 0 ? (L - m) / hy::C : 0;
+        hy::chunk_state_kernel<<<dim3(1, BH), 128, smem_a, st>>>(mk, mv, wfb, nullptr, states, state_s, state_z,
+                                                                 static_cast<int>(jf), nch, s, L - m, ds);
+    }
+    cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) return fail(SWA_ERR_CUDA, "hybrid prefill launch: %s", cudaGetErrorString(e));
+    return SWA_OK;
+}
+
+extern "C" size_t swa_hybrid_decode_workspace_size(int B, int H, int d, int w) {
+    if (B < 1 || H < 1 || d != hy::D || w < 1) return 0;
+    const int BH = B * H;
+    return align256(decode_workspace_bytes(BH, d, w)) + align256(static_cast<size_t>(BH) * 4) +
+           align256(static_cast<size_t>(BH) * (hy::D + 1) * 4);
+}
+
+extern "C" int swa_hybrid_decode_step(const void *q, const void *k_new, const void *v_new, void *k_cache, void *v_cache,
+                                      float *state_s, float *state_z, const void *wf, void *o, int B, int H, int d,
+                                      int w, int s, int64_t t, float scale, void *workspace, size_t workspace_bytes,
+                                      int dtype, void *stream) {
+    fail(SWA_OK, "%s", "");
+    if (dtype != SWA_BF16 || d != hy::D) return fail(SWA_ERR_UNSUPPORTED, "hybrid decode runs on bf16 with d = 128");
+    if (B < 1 || H < 1 || static_cast<int64_t>(B) * H > 65535) return fail(SWA_ERR_INVALID, "need 1 <= B*H <= 65535");
+    if (w < 1 || s < 0 || s >= w) return fail(SWA_ERR_INVALID, "need 0 <= s < w (s=%d, w=%d)", s, w);
+    if (t < 0) return fail(SWA_ERR_INVALID, "t must be >= 0");
+    if (!(scale == scale) || scale <= 0.f || scale > 1e30f)
+        return fail(SWA_ERR_INVALID, "scale must be a positive finite number");
+    if (!q || !k_new || !v_new || !k_cache || !v_cache || !state_s || !state_z || !wf || !o)
+        return fail(SWA_ERR_INVALID, "every tensor argument must be non-null");
+    if ((reinterpret_cast<uintptr_t>(q) | reinterpret_cast<uintptr_t>(k_cache) | reinterpret_cast<uintptr_t>(v_cache) |
+         reinterpret_cast<uintptr_t>(o)) & 15u)
+        return fail(SWA_ERR_INVALID, "q, k_cache, v_cache and o must be 16-byte aligned");
+    if ((reinterpret_cast<uintptr_t>(k_new) | reinterpret_cast<uintptr_t>(v_new) | reinterpret_cast<uintptr_t>(wf)) & 1u)
+        return fail(SWA_ERR_INVALID, "k_new, v_new and wf must be 2-byte aligned");
+    if ((reinterpret_cast<uintptr_t>(state_s) | reinterpret_cast<uintptr_t>(state_z)) & 3u)
+        return fail(SWA_ERR_INVALID, "state_s and state_z must be 4-byte aligned");
+    const size_t need = swa_hybrid_decode_workspace_size(B, H, d, w);
+    if (workspace_bytes < need)
+        return fail(SWA_ERR_INVALID, "workspace of %zu bytes is smaller than the %zu needed", workspace_bytes, need);
+    if (!workspace || (reinterpret_cast<uintptr_t>(workspace) & 255u))
+        return fail(SWA_ERR_INVALID, "workspace must be non-null and 256-byte aligned");
+    const int BH = B * H;
+    const cudaStream_t st = static_cast<cudaStream_t>(stream);
+    char *ws = static_cast<char *>(workspace);
+    const size_t dec_bytes = align256(decode_workspace_bytes(BH, d, w));
+    float *lse = reinterpret_cast<float *>(ws + dec_bytes);
+    float *lin = reinterpret_cast<float *>(ws + dec_bytes + align256(static_cast<size_t>(BH) * 4));
+    hy::decode_state_kernel<<<BH, 128, 0, st>>>(
+        static_cast<const __nv_bfloat16 *>(q), static_cast<const __nv_bfloat16 *>(k_new),
+        static_cast<const __nv_bfloat16 *>(v_new), static_cast<__nv_bfloat16 *>(k_cache),
+        static_cast<__nv_bfloat16 *>(v_cache), state_s, state_z, static_cast<const __nv_bfloat16 *>(wf), lin, w, s, t);
+    cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) return fail(SWA_ERR_CUDA, "hybrid decode state launch: %s", cudaGetErrorString(e));
+    DecodeArgs da{q, k_cache, v_cache, o, lse, BH, d, w, s, t, scale, ws, dec_bytes, 2, st};
+    if (int rc = launch_decode(da)) return rc;
+    hy::combine_kernel<<<BH, 128, 0, st>>>(static_cast<__nv_bfloat16 *>(o), lse, lin);
+    e = cudaGetLastError();
+    if (e != cudaSuccess) return fail(SWA_ERR_CUDA, "hybrid combine launch: %s", cudaGetErrorString(e));
+    return SWA_OK;
+}

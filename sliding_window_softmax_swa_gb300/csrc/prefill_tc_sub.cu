@@ -296,15 +296,6 @@ __device__ __forceinline__ void fadd2(float &d0, float &d1, float a0, float a1, 
         : "f"(a0), "f"(a1), "f"(b0), "f"(b1));
 }
 
-// Bounded wait that ignores the CTA abort flag: used only to drain copies/MMAs before exit.
-__device__ __noinline__ bool mbar_wait_drain(uint64_t *bar, uint32_t parity) {
-    const uint32_t a = smem_u32(bar);
-    const uint64_t t0 = globaltimer_ns();
-    while (!mbar_try_wait(a, parity)) {
-        if (globaltimer_ns() - t0 > kWaitTimeoutNs) return false;
-    }
-    return true;
-}
 
 // S (128 x 64, fp32 in TMEM) (+)= Q (128 x HD) K_sub^T: Q and the 64-row K sub-tile K-major, 128-byte
 // swizzled, one 64-column box after the other.
