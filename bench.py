@@ -313,8 +313,16 @@ def blocksparse_pairs(L, w, s, globals_, block, rand) -> int:
     return total
 
 
+def hybrid_flops(B, H, L, d, w, s) -> float:
+    """The banded SWA FLOPs plus the linear branch in its recurrent form: for each key that leaves the window
+    (L - m - s of them) its feature map (2 d * d/2 * 2) and the rank-1 fold of phi(k)^T v (2 d^2); for each
+    row with a non-empty state (also L - m - s rows) the query's feature map (2 d^2) and phi(q) S (2 d^2)."""
+    n = max(0, L - (w - s) - s)
+    return banded_flops(B, H, L, d, w) + B * H * n * 8.0 * d * d
+
+
 def prefill_leg(swa, wl, steps, warmup, world, rank, clocks, e2e=False, rope=False, dilation=0, window=None,
-                blocksparse=None):
+                blocksparse=None, hybrid=False):
     """Prefill steps; with ``rope`` the RoPE prefill at the positions inside the cache (base 10000): a
     rotation pass over q and k, then the tensor-core prefill on the rotated rows (2 launches a step);
     ``blocksparse`` = (globals, block, rand): the block-sparse prefill with that pattern."""
@@ -327,7 +335,14 @@ def prefill_leg(swa, wl, steps, warmup, world, rank, clocks, e2e=False, rope=Fal
     lib = swa.lib()
     stream = torch.cuda.current_stream().cuda_stream
     dt = 0 if wl.dtype == "bf16" else 1
-    if blocksparse is not None:
+    if hybrid:
+        wf = swa_inputs.hedgehog_weights(d, wl.seed).to("cuda")
+        nws = lib.swa_hybrid_prefill_workspace_size(B, H, L, d)
+        ws = torch.empty(nws, dtype=torch.uint8, device="cuda")
+        args = (q.data_ptr(), k.data_ptr(), v.data_ptr(), wf.data_ptr(), o.data_ptr(), None, None, B, H, L, d, w, s,
+                wl.scale, ws.data_ptr(), nws, dt, stream)
+        call = lib.swa_hybrid_prefill
+    elif blocksparse is not None:
         globals_, block, rand = blocksparse
         g = np.ascontiguousarray(globals_, dtype=np.int32)
         rb = np.ascontiguousarray(rand, dtype=np.int32)
@@ -360,7 +375,10 @@ def prefill_leg(swa, wl, steps, warmup, world, rank, clocks, e2e=False, rope=Fal
 
     t = time_loop(step, steps, warmup, world, clocks, window)
     _check_status(swa)
-    if blocksparse is not None:
+    if hybrid:
+        flops = hybrid_flops(B, H, L, d, w, s)
+        launches = 4
+    elif blocksparse is not None:
         flops = 4.0 * B * H * d * blocksparse_pairs(L, w, s, globals_, block, rand)
         launches = 2 if len(globals_) else 1
     else:
@@ -515,6 +533,51 @@ def decode_leg(swa, wl, world, rank, clocks, steps=None, rope=False, dilation=0)
     return res
 
 
+def hybrid_decode_leg(swa, wl, world, rank, clocks, steps=200):
+    """Decode steps of the SWA + linear-attention hybrid at a full cache (positions T, T+1, ...): per step the
+    state pass (fold of the evicted key, rolling write, phi(q) S), the SWA decode and the combination."""
+    import torch
+    import swa_inputs
+    B, H, d, w, s = wl.B, wl.H, wl.d, wl.w, wl.s
+    T = wl.L
+    seed = wl.seed + 7919 * rank
+    kc = swa_inputs.normal((B, H, w, d), seed, swa_inputs.TID_K, wl.torch_dtype, "cuda")
+    vc = swa_inputs.normal((B, H, w, d), seed, swa_inputs.TID_V, wl.torch_dtype, "cuda")
+    qs = swa_inputs.normal((steps, B, H, d), seed + 1, swa_inputs.TID_Q, wl.torch_dtype, "cuda")
+    ks = swa_inputs.normal((steps, B, H, d), seed + 1, swa_inputs.TID_K, wl.torch_dtype, "cuda")
+    vs = swa_inputs.normal((steps, B, H, d), seed + 1, swa_inputs.TID_V, wl.torch_dtype, "cuda")
+    S = torch.zeros((B, H, d, d), dtype=torch.float32, device="cuda")
+    z = torch.zeros((B, H, d), dtype=torch.float32, device="cuda")
+    wf = swa_inputs.hedgehog_weights(d, wl.seed).to("cuda")
+    o = torch.empty((B, H, d), dtype=qs.dtype, device="cuda")
+    lib = swa.lib()
+    nws = lib.swa_hybrid_decode_workspace_size(B, H, d, w)
+    ws = torch.empty(nws, dtype=torch.uint8, device="cuda")
+    stream = torch.cuda.current_stream().cuda_stream
+    row = B * H * d * qs.element_size()
+    qp, kp, vp = qs.data_ptr(), ks.data_ptr(), vs.data_ptr()
+    cnt = [0]
+
+    def step():
+        i = cnt[0] % steps
+        rc = lib.swa_hybrid_decode_step(qp + i * row, kp + i * row, vp + i * row, kc.data_ptr(), vc.data_ptr(),
+                                        S.data_ptr(), z.data_ptr(), wf.data_ptr(), o.data_ptr(), B, H, d, w, s,
+                                        T + cnt[0], wl.scale, ws.data_ptr(), nws, 0, stream)
+        cnt[0] += 1
+        if rc:
+            raise RuntimeError(swa.last_error())
+
+    t = time_loop(step, steps, 5, world, clocks)
+    _check_status(swa)
+    # bytes per step: the cache (w keys and values), q / k_new / v_new / o, the state read and written
+    step_bytes = B * H * (2 * w * d * 2 + 4 * d * 2 + 2 * (d * d + d) * 4)
+    res = {"steps": steps, "seconds": t, "tok_per_s": B * steps / t, "us_per_step": t / steps * 1e6,
+           "bytes_per_step": step_bytes, "gbs": step_bytes / (t / steps) / 1e9, "launches": 4 * steps}
+    del kc, vc, qs, ks, vs, S, z
+    torch.cuda.empty_cache()
+    return res
+
+
 # ------------------------------------------------------------------------------------------ oracle legs
 def oracle_sample_inputs(wl, heads: int):
     """Host copies of the first `heads` heads of the workload's inputs (drawn on the CPU)."""
@@ -597,7 +660,7 @@ def main():
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--primary-only", action="store_true", help="only the primary prefill leg")
     ap.add_argument("--legs", default="primary,mistral,chunked,decode,decode_rope,prefill_rope,chunked_rope,dilated,"
-                                      "decode_dilated,blocksparse",
+                                      "decode_dilated,blocksparse,hybrid,decode_hybrid",
                     help="comma list of legs to run (profiling runs pick one)")
     ap.add_argument("--decode-steps", type=int, default=None, help="shorter decode stream (profiling only)")
     args = ap.parse_args()
@@ -668,6 +731,24 @@ def main():
             "what": "block-sparse: window + sinks + 128 global tokens + 3 random key blocks of 64 per query block "
                     "(FLOPs over those key sets): host tile lists + their upload, tensor-core prefill, global rows",
             "launches_per_step": r["launches"] // max(3, args.steps // 2)}
+    if "hybrid" in legs:
+        r = prefill_leg(swa, wl, max(3, args.steps // 2), 3, world, rank, clocks, hybrid=True)
+        secondary["prefill_hybrid_linear_llama7b_L8192_w1024_s4"] = {
+            "metric": METRIC, "value": aggregate_rate(r["tflops"], world, 1.0), "unit": "TFLOP/s",
+            "ms_per_step": r["ms_per_step"], "frac_of_bf16_peak": r["tflops"] / peaks["bf16_tflops"],
+            "what": "SWA + Hedgehog linear-attention branch for the evicted keys (FLOPs: banded SWA + the "
+                    "recurrent linear branch, 8 d^2 per evicted key): SWA prefill, chunk states, scan, linear "
+                    "pass with the combination", "launches_per_step": 4}
+    if "decode_hybrid" in legs:
+        dw = swa_inputs.WORKLOADS["decode_llama13b_B64_w1024_s4_20480"]
+        r = hybrid_decode_leg(swa, dw, world, rank, clocks)
+        secondary["decode_hybrid_linear_llama13b_B64_w1024_s4_20480"] = {
+            "metric": "decode tok/s", "value": aggregate_rate(r["tok_per_s"], world, 1.0), "unit": "tok/s",
+            "us_per_step": r["us_per_step"], "what": "SWA + linear-attention hybrid at a full cache: state pass "
+            "(evicted-key fold, rolling write, phi(q) S) + SWA decode + combination",
+            "roofline": {"bound": "hbm", "achieved": r["gbs"], "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                         "frac": r["gbs"] / peaks["hbm_gbs"], "bytes_per_step": r["bytes_per_step"],
+                         "note": "whole step (3 launches), cache + state bytes"}}
     if "chunked_rope" in legs:
         cw = swa_inputs.WORKLOADS["chunked_mistral_L131072_w4096_s4_C4096"]
         r = chunked_leg(swa, cw, 3, 1, world, rank, clocks, rope=True)

@@ -83,3 +83,12 @@ def test_blocksparse_pairs_counts_the_oracle_key_sets():
     assert bench.blocksparse_pairs(60, 10, 2, g, 4, None) == want
     # no pattern: the banded count
     assert bench.blocksparse_pairs(300, 50, 4, [], 16, None) == bench.banded_pairs(300, 50)
+
+
+def test_hybrid_flop_accounting():
+    import bench
+    import oracle
+    # 8 d^2 per key that has left the window by the end (= per row with a non-empty state), on top of the band
+    for L, w, s in [(50, 10, 2), (9, 10, 2), (40, 3, 0), (64, 64, 4)]:
+        n = sum(1 for t in range(L) for i in range(t + 1) if i == t - (w - s) and i >= s and not oracle.is_key(t, i, w, s))
+        assert bench.hybrid_flops(2, 3, L, 16, w, s) == bench.banded_flops(2, 3, L, 16, w) + 2 * 3 * n * 8 * 16 * 16
