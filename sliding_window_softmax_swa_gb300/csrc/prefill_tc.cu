@@ -87,7 +87,8 @@ constexpr uint32_t OFF_BAR = OFF_V + NV * TILE_BYTES;
 constexpr uint32_t OFF_MISC = OFF_BAR + 256;
 constexpr uint32_t OFF_TILES = OFF_MISC + 64;
 constexpr uint32_t OFF_GMASK = OFF_TILES + 2 * MAX_TILES * 12;  // two tile lists (current / next item)
-constexpr uint32_t SMEM_USED = OFF_GMASK + 2 * MAX_TILES * 16;     // and their global-key columns (block-sparse)
+constexpr uint32_t OFF_XCH = OFF_GMASK + 2 * MAX_TILES * 16;       // and their global-key columns (block-sparse)
+constexpr uint32_t SMEM_USED = OFF_XCH + 2 * 2 * BH_ROWS * 4;        // row-value exchange of the softmax halves
 constexpr uint32_t SMEM_BYTES = SMEM_USED + 1024;  // slack to align the base to 1024 bytes
 static_assert(SMEM_BYTES <= 232448, "shared memory budget of one CTA");
 
@@ -232,21 +233,26 @@ __device__ __forceinline__ void fadd2(float &d0, float &d1, float a0, float a1, 
 }
 
 
+// Both issued by a whole converged warp (one elected lane issues each MMA).  Shared-memory addresses stay
+// below 2^18, so a K step only adds its offset / 16 to the low descriptor word.
 __device__ __forceinline__ void issue_qk(uint32_t d_tmem, uint32_t q_addr, uint32_t k_addr) {
+    const uint32_t qlo = sdesc_sw128_lo(q_addr, 16), klo = sdesc_sw128_lo(k_addr, 16);
+    constexpr uint32_t hi = sdesc_sw128_hi(1024);
 #pragma unroll
     for (int kk = 0; kk < HD / 16; ++kk) {
-        const uint32_t off = (kk >> 2) * HALF_BYTES + (kk & 3) * 32;
-        umma_ss(d_tmem, sdesc_sw128(q_addr + off, 16, 1024), sdesc_sw128(k_addr + off, 16, 1024), IDESC_QK,
-                kk > 0 ? 1u : 0u);
+        const uint32_t off = ((kk >> 2) * HALF_BYTES + (kk & 3) * 32) >> 4;
+        umma_ss_warp_lo(d_tmem, qlo + off, klo + off, hi, IDESC_QK, kk > 0 ? 1u : 0u);
     }
 }
 
 __device__ __forceinline__ void issue_pv(uint32_t d_tmem, uint32_t p_tmem, uint32_t v_addr, bool accumulate) {
+    const uint32_t vlo = sdesc_sw128_lo(v_addr, HALF_BYTES);
+    constexpr uint32_t hi = sdesc_sw128_hi(1024);
 #pragma unroll
     for (int kk = 0; kk < BN / 16; ++kk) {
         // P from TMEM: 16 keys = 8 columns of packed bf16 pairs; V: 16 key rows of 128 bytes (MN-major)
-        umma_ts(d_tmem, p_tmem + kk * 8, sdesc_sw128(v_addr + kk * 16 * 128, HALF_BYTES, 1024), IDESC_PV,
-                (accumulate || kk > 0) ? 1u : 0u);
+        umma_ts_warp_lo(d_tmem, p_tmem + kk * 8, vlo + ((kk * 16 * 128) >> 4), hi, IDESC_PV,
+                        (accumulate || kk > 0) ? 1u : 0u);
     }
 }
 
@@ -257,9 +263,9 @@ __global__ void __launch_bounds__(kThreads, 1) swa_prefill_tc_kernel(const __gri
     extern __shared__ uint8_t smem_raw[];
     uint8_t *sm = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     uint64_t *bars = reinterpret_cast<uint64_t *>(sm + OFF_BAR);
-    uint64_t *qfull = bars;           // Q_0, Q_1 of the current item landed
-    uint64_t *qempty = qfull + 1;     // the last QK product of an item is done: Q may be reloaded
-    uint64_t *kfull = qempty + 1;     // [NK]
+    uint64_t *qfull = bars;           // [2]: Q_x of the current item landed
+    uint64_t *qempty = qfull + 2;     // [2]: the item's last QK_x product is done: Q_x may be reloaded
+    uint64_t *kfull = qempty + 2;     // [NK]
     uint64_t *kempty = kfull + NK;    // [NK]
     uint64_t *vfull = kempty + NK;    // [NV]
     uint64_t *vempty = vfull + NV;    // [NV]
@@ -268,7 +274,7 @@ __global__ void __launch_bounds__(kThreads, 1) swa_prefill_tc_kernel(const __gri
     uint64_t *ofull = pfull + 2;      // [2]: the last PV_x product of an item is done
     uint64_t *oempty = ofull + 2;     // [2]: O_x has been read by the epilogue (128 arrivals)
     uint64_t *lready = oempty + 2;    // [2]: tile list buffer b written (1 arrival)
-    uint64_t *lfree = lready + 2;     // [2]: tile list buffer b no longer read (8 softmax warps, MMA, TMA)
+    uint64_t *lfree = lready + 2;     // [2]: tile list buffer b no longer read (8 softmax warps, MMA, 2 loaders)
     uint64_t *drain = lfree + 2;
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(sm + OFF_MISC);
     volatile int *abort_flag = reinterpret_cast<volatile int *>(sm + OFF_MISC + 4);
@@ -281,8 +287,6 @@ __global__ void __launch_bounds__(kThreads, 1) swa_prefill_tc_kernel(const __gri
 
     if (threadIdx.x == 0) {
         *abort_flag = 0;
-        mbar_init(qfull, 1);
-        mbar_init(qempty, 1);
         for (int i = 0; i < NK; ++i) {
             mbar_init(&kfull[i], 1);
             mbar_init(&kempty[i], 1);
@@ -292,12 +296,14 @@ __global__ void __launch_bounds__(kThreads, 1) swa_prefill_tc_kernel(const __gri
             mbar_init(&vempty[i], 1);
         }
         for (int x = 0; x < 2; ++x) {
+            mbar_init(&qfull[x], 1);
+            mbar_init(&qempty[x], 1);
             mbar_init(&sfull[x], 1);
-            mbar_init(&pfull[x], BH_ROWS);
+            mbar_init(&pfull[x], 2 * BH_ROWS);
             mbar_init(&ofull[x], 1);
-            mbar_init(&oempty[x], BH_ROWS);
+            mbar_init(&oempty[x], 2 * BH_ROWS);
             mbar_init(&lready[x], 1);
-            mbar_init(&lfree[x], 10);
+            mbar_init(&lfree[x], 11);
         }
         mbar_init(drain, 1);
         mbar_init_fence();
@@ -313,80 +319,47 @@ __global__ void __launch_bounds__(kThreads, 1) swa_prefill_tc_kernel(const __gri
     const WaitCtl wc{smem_u32(const_cast<int *>(abort_flag)), P.timeout_us, P.status};
 
     if (warp == kWarpTma) {
-        // ------------------------------------------------------------------ TMA producer (K, V)
-        if (lane == 0) {
-            tma_prefetch_desc(&P.tm_k);
-            tma_prefetch_desc(&P.tm_v);
-            // One stream of key tiles over all items of this CTA: the K cursor runs up to NK tiles ahead of
-            // the V cursor, across item boundaries, so the next item's first K tiles load while the current
-            // item's last V tiles are still in flight.
-            int gk = 0, gv = 0;                     // K, V tiles issued so far
-            int itk = -1, jk = 0, nk = 0, bhk = 0;  // K cursor: item, tile, tile count, head
-            int itv = 0, jv = 0;                    // V cursor
-            bool k_done = false, fine = true;
-            while (fine) {
-                while (!k_done && gk < gv + NK) {
-                    if (jk == nk) {  // next item for the K cursor
-                        // at most one item ahead of V: the list of item itv + 2 shares a buffer with item itv
-                        if (itk > itv) break;
-                        ++itk;
-                        const int item = static_cast<int>(blockIdx.x) + itk * G;
-                        if (item >= P.n_items) {
-                            k_done = true;
-                            break;
-                        }
-                        if (!mbar_wait(&lready[itk & 1], (itk >> 1) & 1, wc, 15, itk)) {
-                            fine = false;
-                            break;
-                        }
-                        nk = ntiles_s[itk & 1];
-                        bhk = item % P.BH;
-                        jk = 0;
-                        continue;
-                    }
-                    const int st = gk % NK;
-                    if (!mbar_wait(&kempty[st], ((gk / NK) & 1) ^ 1, wc, 1, jk)) {
+        // ------------------------------------------------------------------ TMA producers (K, V)
+        // Lane 0 streams the K tiles, lane 1 the V tiles, each in its own ring over all items of this CTA in
+        // order, so neither waits for the other: a K slot frees when the QK products that read it are done,
+        // a V slot after its PV products, and the K loads run ahead into the next item on their own.
+        if (lane < 2) {
+            const bool isk = lane == 0;
+            const int ns = isk ? NK : NV;
+            uint64_t *full = isk ? kfull : vfull;
+            uint64_t *empty = isk ? kempty : vempty;
+            uint8_t *ring = sm + (isk ? OFF_K : OFF_V);
+            const CUtensorMap *m_seq = isk ? &P.tm_k : &P.tm_v;
+            const CUtensorMap *m_cache = isk ? &P.tm_kc : &P.tm_vc;
+            tma_prefetch_desc(m_seq);
+            int g = 0;  // tiles issued so far
+            for (int it = 0;; ++it) {
+                const int item = static_cast<int>(blockIdx.x) + it * G;
+                if (item >= P.n_items) break;
+                const int b = it & 1;
+                if (!mbar_wait(&lready[b], (it >> 1) & 1, wc, 15, it)) break;
+                const int n = ntiles_s[b];
+                const int bh = item % P.BH;
+                bool fine = true;
+                for (int j = 0; j < n; ++j) {
+                    const int st = g % ns;
+                    if (!mbar_wait(&empty[st], ((g / ns) & 1) ^ 1, wc, isk ? 1 : 9, j)) {
                         fine = false;
                         break;
                     }
-                    const Tile T = tiles_s[(itk & 1) * MAX_TILES + jk];
-                    const CUtensorMap *mk = (T.flags & 1) ? &P.tm_kc : &P.tm_k;
-                    uint8_t *ks = sm + OFF_K + st * TILE_BYTES;
-                    mbar_arrive_expect_tx(&kfull[st], TILE_BYTES);
-                    tma_load_3d(ks, mk, &kfull[st], 0, T.row0, bhk);
-                    tma_load_3d(ks + HALF_BYTES, mk, &kfull[st], 64, T.row0, bhk);
-                    ++jk;
-                    ++gk;
+                    const Tile T = tiles_s[b * MAX_TILES + j];
+                    const CUtensorMap *mp = (T.flags & 1) ? m_cache : m_seq;
+                    uint8_t *dst = ring + st * TILE_BYTES;
+                    mbar_arrive_expect_tx(&full[st], TILE_BYTES);
+                    tma_load_3d(dst, mp, &full[st], 0, T.row0, bh);
+                    tma_load_3d(dst + HALF_BYTES, mp, &full[st], 64, T.row0, bh);
+                    ++g;
                 }
                 if (!fine) break;
-                if (gv == gk) break;  // every issued K tile has its V tile: nothing left
-                // the V cursor follows the K cursor tile by tile (its item's list was waited for by K)
-                const int nv = ntiles_s[itv & 1];
-                if (jv == nv) {
-                    mbar_arrive(&lfree[itv & 1]);  // the loads of item itv no longer read its list
-                    ++itv;
-                    jv = 0;
-                    continue;
-                }
-                const int item = static_cast<int>(blockIdx.x) + itv * G;
-                const int sv = gv % NV;
-                if (!mbar_wait(&vempty[sv], ((gv / NV) & 1) ^ 1, wc, 9, jv)) {
-                    fine = false;
-                    break;
-                }
-                const Tile T = tiles_s[(itv & 1) * MAX_TILES + jv];
-                const CUtensorMap *mv = (T.flags & 1) ? &P.tm_vc : &P.tm_v;
-                uint8_t *vs = sm + OFF_V + sv * TILE_BYTES;
-                mbar_arrive_expect_tx(&vfull[sv], TILE_BYTES);
-                tma_load_3d(vs, mv, &vfull[sv], 0, T.row0, item % P.BH);
-                tma_load_3d(vs + HALF_BYTES, mv, &vfull[sv], 64, T.row0, item % P.BH);
-                ++jv;
-                ++gv;
+                mbar_arrive(&lfree[b]);  // this lane no longer reads the item's list
             }
-            if (fine && jv > 0 && jv == ntiles_s[itv & 1]) mbar_arrive(&lfree[itv & 1]);
             if (*abort_flag) {  // make sure no copy is still landing in shared memory
-                for (int g = (gk > NK ? gk - NK : 0); g < gk; ++g) mbar_wait_drain(&kfull[g % NK], (g / NK) & 1);
-                for (int g = (gv > NV ? gv - NV : 0); g < gv; ++g) mbar_wait_drain(&vfull[g % NV], (g / NV) & 1);
+                for (int gg = (g > ns ? g - ns : 0); gg < g; ++gg) mbar_wait_drain(&full[gg % ns], (gg / ns) & 1);
             }
         }
     } else if (warp == kWarpList) {
@@ -396,7 +369,8 @@ __global__ void __launch_bounds__(kThreads, 1) swa_prefill_tc_kernel(const __gri
             // (it - 2) has been released by every reader; then Q_0, Q_1 of the item, as soon as the previous
             // item's last QK product is done (about two key tiles before that item ends), and the next
             // item's Q into L2, so that its load does not wait for DRAM.
-            int nq = 0;
+            int nq = 0;              // items whose Q loads were issued
+            int nqx[2] = {0, 0};     // Q_x loads issued
             for (int it = 0;; ++it) {
                 const int item = static_cast<int>(blockIdx.x) + it * G;
                 if (item >= P.n_items) break;
@@ -430,14 +404,21 @@ __global__ void __launch_bounds__(kThreads, 1) swa_prefill_tc_kernel(const __gri
                 if (!BS) mark_tiles(tl, n, q0, qlast, P.s, P.m);
                 ntiles_s[b] = n;
                 mbar_arrive(&lready[b]);  // release: the list is visible to whoever sees the phase complete
-                // Q_0, Q_1 of the item, once the QK products of the previous item's Q are done
-                if (nq >= 1 && !mbar_wait(qempty, (nq - 1) & 1, wc, 13, it)) break;
-                uint8_t *qs = sm + OFF_Q;
-                mbar_arrive_expect_tx(qfull, 2 * TILE_BYTES);
-                for (int x = 0; x < 2; ++x) {
-                    tma_load_3d(qs + x * TILE_BYTES, &P.tm_q, qfull, 0, row_start + x * BH_ROWS, bh);
-                    tma_load_3d(qs + x * TILE_BYTES + HALF_BYTES, &P.tm_q, qfull, 64, row_start + x * BH_ROWS, bh);
+                // Q_x of the item, each as soon as the previous item's last QK_x product is done (query tile 0
+                // usually finishes a key tile before query tile 1)
+                bool qfine = true;
+                for (int x = 0; x < 2 && qfine; ++x) {
+                    if (nq >= 1 && !mbar_wait(&qempty[x], (nq - 1) & 1, wc, 13, it)) {
+                        qfine = false;
+                        break;
+                    }
+                    uint8_t *qs = sm + OFF_Q + x * TILE_BYTES;
+                    mbar_arrive_expect_tx(&qfull[x], TILE_BYTES);
+                    tma_load_3d(qs, &P.tm_q, &qfull[x], 0, row_start + x * BH_ROWS, bh);
+                    tma_load_3d(qs + HALF_BYTES, &P.tm_q, &qfull[x], 64, row_start + x * BH_ROWS, bh);
+                    nqx[x] = nq + 1;
                 }
+                if (!qfine) break;
                 ++nq;
                 // into L2 meanwhile: the next item's Q rows
                 const int nitem = item + G;
@@ -449,46 +430,65 @@ __global__ void __launch_bounds__(kThreads, 1) swa_prefill_tc_kernel(const __gri
                     }
                 }
             }
-            if (*abort_flag && nq > 0) mbar_wait_drain(qfull, (nq - 1) & 1);  // no copy may still be landing
+            if (*abort_flag) {  // no copy may still be landing
+                for (int x = 0; x < 2; ++x)
+                    if (nqx[x] > 0) mbar_wait_drain(&qfull[x], (nqx[x] - 1) & 1);
+            }
         }
     } else if (warp == kWarpMma) {
         // ------------------------------------------------------------------ MMA issuer
         // Per key tile j: PV_0(j), QK_0(j+1), PV_1(j), QK_1(j+1).  While the tensor cores work on one
         // query tile, the softmax warpgroup of the other one turns its S into P.  The first QK products
         // of the next item follow the last PV products of the current one, so they overlap its epilogue.
-        if (lane == 0) {
+        {  // the whole warp runs the loop (uniform operands); one elected lane issues each instruction
+            auto wwait = [&](uint64_t *bar, int parity, unsigned site, unsigned tag) -> bool {
+                return __all_sync(0xFFFFFFFFu, mbar_wait(bar, static_cast<uint32_t>(parity), wc, site, tag));
+            };
             const uint32_t q_addr = smem_u32(sm + OFF_Q);
             const uint32_t k_addr0 = smem_u32(sm + OFF_K), v_addr0 = smem_u32(sm + OFF_V);
             bool issued_any = false, fine = true;
             int gk = 0, gv = 0;                // K, V tiles consumed
             int cp[2] = {0, 0};                // PV_x products issued (pfull parity)
             int ce[2] = {0, 0};                // items in which query tile x had PV products (oempty)
-            int nqf = 0;                       // Q loads consumed (qfull parity)
+            int qf[2] = {0, 0};                // Q_x loads consumed (qfull parity)
             for (int it = 0; fine; ++it) {
                 const int item = static_cast<int>(blockIdx.x) + it * G;
                 if (item >= P.n_items) break;
                 const int b = it & 1;
-                if (!mbar_wait(&lready[b], (it >> 1) & 1, wc, 14, it)) break;  // the item's tile list
-                if (!mbar_wait(qfull, nqf & 1, wc, 2, it)) break;                // Q of this item
-                ++nqf;
+                if (!wwait(&lready[b], (it >> 1) & 1, 14, it)) break;  // the item's tile list
+                bool qready[2] = {false, false};
+                // Q_x of this item, waited for before its first QK_x product
+                auto need_q = [&](int x) -> bool {
+                    if (qready[x]) return true;
+                    if (!wwait(&qfull[x], qf[x] & 1, 2, it)) return false;
+                    ++qf[x];
+                    qready[x] = true;
+                    tc_fence_after();
+                    return true;
+                };
                 const Tile *tl = tiles_s + b * MAX_TILES;
                 const int n = ntiles_s[b];
                 int last_used[2] = {-1, -1};
                 for (int j = 0; j < n; ++j)
                     for (int x = 0; x < 2; ++x)
                         if (tl[j].flags & (2 << x)) last_used[x] = j;
-                if (!mbar_wait(&kfull[gk % NK], (gk / NK) & 1, wc, 3, 0)) { fine = false; break; }
+                if (!wwait(&kfull[gk % NK], (gk / NK) & 1, 3, 0)) { fine = false; break; }
                 tc_fence_after();
                 {
                     const int f = tl[0].flags;
-                    for (int x = 0; x < 2; ++x) {
+                    for (int x = 0; x < 2 && fine; ++x) {
                         if (f & (2 << x)) {
+                            if (!need_q(x)) {
+                                fine = false;
+                                break;
+                            }
                             issue_qk(tmem + col_s(x), q_addr + x * TILE_BYTES, k_addr0 + (gk % NK) * TILE_BYTES);
-                            umma_commit(&sfull[x]);
+                            umma_commit_warp(&sfull[x]);
+                            if (last_used[x] == 0) umma_commit_warp(&qempty[x]);  // Q_x is no longer read
                         }
                     }
-                    if (n == 1) umma_commit(qempty);  // the item's only QK products: Q is no longer read
-                    umma_commit(&kempty[gk % NK]);
+                    if (!fine) break;
+                    umma_commit_warp(&kempty[gk % NK]);
                     ++gk;
                     issued_any = true;
                 }
@@ -500,190 +500,113 @@ __global__ void __launch_bounds__(kThreads, 1) swa_prefill_tc_kernel(const __gri
                     bool v_ready = false, k_ready = (j + 1 >= n);
                     for (int x = 0; x < 2 && fine; ++x) {
                         if (fj & (2 << x)) {
-                            if (!mbar_wait(&pfull[x], cp[x] & 1, wc, 4, j)) { fine = false; break; }
+                            if (!wwait(&pfull[x], cp[x] & 1, 4, j)) { fine = false; break; }
                             if (first_pv[x]) {  // O_x must have been read by the previous item's epilogue
-                                if (!mbar_wait(&oempty[x], (ce[x] & 1) ^ 1, wc, 11, j)) { fine = false; break; }
+                                if (!wwait(&oempty[x], (ce[x] & 1) ^ 1, 11, j)) { fine = false; break; }
                                 ++ce[x];
                             }
                             if (!v_ready) {
-                                if (!mbar_wait(&vfull[sv], (gv / NV) & 1, wc, 5, j)) { fine = false; break; }
+                                if (!wwait(&vfull[sv], (gv / NV) & 1, 5, j)) { fine = false; break; }
                                 v_ready = true;
                             }
                             tc_fence_after();
                             issue_pv(tmem + col_o(x), tmem + col_s(x), v_addr0 + sv * TILE_BYTES, !first_pv[x]);
                             first_pv[x] = false;
                             ++cp[x];
-                            if (j == last_used[x]) umma_commit(&ofull[x]);
+                            if (j == last_used[x]) umma_commit_warp(&ofull[x]);
                         }
                         if (fn & (2 << x)) {  // S_x is free again once PV_x(j) has been issued
                             if (!k_ready) {
-                                if (!mbar_wait(&kfull[sk], (gk / NK) & 1, wc, 3, j + 1)) { fine = false; break; }
+                                if (!wwait(&kfull[sk], (gk / NK) & 1, 3, j + 1)) { fine = false; break; }
                                 k_ready = true;
+                            }
+                            if (!need_q(x)) {
+                                fine = false;
+                                break;
                             }
                             tc_fence_after();
                             issue_qk(tmem + col_s(x), q_addr + x * TILE_BYTES, k_addr0 + sk * TILE_BYTES);
-                            umma_commit(&sfull[x]);
+                            umma_commit_warp(&sfull[x]);
+                            if (j + 1 == last_used[x]) umma_commit_warp(&qempty[x]);  // the item's last QK_x product
                         }
                     }
                     if (!fine) break;
-                    if (j + 2 == n) umma_commit(qempty);  // the item's last QK products were just issued
-                    umma_commit(&vempty[sv]);
+                    umma_commit_warp(&vempty[sv]);
                     ++gv;
                     if (j + 1 < n) {
-                        umma_commit(&kempty[sk]);
+                        umma_commit_warp(&kempty[sk]);
                         ++gk;
                     }
                 }
                 if (!fine) break;
-                mbar_arrive(&lfree[b]);
+                // a query tile with no key tile in this item still takes its Q load and releases it
+                for (int x = 0; x < 2 && fine; ++x) {
+                    if (last_used[x] < 0) {
+                        if (!need_q(x)) {
+                            fine = false;
+                            break;
+                        }
+                        umma_commit_warp(&qempty[x]);
+                    }
+                }
+                if (!fine) break;
+                if (lane == 0) mbar_arrive(&lfree[b]);
             }
             if (issued_any) {  // no MMA may still be running when TMEM is freed
-                umma_commit(drain);
+                umma_commit_warp(drain);
                 mbar_wait_drain(drain, 0);
             }
         }
     } else if (warp < 8) {
         // ------------------------------------------------------------------ softmax + epilogue
-        const int x = warp >> 2;                    // query tile of this warpgroup
-        const int r = threadIdx.x & (BH_ROWS - 1);  // its row == TMEM lane
+        // All eight warps work on every S tile, in the order the MMA thread completes them (S_0(j), S_1(j),
+        // S_0(j+1), ...): warp w reads the TMEM lanes 32 (w mod 4) .. +31 (rows of the query tile) and the
+        // key half hf = w / 4 (columns 64 hf .. 64 hf + 63), so each row is split over two threads, which agree
+        // on the row maximum through shared memory (one named barrier of the 256 softmax threads per tile).
+        // Each thread keeps the running max and its half of the running sum of one row of each query tile.
+        // The epilogue of query tile x (O_x / l) runs when its O_x is next needed: just before the first S_x
+        // tile of the following item (or after the last item), so it overlaps the other tile's work.
+        const int hf = warp >> 2;                   // key half of this warp
+        const int r = threadIdx.x & (BH_ROWS - 1);  // row within a query tile == TMEM lane
         const uint32_t lane_base = static_cast<uint32_t>((warp & 3) * 32) << 16;
-        const uint32_t s_addr = tmem + lane_base + col_s(x);
-        const uint32_t o_addr = tmem + lane_base + col_o(x);
+        float *xch = reinterpret_cast<float *>(sm + OFF_XCH);  // [2 slots][2 halves][128 rows]
         const float sl2 = P.scale_log2;
-        const int bit = 2 << x;
-        int cs = 0;  // tiles processed by this warpgroup (sfull / pfull parity)
-        int ne = 0;  // epilogues done (ofull parity)
+        int cs[2] = {0, 0};  // S_x tiles processed (sfull / pfull parity)
+        int ne[2] = {0, 0};  // epilogues done (ofull parity)
+        int nx = 0;          // exchanges done (slot parity)
+        float mrun[2] = {-INFINITY, -INFINITY}, lrun[2] = {0.f, 0.f};  // running max (log2 units), half sum
+        struct Pending {
+            int on, row_start, bh, qlast;
+        } pend[2] = {{0, 0, 0, 0}, {0, 0, 0, 0}};
         bool fine = true;
-        for (int it = 0; fine; ++it) {
-            const int item = static_cast<int>(blockIdx.x) + it * G;
-            if (item >= P.n_items) break;
-            const int bh = item % P.BH;
-            const int row_start = (P.n_qpairs - 1 - item / P.BH) * BM;
-            const int q0 = P.pos0 + row_start;
-            const int qlast = P.pos0 + min(row_start + BM, P.L) - 1;
-            const int t = q0 + x * BH_ROWS + r;  // absolute position of this thread's row
-            const int b = it & 1;
-            fine = __all_sync(0xFFFFFFFFu, mbar_wait(&lready[b], (it >> 1) & 1, wc, 14, it));
-            if (!fine) break;
-            const Tile *tl = tiles_s + b * MAX_TILES;
-            const int n = ntiles_s[b];
-            float mrun = -INFINITY, lrun = 0.f;  // running max (log2 units) and sum
-            int cnt = 0;
-            for (int j = 0; j < n; ++j) {
-                const Tile T = tl[j];
-                if (!(T.flags & bit)) continue;
-                fine = __all_sync(0xFFFFFFFFu, mbar_wait(&sfull[x], cs & 1, wc, 6, j));
-                if (!fine) break;
-                tc_fence_after();
-                // valid columns of this row: [0, b1] (sinks) and [a2, hc] (window), hc = last causal
-                // column, as four 32-bit column masks; interior tiles need none
-                const int hc = min(static_cast<int>(T.chi), t - T.pbase);
-                const int b1 = min(hc, P.s - 1 - T.pbase);
-                const int a2 = max(0, t - P.m + 1 - T.pbase);
-                bool full = (b1 >= BN - 1) || (hc >= BN - 1 && (a2 <= 0 || b1 >= a2 - 1));
-                uint32_t mw[4];
-#pragma unroll
-                for (int k = 0; k < 4; ++k)
-                    mw[k] = full ? 0xFFFFFFFFu : (range_bits(-32 * k, b1 - 32 * k) | range_bits(a2 - 32 * k, hc - 32 * k));
-                if (BS && !full && t <= qlast) {
-                    // block-sparse: also the global keys of the tile and the row's random key blocks, up to hc
-                    const TileMask gm = gmask_s[b * MAX_TILES + j];
-                    const int* rb = P.bs_rand + static_cast<int64_t>(t / P.bs_block) * P.bs_r;
-                    for (int i = 0; i < P.bs_r; ++i) {
-                        const int kb = rb[i];
-                        if (kb < 0) continue;
-                        const int lo = kb * P.bs_block - T.pbase;
-                        const int hi = min(lo + P.bs_block - 1, hc);
-#pragma unroll
-                        for (int k = 0; k < 4; ++k) mw[k] |= range_bits(lo - 32 * k, hi - 32 * k);
-                    }
-#pragma unroll
-                    for (int k = 0; k < 4; ++k) mw[k] |= gm.w[k] & range_bits(-32 * k, hc - 32 * k);
-                    full = (mw[0] & mw[1] & mw[2] & mw[3]) == 0xFFFFFFFFu;
-                }
-                const bool any_masked = __any_sync(0xFFFFFFFFu, !full);  // warp-uniform: no divergent paths
-                // the whole row of S_x in registers (one TMEM load)
-                float sv[BN];
-                __syncwarp();
-                tmem_ld128(s_addr, sv);
-                if (any_masked) {
-#pragma unroll
-                    for (int c = 0; c < BN; ++c) sv[c] = (mw[c >> 5] & (1u << (c & 31))) ? sv[c] : -INFINITY;
-                }
-                float mx4[4];
-#pragma unroll
-                for (int i = 0; i < 4; ++i) mx4[i] = fmax3(sv[i], sv[4 + i], sv[8 + i]);
-#pragma unroll
-                for (int c = 12; c < BN - 4; c += 8)
-#pragma unroll
-                    for (int i = 0; i < 4; ++i) mx4[i] = fmax3(mx4[i], sv[c + i], sv[c + 4 + i]);
-                const float mx = fmax3(fmax3(mx4[0], mx4[1], sv[BN - 4]), fmax3(mx4[2], mx4[3], sv[BN - 3]),
-                                       fmaxf(sv[BN - 2], sv[BN - 1])) * sl2;
-                float alpha = 1.f;
-                bool resc = false;
-                const float mnew = fmaxf(mrun, mx);
-                if (mnew > mrun + kRescaleLog2) {  // also taken when mrun is still -inf
-                    if (mrun != -INFINITY) {
-                        alpha = ex2(mrun - mnew);
-                        resc = true;
-                    }
-                    mrun = mnew;
-                }
-                if (__any_sync(0xFFFFFFFFu, resc)) {
-                    // O_x holds the PV products of this item's earlier tiles; they are complete,
-                    // because S_x (issued after the last of them) is, and tcgen05 MMAs of one thread
-                    // complete in order.
-                    __syncwarp();
-#pragma unroll 1
-                    for (int c = 0; c < HD; c += 32) {
-                        float ov[32];
-                        tmem_ld32(o_addr + c, ov);
-#pragma unroll
-                        for (int i = 0; i < 32; ++i) ov[i] *= alpha;
-                        tmem_st32(o_addr + c, ov);
-                    }
-                }
-                // p = 2^(scale*log2(e)*s - m); bf16 pairs of keys 0..63 / 64..127 go to columns [0, 32) /
-                // [32, 64) of S_x (already read): the A operand of PV_x
-                const float nmu = (mrun == -INFINITY) ? 0.f : -mrun;
-                float rs4[4] = {0.f, 0.f, 0.f, 0.f};
-#pragma unroll
-                for (int h = 0; h < 2; ++h) {
-                    uint32_t pk[32];
-#pragma unroll
-                    for (int i = 0; i < 32; ++i) {
-                        const int c = 64 * h + 2 * i;
-                        float a0, a1;
-                        ffma2(a0, a1, sv[c], sv[c + 1], sl2, sl2, nmu, nmu);
-                        const float p0 = ex2(a0), p1 = ex2(a1);
-                        const int k = (i & 1) * 2;
-                        fadd2(rs4[k], rs4[k + 1], rs4[k], rs4[k + 1], p0, p1);
-                        pk[i] = pack_bf16x2(p0, p1);
-                    }
-                    __syncwarp();
-                    tmem_st32u_nowait(s_addr + 32 * h, pk);
-                }
-                tmem_wait_st();
-                lrun = lrun * alpha + ((rs4[0] + rs4[1]) + (rs4[2] + rs4[3]));
-                tc_fence_before();
-                mbar_arrive(&pfull[x]);
-                ++cnt;
-                ++cs;
-            }
-            if (!fine) break;
-            if (lane == 0) mbar_arrive(&lfree[b]);  // this warp no longer reads the tile list
-            if (cnt == 0) continue;                // no row of this query tile in the sequence
-            // epilogue: O_x / l -> bf16 in registers, O_x handed back to the MMA, then the rows are
-            // written to global memory (and lse)
-            fine = __all_sync(0xFFFFFFFFu, mbar_wait(&ofull[x], ne & 1, wc, 8, it));
-            if (!fine) break;
-            ++ne;
+        // The row value of this thread's partner (the other key half of the row), through shared memory.  The
+        // barrier also tells every softmax thread whether any of them failed a wait or saw the CTA abort flag
+        // (`stop`), so that all 256 leave together and none is left waiting at a later barrier.
+        const uint32_t abort_a = smem_u32(const_cast<int *>(abort_flag));
+        auto exchange = [&](float v, bool failed, bool &stop) -> float {
+            float *slot = xch + (nx & 1) * 256;
+            slot[hf * 128 + r] = v;
+            stop = named_barrier_or(1, 256, failed || ld_abort(abort_a) != 0);
+            ++nx;
+            return slot[(hf ^ 1) * 128 + r];
+        };
+        // O_x / l of the pending item of query tile x -> bf16 rows in global memory (and lse)
+        auto epilogue = [&](int x) -> bool {
+            const Pending pd = pend[x];
+            pend[x].on = 0;
+            const bool ok = __all_sync(0xFFFFFFFFu, mbar_wait(&ofull[x], ne[x] & 1, wc, 8, pd.row_start));
+            bool stop;
+            const float lpart = exchange(lrun[x], !ok, stop);
+            if (stop) return false;
+            ++ne[x];
             tc_fence_after();
-            const float inv = (lrun > 0.f) ? 1.f / lrun : 0.f;
-            uint32_t ob[HD / 2];
+            const float lsum = lrun[x] + lpart;
+            const float inv = (lsum > 0.f) ? 1.f / lsum : 0.f;
+            uint32_t ob[32];
             __syncwarp();
+            const uint32_t o_addr = tmem + lane_base + col_o(x) + 64 * hf;
 #pragma unroll
-            for (int c = 0; c < HD; c += 32) {
+            for (int c = 0; c < 64; c += 32) {
                 float ov[32];
                 tmem_ld32(o_addr + c, ov);
 #pragma unroll
@@ -691,16 +614,160 @@ __global__ void __launch_bounds__(kThreads, 1) swa_prefill_tc_kernel(const __gri
             }
             tc_fence_before();
             mbar_arrive(&oempty[x]);
-            if (t <= qlast) {
-                const int64_t row = static_cast<int64_t>(bh) * P.seq_stride + row_start + x * BH_ROWS + r;
-                uint8_t *dst = reinterpret_cast<uint8_t *>(static_cast<__nv_bfloat16 *>(P.o) + row * HD);
+            const int t = P.pos0 + pd.row_start + x * BH_ROWS + r;
+            if (t <= pd.qlast) {
+                const int64_t row = static_cast<int64_t>(pd.bh) * P.seq_stride + pd.row_start + x * BH_ROWS + r;
+                uint8_t *dst = reinterpret_cast<uint8_t *>(static_cast<__nv_bfloat16 *>(P.o) + row * HD + 64 * hf);
 #pragma unroll
-                for (int i = 0; i < HD / 16; ++i)
+                for (int i = 0; i < 4; ++i)
                     st_global_v8(dst + 32 * i, ob[8 * i], ob[8 * i + 1], ob[8 * i + 2], ob[8 * i + 3], ob[8 * i + 4],
                                  ob[8 * i + 5], ob[8 * i + 6], ob[8 * i + 7]);
-                if (P.lse) P.lse[row] = (mrun + log2f(lrun)) * 0.69314718055994531f;
+                if (P.lse && hf == 0) P.lse[row] = (mrun[x] + log2f(lsum)) * 0.69314718055994531f;
             }
+            return true;
+        };
+        for (int it = 0; fine; ++it) {
+            const int item = static_cast<int>(blockIdx.x) + it * G;
+            if (item >= P.n_items) break;
+            const int bh = item % P.BH;
+            const int row_start = (P.n_qpairs - 1 - item / P.BH) * BM;
+            const int q0 = P.pos0 + row_start;
+            const int qlast = P.pos0 + min(row_start + BM, P.L) - 1;
+            const int b = it & 1;
+            {
+                const bool ok = mbar_wait(&lready[b], (it >> 1) & 1, wc, 14, it);
+                if (named_barrier_or(1, 256, !ok || ld_abort(abort_a) != 0)) break;  // uniform: all or none go on
+            }
+            const Tile *tl = tiles_s + b * MAX_TILES;
+            const int n = ntiles_s[b];
+            int cnt[2] = {0, 0};
+            for (int j = 0; j < n && fine; ++j) {
+                const Tile T = tl[j];
+                for (int x = 0; x < 2; ++x) {
+                    if (!(T.flags & (2 << x))) continue;
+                    if (cnt[x] == 0) {  // first S_x tile of this item: finish the previous item of tile x
+                        if (pend[x].on && !epilogue(x)) {
+                            fine = false;
+                            break;
+                        }
+                        mrun[x] = -INFINITY;
+                        lrun[x] = 0.f;
+                    }
+                    const int t = q0 + x * BH_ROWS + r;  // absolute position of this thread's row
+                    const uint32_t s_addr = tmem + lane_base + col_s(x);
+                    const bool ok = __all_sync(0xFFFFFFFFu, mbar_wait(&sfull[x], cs[x] & 1, wc, 6, j));
+                    tc_fence_after();
+                    // this half of the score row in registers (not loaded after a failed wait: the exchange
+                    // below then stops every softmax thread)
+                    float sv[64];
+                    __syncwarp();
+                    if (ok) tmem_ld64(s_addr + 64 * hf, sv);
+                    // valid columns of this row: [0, b1] (sinks) and [a2, hc] (window), hc = last causal
+                    // column, as 32-bit column masks of this half; interior tiles need none
+                    const int hc = min(static_cast<int>(T.chi), t - T.pbase);
+                    const int b1 = min(hc, P.s - 1 - T.pbase);
+                    const int a2 = max(0, t - P.m + 1 - T.pbase);
+                    bool full = (b1 >= BN - 1) || (hc >= BN - 1 && (a2 <= 0 || b1 >= a2 - 1));
+                    uint32_t mw[2];
+#pragma unroll
+                    for (int k = 0; k < 2; ++k) {
+                        const int c0 = 64 * hf + 32 * k;
+                        mw[k] = full ? 0xFFFFFFFFu : (range_bits(-c0, b1 - c0) | range_bits(a2 - c0, hc - c0));
+                    }
+                    if (BS && !full && t <= qlast) {
+                        // block-sparse: also the global keys of the tile and the row's random key blocks, up to hc
+                        const TileMask gm = gmask_s[b * MAX_TILES + j];
+                        const int *rb = P.bs_rand + static_cast<int64_t>(t / P.bs_block) * P.bs_r;
+                        for (int i = 0; i < P.bs_r; ++i) {
+                            const int kb = rb[i];
+                            if (kb < 0) continue;
+                            const int lo = kb * P.bs_block - T.pbase;
+                            const int hi = min(lo + P.bs_block - 1, hc);
+#pragma unroll
+                            for (int k = 0; k < 2; ++k) mw[k] |= range_bits(lo - 64 * hf - 32 * k, hi - 64 * hf - 32 * k);
+                        }
+#pragma unroll
+                        for (int k = 0; k < 2; ++k)
+                            mw[k] |= gm.w[2 * hf + k] & range_bits(-64 * hf - 32 * k, hc - 64 * hf - 32 * k);
+                        full = (mw[0] & mw[1]) == 0xFFFFFFFFu;
+                    }
+                    const bool any_masked = __any_sync(0xFFFFFFFFu, (mw[0] & mw[1]) != 0xFFFFFFFFu);
+                    if (any_masked) {
+#pragma unroll
+                        for (int c = 0; c < 64; ++c) sv[c] = (mw[c >> 5] & (1u << (c & 31))) ? sv[c] : -INFINITY;
+                    }
+                    float mx4[4];
+#pragma unroll
+                    for (int i = 0; i < 4; ++i) mx4[i] = fmax3(sv[i], sv[4 + i], sv[8 + i]);
+#pragma unroll
+                    for (int c = 12; c < 60; c += 8)
+#pragma unroll
+                        for (int i = 0; i < 4; ++i) mx4[i] = fmax3(mx4[i], sv[c + i], sv[c + 4 + i]);
+                    const float mxh = fmax3(fmax3(mx4[0], mx4[1], sv[60]), fmax3(mx4[2], mx4[3], sv[61]),
+                                            fmaxf(sv[62], sv[63]));
+                    // the whole row's maximum; both halves of a row take the same decisions from here on, and
+                    // every TMEM load of S_x is complete before either half stores P over it
+                    bool stop;
+                    const float mx = fmaxf(mxh, exchange(mxh, !ok, stop)) * sl2;
+                    if (stop) {
+                        fine = false;
+                        break;
+                    }
+                    float alpha = 1.f;
+                    bool resc = false;
+                    const float mnew = fmaxf(mrun[x], mx);
+                    if (mnew > mrun[x] + kRescaleLog2) {  // also taken when mrun is still -inf
+                        if (mrun[x] != -INFINITY) {
+                            alpha = ex2(mrun[x] - mnew);
+                            resc = true;
+                        }
+                        mrun[x] = mnew;
+                    }
+                    if (__any_sync(0xFFFFFFFFu, resc)) {
+                        // O_x holds the PV products of this item's earlier tiles; they are complete, because
+                        // S_x (issued after the last of them) is, and tcgen05 MMAs of one thread complete in order.
+                        __syncwarp();
+                        const uint32_t o_addr = tmem + lane_base + col_o(x) + 64 * hf;
+#pragma unroll 1
+                        for (int c = 0; c < 64; c += 32) {
+                            float ov[32];
+                            tmem_ld32(o_addr + c, ov);
+#pragma unroll
+                            for (int i = 0; i < 32; ++i) ov[i] *= alpha;
+                            tmem_st32(o_addr + c, ov);
+                        }
+                    }
+                    // p = 2^(scale*log2(e)*s - m); bf16 pairs of this half's keys go to columns
+                    // [32 hf, 32 hf + 32) of S_x (the A operand of PV_x)
+                    const float nmu = (mrun[x] == -INFINITY) ? 0.f : -mrun[x];
+                    float rs4[4] = {0.f, 0.f, 0.f, 0.f};
+                    uint32_t pk[32];
+#pragma unroll
+                    for (int i = 0; i < 32; ++i) {
+                        float a0, a1;
+                        ffma2(a0, a1, sv[2 * i], sv[2 * i + 1], sl2, sl2, nmu, nmu);
+                        const float p0 = ex2(a0), p1 = ex2(a1);
+                        const int k = (i & 1) * 2;
+                        fadd2(rs4[k], rs4[k + 1], rs4[k], rs4[k + 1], p0, p1);
+                        pk[i] = pack_bf16x2(p0, p1);
+                    }
+                    __syncwarp();
+                    tmem_st32u_nowait(s_addr + 32 * hf, pk);
+                    tmem_wait_st();
+                    lrun[x] = lrun[x] * alpha + ((rs4[0] + rs4[1]) + (rs4[2] + rs4[3]));
+                    tc_fence_before();
+                    mbar_arrive(&pfull[x]);
+                    ++cnt[x];
+                    ++cs[x];
+                }
+            }
+            if (!fine) break;
+            if (lane == 0) mbar_arrive(&lfree[b]);  // this warp no longer reads the tile list
+            for (int x = 0; x < 2; ++x)
+                if (cnt[x] > 0) pend[x] = {1, row_start, bh, qlast};
         }
+        for (int x = 0; x < 2 && fine; ++x)
+            if (pend[x].on && !epilogue(x)) fine = false;
     }
 
     tc_fence_before();
