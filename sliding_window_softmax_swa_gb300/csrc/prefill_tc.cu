@@ -75,8 +75,9 @@ constexpr int MAX_TILES = 64;
 constexpr int kThreads = 352;  // warps 0-3 / 4-7: softmax of query tile 0 / 1; 8: TMA; 9: MMA; 10: tile lists
 constexpr int kWarpTma = 8, kWarpMma = 9, kWarpList = 10;
 constexpr uint32_t kTmemCols = 512;
-// TMEM columns: S_0, S_1 (scores, later P in their first 64 columns), O_0, O_1 (accumulators)
-__host__ __device__ constexpr uint32_t col_s(int x) { return static_cast<uint32_t>(x) * 128u; }
+// TMEM columns: S (the scores of one query tile at a time, fp32), P_0, P_1 (bf16 pairs), O_0, O_1 (fp32)
+constexpr uint32_t COL_S = 0;
+__host__ __device__ constexpr uint32_t col_p(int x) { return 128u + static_cast<uint32_t>(x) * 64u; }
 __host__ __device__ constexpr uint32_t col_o(int x) { return 256u + static_cast<uint32_t>(x) * 128u; }
 constexpr float kRescaleLog2 = 8.f;  // rescale O only when the running max grows by more than 2^8
 
@@ -87,8 +88,7 @@ constexpr uint32_t OFF_BAR = OFF_V + NV * TILE_BYTES;
 constexpr uint32_t OFF_MISC = OFF_BAR + 256;
 constexpr uint32_t OFF_TILES = OFF_MISC + 64;
 constexpr uint32_t OFF_GMASK = OFF_TILES + 2 * MAX_TILES * 12;  // two tile lists (current / next item)
-constexpr uint32_t OFF_XCH = OFF_GMASK + 2 * MAX_TILES * 16;       // and their global-key columns (block-sparse)
-constexpr uint32_t SMEM_USED = OFF_XCH + 2 * 2 * BH_ROWS * 4;        // row-value exchange of the softmax halves
+constexpr uint32_t SMEM_USED = OFF_GMASK + 2 * MAX_TILES * 16;     // and their global-key columns (block-sparse)
 constexpr uint32_t SMEM_BYTES = SMEM_USED + 1024;  // slack to align the base to 1024 bytes
 static_assert(SMEM_BYTES <= 232448, "shared memory budget of one CTA");
 
@@ -269,13 +269,15 @@ __global__ void __launch_bounds__(kThreads, 1) swa_prefill_tc_kernel(const __gri
     uint64_t *kempty = kfull + NK;    // [NK]
     uint64_t *vfull = kempty + NK;    // [NV]
     uint64_t *vempty = vfull + NV;    // [NV]
-    uint64_t *sfull = vempty + NV;    // [2]: S_x = Q_x K_j^T ready, one per query tile x
+    uint64_t *sfull = vempty + NV;    // [2]: S = Q_x K_j^T ready (the S buffer holds query tile x's scores)
     uint64_t *pfull = sfull + 2;      // [2]: P_x ready in TMEM (128 arrivals)
     uint64_t *ofull = pfull + 2;      // [2]: the last PV_x product of an item is done
     uint64_t *oempty = ofull + 2;     // [2]: O_x has been read by the epilogue (128 arrivals)
     uint64_t *lready = oempty + 2;    // [2]: tile list buffer b written (1 arrival)
     uint64_t *lfree = lready + 2;     // [2]: tile list buffer b no longer read (8 softmax warps, MMA, 2 loaders)
     uint64_t *drain = lfree + 2;
+    uint64_t *sfree = drain + 1;      // the S buffer has been read by the softmax warps of its last user (4 warps)
+    uint64_t *pempty = sfree + 1;     // [2]: PV_x products issued so far are done (P_x and O_x free)
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(sm + OFF_MISC);
     volatile int *abort_flag = reinterpret_cast<volatile int *>(sm + OFF_MISC + 4);
     int *ntiles_s = reinterpret_cast<int *>(sm + OFF_MISC + 8);  // [2]
@@ -299,13 +301,16 @@ __global__ void __launch_bounds__(kThreads, 1) swa_prefill_tc_kernel(const __gri
             mbar_init(&qfull[x], 1);
             mbar_init(&qempty[x], 1);
             mbar_init(&sfull[x], 1);
-            mbar_init(&pfull[x], 2 * BH_ROWS);
+            mbar_init(&pfull[x], BH_ROWS);
             mbar_init(&ofull[x], 1);
-            mbar_init(&oempty[x], 2 * BH_ROWS);
+            mbar_init(&oempty[x], BH_ROWS);
             mbar_init(&lready[x], 1);
             mbar_init(&lfree[x], 11);
         }
         mbar_init(drain, 1);
+        mbar_init(sfree, 4);
+        mbar_init(&pempty[0], 1);
+        mbar_init(&pempty[1], 1);
         mbar_init_fence();
     }
     if (warp == 0) {
@@ -437,10 +442,13 @@ __global__ void __launch_bounds__(kThreads, 1) swa_prefill_tc_kernel(const __gri
         }
     } else if (warp == kWarpMma) {
         // ------------------------------------------------------------------ MMA issuer
-        // Per key tile j: PV_0(j), QK_0(j+1), PV_1(j), QK_1(j+1).  While the tensor cores work on one
-        // query tile, the softmax warpgroup of the other one turns its S into P.  The first QK products
-        // of the next item follow the last PV products of the current one, so they overlap its epilogue.
-        {  // the whole warp runs the loop (uniform operands); one elected lane issues each instruction
+        // One S buffer serves the two query tiles in turn, and P_x has TMEM columns of its own, so a QK
+        // product needs only the S buffer to have been read by the softmax warps of its previous user, not
+        // their whole softmax.  Per key tile j of an item: QK_0(j), PV_0(j-1), QK_1(j), PV_1(j-1): the tensor
+        // cores take the next QK products while the softmax warps still compute the previous tile's
+        // exponentials.  The whole warp runs the loop (uniform operands); one elected lane issues each
+        // instruction.
+        {
             auto wwait = [&](uint64_t *bar, int parity, unsigned site, unsigned tag) -> bool {
                 return __all_sync(0xFFFFFFFFu, mbar_wait(bar, static_cast<uint32_t>(parity), wc, site, tag));
             };
@@ -451,6 +459,7 @@ __global__ void __launch_bounds__(kThreads, 1) swa_prefill_tc_kernel(const __gri
             int cp[2] = {0, 0};                // PV_x products issued (pfull parity)
             int ce[2] = {0, 0};                // items in which query tile x had PV products (oempty)
             int qf[2] = {0, 0};                // Q_x loads consumed (qfull parity)
+            int u = 0;                         // QK products issued into the S buffer (sfree parity)
             for (int it = 0; fine; ++it) {
                 const int item = static_cast<int>(blockIdx.x) + it * G;
                 if (item >= P.n_items) break;
@@ -472,34 +481,28 @@ __global__ void __launch_bounds__(kThreads, 1) swa_prefill_tc_kernel(const __gri
                 for (int j = 0; j < n; ++j)
                     for (int x = 0; x < 2; ++x)
                         if (tl[j].flags & (2 << x)) last_used[x] = j;
-                if (!wwait(&kfull[gk % NK], (gk / NK) & 1, 3, 0)) { fine = false; break; }
-                tc_fence_after();
-                {
-                    const int f = tl[0].flags;
-                    for (int x = 0; x < 2 && fine; ++x) {
-                        if (f & (2 << x)) {
-                            if (!need_q(x)) {
-                                fine = false;
-                                break;
-                            }
-                            issue_qk(tmem + col_s(x), q_addr + x * TILE_BYTES, k_addr0 + (gk % NK) * TILE_BYTES);
-                            umma_commit_warp(&sfull[x]);
-                            if (last_used[x] == 0) umma_commit_warp(&qempty[x]);  // Q_x is no longer read
-                        }
-                    }
-                    if (!fine) break;
-                    umma_commit_warp(&kempty[gk % NK]);
-                    ++gk;
-                    issued_any = true;
-                }
                 bool first_pv[2] = {true, true};
-                for (int j = 0; fine && j < n; ++j) {
-                    const int fj = tl[j].flags;
-                    const int fn = (j + 1 < n) ? tl[j + 1].flags : 0;
-                    const int sv = gv % NV, sk = gk % NK;
-                    bool v_ready = false, k_ready = (j + 1 >= n);
+                for (int j = 0; fine && j <= n; ++j) {
+                    const int fq = (j < n) ? tl[j].flags : 0;       // QK products of tile j
+                    const int fp = (j >= 1) ? tl[j - 1].flags : 0;  // PV products of tile j - 1
+                    const int sk = gk % NK, sv = gv % NV;
+                    bool k_ready = false, v_ready = false;
                     for (int x = 0; x < 2 && fine; ++x) {
-                        if (fj & (2 << x)) {
+                        if (fq & (2 << x)) {
+                            if (u >= 1 && !wwait(sfree, (u - 1) & 1, 16, j)) { fine = false; break; }
+                            if (!k_ready) {
+                                if (!wwait(&kfull[sk], (gk / NK) & 1, 3, j)) { fine = false; break; }
+                                k_ready = true;
+                            }
+                            if (!need_q(x)) { fine = false; break; }
+                            tc_fence_after();
+                            issue_qk(tmem + COL_S, q_addr + x * TILE_BYTES, k_addr0 + sk * TILE_BYTES);
+                            umma_commit_warp(&sfull[x]);
+                            ++u;
+                            issued_any = true;
+                            if (j == last_used[x]) umma_commit_warp(&qempty[x]);  // the item's last QK_x product
+                        }
+                        if (fp & (2 << x)) {
                             if (!wwait(&pfull[x], cp[x] & 1, 4, j)) { fine = false; break; }
                             if (first_pv[x]) {  // O_x must have been read by the previous item's epilogue
                                 if (!wwait(&oempty[x], (ce[x] & 1) ^ 1, 11, j)) { fine = false; break; }
@@ -510,32 +513,21 @@ __global__ void __launch_bounds__(kThreads, 1) swa_prefill_tc_kernel(const __gri
                                 v_ready = true;
                             }
                             tc_fence_after();
-                            issue_pv(tmem + col_o(x), tmem + col_s(x), v_addr0 + sv * TILE_BYTES, !first_pv[x]);
+                            issue_pv(tmem + col_o(x), tmem + col_p(x), v_addr0 + sv * TILE_BYTES, !first_pv[x]);
                             first_pv[x] = false;
                             ++cp[x];
-                            if (j == last_used[x]) umma_commit_warp(&ofull[x]);
-                        }
-                        if (fn & (2 << x)) {  // S_x is free again once PV_x(j) has been issued
-                            if (!k_ready) {
-                                if (!wwait(&kfull[sk], (gk / NK) & 1, 3, j + 1)) { fine = false; break; }
-                                k_ready = true;
-                            }
-                            if (!need_q(x)) {
-                                fine = false;
-                                break;
-                            }
-                            tc_fence_after();
-                            issue_qk(tmem + col_s(x), q_addr + x * TILE_BYTES, k_addr0 + sk * TILE_BYTES);
-                            umma_commit_warp(&sfull[x]);
-                            if (j + 1 == last_used[x]) umma_commit_warp(&qempty[x]);  // the item's last QK_x product
+                            umma_commit_warp(&pempty[x]);
+                            if (j - 1 == last_used[x]) umma_commit_warp(&ofull[x]);
                         }
                     }
                     if (!fine) break;
-                    umma_commit_warp(&vempty[sv]);
-                    ++gv;
-                    if (j + 1 < n) {
+                    if (fq) {
                         umma_commit_warp(&kempty[sk]);
                         ++gk;
+                    }
+                    if (fp) {
+                        umma_commit_warp(&vempty[sv]);
+                        ++gv;
                     }
                 }
                 if (!fine) break;
@@ -559,73 +551,17 @@ __global__ void __launch_bounds__(kThreads, 1) swa_prefill_tc_kernel(const __gri
         }
     } else if (warp < 8) {
         // ------------------------------------------------------------------ softmax + epilogue
-        // All eight warps work on every S tile, in the order the MMA thread completes them (S_0(j), S_1(j),
-        // S_0(j+1), ...): warp w reads the TMEM lanes 32 (w mod 4) .. +31 (rows of the query tile) and the
-        // key half hf = w / 4 (columns 64 hf .. 64 hf + 63), so each row is split over two threads, which agree
-        // on the row maximum through shared memory (one named barrier of the 256 softmax threads per tile).
-        // Each thread keeps the running max and its half of the running sum of one row of each query tile.
-        // The epilogue of query tile x (O_x / l) runs when its O_x is next needed: just before the first S_x
-        // tile of the following item (or after the last item), so it overlaps the other tile's work.
-        const int hf = warp >> 2;                   // key half of this warp
-        const int r = threadIdx.x & (BH_ROWS - 1);  // row within a query tile == TMEM lane
+        const int x = warp >> 2;                    // query tile of this warpgroup
+        const int r = threadIdx.x & (BH_ROWS - 1);  // its row == TMEM lane
         const uint32_t lane_base = static_cast<uint32_t>((warp & 3) * 32) << 16;
-        float *xch = reinterpret_cast<float *>(sm + OFF_XCH);  // [2 slots][2 halves][128 rows]
+        const uint32_t s_addr = tmem + lane_base + COL_S;
+        const uint32_t p_addr = tmem + lane_base + col_p(x);
+        const uint32_t o_addr = tmem + lane_base + col_o(x);
         const float sl2 = P.scale_log2;
-        int cs[2] = {0, 0};  // S_x tiles processed (sfull / pfull parity)
-        int ne[2] = {0, 0};  // epilogues done (ofull parity)
-        int nx = 0;          // exchanges done (slot parity)
-        float mrun[2] = {-INFINITY, -INFINITY}, lrun[2] = {0.f, 0.f};  // running max (log2 units), half sum
-        struct Pending {
-            int on, row_start, bh, qlast;
-        } pend[2] = {{0, 0, 0, 0}, {0, 0, 0, 0}};
+        const int bit = 2 << x;
+        int cs = 0;  // tiles processed by this warpgroup (sfull / pfull / pempty parity)
+        int ne = 0;  // epilogues done (ofull parity)
         bool fine = true;
-        // The row value of this thread's partner (the other key half of the row), through shared memory.  The
-        // barrier also tells every softmax thread whether any of them failed a wait or saw the CTA abort flag
-        // (`stop`), so that all 256 leave together and none is left waiting at a later barrier.
-        const uint32_t abort_a = smem_u32(const_cast<int *>(abort_flag));
-        auto exchange = [&](float v, bool failed, bool &stop) -> float {
-            float *slot = xch + (nx & 1) * 256;
-            slot[hf * 128 + r] = v;
-            stop = named_barrier_or(1, 256, failed || ld_abort(abort_a) != 0);
-            ++nx;
-            return slot[(hf ^ 1) * 128 + r];
-        };
-        // O_x / l of the pending item of query tile x -> bf16 rows in global memory (and lse)
-        auto epilogue = [&](int x) -> bool {
-            const Pending pd = pend[x];
-            pend[x].on = 0;
-            const bool ok = __all_sync(0xFFFFFFFFu, mbar_wait(&ofull[x], ne[x] & 1, wc, 8, pd.row_start));
-            bool stop;
-            const float lpart = exchange(lrun[x], !ok, stop);
-            if (stop) return false;
-            ++ne[x];
-            tc_fence_after();
-            const float lsum = lrun[x] + lpart;
-            const float inv = (lsum > 0.f) ? 1.f / lsum : 0.f;
-            uint32_t ob[32];
-            __syncwarp();
-            const uint32_t o_addr = tmem + lane_base + col_o(x) + 64 * hf;
-#pragma unroll
-            for (int c = 0; c < 64; c += 32) {
-                float ov[32];
-                tmem_ld32(o_addr + c, ov);
-#pragma unroll
-                for (int i = 0; i < 16; ++i) ob[c / 2 + i] = pack_bf16x2(ov[2 * i] * inv, ov[2 * i + 1] * inv);
-            }
-            tc_fence_before();
-            mbar_arrive(&oempty[x]);
-            const int t = P.pos0 + pd.row_start + x * BH_ROWS + r;
-            if (t <= pd.qlast) {
-                const int64_t row = static_cast<int64_t>(pd.bh) * P.seq_stride + pd.row_start + x * BH_ROWS + r;
-                uint8_t *dst = reinterpret_cast<uint8_t *>(static_cast<__nv_bfloat16 *>(P.o) + row * HD + 64 * hf);
-#pragma unroll
-                for (int i = 0; i < 4; ++i)
-                    st_global_v8(dst + 32 * i, ob[8 * i], ob[8 * i + 1], ob[8 * i + 2], ob[8 * i + 3], ob[8 * i + 4],
-                                 ob[8 * i + 5], ob[8 * i + 6], ob[8 * i + 7]);
-                if (P.lse && hf == 0) P.lse[row] = (mrun[x] + log2f(lsum)) * 0.69314718055994531f;
-            }
-            return true;
-        };
         for (int it = 0; fine; ++it) {
             const int item = static_cast<int>(blockIdx.x) + it * G;
             if (item >= P.n_items) break;
@@ -633,141 +569,153 @@ __global__ void __launch_bounds__(kThreads, 1) swa_prefill_tc_kernel(const __gri
             const int row_start = (P.n_qpairs - 1 - item / P.BH) * BM;
             const int q0 = P.pos0 + row_start;
             const int qlast = P.pos0 + min(row_start + BM, P.L) - 1;
+            const int t = q0 + x * BH_ROWS + r;  // absolute position of this thread's row
             const int b = it & 1;
-            {
-                const bool ok = mbar_wait(&lready[b], (it >> 1) & 1, wc, 14, it);
-                if (named_barrier_or(1, 256, !ok || ld_abort(abort_a) != 0)) break;  // uniform: all or none go on
-            }
+            fine = __all_sync(0xFFFFFFFFu, mbar_wait(&lready[b], (it >> 1) & 1, wc, 14, it));
+            if (!fine) break;
             const Tile *tl = tiles_s + b * MAX_TILES;
             const int n = ntiles_s[b];
-            int cnt[2] = {0, 0};
-            for (int j = 0; j < n && fine; ++j) {
+            float mrun = -INFINITY, lrun = 0.f;  // running max (log2 units) and sum
+            int cnt = 0;
+            for (int j = 0; j < n; ++j) {
                 const Tile T = tl[j];
-                for (int x = 0; x < 2; ++x) {
-                    if (!(T.flags & (2 << x))) continue;
-                    if (cnt[x] == 0) {  // first S_x tile of this item: finish the previous item of tile x
-                        if (pend[x].on && !epilogue(x)) {
-                            fine = false;
-                            break;
-                        }
-                        mrun[x] = -INFINITY;
-                        lrun[x] = 0.f;
+                if (!(T.flags & bit)) continue;
+                fine = __all_sync(0xFFFFFFFFu, mbar_wait(&sfull[x], cs & 1, wc, 6, j));
+                if (!fine) break;
+                tc_fence_after();
+                // valid columns of this row: [0, b1] (sinks) and [a2, hc] (window), hc = last causal
+                // column, as four 32-bit column masks; interior tiles need none
+                const int hc = min(static_cast<int>(T.chi), t - T.pbase);
+                const int b1 = min(hc, P.s - 1 - T.pbase);
+                const int a2 = max(0, t - P.m + 1 - T.pbase);
+                bool full = (b1 >= BN - 1) || (hc >= BN - 1 && (a2 <= 0 || b1 >= a2 - 1));
+                uint32_t mw[4];
+#pragma unroll
+                for (int k = 0; k < 4; ++k)
+                    mw[k] = full ? 0xFFFFFFFFu : (range_bits(-32 * k, b1 - 32 * k) | range_bits(a2 - 32 * k, hc - 32 * k));
+                if (BS && !full && t <= qlast) {
+                    // block-sparse: also the global keys of the tile and the row's random key blocks, up to hc
+                    const TileMask gm = gmask_s[b * MAX_TILES + j];
+                    const int* rb = P.bs_rand + static_cast<int64_t>(t / P.bs_block) * P.bs_r;
+                    for (int i = 0; i < P.bs_r; ++i) {
+                        const int kb = rb[i];
+                        if (kb < 0) continue;
+                        const int lo = kb * P.bs_block - T.pbase;
+                        const int hi = min(lo + P.bs_block - 1, hc);
+#pragma unroll
+                        for (int k = 0; k < 4; ++k) mw[k] |= range_bits(lo - 32 * k, hi - 32 * k);
                     }
-                    const int t = q0 + x * BH_ROWS + r;  // absolute position of this thread's row
-                    const uint32_t s_addr = tmem + lane_base + col_s(x);
-                    const bool ok = __all_sync(0xFFFFFFFFu, mbar_wait(&sfull[x], cs[x] & 1, wc, 6, j));
+#pragma unroll
+                    for (int k = 0; k < 4; ++k) mw[k] |= gm.w[k] & range_bits(-32 * k, hc - 32 * k);
+                    full = (mw[0] & mw[1] & mw[2] & mw[3]) == 0xFFFFFFFFu;
+                }
+                const bool any_masked = __any_sync(0xFFFFFFFFu, !full);  // warp-uniform: no divergent paths
+                // the whole row of S in registers (one TMEM load); then the S buffer is free for the next QK
+                float sv[BN];
+                __syncwarp();
+                tmem_ld128(s_addr, sv);
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(sfree);
+                if (any_masked) {
+#pragma unroll
+                    for (int c = 0; c < BN; ++c) sv[c] = (mw[c >> 5] & (1u << (c & 31))) ? sv[c] : -INFINITY;
+                }
+                float mx4[4];
+#pragma unroll
+                for (int i = 0; i < 4; ++i) mx4[i] = fmax3(sv[i], sv[4 + i], sv[8 + i]);
+#pragma unroll
+                for (int c = 12; c < BN - 4; c += 8)
+#pragma unroll
+                    for (int i = 0; i < 4; ++i) mx4[i] = fmax3(mx4[i], sv[c + i], sv[c + 4 + i]);
+                const float mx = fmax3(fmax3(mx4[0], mx4[1], sv[BN - 4]), fmax3(mx4[2], mx4[3], sv[BN - 3]),
+                                       fmaxf(sv[BN - 2], sv[BN - 1])) * sl2;
+                float alpha = 1.f;
+                bool resc = false;
+                const float mnew = fmaxf(mrun, mx);
+                if (mnew > mrun + kRescaleLog2) {  // also taken when mrun is still -inf
+                    if (mrun != -INFINITY) {
+                        alpha = ex2(mrun - mnew);
+                        resc = true;
+                    }
+                    mrun = mnew;
+                }
+                // P_x and O_x are free once the PV_x products issued so far are done
+                if (cs >= 1) {
+                    fine = __all_sync(0xFFFFFFFFu, mbar_wait(&pempty[x], (cs - 1) & 1, wc, 7, j));
+                    if (!fine) break;
                     tc_fence_after();
-                    // this half of the score row in registers (not loaded after a failed wait: the exchange
-                    // below then stops every softmax thread)
-                    float sv[64];
+                }
+                if (__any_sync(0xFFFFFFFFu, resc)) {
+                    // O_x holds the PV products of this item's earlier tiles, all complete (pempty above)
                     __syncwarp();
-                    if (ok) tmem_ld64(s_addr + 64 * hf, sv);
-                    // valid columns of this row: [0, b1] (sinks) and [a2, hc] (window), hc = last causal
-                    // column, as 32-bit column masks of this half; interior tiles need none
-                    const int hc = min(static_cast<int>(T.chi), t - T.pbase);
-                    const int b1 = min(hc, P.s - 1 - T.pbase);
-                    const int a2 = max(0, t - P.m + 1 - T.pbase);
-                    bool full = (b1 >= BN - 1) || (hc >= BN - 1 && (a2 <= 0 || b1 >= a2 - 1));
-                    uint32_t mw[2];
-#pragma unroll
-                    for (int k = 0; k < 2; ++k) {
-                        const int c0 = 64 * hf + 32 * k;
-                        mw[k] = full ? 0xFFFFFFFFu : (range_bits(-c0, b1 - c0) | range_bits(a2 - c0, hc - c0));
-                    }
-                    if (BS && !full && t <= qlast) {
-                        // block-sparse: also the global keys of the tile and the row's random key blocks, up to hc
-                        const TileMask gm = gmask_s[b * MAX_TILES + j];
-                        const int *rb = P.bs_rand + static_cast<int64_t>(t / P.bs_block) * P.bs_r;
-                        for (int i = 0; i < P.bs_r; ++i) {
-                            const int kb = rb[i];
-                            if (kb < 0) continue;
-                            const int lo = kb * P.bs_block - T.pbase;
-                            const int hi = min(lo + P.bs_block - 1, hc);
-#pragma unroll
-                            for (int k = 0; k < 2; ++k) mw[k] |= range_bits(lo - 64 * hf - 32 * k, hi - 64 * hf - 32 * k);
-                        }
-#pragma unroll
-                        for (int k = 0; k < 2; ++k)
-                            mw[k] |= gm.w[2 * hf + k] & range_bits(-64 * hf - 32 * k, hc - 64 * hf - 32 * k);
-                        full = (mw[0] & mw[1]) == 0xFFFFFFFFu;
-                    }
-                    const bool any_masked = __any_sync(0xFFFFFFFFu, (mw[0] & mw[1]) != 0xFFFFFFFFu);
-                    if (any_masked) {
-#pragma unroll
-                        for (int c = 0; c < 64; ++c) sv[c] = (mw[c >> 5] & (1u << (c & 31))) ? sv[c] : -INFINITY;
-                    }
-                    float mx4[4];
-#pragma unroll
-                    for (int i = 0; i < 4; ++i) mx4[i] = fmax3(sv[i], sv[4 + i], sv[8 + i]);
-#pragma unroll
-                    for (int c = 12; c < 60; c += 8)
-#pragma unroll
-                        for (int i = 0; i < 4; ++i) mx4[i] = fmax3(mx4[i], sv[c + i], sv[c + 4 + i]);
-                    const float mxh = fmax3(fmax3(mx4[0], mx4[1], sv[60]), fmax3(mx4[2], mx4[3], sv[61]),
-                                            fmaxf(sv[62], sv[63]));
-                    // the whole row's maximum; both halves of a row take the same decisions from here on, and
-                    // every TMEM load of S_x is complete before either half stores P over it
-                    bool stop;
-                    const float mx = fmaxf(mxh, exchange(mxh, !ok, stop)) * sl2;
-                    if (stop) {
-                        fine = false;
-                        break;
-                    }
-                    float alpha = 1.f;
-                    bool resc = false;
-                    const float mnew = fmaxf(mrun[x], mx);
-                    if (mnew > mrun[x] + kRescaleLog2) {  // also taken when mrun is still -inf
-                        if (mrun[x] != -INFINITY) {
-                            alpha = ex2(mrun[x] - mnew);
-                            resc = true;
-                        }
-                        mrun[x] = mnew;
-                    }
-                    if (__any_sync(0xFFFFFFFFu, resc)) {
-                        // O_x holds the PV products of this item's earlier tiles; they are complete, because
-                        // S_x (issued after the last of them) is, and tcgen05 MMAs of one thread complete in order.
-                        __syncwarp();
-                        const uint32_t o_addr = tmem + lane_base + col_o(x) + 64 * hf;
 #pragma unroll 1
-                        for (int c = 0; c < 64; c += 32) {
-                            float ov[32];
-                            tmem_ld32(o_addr + c, ov);
+                    for (int c = 0; c < HD; c += 32) {
+                        float ov[32];
+                        tmem_ld32(o_addr + c, ov);
 #pragma unroll
-                            for (int i = 0; i < 32; ++i) ov[i] *= alpha;
-                            tmem_st32(o_addr + c, ov);
-                        }
+                        for (int i = 0; i < 32; ++i) ov[i] *= alpha;
+                        tmem_st32(o_addr + c, ov);
                     }
-                    // p = 2^(scale*log2(e)*s - m); bf16 pairs of this half's keys go to columns
-                    // [32 hf, 32 hf + 32) of S_x (the A operand of PV_x)
-                    const float nmu = (mrun[x] == -INFINITY) ? 0.f : -mrun[x];
-                    float rs4[4] = {0.f, 0.f, 0.f, 0.f};
+                }
+                // p = 2^(scale*log2(e)*s - m); bf16 pairs of keys 0..63 / 64..127 go to columns [0, 32) /
+                // [32, 64) of P_x: the A operand of PV_x
+                const float nmu = (mrun == -INFINITY) ? 0.f : -mrun;
+                float rs4[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+                for (int h = 0; h < 2; ++h) {
                     uint32_t pk[32];
 #pragma unroll
                     for (int i = 0; i < 32; ++i) {
+                        const int c = 64 * h + 2 * i;
                         float a0, a1;
-                        ffma2(a0, a1, sv[2 * i], sv[2 * i + 1], sl2, sl2, nmu, nmu);
+                        ffma2(a0, a1, sv[c], sv[c + 1], sl2, sl2, nmu, nmu);
                         const float p0 = ex2(a0), p1 = ex2(a1);
                         const int k = (i & 1) * 2;
                         fadd2(rs4[k], rs4[k + 1], rs4[k], rs4[k + 1], p0, p1);
                         pk[i] = pack_bf16x2(p0, p1);
                     }
                     __syncwarp();
-                    tmem_st32u_nowait(s_addr + 32 * hf, pk);
-                    tmem_wait_st();
-                    lrun[x] = lrun[x] * alpha + ((rs4[0] + rs4[1]) + (rs4[2] + rs4[3]));
-                    tc_fence_before();
-                    mbar_arrive(&pfull[x]);
-                    ++cnt[x];
-                    ++cs[x];
+                    tmem_st32u_nowait(p_addr + 32 * h, pk);
                 }
+                tmem_wait_st();
+                lrun = lrun * alpha + ((rs4[0] + rs4[1]) + (rs4[2] + rs4[3]));
+                tc_fence_before();
+                mbar_arrive(&pfull[x]);
+                ++cnt;
+                ++cs;
             }
             if (!fine) break;
             if (lane == 0) mbar_arrive(&lfree[b]);  // this warp no longer reads the tile list
-            for (int x = 0; x < 2; ++x)
-                if (cnt[x] > 0) pend[x] = {1, row_start, bh, qlast};
+            if (cnt == 0) continue;                // no row of this query tile in the sequence
+            // epilogue: O_x / l -> bf16 in registers, O_x handed back to the MMA, then the rows are
+            // written to global memory (and lse)
+            fine = __all_sync(0xFFFFFFFFu, mbar_wait(&ofull[x], ne & 1, wc, 8, it));
+            if (!fine) break;
+            ++ne;
+            tc_fence_after();
+            const float inv = (lrun > 0.f) ? 1.f / lrun : 0.f;
+            uint32_t ob[HD / 2];
+            __syncwarp();
+#pragma unroll
+            for (int c = 0; c < HD; c += 32) {
+                float ov[32];
+                tmem_ld32(o_addr + c, ov);
+#pragma unroll
+                for (int i = 0; i < 16; ++i) ob[c / 2 + i] = pack_bf16x2(ov[2 * i] * inv, ov[2 * i + 1] * inv);
+            }
+            tc_fence_before();
+            mbar_arrive(&oempty[x]);
+            if (t <= qlast) {
+                const int64_t row = static_cast<int64_t>(bh) * P.seq_stride + row_start + x * BH_ROWS + r;
+                uint8_t *dst = reinterpret_cast<uint8_t *>(static_cast<__nv_bfloat16 *>(P.o) + row * HD);
+#pragma unroll
+                for (int i = 0; i < HD / 16; ++i)
+                    st_global_v8(dst + 32 * i, ob[8 * i], ob[8 * i + 1], ob[8 * i + 2], ob[8 * i + 3], ob[8 * i + 4],
+                                 ob[8 * i + 5], ob[8 * i + 6], ob[8 * i + 7]);
+                if (P.lse) P.lse[row] = (mrun + log2f(lrun)) * 0.69314718055994531f;
+            }
         }
-        for (int x = 0; x < 2 && fine; ++x)
-            if (pend[x].on && !epilogue(x)) fine = false;
     }
 
     tc_fence_before();
