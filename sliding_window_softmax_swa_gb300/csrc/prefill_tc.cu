@@ -8,36 +8,31 @@
 // O(n^2) -> O(n k), banded patterns are hardware friendly), so each CTA walks only the key tiles that
 // intersect the band or the sink block of its query tile; no skipped tile is ever loaded.
 //
-// Work item = two query tiles of 128 rows (256 consecutive rows) of one (b, h).  The kernel is
-// persistent: one CTA per SM walks the items blockIdx.x, blockIdx.x + gridDim.x, ..., ordered
-// longest-first (the last query pairs of every head, whose windows are full, come first), so the short
-// items fall in the last rounds and the CTAs finish together.  352 threads in five roles:
-//   warps 0-3 / 4-7  softmax + epilogue of query tile 0 / 1: thread r owns row r of its tile
-//              (= TMEM lane r);
-//   warp 10    per item: builds the key-tile list into one of two buffers, one item ahead, loads Q_0 and
-//              Q_1 as soon as the previous item's last QK product is done, and prefetches the next
-//              item's Q into L2;
-//   warp 8     TMA producer: K tiles into a 2-stage ring and V tiles into a 2-stage ring (128 rows x
-//              128 bf16 each, two 64-column boxes with the 128-byte swizzle), as one stream over all
-//              items of the CTA.  A K slot frees as soon as the QK products that read it complete, a V
-//              slot after its PV products, so K loads run up to two tiles ahead, also into the next
-//              item;
-//   warp 9     MMA issuer (one thread).  Per key tile j: PV_0(j), QK_0(j+1), PV_1(j), QK_1(j+1), where
-//              QK_x(j) is S_x = Q_x K_j^T and PV_x(j) is O_x += P_x V_j with P_x (bf16) read by the MMA
-//              straight from tensor memory.  While the tensor cores work on one query tile, the softmax
-//              warpgroup of the other turns its S into P (ping-pong), and each K/V tile loaded from L2
-//              serves 256 query rows.  The next item's first QK products follow the current item's last
-//              PV products, so they overlap its epilogue; the next item's first PV_x waits until the
-//              epilogue has read O_x.
-// TMEM (512 columns): S_0, S_1 = [0,128), [128,256); O_0, O_1 = [256,384), [384,512) (fp32, lane = row).
-// The softmax threads overwrite the first 64 columns of S_x with P_x (two bf16 per column) after
-// reading them.  The online softmax keeps a running max in log2 units and only rescales O (TMEM load,
-// multiply, store) when the max grows by more than 8 (a factor 256), so p <= 256 always fits
-// bf16/fp32 and the rescale is rare; O and l always share the same reference max.  With one S buffer
-// per query tile, S_x(j) complete implies PV_x of the previous tile complete (tcgen05 MMAs of a thread
-// complete in order), so neither the P store nor the rescale needs another wait.
+// Work item = one query tile of 128 rows of one (b, h).  The kernel is persistent: one CTA per SM walks the
+// items blockIdx.x, blockIdx.x + gridDim.x, ..., ordered longest-first (the last query tiles of every head,
+// whose windows are full, come first), so the short items fall in the last rounds and the CTAs finish
+// together.  352 threads in four roles:
+//   warps 0-7  softmax + epilogue: warp w owns TMEM lanes 32 (w mod 4) .. +31 (rows of the tile) and the key
+//              half w / 4 of every score row, so each row is split over two threads of the warps w and w + 4,
+//              which agree on the row maximum through shared memory and a named barrier of the two warps;
+//   warp 8     TMA producers: lane 0 streams K tiles, lane 1 V tiles (128 rows x 128 bf16, two 64-column boxes
+//              with the 128-byte swizzle), each through its own 2-stage ring over all items of the CTA;
+//   warp 9     MMA issuer, the whole warp converged, one elected lane issuing: per item QK(0), then per key
+//              tile j QK(j+1), PV(j), where QK(j) is S = Q K_j^T into S buffer j mod 2 and PV(j) is O += P_j V_j
+//              with P_j (bf16 pairs written over the first 64 columns of its S buffer) read by the MMA straight
+//              from tensor memory.  QK products run one tile ahead of the softmax; S buffer j mod 2 is reused by
+//              QK(j+2) after PV(j) in issue order (tcgen05 MMAs of a thread complete in order);
+//   warp 10    per item: builds the key-tile list into one of two buffers, one item ahead, loads the item's Q
+//              into one of two Q buffers as soon as the last QK product of the buffer's previous item is done,
+//              and prefetches the next item's Q into L2.
+// TMEM (512 columns): S buffers [0,128), [128,256); O buffers [256,384), [384,512) for alternate items (fp32,
+// lane = row), so an item's epilogue (run after the next item's first tile) overlaps that item's products.
+// The online softmax keeps a running max in log2 units and only rescales O (TMEM load, multiply, store) when
+// the max grows by more than 8 (a factor 256), so p <= 256 always fits bf16/fp32 and the rescale is rare; O
+// and l always share the same reference max.  S_j complete implies PV(j-2) complete; a rescale at tile j first
+// waits for PV(j-1).
 //
-// Key tiles.  For the query rows [q0, q1] of a CTA the key positions needed are the sinks [0, min(s, blo)) and
+// Key tiles.  For the query rows [q0, q1] of an item the key positions needed are the sinks [0, min(s, blo)) and
 // the band [blo, q1] with blo = max(0, q0 - m + 1).  Positions >= pos0 are rows of this call's k/v;
 // positions < pos0 (chunked prefill) live in the rolling cache: slot p for p < s, slot
 // s + ((p - s) mod m) for the rest ("滑窗与固定稀疏", eq attn-fixed-rolling and eq attn-fixed-streaming).
@@ -63,8 +58,9 @@
 namespace swa {
 namespace tc {
 
-constexpr int BH_ROWS = 128;               // query rows per query tile (= TMEM lanes)
-constexpr int BM = 2 * BH_ROWS;            // query rows per CTA: two query tiles
+constexpr int BQ = 128;                    // query rows per work item (= TMEM lanes)
+constexpr int BH_ROWS = BQ;                // rows per query tile in the tile-list marks
+constexpr int BM = 2 * BQ;                 // rows of a query pair (the block-sparse lists are built per pair)
 constexpr int BN = 128;                    // keys per key tile
 constexpr int HD = 128;                    // head dimension
 constexpr int NK = 2;                      // K tile stages (a slot frees after its QK products)
@@ -72,13 +68,15 @@ constexpr int NV = 2;                      // V tile stages (a slot frees after 
 constexpr uint32_t HALF_BYTES = 128 * 128;  // one 64-column half of a 128-row bf16 tile (16 KB)
 constexpr uint32_t TILE_BYTES = 2 * HALF_BYTES;
 constexpr int MAX_TILES = 64;
-constexpr int kThreads = 352;  // warps 0-3 / 4-7: softmax of query tile 0 / 1; 8: TMA; 9: MMA; 10: tile lists
-constexpr int kWarpTma = 8, kWarpMma = 9, kWarpList = 10;
+constexpr int kSmWarps = 8;                    // softmax warps: four per key half of a tile
+constexpr int kSmThreads = kSmWarps * 32;
+constexpr int kWarpTma = kSmWarps, kWarpMma = kSmWarps + 1, kWarpList = kSmWarps + 2;
+constexpr int kThreads = (kSmWarps + 3) * 32;  // softmax warps, TMA producers, MMA issuer, tile lists
 constexpr uint32_t kTmemCols = 512;
-// TMEM columns: S (the scores of one query tile at a time, fp32), P_0, P_1 (bf16 pairs), O_0, O_1 (fp32)
-constexpr uint32_t COL_S = 0;
-__host__ __device__ constexpr uint32_t col_p(int x) { return 128u + static_cast<uint32_t>(x) * 64u; }
-__host__ __device__ constexpr uint32_t col_o(int x) { return 256u + static_cast<uint32_t>(x) * 128u; }
+// TMEM columns: S buffers 0, 1 (scores fp32, then P as bf16 pairs in their first 64 columns) and O buffers
+// 0, 1 (fp32 accumulators of alternate items)
+__host__ __device__ constexpr uint32_t col_s(int b) { return static_cast<uint32_t>(b) * 128u; }
+__host__ __device__ constexpr uint32_t col_o(int b) { return 256u + static_cast<uint32_t>(b) * 128u; }
 constexpr float kRescaleLog2 = 8.f;  // rescale O only when the running max grows by more than 2^8
 
 constexpr uint32_t OFF_Q = 0;                         // Q_0, Q_1
@@ -88,7 +86,8 @@ constexpr uint32_t OFF_BAR = OFF_V + NV * TILE_BYTES;
 constexpr uint32_t OFF_MISC = OFF_BAR + 256;
 constexpr uint32_t OFF_TILES = OFF_MISC + 64;
 constexpr uint32_t OFF_GMASK = OFF_TILES + 2 * MAX_TILES * 12;  // two tile lists (current / next item)
-constexpr uint32_t SMEM_USED = OFF_GMASK + 2 * MAX_TILES * 16;     // and their global-key columns (block-sparse)
+constexpr uint32_t OFF_XCH = OFF_GMASK + 2 * MAX_TILES * 16;       // and their global-key columns (block-sparse)
+constexpr uint32_t SMEM_USED = OFF_XCH + 2 * 2 * BQ * 4;             // row-value exchange of the softmax halves
 constexpr uint32_t SMEM_BYTES = SMEM_USED + 1024;  // slack to align the base to 1024 bytes
 static_assert(SMEM_BYTES <= 232448, "shared memory budget of one CTA");
 
@@ -122,7 +121,7 @@ struct Params {
     DeviceStatus *status;
     int64_t seq_stride;  // rows between (b, h) blocks of q/k/v/o/lse
     int L, pos0, w, s, m, BH;
-    int n_qpairs, n_items;  // 256-row query pairs per (b, h); work items = n_qpairs * BH
+    int n_qtiles, n_items;  // 128-row query tiles per (b, h); work items = n_qtiles * BH
     float scale_log2;
     uint32_t timeout_us;
 };
@@ -263,54 +262,48 @@ __global__ void __launch_bounds__(kThreads, 1) swa_prefill_tc_kernel(const __gri
     extern __shared__ uint8_t smem_raw[];
     uint8_t *sm = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     uint64_t *bars = reinterpret_cast<uint64_t *>(sm + OFF_BAR);
-    uint64_t *qfull = bars;           // [2]: Q_x of the current item landed
-    uint64_t *qempty = qfull + 2;     // [2]: the item's last QK_x product is done: Q_x may be reloaded
+    uint64_t *qfull = bars;           // [2]: Q buffer b landed
+    uint64_t *qempty = qfull + 2;     // [2]: the last QK product reading Q buffer b is done
     uint64_t *kfull = qempty + 2;     // [NK]
     uint64_t *kempty = kfull + NK;    // [NK]
     uint64_t *vfull = kempty + NK;    // [NV]
     uint64_t *vempty = vfull + NV;    // [NV]
-    uint64_t *sfull = vempty + NV;    // [2]: S = Q_x K_j^T ready (the S buffer holds query tile x's scores)
-    uint64_t *pfull = sfull + 2;      // [2]: P_x ready in TMEM (128 arrivals)
-    uint64_t *ofull = pfull + 2;      // [2]: the last PV_x product of an item is done
-    uint64_t *oempty = ofull + 2;     // [2]: O_x has been read by the epilogue (128 arrivals)
+    uint64_t *sfull = vempty + NV;    // [2]: S buffer b holds Q K_j^T
+    uint64_t *pfull = sfull + 2;      // P of the next tile written over its S buffer (all softmax threads)
+    uint64_t *pvdone = pfull + 1;     // [2]: the PV product reading S buffer b is done
+    uint64_t *ofull = pvdone + 2;     // [2]: the last PV product of an item into O buffer b is done
+    uint64_t *oempty = ofull + 2;     // [2]: O buffer b has been read by the epilogue (all softmax threads)
     uint64_t *lready = oempty + 2;    // [2]: tile list buffer b written (1 arrival)
-    uint64_t *lfree = lready + 2;     // [2]: tile list buffer b no longer read (8 softmax warps, MMA, 2 loaders)
+    uint64_t *lfree = lready + 2;     // [2]: tile list buffer b no longer read (softmax warps, MMA, 2 loaders)
     uint64_t *drain = lfree + 2;
-    uint64_t *sfree = drain + 1;      // the S buffer has been read by the softmax warps of its last user (4 warps)
-    uint64_t *pempty = sfree + 1;     // [2]: PV_x products issued so far are done (P_x and O_x free)
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(sm + OFF_MISC);
     volatile int *abort_flag = reinterpret_cast<volatile int *>(sm + OFF_MISC + 4);
     int *ntiles_s = reinterpret_cast<int *>(sm + OFF_MISC + 8);  // [2]
     Tile *tiles_s = reinterpret_cast<Tile *>(sm + OFF_TILES);     // [2][MAX_TILES]
     TileMask *gmask_s = reinterpret_cast<TileMask *>(sm + OFF_GMASK);  // [2][MAX_TILES] (block-sparse)
+    float *xch = reinterpret_cast<float *>(sm + OFF_XCH);              // [2 slots][2 halves][128 rows]
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int G = static_cast<int>(gridDim.x);
 
     if (threadIdx.x == 0) {
         *abort_flag = 0;
-        for (int i = 0; i < NK; ++i) {
+        for (int i = 0; i < 2; ++i) {
+            mbar_init(&qfull[i], 1);
+            mbar_init(&qempty[i], 1);
             mbar_init(&kfull[i], 1);
             mbar_init(&kempty[i], 1);
-        }
-        for (int i = 0; i < NV; ++i) {
             mbar_init(&vfull[i], 1);
             mbar_init(&vempty[i], 1);
+            mbar_init(&sfull[i], 1);
+            mbar_init(&pvdone[i], 1);
+            mbar_init(&ofull[i], 1);
+            mbar_init(&oempty[i], kSmThreads);
+            mbar_init(&lready[i], 1);
+            mbar_init(&lfree[i], kSmWarps + 3);
         }
-        for (int x = 0; x < 2; ++x) {
-            mbar_init(&qfull[x], 1);
-            mbar_init(&qempty[x], 1);
-            mbar_init(&sfull[x], 1);
-            mbar_init(&pfull[x], BH_ROWS);
-            mbar_init(&ofull[x], 1);
-            mbar_init(&oempty[x], BH_ROWS);
-            mbar_init(&lready[x], 1);
-            mbar_init(&lfree[x], 11);
-        }
+        mbar_init(pfull, kSmThreads);
         mbar_init(drain, 1);
-        mbar_init(sfree, 4);
-        mbar_init(&pempty[0], 1);
-        mbar_init(&pempty[1], 1);
         mbar_init_fence();
     }
     if (warp == 0) {
@@ -322,15 +315,20 @@ __global__ void __launch_bounds__(kThreads, 1) swa_prefill_tc_kernel(const __gri
     tc_fence_after();
     const uint32_t tmem = *tmem_slot;
     const WaitCtl wc{smem_u32(const_cast<int *>(abort_flag)), P.timeout_us, P.status};
+    // work item -> (b, h) and first row of its query tile (longest-first order: the last query tiles of
+    // every head, whose windows are full, come first)
+    auto item_rows = [&](int item, int &bh, int &row_start) {
+        bh = item % P.BH;
+        row_start = (P.n_qtiles - 1 - item / P.BH) * BQ;
+    };
 
     if (warp == kWarpTma) {
         // ------------------------------------------------------------------ TMA producers (K, V)
         // Lane 0 streams the K tiles, lane 1 the V tiles, each in its own ring over all items of this CTA in
-        // order, so neither waits for the other: a K slot frees when the QK products that read it are done,
-        // a V slot after its PV products, and the K loads run ahead into the next item on their own.
+        // order, so neither waits for the other: a K slot frees when the QK product that read it is done, a V
+        // slot after its PV product, and the K loads run ahead into the next item on their own.
         if (lane < 2) {
             const bool isk = lane == 0;
-            const int ns = isk ? NK : NV;
             uint64_t *full = isk ? kfull : vfull;
             uint64_t *empty = isk ? kempty : vempty;
             uint8_t *ring = sm + (isk ? OFF_K : OFF_V);
@@ -347,8 +345,8 @@ __global__ void __launch_bounds__(kThreads, 1) swa_prefill_tc_kernel(const __gri
                 const int bh = item % P.BH;
                 bool fine = true;
                 for (int j = 0; j < n; ++j) {
-                    const int st = g % ns;
-                    if (!mbar_wait(&empty[st], ((g / ns) & 1) ^ 1, wc, isk ? 1 : 9, j)) {
+                    const int st = g % NK;
+                    if (!mbar_wait(&empty[st], ((g / NK) & 1) ^ 1, wc, isk ? 1 : 9, j)) {
                         fine = false;
                         break;
                     }
@@ -364,181 +362,127 @@ __global__ void __launch_bounds__(kThreads, 1) swa_prefill_tc_kernel(const __gri
                 mbar_arrive(&lfree[b]);  // this lane no longer reads the item's list
             }
             if (*abort_flag) {  // make sure no copy is still landing in shared memory
-                for (int gg = (g > ns ? g - ns : 0); gg < g; ++gg) mbar_wait_drain(&full[gg % ns], (gg / ns) & 1);
+                for (int gg = (g > NK ? g - NK : 0); gg < g; ++gg) mbar_wait_drain(&full[gg % NK], (gg / NK) & 1);
             }
         }
     } else if (warp == kWarpList) {
-        // ------------------------------------------------------------------ tile lists
+        // ------------------------------------------------------------------ tile lists and Q
+        // Per item: the key-tile list goes to buffer it & 1 as soon as the buffer's previous item (it - 2) has
+        // been released by every reader; then the item's Q tile into Q buffer it & 1 as soon as the last QK
+        // product of item it - 2 (the buffer's previous user) is done, and the next item's Q into L2.
         if (lane == 0) {
-            // Per item: the key-tile list goes to buffer it & 1 as soon as the buffer's previous item
-            // (it - 2) has been released by every reader; then Q_0, Q_1 of the item, as soon as the previous
-            // item's last QK product is done (about two key tiles before that item ends), and the next
-            // item's Q into L2, so that its load does not wait for DRAM.
-            int nq = 0;              // items whose Q loads were issued
-            int nqx[2] = {0, 0};     // Q_x loads issued
+            int nq = 0;  // Q loads issued
             for (int it = 0;; ++it) {
                 const int item = static_cast<int>(blockIdx.x) + it * G;
                 if (item >= P.n_items) break;
-                const int bh = item % P.BH;
-                const int row_start = (P.n_qpairs - 1 - item / P.BH) * BM;
+                int bh, row_start;
+                item_rows(item, bh, row_start);
                 const int q0 = P.pos0 + row_start;
-                const int qlast = P.pos0 + min(row_start + BM, P.L) - 1;
+                const int qlast = P.pos0 + min(row_start + BQ, P.L) - 1;
                 const int b = it & 1;
                 if (it >= 2 && !mbar_wait(&lfree[b], ((it - 2) >> 1) & 1, wc, 12, it)) break;
                 Tile *tl = tiles_s + b * MAX_TILES;
-                int n;
-                if (BS) {  // the pair's list, built on the host
-                    const int qp = row_start / BM;
-                    n = P.bs_count[qp];
-                    if (n >= 1 && n <= MAX_TILES) {
+                int n = 0;
+                if (BS) {  // the tiles of the 256-row pair's host-built list that this query tile uses
+                    const int qp = row_start / (2 * BQ), bit = 2 << ((row_start / BQ) & 1);
+                    const int cnt = P.bs_count[qp];
+                    if (cnt >= 1 && cnt <= MAX_TILES) {
                         const Tile *src = P.bs_tiles + static_cast<int64_t>(qp) * MAX_TILES;
                         const TileMask *gsrc = P.bs_gmask + static_cast<int64_t>(qp) * MAX_TILES;
-                        for (int i = 0; i < n; ++i) {
-                            tl[i] = src[i];
-                            gmask_s[b * MAX_TILES + i] = gsrc[i];
+                        for (int i = 0; i < cnt; ++i) {
+                            if (!(src[i].flags & bit)) continue;
+                            tl[n] = src[i];
+                            tl[n].flags = static_cast<short>((src[i].flags & 1) | 2);
+                            gmask_s[b * MAX_TILES + n] = gsrc[i];
+                            ++n;
                         }
                     }
                 } else {
                     n = build_tiles(tl, q0, qlast, P.pos0, P.s, P.m, P.w, false);
+                    if (n >= 1 && n <= MAX_TILES) mark_tiles(tl, n, q0, qlast, P.s, P.m);
                 }
                 if (n < 1 || n > MAX_TILES) {
                     atomicOr(&P.status->word, kDevBadArg);
                     *abort_flag = 1;
                     break;
                 }
-                if (!BS) mark_tiles(tl, n, q0, qlast, P.s, P.m);
                 ntiles_s[b] = n;
                 mbar_arrive(&lready[b]);  // release: the list is visible to whoever sees the phase complete
-                // Q_x of the item, each as soon as the previous item's last QK_x product is done (query tile 0
-                // usually finishes a key tile before query tile 1)
-                bool qfine = true;
-                for (int x = 0; x < 2 && qfine; ++x) {
-                    if (nq >= 1 && !mbar_wait(&qempty[x], (nq - 1) & 1, wc, 13, it)) {
-                        qfine = false;
-                        break;
-                    }
-                    uint8_t *qs = sm + OFF_Q + x * TILE_BYTES;
-                    mbar_arrive_expect_tx(&qfull[x], TILE_BYTES);
-                    tma_load_3d(qs, &P.tm_q, &qfull[x], 0, row_start + x * BH_ROWS, bh);
-                    tma_load_3d(qs + HALF_BYTES, &P.tm_q, &qfull[x], 64, row_start + x * BH_ROWS, bh);
-                    nqx[x] = nq + 1;
-                }
-                if (!qfine) break;
+                // Q of the item, once the QK products of Q buffer b's previous item are done
+                if (it >= 2 && !mbar_wait(&qempty[b], ((it - 2) >> 1) & 1, wc, 13, it)) break;
+                uint8_t *qs = sm + OFF_Q + b * TILE_BYTES;
+                mbar_arrive_expect_tx(&qfull[b], TILE_BYTES);
+                tma_load_3d(qs, &P.tm_q, &qfull[b], 0, row_start, bh);
+                tma_load_3d(qs + HALF_BYTES, &P.tm_q, &qfull[b], 64, row_start, bh);
                 ++nq;
                 // into L2 meanwhile: the next item's Q rows
                 const int nitem = item + G;
                 if (nitem < P.n_items) {
-                    const int nrow = (P.n_qpairs - 1 - nitem / P.BH) * BM;
-                    for (int x = 0; x < 2; ++x) {
-                        tma_prefetch_3d(&P.tm_q, 0, nrow + x * BH_ROWS, nitem % P.BH);
-                        tma_prefetch_3d(&P.tm_q, 64, nrow + x * BH_ROWS, nitem % P.BH);
-                    }
+                    int nbh, nrow;
+                    item_rows(nitem, nbh, nrow);
+                    tma_prefetch_3d(&P.tm_q, 0, nrow, nbh);
+                    tma_prefetch_3d(&P.tm_q, 64, nrow, nbh);
                 }
             }
             if (*abort_flag) {  // no copy may still be landing
-                for (int x = 0; x < 2; ++x)
-                    if (nqx[x] > 0) mbar_wait_drain(&qfull[x], (nqx[x] - 1) & 1);
+                for (int i = (nq > 2 ? nq - 2 : 0); i < nq; ++i) mbar_wait_drain(&qfull[i & 1], (i >> 1) & 1);
             }
         }
     } else if (warp == kWarpMma) {
         // ------------------------------------------------------------------ MMA issuer
-        // One S buffer serves the two query tiles in turn, and P_x has TMEM columns of its own, so a QK
-        // product needs only the S buffer to have been read by the softmax warps of its previous user, not
-        // their whole softmax.  Per key tile j of an item: QK_0(j), PV_0(j-1), QK_1(j), PV_1(j-1): the tensor
-        // cores take the next QK products while the softmax warps still compute the previous tile's
-        // exponentials.  The whole warp runs the loop (uniform operands); one elected lane issues each
-        // instruction.
+        // Per item with key tiles 0..n-1: QK(0), then per j: QK(j + 1), PV(j).  S buffer j & 1 holds Q K_j^T
+        // until the softmax has read it, then P_j (bf16 pairs in its first 64 columns) until PV(j) has read
+        // it; QK(j + 2) reuses the buffer after PV(j) in issue order (tcgen05 MMAs of a thread run in order),
+        // so QK products run one tile ahead of the softmax.  Items alternate between the O buffers, so an
+        // item's first PV product waits only for the epilogue of the item before the previous one.  The whole
+        // warp runs the loop (uniform operands); one elected lane issues each instruction.
         {
             auto wwait = [&](uint64_t *bar, int parity, unsigned site, unsigned tag) -> bool {
                 return __all_sync(0xFFFFFFFFu, mbar_wait(bar, static_cast<uint32_t>(parity), wc, site, tag));
             };
-            const uint32_t q_addr = smem_u32(sm + OFF_Q);
+            const uint32_t q_addr0 = smem_u32(sm + OFF_Q);
             const uint32_t k_addr0 = smem_u32(sm + OFF_K), v_addr0 = smem_u32(sm + OFF_V);
             bool issued_any = false, fine = true;
-            int gk = 0, gv = 0;                // K, V tiles consumed
-            int cp[2] = {0, 0};                // PV_x products issued (pfull parity)
-            int ce[2] = {0, 0};                // items in which query tile x had PV products (oempty)
-            int qf[2] = {0, 0};                // Q_x loads consumed (qfull parity)
-            int u = 0;                         // QK products issued into the S buffer (sfree parity)
+            int gk = 0, gv = 0;  // K, V tiles consumed
+            int u = 0;           // QK products issued (S buffer u & 1)
+            int pv = 0;          // PV products issued (pfull parity, S buffer pv & 1)
             for (int it = 0; fine; ++it) {
                 const int item = static_cast<int>(blockIdx.x) + it * G;
                 if (item >= P.n_items) break;
-                const int b = it & 1;
-                if (!wwait(&lready[b], (it >> 1) & 1, 14, it)) break;  // the item's tile list
-                bool qready[2] = {false, false};
-                // Q_x of this item, waited for before its first QK_x product
-                auto need_q = [&](int x) -> bool {
-                    if (qready[x]) return true;
-                    if (!wwait(&qfull[x], qf[x] & 1, 2, it)) return false;
-                    ++qf[x];
-                    qready[x] = true;
-                    tc_fence_after();
-                    return true;
-                };
-                const Tile *tl = tiles_s + b * MAX_TILES;
+                const int b = it & 1;  // tile list, Q and O buffer of this item
+                if (!wwait(&lready[b], (it >> 1) & 1, 14, it)) break;
+                if (!wwait(&qfull[b], (it >> 1) & 1, 2, it)) break;
+                tc_fence_after();
                 const int n = ntiles_s[b];
-                int last_used[2] = {-1, -1};
-                for (int j = 0; j < n; ++j)
-                    for (int x = 0; x < 2; ++x)
-                        if (tl[j].flags & (2 << x)) last_used[x] = j;
-                bool first_pv[2] = {true, true};
+                const uint32_t q_addr = q_addr0 + b * TILE_BYTES;
+                const uint32_t o_col = col_o(b);
                 for (int j = 0; fine && j <= n; ++j) {
-                    const int fq = (j < n) ? tl[j].flags : 0;       // QK products of tile j
-                    const int fp = (j >= 1) ? tl[j - 1].flags : 0;  // PV products of tile j - 1
-                    const int sk = gk % NK, sv = gv % NV;
-                    bool k_ready = false, v_ready = false;
-                    for (int x = 0; x < 2 && fine; ++x) {
-                        if (fq & (2 << x)) {
-                            if (u >= 1 && !wwait(sfree, (u - 1) & 1, 16, j)) { fine = false; break; }
-                            if (!k_ready) {
-                                if (!wwait(&kfull[sk], (gk / NK) & 1, 3, j)) { fine = false; break; }
-                                k_ready = true;
-                            }
-                            if (!need_q(x)) { fine = false; break; }
-                            tc_fence_after();
-                            issue_qk(tmem + COL_S, q_addr + x * TILE_BYTES, k_addr0 + sk * TILE_BYTES);
-                            umma_commit_warp(&sfull[x]);
-                            ++u;
-                            issued_any = true;
-                            if (j == last_used[x]) umma_commit_warp(&qempty[x]);  // the item's last QK_x product
-                        }
-                        if (fp & (2 << x)) {
-                            if (!wwait(&pfull[x], cp[x] & 1, 4, j)) { fine = false; break; }
-                            if (first_pv[x]) {  // O_x must have been read by the previous item's epilogue
-                                if (!wwait(&oempty[x], (ce[x] & 1) ^ 1, 11, j)) { fine = false; break; }
-                                ++ce[x];
-                            }
-                            if (!v_ready) {
-                                if (!wwait(&vfull[sv], (gv / NV) & 1, 5, j)) { fine = false; break; }
-                                v_ready = true;
-                            }
-                            tc_fence_after();
-                            issue_pv(tmem + col_o(x), tmem + col_p(x), v_addr0 + sv * TILE_BYTES, !first_pv[x]);
-                            first_pv[x] = false;
-                            ++cp[x];
-                            umma_commit_warp(&pempty[x]);
-                            if (j - 1 == last_used[x]) umma_commit_warp(&ofull[x]);
-                        }
-                    }
-                    if (!fine) break;
-                    if (fq) {
+                    if (j < n) {  // QK(j)
+                        const int sk = gk % NK;
+                        if (!wwait(&kfull[sk], (gk / NK) & 1, 3, j)) { fine = false; break; }
+                        tc_fence_after();
+                        issue_qk(tmem + col_s(u & 1), q_addr, k_addr0 + sk * TILE_BYTES);
+                        umma_commit_warp(&sfull[u & 1]);
                         umma_commit_warp(&kempty[sk]);
+                        if (j == n - 1) umma_commit_warp(&qempty[b]);  // the item's last QK product
                         ++gk;
+                        ++u;
+                        issued_any = true;
                     }
-                    if (fp) {
-                        umma_commit_warp(&vempty[sv]);
-                        ++gv;
-                    }
-                }
-                if (!fine) break;
-                // a query tile with no key tile in this item still takes its Q load and releases it
-                for (int x = 0; x < 2 && fine; ++x) {
-                    if (last_used[x] < 0) {
-                        if (!need_q(x)) {
-                            fine = false;
-                            break;
+                    if (j >= 1) {  // PV(j - 1)
+                        const int sv = gv % NV;
+                        if (!wwait(pfull, pv & 1, 4, j)) { fine = false; break; }
+                        if (j == 1 && it >= 2) {  // O buffer b must have been read by item it - 2's epilogue
+                            if (!wwait(&oempty[b], ((it - 2) >> 1) & 1, 11, j)) { fine = false; break; }
                         }
-                        umma_commit_warp(&qempty[x]);
+                        if (!wwait(&vfull[sv], (gv / NV) & 1, 5, j)) { fine = false; break; }
+                        tc_fence_after();
+                        issue_pv(tmem + o_col, tmem + col_s(pv & 1), v_addr0 + sv * TILE_BYTES, j > 1);
+                        umma_commit_warp(&pvdone[pv & 1]);
+                        umma_commit_warp(&vempty[sv]);
+                        if (j == n) umma_commit_warp(&ofull[b]);  // the item's last PV product
+                        ++gv;
+                        ++pv;
                     }
                 }
                 if (!fine) break;
@@ -551,85 +495,151 @@ __global__ void __launch_bounds__(kThreads, 1) swa_prefill_tc_kernel(const __gri
         }
     } else if (warp < 8) {
         // ------------------------------------------------------------------ softmax + epilogue
-        const int x = warp >> 2;                    // query tile of this warpgroup
-        const int r = threadIdx.x & (BH_ROWS - 1);  // its row == TMEM lane
+        // All eight warps work on every S tile, in issue order: warp w reads the TMEM lanes 32 (w mod 4) .. +31
+        // (rows of the query tile) and the key half hf = w / 4 (columns 64 hf .. 64 hf + 63), so each row is
+        // split over two threads, which agree on the row maximum through shared memory (one named barrier of
+        // the two warps per tile).  The epilogue of an item (O / l) runs after the first tile of the
+        // next item, so the tensor cores already have that item's QK and PV products to work on.
+        const int hf = warp >> 2;                // key half of this warp
+        // the two warps that share rows (w and w + 4) synchronise only with each other: named barrier 1 + w mod 4
+        const uint32_t pair_bar = 1u + static_cast<uint32_t>(warp & 3);
+        const int r = threadIdx.x & (BQ - 1);    // row within the query tile == TMEM lane
         const uint32_t lane_base = static_cast<uint32_t>((warp & 3) * 32) << 16;
-        const uint32_t s_addr = tmem + lane_base + COL_S;
-        const uint32_t p_addr = tmem + lane_base + col_p(x);
-        const uint32_t o_addr = tmem + lane_base + col_o(x);
         const float sl2 = P.scale_log2;
-        const int bit = 2 << x;
-        int cs = 0;  // tiles processed by this warpgroup (sfull / pfull / pempty parity)
-        int ne = 0;  // epilogues done (ofull parity)
+        const uint32_t abort_a = smem_u32(const_cast<int *>(abort_flag));
+        int v = 0;   // S tiles processed (S buffer v & 1, sfull / pvdone parity)
+        int nx = 0;  // exchanges done (slot parity)
+        float mrun = -INFINITY, lrun = 0.f;  // running max (log2 units) and this half's running sum
+        struct Pending {
+            int on, it, bh, row_start, qlast;
+            float m, l;
+        } pend = {0, 0, 0, 0, 0, 0.f, 0.f};
         bool fine = true;
+        // The row value of this thread's partner (the other key half of the row), through shared memory.  The
+        // barrier of the two warps also tells both whether either failed a wait or saw the CTA abort flag
+        // (`stop`), so that they leave together and neither is left waiting at a later barrier; no barrier spans
+        // more than one such pair, so pairs that leave at different times never wait for each other.
+        auto exchange = [&](float val, bool failed, bool &stop) -> float {
+            float *slot = xch + (nx & 1) * 256;
+            slot[hf * 128 + r] = val;
+            stop = named_barrier_or(pair_bar, 64, failed || ld_abort(abort_a) != 0);
+            ++nx;
+            return slot[(hf ^ 1) * 128 + r];
+        };
+        // O / l of the pending item -> bf16 rows in global memory (and lse)
+        auto epilogue = [&]() -> bool {
+            const Pending pd = pend;
+            pend.on = 0;
+            const int b = pd.it & 1;
+            const bool ok = __all_sync(0xFFFFFFFFu, mbar_wait(&ofull[b], (pd.it >> 1) & 1, wc, 8, pd.it));
+            bool stop;
+            const float lpart = exchange(pd.l, !ok, stop);
+            if (stop) return false;
+            tc_fence_after();
+            const float lsum = pd.l + lpart;
+            const float inv = (lsum > 0.f) ? 1.f / lsum : 0.f;
+            uint32_t ob[32];
+            __syncwarp();
+            const uint32_t o_addr = tmem + lane_base + col_o(b) + 64 * hf;
+#pragma unroll
+            for (int c = 0; c < 64; c += 32) {
+                float ov[32];
+                tmem_ld32(o_addr + c, ov);
+#pragma unroll
+                for (int i = 0; i < 16; ++i) ob[c / 2 + i] = pack_bf16x2(ov[2 * i] * inv, ov[2 * i + 1] * inv);
+            }
+            tc_fence_before();
+            mbar_arrive(&oempty[b]);
+            const int t = P.pos0 + pd.row_start + r;
+            if (t <= pd.qlast) {
+                const int64_t row = static_cast<int64_t>(pd.bh) * P.seq_stride + pd.row_start + r;
+                uint8_t *dst = reinterpret_cast<uint8_t *>(static_cast<__nv_bfloat16 *>(P.o) + row * HD + 64 * hf);
+#pragma unroll
+                for (int i = 0; i < 4; ++i)
+                    st_global_v8(dst + 32 * i, ob[8 * i], ob[8 * i + 1], ob[8 * i + 2], ob[8 * i + 3], ob[8 * i + 4],
+                                 ob[8 * i + 5], ob[8 * i + 6], ob[8 * i + 7]);
+                if (P.lse && hf == 0) P.lse[row] = (pd.m + log2f(lsum)) * 0.69314718055994531f;
+            }
+            return true;
+        };
         for (int it = 0; fine; ++it) {
             const int item = static_cast<int>(blockIdx.x) + it * G;
             if (item >= P.n_items) break;
-            const int bh = item % P.BH;
-            const int row_start = (P.n_qpairs - 1 - item / P.BH) * BM;
+            int bh, row_start;
+            item_rows(item, bh, row_start);
             const int q0 = P.pos0 + row_start;
-            const int qlast = P.pos0 + min(row_start + BM, P.L) - 1;
-            const int t = q0 + x * BH_ROWS + r;  // absolute position of this thread's row
+            const int qlast = P.pos0 + min(row_start + BQ, P.L) - 1;
+            const int t = q0 + r;  // absolute position of this thread's row
             const int b = it & 1;
-            fine = __all_sync(0xFFFFFFFFu, mbar_wait(&lready[b], (it >> 1) & 1, wc, 14, it));
-            if (!fine) break;
+            {
+                const bool ok = mbar_wait(&lready[b], (it >> 1) & 1, wc, 14, it);
+                if (named_barrier_or(pair_bar, 64, !ok || ld_abort(abort_a) != 0)) break;  // both warps or none go on
+            }
             const Tile *tl = tiles_s + b * MAX_TILES;
             const int n = ntiles_s[b];
-            float mrun = -INFINITY, lrun = 0.f;  // running max (log2 units) and sum
-            int cnt = 0;
-            for (int j = 0; j < n; ++j) {
+            const uint32_t o_addr = tmem + lane_base + col_o(b) + 64 * hf;
+            mrun = -INFINITY;
+            lrun = 0.f;
+            for (int j = 0; j < n && fine; ++j) {
                 const Tile T = tl[j];
-                if (!(T.flags & bit)) continue;
-                fine = __all_sync(0xFFFFFFFFu, mbar_wait(&sfull[x], cs & 1, wc, 6, j));
-                if (!fine) break;
+                const int sb = v & 1;
+                const uint32_t s_addr = tmem + lane_base + col_s(sb);
+                const bool ok = __all_sync(0xFFFFFFFFu, mbar_wait(&sfull[sb], (v >> 1) & 1, wc, 6, j));
                 tc_fence_after();
-                // valid columns of this row: [0, b1] (sinks) and [a2, hc] (window), hc = last causal
-                // column, as four 32-bit column masks; interior tiles need none
+                // this half of the score row in registers (not loaded after a failed wait: the exchange below
+                // then stops every softmax thread)
+                float sv[64];
+                __syncwarp();
+                if (ok) tmem_ld64(s_addr + 64 * hf, sv);
+                // valid columns of this row: [0, b1] (sinks) and [a2, hc] (window), hc = last causal column, as
+                // 32-bit column masks of this half; interior tiles need none
                 const int hc = min(static_cast<int>(T.chi), t - T.pbase);
                 const int b1 = min(hc, P.s - 1 - T.pbase);
                 const int a2 = max(0, t - P.m + 1 - T.pbase);
-                bool full = (b1 >= BN - 1) || (hc >= BN - 1 && (a2 <= 0 || b1 >= a2 - 1));
-                uint32_t mw[4];
+                const bool full = (b1 >= BN - 1) || (hc >= BN - 1 && (a2 <= 0 || b1 >= a2 - 1));
+                uint32_t mw[2];
 #pragma unroll
-                for (int k = 0; k < 4; ++k)
-                    mw[k] = full ? 0xFFFFFFFFu : (range_bits(-32 * k, b1 - 32 * k) | range_bits(a2 - 32 * k, hc - 32 * k));
+                for (int k = 0; k < 2; ++k) {
+                    const int c0 = 64 * hf + 32 * k;
+                    mw[k] = full ? 0xFFFFFFFFu : (range_bits(-c0, b1 - c0) | range_bits(a2 - c0, hc - c0));
+                }
                 if (BS && !full && t <= qlast) {
                     // block-sparse: also the global keys of the tile and the row's random key blocks, up to hc
                     const TileMask gm = gmask_s[b * MAX_TILES + j];
-                    const int* rb = P.bs_rand + static_cast<int64_t>(t / P.bs_block) * P.bs_r;
+                    const int *rb = P.bs_rand + static_cast<int64_t>(t / P.bs_block) * P.bs_r;
                     for (int i = 0; i < P.bs_r; ++i) {
                         const int kb = rb[i];
                         if (kb < 0) continue;
                         const int lo = kb * P.bs_block - T.pbase;
                         const int hi = min(lo + P.bs_block - 1, hc);
 #pragma unroll
-                        for (int k = 0; k < 4; ++k) mw[k] |= range_bits(lo - 32 * k, hi - 32 * k);
+                        for (int k = 0; k < 2; ++k) mw[k] |= range_bits(lo - 64 * hf - 32 * k, hi - 64 * hf - 32 * k);
                     }
 #pragma unroll
-                    for (int k = 0; k < 4; ++k) mw[k] |= gm.w[k] & range_bits(-32 * k, hc - 32 * k);
-                    full = (mw[0] & mw[1] & mw[2] & mw[3]) == 0xFFFFFFFFu;
+                    for (int k = 0; k < 2; ++k)
+                        mw[k] |= gm.w[2 * hf + k] & range_bits(-64 * hf - 32 * k, hc - 64 * hf - 32 * k);
                 }
-                const bool any_masked = __any_sync(0xFFFFFFFFu, !full);  // warp-uniform: no divergent paths
-                // the whole row of S in registers (one TMEM load); then the S buffer is free for the next QK
-                float sv[BN];
-                __syncwarp();
-                tmem_ld128(s_addr, sv);
-                tc_fence_before();
-                __syncwarp();
-                if (lane == 0) mbar_arrive(sfree);
-                if (any_masked) {
+                if (__any_sync(0xFFFFFFFFu, (mw[0] & mw[1]) != 0xFFFFFFFFu)) {
 #pragma unroll
-                    for (int c = 0; c < BN; ++c) sv[c] = (mw[c >> 5] & (1u << (c & 31))) ? sv[c] : -INFINITY;
+                    for (int c = 0; c < 64; ++c) sv[c] = (mw[c >> 5] & (1u << (c & 31))) ? sv[c] : -INFINITY;
                 }
                 float mx4[4];
 #pragma unroll
                 for (int i = 0; i < 4; ++i) mx4[i] = fmax3(sv[i], sv[4 + i], sv[8 + i]);
 #pragma unroll
-                for (int c = 12; c < BN - 4; c += 8)
+                for (int c = 12; c < 60; c += 8)
 #pragma unroll
                     for (int i = 0; i < 4; ++i) mx4[i] = fmax3(mx4[i], sv[c + i], sv[c + 4 + i]);
-                const float mx = fmax3(fmax3(mx4[0], mx4[1], sv[BN - 4]), fmax3(mx4[2], mx4[3], sv[BN - 3]),
-                                       fmaxf(sv[BN - 2], sv[BN - 1])) * sl2;
+                const float mxh =
+                    fmax3(fmax3(mx4[0], mx4[1], sv[60]), fmax3(mx4[2], mx4[3], sv[61]), fmaxf(sv[62], sv[63]));
+                // the whole row's maximum; both halves of a row take the same decisions from here on, and every
+                // TMEM load of this S buffer is complete before either half stores P over it
+                bool stop;
+                const float mx = fmaxf(mxh, exchange(mxh, !ok, stop)) * sl2;
+                if (stop) {
+                    fine = false;
+                    break;
+                }
                 float alpha = 1.f;
                 bool resc = false;
                 const float mnew = fmaxf(mrun, mx);
@@ -640,82 +650,55 @@ __global__ void __launch_bounds__(kThreads, 1) swa_prefill_tc_kernel(const __gri
                     }
                     mrun = mnew;
                 }
-                // P_x and O_x are free once the PV_x products issued so far are done
-                if (cs >= 1) {
-                    fine = __all_sync(0xFFFFFFFFu, mbar_wait(&pempty[x], (cs - 1) & 1, wc, 7, j));
-                    if (!fine) break;
-                    tc_fence_after();
-                }
                 if (__any_sync(0xFFFFFFFFu, resc)) {
-                    // O_x holds the PV products of this item's earlier tiles, all complete (pempty above)
-                    __syncwarp();
+                    // O holds the PV products of this item's earlier tiles: S_j complete implies PV(j - 2) complete
+                    // (in-order MMAs); wait for PV(j - 1), the product of the other S buffer (j >= 1 here)
+                    // (a failed wait sets the CTA abort flag; the next exchange then stops every softmax thread)
+                    if (__all_sync(0xFFFFFFFFu, mbar_wait(&pvdone[sb ^ 1], ((v - 1) >> 1) & 1, wc, 7, j))) {
+                        tc_fence_after();
+                        __syncwarp();
 #pragma unroll 1
-                    for (int c = 0; c < HD; c += 32) {
-                        float ov[32];
-                        tmem_ld32(o_addr + c, ov);
+                        for (int c = 0; c < 64; c += 32) {
+                            float ov[32];
+                            tmem_ld32(o_addr + c, ov);
 #pragma unroll
-                        for (int i = 0; i < 32; ++i) ov[i] *= alpha;
-                        tmem_st32(o_addr + c, ov);
+                            for (int i = 0; i < 32; ++i) ov[i] *= alpha;
+                            tmem_st32(o_addr + c, ov);
+                        }
                     }
                 }
-                // p = 2^(scale*log2(e)*s - m); bf16 pairs of keys 0..63 / 64..127 go to columns [0, 32) /
-                // [32, 64) of P_x: the A operand of PV_x
+                // p = 2^(scale*log2(e)*s - m); bf16 pairs of this half's keys go to columns [32 hf, 32 hf + 32)
+                // of the S buffer: the A operand of PV(j)
                 const float nmu = (mrun == -INFINITY) ? 0.f : -mrun;
                 float rs4[4] = {0.f, 0.f, 0.f, 0.f};
+                uint32_t pk[32];
 #pragma unroll
-                for (int h = 0; h < 2; ++h) {
-                    uint32_t pk[32];
-#pragma unroll
-                    for (int i = 0; i < 32; ++i) {
-                        const int c = 64 * h + 2 * i;
-                        float a0, a1;
-                        ffma2(a0, a1, sv[c], sv[c + 1], sl2, sl2, nmu, nmu);
-                        const float p0 = ex2(a0), p1 = ex2(a1);
-                        const int k = (i & 1) * 2;
-                        fadd2(rs4[k], rs4[k + 1], rs4[k], rs4[k + 1], p0, p1);
-                        pk[i] = pack_bf16x2(p0, p1);
-                    }
-                    __syncwarp();
-                    tmem_st32u_nowait(p_addr + 32 * h, pk);
+                for (int i = 0; i < 32; ++i) {
+                    float a0, a1;
+                    ffma2(a0, a1, sv[2 * i], sv[2 * i + 1], sl2, sl2, nmu, nmu);
+                    const float p0 = ex2(a0), p1 = ex2(a1);
+                    const int k = (i & 1) * 2;
+                    fadd2(rs4[k], rs4[k + 1], rs4[k], rs4[k + 1], p0, p1);
+                    pk[i] = pack_bf16x2(p0, p1);
                 }
+                __syncwarp();
+                tmem_st32u_nowait(s_addr + 32 * hf, pk);
                 tmem_wait_st();
                 lrun = lrun * alpha + ((rs4[0] + rs4[1]) + (rs4[2] + rs4[3]));
                 tc_fence_before();
-                mbar_arrive(&pfull[x]);
-                ++cnt;
-                ++cs;
+                mbar_arrive(pfull);
+                ++v;
+                // the previous item's epilogue, once this item's first P is on its way to the tensor cores
+                if (j == 0 && pend.on && !epilogue()) {
+                    fine = false;
+                    break;
+                }
             }
             if (!fine) break;
             if (lane == 0) mbar_arrive(&lfree[b]);  // this warp no longer reads the tile list
-            if (cnt == 0) continue;                // no row of this query tile in the sequence
-            // epilogue: O_x / l -> bf16 in registers, O_x handed back to the MMA, then the rows are
-            // written to global memory (and lse)
-            fine = __all_sync(0xFFFFFFFFu, mbar_wait(&ofull[x], ne & 1, wc, 8, it));
-            if (!fine) break;
-            ++ne;
-            tc_fence_after();
-            const float inv = (lrun > 0.f) ? 1.f / lrun : 0.f;
-            uint32_t ob[HD / 2];
-            __syncwarp();
-#pragma unroll
-            for (int c = 0; c < HD; c += 32) {
-                float ov[32];
-                tmem_ld32(o_addr + c, ov);
-#pragma unroll
-                for (int i = 0; i < 16; ++i) ob[c / 2 + i] = pack_bf16x2(ov[2 * i] * inv, ov[2 * i + 1] * inv);
-            }
-            tc_fence_before();
-            mbar_arrive(&oempty[x]);
-            if (t <= qlast) {
-                const int64_t row = static_cast<int64_t>(bh) * P.seq_stride + row_start + x * BH_ROWS + r;
-                uint8_t *dst = reinterpret_cast<uint8_t *>(static_cast<__nv_bfloat16 *>(P.o) + row * HD);
-#pragma unroll
-                for (int i = 0; i < HD / 16; ++i)
-                    st_global_v8(dst + 32 * i, ob[8 * i], ob[8 * i + 1], ob[8 * i + 2], ob[8 * i + 3], ob[8 * i + 4],
-                                 ob[8 * i + 5], ob[8 * i + 6], ob[8 * i + 7]);
-                if (P.lse) P.lse[row] = (mrun + log2f(lrun)) * 0.69314718055994531f;
-            }
+            pend = {1, it, bh, row_start, qlast, mrun, lrun};
         }
+        if (fine && pend.on) epilogue();
     }
 
     tc_fence_before();
@@ -877,7 +860,7 @@ static int launch_impl(const PrefillArgs &a, const BlockSparseDev *bs) {
     if (a.q_sink) return fail(SWA_ERR_INVALID, "the RoPE prefill runs on the sub-tile kernel");
     if (!bs && max_tiles_bound(a.w, a.s) > MAX_TILES)
         return fail(SWA_ERR_UNSUPPORTED, "window w=%d needs more than %d key tiles per query tile", a.w, MAX_TILES);
-    if ((a.L + BM - 1) / BM * a.BH > 0x7FFFFFFF) return fail(SWA_ERR_UNSUPPORTED, "too many work items");
+    if ((a.L + BQ - 1) / BQ * a.BH > 0x7FFFFFFF) return fail(SWA_ERR_UNSUPPORTED, "too many work items");
     if (!encode_tiled_fn()) return fail(SWA_ERR_CUDA, "cuTensorMapEncodeTiled is not available");
     unsigned *status = device_status_word();
     if (!status) return SWA_ERR_CUDA;
@@ -907,8 +890,8 @@ static int launch_impl(const PrefillArgs &a, const BlockSparseDev *bs) {
     p.s = a.s;
     p.m = a.w - a.s;
     p.BH = a.BH;
-    p.n_qpairs = static_cast<int>((a.L + BM - 1) / BM);
-    p.n_items = p.n_qpairs * a.BH;
+    p.n_qtiles = static_cast<int>((a.L + BQ - 1) / BQ);
+    p.n_items = p.n_qtiles * a.BH;
     p.scale_log2 = a.scale * 1.4426950408889634f;
     p.timeout_us = kWaitTimeoutUs;
     if (bs) {
