@@ -1,7 +1,8 @@
 """The key walks of the bf16 prefill kernels (host-callable, same functions as on the device) cover every
 key of every query row exactly once, with the right position in every column (CPU only).
 
-The plain kernel walks tiles of up to 128 keys, the RoPE kernel sub-tiles of up to 64; for each the library
+The plain kernel walks, per 128-row query tile, tiles of up to 128 keys; the RoPE kernel, per 256-row pair of
+query tiles, sub-tiles of up to 64; for each the library
 reports (source, first row, position of column 0, last valid column, mask of the query tiles that compute
 it).  Column c <= last holds source row (first row + c).  For the rolling cache the position stored in a slot comes from the oracle's sequential
 replay of the writes; for the call's own rows it is pos0 + row.  Membership of a position in the key set of
@@ -18,7 +19,8 @@ import sliding_window_softmax_swa_gb300 as swa
 BN = 128   # keys per tile of the plain kernel's walk
 SUB = 64   # keys per sub-tile of the RoPE kernel's walk
 BQ = 128   # rows per query tile
-BM = 256   # query rows per CTA (two query tiles)
+BM = 256   # query rows per work item of the RoPE kernel (two query tiles)
+PQ = 128   # query rows per work item of the plain kernel (one query tile)
 
 
 def check_plan(q0, q1, pos0, w, s, L, plan=None, width=BN):
@@ -57,9 +59,9 @@ def check_plan(q0, q1, pos0, w, s, L, plan=None, width=BN):
                                  (300, 200), (256, 130), (17, 16)])
 def test_whole_sequence_tiles(w, s):
     L = 3000
-    for qt in range(0, (L + BM - 1) // BM):
-        q0 = qt * BM
-        q1 = min(q0 + BM, L) - 1
+    for qt in range(0, (L + PQ - 1) // PQ):
+        q0 = qt * PQ
+        q1 = min(q0 + PQ, L) - 1
         check_plan(q0, q1, 0, w, s, L)
 
 
@@ -71,9 +73,9 @@ def test_chunked_tiles_random():
         pos0 = rng.choice([1, 2, s, s + 1, w - 1, w, w + 1, 3 * w + 7, rng.randrange(1, 5 * w + 10)])
         pos0 = max(1, pos0)
         L = rng.randrange(1, 700)
-        qt = rng.randrange(0, (L + BM - 1) // BM)
-        q0 = pos0 + qt * BM
-        q1 = pos0 + min(qt * BM + BM, L) - 1
+        qt = rng.randrange(0, (L + PQ - 1) // PQ)
+        q0 = pos0 + qt * PQ
+        q1 = pos0 + min(qt * PQ + PQ, L) - 1
         check_plan(q0, q1, pos0, w, s, L)
 
 
@@ -81,22 +83,19 @@ def test_chunked_tiles_long_window_boundaries():
     # the chunk shapes of a 131072-token prompt in 4096-token chunks with w = 4096, s = 4
     w, s, C = 4096, 4, 4096
     for pos0 in (C, 2 * C, 7 * C, 31 * C):
-        for qt in (0, 1, 7, 8, 15):
-            q0 = pos0 + qt * BM
-            plan = check_plan(q0, q0 + BM - 1, pos0, w, s, C)
-            assert len(plan) <= 38
+        for qt in (0, 1, 7, 8, 15, 16, 31):
+            q0 = pos0 + qt * PQ
+            plan = check_plan(q0, q0 + PQ - 1, pos0, w, s, C)
+            assert len(plan) <= 37
 
 
 def test_tile_count_is_minimal_for_full_windows():
-    # a full-window pair of query tiles walks ceil((m + 255) / 128) band tiles plus one sink tile, and each
-    # query tile uses only the ceil((m + 127) / 128) band tiles its own rows reach (plus the sink tile)
+    # a full-window query tile walks the ceil((m + 127) / 128) band tiles its rows reach plus one sink tile
     for w, s in [(1024, 4), (4096, 4), (4096, 0)]:
         m = w - s
-        plan = swa.prefill_tile_plan(8192, 8192 + BM - 1, 0, w, s)
-        assert len(plan) == (m + 255 + BN - 1) // BN + (1 if s else 0)
-        for x in (0, 1):
-            used = sum(1 for tl in plan if (tl[4] >> x) & 1)
-            assert used == (m + 127 + BN - 1) // BN + (1 if s else 0)
+        plan = swa.prefill_tile_plan(8192, 8192 + PQ - 1, 0, w, s)
+        assert len(plan) == (m + 127 + BN - 1) // BN + (1 if s else 0)
+        assert all(tl[4] == 1 for tl in plan)
 
 
 def test_rope_sub_tile_count_is_minimal_for_full_windows():
