@@ -64,7 +64,7 @@ typedef enum { SWA_BF16 = 0, SWA_F32 = 1 } swa_dtype;
  *   B, H, L, d, w, s : batch, heads, rows, head dim, window (keys per query, sinks included), sinks.
  *             Requires 0 <= s < w, L >= 0 (L == 0 is a no-op), pos0 + L < 2^31.
  *   scale   : softmax scale (1/sqrt(d) for the usual attention).
- *   dtype   : SWA_BF16 requires d == 128 (tensor-core path: TMA + tcgen05 + TMEM);
+ *   dtype   : SWA_BF16 requires d in {64, 128} (tensor-core path: TMA + tcgen05 + TMEM);
  *             SWA_F32 accepts d in {16, 32, 64, 128} (CUDA-core path).
  */
 int swa_sink_prefill(const void *q, const void *k, const void *v, void *o, float *lse,
@@ -102,10 +102,11 @@ int swa_sink_prefill_host(const void *q_h, const void *k_h, const void *v_h, voi
  *   q, k, v, o, lse : as swa_sink_prefill, with q and k unrotated; bf16, d = 128, contiguous.
  *   rope_base : finite and > 1.
  *   workspace : caller-owned device scratch of swa_sink_prefill_rope_workspace_size(B, H, L, d) bytes
- *             (3 x B*H*L*d bf16: the rotated q, the sink-rotated q and the rotated k), 256-byte aligned.
- *   s <= 128, pos0 = 0 only (SWA_ERR_UNSUPPORTED otherwise).  The rotated q and k are rounded to bf16
- *   before the tensor-core products, which adds up to 2^-8 relative error per product term to the
- *   scores.  Other arguments and errors as swa_sink_prefill.
+ *             (6 x B*H*L*d bf16: the rotated q, the sink-rotated q and the rotated k, each as a bf16 pair
+ *             hi + lo whose sum is the fp32 rotation), 256-byte aligned.
+ *   s <= 128, pos0 = 0 only (SWA_ERR_UNSUPPORTED otherwise).  Each score is formed from three tensor-core
+ *   products of the pairs (hi.hi + hi.lo + lo.hi), so the rotation adds about fp32 rounding, not bf16
+ *   rounding, to the scores.  Other arguments and errors as swa_sink_prefill.
  */
 int swa_sink_prefill_rope(const void *q, const void *k, const void *v, void *o, float *lse, int B, int H,
                           int64_t L, int d, int w, int s, float scale, double rope_base, void *workspace,
@@ -124,8 +125,8 @@ size_t swa_sink_prefill_rope_workspace_size(int B, int H, int64_t L, int d);
  *   rope_base : finite and > 1.
  *   workspace : caller-owned device scratch of swa_sink_prefill_chunked_rope_workspace_size(B, H, L, d, w)
  *             bytes, 256-byte aligned: the rotated q, the sink-rotated q and the rotated k of the whole
- *             sequence (one rotation pass serves every chunk: rotations depend on absolute positions only)
- *             and a [B, H, w, d] cache of rotated keys.
+ *             sequence as bf16 hi/lo pairs (one rotation pass serves every chunk: rotations depend on
+ *             absolute positions only) and two [B, H, w, d] caches of rotated keys (hi and lo).
  *   s <= 128 (SWA_ERR_UNSUPPORTED otherwise).  Other arguments and errors as swa_sink_prefill_chunked.
  */
 int swa_sink_prefill_chunked_rope(const void *q, const void *k, const void *v, void *o, float *lse, void *k_cache,
