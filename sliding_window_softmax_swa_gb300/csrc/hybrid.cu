@@ -12,8 +12,10 @@
 // shared memory, fp32 accumulators in TMEM), with W2 = [wf^T ; -wf^T] (128 x d) so that one product gives
 // both halves of f and phi is exp of it:
 //   1. chunk states, per (head, key chunk j of 128 keys): f(K_j)^T = W2 K_j^T, phi(K_j)^T = exp(.) with the
-//      sinks and the keys past the end zeroed, D_j = phi(K_j)^T V_j (d x d) and z_j = phi(K_j)^T 1;
-//   2. an exclusive scan over j in place: P_j = sum_{j' < j} D_j' (the state of the keys before chunk j);
+//      sinks and the keys past the end zeroed (kept, bf16, for step 3), D_j = phi(K_j)^T V_j (d x d, stored as
+//      bf16) and z_j = phi(K_j)^T 1 (fp32);
+//   2. an exclusive scan over j in place, summed in fp32: P_j = sum_{j' < j} D_j' (the state of the keys before
+//      chunk j, bf16: it enters the tensor cores as an operand);
 //   3. per (head, query tile of 128 rows at a): J = floor((a - m + 1) / 128) (every key below 128 J has left
 //      the window of every row of the tile), then
 //          num = phi(Q) P_J + sum over the <= 2 key tiles from 128 J: (phi(Q) phi(K)^T masked to i <= t - m,
@@ -36,7 +38,6 @@ constexpr int D = 128;                      // head dimension (and feature dimen
 constexpr int C = 128;                      // keys per chunk / rows per query tile
 constexpr uint32_t HALF = 128 * 128;        // one 64-column half of a [128 x 128] bf16 tile
 constexpr uint32_t TILE = 2 * HALF;
-constexpr int STATE_FLOATS = D * D + D;     // D_j / P_j (row-major [feature][column]) then z_j
 constexpr uint32_t IDESC_KK = idesc_bf16_f32(128, 128, false, false);  // A K-major, B K-major (A B^T)
 constexpr uint32_t IDESC_KM = idesc_bf16_f32(128, 128, false, true);   // A K-major, B MN-major (A B)
 constexpr float LOG2E = 1.4426950408889634f;
@@ -70,26 +71,17 @@ __device__ __forceinline__ void st_row32(uint32_t tile, int r, int c0, const flo
     }
 }
 
-// W2 = [wf^T ; -wf^T] into a tile (row j = feature j, columns = the d input coordinates); 128 threads.
-// wf: [d][d/2] bf16 row-major (f = x wf).  Negating a bf16 is exact.
-__device__ __forceinline__ void stage_w2(uint32_t tile, const __nv_bfloat16 *__restrict__ wf) {
-    const int j = threadIdx.x;
-    const int col = j & 63;
+// W2 = [wf^T ; -wf^T] as a row-major [128 x d] bf16 image in global memory (TMA-loaded by the kernels below);
+// grid 128 (row j = feature j) x 128 threads (column x).
+__global__ void __launch_bounds__(128) w2_kernel(const __nv_bfloat16 *__restrict__ wf, __nv_bfloat16 *w2) {
+    const int j = blockIdx.x, x = threadIdx.x;
     const uint16_t sign = j >= 64 ? 0x8000u : 0u;
-    for (int c0 = 0; c0 < D; c0 += 8) {
-        uint32_t u[4];
-#pragma unroll
-        for (int h = 0; h < 4; ++h) {
-            const uint16_t lo = __bfloat16_as_ushort(wf[(c0 + 2 * h) * (D / 2) + col]) ^ sign;
-            const uint16_t hi = __bfloat16_as_ushort(wf[(c0 + 2 * h + 1) * (D / 2) + col]) ^ sign;
-            u[h] = static_cast<uint32_t>(lo) | (static_cast<uint32_t>(hi) << 16);
-        }
-        st_shared_v4(tile + (c0 >> 6) * HALF + sw128_offset(j, c0 & 63), u[0], u[1], u[2], u[3]);
-    }
+    w2[j * D + x] = __ushort_as_bfloat16(__bfloat16_as_ushort(wf[x * (D / 2) + (j & 63)]) ^ sign);
 }
 
+// TMEM address of this warp's 32 lanes (warp w may access lanes 32 (w mod 4) .. +31) at column col.
 __device__ __forceinline__ uint32_t lane_addr(uint32_t tmem, int col) {
-    return tmem + (static_cast<uint32_t>((threadIdx.x >> 5) * 32) << 16) + col;
+    return tmem + (static_cast<uint32_t>(((threadIdx.x >> 5) & 3) * 32) << 16) + col;
 }
 
 // Shared state of one CTA: barriers, TMEM base, abort flag.
@@ -122,20 +114,23 @@ __device__ __forceinline__ void operands_written() {
 
 // ---- 1. chunk states ------------------------------------------------------------------------------
 // grid (chunks, BH), 128 threads.  Key chunk j: keys j*C .. j*C + C - 1; a key counts when s <= key < key_end.
-// out: [BH][chunks][STATE_FLOATS].  Final mode (prefix != nullptr): one chunk per head (index chunk0); the
-// prefix state of that chunk (from the scanned states) is added and the sum goes to out_s [BH][d][d] and
-// out_z [BH][d].
+// Writes, per (bh, j): dmat = D_j = phi(K_j)^T V_j (bf16, row = feature, column = value column), zst = z_j
+// (fp32) and phik = phi(K_j)^T (bf16, row = feature, column = key of the chunk), each [BH][chunks][128][...].
+// Final mode (fin_s != nullptr): one chunk per head (index chunk0); the scanned prefix of that chunk (dmat,
+// zst after the scan) is added to its D and z, and the sums go to fin_s [BH][d][d] and fin_z [BH][d] (fp32).
 __global__ void __launch_bounds__(128, 1) chunk_state_kernel(const __grid_constant__ CUtensorMap mk,
                                                              const __grid_constant__ CUtensorMap mv,
-                                                             const __nv_bfloat16 *__restrict__ wf, float *out,
-                                                             const float *__restrict__ prefix, float *out_s,
-                                                             float *out_z, int chunk0, int nchunks, int s,
-                                                             int64_t key_end, DeviceStatus *status) {
+                                                             const __grid_constant__ CUtensorMap mw2,
+                                                             __nv_bfloat16 *dmat, float *zst, __nv_bfloat16 *phik,
+                                                             float *fin_s, float *fin_z, int chunk0, int nchunks,
+                                                             int s, int64_t key_end, DeviceStatus *status) {
     extern __shared__ uint8_t smem_raw[];
     uint8_t *sm = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     uint8_t *Tw = sm, *Tk = sm + TILE, *Tv = sm + 2 * TILE;
     Ctl *ctl = reinterpret_cast<Ctl *>(sm + 3 * TILE);
     const int j = chunk0 + static_cast<int>(blockIdx.x), bh = blockIdx.y, r = threadIdx.x;
+    const bool fin = fin_s != nullptr;
+    const int64_t rec = static_cast<int64_t>(bh) * nchunks + j;  // (bh, chunk) record index
     if (r == 0) {
         ctl->abort_flag = 0;
         mbar_init(&ctl->load_bar, 1);
@@ -146,14 +141,14 @@ __global__ void __launch_bounds__(128, 1) chunk_state_kernel(const __grid_consta
         tmem_alloc(&ctl->tmem, 256);
         tmem_relinquish();
     }
-    stage_w2(smem_u32(Tw), wf);
     operands_written();
     const uint32_t tmem = ctl->tmem;
     const WaitCtl wc{smem_u32(&ctl->abort_flag), kWaitTimeoutUs, status};
     if (r == 0) {
         tma_prefetch_desc(&mk);
         tma_prefetch_desc(&mv);
-        mbar_arrive_expect_tx(&ctl->load_bar, 2 * TILE);
+        mbar_arrive_expect_tx(&ctl->load_bar, 3 * TILE);
+        load_tile(Tw, &mw2, &ctl->load_bar, 0, 0);
         load_tile(Tk, &mk, &ctl->load_bar, j * C, bh);
         load_tile(Tv, &mv, &ctl->load_bar, j * C, bh);
         if (mbar_wait(&ctl->load_bar, 0, wc, 40)) {
@@ -169,6 +164,7 @@ __global__ void __launch_bounds__(128, 1) chunk_state_kernel(const __grid_consta
     if (fine) {
         // phi(K)^T row r (feature r) over the 128 keys; uncounted keys are zero
         const int64_t k0 = static_cast<int64_t>(j) * C;
+        uint4 *prow = reinterpret_cast<uint4 *>(phik + (rec * D + r) * C);
         for (int c0 = 0; c0 < C; c0 += 32) {
             float x[32];
             tmem_ld32(lane_addr(tmem, c0), x);
@@ -179,6 +175,12 @@ __global__ void __launch_bounds__(128, 1) chunk_state_kernel(const __grid_consta
                 z += x[i];
             }
             st_row32(smem_u32(Tk), r, c0, x);
+            if (!fin) {
+#pragma unroll
+                for (int g = 0; g < 4; ++g)
+                    prow[c0 / 8 + g] = make_uint4(pack_bf16x2(x[8 * g], x[8 * g + 1]), pack_bf16x2(x[8 * g + 2], x[8 * g + 3]),
+                                                  pack_bf16x2(x[8 * g + 4], x[8 * g + 5]), pack_bf16x2(x[8 * g + 6], x[8 * g + 7]));
+            }
         }
     }
     operands_written();
@@ -188,25 +190,37 @@ __global__ void __launch_bounds__(128, 1) chunk_state_kernel(const __grid_consta
     }
     fine = wait_mma(ctl, 1, wc, 42) && fine;
     if (fine) {
-        const bool fin = prefix != nullptr;
-        float *dst = fin ? out_s + static_cast<int64_t>(bh) * D * D
-                         : out + (static_cast<int64_t>(bh) * nchunks + j) * STATE_FLOATS;
-        const float *pre = fin ? prefix + (static_cast<int64_t>(bh) * nchunks + j) * STATE_FLOATS : nullptr;
+        const __nv_bfloat16 *pre = dmat + (rec * D + r) * D;
         for (int c0 = 0; c0 < D; c0 += 32) {
             float x[32];
             tmem_ld32(lane_addr(tmem, 128 + c0), x);
-            if (fin) {
+            if (fin) {  // + the prefix, to fp32
+                const uint4 *pp = reinterpret_cast<const uint4 *>(pre + c0);
 #pragma unroll
-                for (int i = 0; i < 32; ++i) x[i] += pre[r * D + c0 + i];
+                for (int g = 0; g < 4; ++g) {
+                    const uint4 u = pp[g];
+                    const uint32_t w4[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+                    for (int h = 0; h < 4; ++h) {
+                        x[8 * g + 2 * h] += __uint_as_float(w4[h] << 16);
+                        x[8 * g + 2 * h + 1] += __uint_as_float(w4[h] & 0xFFFF0000u);
+                    }
+                }
+                float4 *p4 = reinterpret_cast<float4 *>(fin_s + (static_cast<int64_t>(bh) * D + r) * D + c0);
+#pragma unroll
+                for (int i = 0; i < 8; ++i) p4[i] = make_float4(x[4 * i], x[4 * i + 1], x[4 * i + 2], x[4 * i + 3]);
+            } else {
+                uint4 *pd = reinterpret_cast<uint4 *>(dmat + (rec * D + r) * D + c0);
+#pragma unroll
+                for (int g = 0; g < 4; ++g)
+                    pd[g] = make_uint4(pack_bf16x2(x[8 * g], x[8 * g + 1]), pack_bf16x2(x[8 * g + 2], x[8 * g + 3]),
+                                       pack_bf16x2(x[8 * g + 4], x[8 * g + 5]), pack_bf16x2(x[8 * g + 6], x[8 * g + 7]));
             }
-            float4 *p4 = reinterpret_cast<float4 *>(dst + r * D + c0);
-#pragma unroll
-            for (int i = 0; i < 8; ++i) p4[i] = make_float4(x[4 * i], x[4 * i + 1], x[4 * i + 2], x[4 * i + 3]);
         }
         if (fin)
-            out_z[static_cast<int64_t>(bh) * D + r] = z + pre[D * D + r];
+            fin_z[static_cast<int64_t>(bh) * D + r] = z + zst[rec * D + r];
         else
-            dst[D * D + r] = z;
+            zst[rec * D + r] = z;
     }
     tc_fence_before();
     __syncthreads();
@@ -216,160 +230,188 @@ __global__ void __launch_bounds__(128, 1) chunk_state_kernel(const __grid_consta
     }
 }
 
-// ---- 2. exclusive scan over the chunks, in place ------------------------------------------------------
-__global__ void __launch_bounds__(256) scan_kernel(float *st, int nchunks, int64_t total) {
+// ---- 2. exclusive scan over the chunks, in place: per (bh, pair of matrix entries) in bf16 with an fp32
+// running sum, per (bh, feature) for z in fp32 ---------------------------------------------------------------
+__global__ void __launch_bounds__(256) scan_kernel(uint32_t *dmat, float *zst, int nchunks, int64_t npairs,
+                                                   int64_t nz) {
     const int64_t e = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
-    if (e >= total) return;
-    const int64_t bh = e / STATE_FLOATS, k = e % STATE_FLOATS;
-    float *p = st + bh * nchunks * STATE_FLOATS + k;
-    float run = 0.f;
-    for (int j = 0; j < nchunks; ++j) {
-        const float x = p[static_cast<int64_t>(j) * STATE_FLOATS];
-        p[static_cast<int64_t>(j) * STATE_FLOATS] = run;
-        run += x;
+    constexpr int PAIRS = D * D / 2;  // bf16 pairs per record
+    if (e < npairs) {
+        const int64_t bh = e / PAIRS, k = e % PAIRS;
+        uint32_t *p = dmat + bh * nchunks * PAIRS + k;
+        float r0 = 0.f, r1 = 0.f;
+        for (int j0 = 0; j0 < nchunks; j0 += 16) {  // 16 independent loads in flight, then their prefix
+            uint32_t x[16];
+#pragma unroll
+            for (int i = 0; i < 16; ++i)
+                if (j0 + i < nchunks) x[i] = p[static_cast<int64_t>(j0 + i) * PAIRS];
+#pragma unroll
+            for (int i = 0; i < 16; ++i)
+                if (j0 + i < nchunks) {
+                    p[static_cast<int64_t>(j0 + i) * PAIRS] = pack_bf16x2(r0, r1);
+                    r0 += __uint_as_float(x[i] << 16);
+                    r1 += __uint_as_float(x[i] & 0xFFFF0000u);
+                }
+        }
+    } else if (e < npairs + nz) {
+        const int64_t f = e - npairs, bh = f / D, k = f % D;
+        float *p = zst + bh * nchunks * D + k;
+        float run = 0.f;
+        for (int j0 = 0; j0 < nchunks; j0 += 16) {
+            float x[16];
+#pragma unroll
+            for (int i = 0; i < 16; ++i)
+                if (j0 + i < nchunks) x[i] = p[static_cast<int64_t>(j0 + i) * D];
+#pragma unroll
+            for (int i = 0; i < 16; ++i)
+                if (j0 + i < nchunks) {
+                    p[static_cast<int64_t>(j0 + i) * D] = run;
+                    run += x[i];
+                }
+        }
     }
 }
 
 // ---- 3. linear branch + combination ----------------------------------------------------------------------
-// grid (query tiles, BH), 128 threads; thread r owns query row a + r (and feature r where a tile is indexed by
-// feature).  o holds the SWA prefill's output on entry and the hybrid output on exit; lse is the SWA prefill's.
-__global__ void __launch_bounds__(128, 1) linear_kernel(const __grid_constant__ CUtensorMap mq,
-                                                        const __grid_constant__ CUtensorMap mk,
+// grid (query tiles, BH), 256 threads; thread r (mod 128) owns query row a + r (TMEM lane r) and the column half
+// h = warp / 4 of it.  All loads are issued at once: the Q tile, phi(K)^T and V of the <= 2 key chunks from 128 J, and the
+// prefix state P_J (bf16, from the scan).  TMEM: f(Q), then the scores of chunk J, columns [0, 128); the scores
+// of chunk J + 1, [128, 256); the numerator, [256, 384).  The masked scores go back over their own TMEM columns
+// as bf16 pairs, the A operand of their product with V.  o holds the SWA prefill's output on entry and the hybrid
+// output on exit; lse is the SWA prefill's.
+// A from TMEM: keys 0..63 as bf16 pairs in columns [0, 32), keys 64..127 in columns [64, 96) (each key half is
+// written by the threads that read that half of the scores).
+__device__ __forceinline__ void mma_tv(uint32_t d, uint32_t a_tmem, uint32_t b, bool acc) {
+#pragma unroll
+    for (int kk = 0; kk < 8; ++kk)
+        umma_ts(d, a_tmem + kk * 8 + (kk >= 4 ? 32 : 0), sdesc_sw128(b + kk * 2048, HALF, 1024), IDESC_KM,
+                (acc || kk) ? 1u : 0u);
+}
+
+__global__ void __launch_bounds__(256, 1) linear_kernel(const __grid_constant__ CUtensorMap mq,
                                                         const __grid_constant__ CUtensorMap mv,
-                                                        const __nv_bfloat16 *__restrict__ wf,
-                                                        const float *__restrict__ pstate, __nv_bfloat16 *o,
+                                                        const __grid_constant__ CUtensorMap mpk,
+                                                        const __grid_constant__ CUtensorMap mpj,
+                                                        const __grid_constant__ CUtensorMap mw2,
+                                                        const float *__restrict__ zst, __nv_bfloat16 *o,
                                                         const float *__restrict__ lse, int64_t L, int m, int s,
                                                         int nchunks, DeviceStatus *status) {
     const int64_t a = static_cast<int64_t>(blockIdx.x) * C;
-    const int bh = blockIdx.y, r = threadIdx.x;
+    const int bh = blockIdx.y, r = threadIdx.x & (C - 1), hh = threadIdx.x >> 7;
     const int64_t last = (a + C < L ? a + C : L) - 1;
     if (last - m < s) return;  // no row of the tile has a key outside its window yet
     extern __shared__ uint8_t smem_raw[];
     uint8_t *sm = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-    uint8_t *Tq = sm, *Tw = sm + TILE, *Tk = sm + 2 * TILE, *Tv = sm + 3 * TILE, *Tp = sm + 4 * TILE;
-    Ctl *ctl = reinterpret_cast<Ctl *>(sm + 5 * TILE);
-    if (r == 0) {
+    uint8_t *Tq = sm, *Tw = sm + TILE, *Tk0 = sm + 2 * TILE, *Tk1 = sm + 3 * TILE, *Tv0 = sm + 4 * TILE,
+            *Tv1 = sm + 5 * TILE, *Tp = sm + 6 * TILE;
+    Ctl *ctl = reinterpret_cast<Ctl *>(sm + 7 * TILE);
+    uint64_t *kv_bar = reinterpret_cast<uint64_t *>(sm + 7 * TILE + 64);
+    const int64_t J = a - m + 1 > 0 ? (a - m + 1) / C : 0;
+    const bool two = J * C + C <= last - m;  // the tile's rows reach into chunk J + 1
+    const bool has_p = J > 0;
+    float *dx = reinterpret_cast<float *>(sm + 7 * TILE + 128);  // [2][128] the halves' parts of the denominators
+    const bool t0 = threadIdx.x == 0;
+    if (t0) {
         ctl->abort_flag = 0;
         mbar_init(&ctl->load_bar, 1);
         mbar_init(&ctl->mma_bar, 1);
+        mbar_init(kv_bar, 1);
         mbar_init_fence();
     }
-    if (r < 32) {
+    if (threadIdx.x < 32) {
         tmem_alloc(&ctl->tmem, 512);
         tmem_relinquish();
     }
-    stage_w2(smem_u32(Tw), wf);
+    __syncthreads();
+    if (t0) {  // every load at once
+        mbar_arrive_expect_tx(&ctl->load_bar, 2 * TILE);
+        load_tile(Tq, &mq, &ctl->load_bar, static_cast<int>(a), bh);
+        load_tile(Tw, &mw2, &ctl->load_bar, 0, 0);
+        mbar_arrive_expect_tx(kv_bar, (2 + (two ? 2 : 0) + (has_p ? 1 : 0)) * TILE);
+        load_tile(Tk0, &mpk, kv_bar, static_cast<int>(J * C), bh);
+        load_tile(Tv0, &mv, kv_bar, static_cast<int>(J * C), bh);
+        if (two) {
+            load_tile(Tk1, &mpk, kv_bar, static_cast<int>(J * C + C), bh);
+            load_tile(Tv1, &mv, kv_bar, static_cast<int>(J * C + C), bh);
+        }
+        if (has_p) load_tile(Tp, &mpj, kv_bar, static_cast<int>(J * C), bh);
+    }
     operands_written();
     const uint32_t tmem = ctl->tmem;
-    const uint32_t T_FQ = tmem, T_FK = tmem + 128, T_S = tmem + 256, T_NUM = tmem + 384;
+    const uint32_t T_S0 = tmem, T_S1 = tmem + 128, T_NUM = tmem + 256;
     const WaitCtl wc{smem_u32(&ctl->abort_flag), kWaitTimeoutUs, status};
-    const int64_t J = a - m + 1 > 0 ? (a - m + 1) / C : 0;
-    const float *PJ = pstate + (static_cast<int64_t>(bh) * nchunks + J) * STATE_FLOATS;
-    int lp = 0, mp = 0;  // load / mma phases
-    if (r == 0) {
-        tma_prefetch_desc(&mq);
-        mbar_arrive_expect_tx(&ctl->load_bar, TILE);
-        load_tile(Tq, &mq, &ctl->load_bar, static_cast<int>(a), bh);
+    const float *zJ = zst + (static_cast<int64_t>(bh) * nchunks + J) * D;
+    if (t0) {
         if (mbar_wait(&ctl->load_bar, 0, wc, 43)) {
             tc_fence_after();
-            mma_abt(T_FQ, smem_u32(Tq), smem_u32(Tw), false);  // f(Q): [row][feature]
+            mma_abt(T_S0, smem_u32(Tq), smem_u32(Tw), false);  // f(Q): [row][feature]
         } else {
             mbar_wait_drain(&ctl->load_bar, 0);
         }
         umma_commit(&ctl->mma_bar);
     }
-    ++lp;
-    bool fine = wait_mma(ctl, mp++, wc, 44);
+    bool fine = wait_mma(ctl, 0, wc, 44);
     float den = 0.f;
-    if (fine) {  // phi(Q) (bf16, over the Q tile) and phi(q) z_J (fp32)
-        for (int c0 = 0; c0 < D; c0 += 32) {
+    if (fine) {  // phi(Q) (bf16, over the Q tile) and phi(q) z_J (fp32), this thread's half of the features
+        for (int c0 = 64 * hh; c0 < 64 * hh + 64; c0 += 32) {
             float x[32];
-            tmem_ld32(lane_addr(T_FQ, c0), x);
+            tmem_ld32(lane_addr(T_S0, c0), x);
 #pragma unroll
             for (int i = 0; i < 32; ++i) {
                 x[i] = exp2f(x[i] * LOG2E);
-                den = fmaf(x[i], PJ[D * D + c0 + i], den);
+                den = fmaf(x[i], zJ[c0 + i], den);
             }
             st_row32(smem_u32(Tq), r, c0, x);
         }
     }
+    operands_written();
+    if (t0) {
+        if (fine && mbar_wait(kv_bar, 0, wc, 45)) {
+            tc_fence_after();
+            mma_ab(T_S0, smem_u32(Tq), smem_u32(Tk0), false);                // phi(Q) phi(K_J)^T: [row][key]
+            if (two) mma_ab(T_S1, smem_u32(Tq), smem_u32(Tk1), false);       // chunk J + 1
+            if (has_p) mma_ab(T_NUM, smem_u32(Tq), smem_u32(Tp), false);     // phi(Q) P_J
+        } else {
+            mbar_wait_drain(kv_bar, 0);
+        }
+        umma_commit(&ctl->mma_bar);
+    }
+    fine = wait_mma(ctl, 1, wc, 46) && fine;
     const int64_t t = a + r;  // this thread's query row
-    bool any_num = false;
-    for (int u = 0; u < 2; ++u) {
-        const int64_t kt = J * C + u * C;  // first key of the intra tile
-        if (kt > last - m) break;
-        operands_written();  // phi(Q) (first pass) and the end of the previous tile's readers
-        if (r == 0) {
-            mbar_arrive_expect_tx(&ctl->load_bar, 2 * TILE);
-            load_tile(Tk, &mk, &ctl->load_bar, static_cast<int>(kt), bh);
-            load_tile(Tv, &mv, &ctl->load_bar, static_cast<int>(kt), bh);
-            if (fine && mbar_wait(&ctl->load_bar, lp & 1, wc, 45)) {
-                tc_fence_after();
-                mma_abt(T_FK, smem_u32(Tw), smem_u32(Tk), false);  // f(K)^T: [feature][key]
-            } else {
-                mbar_wait_drain(&ctl->load_bar, lp & 1);
-            }
-            umma_commit(&ctl->mma_bar);
-        }
-        ++lp;
-        fine = wait_mma(ctl, mp++, wc, 46) && fine;
-        if (fine) {
-            for (int c0 = 0; c0 < C; c0 += 32) {
-                float x[32];
-                tmem_ld32(lane_addr(T_FK, c0), x);
-#pragma unroll
-                for (int i = 0; i < 32; ++i) x[i] = exp2f(x[i] * LOG2E);
-                st_row32(smem_u32(Tk), r, c0, x);  // phi(K)^T over the K tile
-            }
-        }
-        operands_written();
-        if (r == 0) {
-            if (fine) mma_ab(T_S, smem_u32(Tq), smem_u32(Tk), false);  // phi(Q) phi(K)^T: [row][key]
-            umma_commit(&ctl->mma_bar);
-        }
-        fine = wait_mma(ctl, mp++, wc, 47) && fine;
-        if (fine) {  // keep s <= key <= t - m; row sums (fp32) into the denominator
-            for (int c0 = 0; c0 < C; c0 += 32) {
-                float x[32];
-                tmem_ld32(lane_addr(T_S, c0), x);
+    if (fine) {  // keep s <= key <= t - m; fp32 row sums into the denominator, bf16 pairs back into TMEM
+        for (int u = 0; u < (two ? 2 : 1); ++u) {
+            const uint32_t ts = u ? T_S1 : T_S0;
+            const int64_t kt = J * C + u * C;
+            {  // this thread's half of the keys; its bf16 pairs go to the first 32 of its own 64 columns
+                float x[64];
+                tmem_ld64(lane_addr(ts, 64 * hh), x);
+                uint32_t pk[32];
 #pragma unroll
                 for (int i = 0; i < 32; ++i) {
-                    const int64_t key = kt + c0 + i;
-                    x[i] = (key >= s && key <= t - m) ? x[i] : 0.f;
-                    den += x[i];
+                    const int64_t k0 = kt + 64 * hh + 2 * i;
+                    const float p0 = (k0 >= s && k0 <= t - m) ? x[2 * i] : 0.f;
+                    const float p1 = (k0 + 1 >= s && k0 + 1 <= t - m) ? x[2 * i + 1] : 0.f;
+                    den += p0 + p1;
+                    pk[i] = pack_bf16x2(p0, p1);
                 }
-                st_row32(smem_u32(Tp), r, c0, x);
+                tmem_st32u_nowait(lane_addr(ts, 64 * hh), pk);
             }
         }
-        operands_written();
-        if (r == 0) {
-            if (fine) mma_ab(T_NUM, smem_u32(Tp), smem_u32(Tv), any_num);  // masked scores x V
-            umma_commit(&ctl->mma_bar);
-        }
-        fine = wait_mma(ctl, mp++, wc, 48) && fine;
-        any_num = true;
+        tmem_wait_st();
     }
-    if (J > 0) {  // phi(Q) P_J: P_J rows are features, columns value columns
+    dx[hh * C + r] = den;  // this half's part of the row's denominator
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    den += dx[(hh ^ 1) * C + r];
+    if (t0) {
         if (fine) {
-            const float4 *src = reinterpret_cast<const float4 *>(PJ + r * D);
-            for (int c0 = 0; c0 < D; c0 += 32) {
-                float x[32];
-#pragma unroll
-                for (int i = 0; i < 8; ++i) {
-                    const float4 f = src[c0 / 4 + i];
-                    x[4 * i] = f.x, x[4 * i + 1] = f.y, x[4 * i + 2] = f.z, x[4 * i + 3] = f.w;
-                }
-                st_row32(smem_u32(Tp), r, c0, x);
-            }
+            mma_tv(T_NUM, T_S0, smem_u32(Tv0), has_p);  // masked scores of chunk J x V_J
+            if (two) mma_tv(T_NUM, T_S1, smem_u32(Tv1), true);
         }
-        operands_written();
-        if (r == 0) {
-            if (fine) mma_ab(T_NUM, smem_u32(Tq), smem_u32(Tp), any_num);
-            umma_commit(&ctl->mma_bar);
-        }
-        fine = wait_mma(ctl, mp++, wc, 49) && fine;
-        any_num = true;
+        umma_commit(&ctl->mma_bar);
     }
+    fine = wait_mma(ctl, 2, wc, 47) && fine;
     if (fine) {
         // tcgen05.ld is warp-collective: every thread loads, only rows t < L read o', lse and write o
         const bool live = t < L;
@@ -377,14 +419,9 @@ __global__ void __launch_bounds__(128, 1) linear_kernel(const __grid_constant__ 
         const float e = live ? exp2f(-lse[row] * LOG2E) : 0.f;  // e^{-lse}
         const float inv = 1.f / fmaf(den, e, 1.f);
         __nv_bfloat16 *orow = o + row * D;
-        for (int c0 = 0; c0 < D; c0 += 32) {
+        for (int c0 = 64 * hh; c0 < 64 * hh + 64; c0 += 32) {
             float x[32];
-            if (any_num) {
-                tmem_ld32(lane_addr(T_NUM, c0), x);
-            } else {
-#pragma unroll
-                for (int i = 0; i < 32; ++i) x[i] = 0.f;
-            }
+            tmem_ld32(lane_addr(T_NUM, c0), x);
             if (!live) continue;
             uint4 *p = reinterpret_cast<uint4 *>(orow + c0);
 #pragma unroll
@@ -403,7 +440,7 @@ __global__ void __launch_bounds__(128, 1) linear_kernel(const __grid_constant__ 
     }
     tc_fence_before();
     __syncthreads();
-    if (r < 32) {
+    if (threadIdx.x < 32) {
         tc_fence_after();
         tmem_dealloc(tmem, 512);
     }
@@ -500,8 +537,10 @@ using namespace swa;
 
 extern "C" size_t swa_hybrid_prefill_workspace_size(int B, int H, int64_t L, int d) {
     if (B < 1 || H < 1 || L < 1 || d != hy::D) return 0;
-    const int64_t BH = static_cast<int64_t>(B) * H;
-    return align256(static_cast<size_t>(BH * L) * 4) + align256(static_cast<size_t>(BH * n_chunks(L)) * hy::STATE_FLOATS * 4);
+    const int64_t BH = static_cast<int64_t>(B) * H, recs = BH * n_chunks(L);
+    // lse, the chunk states (bf16) and their z (fp32), phi(K)^T of every chunk (bf16)
+    return align256(static_cast<size_t>(BH * L) * 4) + 2 * align256(static_cast<size_t>(recs) * hy::D * hy::D * 2) +
+           align256(static_cast<size_t>(recs) * hy::D * 4) + align256(hy::D * hy::D * 2);
 }
 
 extern "C" int swa_hybrid_prefill(const void *q, const void *k, const void *v, const void *wf, void *o, float *state_s,
@@ -541,20 +580,33 @@ extern "C" int swa_hybrid_prefill(const void *q, const void *k, const void *v, c
         return fail(SWA_ERR_INVALID, "workspace must be non-null and 256-byte aligned");
     unsigned *status = device_status_word();
     if (!status) return SWA_ERR_CUDA;
-    float *lse = static_cast<float *>(workspace);
-    float *states = reinterpret_cast<float *>(static_cast<char *>(workspace) + align256(static_cast<size_t>(BH) * L * 4));
     const int nch = static_cast<int>(n_chunks(L));
+    const size_t recs = static_cast<size_t>(BH) * nch;
+    char *wsp = static_cast<char *>(workspace);
+    float *lse = reinterpret_cast<float *>(wsp);
+    wsp += align256(static_cast<size_t>(BH) * L * 4);
+    __nv_bfloat16 *dmat = reinterpret_cast<__nv_bfloat16 *>(wsp);
+    wsp += align256(recs * hy::D * hy::D * 2);
+    __nv_bfloat16 *phik = reinterpret_cast<__nv_bfloat16 *>(wsp);
+    wsp += align256(recs * hy::D * hy::D * 2);
+    float *zst = reinterpret_cast<float *>(wsp);
+    wsp += align256(recs * hy::D * 4);
+    __nv_bfloat16 *w2img = reinterpret_cast<__nv_bfloat16 *>(wsp);
 
     // the SWA branch: o' and lse
     PrefillArgs a{q, k, v, o, lse, nullptr, nullptr, 0, BH, L, d, w, s, scale, L, st};
     if (int rc = launch_prefill_bf16_tc(a)) return rc;
 
-    CUtensorMap mq, mk, mv;
+    CUtensorMap mq, mk, mv, mpk, mpj, mw2;
     if (!encode_tile_map(&mq, q, L, BH) || !encode_tile_map(&mk, k, L, BH) || !encode_tile_map(&mv, v, L, BH))
         return fail(SWA_ERR_INVALID, "cuTensorMapEncodeTiled rejected q, k or v");
+    // phi(K)^T and the scanned states as [BH][chunks * 128 rows][128] tiles
+    if (!encode_tile_map(&mpk, phik, static_cast<int64_t>(nch) * hy::C, BH) ||
+        !encode_tile_map(&mpj, dmat, static_cast<int64_t>(nch) * hy::C, BH) || !encode_tile_map(&mw2, w2img, hy::D, 1))
+        return fail(SWA_ERR_INVALID, "cuTensorMapEncodeTiled rejected the workspace");
     const __nv_bfloat16 *wfb = static_cast<const __nv_bfloat16 *>(wf);
     DeviceStatus *ds = reinterpret_cast<DeviceStatus *>(status);
-    const uint32_t smem_a = 3 * hy::TILE + 1024 + 64, smem_b = 5 * hy::TILE + 1024 + 64;
+    const uint32_t smem_a = 3 * hy::TILE + 1024 + 64, smem_b = 7 * hy::TILE + 1024 + 128 + 1024;
     static bool attr_done = false;  // per process; the attribute is per function and idempotent
     if (!attr_done) {
         cudaError_t e = cudaFuncSetAttribute(hy::chunk_state_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem_a);
@@ -563,17 +615,19 @@ extern "C" int swa_hybrid_prefill(const void *q, const void *k, const void *v, c
         if (e != cudaSuccess) return fail(SWA_ERR_CUDA, "hybrid kernels: %s", cudaGetErrorString(e));
         attr_done = true;
     }
-    // the linear branch: chunk states, their exclusive scan, then per query tile
-    hy::chunk_state_kernel<<<dim3(nch, BH), 128, smem_a, st>>>(mk, mv, wfb, states, nullptr, nullptr, nullptr, 0,
+    // the linear branch: W2, chunk states, their exclusive scan, then per query tile
+    hy::w2_kernel<<<hy::D, hy::D, 0, st>>>(wfb, w2img);
+    hy::chunk_state_kernel<<<dim3(nch, BH), 128, smem_a, st>>>(mk, mv, mw2, dmat, zst, phik, nullptr, nullptr, 0,
                                                                nch, s, L, ds);
-    const int64_t total = static_cast<int64_t>(BH) * hy::STATE_FLOATS;
-    hy::scan_kernel<<<static_cast<unsigned>((total + 255) / 256), 256, 0, st>>>(states, nch, total);
-    hy::linear_kernel<<<dim3(nch, BH), 128, smem_b, st>>>(mq, mk, mv, wfb, states, static_cast<__nv_bfloat16 *>(o),
+    const int64_t npairs = static_cast<int64_t>(BH) * hy::D * hy::D / 2, nz = static_cast<int64_t>(BH) * hy::D;
+    hy::scan_kernel<<<static_cast<unsigned>((npairs + nz + 255) / 256), 256, 0, st>>>(
+        reinterpret_cast<uint32_t *>(dmat), zst, nch, npairs, nz);
+    hy::linear_kernel<<<dim3(nch, BH), 256, smem_b, st>>>(mq, mv, mpk, mpj, mw2, zst, static_cast<__nv_bfloat16 *>(o),
                                                           lse, L, m, s, nch, ds);
     if (state_s) {
         // the state after the last row (keys s .. L-1-m): the prefix of chunk jf plus its keys below L - m
         const int64_t jf = L - m > 0 ? (L - m) / hy::C : 0;
-        hy::chunk_state_kernel<<<dim3(1, BH), 128, smem_a, st>>>(mk, mv, wfb, nullptr, states, state_s, state_z,
+        hy::chunk_state_kernel<<<dim3(1, BH), 128, smem_a, st>>>(mk, mv, mw2, dmat, zst, phik, state_s, state_z,
                                                                  static_cast<int>(jf), nch, s, L - m, ds);
     }
     cudaError_t e = cudaGetLastError();
