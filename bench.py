@@ -351,11 +351,9 @@ def prefill_leg(swa, wl, steps, warmup, world, rank, clocks, e2e=False, rope=Fal
         args = (q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(), None, B, H, L, d, w, s, wl.scale,
                 g.ctypes.data, g.size, block, rb.ctypes.data, rb.shape[1], ws.data_ptr(), nws, dt, stream)
         call = lib.swa_sink_prefill_blocksparse
-    elif dilation:
-        nws = lib.swa_sink_prefill_dilated_workspace_size(B, H, L, d, s, dilation, dt)
-        ws = torch.empty(nws, dtype=torch.uint8, device="cuda")
+    elif dilation:  # bf16, d = 128: in place, no workspace
         args = (q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(), None, B, H, L, d, w, s, dilation, wl.scale,
-                ws.data_ptr(), nws, dt, stream)
+                None, 0, dt, stream)
         call = lib.swa_sink_prefill_dilated
     elif rope:
         nws = lib.swa_sink_prefill_rope_workspace_size(B, H, L, d)
@@ -377,13 +375,14 @@ def prefill_leg(swa, wl, steps, warmup, world, rank, clocks, e2e=False, rope=Fal
     _check_status(swa)
     if hybrid:
         flops = hybrid_flops(B, H, L, d, w, s)
-        launches = 4
+        launches = 5  # the SWA prefill, the feature-map weights, the chunk states, their scan, the linear pass
     elif blocksparse is not None:
         flops = 4.0 * B * H * d * blocksparse_pairs(L, w, s, globals_, block, rand)
         launches = 2 if len(globals_) else 1
     else:
         flops = dilated_flops(B, H, L, d, w, s, dilation) if dilation else banded_flops(B, H, L, d, w)
-        launches = 3 if dilation else 2 if rope else 1
+        # dilated: the tensor-core pass, then the sink rows and the rows past the last whole group of r
+        launches = (2 if s > 0 or L % dilation else 1) if dilation else 2 if rope else 1
     res = {"flops_per_step": flops, "seconds": t, "steps": steps, "tflops": flops * steps / t / 1e12,
            "ms_per_step": t / steps * 1e3, "launches": launches * steps}
     if e2e:
@@ -720,8 +719,9 @@ def main():
         secondary["prefill_dilated_llama7b_L8192_w1024_s4_r2"] = {
             "metric": METRIC, "value": aggregate_rate(r["tflops"], world, 1.0), "unit": "TFLOP/s",
             "ms_per_step": r["ms_per_step"], "frac_of_bf16_peak": r["tflops"] / peaks["bf16_tflops"],
-            "what": "dilated window with sinks, r = 2 (FLOPs over the dilated key sets): gather into virtual "
-                    "heads + tensor-core prefill + scatter", "launches_per_step": 3}
+            "what": "dilated window with sinks, r = 2 (FLOPs over the dilated key sets): tensor-core prefill "
+                    "reading each residue class through 4-D tensor maps, in place, + the sink rows on CUDA cores",
+            "launches_per_step": 2}
     if "blocksparse" in legs:
         globals_, rand = swa_inputs.bigbird_pattern(wl.L, 64, 2, 3, seed=2024)
         r = prefill_leg(swa, wl, max(3, args.steps // 2), 3, world, rank, clocks, blocksparse=(globals_, 64, rand))
@@ -737,8 +737,8 @@ def main():
             "metric": METRIC, "value": aggregate_rate(r["tflops"], world, 1.0), "unit": "TFLOP/s",
             "ms_per_step": r["ms_per_step"], "frac_of_bf16_peak": r["tflops"] / peaks["bf16_tflops"],
             "what": "SWA + Hedgehog linear-attention branch for the evicted keys (FLOPs: banded SWA + the "
-                    "recurrent linear branch, 8 d^2 per evicted key): SWA prefill, chunk states, scan, linear "
-                    "pass with the combination", "launches_per_step": 4}
+                    "recurrent linear branch, 8 d^2 per evicted key): SWA prefill, feature-map weights, chunk "
+                    "states, scan, linear pass with the combination", "launches_per_step": 5}
     if "decode_hybrid" in legs:
         dw = swa_inputs.WORKLOADS["decode_llama13b_B64_w1024_s4_20480"]
         r = hybrid_decode_leg(swa, dw, world, rank, clocks)

@@ -140,14 +140,18 @@ size_t swa_sink_prefill_chunked_rope_workspace_size(int B, int H, int64_t L, int
  * window of "滑窗与固定稀疏" (glossary and Longformer section: attended window positions skip r - 1 tokens),
  * causal and with the sinks of the StreamingLLM section.  Row t attends
  *     {i < s}  |  {t - j r : 0 <= j < m},  m = w - s,  restricted to i <= t  (each key once),
- * so the window reaches (m - 1) r + 1 positions back at the cost of m keys; r = 1 is swa_sink_prefill.
- * Runs as a gather into r virtual heads per (b, h) (the sinks, then one residue class of positions mod r;
- * class-major), the prefill of swa_sink_prefill on them, and a scatter back.
+ * so the window reaches (m - 1) r + 1 positions back at the cost of m keys; r = 1 is swa_sink_prefill (and
+ * runs it).  Each residue class of positions mod r, after the sinks, is a virtual head with the plain band.
+ * bf16 with d = 128 runs in place: the tensor-core prefill reads every class straight from q, k, v through
+ * 4-D tensor maps and writes each row at its own position, for the rows [s, (L / r) r); a CUDA-core pass
+ * does the sink rows and the last L mod r rows.  The other forms (fp32, bf16 d = 64) gather q, k, v into r
+ * virtual heads per (b, h) (class-major), run the prefill of swa_sink_prefill on them and scatter o back.
  *
- *   q, k, v, o, lse : as swa_sink_prefill (pos0 = 0), bf16 with d = 128 (tensor cores) or fp32.
+ *   q, k, v, o, lse : as swa_sink_prefill (pos0 = 0), bf16 with d = 64 or 128 (tensor cores) or fp32.
  *   r       : dilation, 1 <= r <= 65536, B * H * r <= 65535 * 32.
  *   workspace : caller-owned device scratch of swa_sink_prefill_dilated_workspace_size(B, H, L, d, s, r,
- *             dtype) bytes, 256-byte aligned (q, k, v, o of the virtual heads and their lse).
+ *             dtype) bytes, 256-byte aligned (q, k, v, o of the virtual heads and their lse); not read (may
+ *             be NULL with 0 bytes) for bf16 with d = 128 and for r = 1.
  *   Other arguments and errors as swa_sink_prefill.
  */
 int swa_sink_prefill_dilated(const void *q, const void *k, const void *v, void *o, float *lse, int B, int H,

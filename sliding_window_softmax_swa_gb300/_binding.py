@@ -199,19 +199,22 @@ def swa_sink_decode_step_dilated(q, k_cache, v_cache, s: int, r: int, t: int, sc
 
 def swa_sink_prefill_dilated(q, k, v, w: int, s: int, r: int, scale: float | None = None, o=None, lse=None,
                              workspace=None, stream=None):
-    """Prefill over the dilated window with sinks: row t attends the s sinks and t, t - r, ..., t - (m-1) r."""
+    """Prefill over the dilated window with sinks: row t attends the s sinks and t, t - r, ..., t - (m-1) r.
+    bf16 with d = 128 (and any r = 1 call) runs in place and takes no workspace."""
     B, H, L, d = q.shape
     assert k.shape == q.shape and v.shape == q.shape and k.dtype == q.dtype and v.dtype == q.dtype
     if o is None:
         o = torch.empty_like(q)
-    nws = lib().swa_sink_prefill_dilated_workspace_size(B, H, L, d, s, r, _dtype_code(q))
-    if workspace is None:
+    in_place = r == 1 or (q.dtype == torch.bfloat16 and d == 128)
+    if workspace is None and not in_place:
+        nws = lib().swa_sink_prefill_dilated_workspace_size(B, H, L, d, s, r, _dtype_code(q))
         workspace = torch.empty(max(nws, 256), dtype=torch.uint8, device=q.device)
     _dev(q, k, v, o, lse, workspace)
     scale = (1.0 / d ** 0.5) if scale is None else scale
+    nbytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
     _check("swa_sink_prefill_dilated", lib().swa_sink_prefill_dilated(
-        _ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), B, H, L, d, w, s, r, scale, _ptr(workspace),
-        workspace.numel() * workspace.element_size(), _dtype_code(q), _stream(stream)))
+        _ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), B, H, L, d, w, s, r, scale, _ptr(workspace), nbytes,
+        _dtype_code(q), _stream(stream)))
     return o
 
 

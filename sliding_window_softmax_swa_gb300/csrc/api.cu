@@ -622,13 +622,24 @@ extern "C" int swa_sink_prefill_dilated(const void *q, const void *k, const void
     if (r < 1 || r > 65536) return fail(SWA_ERR_INVALID, "dilation r=%d must be in [1, 65536]", r);
     if (static_cast<int64_t>(B) * H * r > 65535 * 32)
         return fail(SWA_ERR_UNSUPPORTED, "B*H*r=%lld exceeds the supported %d", (long long)B * H * r, 65535 * 32);
+    const cudaStream_t st = static_cast<cudaStream_t>(stream);
+    if (r == 1)  // the plain window: the prefill itself (no workspace)
+        return prefill_impl(q, k, v, o, lse, nullptr, nullptr, 0, B, H, L, d, w, s, scale, dtype, L, st);
+    if (dtype == SWA_BF16 && d == 128) {
+        // in place: the tensor-core pass over the whole groups of r positions after the sinks, then the
+        // CUDA-core pass over the sink rows and the last L mod r rows (no workspace)
+        if (L == 0) return SWA_OK;
+        const PrefillArgs a{q, k, v, o, lse, nullptr, nullptr, 0, B * H, L, d, w, s, scale, L, st};
+        rc = launch_prefill_bf16_tc_dilated(a, r);
+        if (rc) return rc;
+        return launch_dilated_rows(a, r);
+    }
     const size_t need = swa_sink_prefill_dilated_workspace_size(B, H, L, d, s, r, dtype);
     if (workspace_bytes < need)
         return fail(SWA_ERR_INVALID, "workspace of %zu bytes is smaller than the %zu needed", workspace_bytes, need);
     if (L == 0) return SWA_OK;
     if (!workspace || (reinterpret_cast<uintptr_t>(workspace) & 255u))
         return fail(SWA_ERR_INVALID, "workspace must be non-null and 256-byte aligned");
-    const cudaStream_t st = static_cast<cudaStream_t>(stream);
     const int es = esize_of(dtype);
     const int VH = B * H * r;
     const int64_t Lv = dilated_rows(L, s, r);

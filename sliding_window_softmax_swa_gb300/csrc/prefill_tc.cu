@@ -121,7 +121,11 @@ struct Params {
     DeviceStatus *status;
     int64_t seq_stride;  // rows between (b, h) blocks of q/k/v/o/lse
     int L, pos0, w, s, m, BH;
-    int n_qtiles, n_items;  // 128-row query tiles per (b, h); work items = n_qtiles * BH
+    int qoff;               // position of query row 0 of an item's sequence: pos0, or s in dilated mode
+    int n_qtiles, n_items;  // 128-row query tiles per (b, h) (per class in dilated mode); work items
+    // dilated mode: dil_r residue classes per (b, h); tm_q / tm_k / tm_v are 4-D maps (d, class, group, (b, h))
+    // over position = group * dil_r + class for the groups [0, dil_G); tm_kc / tm_vc the plain rows (sinks)
+    int dil_r, dil_G;
     float scale_log2;
     uint32_t timeout_us;
 };
@@ -255,10 +259,14 @@ __device__ __forceinline__ void issue_pv(uint32_t d_tmem, uint32_t p_tmem, uint3
     }
 }
 
-// BS: the block-sparse mode (host-built tile lists with global keys and random key blocks; compiled apart, so
-// that the plain kernel carries none of its checks)
-template <bool BS>
+// MODE 0: plain.  MODE 1: block-sparse (host-built tile lists with global keys and random key blocks).  MODE 2:
+// dilated window (a work item is one query tile of one residue class of one (b, h), in the class's virtual
+// rows: the sinks, then the class's positions >= s; the band tiles and Q come through 4-D maps that step r
+// positions per row, and the epilogue writes each row back at its own position).  The modes are compiled apart,
+// so that the plain kernel carries none of the others' work.
+template <int MODE>
 __global__ void __launch_bounds__(kThreads, 1) swa_prefill_tc_kernel(const __grid_constant__ Params P) {
+    constexpr bool BS = MODE == 1, DIL = MODE == 2;
     extern __shared__ uint8_t smem_raw[];
     uint8_t *sm = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     uint64_t *bars = reinterpret_cast<uint64_t *>(sm + OFF_BAR);
@@ -315,12 +323,18 @@ __global__ void __launch_bounds__(kThreads, 1) swa_prefill_tc_kernel(const __gri
     tc_fence_after();
     const uint32_t tmem = *tmem_slot;
     const WaitCtl wc{smem_u32(const_cast<int *>(abort_flag)), P.timeout_us, P.status};
-    // work item -> (b, h) and first row of its query tile (longest-first order: the last query tiles of
-    // every head, whose windows are full, come first)
-    auto item_rows = [&](int item, int &bh, int &row_start) {
-        bh = item % P.BH;
-        row_start = (P.n_qtiles - 1 - item / P.BH) * BQ;
+    // work item -> (b, h), residue class (dilated mode) and first row of its query tile (longest-first order:
+    // the last query tiles of every head, whose windows are full, come first)
+    auto item_rows = [&](int item, int &bh, int &row_start, int &cls) {
+        const int grp = DIL ? P.BH * P.dil_r : P.BH;
+        const int rem = item % grp;
+        bh = rem % P.BH;
+        cls = DIL ? rem / P.BH : 0;
+        row_start = (P.n_qtiles - 1 - item / grp) * BQ;
     };
+    // dilated mode: the first position >= s of class c, and its group
+    auto class_p0 = [&](int c) { return P.s + ((c - P.s) % P.dil_r + P.dil_r) % P.dil_r; };
+    auto class_g0 = [&](int c) { return (class_p0(c) - c) / P.dil_r; };
 
     if (warp == kWarpTma) {
         // ------------------------------------------------------------------ TMA producers (K, V)
@@ -342,7 +356,8 @@ __global__ void __launch_bounds__(kThreads, 1) swa_prefill_tc_kernel(const __gri
                 const int b = it & 1;
                 if (!mbar_wait(&lready[b], (it >> 1) & 1, wc, 15, it)) break;
                 const int n = ntiles_s[b];
-                const int bh = item % P.BH;
+                int bh, row_start, cls;
+                item_rows(item, bh, row_start, cls);
                 bool fine = true;
                 for (int j = 0; j < n; ++j) {
                     const int st = g % NK;
@@ -354,8 +369,13 @@ __global__ void __launch_bounds__(kThreads, 1) swa_prefill_tc_kernel(const __gri
                     const CUtensorMap *mp = (T.flags & 1) ? m_cache : m_seq;
                     uint8_t *dst = ring + st * TILE_BYTES;
                     mbar_arrive_expect_tx(&full[st], TILE_BYTES);
-                    tma_load_3d(dst, mp, &full[st], 0, T.row0, bh);
-                    tma_load_3d(dst + HALF_BYTES, mp, &full[st], 64, T.row0, bh);
+                    if (DIL && !(T.flags & 1)) {  // band rows of the class: row0 is the group index
+                        tma_load_4d(dst, mp, &full[st], 0, cls, T.row0, bh);
+                        tma_load_4d(dst + HALF_BYTES, mp, &full[st], 64, cls, T.row0, bh);
+                    } else {
+                        tma_load_3d(dst, mp, &full[st], 0, T.row0, bh);
+                        tma_load_3d(dst + HALF_BYTES, mp, &full[st], 64, T.row0, bh);
+                    }
                     ++g;
                 }
                 if (!fine) break;
@@ -375,10 +395,10 @@ __global__ void __launch_bounds__(kThreads, 1) swa_prefill_tc_kernel(const __gri
             for (int it = 0;; ++it) {
                 const int item = static_cast<int>(blockIdx.x) + it * G;
                 if (item >= P.n_items) break;
-                int bh, row_start;
-                item_rows(item, bh, row_start);
-                const int q0 = P.pos0 + row_start;
-                const int qlast = P.pos0 + min(row_start + BQ, P.L) - 1;
+                int bh, row_start, cls;
+                item_rows(item, bh, row_start, cls);
+                const int q0 = P.qoff + row_start;
+                const int qlast = P.qoff + min(row_start + BQ, P.L) - 1;
                 const int b = it & 1;
                 if (it >= 2 && !mbar_wait(&lfree[b], ((it - 2) >> 1) & 1, wc, 12, it)) break;
                 Tile *tl = tiles_s + b * MAX_TILES;
@@ -397,6 +417,20 @@ __global__ void __launch_bounds__(kThreads, 1) swa_prefill_tc_kernel(const __gri
                             ++n;
                         }
                     }
+                } else if (DIL) {
+                    // virtual positions: the sinks on their own (plain rows of k / v, source bit set), then the
+                    // band from s, whose tiles start at group g0 + (position - s) of the class
+                    n = build_tiles(tl, q0, qlast, 0, P.s, P.m, P.w, true);
+                    if (n >= 1 && n <= MAX_TILES) {
+                        mark_tiles(tl, n, q0, qlast, P.s, P.m);
+                        const int g0 = class_g0(cls);
+                        for (int i = 0; i < n; ++i) {
+                            if (tl[i].pbase < P.s)
+                                tl[i].flags = static_cast<short>(tl[i].flags | 1);
+                            else
+                                tl[i].row0 = g0 + (tl[i].pbase - P.s);
+                        }
+                    }
                 } else {
                     n = build_tiles(tl, q0, qlast, P.pos0, P.s, P.m, P.w, false);
                     if (n >= 1 && n <= MAX_TILES) mark_tiles(tl, n, q0, qlast, P.s, P.m);
@@ -412,16 +446,28 @@ __global__ void __launch_bounds__(kThreads, 1) swa_prefill_tc_kernel(const __gri
                 if (it >= 2 && !mbar_wait(&qempty[b], ((it - 2) >> 1) & 1, wc, 13, it)) break;
                 uint8_t *qs = sm + OFF_Q + b * TILE_BYTES;
                 mbar_arrive_expect_tx(&qfull[b], TILE_BYTES);
-                tma_load_3d(qs, &P.tm_q, &qfull[b], 0, row_start, bh);
-                tma_load_3d(qs + HALF_BYTES, &P.tm_q, &qfull[b], 64, row_start, bh);
+                if (DIL) {
+                    const int gq = class_g0(cls) + row_start;
+                    tma_load_4d(qs, &P.tm_q, &qfull[b], 0, cls, gq, bh);
+                    tma_load_4d(qs + HALF_BYTES, &P.tm_q, &qfull[b], 64, cls, gq, bh);
+                } else {
+                    tma_load_3d(qs, &P.tm_q, &qfull[b], 0, row_start, bh);
+                    tma_load_3d(qs + HALF_BYTES, &P.tm_q, &qfull[b], 64, row_start, bh);
+                }
                 ++nq;
                 // into L2 meanwhile: the next item's Q rows
                 const int nitem = item + G;
                 if (nitem < P.n_items) {
-                    int nbh, nrow;
-                    item_rows(nitem, nbh, nrow);
-                    tma_prefetch_3d(&P.tm_q, 0, nrow, nbh);
-                    tma_prefetch_3d(&P.tm_q, 64, nrow, nbh);
+                    int nbh, nrow, ncls;
+                    item_rows(nitem, nbh, nrow, ncls);
+                    if (DIL) {
+                        const int gq = class_g0(ncls) + nrow;
+                        tma_prefetch_4d(&P.tm_q, 0, ncls, gq, nbh);
+                        tma_prefetch_4d(&P.tm_q, 64, ncls, gq, nbh);
+                    } else {
+                        tma_prefetch_3d(&P.tm_q, 0, nrow, nbh);
+                        tma_prefetch_3d(&P.tm_q, 64, nrow, nbh);
+                    }
                 }
             }
             if (*abort_flag) {  // no copy may still be landing
@@ -510,10 +556,12 @@ __global__ void __launch_bounds__(kThreads, 1) swa_prefill_tc_kernel(const __gri
         int v = 0;   // S tiles processed (S buffer v & 1, sfull / pvdone parity)
         int nx = 0;  // exchanges done (slot parity)
         float mrun = -INFINITY, lrun = 0.f;  // running max (log2 units) and this half's running sum
+        // an item whose epilogue is still to run: row i < nvalid of its tile goes to row rbase + i * rstep of
+        // its (b, h)
         struct Pending {
-            int on, it, bh, row_start, qlast;
+            int on, it, bh, rbase, rstep, nvalid;
             float m, l;
-        } pend = {0, 0, 0, 0, 0, 0.f, 0.f};
+        } pend = {0, 0, 0, 0, 0, 0, 0.f, 0.f};
         bool fine = true;
         // The row value of this thread's partner (the other key half of the row), through shared memory.  The
         // barrier of the two warps also tells both whether either failed a wait or saw the CTA abort flag
@@ -550,9 +598,8 @@ __global__ void __launch_bounds__(kThreads, 1) swa_prefill_tc_kernel(const __gri
             }
             tc_fence_before();
             mbar_arrive(&oempty[b]);
-            const int t = P.pos0 + pd.row_start + r;
-            if (t <= pd.qlast) {
-                const int64_t row = static_cast<int64_t>(pd.bh) * P.seq_stride + pd.row_start + r;
+            if (r < pd.nvalid) {
+                const int64_t row = static_cast<int64_t>(pd.bh) * P.seq_stride + pd.rbase + r * pd.rstep;
                 uint8_t *dst = reinterpret_cast<uint8_t *>(static_cast<__nv_bfloat16 *>(P.o) + row * HD + 64 * hf);
 #pragma unroll
                 for (int i = 0; i < 4; ++i)
@@ -565,11 +612,11 @@ __global__ void __launch_bounds__(kThreads, 1) swa_prefill_tc_kernel(const __gri
         for (int it = 0; fine; ++it) {
             const int item = static_cast<int>(blockIdx.x) + it * G;
             if (item >= P.n_items) break;
-            int bh, row_start;
-            item_rows(item, bh, row_start);
-            const int q0 = P.pos0 + row_start;
-            const int qlast = P.pos0 + min(row_start + BQ, P.L) - 1;
-            const int t = q0 + r;  // absolute position of this thread's row
+            int bh, row_start, cls;
+            item_rows(item, bh, row_start, cls);
+            const int q0 = P.qoff + row_start;
+            const int qlast = P.qoff + min(row_start + BQ, P.L) - 1;
+            const int t = q0 + r;  // absolute (dilated mode: virtual) position of this thread's row
             const int b = it & 1;
             {
                 const bool ok = mbar_wait(&lready[b], (it >> 1) & 1, wc, 14, it);
@@ -696,7 +743,13 @@ __global__ void __launch_bounds__(kThreads, 1) swa_prefill_tc_kernel(const __gri
             }
             if (!fine) break;
             if (lane == 0) mbar_arrive(&lfree[b]);  // this warp no longer reads the tile list
-            pend = {1, it, bh, row_start, qlast, mrun, lrun};
+            if (DIL) {  // virtual row q0 + i is position p0 + (row_start + i) r; whole groups only (g < dil_G)
+                const int g0 = class_g0(cls);
+                pend = {1, it, bh, class_p0(cls) + row_start * P.dil_r, P.dil_r,
+                        min(qlast - q0 + 1, P.dil_G - g0 - row_start), mrun, lrun};
+            } else {
+                pend = {1, it, bh, row_start, 1, qlast - q0 + 1, mrun, lrun};
+            }
         }
         if (fine && pend.on) epilogue();
     }
@@ -835,6 +888,22 @@ static bool encode_rows_map(CUtensorMap *m, const void *base, uint64_t rows, uin
                CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// A 4-D map over the rows of a residue class: (d, class, group, (b, h)) with position = group * r + class, for the
+// groups [0, groups) (whole groups of r positions only, so that no load leaves the (b, h) block).  The box is one
+// class, 128 consecutive groups, 64 columns: the same 128-byte-swizzled tile as a box of encode_rows_map.
+static bool encode_class_map(CUtensorMap *m, const void *base, uint64_t r, uint64_t groups, uint64_t nbh,
+                             uint64_t bh_stride_rows) {
+    EncodeTiledFn enc = encode_tiled_fn();
+    if (!enc) return false;
+    const cuuint64_t dims[4] = {static_cast<cuuint64_t>(tc::HD), r, groups, nbh};
+    const cuuint64_t strides[3] = {tc::HD * 2, r * tc::HD * 2, bh_stride_rows * tc::HD * 2};
+    const cuuint32_t box[4] = {64, 1, 128, 1};
+    const cuuint32_t estr[4] = {1, 1, 1, 1};
+    return enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void *>(base), dims, strides, box, estr,
+               CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 // Upper bound of the key tiles of one query tile (sink ranges, band ranges split at pos0 and at the
 // ring wrap).
 static int max_tiles_bound(int w, int s) {
@@ -854,21 +923,37 @@ static int sm_count() {
     return cached[dev];
 }
 
-static int launch_impl(const PrefillArgs &a, const BlockSparseDev *bs) {
+// dil_r > 0: the dilated mode (pos0 = 0), over the rows [s, G r) with G = L / dil_r; a call with no such row
+// launches nothing.
+static int launch_impl(const PrefillArgs &a, const BlockSparseDev *bs, int dil_r = 0) {
     using namespace tc;
     if (a.d != HD) return fail(SWA_ERR_UNSUPPORTED, "tensor-core prefill needs d = %d", HD);
     if (a.q_sink) return fail(SWA_ERR_INVALID, "the RoPE prefill runs on the sub-tile kernel");
     if (!bs && max_tiles_bound(a.w, a.s) > MAX_TILES)
         return fail(SWA_ERR_UNSUPPORTED, "window w=%d needs more than %d key tiles per query tile", a.w, MAX_TILES);
-    if ((a.L + BQ - 1) / BQ * a.BH > 0x7FFFFFFF) return fail(SWA_ERR_UNSUPPORTED, "too many work items");
+    // dilated mode: every class runs over the virtual rows [s, s + nrows), nrows = the rows of the longest
+    // class among the positions [s, G r); a shorter class's last virtual row reads zeros and is not written
+    const int64_t dil_G = dil_r > 0 ? a.L / dil_r : 0;
+    const int64_t nrows = dil_r > 0 ? (dil_G * dil_r > a.s ? (dil_G * dil_r - a.s + dil_r - 1) / dil_r : 0) : a.L;
+    if (dil_r > 0 && a.pos0 != 0) return fail(SWA_ERR_INVALID, "dilated mode needs pos0 = 0");
+    if (nrows == 0) return SWA_OK;
+    if ((nrows + BQ - 1) / BQ * a.BH * (dil_r > 0 ? dil_r : 1) > 0x7FFFFFFF)
+        return fail(SWA_ERR_UNSUPPORTED, "too many work items");
     if (!encode_tiled_fn()) return fail(SWA_ERR_CUDA, "cuTensorMapEncodeTiled is not available");
     unsigned *status = device_status_word();
     if (!status) return SWA_ERR_CUDA;
     Params p;
     memset(&p, 0, sizeof(p));
     const uint64_t L = static_cast<uint64_t>(a.L), st = static_cast<uint64_t>(a.seq_stride);
-    bool okm = encode_rows_map(&p.tm_q, a.q, L, a.BH, st) && encode_rows_map(&p.tm_k, a.k, L, a.BH, st) &&
-               encode_rows_map(&p.tm_v, a.v, L, a.BH, st);
+    bool okm;
+    if (dil_r > 0) {
+        const uint64_t r = static_cast<uint64_t>(dil_r), G = static_cast<uint64_t>(dil_G);
+        okm = encode_class_map(&p.tm_q, a.q, r, G, a.BH, st) && encode_class_map(&p.tm_k, a.k, r, G, a.BH, st) &&
+              encode_class_map(&p.tm_v, a.v, r, G, a.BH, st);
+    } else {
+        okm = encode_rows_map(&p.tm_q, a.q, L, a.BH, st) && encode_rows_map(&p.tm_k, a.k, L, a.BH, st) &&
+              encode_rows_map(&p.tm_v, a.v, L, a.BH, st);
+    }
     if (a.pos0 > 0) {
         // Only slots 0..min(pos0, w)-1 have been written; the map stops there so that TMA zero-fills the
         // rest of a tile instead of loading stale bytes (a masked column still multiplies its V row by 0,
@@ -884,14 +969,17 @@ static int launch_impl(const PrefillArgs &a, const BlockSparseDev *bs) {
     p.lse = a.lse;
     p.status = reinterpret_cast<DeviceStatus *>(status);
     p.seq_stride = a.seq_stride;
-    p.L = static_cast<int>(a.L);
+    p.L = static_cast<int>(nrows);
     p.pos0 = static_cast<int>(a.pos0);
+    p.qoff = dil_r > 0 ? a.s : p.pos0;
     p.w = a.w;
     p.s = a.s;
     p.m = a.w - a.s;
     p.BH = a.BH;
-    p.n_qtiles = static_cast<int>((a.L + BQ - 1) / BQ);
-    p.n_items = p.n_qtiles * a.BH;
+    p.dil_r = dil_r > 0 ? dil_r : 1;
+    p.dil_G = static_cast<int>(dil_G);
+    p.n_qtiles = static_cast<int>((nrows + BQ - 1) / BQ);
+    p.n_items = p.n_qtiles * a.BH * p.dil_r;
     p.scale_log2 = a.scale * 1.4426950408889634f;
     p.timeout_us = kWaitTimeoutUs;
     if (bs) {
@@ -902,7 +990,7 @@ static int launch_impl(const PrefillArgs &a, const BlockSparseDev *bs) {
         p.bs_block = bs->block;
         p.bs_r = bs->r;
     }
-    auto *kern = bs ? swa_prefill_tc_kernel<true> : swa_prefill_tc_kernel<false>;
+    auto *kern = bs ? swa_prefill_tc_kernel<1> : dil_r > 0 ? swa_prefill_tc_kernel<2> : swa_prefill_tc_kernel<0>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          static_cast<int>(SMEM_BYTES));
     if (e != cudaSuccess) return fail(SWA_ERR_CUDA, "prefill smem attribute: %s", cudaGetErrorString(e));
@@ -919,6 +1007,8 @@ static int launch_impl(const PrefillArgs &a, const BlockSparseDev *bs) {
 int launch_prefill_bf16_tc_plain(const PrefillArgs &a) { return launch_impl(a, nullptr); }
 
 int launch_prefill_bf16_tc_blocksparse(const PrefillArgs &a, const BlockSparseDev &bs) { return launch_impl(a, &bs); }
+
+int launch_prefill_bf16_tc_dilated(const PrefillArgs &a, int r) { return launch_impl(a, nullptr, r); }
 
 // Host: the key-tile lists of the block-sparse prefill, one per 256-row query pair, in the kernel's layout.  A
 // pair [q0, qlast] needs the sinks, its band [q0 - m + 1, qlast], every global position <= qlast, and the

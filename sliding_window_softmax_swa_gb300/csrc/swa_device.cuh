@@ -168,6 +168,22 @@ __device__ __forceinline__ void tma_prefetch_3d(const CUtensorMap *m, int x, int
                  : "memory");
 }
 
+// 4-D tiled load and L2 prefetch (same 16-byte rule on x).
+__device__ __forceinline__ void tma_load_4d(void *dst, const CUtensorMap *m, uint64_t *bar, int x, int y, int z,
+                                            int u) {
+    asm volatile(
+        "cp.async.bulk.tensor.4d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+        " [%0], [%1, {%3, %4, %5, %6}], [%2];" ::"r"(smem_u32(dst)),
+        "l"(reinterpret_cast<uint64_t>(m)), "r"(smem_u32(bar)), "r"(x), "r"(y), "r"(z), "r"(u)
+        : "memory");
+}
+__device__ __forceinline__ void tma_prefetch_4d(const CUtensorMap *m, int x, int y, int z, int u) {
+    asm volatile("cp.async.bulk.prefetch.tensor.4d.L2.global.tile [%0, {%1, %2, %3, %4}];" ::"l"(
+                     reinterpret_cast<uint64_t>(m)),
+                 "r"(x), "r"(y), "r"(z), "r"(u)
+                 : "memory");
+}
+
 // ---- tcgen05 ------------------------------------------------------------------------------------
 // TMEM allocation (whole warp).  Writes the TMEM base address to *dst (shared memory).
 __device__ __forceinline__ void tmem_alloc(uint32_t *dst, uint32_t ncols) {

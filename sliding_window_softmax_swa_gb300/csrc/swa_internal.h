@@ -62,6 +62,11 @@ size_t blocksparse_tile_list_bytes(int64_t L);  // tiles and global-key masks of
 int blocksparse_build_lists(int64_t L, int w, int s, const int32_t *globals, int n_globals, int block,
                             const int32_t *rand, int r, void *tiles_out, void *gmask_out, int *count_out);
 int launch_prefill_bf16_tc_sub(const PrefillArgs &a);
+// Dilated-window prefill in place (bf16, d = 128, pos0 = 0, contiguous [BH, L, d]): the tensor-core pass over the
+// rows [s, (L / r) r), every residue class a virtual head read through 4-D maps, and the CUDA-core pass over the
+// other rows (the sinks t < s and the last L mod r rows).
+int launch_prefill_bf16_tc_dilated(const PrefillArgs &a, int r);
+int launch_dilated_rows(const PrefillArgs &a, int r);
 // Layout passes of the dilated-window prefill: rows of one virtual head (sinks + one residue class), the
 // gather of q, k, v into the virtual heads [BH * r, Lv, d] and the scatter of o (and lse) back.
 int64_t dilated_rows(int64_t L, int s, int r);

@@ -185,11 +185,12 @@ def test_rope_prefills_validate_before_launch(lib):
 
 
 def test_dilated_prefill_validates_before_launch(lib):
+    # the workspace rules of the gathered form (fp32 here; bf16 with d = 128 runs in place and reads none)
     f = 1 << 20
-    need = lib.swa_sink_prefill_dilated_workspace_size(1, 2, 300, 128, 4, 3, swa.SWA_BF16)
+    need = lib.swa_sink_prefill_dilated_workspace_size(1, 2, 300, 128, 4, 3, swa.SWA_F32)
     rows = 2 * 3 * (4 + (300 - 4 + 2) // 3)  # virtual heads x (sinks + the longest residue class)
-    assert need >= 4 * rows * 128 * 2 + rows * 4
-    ok = [f, f, f, f, None, 1, 2, 300, 128, 64, 4, 3, 0.1, f << 8, need, swa.SWA_BF16, None]
+    assert need >= 4 * rows * 128 * 4 + rows * 4
+    ok = [f, f, f, f, None, 1, 2, 300, 128, 64, 4, 3, 0.1, f << 8, need, swa.SWA_F32, None]
     bad = list(ok)
     bad[11] = 0  # dilation >= 1
     assert lib.swa_sink_prefill_dilated(*bad) == swa.SWA_ERR_INVALID
@@ -198,6 +199,6 @@ def test_dilated_prefill_validates_before_launch(lib):
     assert lib.swa_sink_prefill_dilated(*bad) == swa.SWA_ERR_INVALID
     bad = list(ok)
     bad[5], bad[6], bad[11] = 65535, 32, 2  # B * H * r past the supported virtual heads
-    bad[14] = lib.swa_sink_prefill_dilated_workspace_size(65535, 32, 300, 128, 4, 2, swa.SWA_BF16)
+    bad[14] = lib.swa_sink_prefill_dilated_workspace_size(65535, 32, 300, 128, 4, 2, swa.SWA_F32)
     assert lib.swa_sink_prefill_dilated(*bad) == swa.SWA_ERR_UNSUPPORTED
     assert lib.swa_sink_prefill_dilated_workspace_size(1, 2, 300, 128, 4, 0, swa.SWA_BF16) == 0

@@ -1,6 +1,8 @@
 """GPU parity of the prefill over a dilated window with sinks (swa_sink_prefill_dilated) against the oracle's
-definition, element by element: bf16 outputs within the tolerances of every bf16 path (the virtual heads go
-through the same tensor-core prefill, one rounding of o), fp32 within 1e-4, lse within 1e-3."""
+definition, element by element: bf16 outputs within the tolerances of every bf16 path (one rounding of o),
+fp32 within 1e-4, lse within 1e-3.  bf16 with d = 128 runs in place (the tensor-core pass over whole groups of r
+positions after the sinks, read through 4-D maps, and a CUDA-core pass over the sink rows and the last L mod r
+rows); the other forms gather into virtual heads and scatter back."""
 import math
 
 import numpy as np
@@ -22,6 +24,12 @@ pytestmark = pytest.mark.gpu
     (16, 2, 300, 128, 100, 4, 2, torch.bfloat16),  # 64 virtual heads
     (1, 1, 200, 128, 40, 32, 5, torch.bfloat16),   # many sinks
     (1, 1, 3, 128, 2, 1, 3, torch.bfloat16),       # fewer rows than r
+    (1, 2, 263, 128, 300, 5, 2, torch.bfloat16),   # classes of 129 and 128 rows: one tile holds a phantom row only
+    (1, 2, 700, 128, 300, 130, 2, torch.bfloat16), # more sinks than a key tile
+    (1, 2, 1000, 128, 64, 4, 64, torch.bfloat16),  # r = 64: short classes, 40 rows past the last whole group
+    (2, 3, 2000, 128, 1024, 4, 3, torch.bfloat16), # several query tiles per class, full windows
+    (1, 2, 11, 128, 16, 8, 2, torch.bfloat16),     # one whole group after the sinks, then one row past it
+    (1, 2, 300, 64, 100, 4, 3, torch.bfloat16),    # d = 64: the gathered form
     (1, 2, 130, 16, 16, 4, 3, torch.float32),      # the fp32 path
 ])
 def test_dilated_prefill_every_row(B, H, L, d, w, s, r, dtype):
@@ -36,7 +44,7 @@ def test_dilated_prefill_every_row(B, H, L, d, w, s, r, dtype):
 
 
 def test_dilation_one_is_the_plain_prefill_bit_for_bit():
-    # r = 1: the single virtual head is the sequence itself, so the same kernel sees the same bytes
+    # r = 1 is the plain window: the call runs the plain prefill
     swa = require_gpu()
     q, k, v = (x.cuda() for x in swa_inputs.prefill_inputs(1, 4, 900, 128, 31, torch.bfloat16, "cpu", True))
     la = torch.empty((1, 4, 900), dtype=torch.float32, device="cuda")
