@@ -87,7 +87,7 @@ constexpr uint32_t OFF_MISC = OFF_BAR + 256;
 constexpr uint32_t OFF_TILES = OFF_MISC + 64;
 constexpr uint32_t OFF_GMASK = OFF_TILES + 2 * MAX_TILES * 12;  // two tile lists (current / next item)
 constexpr uint32_t OFF_XCH = OFF_GMASK + 2 * MAX_TILES * 16;       // and their global-key columns (block-sparse)
-constexpr uint32_t SMEM_USED = OFF_XCH + 2 * 2 * BQ * 4;             // row-value exchange of the softmax halves
+constexpr uint32_t SMEM_USED = OFF_XCH + 2 * 4 * BQ * 4;             // (max, sum) exchange of the two streams
 constexpr uint32_t SMEM_BYTES = SMEM_USED + 1024;  // slack to align the base to 1024 bytes
 static_assert(SMEM_BYTES <= 232448, "shared memory budget of one CTA");
 
@@ -276,12 +276,11 @@ __global__ void __launch_bounds__(kThreads, 1) swa_prefill_tc_kernel(const __gri
     uint64_t *kempty = kfull + NK;    // [NK]
     uint64_t *vfull = kempty + NK;    // [NV]
     uint64_t *vempty = vfull + NV;    // [NV]
-    uint64_t *sfull = vempty + NV;    // [2]: S buffer b holds Q K_j^T
-    uint64_t *pfull = sfull + 2;      // P of the next tile written over its S buffer (all softmax threads)
-    uint64_t *pvdone = pfull + 1;     // [2]: the PV product reading S buffer b is done
-    uint64_t *ofull = pvdone + 2;     // [2]: the last PV product of an item into O buffer b is done
-    uint64_t *oempty = ofull + 2;     // [2]: O buffer b has been read by the epilogue (all softmax threads)
-    uint64_t *lready = oempty + 2;    // [2]: tile list buffer b written (1 arrival)
+    uint64_t *sfull = vempty + NV;    // [2]: S buffer g holds Q K_j^T of stream g
+    uint64_t *pfull = sfull + 2;      // [2]: P_j written over S buffer g (the stream's 128 softmax threads)
+    uint64_t *ofull = pfull + 2;      // the last PV product of an item is done
+    uint64_t *oempty = ofull + 1;     // both O buffers have been read by the item's epilogue (all softmax threads)
+    uint64_t *lready = oempty + 1;    // [2]: tile list buffer b written (1 arrival)
     uint64_t *lfree = lready + 2;     // [2]: tile list buffer b no longer read (softmax warps, MMA, 2 loaders)
     uint64_t *drain = lfree + 2;
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(sm + OFF_MISC);
@@ -289,7 +288,7 @@ __global__ void __launch_bounds__(kThreads, 1) swa_prefill_tc_kernel(const __gri
     int *ntiles_s = reinterpret_cast<int *>(sm + OFF_MISC + 8);  // [2]
     Tile *tiles_s = reinterpret_cast<Tile *>(sm + OFF_TILES);     // [2][MAX_TILES]
     TileMask *gmask_s = reinterpret_cast<TileMask *>(sm + OFF_GMASK);  // [2][MAX_TILES] (block-sparse)
-    float *xch = reinterpret_cast<float *>(sm + OFF_XCH);              // [2 slots][2 halves][128 rows]
+    float *xch = reinterpret_cast<float *>(sm + OFF_XCH);  // [2 slots][2 streams][max, sum][128 rows]
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int G = static_cast<int>(gridDim.x);
@@ -304,13 +303,12 @@ __global__ void __launch_bounds__(kThreads, 1) swa_prefill_tc_kernel(const __gri
             mbar_init(&vfull[i], 1);
             mbar_init(&vempty[i], 1);
             mbar_init(&sfull[i], 1);
-            mbar_init(&pvdone[i], 1);
-            mbar_init(&ofull[i], 1);
-            mbar_init(&oempty[i], kSmThreads);
+            mbar_init(&pfull[i], kSmThreads / 2);
             mbar_init(&lready[i], 1);
             mbar_init(&lfree[i], kSmWarps + 3);
         }
-        mbar_init(pfull, kSmThreads);
+        mbar_init(ofull, 1);
+        mbar_init(oempty, kSmThreads);
         mbar_init(drain, 1);
         mbar_init_fence();
     }
@@ -476,12 +474,13 @@ __global__ void __launch_bounds__(kThreads, 1) swa_prefill_tc_kernel(const __gri
         }
     } else if (warp == kWarpMma) {
         // ------------------------------------------------------------------ MMA issuer
-        // Per item with key tiles 0..n-1: QK(0), then per j: QK(j + 1), PV(j).  S buffer j & 1 holds Q K_j^T
-        // until the softmax has read it, then P_j (bf16 pairs in its first 64 columns) until PV(j) has read
-        // it; QK(j + 2) reuses the buffer after PV(j) in issue order (tcgen05 MMAs of a thread run in order),
-        // so QK products run one tile ahead of the softmax.  Items alternate between the O buffers, so an
-        // item's first PV product waits only for the epilogue of the item before the previous one.  The whole
-        // warp runs the loop (uniform operands); one elected lane issues each instruction.
+        // Two streams per item: key tile j belongs to stream j mod 2, which owns S buffer and O buffer j mod 2.
+        // Per item with key tiles 0..n-1: QK(0), QK(1), then per j: PV(j) into O buffer j mod 2 once P_j is in
+        // S buffer j mod 2, followed by QK(j + 2) into that S buffer (tcgen05 MMAs of a thread run in order, so
+        // QK(j + 2) overwrites P_j only after PV(j) has read it).  While one stream's softmax works on its tile,
+        // the tensor cores run the other stream's products; the single issue order keeps the two streams out
+        // of phase.  An item's first PV product waits until the previous item's epilogue has read both O
+        // buffers.  The whole warp runs the loop (uniform operands); one elected lane issues each instruction.
         {
             auto wwait = [&](uint64_t *bar, int parity, unsigned site, unsigned tag) -> bool {
                 return __all_sync(0xFFFFFFFFu, mbar_wait(bar, static_cast<uint32_t>(parity), wc, site, tag));
@@ -489,47 +488,44 @@ __global__ void __launch_bounds__(kThreads, 1) swa_prefill_tc_kernel(const __gri
             const uint32_t q_addr0 = smem_u32(sm + OFF_Q);
             const uint32_t k_addr0 = smem_u32(sm + OFF_K), v_addr0 = smem_u32(sm + OFF_V);
             bool issued_any = false, fine = true;
-            int gk = 0, gv = 0;  // K, V tiles consumed
-            int u = 0;           // QK products issued (S buffer u & 1)
-            int pv = 0;          // PV products issued (pfull parity, S buffer pv & 1)
+            int gk = 0, gv = 0;    // K, V tiles consumed
+            int np0 = 0, np1 = 0;  // P tiles consumed per stream (pfull parity)
             for (int it = 0; fine; ++it) {
                 const int item = static_cast<int>(blockIdx.x) + it * G;
                 if (item >= P.n_items) break;
-                const int b = it & 1;  // tile list, Q and O buffer of this item
+                const int b = it & 1;  // tile list and Q buffer of this item
                 if (!wwait(&lready[b], (it >> 1) & 1, 14, it)) break;
                 if (!wwait(&qfull[b], (it >> 1) & 1, 2, it)) break;
                 tc_fence_after();
                 const int n = ntiles_s[b];
                 const uint32_t q_addr = q_addr0 + b * TILE_BYTES;
-                const uint32_t o_col = col_o(b);
-                for (int j = 0; fine && j <= n; ++j) {
-                    if (j < n) {  // QK(j)
-                        const int sk = gk % NK;
-                        if (!wwait(&kfull[sk], (gk / NK) & 1, 3, j)) { fine = false; break; }
-                        tc_fence_after();
-                        issue_qk(tmem + col_s(u & 1), q_addr, k_addr0 + sk * TILE_BYTES);
-                        umma_commit_warp(&sfull[u & 1]);
-                        umma_commit_warp(&kempty[sk]);
-                        if (j == n - 1) umma_commit_warp(&qempty[b]);  // the item's last QK product
-                        ++gk;
-                        ++u;
-                        issued_any = true;
-                    }
-                    if (j >= 1) {  // PV(j - 1)
-                        const int sv = gv % NV;
-                        if (!wwait(pfull, pv & 1, 4, j)) { fine = false; break; }
-                        if (j == 1 && it >= 2) {  // O buffer b must have been read by item it - 2's epilogue
-                            if (!wwait(&oempty[b], ((it - 2) >> 1) & 1, 11, j)) { fine = false; break; }
-                        }
-                        if (!wwait(&vfull[sv], (gv / NV) & 1, 5, j)) { fine = false; break; }
-                        tc_fence_after();
-                        issue_pv(tmem + o_col, tmem + col_s(pv & 1), v_addr0 + sv * TILE_BYTES, j > 1);
-                        umma_commit_warp(&pvdone[pv & 1]);
-                        umma_commit_warp(&vempty[sv]);
-                        if (j == n) umma_commit_warp(&ofull[b]);  // the item's last PV product
-                        ++gv;
-                        ++pv;
-                    }
+                auto qk = [&](int j) -> bool {  // QK(j) into S buffer j mod 2
+                    const int sk = gk % NK;
+                    if (!wwait(&kfull[sk], (gk / NK) & 1, 3, j)) return false;
+                    tc_fence_after();
+                    issue_qk(tmem + col_s(j & 1), q_addr, k_addr0 + sk * TILE_BYTES);
+                    umma_commit_warp(&sfull[j & 1]);
+                    umma_commit_warp(&kempty[sk]);
+                    if (j == n - 1) umma_commit_warp(&qempty[b]);  // the item's last QK product
+                    ++gk;
+                    issued_any = true;
+                    return true;
+                };
+                fine = qk(0) && (n < 2 || qk(1));
+                for (int j = 0; fine && j < n; ++j) {
+                    const int st = j & 1;
+                    if (!wwait(&pfull[st], (st ? np1 : np0) & 1, 4, j)) { fine = false; break; }
+                    np1 += st;
+                    np0 += st ^ 1;
+                    if (j == 0 && it >= 1 && !wwait(oempty, (it - 1) & 1, 11, j)) { fine = false; break; }
+                    const int sv = gv % NV;
+                    if (!wwait(&vfull[sv], (gv / NV) & 1, 5, j)) { fine = false; break; }
+                    tc_fence_after();
+                    issue_pv(tmem + col_o(st), tmem + col_s(st), v_addr0 + sv * TILE_BYTES, j >= 2);
+                    umma_commit_warp(&vempty[sv]);
+                    if (j == n - 1) umma_commit_warp(ofull);  // the item's last product
+                    ++gv;
+                    if (j + 2 < n && !qk(j + 2)) { fine = false; break; }
                 }
                 if (!fine) break;
                 if (lane == 0) mbar_arrive(&lfree[b]);
@@ -541,75 +537,23 @@ __global__ void __launch_bounds__(kThreads, 1) swa_prefill_tc_kernel(const __gri
         }
     } else if (warp < 8) {
         // ------------------------------------------------------------------ softmax + epilogue
-        // All eight warps work on every S tile, in issue order: warp w reads the TMEM lanes 32 (w mod 4) .. +31
-        // (rows of the query tile) and the key half hf = w / 4 (columns 64 hf .. 64 hf + 63), so each row is
-        // split over two threads, which agree on the row maximum through shared memory (one named barrier of
-        // the two warps per tile).  The epilogue of an item (O / l) runs after the first tile of the
-        // next item, so the tensor cores already have that item's QK and PV products to work on.
-        const int hf = warp >> 2;                // key half of this warp
-        // the two warps that share rows (w and w + 4) synchronise only with each other: named barrier 1 + w mod 4
+        // Stream g = warp / 4: the warps 4 g .. 4 g + 3 take the key tiles j = g, g + 2, ... of every item, with
+        // S buffer g, O buffer g and their own running max and sum.  Thread = row of the query tile = TMEM lane
+        // 32 (w mod 4) + lane, all 128 columns of its score row, so the softmax needs no exchange per tile.  At
+        // the end of an item the two threads of a row (warps w and w + 4) exchange (max, sum) through shared
+        // memory and merge the two O buffers, each writing half of the row's columns.
+        const int g = warp >> 2;
+        // the two warps that share rows (w and w + 4) meet once per item: named barrier 1 + w mod 4
         const uint32_t pair_bar = 1u + static_cast<uint32_t>(warp & 3);
-        const int r = threadIdx.x & (BQ - 1);    // row within the query tile == TMEM lane
+        const int r = threadIdx.x & (BQ - 1);  // row within the query tile == TMEM lane
         const uint32_t lane_base = static_cast<uint32_t>((warp & 3) * 32) << 16;
+        const uint32_t s_addr = tmem + lane_base + col_s(g);
+        const uint32_t o_addr = tmem + lane_base + col_o(g);
         const float sl2 = P.scale_log2;
         const uint32_t abort_a = smem_u32(const_cast<int *>(abort_flag));
-        int v = 0;   // S tiles processed (S buffer v & 1, sfull / pvdone parity)
+        int v = 0;   // S tiles of this stream processed (sfull / pfull parity)
         int nx = 0;  // exchanges done (slot parity)
-        float mrun = -INFINITY, lrun = 0.f;  // running max (log2 units) and this half's running sum
-        // an item whose epilogue is still to run: row i < nvalid of its tile goes to row rbase + i * rstep of
-        // its (b, h)
-        struct Pending {
-            int on, it, bh, rbase, rstep, nvalid;
-            float m, l;
-        } pend = {0, 0, 0, 0, 0, 0, 0.f, 0.f};
-        bool fine = true;
-        // The row value of this thread's partner (the other key half of the row), through shared memory.  The
-        // barrier of the two warps also tells both whether either failed a wait or saw the CTA abort flag
-        // (`stop`), so that they leave together and neither is left waiting at a later barrier; no barrier spans
-        // more than one such pair, so pairs that leave at different times never wait for each other.
-        auto exchange = [&](float val, bool failed, bool &stop) -> float {
-            float *slot = xch + (nx & 1) * 256;
-            slot[hf * 128 + r] = val;
-            stop = named_barrier_or(pair_bar, 64, failed || ld_abort(abort_a) != 0);
-            ++nx;
-            return slot[(hf ^ 1) * 128 + r];
-        };
-        // O / l of the pending item -> bf16 rows in global memory (and lse)
-        auto epilogue = [&]() -> bool {
-            const Pending pd = pend;
-            pend.on = 0;
-            const int b = pd.it & 1;
-            const bool ok = __all_sync(0xFFFFFFFFu, mbar_wait(&ofull[b], (pd.it >> 1) & 1, wc, 8, pd.it));
-            bool stop;
-            const float lpart = exchange(pd.l, !ok, stop);
-            if (stop) return false;
-            tc_fence_after();
-            const float lsum = pd.l + lpart;
-            const float inv = (lsum > 0.f) ? 1.f / lsum : 0.f;
-            uint32_t ob[32];
-            __syncwarp();
-            const uint32_t o_addr = tmem + lane_base + col_o(b) + 64 * hf;
-#pragma unroll
-            for (int c = 0; c < 64; c += 32) {
-                float ov[32];
-                tmem_ld32(o_addr + c, ov);
-#pragma unroll
-                for (int i = 0; i < 16; ++i) ob[c / 2 + i] = pack_bf16x2(ov[2 * i] * inv, ov[2 * i + 1] * inv);
-            }
-            tc_fence_before();
-            mbar_arrive(&oempty[b]);
-            if (r < pd.nvalid) {
-                const int64_t row = static_cast<int64_t>(pd.bh) * P.seq_stride + pd.rbase + r * pd.rstep;
-                uint8_t *dst = reinterpret_cast<uint8_t *>(static_cast<__nv_bfloat16 *>(P.o) + row * HD + 64 * hf);
-#pragma unroll
-                for (int i = 0; i < 4; ++i)
-                    st_global_v8(dst + 32 * i, ob[8 * i], ob[8 * i + 1], ob[8 * i + 2], ob[8 * i + 3], ob[8 * i + 4],
-                                 ob[8 * i + 5], ob[8 * i + 6], ob[8 * i + 7]);
-                if (P.lse && hf == 0) P.lse[row] = (pd.m + log2f(lsum)) * 0.69314718055994531f;
-            }
-            return true;
-        };
-        for (int it = 0; fine; ++it) {
+        for (int it = 0;; ++it) {
             const int item = static_cast<int>(blockIdx.x) + it * G;
             if (item >= P.n_items) break;
             int bh, row_start, cls;
@@ -618,38 +562,29 @@ __global__ void __launch_bounds__(kThreads, 1) swa_prefill_tc_kernel(const __gri
             const int qlast = P.qoff + min(row_start + BQ, P.L) - 1;
             const int t = q0 + r;  // absolute (dilated mode: virtual) position of this thread's row
             const int b = it & 1;
-            {
-                const bool ok = mbar_wait(&lready[b], (it >> 1) & 1, wc, 14, it);
-                if (named_barrier_or(pair_bar, 64, !ok || ld_abort(abort_a) != 0)) break;  // both warps or none go on
-            }
+            // a failed wait ends this stream's tiles; the exchange below then stops both warps of the pair
+            bool ok = __all_sync(0xFFFFFFFFu, mbar_wait(&lready[b], (it >> 1) & 1, wc, 14, it));
             const Tile *tl = tiles_s + b * MAX_TILES;
-            const int n = ntiles_s[b];
-            const uint32_t o_addr = tmem + lane_base + col_o(b) + 64 * hf;
-            mrun = -INFINITY;
-            lrun = 0.f;
-            for (int j = 0; j < n && fine; ++j) {
+            const int n = ok ? ntiles_s[b] : 0;
+            float mrun = -INFINITY, lrun = 0.f;  // running max (log2 units) and sum of this stream
+            for (int j = g; j < n; j += 2) {
                 const Tile T = tl[j];
-                const int sb = v & 1;
-                const uint32_t s_addr = tmem + lane_base + col_s(sb);
-                const bool ok = __all_sync(0xFFFFFFFFu, mbar_wait(&sfull[sb], (v >> 1) & 1, wc, 6, j));
+                ok = __all_sync(0xFFFFFFFFu, mbar_wait(&sfull[g], v & 1, wc, 6, j));
+                if (!ok) break;
                 tc_fence_after();
-                // this half of the score row in registers (not loaded after a failed wait: the exchange below
-                // then stops every softmax thread)
-                float sv[64];
+                float sv[128];
                 __syncwarp();
-                if (ok) tmem_ld64(s_addr + 64 * hf, sv);
+                tmem_ld128(s_addr, sv);
                 // valid columns of this row: [0, b1] (sinks) and [a2, hc] (window), hc = last causal column, as
-                // 32-bit column masks of this half; interior tiles need none
+                // 32-bit column masks; interior tiles need none
                 const int hc = min(static_cast<int>(T.chi), t - T.pbase);
                 const int b1 = min(hc, P.s - 1 - T.pbase);
                 const int a2 = max(0, t - P.m + 1 - T.pbase);
                 const bool full = (b1 >= BN - 1) || (hc >= BN - 1 && (a2 <= 0 || b1 >= a2 - 1));
-                uint32_t mw[2];
+                uint32_t mw[4];
 #pragma unroll
-                for (int k = 0; k < 2; ++k) {
-                    const int c0 = 64 * hf + 32 * k;
-                    mw[k] = full ? 0xFFFFFFFFu : (range_bits(-c0, b1 - c0) | range_bits(a2 - c0, hc - c0));
-                }
+                for (int k = 0; k < 4; ++k)
+                    mw[k] = full ? 0xFFFFFFFFu : (range_bits(-32 * k, b1 - 32 * k) | range_bits(a2 - 32 * k, hc - 32 * k));
                 if (BS && !full && t <= qlast) {
                     // block-sparse: also the global keys of the tile and the row's random key blocks, up to hc
                     const TileMask gm = gmask_s[b * MAX_TILES + j];
@@ -660,33 +595,26 @@ __global__ void __launch_bounds__(kThreads, 1) swa_prefill_tc_kernel(const __gri
                         const int lo = kb * P.bs_block - T.pbase;
                         const int hi = min(lo + P.bs_block - 1, hc);
 #pragma unroll
-                        for (int k = 0; k < 2; ++k) mw[k] |= range_bits(lo - 64 * hf - 32 * k, hi - 64 * hf - 32 * k);
+                        for (int k = 0; k < 4; ++k) mw[k] |= range_bits(lo - 32 * k, hi - 32 * k);
                     }
 #pragma unroll
-                    for (int k = 0; k < 2; ++k)
-                        mw[k] |= gm.w[2 * hf + k] & range_bits(-64 * hf - 32 * k, hc - 64 * hf - 32 * k);
+                    for (int k = 0; k < 4; ++k) mw[k] |= gm.w[k] & range_bits(-32 * k, hc - 32 * k);
                 }
-                if (__any_sync(0xFFFFFFFFu, (mw[0] & mw[1]) != 0xFFFFFFFFu)) {
+                if (__any_sync(0xFFFFFFFFu, (mw[0] & mw[1] & mw[2] & mw[3]) != 0xFFFFFFFFu)) {
 #pragma unroll
-                    for (int c = 0; c < 64; ++c) sv[c] = (mw[c >> 5] & (1u << (c & 31))) ? sv[c] : -INFINITY;
+                    for (int c = 0; c < 128; ++c) sv[c] = (mw[c >> 5] & (1u << (c & 31))) ? sv[c] : -INFINITY;
                 }
-                float mx4[4];
+                float mx8[8];
 #pragma unroll
-                for (int i = 0; i < 4; ++i) mx4[i] = fmax3(sv[i], sv[4 + i], sv[8 + i]);
+                for (int i = 0; i < 8; ++i) mx8[i] = fmax3(sv[i], sv[8 + i], sv[16 + i]);
 #pragma unroll
-                for (int c = 12; c < 60; c += 8)
+                for (int c = 24; c < 120; c += 16)
 #pragma unroll
-                    for (int i = 0; i < 4; ++i) mx4[i] = fmax3(mx4[i], sv[c + i], sv[c + 4 + i]);
-                const float mxh =
-                    fmax3(fmax3(mx4[0], mx4[1], sv[60]), fmax3(mx4[2], mx4[3], sv[61]), fmaxf(sv[62], sv[63]));
-                // the whole row's maximum; both halves of a row take the same decisions from here on, and every
-                // TMEM load of this S buffer is complete before either half stores P over it
-                bool stop;
-                const float mx = fmaxf(mxh, exchange(mxh, !ok, stop)) * sl2;
-                if (stop) {
-                    fine = false;
-                    break;
-                }
+                    for (int i = 0; i < 8; ++i) mx8[i] = fmax3(mx8[i], sv[c + i], sv[c + 8 + i]);
+#pragma unroll
+                for (int i = 0; i < 8; ++i) mx8[i] = fmaxf(mx8[i], sv[120 + i]);
+                const float mx =
+                    fmax3(fmax3(mx8[0], mx8[1], mx8[2]), fmax3(mx8[3], mx8[4], mx8[5]), fmaxf(mx8[6], mx8[7])) * sl2;
                 float alpha = 1.f;
                 bool resc = false;
                 const float mnew = fmaxf(mrun, mx);
@@ -697,61 +625,98 @@ __global__ void __launch_bounds__(kThreads, 1) swa_prefill_tc_kernel(const __gri
                     }
                     mrun = mnew;
                 }
-                if (__any_sync(0xFFFFFFFFu, resc)) {
-                    // O holds the PV products of this item's earlier tiles: S_j complete implies PV(j - 2) complete
-                    // (in-order MMAs); wait for PV(j - 1), the product of the other S buffer (j >= 1 here)
-                    // (a failed wait sets the CTA abort flag; the next exchange then stops every softmax thread)
-                    if (__all_sync(0xFFFFFFFFu, mbar_wait(&pvdone[sb ^ 1], ((v - 1) >> 1) & 1, wc, 7, j))) {
-                        tc_fence_after();
-                        __syncwarp();
-#pragma unroll 1
-                        for (int c = 0; c < 64; c += 32) {
-                            float ov[32];
-                            tmem_ld32(o_addr + c, ov);
-#pragma unroll
-                            for (int i = 0; i < 32; ++i) ov[i] *= alpha;
-                            tmem_st32(o_addr + c, ov);
-                        }
-                    }
-                }
-                // p = 2^(scale*log2(e)*s - m); bf16 pairs of this half's keys go to columns [32 hf, 32 hf + 32)
-                // of the S buffer: the A operand of PV(j)
+                // p = 2^(scale*log2(e)*s - m); bf16 pairs go to columns [0, 64) of the S buffer: the A operand
+                // of PV(j)
                 const float nmu = (mrun == -INFINITY) ? 0.f : -mrun;
                 float rs4[4] = {0.f, 0.f, 0.f, 0.f};
-                uint32_t pk[32];
 #pragma unroll
-                for (int i = 0; i < 32; ++i) {
-                    float a0, a1;
-                    ffma2(a0, a1, sv[2 * i], sv[2 * i + 1], sl2, sl2, nmu, nmu);
-                    const float p0 = ex2(a0), p1 = ex2(a1);
-                    const int k = (i & 1) * 2;
-                    fadd2(rs4[k], rs4[k + 1], rs4[k], rs4[k + 1], p0, p1);
-                    pk[i] = pack_bf16x2(p0, p1);
+                for (int h = 0; h < 2; ++h) {
+                    uint32_t pk[32];
+#pragma unroll
+                    for (int i = 0; i < 32; ++i) {
+                        float a0, a1;
+                        ffma2(a0, a1, sv[64 * h + 2 * i], sv[64 * h + 2 * i + 1], sl2, sl2, nmu, nmu);
+                        const float p0 = ex2(a0), p1 = ex2(a1);
+                        const int k = (i & 1) * 2;
+                        fadd2(rs4[k], rs4[k + 1], rs4[k], rs4[k + 1], p0, p1);
+                        pk[i] = pack_bf16x2(p0, p1);
+                    }
+                    __syncwarp();
+                    tmem_st32u_nowait(s_addr + 32 * h, pk);
                 }
-                __syncwarp();
-                tmem_st32u_nowait(s_addr + 32 * hf, pk);
-                tmem_wait_st();
                 lrun = lrun * alpha + ((rs4[0] + rs4[1]) + (rs4[2] + rs4[3]));
-                tc_fence_before();
-                mbar_arrive(pfull);
-                ++v;
-                // the previous item's epilogue, once this item's first P is on its way to the tensor cores
-                if (j == 0 && pend.on && !epilogue()) {
-                    fine = false;
-                    break;
+                if (__any_sync(0xFFFFFFFFu, resc)) {
+                    // O holds this stream's earlier PV products, all complete: S_j complete implies every MMA
+                    // issued before QK(j) is, and PV(j) comes only after P_j
+                    __syncwarp();
+#pragma unroll 1
+                    for (int c = 0; c < 128; c += 32) {
+                        float ov[32];
+                        tmem_ld32(o_addr + c, ov);
+#pragma unroll
+                        for (int i = 0; i < 32; ++i) ov[i] *= alpha;
+                        tmem_st32(o_addr + c, ov);
+                    }
                 }
+                tmem_wait_st();
+                tc_fence_before();
+                mbar_arrive(&pfull[g]);
+                ++v;
             }
-            if (!fine) break;
             if (lane == 0) mbar_arrive(&lfree[b]);  // this warp no longer reads the tile list
+            // ---- epilogue: merge the two streams of each row, O / l -> bf16 rows (and lse)
+            ok = ok && __all_sync(0xFFFFFFFFu, mbar_wait(ofull, it & 1, wc, 8, it));
+            float *slot = xch + (nx & 1) * 512;
+            slot[g * 256 + r] = mrun;
+            slot[g * 256 + 128 + r] = lrun;
+            if (named_barrier_or(pair_bar, 64, !ok || ld_abort(abort_a) != 0)) break;  // both warps or none go on
+            ++nx;
+            const float mo = slot[(g ^ 1) * 256 + r], lo = slot[(g ^ 1) * 256 + 128 + r];
+            tc_fence_after();
+            const float mtot = fmaxf(mrun, mo);   // finite for every row that has a key
+            const float wme = ex2(mrun - mtot);   // 0 for a stream that saw no key of the row
+            const float wot = ex2(mo - mtot);
+            const float lsum = lrun * wme + lo * wot;
+            const float inv = (lsum > 0.f) ? 1.f / lsum : 0.f;
+            const float c0 = (g == 0 ? wme : wot) * inv, c1 = (g == 0 ? wot : wme) * inv;
+            uint32_t ob[32];
+            __syncwarp();
+            const uint32_t oa = tmem + lane_base + col_o(0) + 64 * g;  // this thread's half of both O buffers
+#pragma unroll
+            for (int c = 0; c < 64; c += 32) {
+                float x0[32];
+                tmem_ld32(oa + c, x0);
+                if (n >= 2) {  // stream 1 wrote O buffer 1 in this item
+                    float x1[32];
+                    tmem_ld32(oa + 128 + c, x1);
+#pragma unroll
+                    for (int i = 0; i < 32; ++i) x0[i] = x0[i] * c0 + x1[i] * c1;
+                } else {
+#pragma unroll
+                    for (int i = 0; i < 32; ++i) x0[i] *= c0;
+                }
+#pragma unroll
+                for (int i = 0; i < 16; ++i) ob[c / 2 + i] = pack_bf16x2(x0[2 * i], x0[2 * i + 1]);
+            }
+            tc_fence_before();
+            mbar_arrive(oempty);
+            // row i < nvalid of the tile goes to row rbase + i * rstep of its (b, h)
+            int rbase = row_start, rstep = 1, nvalid = qlast - q0 + 1;
             if (DIL) {  // virtual row q0 + i is position p0 + (row_start + i) r; whole groups only (g < dil_G)
-                const int g0 = class_g0(cls);
-                pend = {1, it, bh, class_p0(cls) + row_start * P.dil_r, P.dil_r,
-                        min(qlast - q0 + 1, P.dil_G - g0 - row_start), mrun, lrun};
-            } else {
-                pend = {1, it, bh, row_start, 1, qlast - q0 + 1, mrun, lrun};
+                rbase = class_p0(cls) + row_start * P.dil_r;
+                rstep = P.dil_r;
+                nvalid = min(nvalid, P.dil_G - class_g0(cls) - row_start);
+            }
+            if (r < nvalid) {
+                const int64_t row = static_cast<int64_t>(bh) * P.seq_stride + rbase + r * rstep;
+                uint8_t *dst = reinterpret_cast<uint8_t *>(static_cast<__nv_bfloat16 *>(P.o) + row * HD + 64 * g);
+#pragma unroll
+                for (int i = 0; i < 4; ++i)
+                    st_global_v8(dst + 32 * i, ob[8 * i], ob[8 * i + 1], ob[8 * i + 2], ob[8 * i + 3], ob[8 * i + 4],
+                                 ob[8 * i + 5], ob[8 * i + 6], ob[8 * i + 7]);
+                if (P.lse && g == 0) P.lse[row] = (mtot + log2f(lsum)) * 0.69314718055994531f;
             }
         }
-        if (fine && pend.on) epilogue();
     }
 
     tc_fence_before();
