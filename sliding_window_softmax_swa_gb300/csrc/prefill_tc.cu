@@ -108,7 +108,7 @@ struct TileMask {
 };
 
 struct Params {
-    CUtensorMap tm_q, tm_k, tm_v, tm_kc, tm_vc;
+    CUtensorMap tm_q, tm_k, tm_v, tm_kc, tm_vc, tm_o;  // tm_o: the rows of o, laid out as tm_q
     // block-sparse mode: the host-built key-tile lists of every 256-row query pair (MAX_TILES entries per pair,
     // bs_count[pair] used), their global-key columns, and the random key blocks of each query block
     const Tile *bs_tiles;
@@ -271,8 +271,8 @@ __global__ void __launch_bounds__(kThreads, 1) swa_prefill_tc_kernel(const __gri
     uint8_t *sm = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     uint64_t *bars = reinterpret_cast<uint64_t *>(sm + OFF_BAR);
     uint64_t *qfull = bars;           // [2]: Q buffer b landed
-    uint64_t *qempty = qfull + 2;     // [2]: the last QK product reading Q buffer b is done
-    uint64_t *kfull = qempty + 2;     // [NK]
+    uint64_t *ostage = qfull + 2;     // [2]: the item's O rows staged in Q buffer b (all softmax threads)
+    uint64_t *kfull = ostage + 2;     // [NK]
     uint64_t *kempty = kfull + NK;    // [NK]
     uint64_t *vfull = kempty + NK;    // [NV]
     uint64_t *vempty = vfull + NV;    // [NV]
@@ -297,7 +297,7 @@ __global__ void __launch_bounds__(kThreads, 1) swa_prefill_tc_kernel(const __gri
         *abort_flag = 0;
         for (int i = 0; i < 2; ++i) {
             mbar_init(&qfull[i], 1);
-            mbar_init(&qempty[i], 1);
+            mbar_init(&ostage[i], kSmThreads);
             mbar_init(&kfull[i], 1);
             mbar_init(&kempty[i], 1);
             mbar_init(&vfull[i], 1);
@@ -386,9 +386,24 @@ __global__ void __launch_bounds__(kThreads, 1) swa_prefill_tc_kernel(const __gri
     } else if (warp == kWarpList) {
         // ------------------------------------------------------------------ tile lists and Q
         // Per item: the key-tile list goes to buffer it & 1 as soon as the buffer's previous item (it - 2) has
-        // been released by every reader; then the item's Q tile into Q buffer it & 1 as soon as the last QK
-        // product of item it - 2 (the buffer's previous user) is done, and the next item's Q into L2.
+        // been released by every reader.  Q buffer it & 1 then holds item it - 2's O rows, staged there by its
+        // epilogue: they go to global memory by TMA (the epilogue's own threads never wait for global stores),
+        // and once the store has read them the item's Q tile is loaded there, and the next item's Q into L2.
         if (lane == 0) {
+            // the O tile of an item, staged in a Q buffer, to global memory (rows outside o are not written)
+            auto store_o = [&](int oitem, const uint8_t *src) {
+                int obh, orow, ocls;
+                item_rows(oitem, obh, orow, ocls);
+                if (DIL) {
+                    const int gq = class_g0(ocls) + orow;
+                    tma_store_4d(&P.tm_o, src, 0, ocls, gq, obh);
+                    tma_store_4d(&P.tm_o, src + HALF_BYTES, 64, ocls, gq, obh);
+                } else {
+                    tma_store_3d(&P.tm_o, src, 0, orow, obh);
+                    tma_store_3d(&P.tm_o, src + HALF_BYTES, 64, orow, obh);
+                }
+                bulk_commit_group();
+            };
             int nq = 0;  // Q loads issued
             for (int it = 0;; ++it) {
                 const int item = static_cast<int>(blockIdx.x) + it * G;
@@ -440,9 +455,13 @@ __global__ void __launch_bounds__(kThreads, 1) swa_prefill_tc_kernel(const __gri
                 }
                 ntiles_s[b] = n;
                 mbar_arrive(&lready[b]);  // release: the list is visible to whoever sees the phase complete
-                // Q of the item, once the QK products of Q buffer b's previous item are done
-                if (it >= 2 && !mbar_wait(&qempty[b], ((it - 2) >> 1) & 1, wc, 13, it)) break;
+                // Q buffer b: item it - 2's O rows, staged there by its epilogue, go out first; then the item's Q
                 uint8_t *qs = sm + OFF_Q + b * TILE_BYTES;
+                if (it >= 2) {
+                    if (!mbar_wait(&ostage[b], ((it - 2) >> 1) & 1, wc, 13, it)) break;
+                    store_o(item - 2 * G, qs);
+                    bulk_wait_read_all();
+                }
                 mbar_arrive_expect_tx(&qfull[b], TILE_BYTES);
                 if (DIL) {
                     const int gq = class_g0(cls) + row_start;
@@ -468,6 +487,13 @@ __global__ void __launch_bounds__(kThreads, 1) swa_prefill_tc_kernel(const __gri
                     }
                 }
             }
+            // the O rows of the last two items
+            const int it_end = (P.n_items - static_cast<int>(blockIdx.x) + G - 1) / G;  // items of this CTA
+            for (int it = (it_end > 2 ? it_end - 2 : 0); it < it_end && !*abort_flag; ++it) {
+                if (!mbar_wait(&ostage[it & 1], (it >> 1) & 1, wc, 13, it)) break;
+                store_o(static_cast<int>(blockIdx.x) + it * G, sm + OFF_Q + (it & 1) * TILE_BYTES);
+            }
+            bulk_wait_all();
             if (*abort_flag) {  // no copy may still be landing
                 for (int i = (nq > 2 ? nq - 2 : 0); i < nq; ++i) mbar_wait_drain(&qfull[i & 1], (i >> 1) & 1);
             }
@@ -506,7 +532,6 @@ __global__ void __launch_bounds__(kThreads, 1) swa_prefill_tc_kernel(const __gri
                     issue_qk(tmem + col_s(j & 1), q_addr, k_addr0 + sk * TILE_BYTES);
                     umma_commit_warp(&sfull[j & 1]);
                     umma_commit_warp(&kempty[sk]);
-                    if (j == n - 1) umma_commit_warp(&qempty[b]);  // the item's last QK product
                     ++gk;
                     issued_any = true;
                     return true;
@@ -700,21 +725,25 @@ __global__ void __launch_bounds__(kThreads, 1) swa_prefill_tc_kernel(const __gri
             }
             tc_fence_before();
             mbar_arrive(oempty);
-            // row i < nvalid of the tile goes to row rbase + i * rstep of its (b, h)
-            int rbase = row_start, rstep = 1, nvalid = qlast - q0 + 1;
-            if (DIL) {  // virtual row q0 + i is position p0 + (row_start + i) r; whole groups only (g < dil_G)
-                rbase = class_p0(cls) + row_start * P.dil_r;
-                rstep = P.dil_r;
-                nvalid = min(nvalid, P.dil_G - class_g0(cls) - row_start);
-            }
-            if (r < nvalid) {
-                const int64_t row = static_cast<int64_t>(bh) * P.seq_stride + rbase + r * rstep;
-                uint8_t *dst = reinterpret_cast<uint8_t *>(static_cast<__nv_bfloat16 *>(P.o) + row * HD + 64 * g);
+            // the row's half g into Q buffer b (free: every QK product of the item is done) in the 128-byte
+            // swizzled layout of the tensor map; the tile-list warp stores the tile with TMA
+            const uint32_t stage = smem_u32(sm + OFF_Q + b * TILE_BYTES + g * HALF_BYTES);
 #pragma unroll
-                for (int i = 0; i < 4; ++i)
-                    st_global_v8(dst + 32 * i, ob[8 * i], ob[8 * i + 1], ob[8 * i + 2], ob[8 * i + 3], ob[8 * i + 4],
-                                 ob[8 * i + 5], ob[8 * i + 6], ob[8 * i + 7]);
-                if (P.lse && g == 0) P.lse[row] = (mtot + log2f(lsum)) * 0.69314718055994531f;
+            for (int k = 0; k < 8; ++k)
+                st_shared_v4(stage + sw128_offset(r, 8 * k), ob[4 * k], ob[4 * k + 1], ob[4 * k + 2], ob[4 * k + 3]);
+            fence_proxy_async_smem();
+            mbar_arrive(&ostage[b]);
+            if (P.lse && g == 0) {
+                // row i < nvalid of the tile is row rbase + i * rstep of its (b, h)
+                int rbase = row_start, rstep = 1, nvalid = qlast - q0 + 1;
+                if (DIL) {  // virtual row q0 + i is position p0 + (row_start + i) r; whole groups only (g < dil_G)
+                    rbase = class_p0(cls) + row_start * P.dil_r;
+                    rstep = P.dil_r;
+                    nvalid = min(nvalid, P.dil_G - class_g0(cls) - row_start);
+                }
+                if (r < nvalid)
+                    P.lse[static_cast<int64_t>(bh) * P.seq_stride + rbase + r * rstep] =
+                        (mtot + log2f(lsum)) * 0.69314718055994531f;
             }
         }
     }
@@ -914,10 +943,10 @@ static int launch_impl(const PrefillArgs &a, const BlockSparseDev *bs, int dil_r
     if (dil_r > 0) {
         const uint64_t r = static_cast<uint64_t>(dil_r), G = static_cast<uint64_t>(dil_G);
         okm = encode_class_map(&p.tm_q, a.q, r, G, a.BH, st) && encode_class_map(&p.tm_k, a.k, r, G, a.BH, st) &&
-              encode_class_map(&p.tm_v, a.v, r, G, a.BH, st);
+              encode_class_map(&p.tm_v, a.v, r, G, a.BH, st) && encode_class_map(&p.tm_o, a.o, r, G, a.BH, st);
     } else {
         okm = encode_rows_map(&p.tm_q, a.q, L, a.BH, st) && encode_rows_map(&p.tm_k, a.k, L, a.BH, st) &&
-              encode_rows_map(&p.tm_v, a.v, L, a.BH, st);
+              encode_rows_map(&p.tm_v, a.v, L, a.BH, st) && encode_rows_map(&p.tm_o, a.o, L, a.BH, st);
     }
     if (a.pos0 > 0) {
         // Only slots 0..min(pos0, w)-1 have been written; the map stops there so that TMA zero-fills the

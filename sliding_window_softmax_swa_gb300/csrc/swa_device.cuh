@@ -184,6 +184,26 @@ __device__ __forceinline__ void tma_prefetch_4d(const CUtensorMap *m, int x, int
                  : "memory");
 }
 
+// Tiled stores from shared memory (bulk async-group completion; rows outside the tensor are not written).  The
+// coordinates must not be negative, and x (elements) must be a multiple of 8 for 16-bit data.
+__device__ __forceinline__ void tma_store_3d(const CUtensorMap *m, const void *src, int x, int y, int z) {
+    asm volatile("cp.async.bulk.tensor.3d.global.shared::cta.tile.bulk_group [%0, {%2, %3, %4}], [%1];" ::"l"(
+                     reinterpret_cast<uint64_t>(m)),
+                 "r"(smem_u32(src)), "r"(x), "r"(y), "r"(z)
+                 : "memory");
+}
+__device__ __forceinline__ void tma_store_4d(const CUtensorMap *m, const void *src, int x, int y, int z, int u) {
+    asm volatile("cp.async.bulk.tensor.4d.global.shared::cta.tile.bulk_group [%0, {%2, %3, %4, %5}], [%1];" ::"l"(
+                     reinterpret_cast<uint64_t>(m)),
+                 "r"(smem_u32(src)), "r"(x), "r"(y), "r"(z), "r"(u)
+                 : "memory");
+}
+__device__ __forceinline__ void bulk_commit_group() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
+// Wait until the shared memory of every committed bulk store has been read (it may be overwritten).
+__device__ __forceinline__ void bulk_wait_read_all() { asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory"); }
+// Wait until every committed bulk store has completed.
+__device__ __forceinline__ void bulk_wait_all() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }
+
 // ---- tcgen05 ------------------------------------------------------------------------------------
 // TMEM allocation (whole warp).  Writes the TMEM base address to *dst (shared memory).
 __device__ __forceinline__ void tmem_alloc(uint32_t *dst, uint32_t ncols) {
