@@ -92,6 +92,7 @@ constexpr uint32_t SMEM_BYTES = SMEM_USED + 1024;  // slack to align the base to
 static_assert(SMEM_BYTES <= 232448, "shared memory budget of one CTA");
 
 constexpr uint32_t IDESC_QK = idesc_bf16_f32(128, 128, false, false);  // Q, K both K-major
+constexpr uint32_t IDESC_QK16 = idesc_bf16_f32(128, 16, false, false);  // a narrow tile: its first 16 keys
 constexpr uint32_t IDESC_PV = idesc_bf16_f32(128, 128, false, true);   // P K-major, V MN-major
 
 struct Tile {
@@ -238,21 +239,27 @@ __device__ __forceinline__ void fadd2(float &d0, float &d1, float a0, float a1, 
 
 // Both issued by a whole converged warp (one elected lane issues each MMA).  Shared-memory addresses stay
 // below 2^18, so a K step only adds its offset / 16 to the low descriptor word.
-__device__ __forceinline__ void issue_qk(uint32_t d_tmem, uint32_t q_addr, uint32_t k_addr) {
+// A narrow tile (every key in its first 16 columns, as the sink tile with s <= 16) takes a 16-column QK
+// product and one 16-key PV product.
+__device__ __forceinline__ void issue_qk(uint32_t d_tmem, uint32_t q_addr, uint32_t k_addr, bool narrow) {
     const uint32_t qlo = sdesc_sw128_lo(q_addr, 16), klo = sdesc_sw128_lo(k_addr, 16);
     constexpr uint32_t hi = sdesc_sw128_hi(1024);
+    const uint32_t idesc = narrow ? IDESC_QK16 : IDESC_QK;
 #pragma unroll
     for (int kk = 0; kk < HD / 16; ++kk) {
         const uint32_t off = ((kk >> 2) * HALF_BYTES + (kk & 3) * 32) >> 4;
-        umma_ss_warp_lo(d_tmem, qlo + off, klo + off, hi, IDESC_QK, kk > 0 ? 1u : 0u);
+        umma_ss_warp_lo(d_tmem, qlo + off, klo + off, hi, idesc, kk > 0 ? 1u : 0u);
     }
 }
 
-__device__ __forceinline__ void issue_pv(uint32_t d_tmem, uint32_t p_tmem, uint32_t v_addr, bool accumulate) {
+__device__ __forceinline__ void issue_pv(uint32_t d_tmem, uint32_t p_tmem, uint32_t v_addr, bool accumulate,
+                                         bool narrow) {
     const uint32_t vlo = sdesc_sw128_lo(v_addr, HALF_BYTES);
     constexpr uint32_t hi = sdesc_sw128_hi(1024);
+    const int nkk = narrow ? 1 : BN / 16;
 #pragma unroll
     for (int kk = 0; kk < BN / 16; ++kk) {
+        if (kk >= nkk) break;
         // P from TMEM: 16 keys = 8 columns of packed bf16 pairs; V: 16 key rows of 128 bytes (MN-major)
         umma_ts_warp_lo(d_tmem, p_tmem + kk * 8, vlo + ((kk * 16 * 128) >> 4), hi, IDESC_PV,
                         (accumulate || kk > 0) ? 1u : 0u);
@@ -525,11 +532,12 @@ __global__ void __launch_bounds__(kThreads, 1) swa_prefill_tc_kernel(const __gri
                 tc_fence_after();
                 const int n = ntiles_s[b];
                 const uint32_t q_addr = q_addr0 + b * TILE_BYTES;
+                const Tile *tl = tiles_s + b * MAX_TILES;
                 auto qk = [&](int j) -> bool {  // QK(j) into S buffer j mod 2
                     const int sk = gk % NK;
                     if (!wwait(&kfull[sk], (gk / NK) & 1, 3, j)) return false;
                     tc_fence_after();
-                    issue_qk(tmem + col_s(j & 1), q_addr, k_addr0 + sk * TILE_BYTES);
+                    issue_qk(tmem + col_s(j & 1), q_addr, k_addr0 + sk * TILE_BYTES, tl[j].chi < 16);
                     umma_commit_warp(&sfull[j & 1]);
                     umma_commit_warp(&kempty[sk]);
                     ++gk;
@@ -546,7 +554,7 @@ __global__ void __launch_bounds__(kThreads, 1) swa_prefill_tc_kernel(const __gri
                     const int sv = gv % NV;
                     if (!wwait(&vfull[sv], (gv / NV) & 1, 5, j)) { fine = false; break; }
                     tc_fence_after();
-                    issue_pv(tmem + col_o(st), tmem + col_s(st), v_addr0 + sv * TILE_BYTES, j >= 2);
+                    issue_pv(tmem + col_o(st), tmem + col_s(st), v_addr0 + sv * TILE_BYTES, j >= 2, tl[j].chi < 16);
                     umma_commit_warp(&vempty[sv]);
                     if (j == n - 1) umma_commit_warp(ofull);  // the item's last product
                     ++gv;
@@ -597,9 +605,6 @@ __global__ void __launch_bounds__(kThreads, 1) swa_prefill_tc_kernel(const __gri
                 ok = __all_sync(0xFFFFFFFFu, mbar_wait(&sfull[g], v & 1, wc, 6, j));
                 if (!ok) break;
                 tc_fence_after();
-                float sv[128];
-                __syncwarp();
-                tmem_ld128(s_addr, sv);
                 // valid columns of this row: [0, b1] (sinks) and [a2, hc] (window), hc = last causal column, as
                 // 32-bit column masks; interior tiles need none
                 const int hc = min(static_cast<int>(T.chi), t - T.pbase);
@@ -625,49 +630,83 @@ __global__ void __launch_bounds__(kThreads, 1) swa_prefill_tc_kernel(const __gri
 #pragma unroll
                     for (int k = 0; k < 4; ++k) mw[k] |= gm.w[k] & range_bits(-32 * k, hc - 32 * k);
                 }
-                if (__any_sync(0xFFFFFFFFu, (mw[0] & mw[1] & mw[2] & mw[3]) != 0xFFFFFFFFu)) {
-#pragma unroll
-                    for (int c = 0; c < 128; ++c) sv[c] = (mw[c >> 5] & (1u << (c & 31))) ? sv[c] : -INFINITY;
-                }
-                float mx8[8];
-#pragma unroll
-                for (int i = 0; i < 8; ++i) mx8[i] = fmax3(sv[i], sv[8 + i], sv[16 + i]);
-#pragma unroll
-                for (int c = 24; c < 120; c += 16)
-#pragma unroll
-                    for (int i = 0; i < 8; ++i) mx8[i] = fmax3(mx8[i], sv[c + i], sv[c + 8 + i]);
-#pragma unroll
-                for (int i = 0; i < 8; ++i) mx8[i] = fmaxf(mx8[i], sv[120 + i]);
-                const float mx =
-                    fmax3(fmax3(mx8[0], mx8[1], mx8[2]), fmax3(mx8[3], mx8[4], mx8[5]), fmaxf(mx8[6], mx8[7])) * sl2;
+                // the running max: O is rescaled only when it grows by more than 2^8 (also taken when mrun is
+                // still -inf); returns -m for the exponent
                 float alpha = 1.f;
                 bool resc = false;
-                const float mnew = fmaxf(mrun, mx);
-                if (mnew > mrun + kRescaleLog2) {  // also taken when mrun is still -inf
-                    if (mrun != -INFINITY) {
-                        alpha = ex2(mrun - mnew);
-                        resc = true;
+                auto new_max = [&](float mx) -> float {
+                    const float mnew = fmaxf(mrun, mx);
+                    if (mnew > mrun + kRescaleLog2) {
+                        if (mrun != -INFINITY) {
+                            alpha = ex2(mrun - mnew);
+                            resc = true;
+                        }
+                        mrun = mnew;
                     }
-                    mrun = mnew;
-                }
+                    return (mrun == -INFINITY) ? 0.f : -mrun;
+                };
                 // p = 2^(scale*log2(e)*s - m); bf16 pairs go to columns [0, 64) of the S buffer: the A operand
                 // of PV(j)
-                const float nmu = (mrun == -INFINITY) ? 0.f : -mrun;
                 float rs4[4] = {0.f, 0.f, 0.f, 0.f};
+                if (T.chi < 16) {
+                    // a narrow tile (every key in columns 0..15, as the sink tile): its QK product had N = 16, and
+                    // PV reads 16 keys, 8 packed columns
+                    float sv[16];
+                    __syncwarp();
+                    tmem_ld16(s_addr, sv);
 #pragma unroll
-                for (int h = 0; h < 2; ++h) {
-                    uint32_t pk[32];
+                    for (int c = 0; c < 16; ++c) sv[c] = (mw[0] & (1u << c)) ? sv[c] : -INFINITY;
+                    float m4[4];
 #pragma unroll
-                    for (int i = 0; i < 32; ++i) {
+                    for (int i = 0; i < 4; ++i) m4[i] = fmax3(sv[i], sv[4 + i], fmaxf(sv[8 + i], sv[12 + i]));
+                    const float nmu = new_max(fmax3(m4[0], m4[1], fmaxf(m4[2], m4[3])) * sl2);
+                    uint32_t pk[8];
+#pragma unroll
+                    for (int i = 0; i < 8; ++i) {
                         float a0, a1;
-                        ffma2(a0, a1, sv[64 * h + 2 * i], sv[64 * h + 2 * i + 1], sl2, sl2, nmu, nmu);
+                        ffma2(a0, a1, sv[2 * i], sv[2 * i + 1], sl2, sl2, nmu, nmu);
                         const float p0 = ex2(a0), p1 = ex2(a1);
                         const int k = (i & 1) * 2;
                         fadd2(rs4[k], rs4[k + 1], rs4[k], rs4[k + 1], p0, p1);
                         pk[i] = pack_bf16x2(p0, p1);
                     }
                     __syncwarp();
-                    tmem_st32u_nowait(s_addr + 32 * h, pk);
+                    tmem_st8u_nowait(s_addr, pk);
+                } else {
+                    float sv[128];
+                    __syncwarp();
+                    tmem_ld128(s_addr, sv);
+                    if (__any_sync(0xFFFFFFFFu, (mw[0] & mw[1] & mw[2] & mw[3]) != 0xFFFFFFFFu)) {
+#pragma unroll
+                        for (int c = 0; c < 128; ++c) sv[c] = (mw[c >> 5] & (1u << (c & 31))) ? sv[c] : -INFINITY;
+                    }
+                    float mx8[8];
+#pragma unroll
+                    for (int i = 0; i < 8; ++i) mx8[i] = fmax3(sv[i], sv[8 + i], sv[16 + i]);
+#pragma unroll
+                    for (int c = 24; c < 120; c += 16)
+#pragma unroll
+                        for (int i = 0; i < 8; ++i) mx8[i] = fmax3(mx8[i], sv[c + i], sv[c + 8 + i]);
+#pragma unroll
+                    for (int i = 0; i < 8; ++i) mx8[i] = fmaxf(mx8[i], sv[120 + i]);
+                    const float nmu = new_max(
+                        fmax3(fmax3(mx8[0], mx8[1], mx8[2]), fmax3(mx8[3], mx8[4], mx8[5]), fmaxf(mx8[6], mx8[7])) *
+                        sl2);
+#pragma unroll
+                    for (int h = 0; h < 2; ++h) {
+                        uint32_t pk[32];
+#pragma unroll
+                        for (int i = 0; i < 32; ++i) {
+                            float a0, a1;
+                            ffma2(a0, a1, sv[64 * h + 2 * i], sv[64 * h + 2 * i + 1], sl2, sl2, nmu, nmu);
+                            const float p0 = ex2(a0), p1 = ex2(a1);
+                            const int k = (i & 1) * 2;
+                            fadd2(rs4[k], rs4[k + 1], rs4[k], rs4[k + 1], p0, p1);
+                            pk[i] = pack_bf16x2(p0, p1);
+                        }
+                        __syncwarp();
+                        tmem_st32u_nowait(s_addr + 32 * h, pk);
+                    }
                 }
                 lrun = lrun * alpha + ((rs4[0] + rs4[1]) + (rs4[2] + rs4[3]));
                 if (__any_sync(0xFFFFFFFFu, resc)) {
