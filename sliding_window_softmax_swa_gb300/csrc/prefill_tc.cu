@@ -11,26 +11,33 @@
 // Work item = one query tile of 128 rows of one (b, h).  The kernel is persistent: one CTA per SM walks the
 // items blockIdx.x, blockIdx.x + gridDim.x, ..., ordered longest-first (the last query tiles of every head,
 // whose windows are full, come first), so the short items fall in the last rounds and the CTAs finish
-// together.  352 threads in four roles:
-//   warps 0-7  softmax + epilogue: warp w owns TMEM lanes 32 (w mod 4) .. +31 (rows of the tile) and the key
-//              half w / 4 of every score row, so each row is split over two threads of the warps w and w + 4,
-//              which agree on the row maximum through shared memory and a named barrier of the two warps;
+// together.  The key tiles of an item are split into two streams, the even and the odd tiles, each with its
+// own S buffer, O accumulator, running max and sum: while one stream's softmax works on its tile, the tensor
+// cores run the other stream's products, and no thread exchanges anything with another during the tile walk.
+// The epilogue merges the two streams of each row by their maxima.  352 threads in four roles:
+//   warps 0-7  softmax + epilogue: stream g = w / 4; warp w owns TMEM lanes 32 (w mod 4) .. +31 (rows of the
+//              tile), one thread per row with all 128 columns of its score row.  At the end of an item the two
+//              threads of a row (warps w and w + 4) exchange (max, sum) through shared memory at a named
+//              barrier of the two warps, each merges half of the row's columns of both O buffers, and the
+//              bf16 rows are staged in the item's Q buffer (free once its QK products are done);
 //   warp 8     TMA producers: lane 0 streams K tiles, lane 1 V tiles (128 rows x 128 bf16, two 64-column boxes
 //              with the 128-byte swizzle), each through its own 2-stage ring over all items of the CTA;
-//   warp 9     MMA issuer, the whole warp converged, one elected lane issuing: per item QK(0), then per key
-//              tile j QK(j+1), PV(j), where QK(j) is S = Q K_j^T into S buffer j mod 2 and PV(j) is O += P_j V_j
-//              with P_j (bf16 pairs written over the first 64 columns of its S buffer) read by the MMA straight
-//              from tensor memory.  QK products run one tile ahead of the softmax; S buffer j mod 2 is reused by
-//              QK(j+2) after PV(j) in issue order (tcgen05 MMAs of a thread complete in order);
-//   warp 10    per item: builds the key-tile list into one of two buffers, one item ahead, loads the item's Q
-//              into one of two Q buffers as soon as the last QK product of the buffer's previous item is done,
-//              and prefetches the next item's Q into L2.
-// TMEM (512 columns): S buffers [0,128), [128,256); O buffers [256,384), [384,512) for alternate items (fp32,
-// lane = row), so an item's epilogue (run after the next item's first tile) overlaps that item's products.
-// The online softmax keeps a running max in log2 units and only rescales O (TMEM load, multiply, store) when
-// the max grows by more than 8 (a factor 256), so p <= 256 always fits bf16/fp32 and the rescale is rare; O
-// and l always share the same reference max.  S_j complete implies PV(j-2) complete; a rescale at tile j first
-// waits for PV(j-1).
+//   warp 9     MMA issuer, the whole warp converged, one elected lane issuing: per item QK(0), QK(1), then per
+//              key tile j PV(j), QK(j+2), where QK(j) is S = Q K_j^T into S buffer j mod 2 and PV(j) is
+//              O_{j mod 2} += P_j V_j with P_j (bf16 pairs written over the first 64 columns of its S buffer)
+//              read by the MMA straight from tensor memory; S buffer j mod 2 is reused by QK(j+2) after PV(j) in
+//              issue order (tcgen05 MMAs of a thread complete in order).  The single issue order keeps the two
+//              streams out of phase.  A narrow tile (all keys in its first 16 columns, such as the sink tile)
+//              takes an N = 16 QK product and one 16-key PV product;
+//   warp 10    per item: builds the key-tile list into one of two buffers, one item ahead; stores the O rows
+//              that the epilogue of the item two back staged in the item's Q buffer (TMA, so that the softmax
+//              threads never wait on global stores), then loads the item's Q there and prefetches the next
+//              item's Q into L2.
+// TMEM (512 columns): S buffers [0,128), [128,256) and O buffers [256,384), [384,512) of the two streams (fp32,
+// lane = row).  The online softmax keeps a running max in log2 units and only rescales O (TMEM load,
+// multiply, store) when the max grows by more than 8 (a factor 256), so p <= 256 always fits bf16/fp32 and
+// the rescale is rare; O and l of a stream always share the same reference max.  S_j complete implies every
+// MMA issued before QK(j), in particular the stream's PV(j-2), is complete, so a rescale needs no wait.
 //
 // Key tiles.  For the query rows [q0, q1] of an item the key positions needed are the sinks [0, min(s, blo)) and
 // the band [blo, q1] with blo = max(0, q0 - m + 1).  Positions >= pos0 are rows of this call's k/v;
