@@ -613,15 +613,20 @@ __global__ void __launch_bounds__(kThreads, 1) swa_prefill_tc_kernel(const __gri
                 if (!ok) break;
                 tc_fence_after();
                 // valid columns of this row: [0, b1] (sinks) and [a2, hc] (window), hc = last causal column, as
-                // 32-bit column masks; interior tiles need none
+                // 32-bit column masks, built only where some row of the warp needs one (interior tiles need none)
                 const int hc = min(static_cast<int>(T.chi), t - T.pbase);
                 const int b1 = min(hc, P.s - 1 - T.pbase);
                 const int a2 = max(0, t - P.m + 1 - T.pbase);
                 const bool full = (b1 >= BN - 1) || (hc >= BN - 1 && (a2 <= 0 || b1 >= a2 - 1));
-                uint32_t mw[4];
+                const bool narrow = T.chi < 16;
+                const bool masked = __any_sync(0xFFFFFFFFu, !full) || narrow;
+                uint32_t mw[4] = {0xFFFFFFFFu, 0xFFFFFFFFu, 0xFFFFFFFFu, 0xFFFFFFFFu};
+                if (masked) {
 #pragma unroll
-                for (int k = 0; k < 4; ++k)
-                    mw[k] = full ? 0xFFFFFFFFu : (range_bits(-32 * k, b1 - 32 * k) | range_bits(a2 - 32 * k, hc - 32 * k));
+                    for (int k = 0; k < 4; ++k)
+                        mw[k] = full ? 0xFFFFFFFFu
+                                     : (range_bits(-32 * k, b1 - 32 * k) | range_bits(a2 - 32 * k, hc - 32 * k));
+                }
                 if (BS && !full && t <= qlast) {
                     // block-sparse: also the global keys of the tile and the row's random key blocks, up to hc
                     const TileMask gm = gmask_s[b * MAX_TILES + j];
@@ -655,7 +660,7 @@ __global__ void __launch_bounds__(kThreads, 1) swa_prefill_tc_kernel(const __gri
                 // p = 2^(scale*log2(e)*s - m); bf16 pairs go to columns [0, 64) of the S buffer: the A operand
                 // of PV(j)
                 float rs4[4] = {0.f, 0.f, 0.f, 0.f};
-                if (T.chi < 16) {
+                if (narrow) {
                     // a narrow tile (every key in columns 0..15, as the sink tile): its QK product had N = 16, and
                     // PV reads 16 keys, 8 packed columns
                     float sv[16];
@@ -683,7 +688,7 @@ __global__ void __launch_bounds__(kThreads, 1) swa_prefill_tc_kernel(const __gri
                     float sv[128];
                     __syncwarp();
                     tmem_ld128(s_addr, sv);
-                    if (__any_sync(0xFFFFFFFFu, (mw[0] & mw[1] & mw[2] & mw[3]) != 0xFFFFFFFFu)) {
+                    if (masked) {
 #pragma unroll
                         for (int c = 0; c < 128; ++c) sv[c] = (mw[c >> 5] & (1u << (c & 31))) ? sv[c] : -INFINITY;
                     }
