@@ -397,8 +397,8 @@ int swa_selftest_umma(const void *a, const void *b, float *c, int mode, void *st
 
 /*
  * swa_prefill_tile_plan -- diagnostics (host only, no CUDA call): the key tiles the bf16 prefill kernel
- * walks for the query rows at absolute positions q0..q1 (one CTA: two query tiles of 128 rows, rows
- * q0..q0+127 and q0+128..q1) of a call starting at pos0.  For tile i, tiles[5i..5i+4] = {source (0 = the
+ * walks for the query rows at absolute positions q0..q1 (one or two query tiles of 128 rows, rows
+ * q0..q0+127 and q0+128..q1; a work item of the kernel is one of them) of a call starting at pos0.  For tile i, tiles[5i..5i+4] = {source (0 = the
  * call's k/v, 1 = rolling cache), first source row, absolute position of column 0, last valid column,
  * bit mask of the query tiles that use it}; columns c <= last valid column hold position
  * (column-0 position + c).  Writes at most max_tiles entries; returns the tile count or a negative
@@ -408,6 +408,19 @@ int swa_prefill_tile_plan(int64_t q0, int64_t q1, int64_t pos0, int w, int s, in
 /* The same for the RoPE prefills (pos0 = 0, or pos0 >= s in chunked prefill): the sinks form the first
  * tile on their own, the band starts at position s.  s <= 128. */
 int swa_prefill_tile_plan_rope(int64_t q0, int64_t q1, int64_t pos0, int w, int s, int *tiles, int max_tiles);
+/* The same for the in-place dilated prefill of swa_sink_prefill_dilated (bf16, d = 128; host only, no CUDA
+ * call).  swa_prefill_dilated_split writes out[0..3] = {nrows, G, ns, tail0}: the tensor-core pass runs every
+ * residue class c over its virtual rows s .. s + nrows - 1 (virtual row s + i is position p0(c) + i r with
+ * p0(c) = s + ((c - s) mod r), and is stored when that position is below G r, G = L / r); the CUDA-core pass
+ * takes the rows [0, ns) and [tail0, L).  swa_prefill_tile_plan_dilated lists the key tiles of the work item
+ * of class cls whose query tile starts at virtual row s + row_start (row_start a multiple of 128 below nrows),
+ * as swa_prefill_tile_plan does, in virtual positions: a tile of source 1 holds plain rows (the sinks; column
+ * c is row first-row + c), a tile of source 0 holds groups of the class (column c is group first-row + c,
+ * position (first-row + c) r + cls; groups from G on are zero-filled by the tensor map).  Errors as
+ * swa_prefill_tile_plan. */
+int swa_prefill_dilated_split(int64_t L, int s, int r, int64_t *out);
+int swa_prefill_tile_plan_dilated(int64_t L, int w, int s, int r, int cls, int64_t row_start, int *tiles,
+                                  int max_tiles);
 /* The same for swa_sink_prefill_blocksparse (host only, no CUDA call): the key tiles of query pair `pair`
  * (rows 256*pair .. 256*pair + 255) for the pattern (globals, block, rand_blocks, r) of a sequence of L
  * positions.  For tile i, tiles[7i..7i+6] = {absolute position of column 0, last valid column, bit mask of

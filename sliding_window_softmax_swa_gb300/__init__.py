@@ -8,7 +8,8 @@ built with ``build.build()``.
 """
 from ._binding import (SWA_BF16, SWA_ERR_CUDA, SWA_ERR_INVALID, SWA_ERR_TIMEOUT, SWA_ERR_UNSUPPORTED, SWA_F32,
                        SWA_OK, SIGNATURES, SwaError, kv_rolling_write, last_error, lib, library_path,
-                       prefill_tile_plan, prefill_tile_plan_rope, swa_device_status, swa_sink_decode_step,
+                       prefill_tile_plan, prefill_tile_plan_rope, prefill_tile_plan_dilated, prefill_dilated_split,
+                       swa_device_status, swa_sink_decode_step,
                        swa_sink_decode_step_dilated, swa_sink_dilated_cache_write,
                        swa_sink_decode_step_rope, swa_sink_decode_workspace_size, swa_sink_prefill,
                        swa_sink_prefill_chunked, swa_sink_prefill_chunked_dilated, swa_sink_prefill_chunked_rope,
@@ -22,5 +23,6 @@ __all__ = ["swa_sink_prefill", "swa_sink_prefill_chunked", "swa_sink_prefill_hos
            "swa_sink_decode_step_dilated", "swa_sink_prefill_blocksparse", "prefill_blocksparse_plan",
            "swa_hybrid_prefill", "swa_hybrid_decode_step",
            "swa_sink_decode_workspace_size", "swa_device_status", "prefill_tile_plan", "prefill_tile_plan_rope",
+           "prefill_tile_plan_dilated", "prefill_dilated_split",
            "last_error", "lib", "library_path", "SwaError", "SIGNATURES", "SWA_OK", "SWA_ERR_INVALID",
            "SWA_ERR_UNSUPPORTED", "SWA_ERR_CUDA", "SWA_ERR_TIMEOUT", "SWA_BF16", "SWA_F32"]

@@ -41,6 +41,8 @@ SIGNATURES = {
     "swa_selftest_umma": (_i, [_vp, _vp, _vp, _i, _vp]),
     "swa_prefill_tile_plan": (_i, [_i64, _i64, _i64, _i, _i, ctypes.POINTER(ctypes.c_int), _i]),
     "swa_prefill_tile_plan_rope": (_i, [_i64, _i64, _i64, _i, _i, ctypes.POINTER(ctypes.c_int), _i]),
+    "swa_prefill_dilated_split": (_i, [_i64, _i, _i, ctypes.POINTER(ctypes.c_int64)]),
+    "swa_prefill_tile_plan_dilated": (_i, [_i64, _i, _i, _i, _i, _i64, ctypes.POINTER(ctypes.c_int), _i]),
     "swa_prefill_blocksparse_plan": (_i, [_i64, _i, _i, _vp, _i, _i, _vp, _i, _i64, ctypes.POINTER(ctypes.c_int), _i]),
     "swa_sink_prefill_dilated": (_i, [_vp, _vp, _vp, _vp, _vp, _i, _i, _i64, _i, _i, _i, _i, _f, _vp, _sz, _i, _vp]),
     "swa_sink_prefill_chunked_dilated": (_i, [_vp, _vp, _vp, _vp, _vp, _vp, _vp, _i, _i, _i64, _i, _i, _i, _i, _f, _i64,
@@ -431,6 +433,23 @@ def prefill_tile_plan_rope(q0: int, q1: int, pos0: int, w: int, s: int):
     n = lib().swa_prefill_tile_plan_rope(q0, q1, pos0, w, s, buf, 256)
     if n < 0:
         raise SwaError("swa_prefill_tile_plan_rope", n, last_error())
+    return [tuple(buf[5 * i:5 * i + 5]) for i in range(min(n, 256))]
+
+
+def prefill_dilated_split(L: int, s: int, r: int):
+    """How the in-place dilated prefill splits the rows of a (b, h): (nrows, G, ns, tail0)."""
+    out = (ctypes.c_int64 * 4)()
+    _check("swa_prefill_dilated_split", lib().swa_prefill_dilated_split(L, s, r, out))
+    return tuple(out)
+
+
+def prefill_tile_plan_dilated(L: int, w: int, s: int, r: int, cls: int, row_start: int):
+    """The key tiles of the in-place dilated prefill's work item (class cls, query tile at virtual row
+    s + row_start): list of (src, row0, pbase, chi, used_by_mask); src 1 = plain rows, src 0 = groups."""
+    buf = (ctypes.c_int * (5 * 256))()
+    n = lib().swa_prefill_tile_plan_dilated(L, w, s, r, cls, row_start, buf, 256)
+    if n < 0:
+        raise SwaError("swa_prefill_tile_plan_dilated", n, last_error())
     return [tuple(buf[5 * i:5 * i + 5]) for i in range(min(n, 256))]
 
 

@@ -604,6 +604,30 @@ extern "C" int swa_prefill_tile_plan_rope(int64_t q0, int64_t q1, int64_t pos0, 
                              max_tiles);
 }
 
+extern "C" int swa_prefill_dilated_split(int64_t L, int s, int r, int64_t *out) {
+    t_err[0] = 0;
+    if (L < 0 || L >= (int64_t(1) << 31) || s < 0 || r < 1 || r > 65536)
+        return fail(SWA_ERR_INVALID, "need 0 <= L < 2^31, s >= 0, 1 <= r <= 65536");
+    if (!out) return fail(SWA_ERR_INVALID, "out must be non-null");
+    const DilatedSplit d = dilated_split(L, s, r);
+    out[0] = d.nrows;
+    out[1] = d.G;
+    out[2] = d.ns;
+    out[3] = d.tail0;
+    return SWA_OK;
+}
+
+extern "C" int swa_prefill_tile_plan_dilated(int64_t L, int w, int s, int r, int cls, int64_t row_start, int *tiles,
+                                             int max_tiles) {
+    t_err[0] = 0;
+    if (w < 1 || s < 0 || s >= w) return fail(SWA_ERR_INVALID, "need 0 <= s < w (s=%d, w=%d)", s, w);
+    if (L < 1 || L >= (int64_t(1) << 31) || r < 1 || r > 65536 || cls < 0 || cls >= r)
+        return fail(SWA_ERR_INVALID, "need 1 <= L < 2^31, 1 <= r <= 65536, 0 <= cls < r");
+    if (row_start < 0 || row_start >= (int64_t(1) << 31)) return fail(SWA_ERR_INVALID, "row_start out of range");
+    if (!tiles || max_tiles < 0) return fail(SWA_ERR_INVALID, "tiles must be non-null");
+    return prefill_tile_plan_dilated(L, w, s, r, cls, static_cast<int>(row_start), tiles, max_tiles);
+}
+
 static size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
 
 extern "C" size_t swa_sink_prefill_dilated_workspace_size(int B, int H, int64_t L, int d, int s, int r, int dtype) {

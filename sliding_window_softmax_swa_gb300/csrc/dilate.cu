@@ -29,6 +29,18 @@ int64_t dilated_rows(int64_t L, int s, int r) {
     return head + tail;
 }
 
+// How the in-place dilated prefill splits the rows of a (b, h): the tensor-core pass over the whole groups of r
+// positions after the sinks ([s, G r), G = L / r; every class runs over the rows of the longest class), the
+// CUDA-core pass over [0, ns) and [tail0, L).
+DilatedSplit dilated_split(int64_t L, int s, int r) {
+    DilatedSplit d;
+    d.G = L / r;
+    d.nrows = d.G * r > s ? (d.G * r - s + r - 1) / r : 0;
+    d.ns = L < s ? L : s;
+    d.tail0 = d.G * r > d.ns ? d.G * r : d.ns;
+    return d;
+}
+
 // Original position of row u of virtual head class c, or -1 past the end of the sequence.
 __device__ __forceinline__ int64_t dilated_source(int64_t u, int c, int s, int r, int64_t L) {
     if (u < s) return u < L ? u : -1;
@@ -193,9 +205,10 @@ int launch_dilate_scatter(const void *ov, const float *lsev, void *o, float *lse
 }
 
 int launch_dilated_rows(const PrefillArgs &a, int r) {
-    const int64_t L = a.L, G = L / r;
-    const int ns = static_cast<int>(L < a.s ? L : a.s);
-    const int64_t tail0 = G * r > ns ? G * r : ns;
+    const int64_t L = a.L;
+    const DilatedSplit sp = dilated_split(L, a.s, r);
+    const int ns = static_cast<int>(sp.ns);
+    const int64_t tail0 = sp.tail0;
     const int64_t rows = static_cast<int64_t>(a.BH) * (ns + (L - tail0));
     if (rows == 0) return SWA_OK;
     const int grid = static_cast<int>(rows < 152 * 16 ? rows : 152 * 16);

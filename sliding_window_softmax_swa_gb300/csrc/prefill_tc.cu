@@ -204,6 +204,32 @@ __host__ __device__ void mark_tiles(Tile *tl, int n, int q0, int qlast, int s, i
     }
 }
 
+// Dilated mode.  Residue class c of the positions mod r starts (after the sinks) at position p0(c) =
+// s + ((c - s) mod r), in group g0(c) = (p0(c) - c) / r of the 4-D map (position = group * r + class).
+__host__ __device__ inline int dil_p0(int c, int s, int r) { return s + ((c - s) % r + r) % r; }
+__host__ __device__ inline int dil_g0(int c, int s, int r) { return (dil_p0(c, s, r) - c) / r; }
+
+// The key tiles of the dilated-mode work item over the class-c virtual rows [s + row_start, s + row_start + 127]
+// (clipped to s + nrows - 1), in virtual positions (the sinks, then the class's positions >= s one per row):
+// the sinks on their own (source bit set: plain rows of k / v), then the band from s, whose tiles start at group
+// g0 + (position - s) of the class.  Returns the tile count as build_tiles does.
+__host__ __device__ int build_tiles_dilated(Tile *tl, int row_start, int c, int s, int m, int w, int r, int nrows) {
+    const int q0 = s + row_start;
+    const int qlast = s + (row_start + BQ < nrows ? row_start + BQ : nrows) - 1;
+    const int n = build_tiles(tl, q0, qlast, 0, s, m, w, true);
+    if (n >= 1 && n <= MAX_TILES) {
+        mark_tiles(tl, n, q0, qlast, s, m);
+        const int g0 = dil_g0(c, s, r);
+        for (int i = 0; i < n; ++i) {
+            if (tl[i].pbase < s)
+                tl[i].flags = static_cast<short>(tl[i].flags | 1);
+            else
+                tl[i].row0 = g0 + (tl[i].pbase - s);
+        }
+    }
+    return n;
+}
+
 // Bits [lo, hi] of a 32-bit word (clipped to [0, 31]; 0 when the range is empty).
 __device__ __forceinline__ uint32_t range_bits(int lo, int hi) {
     lo = lo < 0 ? 0 : lo;
@@ -345,8 +371,8 @@ __global__ void __launch_bounds__(kThreads, 1) swa_prefill_tc_kernel(const __gri
         row_start = (P.n_qtiles - 1 - item / grp) * BQ;
     };
     // dilated mode: the first position >= s of class c, and its group
-    auto class_p0 = [&](int c) { return P.s + ((c - P.s) % P.dil_r + P.dil_r) % P.dil_r; };
-    auto class_g0 = [&](int c) { return (class_p0(c) - c) / P.dil_r; };
+    auto class_p0 = [&](int c) { return dil_p0(c, P.s, P.dil_r); };
+    auto class_g0 = [&](int c) { return dil_g0(c, P.s, P.dil_r); };
 
     if (warp == kWarpTma) {
         // ------------------------------------------------------------------ TMA producers (K, V)
@@ -445,19 +471,7 @@ __global__ void __launch_bounds__(kThreads, 1) swa_prefill_tc_kernel(const __gri
                         }
                     }
                 } else if (DIL) {
-                    // virtual positions: the sinks on their own (plain rows of k / v, source bit set), then the
-                    // band from s, whose tiles start at group g0 + (position - s) of the class
-                    n = build_tiles(tl, q0, qlast, 0, P.s, P.m, P.w, true);
-                    if (n >= 1 && n <= MAX_TILES) {
-                        mark_tiles(tl, n, q0, qlast, P.s, P.m);
-                        const int g0 = class_g0(cls);
-                        for (int i = 0; i < n; ++i) {
-                            if (tl[i].pbase < P.s)
-                                tl[i].flags = static_cast<short>(tl[i].flags | 1);
-                            else
-                                tl[i].row0 = g0 + (tl[i].pbase - P.s);
-                        }
-                    }
+                    n = build_tiles_dilated(tl, row_start, cls, P.s, P.m, P.w, P.dil_r, P.L);
                 } else {
                     n = build_tiles(tl, q0, qlast, P.pos0, P.s, P.m, P.w, false);
                     if (n >= 1 && n <= MAX_TILES) mark_tiles(tl, n, q0, qlast, P.s, P.m);
@@ -978,8 +992,10 @@ static int launch_impl(const PrefillArgs &a, const BlockSparseDev *bs, int dil_r
         return fail(SWA_ERR_UNSUPPORTED, "window w=%d needs more than %d key tiles per query tile", a.w, MAX_TILES);
     // dilated mode: every class runs over the virtual rows [s, s + nrows), nrows = the rows of the longest
     // class among the positions [s, G r); a shorter class's last virtual row reads zeros and is not written
-    const int64_t dil_G = dil_r > 0 ? a.L / dil_r : 0;
-    const int64_t nrows = dil_r > 0 ? (dil_G * dil_r > a.s ? (dil_G * dil_r - a.s + dil_r - 1) / dil_r : 0) : a.L;
+    DilatedSplit dsp{};
+    if (dil_r > 0) dsp = dilated_split(a.L, a.s, dil_r);
+    const int64_t dil_G = dsp.G;
+    const int64_t nrows = dil_r > 0 ? dsp.nrows : a.L;
     if (dil_r > 0 && a.pos0 != 0) return fail(SWA_ERR_INVALID, "dilated mode needs pos0 = 0");
     if (nrows == 0) return SWA_OK;
     if ((nrows + BQ - 1) / BQ * a.BH * (dil_r > 0 ? dil_r : 1) > 0x7FFFFFFF)
@@ -1138,6 +1154,23 @@ int prefill_tile_plan(int q0, int q1, int pos0, int w, int s, int rope, int *out
     tc::Tile tl[tc::MAX_TILES];
     const int n = tc::build_tiles(tl, q0, q1, pos0, s, w - s, w, rope != 0);
     tc::mark_tiles(tl, n, q0, q1, s, w - s);
+    for (int i = 0; i < n && i < max_tiles && i < tc::MAX_TILES; ++i) {
+        out[5 * i + 0] = tl[i].flags & 1;
+        out[5 * i + 1] = tl[i].row0;
+        out[5 * i + 2] = tl[i].pbase;
+        out[5 * i + 3] = tl[i].chi;
+        out[5 * i + 4] = tl[i].flags >> 1;
+    }
+    return n;
+}
+
+int prefill_tile_plan_dilated(int64_t L, int w, int s, int r, int cls, int row_start, int *out, int max_tiles) {
+    const DilatedSplit sp = dilated_split(L, s, r);
+    if (row_start < 0 || row_start % tc::BQ != 0 || row_start >= sp.nrows)
+        return fail(SWA_ERR_INVALID, "row_start=%d is not the first row of a query tile of the %lld rows of a class",
+                    row_start, (long long)sp.nrows);
+    tc::Tile tl[tc::MAX_TILES];
+    const int n = tc::build_tiles_dilated(tl, row_start, cls, s, w - s, w, r, static_cast<int>(sp.nrows));
     for (int i = 0; i < n && i < max_tiles && i < tc::MAX_TILES; ++i) {
         out[5 * i + 0] = tl[i].flags & 1;
         out[5 * i + 1] = tl[i].row0;

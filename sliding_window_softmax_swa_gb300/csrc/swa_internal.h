@@ -67,6 +67,15 @@ int launch_prefill_bf16_tc_sub(const PrefillArgs &a);
 // other rows (the sinks t < s and the last L mod r rows).
 int launch_prefill_bf16_tc_dilated(const PrefillArgs &a, int r);
 int launch_dilated_rows(const PrefillArgs &a, int r);
+struct DilatedSplit {
+    int64_t nrows;  // virtual rows after the sinks that every class runs over in the tensor-core pass
+    int64_t G;      // whole groups of r positions
+    int64_t ns;     // the CUDA-core pass: rows [0, ns) and [tail0, L)
+    int64_t tail0;
+};
+DilatedSplit dilated_split(int64_t L, int s, int r);
+// the key tiles of one dilated-mode work item (as prefill_tile_plan; source 0 rows are groups of the class)
+int prefill_tile_plan_dilated(int64_t L, int w, int s, int r, int cls, int row_start, int *out, int max_tiles);
 // Layout passes of the dilated-window prefill: rows of one virtual head (sinks + one residue class), the
 // gather of q, k, v into the virtual heads [BH * r, Lv, d] and the scatter of o (and lse) back.
 int64_t dilated_rows(int64_t L, int s, int r);

@@ -1,5 +1,6 @@
 """The key walks of the bf16 prefill kernels (host-callable, same functions as on the device) cover every
-key of every query row exactly once, with the right position in every column (CPU only).
+key of every query row exactly once, with the right position in every column (CPU only); and the in-place
+dilated prefill computes every row once with exactly its dilated key set.
 
 The plain kernel walks, per 128-row query tile, tiles of up to 128 keys; the RoPE kernel, per 256-row pair of
 query tiles, sub-tiles of up to 64; for each the library
@@ -155,3 +156,59 @@ def test_rope_chunked_tiles_random():
         ns = sink_prefix(plan, s, s, src=1)
         for src, row0, pbase, chi, used in plan[ns:]:
             assert pbase >= s
+
+
+def check_dilated(L, w, s, r):
+    """The in-place dilated prefill (the library's own split and per-item tile lists): every row of a (b, h) is
+    computed exactly once, by the tensor-core pass or the CUDA-core rows, and each row the tensor-core pass
+    stores sees exactly the oracle's dilated key set through the virtual positions of its class."""
+    m = w - s
+    nrows, G, ns, tail0 = swa.prefill_dilated_split(L, s, r)
+    done = np.zeros(L, dtype=np.int64)
+    done[:ns] += 1
+    done[tail0:] += 1
+    for c in range(r):
+        p0 = s + (c - s) % r  # the first position >= s of class c
+        assert p0 % r == c
+        for row_start in range(0, nrows, BQ):
+            plan = swa.prefill_tile_plan_dilated(L, w, s, r, c, row_start)
+            q0 = s + row_start
+            qlast = s + min(row_start + BQ, nrows) - 1
+            for u in range(q0, qlast + 1):
+                p = p0 + (u - s) * r  # real position of virtual row u
+                if p >= G * r:
+                    continue  # a row past the last whole group: not stored by this pass
+                done[p] += 1
+                keys = []
+                for src, row0, pbase, chi, used in plan:
+                    assert used == 1
+                    for col in range(chi + 1):
+                        vpos = pbase + col  # virtual key position; the kernel's per-row mask rule
+                        if vpos > u or not (vpos < s or vpos >= u - m + 1):
+                            continue
+                        if src == 1:  # plain rows: the sinks
+                            assert vpos < s and row0 + col == vpos
+                            keys.append(vpos)
+                        else:  # groups of the class; groups from G on would read zeros
+                            g = row0 + col
+                            assert g < G, ("a stored row attends a zero-filled key", L, w, s, r, c, u)
+                            keys.append(g * r + c)
+                want = [i for i in range(p + 1) if oracle.is_key_dilated(p, i, w, s, r)]
+                assert sorted(keys) == want, (L, w, s, r, c, p)
+    assert (done == 1).all(), (L, w, s, r, np.flatnonzero(done != 1)[:8])
+
+
+@pytest.mark.parametrize("L,w,s,r", [(512, 256, 4, 2), (700, 40, 4, 3), (300, 64, 0, 1), (257, 300, 130, 2),
+                                     (263, 300, 5, 2), (1000, 64, 4, 64), (50, 20, 4, 7), (11, 16, 8, 2),
+                                     (9, 8, 4, 4), (3, 2, 1, 3), (1001, 200, 4, 7)])
+def test_dilated_in_place_plan(L, w, s, r):
+    check_dilated(L, w, s, r)
+
+
+def test_dilated_in_place_plan_random():
+    rng = random.Random(77)
+    for _ in range(25):
+        r = rng.choice([1, 2, 3, 4, 5, 8, 16])
+        w = rng.choice([2, 8, 40, 100, 129, 300])
+        s = min(w - 1, rng.choice([0, 1, 4, 16, w - 1]))
+        check_dilated(rng.randrange(1, 700), w, s, r)
