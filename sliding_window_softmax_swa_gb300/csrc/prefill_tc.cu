@@ -772,21 +772,22 @@ __global__ void __launch_bounds__(kThreads, 1) swa_prefill_tc_kernel(const __gri
             uint32_t ob[32];
             __syncwarp();
             const uint32_t oa = tmem + lane_base + col_o(0) + 64 * g;  // this thread's half of both O buffers
+            // both buffers' columns in flight before one wait; O buffer 1 holds stream 1's products only when
+            // n >= 2 (otherwise its contents are selected away, never multiplied)
+            const bool two = n >= 2;
 #pragma unroll
             for (int c = 0; c < 64; c += 32) {
-                float x0[32];
-                tmem_ld32(oa + c, x0);
-                if (n >= 2) {  // stream 1 wrote O buffer 1 in this item
-                    float x1[32];
-                    tmem_ld32(oa + 128 + c, x1);
+                uint32_t x0[32], x1[32];
+                tmem_ld32_nowait(oa + c, x0);
+                tmem_ld32_nowait(oa + 128 + c, x1);
+                tmem_wait_ld();
 #pragma unroll
-                    for (int i = 0; i < 32; ++i) x0[i] = x0[i] * c0 + x1[i] * c1;
-                } else {
-#pragma unroll
-                    for (int i = 0; i < 32; ++i) x0[i] *= c0;
+                for (int i = 0; i < 16; ++i) {
+                    const float a0 = __uint_as_float(x0[2 * i]) * c0, a1 = __uint_as_float(x0[2 * i + 1]) * c0;
+                    const float b0 = two ? __uint_as_float(x1[2 * i]) * c1 : 0.f;
+                    const float b1 = two ? __uint_as_float(x1[2 * i + 1]) * c1 : 0.f;
+                    ob[c / 2 + i] = pack_bf16x2(a0 + b0, a1 + b1);
                 }
-#pragma unroll
-                for (int i = 0; i < 16; ++i) ob[c / 2 + i] = pack_bf16x2(x0[2 * i], x0[2 * i + 1]);
             }
             tc_fence_before();
             mbar_arrive(oempty);
