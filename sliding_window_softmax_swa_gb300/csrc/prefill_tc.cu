@@ -75,18 +75,18 @@ constexpr int NV = 2;                      // V tile stages (a slot frees after 
 constexpr uint32_t HALF_BYTES = 128 * 128;  // one 64-column half of a 128-row bf16 tile (16 KB)
 constexpr uint32_t TILE_BYTES = 2 * HALF_BYTES;
 constexpr int MAX_TILES = 64;
-constexpr int kSmWarps = 8;                    // softmax warps: four per key half of a tile
+constexpr int kSmWarps = 8;                    // softmax warps: four per stream
 constexpr int kSmThreads = kSmWarps * 32;
 constexpr int kWarpTma = kSmWarps, kWarpMma = kSmWarps + 1, kWarpList = kSmWarps + 2;
 constexpr int kThreads = (kSmWarps + 3) * 32;  // softmax warps, TMA producers, MMA issuer, tile lists
 constexpr uint32_t kTmemCols = 512;
-// TMEM columns: S buffers 0, 1 (scores fp32, then P as bf16 pairs in their first 64 columns) and O buffers
-// 0, 1 (fp32 accumulators of alternate items)
+// TMEM columns: S buffers 0, 1 of the two streams (scores fp32, then P as bf16 pairs in their first 64
+// columns) and their O buffers 0, 1 (fp32 accumulators)
 __host__ __device__ constexpr uint32_t col_s(int b) { return static_cast<uint32_t>(b) * 128u; }
 __host__ __device__ constexpr uint32_t col_o(int b) { return 256u + static_cast<uint32_t>(b) * 128u; }
 constexpr float kRescaleLog2 = 8.f;  // rescale O only when the running max grows by more than 2^8
 
-constexpr uint32_t OFF_Q = 0;                         // Q_0, Q_1
+constexpr uint32_t OFF_Q = 0;                         // Q buffers 0, 1 (alternate items; the O staging)
 constexpr uint32_t OFF_K = OFF_Q + 2 * TILE_BYTES;
 constexpr uint32_t OFF_V = OFF_K + NK * TILE_BYTES;
 constexpr uint32_t OFF_BAR = OFF_V + NV * TILE_BYTES;
