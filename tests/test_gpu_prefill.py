@@ -57,6 +57,8 @@ BF16_SHAPES = [
     (1, 1, 9000, 7296, 4),   # the largest window the 64-entry key-tile list takes at s = 4
     (8, 300, 64, 16, 4),     # 2400 (b, h) rows of one short query pair: many rounds of the persistent grid
     (1, 1, 640, 256, 130),
+    (1, 2, 600, 14, 4),      # band of 137 keys per query tile: a 9-key narrow tile (N = 16 product) after each full one
+    (1, 1, 700, 300, 17),    # a sink tile of 17 keys: just past the narrow-tile limit, on the full-width path
 ]
 
 
