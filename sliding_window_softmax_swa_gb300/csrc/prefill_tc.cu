@@ -70,7 +70,7 @@ constexpr int BH_ROWS = BQ;                // rows per query tile in the tile-li
 constexpr int BM = 2 * BQ;                 // rows of a query pair (the block-sparse lists are built per pair)
 constexpr int BN = 128;                    // keys per key tile
 constexpr int HD = 128;                    // head dimension
-constexpr int NK = 2;                      // K tile stages (a slot frees after its QK products)
+constexpr int NK = 2;                      // K tile slots: slot j mod 2 holds key tile j of an item
 constexpr int NV = 2;                      // V tile stages (a slot frees after its PV products)
 constexpr uint32_t HALF_BYTES = 128 * 128;  // one 64-column half of a 128-row bf16 tile (16 KB)
 constexpr uint32_t TILE_BYTES = 2 * HALF_BYTES;
@@ -312,9 +312,8 @@ __global__ void __launch_bounds__(kThreads, 1) swa_prefill_tc_kernel(const __gri
     uint64_t *bars = reinterpret_cast<uint64_t *>(sm + OFF_BAR);
     uint64_t *qfull = bars;           // [2]: Q buffer b landed
     uint64_t *ostage = qfull + 2;     // [2]: the item's O rows staged in Q buffer b (all softmax threads)
-    uint64_t *kfull = ostage + 2;     // [NK]
-    uint64_t *kempty = kfull + NK;    // [NK]
-    uint64_t *vfull = kempty + NK;    // [NV]
+    uint64_t *kfull = ostage + 2;     // [NK] (K slot g is free again once sfull[g] completes)
+    uint64_t *vfull = kfull + NK;     // [NV]
     uint64_t *vempty = vfull + NV;    // [NV]
     uint64_t *sfull = vempty + NV;    // [2]: S buffer g holds Q K_j^T of stream g
     uint64_t *pfull = sfull + 2;      // [2]: P_j written over S buffer g (the stream's 128 softmax threads)
@@ -339,7 +338,6 @@ __global__ void __launch_bounds__(kThreads, 1) swa_prefill_tc_kernel(const __gri
             mbar_init(&qfull[i], 1);
             mbar_init(&ostage[i], kSmThreads);
             mbar_init(&kfull[i], 1);
-            mbar_init(&kempty[i], 1);
             mbar_init(&vfull[i], 1);
             mbar_init(&vempty[i], 1);
             mbar_init(&sfull[i], 1);
@@ -376,18 +374,21 @@ __global__ void __launch_bounds__(kThreads, 1) swa_prefill_tc_kernel(const __gri
 
     if (warp == kWarpTma) {
         // ------------------------------------------------------------------ TMA producers (K, V)
-        // Lane 0 streams the K tiles, lane 1 the V tiles, each in its own ring over all items of this CTA in
-        // order, so neither waits for the other: a K slot frees when the QK product that read it is done, a V
-        // slot after its PV product, and the K loads run ahead into the next item on their own.
+        // Lane 0 streams the K tiles, lane 1 the V tiles, each over all items of this CTA in order, so neither
+        // waits for the other, and the K loads run ahead into the next item on their own.  Key tile j of an
+        // item goes to K slot j mod 2, the index of the S buffer its QK product writes, so the slot is free
+        // again when the previous QK product into that S buffer is done: the sfull phase the softmax waits for
+        // (no commit of its own).  The V tiles run through a 2-stage ring whose slots free after their PV
+        // products.
         if (lane < 2) {
             const bool isk = lane == 0;
             uint64_t *full = isk ? kfull : vfull;
-            uint64_t *empty = isk ? kempty : vempty;
             uint8_t *ring = sm + (isk ? OFF_K : OFF_V);
             const CUtensorMap *m_seq = isk ? &P.tm_k : &P.tm_v;
             const CUtensorMap *m_cache = isk ? &P.tm_kc : &P.tm_vc;
             tma_prefetch_desc(m_seq);
-            int g = 0;  // tiles issued so far
+            int g = 0;           // tiles issued so far
+            int nk0 = 0, nk1 = 0;  // K lane: tiles loaded into slot 0 / 1
             for (int it = 0;; ++it) {
                 const int item = static_cast<int>(blockIdx.x) + it * G;
                 if (item >= P.n_items) break;
@@ -398,8 +399,11 @@ __global__ void __launch_bounds__(kThreads, 1) swa_prefill_tc_kernel(const __gri
                 item_rows(item, bh, row_start, cls);
                 bool fine = true;
                 for (int j = 0; j < n; ++j) {
-                    const int st = g % NK;
-                    if (!mbar_wait(&empty[st], ((g / NK) & 1) ^ 1, wc, isk ? 1 : 9, j)) {
+                    const int st = isk ? (j & 1) : g % NV;
+                    const int nst = st ? nk1 : nk0;  // K: earlier loads into this slot
+                    const bool ready = isk ? (nst == 0 || mbar_wait(&sfull[st], (nst - 1) & 1, wc, 1, j))
+                                           : mbar_wait(&vempty[st], ((g / NV) & 1) ^ 1, wc, 9, j);
+                    if (!ready) {
                         fine = false;
                         break;
                     }
@@ -414,13 +418,22 @@ __global__ void __launch_bounds__(kThreads, 1) swa_prefill_tc_kernel(const __gri
                         tma_load_3d(dst, mp, &full[st], 0, T.row0, bh);
                         tma_load_3d(dst + HALF_BYTES, mp, &full[st], 64, T.row0, bh);
                     }
+                    if (isk) {
+                        nk0 += st ^ 1;
+                        nk1 += st;
+                    }
                     ++g;
                 }
                 if (!fine) break;
                 mbar_arrive(&lfree[b]);  // this lane no longer reads the item's list
             }
             if (*abort_flag) {  // make sure no copy is still landing in shared memory
-                for (int gg = (g > NK ? g - NK : 0); gg < g; ++gg) mbar_wait_drain(&full[gg % NK], (gg / NK) & 1);
+                if (isk) {
+                    if (nk0 > 0) mbar_wait_drain(&full[0], (nk0 - 1) & 1);
+                    if (nk1 > 0) mbar_wait_drain(&full[1], (nk1 - 1) & 1);
+                } else {
+                    for (int gg = (g > NV ? g - NV : 0); gg < g; ++gg) mbar_wait_drain(&full[gg % NV], (gg / NV) & 1);
+                }
             }
         }
     } else if (warp == kWarpList) {
@@ -542,7 +555,8 @@ __global__ void __launch_bounds__(kThreads, 1) swa_prefill_tc_kernel(const __gri
             const uint32_t q_addr0 = smem_u32(sm + OFF_Q);
             const uint32_t k_addr0 = smem_u32(sm + OFF_K), v_addr0 = smem_u32(sm + OFF_V);
             bool issued_any = false, fine = true;
-            int gk = 0, gv = 0;    // K, V tiles consumed
+            int nk0 = 0, nk1 = 0;  // K tiles consumed from slot 0 / 1
+            int gv = 0;            // V tiles consumed
             int np0 = 0, np1 = 0;  // P tiles consumed per stream (pfull parity)
             for (int it = 0; fine; ++it) {
                 const int item = static_cast<int>(blockIdx.x) + it * G;
@@ -554,14 +568,14 @@ __global__ void __launch_bounds__(kThreads, 1) swa_prefill_tc_kernel(const __gri
                 const int n = ntiles_s[b];
                 const uint32_t q_addr = q_addr0 + b * TILE_BYTES;
                 const Tile *tl = tiles_s + b * MAX_TILES;
-                auto qk = [&](int j) -> bool {  // QK(j) into S buffer j mod 2
-                    const int sk = gk % NK;
-                    if (!wwait(&kfull[sk], (gk / NK) & 1, 3, j)) return false;
+                auto qk = [&](int j) -> bool {  // QK(j) into S buffer j mod 2, K from slot j mod 2
+                    const int sk = j & 1;
+                    if (!wwait(&kfull[sk], (sk ? nk1 : nk0) & 1, 3, j)) return false;
                     tc_fence_after();
-                    issue_qk(tmem + col_s(j & 1), q_addr, k_addr0 + sk * TILE_BYTES, tl[j].chi < 16);
-                    umma_commit_warp(&sfull[j & 1]);
-                    umma_commit_warp(&kempty[sk]);
-                    ++gk;
+                    issue_qk(tmem + col_s(sk), q_addr, k_addr0 + sk * TILE_BYTES, tl[j].chi < 16);
+                    umma_commit_warp(&sfull[sk]);  // S ready, and K slot sk free
+                    nk0 += sk ^ 1;
+                    nk1 += sk;
                     issued_any = true;
                     return true;
                 };
