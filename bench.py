@@ -356,7 +356,7 @@ def prefill_leg(swa, wl, steps, warmup, world, rank, clocks, e2e=False, rope=Fal
                 None, 0, dt, stream)
         call = lib.swa_sink_prefill_dilated
     elif rope:
-        nws = lib.swa_sink_prefill_rope_workspace_size(B, H, L, d)
+        nws = lib.swa_sink_prefill_rope_workspace_size(B, H, L, d, s)
         ws = torch.empty(nws, dtype=torch.uint8, device="cuda")
         args = (q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(), None, B, H, L, d, w, s, wl.scale, 10000.0,
                 ws.data_ptr(), nws, dt, stream)
@@ -421,7 +421,7 @@ def chunked_leg(swa, wl, steps, warmup, world, rank, clocks, rope=False):
     lib = swa.lib()
     stream = torch.cuda.current_stream().cuda_stream
     if rope:
-        nws = lib.swa_sink_prefill_chunked_rope_workspace_size(B, H, L, d, w)
+        nws = lib.swa_sink_prefill_chunked_rope_workspace_size(B, H, L, d, w, s)
         ws = torch.empty(nws, dtype=torch.uint8, device="cuda")
         args = (q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(), None, kc.data_ptr(), vc.data_ptr(), B, H, L,
                 d, w, s, wl.scale, C, 10000.0, ws.data_ptr(), nws, 0, stream)

@@ -101,17 +101,20 @@ int swa_sink_prefill_host(const void *q_h, const void *k_h, const void *v_h, voi
  *
  *   q, k, v, o, lse : as swa_sink_prefill, with q and k unrotated; bf16, d = 128, contiguous.
  *   rope_base : finite and > 1.
- *   workspace : caller-owned device scratch of swa_sink_prefill_rope_workspace_size(B, H, L, d) bytes
- *             (6 x B*H*L*d bf16: the rotated q, the sink-rotated q and the rotated k, each as a bf16 pair
- *             hi + lo whose sum is the fp32 rotation), 256-byte aligned.
- *   s <= 128, pos0 = 0 only (SWA_ERR_UNSUPPORTED otherwise).  Each score is formed from three tensor-core
- *   products of the pairs (hi.hi + hi.lo + lo.hi), so the rotation adds about fp32 rounding, not bf16
- *   rounding, to the scores.  Other arguments and errors as swa_sink_prefill.
+ *   workspace : caller-owned device scratch of swa_sink_prefill_rope_workspace_size(B, H, L, d, s) bytes,
+ *             256-byte aligned: the rotated q and k (4 x B*H*L*d bf16: each as a bf16 pair hi + lo whose sum
+ *             is the fp32 rotation), the sink scores (B*H*L rows of s rounded up to a multiple of 4, fp32)
+ *             and the rotated sink keys (B*H*s*d fp32).
+ *   s <= 128, pos0 = 0 only (SWA_ERR_UNSUPPORTED otherwise).  Each window score is formed from three
+ *   tensor-core products of the pairs (hi.hi + hi.lo + lo.hi), so the rotation adds about fp32 rounding, not
+ *   bf16 rounding, to the scores; the sink scores (the query rotated at min(t, w - 1)) are fp32 dot products
+ *   of fp32 rotations made by the rotation pass.  Other arguments and errors as swa_sink_prefill.
  */
 int swa_sink_prefill_rope(const void *q, const void *k, const void *v, void *o, float *lse, int B, int H,
                           int64_t L, int d, int w, int s, float scale, double rope_base, void *workspace,
                           size_t workspace_bytes, int dtype, void *stream);
-size_t swa_sink_prefill_rope_workspace_size(int B, int H, int64_t L, int d);
+/* The workspace of swa_sink_prefill_rope in bytes; 0 for arguments it does not take (d != 128, s > 128). */
+size_t swa_sink_prefill_rope_workspace_size(int B, int H, int64_t L, int d, int s);
 
 /*
  * swa_sink_prefill_chunked_rope -- swa_sink_prefill_chunked with RoPE at the positions inside the cache
@@ -123,17 +126,19 @@ size_t swa_sink_prefill_rope_workspace_size(int B, int H, int64_t L, int d);
  *   q, k, v, o, lse, k_cache, v_cache, chunk : as swa_sink_prefill_chunked; q and k unrotated; bf16,
  *             d = 128; chunk >= max(1, s).
  *   rope_base : finite and > 1.
- *   workspace : caller-owned device scratch of swa_sink_prefill_chunked_rope_workspace_size(B, H, L, d, w)
- *             bytes, 256-byte aligned: the rotated q, the sink-rotated q and the rotated k of the whole
- *             sequence as bf16 hi/lo pairs (one rotation pass serves every chunk: rotations depend on
- *             absolute positions only) and two [B, H, w, d] caches of rotated keys (hi and lo).
- *   s <= 128 (SWA_ERR_UNSUPPORTED otherwise).  Other arguments and errors as swa_sink_prefill_chunked.
+ *   workspace : caller-owned device scratch of swa_sink_prefill_chunked_rope_workspace_size(B, H, L, d, w, s)
+ *             bytes, 256-byte aligned: what swa_sink_prefill_rope keeps for the whole sequence (one rotation
+ *             pass serves every chunk: rotations depend on absolute positions only) and two [B, H, w, d] bf16
+ *             caches of rotated keys (hi and lo).
+ *   s <= 128 (SWA_ERR_UNSUPPORTED otherwise).  Scores as swa_sink_prefill_rope; other arguments and errors as
+ *   swa_sink_prefill_chunked.
  */
 int swa_sink_prefill_chunked_rope(const void *q, const void *k, const void *v, void *o, float *lse, void *k_cache,
                                   void *v_cache, int B, int H, int64_t L, int d, int w, int s, float scale,
                                   int64_t chunk, double rope_base, void *workspace, size_t workspace_bytes, int dtype,
                                   void *stream);
-size_t swa_sink_prefill_chunked_rope_workspace_size(int B, int H, int64_t L, int d, int w);
+/* The workspace of swa_sink_prefill_chunked_rope in bytes; 0 for arguments it does not take. */
+size_t swa_sink_prefill_chunked_rope_workspace_size(int B, int H, int64_t L, int d, int w, int s);
 
 /*
  * swa_sink_prefill_dilated -- whole-sequence prefill over a dilated window with sinks: the dilated sliding

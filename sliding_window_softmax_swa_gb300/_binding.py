@@ -53,10 +53,10 @@ SIGNATURES = {
     "swa_sink_prefill_dilated_workspace_size": (_sz, [_i, _i, _i64, _i, _i, _i, _i]),
     "swa_sink_prefill_chunked_rope": (_i, [_vp, _vp, _vp, _vp, _vp, _vp, _vp, _i, _i, _i64, _i, _i, _i, _f, _i64,
                                            ctypes.c_double, _vp, _sz, _i, _vp]),
-    "swa_sink_prefill_chunked_rope_workspace_size": (_sz, [_i, _i, _i64, _i, _i]),
+    "swa_sink_prefill_chunked_rope_workspace_size": (_sz, [_i, _i, _i64, _i, _i, _i]),
     "swa_sink_prefill_rope": (_i, [_vp, _vp, _vp, _vp, _vp, _i, _i, _i64, _i, _i, _i, _f, ctypes.c_double, _vp,
                                    _sz, _i, _vp]),
-    "swa_sink_prefill_rope_workspace_size": (_sz, [_i, _i, _i64, _i]),
+    "swa_sink_prefill_rope_workspace_size": (_sz, [_i, _i, _i64, _i, _i]),
     "swa_sink_prefill_blocksparse": (_i, [_vp, _vp, _vp, _vp, _vp, _i, _i, _i64, _i, _i, _i, _f, _vp, _i, _i, _vp, _i,
                                           _vp, _sz, _i, _vp]),
     "swa_sink_prefill_blocksparse_workspace_size": (_sz, [_i64, _i, _i, _i]),
@@ -227,7 +227,7 @@ def swa_sink_prefill_rope(q, k, v, w: int, s: int, rope_base: float = 10000.0, s
     assert k.shape == q.shape and v.shape == q.shape and k.dtype == q.dtype and v.dtype == q.dtype
     if o is None:
         o = torch.empty_like(q)
-    nws = lib().swa_sink_prefill_rope_workspace_size(B, H, L, d)
+    nws = lib().swa_sink_prefill_rope_workspace_size(B, H, L, d, s)
     if workspace is None:
         workspace = torch.empty(max(nws, 256), dtype=torch.uint8, device=q.device)
     _dev(q, k, v, o, lse, workspace)
@@ -246,7 +246,7 @@ def swa_sink_prefill_chunked_rope(q, k, v, w: int, s: int, chunk: int, k_cache, 
     w_ = k_cache.shape[2]
     if o is None:
         o = torch.empty_like(q)
-    nws = lib().swa_sink_prefill_chunked_rope_workspace_size(B, H, L, d, w_)
+    nws = lib().swa_sink_prefill_chunked_rope_workspace_size(B, H, L, d, w_, s)
     if workspace is None:
         workspace = torch.empty(max(nws, 256), dtype=torch.uint8, device=q.device)
     _dev(q, k, v, o, lse, k_cache, v_cache, workspace)

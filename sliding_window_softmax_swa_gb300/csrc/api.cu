@@ -64,7 +64,7 @@ unsigned long long *device_timeout_info() {
 }
 
 int launch_prefill_bf16_tc(const PrefillArgs &a) {
-    if (a.q_sink != nullptr || a.d == 64) return launch_prefill_bf16_tc_sub(a);
+    if (a.rope || a.d == 64) return launch_prefill_bf16_tc_sub(a);
     return launch_prefill_bf16_tc_plain(a);
 }
 
@@ -208,7 +208,8 @@ static ChunkStreams *chunk_streams() {
 // RoPE mode of the chunk loop: q and k passed to it are the rotated rows (hi parts); these are the rest.
 struct ChunkRope {
     const void *q_lo;                  // [BH, L, d] lo parts of the rotated query rows
-    const void *q_sink, *q_sink_lo;    // [BH, L, d] query rows rotated for the sink keys (hi, lo)
+    const float *ssink;                // [BH, L, sstride] the sink scores of every row (fp32)
+    int sstride;
     const void *k_lo;                  // [BH, L, d] lo parts of the rotated keys
     const void *k_raw;                 // [BH, L, d] unrotated keys: they go into the caller's cache
     void *kc_rot, *kc_rot_lo;          // [BH, w, d] scratch cache of rotated keys (hi, lo), read by the
@@ -263,8 +264,10 @@ static int chunk_loop(const void *q, const void *k, const void *v, void *o, floa
                 // rotated rows against the rotated cache; then the chunk's rotated keys (hi and lo) into the
                 // scratch caches, its unrotated keys and its values into the caller's
                 PrefillArgs a{qc, kc, vc, oc, lc, krg, vcg, c0, r1 - r0, n, d, w, s, scale, stride, gs};
-                a.q_sink = static_cast<const char *>(rp->q_sink) + off;
-                a.q_sink_lo = static_cast<const char *>(rp->q_sink_lo) + off;
+                a.rope = true;
+                a.rope_ssink = rp->ssink + (static_cast<size_t>(r0) * static_cast<size_t>(stride) + static_cast<size_t>(c0)) *
+                                               static_cast<size_t>(rp->sstride);
+                a.rope_sstride = rp->sstride;
                 a.q_lo = static_cast<const char *>(rp->q_lo) + off;
                 a.k_lo = static_cast<const char *>(rp->k_lo) + off;
                 a.k_cache_lo = krg_lo;
@@ -304,9 +307,9 @@ extern "C" int swa_sink_prefill_chunked(const void *q, const void *k, const void
                       static_cast<cudaStream_t>(stream), nullptr);
 }
 
-extern "C" size_t swa_sink_prefill_chunked_rope_workspace_size(int B, int H, int64_t L, int d, int w) {
-    if (B < 1 || H < 1 || L < 0 || d != 128 || w < 1) return 0;
-    return rope_prefill_workspace_bytes(B * H, L, d) + 2 * static_cast<size_t>(B) * H * w * d * 2;
+extern "C" size_t swa_sink_prefill_chunked_rope_workspace_size(int B, int H, int64_t L, int d, int w, int s) {
+    if (B < 1 || H < 1 || L < 0 || d != 128 || w < 1 || s < 0 || s > 128) return 0;
+    return rope_prefill_workspace_bytes(B * H, L, d, s) + 2 * static_cast<size_t>(B) * H * w * d * 2;
 }
 
 extern "C" int swa_sink_prefill_chunked_rope(const void *q, const void *k, const void *v, void *o, float *lse,
@@ -322,7 +325,7 @@ extern "C" int swa_sink_prefill_chunked_rope(const void *q, const void *k, const
         return fail(SWA_ERR_INVALID, "chunk=%lld must be >= max(1, s) with RoPE", (long long)chunk);
     if (!(rope_base == rope_base) || rope_base <= 1.0 || rope_base > 1e30)
         return fail(SWA_ERR_INVALID, "rope_base must be a finite number > 1");
-    const size_t need = swa_sink_prefill_chunked_rope_workspace_size(B, H, L, d, w);
+    const size_t need = swa_sink_prefill_chunked_rope_workspace_size(B, H, L, d, w, s);
     if (workspace_bytes < need)
         return fail(SWA_ERR_INVALID, "workspace of %zu bytes is smaller than the %zu needed", workspace_bytes, need);
     if (L == 0) return SWA_OK;
@@ -333,13 +336,13 @@ extern "C" int swa_sink_prefill_chunked_rope(const void *q, const void *k, const
         return fail(SWA_ERR_INVALID, "workspace must be non-null and 256-byte aligned");
     const cudaStream_t st = static_cast<cudaStream_t>(stream);
     char *ws = static_cast<char *>(workspace);
-    const RopeParts rpt = rope_parts(ws, B * H, L, d);
-    char *kc_rot = ws + rope_prefill_workspace_bytes(B * H, L, d);
+    const RopeParts rpt = rope_parts(ws, B * H, L, d, s);
+    char *kc_rot = ws + rope_prefill_workspace_bytes(B * H, L, d, s);
     char *kc_rot_lo = kc_rot + static_cast<size_t>(B) * H * w * d * 2;
     // the rotations depend on absolute positions only, so one pass serves every chunk
-    rc = launch_rope_prep(q, k, rpt, B * H, L, d, w, rope_base, st);
+    rc = launch_rope_prep(q, k, rpt, B * H, L, d, w, s, rope_base, st);
     if (rc) return rc;
-    const ChunkRope rp{rpt.qr_lo, rpt.qs, rpt.qs_lo, rpt.kr_lo, k, kc_rot, kc_rot_lo};
+    const ChunkRope rp{rpt.qr_lo, rpt.ssink, rpt.sstride, rpt.kr_lo, k, kc_rot, kc_rot_lo};
     return chunk_loop(rpt.qr, rpt.kr, v, o, lse, k_cache, v_cache, B, H, L, L, d, w, s, scale, chunk, dtype, st, &rp);
 }
 
@@ -738,9 +741,9 @@ extern "C" int swa_sink_prefill_chunked_dilated(const void *q, const void *k, co
     return launch_dilate_scatter(ov, lsev, o, lse, B * H, L, d, es, s, r, st);
 }
 
-extern "C" size_t swa_sink_prefill_rope_workspace_size(int B, int H, int64_t L, int d) {
-    if (B < 1 || H < 1 || L < 0 || d != 128) return 0;
-    return rope_prefill_workspace_bytes(B * H, L, d);
+extern "C" size_t swa_sink_prefill_rope_workspace_size(int B, int H, int64_t L, int d, int s) {
+    if (B < 1 || H < 1 || L < 0 || d != 128 || s < 0 || s > 128) return 0;
+    return rope_prefill_workspace_bytes(B * H, L, d, s);
 }
 
 extern "C" int swa_sink_prefill_rope(const void *q, const void *k, const void *v, void *o, float *lse, int B, int H,
@@ -753,19 +756,20 @@ extern "C" int swa_sink_prefill_rope(const void *q, const void *k, const void *v
     if (s > 128) return fail(SWA_ERR_UNSUPPORTED, "RoPE prefill needs s <= 128 (s=%d)", s);
     if (!(rope_base == rope_base) || rope_base <= 1.0 || rope_base > 1e30)
         return fail(SWA_ERR_INVALID, "rope_base must be a finite number > 1");
-    const size_t need = rope_prefill_workspace_bytes(B * H, L, d);
+    const size_t need = rope_prefill_workspace_bytes(B * H, L, d, s);
     if (workspace_bytes < need)
         return fail(SWA_ERR_INVALID, "workspace of %zu bytes is smaller than the %zu needed", workspace_bytes, need);
     if (L == 0) return SWA_OK;
     if (!workspace || (reinterpret_cast<uintptr_t>(workspace) & 255u))
         return fail(SWA_ERR_INVALID, "workspace must be non-null and 256-byte aligned");
     const cudaStream_t st = static_cast<cudaStream_t>(stream);
-    const RopeParts rpt = rope_parts(workspace, B * H, L, d);
-    rc = launch_rope_prep(q, k, rpt, B * H, L, d, w, rope_base, st);
+    const RopeParts rpt = rope_parts(workspace, B * H, L, d, s);
+    rc = launch_rope_prep(q, k, rpt, B * H, L, d, w, s, rope_base, st);
     if (rc) return rc;
     PrefillArgs a{rpt.qr, rpt.kr, v, o, lse, nullptr, nullptr, 0, B * H, L, d, w, s, scale, L, st};
-    a.q_sink = rpt.qs;
-    a.q_sink_lo = rpt.qs_lo;
+    a.rope = true;
+    a.rope_ssink = rpt.ssink;
+    a.rope_sstride = rpt.sstride;
     a.q_lo = rpt.qr_lo;
     a.k_lo = rpt.kr_lo;
     return launch_prefill_bf16_tc(a);

@@ -1002,7 +1002,7 @@ static int sm_count() {
 static int launch_impl(const PrefillArgs &a, const BlockSparseDev *bs, int dil_r = 0) {
     using namespace tc;
     if (a.d != HD) return fail(SWA_ERR_UNSUPPORTED, "tensor-core prefill needs d = %d", HD);
-    if (a.q_sink) return fail(SWA_ERR_INVALID, "the RoPE prefill runs on the sub-tile kernel");
+    if (a.rope) return fail(SWA_ERR_INVALID, "the RoPE prefill runs on the sub-tile kernel");
     if (!bs && max_tiles_bound(a.w, a.s) > MAX_TILES)
         return fail(SWA_ERR_UNSUPPORTED, "window w=%d needs more than %d key tiles per query tile", a.w, MAX_TILES);
     // dilated mode: every class runs over the virtual rows [s, s + nrows), nrows = the rows of the longest

@@ -123,9 +123,11 @@ static_assert(sizeof(Tile) == 12, "tile record");
 
 struct Params {
     CUtensorMap tm_q, tm_k, tm_v, tm_kc, tm_vc;
-    CUtensorMap tm_qs;  // RoPE mode: query rows rotated for the sink keys (the sink tile, first in every
-                        // list, is scored with them; the band with tm_q)
-    CUtensorMap tm_ql, tm_qsl, tm_kl, tm_kcl;  // HILO: the lo parts of q, q_sink, k and the cached keys
+    CUtensorMap tm_ql, tm_kl, tm_kcl;  // HILO: the lo parts of q, k and the cached keys
+    // RoPE mode: the sink tile's scores (the query rotated at min(t, w - 1) against the rotated sinks), fp32,
+    // row (b, h) * seq_stride + local row, sstride floats per row
+    const float *ssink;
+    int sstride;
     void *o;
     float *lse;
     DeviceStatus *status;
@@ -428,6 +430,12 @@ __global__ void __launch_bounds__(kThreads, 1) swa_prefill_tc_kernel(const __gri
                     const int row = T.row0 + SUB * h;
                     uint8_t *dst = ring + st * slot_bytes;
                     (isk ? kseq : vseq)[st] = g;
+                    if (ROPE && isk && T.pbase < P.s) {  // the sink scores are ready-made: no K rows
+                        mbar_arrive(&full[st]);
+                        ++g;
+                        walk_step(j, h);
+                        continue;
+                    }
                     mbar_arrive_expect_tx(&full[st], slot_bytes);
                     if (isk) {
                         const CUtensorMap *mk = (T.flags & 1) ? &P.tm_kc : &P.tm_k;
@@ -482,39 +490,29 @@ __global__ void __launch_bounds__(kThreads, 1) swa_prefill_tc_kernel(const __gri
                 mark_tiles(tl, n, q0, qlast, P.s, P.m);
                 ntiles_s[b] = n;
                 mbar_arrive(&lready[b]);  // release: the list is visible to whoever sees the phase complete
-                // Q loads of the item: one (tm_q), or in RoPE mode with sinks the sink-rotated rows for
-                // the first tile and then, once its QK products are done, the band-rotated rows.  Every
-                // load waits until the QK products of the previous one are done.
-                const CUtensorMap *mq0 = (ROPE && P.s > 0) ? &P.tm_qs : &P.tm_q;
-                const CUtensorMap *mq0l = (ROPE && P.s > 0) ? &P.tm_qsl : &P.tm_ql;
-                const bool two = ROPE && P.s > 0 && n >= 2;
+                // Q_0, Q_1 of the item (in HILO mode hi and lo parts), once the previous item's QK products are
+                // done; then the next item's Q into L2, so that its load does not wait for DRAM
                 bool ok = true;
-                for (int ph = 0; ph < (two ? 2 : 1) && ok; ++ph) {
-                    const CUtensorMap *mq = ph == 0 ? mq0 : &P.tm_q;
-                    const CUtensorMap *mql = ph == 0 ? mq0l : &P.tm_ql;
-                    if (nq >= 1 && !mbar_wait(qempty, (nq - 1) & 1, wc, 13, it)) {
-                        ok = false;
-                        break;
-                    }
+                if (nq >= 1 && !mbar_wait(qempty, (nq - 1) & 1, wc, 13, it)) {
+                    ok = false;
+                } else {
                     uint8_t *qs = sm + LYQ::OFF_Q;
                     mbar_arrive_expect_tx(qfull, 2 * LYQ::QTILE);
                     for (int x = 0; x < 2; ++x) {
 #pragma unroll
                         for (int c = 0; c < LYQ::NB; ++c) {
-                            tma_load_3d(qs + x * LYQ::QTILE + c * QBOX, mq, qfull, 64 * c, row_start + x * BH_ROWS, bh);
+                            tma_load_3d(qs + x * LYQ::QTILE + c * QBOX, &P.tm_q, qfull, 64 * c, row_start + x * BH_ROWS, bh);
                             if (ROPE)
-                                tma_load_3d(qs + x * LYQ::QTILE + LYQ::QPART + c * QBOX, mql, qfull, 64 * c,
+                                tma_load_3d(qs + x * LYQ::QTILE + LYQ::QPART + c * QBOX, &P.tm_ql, qfull, 64 * c,
                                             row_start + x * BH_ROWS, bh);
                         }
                     }
                     ++nq;
-                    // into L2 meanwhile: the band rows of this item (RoPE), else the next item's first rows
-                    const int nitem = (two && ph == 0) ? item : item + G;
-                    const CUtensorMap *mp = (two && ph == 0) ? &P.tm_q : mq0;
+                    const int nitem = item + G;
                     if (nitem < P.n_items) {
                         const int nrow = (P.n_qpairs - 1 - nitem / P.BH) * BM;
                         for (int x = 0; x < 2; ++x)
-                            for (int c = 0; c < LYQ::NB; ++c) tma_prefetch_3d(mp, 64 * c, nrow + x * BH_ROWS, nitem % P.BH);
+                            for (int c = 0; c < LYQ::NB; ++c) tma_prefetch_3d(&P.tm_q, 64 * c, nrow + x * BH_ROWS, nitem % P.BH);
                     }
                 }
                 if (!ok) break;
@@ -566,29 +564,28 @@ __global__ void __launch_bounds__(kThreads, 1) swa_prefill_tc_kernel(const __gri
                         nwalk += u ? 1 : 0;
                     }
                 int left_qk = left_pv;  // QK_x products of this item still to issue
-                // RoPE mode with sinks: the sink tile (tile 0) uses the first Q load, the band a second one
-                const bool two = ROPE && P.s > 0 && n >= 2;
-                bool q_band = !two;
                 int kj = 0, kh = 0, kg = gbase;  // QK walk position (stream index kg)
-                // QK_x of the next sub-tile x needs: 1 if issued, 0 if there is none (in this item, or before
-                // the band-rotated Q is loaded), -1 on a failed wait
+                // QK_x of the next sub-tile x needs: 1 if issued, 0 if there is none in this item, -1 on a failed
+                // wait.  In RoPE mode the sink sub-tiles take no product (their scores are ready-made), only the
+                // commit that tells the softmax its turn has come and the K slot's (empty) load has landed.
                 auto qk_step = [&]() -> int {
                     if (!seek_mine(tl, n, kj, kh, kg, mybit)) return 0;
-                    if (!q_band && kj != 0) return 0;  // band products wait for the band-rotated Q
                     const int st = kg % NK;
                     if (!slot_wait(&kseq[st], kg, wc, 16) || !mbar_wait(&kfull[st], (kg / NK) & 1, wc, 3, kg)) return -1;
                     tc_fence_after();
                     const uint32_t ka = k_addr0 + st * LYM::KSLOT;
                     const uint32_t d = s_tm + SUB * (qi & 1);
-                    issue_qk<HD>(d, qa, ka, false);
-                    if (ROPE) {  // + hi_q lo_k + lo_q hi_k
-                        issue_qk<HD>(d, qa, ka + LYM::KPART, true);
-                        issue_qk<HD>(d, qa + LYM::QPART, ka, true);
+                    if (!(ROPE && tl[kj].pbase < P.s)) {
+                        issue_qk<HD>(d, qa, ka, false);
+                        if (ROPE) {  // + hi_q lo_k + lo_q hi_k
+                            issue_qk<HD>(d, qa, ka + LYM::KPART, true);
+                            issue_qk<HD>(d, qa + LYM::QPART, ka, true);
+                        }
                     }
                     umma_commit(&sfull[x * 2 + (qi & 1)]);  // the softmax releases the K slot once this is done
                     ++qi;
                     issued_any = true;
-                    if (--left_qk == 0 && q_band) umma_commit(qempty);  // the item's last QK_x product
+                    if (--left_qk == 0) umma_commit(qempty);  // the item's last QK_x product
                     walk_step(kj, kh);
                     ++kg;
                     return 1;
@@ -602,19 +599,6 @@ __global__ void __launch_bounds__(kThreads, 1) swa_prefill_tc_kernel(const __gri
                     }
                     return true;
                 };
-                if (two) {
-                    // the sink sub-tiles (tile 0, at most two) with the sink-rotated Q, then the band-rotated Q
-                    while (left_qk > 0 && qi - cnt < 2) {
-                        const int r = qk_step();
-                        if (r < 0) fine = false;
-                        if (r <= 0) break;
-                    }
-                    if (!fine) break;
-                    umma_commit(qempty);  // the sink-rotated Q is no longer read once these are done
-                    if (!mbar_wait(qfull, nqf & 1, wc, 2, it)) break;
-                    ++nqf;
-                    q_band = true;
-                }
                 if (left_qk == 0) umma_commit(qempty);  // no (more) QK_x product in this item
                 if (!top_up()) break;
                 int pj = 0, ph = 0, pg = gbase;  // PV walk position
@@ -708,7 +692,16 @@ __global__ void __launch_bounds__(kThreads, 1) swa_prefill_tc_kernel(const __gri
                 // the row's 64 scores of this half of S_x in registers (one TMEM load)
                 float sv[SUB];
                 __syncwarp();
-                tmem_ld64(s_addr + SUB * hs, sv);
+                if (ROPE && T.pbase < P.s) {
+                    // a sink sub-tile of RoPE mode: the rotation pass's fp32 scores (rows of this call only)
+                    const int lrow = row_start + x * BH_ROWS + r;
+                    const bool rowok = lrow < P.L;
+                    const float *sr = P.ssink + (static_cast<int64_t>(bh) * P.seq_stride + lrow) * P.sstride + pb;
+#pragma unroll
+                    for (int c = 0; c < SUB; ++c) sv[c] = (rowok && c <= chi) ? sr[c] : -INFINITY;
+                } else {
+                    tmem_ld64(s_addr + SUB * hs, sv);
+                }
                 if (any_masked) {
 #pragma unroll
                     for (int c = 0; c < SUB; ++c) sv[c] = (mw[c >> 5] & (1u << (c & 31))) ? sv[c] : -INFINITY;
@@ -877,9 +870,10 @@ static int launch_typed(const tcs::Params &p, int n_ctas, cudaStream_t stream) {
 int launch_prefill_bf16_tc_sub(const PrefillArgs &a) {
     using namespace tcs;
     if (a.d != 64 && a.d != 128) return fail(SWA_ERR_UNSUPPORTED, "tensor-core prefill needs d = 64 or 128");
-    const bool rope = a.q_sink != nullptr;
-    if (rope && (a.d != 128 || !a.q_lo || !a.q_sink_lo || !a.k_lo || (a.pos0 > 0 && !a.k_cache_lo)))
-        return fail(SWA_ERR_INVALID, "RoPE prefill needs d = 128 and the lo parts of q, q_sink and k");
+    const bool rope = a.rope;
+    if (rope && (a.d != 128 || !a.q_lo || !a.k_lo || (a.pos0 > 0 && !a.k_cache_lo) || (a.s > 0 && !a.rope_ssink) ||
+                 a.rope_sstride < a.s))
+        return fail(SWA_ERR_INVALID, "RoPE prefill needs d = 128, the lo parts of q and k and the sink scores");
     if (rope && ((a.pos0 > 0 && a.pos0 < a.s) || a.s > BN))
         return fail(SWA_ERR_UNSUPPORTED, "RoPE prefill needs pos0 = 0 or pos0 >= s, and s <= %d", BN);
     if (max_tiles_bound(a.w, a.s) + (rope ? 1 : 0) > MAX_TILES)
@@ -903,10 +897,8 @@ int launch_prefill_bf16_tc_sub(const PrefillArgs &a) {
               encode_rows_map(&p.tm_vc, a.v_cache, written, a.BH, a.w, d, 64);
     else
         okm = okm && encode_rows_map(&p.tm_kc, a.k, L, a.BH, st, d, 64) && encode_rows_map(&p.tm_vc, a.v, L, a.BH, st, d, 64);
-    okm = okm && encode_rows_map(&p.tm_qs, rope ? a.q_sink : a.q, L, a.BH, st, d, 128);
     if (rope) {
         okm = okm && encode_rows_map(&p.tm_ql, a.q_lo, L, a.BH, st, d, 128) &&
-              encode_rows_map(&p.tm_qsl, a.q_sink_lo, L, a.BH, st, d, 128) &&
               encode_rows_map(&p.tm_kl, a.k_lo, L, a.BH, st, d, 64);
         if (a.pos0 > 0)
             okm = okm && encode_rows_map(&p.tm_kcl, a.k_cache_lo, written, a.BH, a.w, d, 64);
@@ -914,10 +906,11 @@ int launch_prefill_bf16_tc_sub(const PrefillArgs &a) {
             okm = okm && encode_rows_map(&p.tm_kcl, a.k_lo, L, a.BH, st, d, 64);
     } else {
         p.tm_ql = p.tm_q;
-        p.tm_qsl = p.tm_qs;
         p.tm_kl = p.tm_k;
         p.tm_kcl = p.tm_kc;
     }
+    p.ssink = a.rope_ssink;
+    p.sstride = a.rope_sstride;
     if (!okm) return fail(SWA_ERR_INVALID, "cuTensorMapEncodeTiled rejected a tensor (alignment or size)");
     p.o = a.o;
     p.lse = a.lse;

@@ -36,12 +36,14 @@ struct PrefillArgs {
     int64_t seq_stride;  // rows between consecutive (b, h) blocks (== L for contiguous tensors)
     cudaStream_t stream;
     // RoPE at the positions inside the cache (bf16 tensor-core prefill, d = 128): q and k are the rotated
-    // rows (their bf16 hi parts), q_sink the query rows rotated for the sink keys; the sinks get their own
-    // key tile, scored with q_sink, and the band starts at position s.  Every rotated operand comes as a
-    // (hi, lo) bf16 pair whose sum is the fp32 rotation: q_lo, q_sink_lo, k_lo, and k_cache_lo for the
-    // rotated keys of the cache (pos0 > 0)
-    const void *q_sink = nullptr;
-    const void *q_lo = nullptr, *q_sink_lo = nullptr, *k_lo = nullptr, *k_cache_lo = nullptr;
+    // rows (their bf16 hi parts); the sinks get their own key tile, whose scores are read ready-made from
+    // rope_ssink (fp32, row (b, h) * seq_stride + local row, rope_sstride floats per row), and the band starts
+    // at position s.  Every rotated operand comes as a (hi, lo) bf16 pair whose sum is the fp32 rotation:
+    // q_lo, k_lo, and k_cache_lo for the rotated keys of the cache (pos0 > 0)
+    bool rope = false;
+    const float *rope_ssink = nullptr;
+    int rope_sstride = 0;
+    const void *q_lo = nullptr, *k_lo = nullptr, *k_cache_lo = nullptr;
 };
 
 int launch_prefill_f32(const PrefillArgs &a);
@@ -83,16 +85,20 @@ int launch_dilate_gather(const void *q, const void *k, const void *v, void *qv, 
                          int d, int esize, int s, int r, cudaStream_t stream);
 int launch_dilate_scatter(const void *ov, const float *lsev, void *o, float *lse, int BH, int64_t L, int d, int esize,
                           int s, int r, cudaStream_t stream);
-// The rotation pass of RoPE prefill: for the rows of [BH, L, d] (d = 128, bf16) qr = R(t) q, qs = R(min(t, w - 1)) q
-// and kr = R(t) k, each written as a bf16 (hi, lo) pair with hi + lo the fp32 rotation.  The workspace holds
-// the six [BH, L, d] tensors in this order.
+// The rotation pass of RoPE prefill: for the rows of [BH, L, d] (d = 128, bf16) qr = R(t) q and kr = R(t) k, each
+// written as a bf16 (hi, lo) pair with hi + lo the fp32 rotation, and the sink scores
+// ssink[t][i] = (R(min(t, w - 1)) q_t) . (R(i) k_i), i < s, in fp32 (sstride floats per row); ks holds the
+// rotated sink keys (fp32 [BH, s, d]) the scores are made from.
 struct RopeParts {
-    void *qr, *qr_lo, *qs, *qs_lo, *kr, *kr_lo;
+    void *qr, *qr_lo, *kr, *kr_lo;
+    float *ssink, *ks;
+    int sstride;
 };
-size_t rope_prefill_workspace_bytes(int BH, int64_t L, int d);
-RopeParts rope_parts(void *workspace, int BH, int64_t L, int d);
-int launch_rope_prep(const void *q, const void *k, const RopeParts &out, int BH, int64_t L, int d, int w, double base,
-                     cudaStream_t stream);
+int rope_sink_stride(int s);
+size_t rope_prefill_workspace_bytes(int BH, int64_t L, int d, int s);
+RopeParts rope_parts(void *workspace, int BH, int64_t L, int d, int s);
+int launch_rope_prep(const void *q, const void *k, const RopeParts &out, int BH, int64_t L, int d, int w, int s,
+                     double base, cudaStream_t stream);
 
 // Rolling-cache write of positions pos0..pos0+n-1; source rows of (b, h) start at bh*src_stride.  With
 // v_new == nullptr only the keys are written.

@@ -71,35 +71,44 @@ def oracle_rows(q, k, v, bh_list, row_blocks, w, s, scale, pos_offset=0):
 # ---------------------------------------------------------------- RoPE prefill: rotated operands
 def check_rope_prefill(name, o_got, lse_got, ops, qf, kf, vf, rows, w, s, scale, base, o_ref, l_ref):
     """RoPE prefill rows, in two parts.
-    (a) The rotation pass: ops = (qr, qs, kr), the kernel's operands read back from its workspace as
-        hi + lo (qr, qs at the selected rows, kr at positions 0..max(rows)), each element within 2^-16 relative
-        of the oracle's fp64 rotation (q at t, q at min(t, w - 1), k at i; the (hi, lo) bf16 pair keeps ~17
-        bits), plus 1e-5 of the row's largest input magnitude for the fp32 sin/cos (absolute error ~5e-7)
-        where x cos - y sin cancels.
+    (a) The rotation pass: ops = (qr, kr, ssink), read back from the kernel's workspace.  qr (at the selected
+        rows) and kr (at positions 0..max(rows)) as hi + lo: each element within 2^-16 relative of the oracle's
+        fp64 rotation (q at t, k at i; the (hi, lo) bf16 pair keeps ~17 bits), plus 1e-5 of the row's largest
+        input magnitude for the fp32 sin/cos (absolute error ~5e-7) where x cos - y sin cancels.
+        ssink[row, i], i < s, is the sink score (R(min(t, w - 1)) q_t) . (R(i) k_i): within 1e-5 |R q| |R k| of
+        the oracle's fp64 dot product of its fp64 rotations (fp32 rotations and an fp32 sum of 128 terms).
     (b) The result against the oracle's exact definition (o_ref, l_ref) with the bf16 tolerances of every
-        path and 1e-3 on the log-sum-exp: the scores are formed from the (hi, lo) operands with the error of
-        fp32 ones, far below what the bf16 output rounding allows.
+        path and 1e-3 on the log-sum-exp: the window scores are formed from the (hi, lo) operands with the error
+        of fp32 ones, the sink scores in fp32, far below what the bf16 output rounding allows.
     o_got [nh, nr, d], lse_got [nh, nr]: numpy fp64."""
-    qr, qs, kr = ops
+    qr, kr, ssink = ops
     top = max(rows) + 1
     pos = np.arange(top, dtype=np.float64)
     rows_f = np.asarray(rows, dtype=np.float64)
     for got, src, want, what in ((qr, qf[:, rows], oracle.rope(qf[:, rows], rows_f, base), "q at t"),
-                                 (qs, qf[:, rows], oracle.rope(qf[:, rows], np.minimum(rows_f, w - 1), base),
-                                  "q at min(t, w-1)"),
                                  (kr, kf[:, :top], oracle.rope(kf[:, :top], pos, base), "k at i")):
         slack = 1e-5 * np.abs(src).max(axis=-1, keepdims=True)
         assert (np.abs(got - want) <= 2.0 ** -16 * np.abs(want) + slack).all(), f"{name}: rotated {what}"
+    if s > 0:
+        qs = oracle.rope(qf[:, rows], np.minimum(rows_f, w - 1), base)   # [nh, nr, d]
+        ks = oracle.rope(kf[:, :s], np.arange(s, dtype=np.float64), base)  # [nh, s, d]
+        want = np.einsum("hrd,hid->hri", qs, ks)
+        bound = 1e-5 * np.linalg.norm(qs, axis=-1)[:, :, None] * np.linalg.norm(ks, axis=-1)[:, None, :]
+        assert (np.abs(ssink - want) <= bound).all(), f"{name}: sink scores"
     compare(f"{name} vs oracle", o_got, o_ref, torch.bfloat16)
     assert np.abs(lse_got - l_ref).max() < LSE_ABS, f"{name}: lse vs oracle"
 
 
-def rope_workspace_operands(ws, B, H, L, d, rows):
-    """The rotated operands a RoPE prefill left in its workspace (qr, qr_lo, qs, qs_lo, kr, kr_lo: bf16
-    [B*H, L, d] each), as hi + lo in fp64: qr and qs at the selected rows, kr at positions 0..max(rows)."""
+def rope_workspace_operands(ws, B, H, L, d, s, rows):
+    """What a RoPE prefill left in its workspace (qr, qr_lo, kr, kr_lo: bf16 [B*H, L, d] each; then the sink
+    scores, fp32 [B*H, L, 4 ceil(s/4)]), in fp64: qr as hi + lo at the selected rows, kr as hi + lo at positions
+    0..max(rows), and the first s sink scores of the selected rows."""
     nh = B * H
-    t = ws[:6 * nh * L * d * 2].view(torch.bfloat16).reshape(6, nh, L, d).double()
+    one = nh * L * d
+    t = ws[:4 * one * 2].view(torch.bfloat16).reshape(4, nh, L, d).double()
     top = max(rows) + 1
     ridx = torch.as_tensor(rows, device=ws.device)
-    qr, qs, kr = t[0] + t[1], t[2] + t[3], t[4] + t[5]
-    return qr[:, ridx].cpu().numpy(), qs[:, ridx].cpu().numpy(), kr[:, :top].cpu().numpy()
+    qr, kr = t[0] + t[1], t[2] + t[3]
+    sst = (s + 3) // 4 * 4
+    ss = ws[4 * one * 2:4 * one * 2 + nh * L * sst * 4].view(torch.float32).reshape(nh, L, sst).double()
+    return qr[:, ridx].cpu().numpy(), kr[:, :top].cpu().numpy(), ss[:, ridx, :s].cpu().numpy()

@@ -154,8 +154,12 @@ def test_rope_decode_validates_before_launch(lib):
 
 def test_rope_prefills_validate_before_launch(lib):
     f = 1 << 20  # never dereferenced: validation fails first
-    need = lib.swa_sink_prefill_rope_workspace_size(1, 2, 300, 128)
-    assert need == 6 * 2 * 300 * 128 * 2  # rotated q, sink-rotated q and rotated k, each as a (hi, lo) pair
+    need = lib.swa_sink_prefill_rope_workspace_size(1, 2, 300, 128, 4)
+    # rotated q and k as (hi, lo) bf16 pairs, the sink scores (fp32, 4 per row) and the rotated sink keys (fp32)
+    assert need == 4 * (2 * 300 * 128 * 2) + 2 * 300 * 4 * 4 + 2 * 4 * 128 * 4
+    assert lib.swa_sink_prefill_rope_workspace_size(1, 2, 300, 128, 5) == 4 * (2 * 300 * 128 * 2) + 2 * 300 * 8 * 4 + 2 * 5 * 128 * 4
+    assert lib.swa_sink_prefill_rope_workspace_size(1, 2, 300, 128, 129) == 0
+    assert lib.swa_sink_prefill_rope_workspace_size(1, 2, 300, 64, 4) == 0
     ok = [f, f, f, f, None, 1, 2, 300, 128, 64, 4, 0.1, 10000.0, f << 8, need, swa.SWA_BF16, None]
     bad = list(ok)
     bad[15] = swa.SWA_F32  # the RoPE prefill runs on the tensor cores only
@@ -170,8 +174,9 @@ def test_rope_prefills_validate_before_launch(lib):
     bad[14] = need - 1
     assert lib.swa_sink_prefill_rope(*bad) == swa.SWA_ERR_INVALID
     # chunked: chunks shorter than the sinks are refused, and the workspace adds a rotated-key cache
-    cneed = lib.swa_sink_prefill_chunked_rope_workspace_size(1, 2, 300, 128, 64)
-    assert cneed == need + 2 * 2 * 64 * 128 * 2  # + the rotated-key cache (hi, lo)
+    cneed = lib.swa_sink_prefill_chunked_rope_workspace_size(1, 2, 300, 128, 64, 8)
+    # + the rotated-key cache (hi, lo)
+    assert cneed == lib.swa_sink_prefill_rope_workspace_size(1, 2, 300, 128, 8) + 2 * 2 * 64 * 128 * 2
     cok = [f, f, f, f, None, f, f, 1, 2, 300, 128, 64, 8, 0.1, 32, 10000.0, f << 8, cneed, swa.SWA_BF16, None]
     bad = list(cok)
     bad[14] = 4  # chunk < s

@@ -149,7 +149,7 @@ def test_full_size_prefill_rope_sampled_rows():
     wl = swa_inputs.WORKLOADS["prefill_llama7b_L8192_w1024_s4"]
     q, k, v = swa_inputs.workload_inputs(wl, "cuda")
     lse = torch.empty((wl.B, wl.H, wl.L), dtype=torch.float32, device="cuda")
-    ws = torch.empty(swa.lib().swa_sink_prefill_rope_workspace_size(wl.B, wl.H, wl.L, wl.d), dtype=torch.uint8,
+    ws = torch.empty(swa.lib().swa_sink_prefill_rope_workspace_size(wl.B, wl.H, wl.L, wl.d, wl.s), dtype=torch.uint8,
                      device="cuda")
     o = swa.swa_sink_prefill_rope(q, k, v, wl.w, wl.s, lse=lse, workspace=ws)
     assert swa.swa_device_status() == swa.SWA_OK, swa.last_error()
@@ -163,7 +163,7 @@ def test_full_size_prefill_rope_sampled_rows():
     check_rope_prefill("rope prefill llama7b sampled rows",
                        o[:, :, rows].reshape(nh, len(rows), d).cpu().double().numpy(),
                        lse[:, :, rows].reshape(nh, len(rows)).cpu().double().numpy(),
-                       rope_workspace_operands(ws, wl.B, wl.H, wl.L, d, rows), qf, kf, vf, rows, wl.w, wl.s,
+                       rope_workspace_operands(ws, wl.B, wl.H, wl.L, d, wl.s, rows), qf, kf, vf, rows, wl.w, wl.s,
                        wl.scale, 10000.0, o_ref.reshape(nh, len(rows), d), l_ref.reshape(nh, len(rows)))
 
 
@@ -177,7 +177,7 @@ def test_full_size_chunked_prefill_rope_sampled_rows():
     kc = torch.zeros((wl.B, wl.H, wl.w, wl.d), dtype=torch.bfloat16, device="cuda")
     vc = torch.zeros_like(kc)
     lse = torch.empty((wl.B, wl.H, wl.L), dtype=torch.float32, device="cuda")
-    ws = torch.empty(swa.lib().swa_sink_prefill_chunked_rope_workspace_size(wl.B, wl.H, wl.L, wl.d, wl.w),
+    ws = torch.empty(swa.lib().swa_sink_prefill_chunked_rope_workspace_size(wl.B, wl.H, wl.L, wl.d, wl.w, wl.s),
                      dtype=torch.uint8, device="cuda")
     o = swa.swa_sink_prefill_chunked_rope(q, k, v, wl.w, wl.s, wl.chunk, kc, vc, lse=lse, workspace=ws)
     assert swa.swa_device_status() == swa.SWA_OK, swa.last_error()
@@ -190,7 +190,7 @@ def test_full_size_chunked_prefill_rope_sampled_rows():
     o_ref, l_ref = oracle.prefill_rope(qc, kc_, vc_, wl.w, wl.s, wl.scale, rows=rows)
     nh, d = wl.B * wl.H, wl.d
     qf, kf, vf = (x.double().numpy().reshape(nh, top, d) for x in (qc, kc_, vc_))
-    ops = rope_workspace_operands(ws, wl.B, wl.H, wl.L, d, rows)
+    ops = rope_workspace_operands(ws, wl.B, wl.H, wl.L, d, wl.s, rows)
     check_rope_prefill("rope chunked L131072 sampled rows",
                        o[:, :, rows].reshape(nh, len(rows), d).cpu().double().numpy(),
                        lse[:, :, rows].reshape(nh, len(rows)).cpu().double().numpy(), ops, qf, kf, vf, rows, wl.w,

@@ -1,9 +1,10 @@
 """GPU parity of the prefill with RoPE at the positions inside the cache (swa_sink_prefill_rope) against
 the oracle's definition (row t = the streaming decode at step t over unrotated keys), element by element.
 
-The rotation pass writes every rotated operand as a bf16 (hi, lo) pair and the kernel forms each score from
-three tensor-core products (hi hi + hi lo + lo hi), so the scores carry the error of fp32 operands and the
-results meet the same tolerances as every other path (gpu_common.check_rope_prefill): the rotated operands
+The rotation pass writes the rotated q and k as bf16 (hi, lo) pairs, from which the kernel forms each window
+score with three tensor-core products (hi hi + hi lo + lo hi), and the sink scores (the query rotated at
+min(t, w - 1)) as fp32 dot products; so every score carries the error of fp32 operands and the results meet the
+same tolerances as every other path (gpu_common.check_rope_prefill): the rotated operands and sink scores
 against the oracle's fp64 rotation, and the output and log-sum-exp against the oracle's exact definition.
 """
 import math
@@ -33,7 +34,7 @@ def test_rope_prefill_every_row(B, H, L, w, s, base):
     d = 128
     q, k, v = swa_inputs.prefill_inputs(B, H, L, d, 900 + L + s, torch.bfloat16, "cpu", sink_boost=True)
     lse = torch.empty((B, H, L), dtype=torch.float32, device="cuda")
-    ws = torch.empty(swa.lib().swa_sink_prefill_rope_workspace_size(B, H, L, d), dtype=torch.uint8, device="cuda")
+    ws = torch.empty(swa.lib().swa_sink_prefill_rope_workspace_size(B, H, L, d, s), dtype=torch.uint8, device="cuda")
     o = swa.swa_sink_prefill_rope(q.cuda(), k.cuda(), v.cuda(), w, s, rope_base=base, lse=lse, workspace=ws)
     assert swa.swa_device_status() == swa.SWA_OK, swa.last_error()
     scale = 1.0 / math.sqrt(d)
@@ -42,7 +43,7 @@ def test_rope_prefill_every_row(B, H, L, w, s, base):
     rows = list(range(L))
     qf, kf, vf = (x.double().numpy().reshape(nh, L, d) for x in (q, k, v))
     check_rope_prefill(f"rope prefill {B, H, L, w, s}", o.cpu().double().numpy().reshape(nh, L, d),
-                       lse.cpu().double().numpy().reshape(nh, L), rope_workspace_operands(ws, B, H, L, d, rows),
+                       lse.cpu().double().numpy().reshape(nh, L), rope_workspace_operands(ws, B, H, L, d, s, rows),
                        qf, kf, vf, rows, w, s, scale, base, o_ref.reshape(nh, L, d), l_ref.reshape(nh, L))
 
 
@@ -67,8 +68,8 @@ def test_rope_prefill_row_equals_rope_decode_step():
 def test_rope_prefill_workspace_is_checked():
     swa = require_gpu()
     q = torch.zeros((1, 1, 300, 128), dtype=torch.bfloat16, device="cuda")
-    need = swa.lib().swa_sink_prefill_rope_workspace_size(1, 1, 300, 128)
-    assert need == 6 * 300 * 128 * 2
+    need = swa.lib().swa_sink_prefill_rope_workspace_size(1, 1, 300, 128, 4)
+    assert need == 4 * 300 * 128 * 2 + 300 * 4 * 4 + 4 * 128 * 4
     ws = torch.empty(need - 256, dtype=torch.uint8, device="cuda")
     with pytest.raises(swa.SwaError):
         swa.swa_sink_prefill_rope(q, q, q, 64, 4, workspace=ws)
@@ -91,7 +92,7 @@ def test_rope_chunked_prefill_every_row(B, H, L, w, s, C):
     kc = torch.full((B, H, w, d), float("nan"), dtype=torch.bfloat16, device="cuda")
     vc = torch.full_like(kc, float("nan"))
     lse = torch.empty((B, H, L), dtype=torch.float32, device="cuda")
-    ws = torch.empty(swa.lib().swa_sink_prefill_chunked_rope_workspace_size(B, H, L, d, w), dtype=torch.uint8,
+    ws = torch.empty(swa.lib().swa_sink_prefill_chunked_rope_workspace_size(B, H, L, d, w, s), dtype=torch.uint8,
                      device="cuda")
     o = swa.swa_sink_prefill_chunked_rope(q.cuda(), k.cuda(), v.cuda(), w, s, C, kc, vc, lse=lse, workspace=ws)
     assert swa.swa_device_status() == swa.SWA_OK, swa.last_error()
@@ -101,7 +102,7 @@ def test_rope_chunked_prefill_every_row(B, H, L, w, s, C):
     rows = list(range(L))
     qf, kf, vf = (x.double().numpy().reshape(nh, L, d) for x in (q, k, v))
     check_rope_prefill(f"rope chunked {B, H, L, w, s, C}", o.cpu().double().numpy().reshape(nh, L, d),
-                       lse.cpu().double().numpy().reshape(nh, L), rope_workspace_operands(ws, B, H, L, d, rows),
+                       lse.cpu().double().numpy().reshape(nh, L), rope_workspace_operands(ws, B, H, L, d, s, rows),
                        qf, kf, vf, rows, w, s, scale, 10000.0, o_ref.reshape(nh, L, d), l_ref.reshape(nh, L))
     kc2 = torch.full_like(kc, float("nan"))
     vc2 = torch.full_like(vc, float("nan"))
