@@ -154,24 +154,42 @@ __global__ void __launch_bounds__(256) rope_prep_kernel(const uint2 *__restrict_
             if (t >= w - 1) rotate(qa, qb, sw, cw, x, y);
         }
         if (out.s > 0) {
-            // the query against each rotated sink key: a dot product over the 16 lanes of the row
+            // the query against each rotated sink key: dot products over the 16 lanes of the row, four sinks at a
+            // time, reduced by halving the four values across the lanes (5 shuffles for 4 sums): after the steps
+            // over lane bits 3 and 2 each lane keeps the partial of sink 2 b3 + b2, and after bits 1 and 0 lanes
+            // 0, 4, 8, 12 hold the sums of sinks 0, 1, 2, 3
             const float4 *ksr = out.ks + (valid ? row / L : 0) * out.s * 32;
-            for (int i = 0; i < out.s; ++i) {
-                float part = 0.f;
-                if (valid) {
-                    const float4 a = ksr[i * 32 + sub], b = ksr[i * 32 + 16 + sub];
-                    part = x[0] * a.x;
-                    part = fmaf(x[1], a.y, part);
-                    part = fmaf(x[2], a.z, part);
-                    part = fmaf(x[3], a.w, part);
-                    part = fmaf(y[0], b.x, part);
-                    part = fmaf(y[1], b.y, part);
-                    part = fmaf(y[2], b.z, part);
-                    part = fmaf(y[3], b.w, part);
-                }
+            for (int i0 = 0; i0 < out.s; i0 += 4) {
+                float p[4];
 #pragma unroll
-                for (int o = kRopeLanes / 2; o >= 1; o >>= 1) part += __shfl_xor_sync(0xFFFFFFFFu, part, o, kRopeLanes);
-                if (valid && sub == 0) out.ssink[row * out.sstride + i] = part;
+                for (int u = 0; u < 4; ++u) {
+                    p[u] = 0.f;
+                    if (valid && i0 + u < out.s) {
+                        const float4 a = ksr[(i0 + u) * 32 + sub], b = ksr[(i0 + u) * 32 + 16 + sub];
+                        float part = x[0] * a.x;
+                        part = fmaf(x[1], a.y, part);
+                        part = fmaf(x[2], a.z, part);
+                        part = fmaf(x[3], a.w, part);
+                        part = fmaf(y[0], b.x, part);
+                        part = fmaf(y[1], b.y, part);
+                        part = fmaf(y[2], b.z, part);
+                        part = fmaf(y[3], b.w, part);
+                        p[u] = part;
+                    }
+                }
+                // lane bit 3: the lower half keeps sinks 0, 1, the upper half sinks 2, 3
+                const bool hi3 = (sub & 8) != 0;
+                const float s0 = __shfl_xor_sync(0xFFFFFFFFu, hi3 ? p[0] : p[2], 8, kRopeLanes);
+                const float s1 = __shfl_xor_sync(0xFFFFFFFFu, hi3 ? p[1] : p[3], 8, kRopeLanes);
+                const float q0 = (hi3 ? p[2] : p[0]) + s0;
+                const float q1 = (hi3 ? p[3] : p[1]) + s1;
+                // lane bit 2: keep the first or the second of the two
+                const bool hi2 = (sub & 4) != 0;
+                float v = (hi2 ? q1 : q0) + __shfl_xor_sync(0xFFFFFFFFu, hi2 ? q0 : q1, 4, kRopeLanes);
+                v += __shfl_xor_sync(0xFFFFFFFFu, v, 2, kRopeLanes);
+                v += __shfl_xor_sync(0xFFFFFFFFu, v, 1, kRopeLanes);
+                const int i = i0 + (sub >> 2);
+                if (valid && (sub & 3) == 0 && i < out.s) out.ssink[row * out.sstride + i] = v;
             }
         }
     }
