@@ -40,8 +40,10 @@
 // product (the only one that can still be in flight).
 //
 // Precision mode (HILO, used by the RoPE prefill): q and k arrive as a bf16 pair (hi, lo) with
-// hi + lo the rotated fp32 value, and every S = hi_q hi_k + hi_q lo_k + lo_q hi_k (three products
-// accumulated in fp32), so the scores carry the error of fp32 operands, not of bf16 ones.
+// hi + lo the rotated fp32 value, and every window score S = hi_q hi_k + hi_q lo_k + lo_q hi_k (three
+// products accumulated in fp32), so the scores carry the error of fp32 operands, not of bf16 ones.  The
+// sink scores, whose query rotation differs, come ready-made from the rotation pass (fp32): the sink
+// sub-tiles take no K load and no QK product, only their PV product, and Q is loaded once per item.
 //
 // Key tiles.  For the query rows [q0, q1] of a CTA the key positions needed are the sinks [0, min(s, blo)) and
 // the band [blo, q1] with blo = max(0, q0 - m + 1).  Positions >= pos0 are rows of this call's k/v;
