@@ -273,12 +273,16 @@ __global__ void __launch_bounds__(256) scan_kernel(uint32_t *dmat, float *zst, i
 }
 
 // ---- 3. linear branch + combination ----------------------------------------------------------------------
-// grid (query tiles, BH), 256 threads; thread r (mod 128) owns query row a + r (TMEM lane r) and the column half
-// h = warp / 4 of it.  All loads are issued at once: the Q tile, phi(K)^T and V of the <= 2 key chunks from 128 J, and the
-// prefix state P_J (bf16, from the scan).  TMEM: f(Q), then the scores of chunk J, columns [0, 128); the scores
-// of chunk J + 1, [128, 256); the numerator, [256, 384).  The masked scores go back over their own TMEM columns
-// as bf16 pairs, the A operand of their product with V.  o holds the SWA prefill's output on entry and the hybrid
-// output on exit; lse is the SWA prefill's.
+// Persistent: one CTA per SM walks the work items (query tile, bh) with item = tile * BH + bh, from blockIdx.x
+// in steps of gridDim.x, skipping the tiles whose rows have no key outside their window yet.  256 threads;
+// thread r (mod 128) owns query row a + r (TMEM lane r) and the column half h = warp / 4 of it.  Per item: the Q
+// tile, phi(K)^T and V of the <= 2 key chunks from 128 J, and the prefix state P_J (bf16, from the scan); W2 is
+// loaded once per CTA.  The next item's Q, phi(K) and P_J are loaded as soon as this item's products that read
+// them are done (before its masking, PV products and combination), and its V tiles once this item's PV
+// products are: the loads overlap the rest of the item.  TMEM: f(Q), then the scores of chunk J, columns
+// [0, 128); the scores of chunk J + 1, [128, 256); the numerator, [256, 384).  The masked scores go back over
+// their own TMEM columns as bf16 pairs, the A operand of their product with V.  o holds the SWA prefill's output
+// on entry and the hybrid output on exit; lse is the SWA prefill's.
 // A from TMEM: keys 0..63 as bf16 pairs in columns [0, 32), keys 64..127 in columns [64, 96) (each key half is
 // written by the threads that read that half of the scores).
 __device__ __forceinline__ void mma_tv(uint32_t d, uint32_t a_tmem, uint32_t b, bool acc) {
@@ -288,6 +292,29 @@ __device__ __forceinline__ void mma_tv(uint32_t d, uint32_t a_tmem, uint32_t b, 
                 (acc || kk) ? 1u : 0u);
 }
 
+// The shape of one work item of the linear pass.
+struct LinItem {
+    int64_t a, last, J;  // first row, last row, first key chunk
+    int bh;
+    bool two, has_p;     // the rows reach into chunk J + 1; a prefix state before chunk J
+};
+__device__ __forceinline__ bool lin_item(int item, int BH, int64_t L, int m, int s, LinItem &it) {
+    it.a = static_cast<int64_t>(item / BH) * C;
+    it.bh = item % BH;
+    it.last = (it.a + C < L ? it.a + C : L) - 1;
+    if (it.last - m < s) return false;  // no row of the tile has a key outside its window yet
+    it.J = it.a - m + 1 > 0 ? (it.a - m + 1) / C : 0;
+    it.two = it.J * C + C <= it.last - m;
+    it.has_p = it.J > 0;
+    return true;
+}
+// The next item of this CTA with work from item on (n_items if none).
+__device__ __forceinline__ int lin_next(int item, int n_items, int BH, int64_t L, int m, int s, LinItem &it) {
+    for (; item < n_items; item += static_cast<int>(gridDim.x))
+        if (lin_item(item, BH, L, m, s, it)) return item;
+    return n_items;
+}
+
 __global__ void __launch_bounds__(256, 1) linear_kernel(const __grid_constant__ CUtensorMap mq,
                                                         const __grid_constant__ CUtensorMap mv,
                                                         const __grid_constant__ CUtensorMap mpk,
@@ -295,27 +322,27 @@ __global__ void __launch_bounds__(256, 1) linear_kernel(const __grid_constant__ 
                                                         const __grid_constant__ CUtensorMap mw2,
                                                         const float *__restrict__ zst, __nv_bfloat16 *o,
                                                         const float *__restrict__ lse, int64_t L, int m, int s,
-                                                        int nchunks, DeviceStatus *status) {
-    const int64_t a = static_cast<int64_t>(blockIdx.x) * C;
-    const int bh = blockIdx.y, r = threadIdx.x & (C - 1), hh = threadIdx.x >> 7;
-    const int64_t last = (a + C < L ? a + C : L) - 1;
-    if (last - m < s) return;  // no row of the tile has a key outside its window yet
+                                                        int nchunks, int BH, DeviceStatus *status) {
+    const int r = threadIdx.x & (C - 1), hh = threadIdx.x >> 7;
+    const int n_items = nchunks * BH;
+    LinItem cur;
+    int item = lin_next(static_cast<int>(blockIdx.x), n_items, BH, L, m, s, cur);
+    if (item >= n_items) return;  // uniform: no work for this CTA
     extern __shared__ uint8_t smem_raw[];
     uint8_t *sm = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     uint8_t *Tq = sm, *Tw = sm + TILE, *Tk0 = sm + 2 * TILE, *Tk1 = sm + 3 * TILE, *Tv0 = sm + 4 * TILE,
             *Tv1 = sm + 5 * TILE, *Tp = sm + 6 * TILE;
     Ctl *ctl = reinterpret_cast<Ctl *>(sm + 7 * TILE);
-    uint64_t *kv_bar = reinterpret_cast<uint64_t *>(sm + 7 * TILE + 64);
-    const int64_t J = a - m + 1 > 0 ? (a - m + 1) / C : 0;
-    const bool two = J * C + C <= last - m;  // the tile's rows reach into chunk J + 1
-    const bool has_p = J > 0;
+    uint64_t *k_bar = reinterpret_cast<uint64_t *>(sm + 7 * TILE + 64);  // phi(K) tiles and P_J of an item
+    uint64_t *v_bar = k_bar + 1;                                           // V tiles of an item
     float *dx = reinterpret_cast<float *>(sm + 7 * TILE + 128);  // [2][128] the halves' parts of the denominators
     const bool t0 = threadIdx.x == 0;
     if (t0) {
         ctl->abort_flag = 0;
         mbar_init(&ctl->load_bar, 1);
         mbar_init(&ctl->mma_bar, 1);
-        mbar_init(kv_bar, 1);
+        mbar_init(k_bar, 1);
+        mbar_init(v_bar, 1);
         mbar_init_fence();
     }
     if (threadIdx.x < 32) {
@@ -323,120 +350,148 @@ __global__ void __launch_bounds__(256, 1) linear_kernel(const __grid_constant__ 
         tmem_relinquish();
     }
     __syncthreads();
-    if (t0) {  // every load at once
-        mbar_arrive_expect_tx(&ctl->load_bar, 2 * TILE);
-        load_tile(Tq, &mq, &ctl->load_bar, static_cast<int>(a), bh);
-        load_tile(Tw, &mw2, &ctl->load_bar, 0, 0);
-        mbar_arrive_expect_tx(kv_bar, (2 + (two ? 2 : 0) + (has_p ? 1 : 0)) * TILE);
-        load_tile(Tk0, &mpk, kv_bar, static_cast<int>(J * C), bh);
-        load_tile(Tv0, &mv, kv_bar, static_cast<int>(J * C), bh);
-        if (two) {
-            load_tile(Tk1, &mpk, kv_bar, static_cast<int>(J * C + C), bh);
-            load_tile(Tv1, &mv, kv_bar, static_cast<int>(J * C + C), bh);
-        }
-        if (has_p) load_tile(Tp, &mpj, kv_bar, static_cast<int>(J * C), bh);
+    int lq = 0, lv = 0;  // thread 0: Q / phi(K) loads and V loads issued (the phase each barrier is in)
+    auto load_qk = [&](const LinItem &it, bool with_w2) {  // thread 0: Q (and W2), then phi(K) and P_J
+        ++lq;
+        mbar_arrive_expect_tx(&ctl->load_bar, (with_w2 ? 2 : 1) * TILE);
+        load_tile(Tq, &mq, &ctl->load_bar, static_cast<int>(it.a), it.bh);
+        if (with_w2) load_tile(Tw, &mw2, &ctl->load_bar, 0, 0);
+        mbar_arrive_expect_tx(k_bar, (1 + (it.two ? 1 : 0) + (it.has_p ? 1 : 0)) * TILE);
+        load_tile(Tk0, &mpk, k_bar, static_cast<int>(it.J * C), it.bh);
+        if (it.two) load_tile(Tk1, &mpk, k_bar, static_cast<int>(it.J * C + C), it.bh);
+        if (it.has_p) load_tile(Tp, &mpj, k_bar, static_cast<int>(it.J * C), it.bh);
+    };
+    auto load_v = [&](const LinItem &it) {  // thread 0: the V tiles
+        ++lv;
+        mbar_arrive_expect_tx(v_bar, (1 + (it.two ? 1 : 0)) * TILE);
+        load_tile(Tv0, &mv, v_bar, static_cast<int>(it.J * C), it.bh);
+        if (it.two) load_tile(Tv1, &mv, v_bar, static_cast<int>(it.J * C + C), it.bh);
+    };
+    if (t0) {
+        load_qk(cur, true);
+        load_v(cur);
     }
     operands_written();
     const uint32_t tmem = ctl->tmem;
     const uint32_t T_S0 = tmem, T_S1 = tmem + 128, T_NUM = tmem + 256;
     const WaitCtl wc{smem_u32(&ctl->abort_flag), kWaitTimeoutUs, status};
-    const float *zJ = zst + (static_cast<int64_t>(bh) * nchunks + J) * D;
-    if (t0) {
-        if (mbar_wait(&ctl->load_bar, 0, wc, 43)) {
-            tc_fence_after();
-            mma_abt(T_S0, smem_u32(Tq), smem_u32(Tw), false);  // f(Q): [row][feature]
-        } else {
-            mbar_wait_drain(&ctl->load_bar, 0);
-        }
-        umma_commit(&ctl->mma_bar);
-    }
-    bool fine = wait_mma(ctl, 0, wc, 44);
-    float den = 0.f;
-    if (fine) {  // phi(Q) (bf16, over the Q tile) and phi(q) z_J (fp32), this thread's half of the features
-        for (int c0 = 64 * hh; c0 < 64 * hh + 64; c0 += 32) {
-            float x[32];
-            tmem_ld32(lane_addr(T_S0, c0), x);
-#pragma unroll
-            for (int i = 0; i < 32; ++i) {
-                x[i] = exp2f(x[i] * LOG2E);
-                den = fmaf(x[i], zJ[c0 + i], den);
+    int mph = 0;  // mma_bar phases waited so far
+    bool fine = true;
+    for (int n = 0; fine && item < n_items; ++n) {
+        LinItem nxt;
+        const int next = lin_next(item + static_cast<int>(gridDim.x), n_items, BH, L, m, s, nxt);
+        const float *zJ = zst + (static_cast<int64_t>(cur.bh) * nchunks + cur.J) * D;
+        if (t0) {
+            if (mbar_wait(&ctl->load_bar, n & 1, wc, 43)) {
+                tc_fence_after();
+                mma_abt(T_S0, smem_u32(Tq), smem_u32(Tw), false);  // f(Q): [row][feature]
+            } else {
+                mbar_wait_drain(&ctl->load_bar, n & 1);
             }
-            st_row32(smem_u32(Tq), r, c0, x);
+            umma_commit(&ctl->mma_bar);
         }
-    }
-    operands_written();
-    if (t0) {
-        if (fine && mbar_wait(kv_bar, 0, wc, 45)) {
-            tc_fence_after();
-            mma_ab(T_S0, smem_u32(Tq), smem_u32(Tk0), false);                // phi(Q) phi(K_J)^T: [row][key]
-            if (two) mma_ab(T_S1, smem_u32(Tq), smem_u32(Tk1), false);       // chunk J + 1
-            if (has_p) mma_ab(T_NUM, smem_u32(Tq), smem_u32(Tp), false);     // phi(Q) P_J
-        } else {
-            mbar_wait_drain(kv_bar, 0);
-        }
-        umma_commit(&ctl->mma_bar);
-    }
-    fine = wait_mma(ctl, 1, wc, 46) && fine;
-    const int64_t t = a + r;  // this thread's query row
-    if (fine) {  // keep s <= key <= t - m; fp32 row sums into the denominator, bf16 pairs back into TMEM
-        for (int u = 0; u < (two ? 2 : 1); ++u) {
-            const uint32_t ts = u ? T_S1 : T_S0;
-            const int64_t kt = J * C + u * C;
-            {  // this thread's half of the keys; its bf16 pairs go to the first 32 of its own 64 columns
-                float x[64];
-                tmem_ld64(lane_addr(ts, 64 * hh), x);
-                uint32_t pk[32];
+        fine = wait_mma(ctl, mph++, wc, 44);
+        float den = 0.f;
+        if (fine) {  // phi(Q) (bf16, over the Q tile) and phi(q) z_J (fp32), this thread's half of the features
+            for (int c0 = 64 * hh; c0 < 64 * hh + 64; c0 += 32) {
+                float x[32];
+                tmem_ld32(lane_addr(T_S0, c0), x);
 #pragma unroll
                 for (int i = 0; i < 32; ++i) {
-                    const int64_t k0 = kt + 64 * hh + 2 * i;
-                    const float p0 = (k0 >= s && k0 <= t - m) ? x[2 * i] : 0.f;
-                    const float p1 = (k0 + 1 >= s && k0 + 1 <= t - m) ? x[2 * i + 1] : 0.f;
-                    den += p0 + p1;
-                    pk[i] = pack_bf16x2(p0, p1);
+                    x[i] = exp2f(x[i] * LOG2E);
+                    den = fmaf(x[i], zJ[c0 + i], den);
                 }
-                tmem_st32u_nowait(lane_addr(ts, 64 * hh), pk);
+                st_row32(smem_u32(Tq), r, c0, x);
             }
         }
-        tmem_wait_st();
-    }
-    dx[hh * C + r] = den;  // this half's part of the row's denominator
-    tc_fence_before();
-    __syncthreads();
-    tc_fence_after();
-    den += dx[(hh ^ 1) * C + r];
-    if (t0) {
+        operands_written();
+        if (t0) {
+            if (fine && mbar_wait(k_bar, n & 1, wc, 45)) {
+                tc_fence_after();
+                mma_ab(T_S0, smem_u32(Tq), smem_u32(Tk0), false);                  // phi(Q) phi(K_J)^T: [row][key]
+                if (cur.two) mma_ab(T_S1, smem_u32(Tq), smem_u32(Tk1), false);     // chunk J + 1
+                if (cur.has_p) mma_ab(T_NUM, smem_u32(Tq), smem_u32(Tp), false);   // phi(Q) P_J
+            } else {
+                mbar_wait_drain(k_bar, n & 1);
+            }
+            umma_commit(&ctl->mma_bar);
+        }
+        fine = wait_mma(ctl, mph++, wc, 46) && fine;
+        // Q, phi(K) and P_J are read: the next item's go in now
+        if (t0 && fine && next < n_items) load_qk(nxt, false);
+        const int64_t t = cur.a + r;  // this thread's query row
+        if (fine) {  // keep s <= key <= t - m; fp32 row sums into the denominator, bf16 pairs back into TMEM
+            for (int u = 0; u < (cur.two ? 2 : 1); ++u) {
+                const uint32_t ts = u ? T_S1 : T_S0;
+                const int64_t kt = cur.J * C + u * C;
+                {  // this thread's half of the keys; its bf16 pairs go to the first 32 of its own 64 columns
+                    float x[64];
+                    tmem_ld64(lane_addr(ts, 64 * hh), x);
+                    uint32_t pk[32];
+#pragma unroll
+                    for (int i = 0; i < 32; ++i) {
+                        const int64_t k0 = kt + 64 * hh + 2 * i;
+                        const float p0 = (k0 >= s && k0 <= t - m) ? x[2 * i] : 0.f;
+                        const float p1 = (k0 + 1 >= s && k0 + 1 <= t - m) ? x[2 * i + 1] : 0.f;
+                        den += p0 + p1;
+                        pk[i] = pack_bf16x2(p0, p1);
+                    }
+                    tmem_st32u_nowait(lane_addr(ts, 64 * hh), pk);
+                }
+            }
+            tmem_wait_st();
+        }
+        dx[hh * C + r] = den;  // this half's part of the row's denominator
+        tc_fence_before();
+        __syncthreads();
+        tc_fence_after();
+        den += dx[(hh ^ 1) * C + r];
+        if (t0) {
+            if (fine && mbar_wait(v_bar, n & 1, wc, 47)) {
+                tc_fence_after();
+                mma_tv(T_NUM, T_S0, smem_u32(Tv0), cur.has_p);  // masked scores of chunk J x V_J
+                if (cur.two) mma_tv(T_NUM, T_S1, smem_u32(Tv1), true);
+            } else {
+                mbar_wait_drain(v_bar, n & 1);
+            }
+            umma_commit(&ctl->mma_bar);
+        }
+        fine = wait_mma(ctl, mph++, wc, 48) && fine;
+        // the V tiles are read: the next item's go in now
+        if (t0 && fine && next < n_items) load_v(nxt);
         if (fine) {
-            mma_tv(T_NUM, T_S0, smem_u32(Tv0), has_p);  // masked scores of chunk J x V_J
-            if (two) mma_tv(T_NUM, T_S1, smem_u32(Tv1), true);
-        }
-        umma_commit(&ctl->mma_bar);
-    }
-    fine = wait_mma(ctl, 2, wc, 47) && fine;
-    if (fine) {
-        // tcgen05.ld is warp-collective: every thread loads, only rows t < L read o', lse and write o
-        const bool live = t < L;
-        const int64_t row = static_cast<int64_t>(bh) * L + (live ? t : 0);
-        const float e = live ? exp2f(-lse[row] * LOG2E) : 0.f;  // e^{-lse}
-        const float inv = 1.f / fmaf(den, e, 1.f);
-        __nv_bfloat16 *orow = o + row * D;
-        for (int c0 = 64 * hh; c0 < 64 * hh + 64; c0 += 32) {
-            float x[32];
-            tmem_ld32(lane_addr(T_NUM, c0), x);
-            if (!live) continue;
-            uint4 *p = reinterpret_cast<uint4 *>(orow + c0);
+            // tcgen05.ld is warp-collective: every thread loads, only rows t < L read o', lse and write o
+            const bool live = t < L;
+            const int64_t row = static_cast<int64_t>(cur.bh) * L + (live ? t : 0);
+            const float e = live ? exp2f(-lse[row] * LOG2E) : 0.f;  // e^{-lse}
+            const float inv = 1.f / fmaf(den, e, 1.f);
+            __nv_bfloat16 *orow = o + row * D;
+            for (int c0 = 64 * hh; c0 < 64 * hh + 64; c0 += 32) {
+                float x[32];
+                tmem_ld32(lane_addr(T_NUM, c0), x);
+                if (!live) continue;
+                uint4 *p = reinterpret_cast<uint4 *>(orow + c0);
 #pragma unroll
-            for (int g = 0; g < 4; ++g) {
-                const uint4 ov = p[g];
-                const uint32_t w4[4] = {ov.x, ov.y, ov.z, ov.w};
-                uint32_t res[4];
+                for (int g = 0; g < 4; ++g) {
+                    const uint4 ov = p[g];
+                    const uint32_t w4[4] = {ov.x, ov.y, ov.z, ov.w};
+                    uint32_t res[4];
 #pragma unroll
-                for (int h = 0; h < 4; ++h) {
-                    const float lo = __uint_as_float(w4[h] << 16), hi = __uint_as_float(w4[h] & 0xFFFF0000u);
-                    res[h] = pack_bf16x2(fmaf(x[8 * g + 2 * h], e, lo) * inv, fmaf(x[8 * g + 2 * h + 1], e, hi) * inv);
+                    for (int h = 0; h < 4; ++h) {
+                        const float lo = __uint_as_float(w4[h] << 16), hi = __uint_as_float(w4[h] & 0xFFFF0000u);
+                        res[h] = pack_bf16x2(fmaf(x[8 * g + 2 * h], e, lo) * inv, fmaf(x[8 * g + 2 * h + 1], e, hi) * inv);
+                    }
+                    p[g] = make_uint4(res[0], res[1], res[2], res[3]);
                 }
-                p[g] = make_uint4(res[0], res[1], res[2], res[3]);
             }
         }
+        item = next;
+        cur = nxt;
+    }
+    if (t0 && !fine) {  // no copy may still be landing when the CTA exits: the last loads issued on each barrier
+        mbar_wait_drain(&ctl->load_bar, (lq - 1) & 1);
+        mbar_wait_drain(k_bar, (lq - 1) & 1);
+        mbar_wait_drain(v_bar, (lv - 1) & 1);
     }
     tc_fence_before();
     __syncthreads();
@@ -622,8 +677,14 @@ extern "C" int swa_hybrid_prefill(const void *q, const void *k, const void *v, c
     const int64_t npairs = static_cast<int64_t>(BH) * hy::D * hy::D / 2, nz = static_cast<int64_t>(BH) * hy::D;
     hy::scan_kernel<<<static_cast<unsigned>((npairs + nz + 255) / 256), 256, 0, st>>>(
         reinterpret_cast<uint32_t *>(dmat), zst, nch, npairs, nz);
-    hy::linear_kernel<<<dim3(nch, BH), 256, smem_b, st>>>(mq, mv, mpk, mpj, mw2, zst, static_cast<__nv_bfloat16 *>(o),
-                                                          lse, L, m, s, nch, ds);
+    int sms = 0, dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess ||
+        sms <= 0)
+        return fail(SWA_ERR_CUDA, "cannot read the multiprocessor count");
+    const int n_lin = nch * BH;  // persistent: one CTA per SM over the (query tile, bh) items
+    hy::linear_kernel<<<n_lin < sms ? n_lin : sms, 256, smem_b, st>>>(mq, mv, mpk, mpj, mw2, zst,
+                                                                      static_cast<__nv_bfloat16 *>(o), lse, L, m, s,
+                                                                      nch, BH, ds);
     if (state_s) {
         // the state after the last row (keys s .. L-1-m): the prefix of chunk jf plus its keys below L - m
         const int64_t jf = L - m > 0 ? (L - m) / hy::C : 0;
