@@ -428,9 +428,12 @@ int swa_prefill_tile_plan_dilated(int64_t L, int w, int s, int r, int cls, int64
                                   int max_tiles);
 /* The same for swa_sink_prefill_blocksparse (host only, no CUDA call): the key tiles of query pair `pair`
  * (rows 256*pair .. 256*pair + 255) for the pattern (globals, block, rand_blocks, r) of a sequence of L
- * positions.  For tile i, tiles[7i..7i+6] = {absolute position of column 0, last valid column, bit mask of
- * the query tiles that use it, and four 32-bit words whose bit c (of word c / 32) marks a column holding a
- * global token}.  Pattern arguments and errors as swa_sink_prefill_blocksparse. */
+ * positions.  For tile i, tiles[8i..8i+7] = {absolute position of column 0, last valid column, bit mask of
+ * the query tiles that use it, four 32-bit words whose bit c (of word c / 32) marks a column holding a global
+ * token, and -1 or, for a packed tile, the absolute position of column 64}.  A packed tile holds two runs of 64
+ * keys outside the sinks and the pair's band: columns 0..63 are positions first .. first + 63 and columns
+ * 64..127 positions second .. second + 63.  `tiles` holds 8 * max_tiles ints.  Pattern arguments and errors
+ * as swa_sink_prefill_blocksparse. */
 int swa_prefill_blocksparse_plan(int64_t L, int w, int s, const int32_t *globals, int n_globals, int block,
                                  const int32_t *rand_blocks, int r, int64_t pair, int *tiles, int max_tiles);
 

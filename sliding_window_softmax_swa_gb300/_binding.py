@@ -455,18 +455,19 @@ def prefill_tile_plan_dilated(L: int, w: int, s: int, r: int, cls: int, row_star
 
 def prefill_blocksparse_plan(L: int, w: int, s: int, globals_, block: int, rand_blocks, pair: int):
     """The key tiles of the block-sparse prefill for query pair ``pair`` (rows 256*pair ..): list of
-    (pbase, chi, used_by_mask, global-column mask as one 128-bit int)."""
+    (pbase, chi, used_by_mask, global-column mask as one 128-bit int, pbase1).  pbase1 is -1, or for a packed
+    tile the position of column 64 (columns 64..127 hold pbase1 .. pbase1 + 63)."""
     g, r, rb = _pattern(globals_, rand_blocks)
-    buf = (ctypes.c_int * (7 * 64))()
+    buf = (ctypes.c_int * (8 * 64))()
     n = lib().swa_prefill_blocksparse_plan(L, w, s, g.ctypes.data if g.size else None, g.size, block,
                                            rb.ctypes.data if r else None, r, pair, buf, 64)
     if n < 0:
         raise SwaError("swa_prefill_blocksparse_plan", n, last_error())
     out = []
     for i in range(min(n, 64)):
-        rec = buf[7 * i:7 * i + 7]
+        rec = buf[8 * i:8 * i + 8]
         gm = sum((rec[3 + k] & 0xFFFFFFFF) << (32 * k) for k in range(4))
-        out.append((rec[0], rec[1], rec[2], gm))
+        out.append((rec[0], rec[1], rec[2], gm, rec[7]))
     return out
 
 

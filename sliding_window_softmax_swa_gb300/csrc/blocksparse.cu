@@ -108,9 +108,11 @@ static int check_pattern(int64_t L, int w, int s, const int32_t *globals, int n_
     return SWA_OK;
 }
 
-// The tile lists of every query pair, built on the host: records of 12 bytes (row0, pbase, chi, flags) for
-// all pairs, then their 16-byte global-key column masks.
+// The tile lists of every query pair, built on the host: records of 16 bytes (row0, pbase, chi | flags, row1)
+// for all pairs, then their 16-byte global-key column masks.
 struct HostLists {
+    static constexpr size_t kRecord = 16;
+    static constexpr int kPacked = 8;  // flags bit: two 64-key blocks, columns 64..127 from row1
     std::vector<unsigned char> bytes;
     std::vector<int> count;
     size_t tiles_bytes = 0;
@@ -119,8 +121,8 @@ struct HostLists {
               int r) {
         const int64_t pairs = ceil_div(L, 256);
         const size_t list_bytes = blocksparse_tile_list_bytes(L);
-        tiles_bytes = list_bytes / (12 + 16) * 12;
-        per_pair = static_cast<int>(tiles_bytes / 12 / pairs);
+        tiles_bytes = list_bytes / (kRecord + 16) * kRecord;
+        per_pair = static_cast<int>(tiles_bytes / kRecord / pairs);
         bytes.assign(list_bytes, 0);
         count.assign(static_cast<size_t>(pairs), 0);
         return blocksparse_build_lists(L, w, s, globals, n_globals, block, rand_blocks, r, bytes.data(),
@@ -142,14 +144,17 @@ extern "C" int swa_prefill_blocksparse_plan(int64_t L, int w, int s, const int32
     const int n = hl.count[static_cast<size_t>(pair)];
     for (int i = 0; i < n && i < max_tiles; ++i) {
         const size_t idx = static_cast<size_t>(pair) * hl.per_pair + i;
-        int32_t rec[3];  // row0, pbase, chi (low half) | flags (high half)
-        std::memcpy(rec, hl.bytes.data() + idx * 12, 12);
+        int32_t rec[4];  // row0, pbase, chi (low half) | flags (high half), row1
+        std::memcpy(rec, hl.bytes.data() + idx * HostLists::kRecord, HostLists::kRecord);
         uint32_t gm[4];
         std::memcpy(gm, hl.bytes.data() + hl.tiles_bytes + idx * 16, 16);
-        tiles[7 * i + 0] = rec[1];
-        tiles[7 * i + 1] = static_cast<int16_t>(rec[2] & 0xFFFF);
-        tiles[7 * i + 2] = static_cast<int16_t>(static_cast<uint32_t>(rec[2]) >> 16) >> 1;
-        for (int k = 0; k < 4; ++k) tiles[7 * i + 3 + k] = static_cast<int>(gm[k]);
+        const int flags = static_cast<int16_t>(static_cast<uint32_t>(rec[2]) >> 16);
+        int *out = tiles + 8 * static_cast<int64_t>(i);
+        out[0] = rec[1];
+        out[1] = static_cast<int16_t>(rec[2] & 0xFFFF);
+        out[2] = (flags >> 1) & 3;
+        for (int k = 0; k < 4; ++k) out[3 + k] = static_cast<int>(gm[k]);
+        out[7] = (flags & HostLists::kPacked) ? rec[3] : -1;
     }
     return n;
 }

@@ -92,7 +92,8 @@ constexpr uint32_t OFF_V = OFF_K + NK * TILE_BYTES;
 constexpr uint32_t OFF_BAR = OFF_V + NV * TILE_BYTES;
 constexpr uint32_t OFF_MISC = OFF_BAR + 256;
 constexpr uint32_t OFF_TILES = OFF_MISC + 64;
-constexpr uint32_t OFF_GMASK = OFF_TILES + 2 * MAX_TILES * 12;  // two tile lists (current / next item)
+constexpr uint32_t TILE_RECORD = 16;                              // bytes of one tile record (struct Tile)
+constexpr uint32_t OFF_GMASK = OFF_TILES + 2 * MAX_TILES * TILE_RECORD;  // two tile lists (current / next item)
 constexpr uint32_t OFF_XCH = OFF_GMASK + 2 * MAX_TILES * 16;       // and their global-key columns (block-sparse)
 constexpr uint32_t SMEM_USED = OFF_XCH + 2 * 4 * BQ * 4;             // (max, sum) exchange of the two streams
 constexpr uint32_t SMEM_BYTES = SMEM_USED + 1024;  // slack to align the base to 1024 bytes
@@ -106,9 +107,12 @@ struct Tile {
     int row0;     // first source row (TMA row coordinate)
     int pbase;    // absolute position of column 0
     short chi;    // last valid column (columns past it belong to another tile or to nothing)
-    short flags;  // bit 0: source (0 = this call's k/v rows, 1 = rolling cache); bit 1 + x: needed by query tile x
+    short flags;  // bit 0: source (0 = this call's k/v rows, 1 = rolling cache); bit 1 + x: needed by query tile x;
+                  // bit 3: a packed tile of two 64-key blocks (block-sparse mode, rows = positions)
+    int row1;     // packed tile: first row (= position) of columns 64..127 (rows row0 .. row0 + 63 fill 0..63)
 };
-static_assert(sizeof(Tile) == 12, "tile record");
+static_assert(sizeof(Tile) == TILE_RECORD, "tile record");
+constexpr short kTilePacked = 8;
 
 // Block-sparse mode: per column of a key tile, whether it holds a global key (bit c of word c / 32).
 struct TileMask {
@@ -117,6 +121,7 @@ struct TileMask {
 
 struct Params {
     CUtensorMap tm_q, tm_k, tm_v, tm_kc, tm_vc, tm_o;  // tm_o: the rows of o, laid out as tm_q
+    CUtensorMap tm_k64, tm_v64;  // block-sparse mode: 64-row boxes of k / v, the halves of a packed tile
     // block-sparse mode: the host-built key-tile lists of every 256-row query pair (MAX_TILES entries per pair,
     // bs_count[pair] used), their global-key columns, and the random key blocks of each query block
     const Tile *bs_tiles;
@@ -152,6 +157,7 @@ __host__ __device__ int build_tiles(Tile *tl, int q0, int q1, int pos0, int s, i
                 tl[n].pbase = p;
                 tl[n].chi = static_cast<short>((pb - p < BN - 1) ? pb - p : BN - 1);
                 tl[n].flags = static_cast<short>(src);
+                tl[n].row1 = 0;
             }
             ++n;
         }
@@ -414,6 +420,12 @@ __global__ void __launch_bounds__(kThreads, 1) swa_prefill_tc_kernel(const __gri
                     if (DIL && !(T.flags & 1)) {  // band rows of the class: row0 is the group index
                         tma_load_4d(dst, mp, &full[st], 0, cls, T.row0, bh);
                         tma_load_4d(dst + HALF_BYTES, mp, &full[st], 64, cls, T.row0, bh);
+                    } else if (BS && (T.flags & kTilePacked)) {  // two 64-row blocks: rows 0..63 and 64..127
+                        const CUtensorMap *m64 = isk ? &P.tm_k64 : &P.tm_v64;
+                        tma_load_3d(dst, m64, &full[st], 0, T.row0, bh);
+                        tma_load_3d(dst + HALF_BYTES, m64, &full[st], 64, T.row0, bh);
+                        tma_load_3d(dst + 64 * 128, m64, &full[st], 0, T.row1, bh);
+                        tma_load_3d(dst + HALF_BYTES + 64 * 128, m64, &full[st], 64, T.row1, bh);
                     } else {
                         tma_load_3d(dst, mp, &full[st], 0, T.row0, bh);
                         tma_load_3d(dst + HALF_BYTES, mp, &full[st], 64, T.row0, bh);
@@ -478,7 +490,7 @@ __global__ void __launch_bounds__(kThreads, 1) swa_prefill_tc_kernel(const __gri
                         for (int i = 0; i < cnt; ++i) {
                             if (!(src[i].flags & bit)) continue;
                             tl[n] = src[i];
-                            tl[n].flags = static_cast<short>((src[i].flags & 1) | 2);
+                            tl[n].flags = static_cast<short>((src[i].flags & (1 | kTilePacked)) | 2);
                             gmask_s[b * MAX_TILES + n] = gsrc[i];
                             ++n;
                         }
@@ -645,17 +657,40 @@ __global__ void __launch_bounds__(kThreads, 1) swa_prefill_tc_kernel(const __gri
                 const int hc = min(static_cast<int>(T.chi), t - T.pbase);
                 const int b1 = min(hc, P.s - 1 - T.pbase);
                 const int a2 = max(0, t - P.m + 1 - T.pbase);
-                const bool full = (b1 >= BN - 1) || (hc >= BN - 1 && (a2 <= 0 || b1 >= a2 - 1));
+                // a packed tile (block-sparse) holds two lone 64-key blocks, outside every window and the sinks
+                const bool packed = BS && (T.flags & kTilePacked);
+                const bool full = !packed && ((b1 >= BN - 1) || (hc >= BN - 1 && (a2 <= 0 || b1 >= a2 - 1)));
                 const bool narrow = T.chi < 16;
                 const bool masked = __any_sync(0xFFFFFFFFu, !full) || narrow;
                 uint32_t mw[4] = {0xFFFFFFFFu, 0xFFFFFFFFu, 0xFFFFFFFFu, 0xFFFFFFFFu};
                 if (masked) {
 #pragma unroll
                     for (int k = 0; k < 4; ++k)
-                        mw[k] = full ? 0xFFFFFFFFu
-                                     : (range_bits(-32 * k, b1 - 32 * k) | range_bits(a2 - 32 * k, hc - 32 * k));
+                        mw[k] = (full || packed) ? (full ? 0xFFFFFFFFu : 0u)
+                                                 : (range_bits(-32 * k, b1 - 32 * k) | range_bits(a2 - 32 * k, hc - 32 * k));
                 }
-                if (BS && !full && t <= qlast) {
+                if (BS && packed && t <= qlast) {
+                    // per half h: column c holds position base_h + c; the row's random blocks and the global keys,
+                    // up to the row's own position
+                    const TileMask gm = gmask_s[b * MAX_TILES + j];
+                    const int *rb = P.bs_rand + static_cast<int64_t>(t / P.bs_block) * P.bs_r;
+#pragma unroll
+                    for (int h = 0; h < 2; ++h) {
+                        const int base = h ? T.row1 - 64 : T.pbase;
+                        const int hch = min(64 * h + 63, t - base);  // the half's last causal column
+                        for (int i = 0; i < P.bs_r; ++i) {
+                            const int kb = rb[i];
+                            if (kb < 0) continue;
+                            const int lo = max(kb * P.bs_block - base, 64 * h);
+                            const int hi = min(kb * P.bs_block - base + P.bs_block - 1, hch);
+#pragma unroll
+                            for (int k = 2 * h; k < 2 * h + 2; ++k) mw[k] |= range_bits(lo - 32 * k, hi - 32 * k);
+                        }
+#pragma unroll
+                        for (int k = 2 * h; k < 2 * h + 2; ++k)
+                            mw[k] |= gm.w[k] & range_bits(64 * h - 32 * k, hch - 32 * k);
+                    }
+                } else if (BS && !full && t <= qlast) {
                     // block-sparse: also the global keys of the tile and the row's random key blocks, up to hc
                     const TileMask gm = gmask_s[b * MAX_TILES + j];
                     const int *rb = P.bs_rand + static_cast<int64_t>(t / P.bs_block) * P.bs_r;
@@ -950,12 +985,13 @@ __global__ void __launch_bounds__(128, 1) selftest_umma_kernel(const __grid_cons
 }  // namespace tc
 
 // ---------------------------------------------------------------------------------------- host side
-static bool encode_rows_map(CUtensorMap *m, const void *base, uint64_t rows, uint64_t nbh, uint64_t bh_stride_rows) {
+static bool encode_rows_map(CUtensorMap *m, const void *base, uint64_t rows, uint64_t nbh, uint64_t bh_stride_rows,
+                            uint32_t box_rows = 128) {
     EncodeTiledFn enc = encode_tiled_fn();
     if (!enc) return false;
     const cuuint64_t dims[3] = {static_cast<cuuint64_t>(tc::HD), rows, nbh};
     const cuuint64_t strides[2] = {tc::HD * 2, bh_stride_rows * tc::HD * 2};
-    const cuuint32_t box[3] = {64, 128, 1};
+    const cuuint32_t box[3] = {64, box_rows, 1};
     const cuuint32_t estr[3] = {1, 1, 1};
     return enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void *>(base), dims, strides, box, estr,
                CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
@@ -1040,6 +1076,8 @@ static int launch_impl(const PrefillArgs &a, const BlockSparseDev *bs, int dil_r
     }
     else
         okm = okm && encode_rows_map(&p.tm_kc, a.k, L, a.BH, st) && encode_rows_map(&p.tm_vc, a.v, L, a.BH, st);
+    if (bs)  // the 64-row halves of packed tiles
+        okm = okm && encode_rows_map(&p.tm_k64, a.k, L, a.BH, st, 64) && encode_rows_map(&p.tm_v64, a.v, L, a.BH, st, 64);
     if (!okm) return fail(SWA_ERR_INVALID, "cuTensorMapEncodeTiled rejected a tensor (alignment or size)");
     p.o = a.o;
     p.lse = a.lse;
@@ -1091,7 +1129,9 @@ int launch_prefill_bf16_tc_dilated(const PrefillArgs &a, int r) { return launch_
 // random key blocks (<= qlast) of every query block it overlaps: these ranges are merged into disjoint runs,
 // so that each key position appears in exactly one tile, and cut into tiles of up to 128 keys.  Per tile the
 // columns holding a global key are listed (the per-row masks of the kernel add them to the band and sinks),
-// and the tile is marked for the query tiles that have some row it can serve.  Returns SWA_OK or an error.
+// and the tile is marked for the query tiles that have some row it can serve.  Two 64-key tiles outside the sinks
+// and the band that serve the same query tiles are packed into one (one QK and one PV product for both).  Returns
+// SWA_OK or an error.
 size_t blocksparse_tile_list_bytes(int64_t L) {
     const size_t pairs = static_cast<size_t>((L + tc::BM - 1) / tc::BM);
     return pairs * tc::MAX_TILES * (sizeof(tc::Tile) + sizeof(tc::TileMask));
@@ -1105,6 +1145,9 @@ int blocksparse_build_lists(int64_t L, int w, int s, const int32_t *globals, int
     Tile *tiles = static_cast<Tile *>(tiles_out);
     TileMask *gmask = static_cast<TileMask *>(gmask_out);
     std::vector<std::pair<int, int>> iv;
+    std::vector<Tile> tv;
+    std::vector<TileMask> mv;
+    std::vector<int> mate;  // per tile of tv: the tile it is packed with, or -1
     for (int qp = 0; qp < pairs; ++qp) {
         const int q0 = qp * BM;
         const int qlast = static_cast<int>(std::min<int64_t>(q0 + BM, L)) - 1;
@@ -1120,22 +1163,18 @@ int blocksparse_build_lists(int64_t L, int w, int s, const int32_t *globals, int
                 iv.emplace_back(kb * block, static_cast<int>(std::min<int64_t>(static_cast<int64_t>(kb) * block + block - 1, qlast)));
             }
         std::sort(iv.begin(), iv.end());
-        int n = 0;
-        Tile *tl = tiles + static_cast<int64_t>(qp) * MAX_TILES;
-        TileMask *gm = gmask + static_cast<int64_t>(qp) * MAX_TILES;
+        tv.clear();
+        mv.clear();
         size_t k = 0;
         while (k < iv.size()) {
             int a = iv[k].first, b = iv[k].second;
             for (++k; k < iv.size() && iv[k].first <= b + 1; ++k) b = std::max(b, iv[k].second);
             for (int p = a; p <= b; p += BN) {
-                if (n >= MAX_TILES)
-                    return fail(SWA_ERR_UNSUPPORTED, "query rows %d..%d need more than %d key tiles", q0, qlast, MAX_TILES);
-                Tile &T = tl[n];
+                Tile T{};
                 T.row0 = p;
                 T.pbase = p;
                 T.chi = static_cast<short>(std::min(b - p, BN - 1));
-                TileMask &G = gm[n];
-                G.w[0] = G.w[1] = G.w[2] = G.w[3] = 0;
+                TileMask G{};
                 const int32_t *g0 = std::lower_bound(globals, globals + n_globals, p);
                 for (const int32_t *gp = g0; gp < globals + n_globals && *gp <= p + T.chi; ++gp)
                     G.w[(*gp - p) >> 5] |= 1u << ((*gp - p) & 31);
@@ -1156,8 +1195,48 @@ int blocksparse_build_lists(int64_t L, int w, int s, const int32_t *globals, int
                     if (need) f |= 2 << x;
                 }
                 T.flags = static_cast<short>(f);
-                if (f) ++n;  // a tile no query tile needs is dropped
+                if (!f) continue;  // a tile no query tile needs is dropped
+                tv.push_back(T);
+                mv.push_back(G);
             }
+        }
+        // Packing: a tile of exactly 64 keys that holds no sink and no band position of the pair (only random
+        // blocks and global tokens) shares a 128-key tile with another such tile: first with one used by the same
+        // query tiles, then a tile used by both query tiles with one used by a single query tile (each pairing
+        // saves a walk of some query tile).  Columns 0..63 hold the earlier, 64..127 the later, each loaded as
+        // a 64-row box.
+        auto lone = [&](const Tile &T) { return T.chi == 63 && T.pbase >= s && T.pbase + 63 < blo; };
+        mate.assign(tv.size(), -1);
+        for (int pass = 0; pass < 2; ++pass)
+            for (size_t i = 0; i < tv.size(); ++i) {
+                if (mate[i] >= 0 || !lone(tv[i])) continue;
+                for (size_t j = i + 1; j < tv.size(); ++j) {
+                    const int fi = tv[i].flags, fj = tv[j].flags;
+                    if (mate[j] >= 0 || !lone(tv[j])) continue;
+                    if (pass == 0 ? fi != fj : (fi | fj) != (fi > fj ? fi : fj)) continue;
+                    mate[i] = static_cast<int>(j);
+                    mate[j] = static_cast<int>(i);
+                    break;
+                }
+            }
+        int n = 0;
+        Tile *tl = tiles + static_cast<int64_t>(qp) * MAX_TILES;
+        TileMask *gm = gmask + static_cast<int64_t>(qp) * MAX_TILES;
+        for (size_t i = 0; i < tv.size(); ++i) {
+            if (mate[i] >= 0 && static_cast<size_t>(mate[i]) < i) continue;  // the upper half of a packed tile
+            if (n >= MAX_TILES)
+                return fail(SWA_ERR_UNSUPPORTED, "query rows %d..%d need more than %d key tiles", q0, qlast, MAX_TILES);
+            tl[n] = tv[i];
+            gm[n] = mv[i];
+            if (mate[i] >= 0) {
+                const size_t j = static_cast<size_t>(mate[i]);
+                tl[n].chi = BN - 1;
+                tl[n].row1 = tv[j].pbase;
+                tl[n].flags = static_cast<short>(tv[i].flags | tv[j].flags | kTilePacked);
+                gm[n].w[2] = mv[j].w[0];
+                gm[n].w[3] = mv[j].w[1];
+            }
+            ++n;
         }
         count_out[qp] = n;
     }

@@ -4,7 +4,9 @@ diagnostics) against the oracle's membership predicate is_key_blocksparse (CPU o
 For every query pair: tiles hold disjoint runs of positions inside the causal range of the pair; the
 global-column words mark exactly the global tokens of each tile; every key of every non-global row's key set
 lies in a tile its query tile uses; and every used tile holds at least one key of a row of that query tile.
-(Global rows are recomputed over their whole prefix by a separate pass.)"""
+(Global rows are recomputed over their whole prefix by a separate pass.)  A packed tile holds two runs of 64
+keys, columns 0..63 and 64..127, neither touching the sinks or the pair's band (its per-row masks have only
+random blocks and global tokens)."""
 import numpy as np
 import pytest
 
@@ -15,20 +17,34 @@ import sliding_window_softmax_swa_gb300 as swa
 BM, BQ = 256, 128
 
 
+def column_position(pbase, pbase1, c):
+    """The key position held by column c of a tile (packed tiles: columns 64.. start again at pbase1)."""
+    return pbase + c if pbase1 < 0 or c < 64 else pbase1 + c - 64
+
+
 def check_pattern(L, w, s, globals_, block, rand):
+    """Checks every pair's tile list; returns the number of packed tiles seen."""
     rd = swa_inputs.rand_blocks_dict(rand) if rand is not None else None
     gset = set(globals_)
+    m = w - s
+    packed = 0
     for pair in range((L + BM - 1) // BM):
         q0, qlast = pair * BM, min(pair * BM + BM, L) - 1
         plan = swa.prefill_blocksparse_plan(L, w, s, globals_, block, rand, pair)
         seen = {}
-        for j, (pbase, chi, used, gm) in enumerate(plan):
+        for j, (pbase, chi, used, gm, pbase1) in enumerate(plan):
             assert 0 <= chi < 128 and used in (1, 2, 3)
-            assert 0 <= pbase and pbase + chi <= qlast
+            assert 0 <= pbase and column_position(pbase, pbase1, chi) <= qlast
+            if pbase1 >= 0:
+                packed += 1
+                assert chi == 127
+                for first in (pbase, pbase1):  # outside the sinks and the band of every row of the pair
+                    assert first >= s and first + 63 < max(0, q0 - m + 1), (pair, first)
             for c in range(chi + 1):
-                assert pbase + c not in seen, f"position {pbase + c} in two tiles"
-                seen[pbase + c] = j
-                assert bool(gm >> c & 1) == (pbase + c in gset), f"global mask of column {c} at {pbase}"
+                pos = column_position(pbase, pbase1, c)
+                assert pos not in seen, f"position {pos} in two tiles"
+                seen[pos] = j
+                assert bool(gm >> c & 1) == (pos in gset), f"global mask of column {c} at {pbase}"
             assert gm >> (chi + 1) == 0
         useful = set()
         for t in range(q0, qlast + 1):
@@ -41,12 +57,13 @@ def check_pattern(L, w, s, globals_, block, rand):
                     j = seen[i]
                     assert plan[j][2] >> x & 1, f"key {i} of row {t}: its tile is not walked by query tile {x}"
                     useful.add((j, x))
-        for j, (_, _, used, _) in enumerate(plan):
+        for j, (_, _, used, _, _) in enumerate(plan):
             for x in range(2):
                 if used >> x & 1:
                     # a global row may be the only user; the pass still walks the tile (its rows are overwritten)
                     rows = range(q0 + x * BQ, min(q0 + x * BQ + BQ, qlast + 1))
                     assert (j, x) in useful or any(t in gset for t in rows), f"tile {j} walked by {x} for nothing"
+    return packed
 
 
 def test_hand_pattern():
@@ -64,7 +81,21 @@ def test_hand_pattern():
 ])
 def test_random_patterns(L, w, s, ng, block, r, seed):
     globals_, rand = swa_inputs.bigbird_pattern(L, block, ng, r, seed)
-    check_pattern(L, w, s, globals_, block, rand if r else None)
+    packed = check_pattern(L, w, s, globals_, block, rand if r else None)
+    if block == 64 and r >= 2 and L >= 1000:
+        assert packed > 0  # lone random blocks far behind the band share tiles
+
+
+def test_packed_halves_by_hand():
+    # query block 9 (rows 576..639, query tile 4 of pair 2) -> key blocks 0 and 3; w = 64: both lie outside
+    # the sinks and the band, serve the same query tile, and so share one tile
+    L, block = 700, 64
+    rand = np.full((11, 2), -1, dtype=np.int32)
+    rand[9] = [3, 1]
+    plan = swa.prefill_blocksparse_plan(L, 64, 4, [], block, rand, 2)
+    packed = [t for t in plan if t[4] >= 0]
+    assert [(t[0], t[1], t[2], t[4]) for t in packed] == [(64, 127, 1, 192)]
+    check_pattern(L, 64, 4, [], block, rand)
 
 
 def test_scattered_globals():
@@ -77,7 +108,7 @@ def test_without_globals_and_blocks_matches_plain_walk():
     L, w, s = 1000, 300, 4
     for pair in range((L + BM - 1) // BM):
         q0, q1 = pair * BM, min(pair * BM + BM, L) - 1
-        bs = [(p, c, u) for p, c, u, _ in swa.prefill_blocksparse_plan(L, w, s, [], 16, None, pair)]
+        bs = [(p, c, u) for p, c, u, _, _ in swa.prefill_blocksparse_plan(L, w, s, [], 16, None, pair)]
         plain = [(pb, c, u) for _, _, pb, c, u in swa.prefill_tile_plan(q0, q1, 0, w, s)]
         cover = lambda tl: sorted(p for pb, c, _ in tl for p in range(pb, pb + c + 1))
         assert cover(bs) == cover(plain)
