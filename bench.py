@@ -378,7 +378,7 @@ def prefill_leg(swa, wl, steps, warmup, world, rank, clocks, e2e=False, rope=Fal
         launches = 5  # the SWA prefill, the feature-map weights, the chunk states, their scan, the linear pass
     elif blocksparse is not None:
         flops = 4.0 * B * H * d * blocksparse_pairs(L, w, s, globals_, block, rand)
-        launches = 2 if len(globals_) else 1
+        launches = 2 if any(int(x) >= w for x in globals_) else 1  # global rows past the window: second pass
     else:
         flops = dilated_flops(B, H, L, d, w, s, dilation) if dilation else banded_flops(B, H, L, d, w)
         # dilated: the tensor-core pass, then the sink rows and the rows past the last whole group of r
@@ -729,7 +729,8 @@ def main():
             "metric": METRIC, "value": aggregate_rate(r["tflops"], world, 1.0), "unit": "TFLOP/s",
             "ms_per_step": r["ms_per_step"], "frac_of_bf16_peak": r["tflops"] / peaks["bf16_tflops"],
             "what": "block-sparse: window + sinks + 128 global tokens + 3 random key blocks of 64 per query block "
-                    "(FLOPs over those key sets): host tile lists + their upload, tensor-core prefill, global rows",
+                    "(FLOPs over those key sets): host tile lists + their upload, tensor-core prefill (+ the global "
+                    "rows at or past w, none here: every global row below w is complete after the tiled pass)",
             "launches_per_step": r["launches"] // max(3, args.steps // 2)}
     if "hybrid" in legs:
         r = prefill_leg(swa, wl, max(3, args.steps // 2), 3, world, rank, clocks, hybrid=True)

@@ -194,8 +194,11 @@ int swa_sink_prefill_chunked_dilated(const void *q, const void *k, const void *v
  *             i*block + block - 1) attended by each query block, -1 for an unused entry; 0 <= r <= 16.  The random
  *             choice is the caller's: the library draws nothing.
  *   workspace : caller-owned device scratch of swa_sink_prefill_blocksparse_workspace_size(L, n_globals, block, r)
- *             bytes, 256-byte aligned (the tile lists and the pattern, uploaded with cudaMemcpyAsync from pageable
- *             host memory: the call is not capturable into a CUDA graph).
+ *             bytes, 256-byte aligned.  The tile lists and the pattern are built on the host into one of two
+ *             pinned staging buffers the library keeps per device (allocated on first use, grown as needed) and
+ *             uploaded with one cudaMemcpyAsync on `stream`; a buffer is reused only after its copy has completed
+ *             (an event wait), so the host may prepare the next call while the device runs this one.  The call
+ *             is not capturable into a CUDA graph (the copy's source changes from call to call).
  *   A query pair (256 rows) whose keys need more than 64 tiles of 128 keys is refused with SWA_ERR_UNSUPPORTED.
  *   Other arguments and errors as swa_sink_prefill.
  */

@@ -8,10 +8,13 @@
 // 256-row query pair (band + sinks + global keys + random blocks, merged into disjoint runs, cut into tiles of
 // up to 128 keys, with the global-key columns of each tile), and the kernel's per-row column masks add the
 // global keys and the row's random blocks to its band and sinks.  The global rows, whose key set is the whole
-// causal prefix, are then recomputed by full_rows_kernel and overwrite what the tiled pass wrote for them.
+// causal prefix, are then recomputed by full_rows_kernel and overwrite what the tiled pass wrote for them (a
+// global row t < w needs no second pass: its sinks and window already cover [0, t]).
 #include <cuda_bf16.h>
 
+#include <algorithm>
 #include <cstring>
+#include <mutex>
 #include <vector>
 
 #include "../../include/swa_sink.h"
@@ -130,6 +133,58 @@ struct HostLists {
     }
 };
 
+// Pinned staging of what a call uploads (its tile lists, counts, random blocks and global positions, in the
+// workspace's layout): two slots per device, used in turn.  A slot is written again only once the copy that read
+// it has completed (its event), so the host builds a call's lists while the device still runs the previous call,
+// and the whole upload is one asynchronous copy.
+struct StageSlot {
+    void *host = nullptr;
+    size_t cap = 0;
+    cudaEvent_t done = nullptr;
+    bool pending = false;
+};
+constexpr int kStageDevices = 64;
+static std::mutex g_stage_mu;
+static StageSlot g_stage[kStageDevices][2];
+static unsigned g_stage_turn[kStageDevices];
+
+// Takes the next slot of the current device with room for `bytes` (waiting for its previous copy), or null with
+// the error set.  The caller holds g_stage_mu until it has recorded the slot's event.
+static StageSlot *stage_slot(size_t bytes) {
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess || dev < 0 || dev >= kStageDevices) {
+        fail(SWA_ERR_CUDA, "cudaGetDevice: %s", cudaGetErrorString(e));
+        return nullptr;
+    }
+    StageSlot &sl = g_stage[dev][g_stage_turn[dev]++ & 1];
+    if (!sl.done && (e = cudaEventCreateWithFlags(&sl.done, cudaEventDisableTiming)) != cudaSuccess) {
+        sl.done = nullptr;
+        fail(SWA_ERR_CUDA, "staging event: %s", cudaGetErrorString(e));
+        return nullptr;
+    }
+    if (sl.pending) {
+        if ((e = cudaEventSynchronize(sl.done)) != cudaSuccess) {
+            fail(SWA_ERR_CUDA, "staging wait: %s", cudaGetErrorString(e));
+            return nullptr;
+        }
+        sl.pending = false;
+    }
+    if (sl.cap < bytes) {
+        if (sl.host) cudaFreeHost(sl.host);
+        sl.host = nullptr;
+        sl.cap = 0;
+        const size_t cap = bytes + bytes / 4;
+        if ((e = cudaHostAlloc(&sl.host, cap, cudaHostAllocDefault)) != cudaSuccess) {
+            sl.host = nullptr;
+            fail(SWA_ERR_CUDA, "pinned staging of %zu bytes: %s", cap, cudaGetErrorString(e));
+            return nullptr;
+        }
+        sl.cap = cap;
+    }
+    return &sl;
+}
+
 extern "C" int swa_prefill_blocksparse_plan(int64_t L, int w, int s, const int32_t *globals, int n_globals,
                                             int block, const int32_t *rand_blocks, int r, int64_t pair, int *tiles,
                                             int max_tiles) {
@@ -189,34 +244,49 @@ extern "C" int swa_sink_prefill_blocksparse(const void *q, const void *k, const 
     if (!workspace || (reinterpret_cast<uintptr_t>(workspace) & 255u))
         return fail(SWA_ERR_INVALID, "workspace must be non-null and 256-byte aligned");
 
-    // the tile lists, built on the host and copied with the pattern into the workspace
+    // the tile lists, built on the host into a pinned slot laid out as the workspace, then one copy:
+    // [tiles | global-column words] [counts] [random blocks] [global positions], each part 256-byte aligned
     const int64_t pairs = ceil_div(L, 256);
-    HostLists hl;
-    if (int rc = hl.build(L, w, s, globals, n_globals, block, rand_blocks, r)) return rc;
-    const size_t list_bytes = hl.bytes.size();
+    const size_t list_bytes = blocksparse_tile_list_bytes(L);
+    const size_t tiles_bytes = list_bytes / (HostLists::kRecord + 16) * HostLists::kRecord;
+    const size_t off_count = align256(list_bytes);
+    const size_t off_rand = off_count + align256(static_cast<size_t>(pairs) * 4);
+    const size_t off_glob = off_rand + align256(static_cast<size_t>(qblocks) * r * 4 + 4);
+    const size_t upload = off_glob + static_cast<size_t>(n_globals) * 4;
     char *ws = static_cast<char *>(workspace);
-    char *d_lists = ws;
-    int *d_count = reinterpret_cast<int *>(ws + align256(list_bytes));
-    int *d_rand = reinterpret_cast<int *>(reinterpret_cast<char *>(d_count) + align256(static_cast<size_t>(pairs) * 4));
-    int *d_glob = reinterpret_cast<int *>(reinterpret_cast<char *>(d_rand) + align256(static_cast<size_t>(qblocks) * r * 4 + 4));
     const cudaStream_t st = static_cast<cudaStream_t>(stream);
-    // pageable host sources: each copy is staged before cudaMemcpyAsync returns, so the vectors may go
-    cudaError_t e = cudaMemcpyAsync(d_lists, hl.bytes.data(), list_bytes, cudaMemcpyHostToDevice, st);
-    if (e == cudaSuccess) e = cudaMemcpyAsync(d_count, hl.count.data(), hl.count.size() * 4, cudaMemcpyHostToDevice, st);
-    if (e == cudaSuccess && r > 0)
-        e = cudaMemcpyAsync(d_rand, rand_blocks, static_cast<size_t>(qblocks) * r * 4, cudaMemcpyHostToDevice, st);
-    if (e == cudaSuccess && n_globals > 0)
-        e = cudaMemcpyAsync(d_glob, globals, static_cast<size_t>(n_globals) * 4, cudaMemcpyHostToDevice, st);
-    if (e != cudaSuccess) return fail(SWA_ERR_CUDA, "block-sparse pattern upload: %s", cudaGetErrorString(e));
+    {
+        std::lock_guard<std::mutex> lk(g_stage_mu);
+        StageSlot *sl = stage_slot(upload);
+        if (!sl) return SWA_ERR_CUDA;
+        char *h = static_cast<char *>(sl->host);
+        if (int rc = blocksparse_build_lists(L, w, s, globals, n_globals, block, rand_blocks, r, h, h + tiles_bytes,
+                                             reinterpret_cast<int *>(h + off_count)))
+            return rc;
+        if (r > 0) std::memcpy(h + off_rand, rand_blocks, static_cast<size_t>(qblocks) * r * 4);
+        if (n_globals > 0) std::memcpy(h + off_glob, globals, static_cast<size_t>(n_globals) * 4);
+        cudaError_t e = cudaMemcpyAsync(ws, h, upload, cudaMemcpyHostToDevice, st);
+        if (e == cudaSuccess) e = cudaEventRecord(sl->done, st);
+        if (e != cudaSuccess) return fail(SWA_ERR_CUDA, "block-sparse pattern upload: %s", cudaGetErrorString(e));
+        sl->pending = true;
+    }
+    char *d_lists = ws;
+    int *d_count = reinterpret_cast<int *>(ws + off_count);
+    int *d_rand = reinterpret_cast<int *>(ws + off_rand);
+    int *d_glob = reinterpret_cast<int *>(ws + off_glob);
     PrefillArgs a{q, k, v, o, lse, nullptr, nullptr, 0, B * H, L, d, w, s, scale, L, st};
-    const BlockSparseDev bs{d_lists, d_lists + hl.tiles_bytes, d_count, d_rand, block, r};
+    const BlockSparseDev bs{d_lists, d_lists + tiles_bytes, d_count, d_rand, block, r};
     if (int rc = launch_prefill_bf16_tc_blocksparse(a, bs)) return rc;
-    if (n_globals > 0) {  // the global rows attend their whole causal prefix
-        full_rows_kernel<<<dim3(static_cast<unsigned>(n_globals), static_cast<unsigned>(B * H)), 128, 0, st>>>(
+    // The global rows attend their whole causal prefix.  For a global row t < w that prefix is already its sinks
+    // and window ([0, s) and [t - m + 1, t] cover [0, t]), which the tiled pass computed: only the rows t >= w
+    // are recomputed.
+    const int n_near = static_cast<int>(std::lower_bound(globals, globals + n_globals, w) - globals);
+    if (n_globals > n_near) {
+        full_rows_kernel<<<dim3(static_cast<unsigned>(n_globals - n_near), static_cast<unsigned>(B * H)), 128, 0, st>>>(
             static_cast<const __nv_bfloat16 *>(q), static_cast<const __nv_bfloat16 *>(k),
-            static_cast<const __nv_bfloat16 *>(v), static_cast<__nv_bfloat16 *>(o), lse, d_glob, L,
+            static_cast<const __nv_bfloat16 *>(v), static_cast<__nv_bfloat16 *>(o), lse, d_glob + n_near, L,
             scale * 1.4426950408889634f);
-        e = cudaGetLastError();
+        const cudaError_t e = cudaGetLastError();
         if (e != cudaSuccess) return fail(SWA_ERR_CUDA, "global rows launch: %s", cudaGetErrorString(e));
     }
     return SWA_OK;

@@ -95,7 +95,8 @@ constexpr uint32_t OFF_TILES = OFF_MISC + 64;
 constexpr uint32_t TILE_RECORD = 16;                              // bytes of one tile record (struct Tile)
 constexpr uint32_t OFF_GMASK = OFF_TILES + 2 * MAX_TILES * TILE_RECORD;  // two tile lists (current / next item)
 constexpr uint32_t OFF_XCH = OFF_GMASK + 2 * MAX_TILES * 16;       // and their global-key columns (block-sparse)
-constexpr uint32_t SMEM_USED = OFF_XCH + 2 * 4 * BQ * 4;             // (max, sum) exchange of the two streams
+constexpr uint32_t OFF_RKS = OFF_XCH + 2 * 4 * BQ * 4;               // (max, sum) exchange of the two streams
+constexpr uint32_t SMEM_USED = OFF_RKS + 2 * BQ * 8;                // per softmax thread: its row's random blocks
 constexpr uint32_t SMEM_BYTES = SMEM_USED + 1024;  // slack to align the base to 1024 bytes
 static_assert(SMEM_BYTES <= 232448, "shared memory budget of one CTA");
 
@@ -129,6 +130,7 @@ struct Params {
     const int *bs_count;
     const int *bs_rand;  // [ceil(L / bs_block)][bs_r]; -1 = no block
     int bs_block, bs_r;
+    int bs_kblocks;  // key blocks of the sequence: ceil(L / bs_block)
     void *o;
     float *lse;
     DeviceStatus *status;
@@ -334,6 +336,7 @@ __global__ void __launch_bounds__(kThreads, 1) swa_prefill_tc_kernel(const __gri
     Tile *tiles_s = reinterpret_cast<Tile *>(sm + OFF_TILES);     // [2][MAX_TILES]
     TileMask *gmask_s = reinterpret_cast<TileMask *>(sm + OFF_GMASK);  // [2][MAX_TILES] (block-sparse)
     float *xch = reinterpret_cast<float *>(sm + OFF_XCH);  // [2 slots][2 streams][max, sum][128 rows]
+    uint2 *rks_s = reinterpret_cast<uint2 *>(sm + OFF_RKS);  // [2 streams][128 rows] (block-sparse)
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int G = static_cast<int>(gridDim.x);
@@ -646,6 +649,23 @@ __global__ void __launch_bounds__(kThreads, 1) swa_prefill_tc_kernel(const __gri
             bool ok = __all_sync(0xFFFFFFFFu, mbar_wait(&lready[b], (it >> 1) & 1, wc, 14, it));
             const Tile *tl = tiles_s + b * MAX_TILES;
             const int n = ok ? ntiles_s[b] : 0;
+            // block-sparse: the row's random key blocks (its query block's), the first four kept in this thread's
+            // shared slot for the item as 16-bit block indices (0xFFFF = none) when every index fits, the rest read
+            // per tile; rows past the end have none
+            if (BS) {
+                const int nr_slot = P.bs_kblocks < 0xFFFF ? min(P.bs_r, 4) : 0;
+                uint32_t rkp[2] = {0xFFFFFFFFu, 0xFFFFFFFFu};
+                if (t <= qlast) {
+                    const int *rb = P.bs_rand + static_cast<int64_t>(t / P.bs_block) * P.bs_r;
+#pragma unroll
+                    for (int i = 0; i < 4; ++i) {
+                        const int kb = i < nr_slot ? rb[i] : -1;
+                        const uint32_t v16 = kb >= 0 ? static_cast<uint32_t>(kb) : 0xFFFFu;
+                        rkp[i >> 1] = (rkp[i >> 1] & ~(0xFFFFu << (16 * (i & 1)))) | (v16 << (16 * (i & 1)));
+                    }
+                }
+                rks_s[g * BQ + r] = make_uint2(rkp[0], rkp[1]);
+            }
             float mrun = -INFINITY, lrun = 0.f;  // running max (log2 units) and sum of this stream
             for (int j = g; j < n; j += 2) {
                 const Tile T = tl[j];
@@ -669,41 +689,43 @@ __global__ void __launch_bounds__(kThreads, 1) swa_prefill_tc_kernel(const __gri
                         mw[k] = (full || packed) ? (full ? 0xFFFFFFFFu : 0u)
                                                  : (range_bits(-32 * k, b1 - 32 * k) | range_bits(a2 - 32 * k, hc - 32 * k));
                 }
-                if (BS && packed && t <= qlast) {
-                    // per half h: column c holds position base_h + c; the row's random blocks and the global keys,
-                    // up to the row's own position
+                if (BS && (packed || !full) && t <= qlast) {
+                    // block-sparse: also the global keys of the tile and the row's random key blocks, up to the
+                    // row's own position.  Columns [c0, c1] of the tile hold positions base + c0 .. base + c1: the
+                    // whole tile (hc = its last causal column), or for a packed tile each 64-column half (h) with
+                    // its own base.
                     const TileMask gm = gmask_s[b * MAX_TILES + j];
-                    const int *rb = P.bs_rand + static_cast<int64_t>(t / P.bs_block) * P.bs_r;
+                    const uint2 rk = rks_s[g * BQ + r];
+                    auto add_cols = [&](int base, int c0, int c1, int kw0, int kw1) {
+                        auto add_block = [&](int start) {
+                            const int lo = max(start - base, c0), hi = min(start - base + P.bs_block - 1, c1);
 #pragma unroll
-                    for (int h = 0; h < 2; ++h) {
-                        const int base = h ? T.row1 - 64 : T.pbase;
-                        const int hch = min(64 * h + 63, t - base);  // the half's last causal column
-                        for (int i = 0; i < P.bs_r; ++i) {
-                            const int kb = rb[i];
-                            if (kb < 0) continue;
-                            const int lo = max(kb * P.bs_block - base, 64 * h);
-                            const int hi = min(kb * P.bs_block - base + P.bs_block - 1, hch);
+                            for (int k = 0; k < 4; ++k)
+                                if (k >= kw0 && k < kw1) mw[k] |= range_bits(lo - 32 * k, hi - 32 * k);
+                        };
 #pragma unroll
-                            for (int k = 2 * h; k < 2 * h + 2; ++k) mw[k] |= range_bits(lo - 32 * k, hi - 32 * k);
+                        for (int i = 0; i < 4; ++i) {
+                            const uint32_t kb = ((i < 2 ? rk.x : rk.y) >> (16 * (i & 1))) & 0xFFFFu;
+                            if (kb != 0xFFFFu) add_block(static_cast<int>(kb) * P.bs_block);
+                        }
+                        const int nr_slot = P.bs_kblocks < 0xFFFF ? min(P.bs_r, 4) : 0;
+                        if (P.bs_r > nr_slot) {
+                            const int *rb = P.bs_rand + static_cast<int64_t>(t / P.bs_block) * P.bs_r;
+                            for (int i = nr_slot; i < P.bs_r; ++i) {
+                                const int kb = rb[i];
+                                if (kb >= 0) add_block(kb * P.bs_block);
+                            }
                         }
 #pragma unroll
-                        for (int k = 2 * h; k < 2 * h + 2; ++k)
-                            mw[k] |= gm.w[k] & range_bits(64 * h - 32 * k, hch - 32 * k);
+                        for (int k = 0; k < 4; ++k)
+                            if (k >= kw0 && k < kw1) mw[k] |= gm.w[k] & range_bits(c0 - 32 * k, c1 - 32 * k);
+                    };
+                    if (packed) {
+                        add_cols(T.pbase, 0, min(63, t - T.pbase), 0, 2);
+                        add_cols(T.row1 - 64, 64, min(127, t - (T.row1 - 64)), 2, 4);
+                    } else {
+                        add_cols(T.pbase, 0, hc, 0, 4);
                     }
-                } else if (BS && !full && t <= qlast) {
-                    // block-sparse: also the global keys of the tile and the row's random key blocks, up to hc
-                    const TileMask gm = gmask_s[b * MAX_TILES + j];
-                    const int *rb = P.bs_rand + static_cast<int64_t>(t / P.bs_block) * P.bs_r;
-                    for (int i = 0; i < P.bs_r; ++i) {
-                        const int kb = rb[i];
-                        if (kb < 0) continue;
-                        const int lo = kb * P.bs_block - T.pbase;
-                        const int hi = min(lo + P.bs_block - 1, hc);
-#pragma unroll
-                        for (int k = 0; k < 4; ++k) mw[k] |= range_bits(lo - 32 * k, hi - 32 * k);
-                    }
-#pragma unroll
-                    for (int k = 0; k < 4; ++k) mw[k] |= gm.w[k] & range_bits(-32 * k, hc - 32 * k);
                 }
                 // the running max: O is rescaled only when it grows by more than 2^8 (also taken when mrun is
                 // still -inf); returns -m for the exponent
@@ -1103,6 +1125,7 @@ static int launch_impl(const PrefillArgs &a, const BlockSparseDev *bs, int dil_r
         p.bs_rand = bs->rand;
         p.bs_block = bs->block;
         p.bs_r = bs->r;
+        p.bs_kblocks = static_cast<int>((a.L + bs->block - 1) / bs->block);
     }
     auto *kern = bs ? swa_prefill_tc_kernel<1> : dil_r > 0 ? swa_prefill_tc_kernel<2> : swa_prefill_tc_kernel<0>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
