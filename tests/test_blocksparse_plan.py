@@ -131,3 +131,19 @@ def test_pattern_errors():
     globals_ = [200 * i for i in range(70)]
     with pytest.raises(swa.SwaError):
         swa.prefill_blocksparse_plan(L, 16, 4, globals_, 64, None, (L - 1) // BM)
+
+
+def test_packed_tiles_with_globals_and_shared_blocks():
+    # the pattern of the GPU packed-tile test: blocks used by both query tiles pair first, then within one
+    # query tile; global tokens inside packed halves keep their columns
+    L, w, s, block = 1300, 64, 4, 64
+    rand = np.full(((L + block - 1) // block, 2), -1, dtype=np.int32)
+    rand[16] = [1, 5]
+    rand[17] = [3, -1]
+    rand[18] = [3, 9]
+    rand[19] = [11, 0]
+    plan = swa.prefill_blocksparse_plan(L, w, s, [200, 330], block, rand, 4)
+    packed = [t for t in plan if t[4] >= 0]
+    assert [(t[0], t[4], t[2]) for t in packed] == [(192, 320, 3), (576, 704, 2)]
+    assert packed[0][3] == (1 << (200 - 192)) | (1 << (64 + 330 - 320))
+    assert check_pattern(L, w, s, [200, 330], block, rand) >= 2

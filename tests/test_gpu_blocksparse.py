@@ -86,3 +86,20 @@ def test_rejects_bad_patterns():
     bad = np.full((7, 1), 9, dtype=np.int32)  # key block 9 does not exist (7 blocks of 16)
     with pytest.raises(swa.SwaError):
         swa.swa_sink_prefill_blocksparse(q, q, q, 16, 4, [], 16, bad)
+
+
+def test_packed_tiles():
+    # query pair 4 (rows 1024..1279, w = 64): query tile 0 takes key blocks 1, 3, 5, query tile 1 blocks 3, 9, 11
+    # and 0 (with the sinks); the global tokens 200 and 330 sit in blocks 3 and 5.  Blocks 3 and 5 (both query
+    # tiles) share one packed tile, each half with a global column, and so do blocks 9 and 11 (query tile 1)
+    swa = require_gpu()
+    L, w, s, block = 1300, 64, 4, 64
+    rand = np.full(((L + block - 1) // block, 2), -1, dtype=np.int32)
+    rand[16] = [1, 5]
+    rand[17] = [3, -1]
+    rand[18] = [3, 9]
+    rand[19] = [11, 0]
+    globals_ = [200, 330]
+    packed = [(t[0], t[4], t[2]) for t in swa.prefill_blocksparse_plan(L, w, s, globals_, block, rand, 4) if t[4] >= 0]
+    assert packed == [(192, 320, 3), (576, 704, 2)], packed
+    run(1, 2, L, w, s, globals_, block, rand, 77)
