@@ -130,19 +130,37 @@ __global__ void __launch_bounds__(256) rope_prep_kernel(const uint2 *__restrict_
     const int64_t step = static_cast<int64_t>(gridDim.x) * rows_per_cta;
     // A warp holds two rows (lanes 0-15 and 16-31).  Both halves walk the loop together, a half whose row is
     // past the end only idling, so that the 16-lane shuffles below always have the whole warp.
+    // Each pass of the loop takes two row pairs, `step` apart, and issues the loads of both before working on
+    // either, so that twice the bytes are in flight per thread.
     const int64_t first = static_cast<int64_t>(blockIdx.x) * rows_per_cta + (threadIdx.x / 32) * 2;
-    for (int64_t pair = first; pair < rows; pair += step) {
-        const int64_t row = pair + (threadIdx.x / kRopeLanes) % 2;
+    for (int64_t pair0 = first; pair0 < rows; pair0 += 2 * step) {
+      uint2 ld[2][4];
+#pragma unroll
+      for (int u = 0; u < 2; ++u) {
+        const int64_t row = pair0 + u * step + (threadIdx.x / kRopeLanes) % 2;
+        const int64_t ia = row * 32 + sub, ib = ia + 16;
+        if (row < rows) {
+            ld[u][0] = __ldg(q + ia);
+            ld[u][1] = __ldg(q + ib);
+            ld[u][2] = __ldg(k + ia);
+            ld[u][3] = __ldg(k + ib);
+        } else {
+            ld[u][0] = ld[u][1] = ld[u][2] = ld[u][3] = make_uint2(0u, 0u);
+        }
+      }
+#pragma unroll
+      for (int u = 0; u < 2; ++u) {
+        const int64_t row = pair0 + u * step + (threadIdx.x / kRopeLanes) % 2;
         const bool valid = row < rows;
         const int64_t t = row % L;
         const int64_t ia = row * 32 + sub, ib = ia + 16;
         float x[4] = {0.f, 0.f, 0.f, 0.f}, y[4] = {0.f, 0.f, 0.f, 0.f};
         if (valid) {
             float qa[4], qb[4], ka[4], kb[4];
-            unpack4(__ldg(q + ia), qa);
-            unpack4(__ldg(q + ib), qb);
-            unpack4(__ldg(k + ia), ka);
-            unpack4(__ldg(k + ib), kb);
+            unpack4(ld[u][0], qa);
+            unpack4(ld[u][1], qb);
+            unpack4(ld[u][2], ka);
+            unpack4(ld[u][3], kb);
             float sn[kRopePpl], c[kRopePpl];
 #pragma unroll
             for (int p = 0; p < kRopePpl; ++p) turn_sincos(static_cast<uint32_t>(t), f[p], sn[p], c[p]);
@@ -192,6 +210,7 @@ __global__ void __launch_bounds__(256) rope_prep_kernel(const uint2 *__restrict_
                 if (valid && (sub & 3) == 0 && i < out.s) out.ssink[row * out.sstride + i] = v;
             }
         }
+      }
     }
 }
 
@@ -238,7 +257,13 @@ int launch_rope_prep(const void *q, const void *k, const RopeParts &o, int BH, i
     }
     const int64_t rows = static_cast<int64_t>(BH) * L;
     const int64_t ctas_needed = (rows + rows_per_cta - 1) / rows_per_cta;
-    const int ctas = static_cast<int>(ctas_needed < 152 * 8 ? ctas_needed : 152 * 8);
+    // one wave: as many CTAs as the SMs hold at once (the loop strides over the rest)
+    int dev = 0, sms = 0, per_sm = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess ||
+        cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, rope_prep_kernel, 256, 0) != cudaSuccess || per_sm < 1)
+        return fail(SWA_ERR_CUDA, "rope prefill pass: device attributes");
+    const int64_t wave = static_cast<int64_t>(sms) * per_sm;
+    const int ctas = static_cast<int>(ctas_needed < wave ? ctas_needed : wave);
     const RopeOut out{static_cast<uint2 *>(o.qr), static_cast<uint2 *>(o.qr_lo), static_cast<uint2 *>(o.kr),
                       static_cast<uint2 *>(o.kr_lo), o.ssink, reinterpret_cast<const float4 *>(o.ks), s, o.sstride};
     rope_prep_kernel<<<ctas, 256, 0, stream>>>(static_cast<const uint2 *>(q), static_cast<const uint2 *>(k), out,
