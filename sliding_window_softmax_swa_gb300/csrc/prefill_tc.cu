@@ -26,8 +26,9 @@
 //              key tile j PV(j), QK(j+2), where QK(j) is S = Q K_j^T into S buffer j mod 2 and PV(j) is
 //              O_{j mod 2} += P_j V_j with P_j (bf16 pairs written over the first 64 columns of its S buffer)
 //              read by the MMA straight from tensor memory; S buffer j mod 2 is reused by QK(j+2) after PV(j) in
-//              issue order (tcgen05 MMAs of a thread complete in order).  The single issue order keeps the two
-//              streams out of phase.  A narrow tile (all keys in its first 16 columns, such as the sink tile)
+//              issue order (tcgen05 MMAs of a thread complete in order).  In block-sparse mode PV(j) runs in two
+//              parts: keys 0..63 once that half of P_j is written (and O rescaled), the rest once all of it is.
+//              The single issue order keeps the two streams out of phase.  A narrow tile (all keys in its first 16 columns, such as the sink tile)
 //              takes an N = 16 QK product and one 16-key PV product;
 //   warp 10    per item: builds the key-tile list into one of two buffers, one item ahead; stores the O rows
 //              that the epilogue of the item two back staged in the item's Q buffer (TMA, so that the softmax
@@ -293,14 +294,15 @@ __device__ __forceinline__ void issue_qk(uint32_t d_tmem, uint32_t q_addr, uint3
     }
 }
 
+// Key steps [k0, k1) of 16 keys each (block-sparse mode runs PV in two parts, keys 0..63 as soon as their half
+// of P is written).
 __device__ __forceinline__ void issue_pv(uint32_t d_tmem, uint32_t p_tmem, uint32_t v_addr, bool accumulate,
-                                         bool narrow) {
+                                         int k0, int k1) {
     const uint32_t vlo = sdesc_sw128_lo(v_addr, HALF_BYTES);
     constexpr uint32_t hi = sdesc_sw128_hi(1024);
-    const int nkk = narrow ? 1 : BN / 16;
 #pragma unroll
     for (int kk = 0; kk < BN / 16; ++kk) {
-        if (kk >= nkk) break;
+        if (kk < k0 || kk >= k1) continue;
         // P from TMEM: 16 keys = 8 columns of packed bf16 pairs; V: 16 key rows of 128 bytes (MN-major)
         umma_ts_warp_lo(d_tmem, p_tmem + kk * 8, vlo + ((kk * 16 * 128) >> 4), hi, IDESC_PV,
                         (accumulate || kk > 0) ? 1u : 0u);
@@ -330,6 +332,7 @@ __global__ void __launch_bounds__(kThreads, 1) swa_prefill_tc_kernel(const __gri
     uint64_t *lready = oempty + 1;    // [2]: tile list buffer b written (1 arrival)
     uint64_t *lfree = lready + 2;     // [2]: tile list buffer b no longer read (softmax warps, MMA, 2 loaders)
     uint64_t *drain = lfree + 2;
+    uint64_t *phalf = drain + 1;      // [2] (block-sparse mode): keys 0..63 of P_j written and O rescaled
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(sm + OFF_MISC);
     volatile int *abort_flag = reinterpret_cast<volatile int *>(sm + OFF_MISC + 4);
     int *ntiles_s = reinterpret_cast<int *>(sm + OFF_MISC + 8);  // [2]
@@ -351,6 +354,7 @@ __global__ void __launch_bounds__(kThreads, 1) swa_prefill_tc_kernel(const __gri
             mbar_init(&vempty[i], 1);
             mbar_init(&sfull[i], 1);
             mbar_init(&pfull[i], kSmThreads / 2);
+            mbar_init(&phalf[i], kSmThreads / 2);
             mbar_init(&lready[i], 1);
             mbar_init(&lfree[i], kSmWarps + 3);
         }
@@ -597,14 +601,26 @@ __global__ void __launch_bounds__(kThreads, 1) swa_prefill_tc_kernel(const __gri
                 fine = qk(0) && (n < 2 || qk(1));
                 for (int j = 0; fine && j < n; ++j) {
                     const int st = j & 1;
-                    if (!wwait(&pfull[st], (st ? np1 : np0) & 1, 4, j)) { fine = false; break; }
+                    // block-sparse mode: PV(j) in two parts, keys 0..63 once their half of P is written (the
+                    // softmax threads write the other half meanwhile), keys 64..127 once all of P is
+                    const int pp = (st ? np1 : np0) & 1;
+                    if (!wwait(BS ? &phalf[st] : &pfull[st], pp, BS ? 16 : 4, j)) { fine = false; break; }
                     np1 += st;
                     np0 += st ^ 1;
                     if (j == 0 && it >= 1 && !wwait(oempty, (it - 1) & 1, 11, j)) { fine = false; break; }
                     const int sv = gv % NV;
                     if (!wwait(&vfull[sv], (gv / NV) & 1, 5, j)) { fine = false; break; }
                     tc_fence_after();
-                    issue_pv(tmem + col_o(st), tmem + col_s(st), v_addr0 + sv * TILE_BYTES, j >= 2, tl[j].chi < 16);
+                    const bool nar = tl[j].chi < 16;
+                    const uint32_t o_t = tmem + col_o(st), p_t = tmem + col_s(st), v_a = v_addr0 + sv * TILE_BYTES;
+                    if (BS) {
+                        issue_pv(o_t, p_t, v_a, j >= 2, 0, nar ? 1 : BN / 32);
+                        if (!wwait(&pfull[st], pp, 4, j)) { fine = false; break; }
+                        tc_fence_after();
+                        if (!nar) issue_pv(o_t, p_t, v_a, true, BN / 32, BN / 16);
+                    } else {
+                        issue_pv(o_t, p_t, v_a, j >= 2, 0, nar ? 1 : BN / 16);
+                    }
                     umma_commit_warp(&vempty[sv]);
                     if (j == n - 1) umma_commit_warp(ofull);  // the item's last product
                     ++gv;
@@ -742,6 +758,22 @@ __global__ void __launch_bounds__(kThreads, 1) swa_prefill_tc_kernel(const __gri
                     }
                     return (mrun == -INFINITY) ? 0.f : -mrun;
                 };
+                // block-sparse mode: O rescaled before the first half of P_j is announced (PV(j) starts on it),
+                // 16 columns at a time while half of the scores are still live
+                auto rescale_o16 = [&]() {
+                    if (__any_sync(0xFFFFFFFFu, resc)) {
+                        __syncwarp();
+#pragma unroll 1
+                        for (int c = 0; c < 128; c += 16) {
+                            float ov[16];
+                            tmem_ld16(o_addr + c, ov);
+                            uint32_t ou[16];
+#pragma unroll
+                            for (int i = 0; i < 16; ++i) ou[i] = __float_as_uint(ov[i] * alpha);
+                            tmem_st16u_nowait(o_addr + c, ou);
+                        }
+                    }
+                };
                 // p = 2^(scale*log2(e)*s - m); bf16 pairs go to columns [0, 64) of the S buffer: the A operand
                 // of PV(j)
                 float rs4[4] = {0.f, 0.f, 0.f, 0.f};
@@ -769,6 +801,12 @@ __global__ void __launch_bounds__(kThreads, 1) swa_prefill_tc_kernel(const __gri
                     }
                     __syncwarp();
                     tmem_st8u_nowait(s_addr, pk);
+                    if (BS) {
+                        rescale_o16();
+                        tmem_wait_st();
+                        tc_fence_before();
+                        mbar_arrive(&phalf[g]);
+                    }
                 } else {
                     float sv[128];
                     __syncwarp();
@@ -803,10 +841,16 @@ __global__ void __launch_bounds__(kThreads, 1) swa_prefill_tc_kernel(const __gri
                         }
                         __syncwarp();
                         tmem_st32u_nowait(s_addr + 32 * h, pk);
+                        if (BS && h == 0) {
+                            rescale_o16();
+                            tmem_wait_st();
+                            tc_fence_before();
+                            mbar_arrive(&phalf[g]);
+                        }
                     }
                 }
                 lrun = lrun * alpha + ((rs4[0] + rs4[1]) + (rs4[2] + rs4[3]));
-                if (__any_sync(0xFFFFFFFFu, resc)) {
+                if (!BS && __any_sync(0xFFFFFFFFu, resc)) {
                     // O holds this stream's earlier PV products, all complete: S_j complete implies every MMA
                     // issued before QK(j) is, and PV(j) comes only after P_j
                     __syncwarp();
